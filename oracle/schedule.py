@@ -1,0 +1,426 @@
+"""Lowering of a static op graph into tile instructions, dependency counters and placement.
+
+This is the plain restatement of the compiler's integer work, used to check it bit for bit.
+It follows the scheduler of "MegaKittens Internals" §04: phase 1 (count and place: each node
+gets a contiguous range, rounded up to the cluster size with Noops), phase 3 (fine-grained
+barriers: a consumer's dependency set is the set of producer instructions whose write boxes
+meet its read boxes; every distinct (producer, set) pair is one counter whose target is the set
+size), and §05 (instruction i runs on SM i mod S in iteration i div S). Phase 2's buffer pool is
+not part of this graph model: every buffer is caller-owned and no node may write a region an
+earlier node reads or writes.
+
+Unlike the page, which finds the sets through per-edge GCD unit cells, this module intersects
+every read box with every write box of the earlier phases (brute force).
+
+Graph description (plain dicts, shared with the tests):
+  tensors: [{"rows": R, "cols": C, "dtype": "f16"|"bf16"|"f32"}, ...]
+  ref      = (tensor_id, r0, c0, rows, cols)      a 2-D window of a tensor
+  nodes:   [{"kind": "matmul", "a", "b", "c", "bias"?, "residual"?, "gamma"?, "b2"?, ...},
+            {"kind": "ew", "op", "ins": [refs], "out"},
+            {"kind": "rmsnorm", "x", "gamma", "out"},
+            {"kind": "rope", "x", "out_q", "out_k", "out_v"?, "n_q_heads", "n_kv_heads", "head_dim"},
+            {"kind": "attention", "q", "k", "v", "out", "n_q_heads", "n_kv_heads", "head_dim",
+             "causal", "q_pos0"}]
+
+Lowering rules per node (tile sizes come from ``opts``; see ``DEFAULT_OPTS``):
+  matmul, M > gemv_max_m  -> GEMM tiles tile_m × tn (tn = tile_n, or tile_n/2 with a second
+      weight "b2" for SiLU·mul), row-major over (mt, nt), each tile repeated ``cluster`` times
+      (aux0 = rank). Reads A rows×[0,K), B [0,K)×cols (and b2), bias/residual on the tile box;
+      writes the tile box (every instruction of a cluster writes the whole cluster tile).
+  matmul, M <= gemv_max_m -> GEMV tiles: column tiles of gemv_tile_n, each split along K into
+      S chunks (gemv_splits, or max(1, n_sm div n_col_tiles) when 0); the chunk length is
+      ceil(K/S) rounded up to gemv_kstep and S is then recomputed as ceil(K/chunk). Order: column
+      tile outer, split inner; aux0 = split index, aux1 = S. Split s reads A[:, chunk] (all of A
+      with a norm gamma), B[chunk, cols]; only split 0 carries the output box; every split carries
+      split 0's counter arrivals, because the last split to finish reduces and publishes the tile.
+      Each tile owns one split semaphore, numbered after the dependency counters.
+  ew      -> tiles ew_rows × (ew_cols·ew_tiles), row-major; reads each input and writes the
+      output on the same box; aux0 = elementwise op code.
+  rmsnorm -> one instruction per norm_rows rows (all columns).
+  rope    -> one instruction per norm_rows rows; reads all of x's columns, writes out_q, out_k
+      (and out_v) on those rows.
+  attention with one query row (decode) -> two phases:
+      partial: for kv head g, for chunk c of attn_chunk keys: reads q (the G = Hq/Hkv heads of
+        group g), k and v rows of the chunk (columns of head g); writes rows (g·C + c)·G ..+G
+        of a per-node fp32 scratch [Hkv·C·G × (d+2)]. n0 = g, k0 = first key, klen = keys,
+        aux0 = c, aux1 = C.
+      reduce: one per g; reads the group's C·G scratch rows; writes the group's output columns.
+  attention with several query rows (prefill) -> one instruction per (q tile t of attn_tile_q
+      rows, q head h), t descending (longest first), then h ascending; reads q rows of the tile,
+      k and v rows [0, kmax) with kmax = min(Tk, q_pos0 + end of tile) when causal.
+
+Counters: consumer instructions are visited in index order, their read boxes in order, and for
+each the earlier phases in order; a new (phase, set) key takes the next counter id. A consumer's
+source list holds each counter once (first occurrence order) with its target; producers list the
+counters they arrive on in increasing id order.
+"""
+import numpy as np
+
+OP_NOOP, OP_GEMM, OP_GEMV, OP_EW, OP_RMSNORM, OP_ROPE, OP_ATTN_PARTIAL, OP_ATTN_REDUCE, \
+    OP_ATTN_PREFILL = range(9)
+EW_CODES = {"add": 0, "relu": 1, "copy": 2, "silu_mul": 3}
+FLAG_B_DEP = 1
+
+ROLE_A, ROLE_B, ROLE_E = 0, 1, 2
+
+DEFAULT_OPTS = dict(
+    gemm_tile_m=128, gemm_tile_n=256, cluster=1,
+    ew_rows=128, ew_cols=128, ew_tiles=1,
+    norm_rows=16,
+    gemv_max_m=8, gemv_tile_n=128, gemv_splits=0, gemv_kstep=64,
+    attn_chunk=64, attn_tile_q=128,
+)
+
+
+def cdiv(a, b):
+    return -(-a // b)
+
+
+def _box(ref, r0, r1, c0, c1):
+    """Window [r0,r1)×[c0,c1) of a ref, in the base tensor's coordinates."""
+    t, br, bc, rows, cols = ref
+    r1 = min(r1, rows)
+    c1 = min(c1, cols)
+    return (t, br + r0, br + r1, bc + c0, bc + c1)
+
+
+def _full(ref):
+    return _box(ref, 0, ref[3], 0, ref[4])
+
+
+class Instr:
+    __slots__ = ("op", "flags", "node", "m0", "n0", "k0", "klen", "aux0", "aux1", "sem",
+                 "reads", "writes", "src", "dst", "tile")
+
+    def __init__(self, op, node, m0=0, n0=0, k0=0, klen=0, aux0=0, aux1=0):
+        self.op, self.node = op, node
+        self.flags = 0
+        self.m0, self.n0, self.k0, self.klen, self.aux0, self.aux1 = m0, n0, k0, klen, aux0, aux1
+        self.sem = 0
+        self.reads = []      # (box, role)
+        self.writes = []     # box
+        self.src = []        # (counter, target)
+        self.dst = []        # counter ids
+        self.tile = None     # GEMV tile ordinal (shares arrivals and semaphore)
+
+    def key(self):
+        return (self.op, self.flags, self.node, self.m0, self.n0, self.k0, self.klen,
+                self.aux0, self.aux1, self.sem)
+
+
+def _lower_matmul(ni, nd, opts, phases, sem_tiles):
+    a, b, c = nd["a"], nd["b"], nd["c"]
+    m, k = a[3], a[4]
+    n = c[4]
+    b2 = nd.get("b2")
+    gamma = nd.get("gamma")
+    epi = [(nd[x], x) for x in ("bias", "residual") if nd.get(x) is not None]
+    out = []
+    if m <= opts["gemv_max_m"]:
+        w = opts["gemv_tile_n"]
+        n_ct = cdiv(n, w)
+        s0 = opts["gemv_splits"] if opts["gemv_splits"] > 0 else max(1, opts["n_sm"] // n_ct)
+        chunk = cdiv(cdiv(k, s0), opts["gemv_kstep"]) * opts["gemv_kstep"]
+        s = max(1, cdiv(k, chunk))
+        for ct in range(n_ct):
+            n0 = ct * w
+            tile = len(sem_tiles)
+            sem_tiles.append(tile)
+            for si in range(s):
+                k0 = si * chunk
+                kl = min(chunk, k - k0)
+                ins = Instr(OP_GEMV, ni, 0, n0, k0, kl, si, s)
+                ins.tile = tile
+                if gamma is not None:
+                    ins.reads.append((_full(a), ROLE_A))
+                    ins.reads.append((_full(gamma), ROLE_A))
+                else:
+                    ins.reads.append((_box(a, 0, m, k0, k0 + kl), ROLE_A))
+                ins.reads.append((_box(b, k0, k0 + kl, n0, n0 + w), ROLE_B))
+                if b2 is not None:
+                    ins.reads.append((_box(b2, k0, k0 + kl, n0, n0 + w), ROLE_B))
+                for r, _ in epi:
+                    ins.reads.append((_box(r, 0, m, n0, n0 + w), ROLE_E))
+                if si == 0:
+                    ins.writes.append(_box(c, 0, m, n0, n0 + w))
+                out.append(ins)
+    else:
+        tm = opts["gemm_tile_m"]
+        tn = opts["gemm_tile_n"] // 2 if b2 is not None else opts["gemm_tile_n"]
+        for mt in range(cdiv(m, tm)):
+            for nt in range(cdiv(n, tn)):
+                m0, n0 = mt * tm, nt * tn
+                for r in range(opts["cluster"]):
+                    ins = Instr(OP_GEMM, ni, m0, n0, 0, k, r, 0)
+                    ins.reads.append((_box(a, m0, m0 + tm, 0, k), ROLE_A))
+                    ins.reads.append((_box(b, 0, k, n0, n0 + tn), ROLE_B))
+                    if b2 is not None:
+                        ins.reads.append((_box(b2, 0, k, n0, n0 + tn), ROLE_B))
+                    for ref, _ in epi:
+                        ins.reads.append((_box(ref, m0, m0 + tm, n0, n0 + tn), ROLE_E))
+                    ins.writes.append(_box(c, m0, m0 + tm, n0, n0 + tn))
+                    out.append(ins)
+    phases.append(out)
+
+
+def _lower_ew(ni, nd, opts, phases):
+    o = nd["out"]
+    rows, cols = o[3], o[4]
+    er, ew = opts["ew_rows"], opts["ew_cols"] * opts["ew_tiles"]
+    out = []
+    for rt in range(cdiv(rows, er)):
+        for ct in range(cdiv(cols, ew)):
+            m0, n0 = rt * er, ct * ew
+            ins = Instr(OP_EW, ni, m0, n0, 0, 0, EW_CODES[nd["op"]], 0)
+            for r in nd["ins"]:
+                ins.reads.append((_box(r, m0, m0 + er, n0, n0 + ew), ROLE_E))
+            ins.writes.append(_box(o, m0, m0 + er, n0, n0 + ew))
+            out.append(ins)
+    phases.append(out)
+
+
+def _lower_rows(ni, nd, opts, phases, op):
+    nr = opts["norm_rows"]
+    x = nd["x"]
+    rows = x[3]
+    outs = [nd[k] for k in ("out", "out_q", "out_k", "out_v") if nd.get(k) is not None]
+    out = []
+    for rt in range(cdiv(rows, nr)):
+        m0 = rt * nr
+        ins = Instr(op, ni, m0)
+        ins.reads.append((_box(x, m0, m0 + nr, 0, x[4]), ROLE_E))
+        if nd.get("gamma") is not None:
+            ins.reads.append((_full(nd["gamma"]), ROLE_E))
+        for o in outs:
+            ins.writes.append(_box(o, m0, m0 + nr, 0, o[4]))
+        out.append(ins)
+    phases.append(out)
+
+
+def _lower_attention(ni, nd, opts, phases, tensors):
+    q, k, v, o = nd["q"], nd["k"], nd["v"], nd["out"]
+    hq, hkv, d = nd["n_q_heads"], nd["n_kv_heads"], nd["head_dim"]
+    g_sz = hq // hkv
+    tq, tk = q[3], k[3]
+    if tq == 1:
+        ch = opts["attn_chunk"]
+        nc = cdiv(tk, ch)
+        scratch_id = len(tensors)
+        tensors.append({"rows": hkv * nc * g_sz, "cols": d + 2, "dtype": "f32", "internal": True})
+        scratch = (scratch_id, 0, 0, hkv * nc * g_sz, d + 2)
+        part = []
+        for g in range(hkv):
+            for c in range(nc):
+                k0 = c * ch
+                kl = min(ch, tk - k0)
+                ins = Instr(OP_ATTN_PARTIAL, ni, 0, g, k0, kl, c, nc)
+                ins.reads.append((_box(q, 0, 1, g * g_sz * d, (g + 1) * g_sz * d), ROLE_E))
+                ins.reads.append((_box(k, k0, k0 + kl, g * d, (g + 1) * d), ROLE_E))
+                ins.reads.append((_box(v, k0, k0 + kl, g * d, (g + 1) * d), ROLE_E))
+                r0 = (g * nc + c) * g_sz
+                ins.writes.append(_box(scratch, r0, r0 + g_sz, 0, d + 2))
+                part.append(ins)
+        red = []
+        for g in range(hkv):
+            ins = Instr(OP_ATTN_REDUCE, ni, 0, g, 0, 0, 0, nc)
+            r0 = g * nc * g_sz
+            ins.reads.append((_box(scratch, r0, r0 + nc * g_sz, 0, d + 2), ROLE_E))
+            ins.writes.append(_box(o, 0, 1, g * g_sz * d, (g + 1) * g_sz * d))
+            red.append(ins)
+        phases.append(part)
+        phases.append(red)
+    else:
+        tt = opts["attn_tile_q"]
+        out = []
+        for t in reversed(range(cdiv(tq, tt))):
+            m0 = t * tt
+            kmax = min(tk, nd.get("q_pos0", 0) + m0 + tt) if nd["causal"] else tk
+            for h in range(hq):
+                g = h // g_sz
+                ins = Instr(OP_ATTN_PREFILL, ni, m0, h, 0, kmax)
+                ins.reads.append((_box(q, m0, m0 + tt, h * d, (h + 1) * d), ROLE_E))
+                ins.reads.append((_box(k, 0, kmax, g * d, (g + 1) * d), ROLE_E))
+                ins.reads.append((_box(v, 0, kmax, g * d, (g + 1) * d), ROLE_E))
+                ins.writes.append(_box(o, m0, m0 + tt, h * d, (h + 1) * d))
+                out.append(ins)
+        phases.append(out)
+
+
+class Plan:
+    """The oracle's schedule: flat instruction list (Noop-padded), counters and placement."""
+
+    def __init__(self, instrs, targets, n_dep, n_sm, sem_count):
+        self.instrs = instrs
+        self.targets = targets          # per dependency counter
+        self.n_dep = n_dep
+        self.n_sem = sem_count
+        self.n_sm = n_sm
+
+    @property
+    def n_instr(self):
+        return len(self.instrs)
+
+    @property
+    def waves(self):
+        return self.n_instr / self.n_sm
+
+    def placement(self, i):
+        """(SM, iteration) of instruction i under the static round-robin placement."""
+        return i % self.n_sm, i // self.n_sm
+
+    def final_counters(self):
+        """Value of every counter after one complete run: deps reach their targets, each GEMV
+        tile's split semaphore counts its splits."""
+        sems = [0] * self.n_sem
+        for ins in self.instrs:
+            if ins.op == OP_GEMV:
+                sems[ins.sem - self.n_dep] += 1
+        return list(self.targets) + sems
+
+    def records(self):
+        """Per-instruction fields the compiler must reproduce exactly."""
+        return [(ins.key(), tuple(ins.src), tuple(ins.dst)) for ins in self.instrs]
+
+
+def lower(graph, opts):
+    """Lower a graph description into a Plan (see the module docstring for the rules)."""
+    o = dict(DEFAULT_OPTS)
+    o.update(opts)
+    tensors = [dict(t) for t in graph["tensors"]]
+    phases = []
+    sem_tiles = []
+    for ni, nd in enumerate(graph["nodes"]):
+        kind = nd["kind"]
+        if kind == "matmul":
+            _lower_matmul(ni, nd, o, phases, sem_tiles)
+        elif kind == "ew":
+            _lower_ew(ni, nd, o, phases)
+        elif kind == "rmsnorm":
+            _lower_rows(ni, nd, o, phases, OP_RMSNORM)
+        elif kind == "rope":
+            _lower_rows(ni, nd, o, phases, OP_ROPE)
+        elif kind == "attention":
+            _lower_attention(ni, nd, o, phases, tensors)
+        else:
+            raise ValueError(kind)
+
+    # Phase 1: contiguous ranges, each rounded up to the cluster size with Noops.
+    instrs, phase_of, ranges = [], [], []
+    for pi, ph in enumerate(phases):
+        start = len(instrs)
+        instrs.extend(ph)
+        pad = (-len(ph)) % o["cluster"]
+        instrs.extend(Instr(OP_NOOP, 0) for _ in range(pad))
+        ranges.append((start, len(instrs)))
+        phase_of.extend([pi] * (len(instrs) - start))
+
+    # Phase 3: dependency sets by brute-force intersection; one counter per (phase, set).
+    # For every phase and tensor, the write boxes as arrays (instruction, r0, r1, c0, c1).
+    wtab = {}
+    for qi, (s0, s1) in enumerate(ranges):
+        per = {}
+        for p in range(s0, s1):
+            for w in instrs[p].writes:
+                per.setdefault(w[0], []).append((p, w[1], w[2], w[3], w[4]))
+        for t, rows in per.items():
+            wtab.setdefault(t, []).append((qi, np.array(rows, dtype=np.int64).reshape(-1, 5)))
+    keys = {}
+    targets = []
+    members = []
+    for ci, c in enumerate(instrs):
+        seen = set()
+        for box, role in c.reads:
+            if box[1] >= box[2] or box[3] >= box[4]:
+                continue
+            for qi, arr in wtab.get(box[0], []):
+                if qi >= phase_of[ci]:
+                    break
+                hit = ((arr[:, 1] < box[2]) & (box[1] < arr[:, 2]) & (arr[:, 3] < box[4])
+                       & (box[3] < arr[:, 4]) & (arr[:, 1] < arr[:, 2]) & (arr[:, 3] < arr[:, 4]))
+                st = tuple(sorted(set(int(p) for p in arr[hit, 0])))
+                if not st:
+                    continue
+                key = (qi, st)
+                if key not in keys:
+                    keys[key] = len(targets)
+                    targets.append(len(st))
+                    members.append(st)
+                cid = keys[key]
+                if role == ROLE_B and c.op in (OP_GEMM, OP_GEMV):
+                    c.flags |= FLAG_B_DEP
+                if cid not in seen:
+                    seen.add(cid)
+                    c.src.append((cid, len(st)))
+    for cid, st in enumerate(members):
+        for p in st:
+            instrs[p].dst.append(cid)
+    n_dep = len(targets)
+
+    # GEMV tiles: every split publishes with split 0's arrivals and shares one semaphore.
+    first = {}
+    for ins in instrs:
+        if ins.op == OP_GEMV:
+            if ins.aux0 == 0:
+                first[ins.tile] = ins
+    for ins in instrs:
+        if ins.op == OP_GEMV:
+            ins.dst = list(first[ins.tile].dst)
+            ins.sem = n_dep + ins.tile
+    return Plan(instrs, targets, n_dep, o["n_sm"], len(sem_tiles))
+
+
+def topologically_valid(plan):
+    """Every counter a consumer waits on is fed only by lower-index instructions, and every
+    counter's target equals the number of distinct instructions that arrive on it (split
+    copies of a GEMV tile count once). With placement i -> (i mod S, i div S) this is the
+    deadlock-freedom argument of "MegaKittens Internals" §11."""
+    feeders = {}
+    for i, ins in enumerate(plan.instrs):
+        key = ins.tile if ins.op == OP_GEMV else ("i", i)
+        for cid in ins.dst:
+            feeders.setdefault(cid, {})
+            feeders[cid].setdefault(key, []).append(i)
+    for cid, t in enumerate(plan.targets):
+        if len(feeders.get(cid, {})) != t:
+            return False
+    for i, ins in enumerate(plan.instrs):
+        for cid, t in ins.src:
+            for idxs in feeders[cid].values():
+                if max(idxs) >= i:
+                    return False
+    return True
+
+
+def levels(plan):
+    """Host-side level of each instruction: 0 without sources, else 1 + max level of the
+    instructions feeding its counters ("Implementing a Mega Kernel for B300" §7). Used only as
+    an independent check of acyclicity."""
+    feeders = {}
+    for i, ins in enumerate(plan.instrs):
+        for cid in ins.dst:
+            feeders.setdefault(cid, []).append(i)
+    lv = []
+    for i, ins in enumerate(plan.instrs):
+        best = -1
+        for cid, _ in ins.src:
+            for p in feeders[cid]:
+                best = max(best, lv[p])
+        lv.append(best + 1)
+    return lv
+
+
+def waves_text(plan):
+    return f"{plan.waves:.2f}"
+
+
+def as_array(plan):
+    """Per-instruction integer fields as an int64 array [N, 10] (op, flags, node, m0, n0, k0,
+    klen, aux0, aux1, sem)."""
+    return np.array([ins.key() for ins in plan.instrs], dtype=np.int64).reshape(-1, 10)
+
+
+def count_by_op(plan):
+    out = {}
+    for ins in plan.instrs:
+        out[ins.op] = out.get(ins.op, 0) + 1
+    return out
