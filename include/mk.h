@@ -1,0 +1,247 @@
+/*
+ * mk.h — C ABI of the GB300 persistent megakernel library (libmk.so).
+ *
+ * A caller builds a static op graph over its own device buffers, compiles it once into a
+ * plan (a flat list of fixed-size tile instructions, per-tile dependency counters and a node
+ * table), and runs the plan as ONE persistent kernel launch per call on its own stream.
+ *
+ * Where the operations come from (page title, section):
+ *  - graph of ops with fused epilogue flags, lowered to tile tasks:
+ *      "Implementing a Mega Kernel for B300", §1 "Build the graph", §2 "Lower each op into tasks"
+ *  - flat instruction list, per-tile integer counters, round-robin placement, counter zeroing
+ *    per call: "MegaKittens Internals", §04 "Scheduler", §05 "The real schedule", §07
+ *    "Dispatcher, JIT and launch", §11 "The TMEM token and global barriers"
+ *  - the GEMM tile (TMA, mbarriers, TMEM, tcgen05): "Hand-writing a Blackwell GEMM", steps 1-8
+ *  - split-KV attention partial + combine: "Implementing a Mega Kernel for B300", §2 and §8
+ *
+ * Conventions
+ *  - Every function returns an mk_status; MK_OK is 0. On failure mk_last_error() returns a
+ *    message (thread-local, valid until the next call on the same thread). No function aborts.
+ *  - Tensors are caller-owned device memory, registered by pointer. The library never frees
+ *    or allocates them. A plan is bound to the pointers given at compile time.
+ *  - Tensor ids and node ids are small non-negative integers local to one graph.
+ *  - Element types: MK_F16 (IEEE half), MK_BF16 (bfloat16), MK_F32.
+ *  - Row-major 2-D view of every tensor: the innermost dimension is the column dimension and
+ *    must have stride 1; all outer dimensions fold into rows and must be contiguous with each
+ *    other. Row stride (elements) = strides[rank-2].
+ *  - Threading: a graph or plan must not be used from two threads at once. Different plans
+ *    may run concurrently on different streams.
+ */
+#ifndef MK_H_
+#define MK_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MK_ABI_VERSION 1
+
+typedef struct mk_graph* mk_graph_t;
+typedef struct mk_plan* mk_plan_t;
+typedef int32_t mk_status;
+
+enum {
+  MK_OK = 0,
+  MK_ERR_INVALID_ARG = 1,   /* bad id, shape mismatch, null pointer */
+  MK_ERR_UNSUPPORTED = 2,   /* valid graph the kernel cannot run: dtype, alignment, sizes */
+  MK_ERR_HAZARD = 3,        /* a node writes a region an earlier node reads or writes */
+  MK_ERR_OOM = 4,           /* device or host allocation failed */
+  MK_ERR_CUDA = 5,          /* a CUDA runtime/driver call failed (message has the name) */
+  MK_ERR_TIMEOUT = 6,       /* a device-side wait exceeded its limit; see mk_device_status */
+  MK_ERR_DEVICE_CHECK = 7,  /* a device-side consistency check failed; see mk_device_status */
+};
+
+enum { MK_F16 = 0, MK_BF16 = 1, MK_F32 = 2 };
+
+/* ---------------------------------------------------------------- graph construction */
+
+/* Create an empty graph. *out receives the handle (owned by the caller; free with
+ * mk_graph_destroy). */
+mk_status mk_graph_create(mk_graph_t* out);
+mk_status mk_graph_destroy(mk_graph_t g);
+
+/* Register a caller-owned device tensor.
+ *   dev_ptr  device address (16-byte aligned for any tensor read or written by TMA: GEMM and
+ *            GEMV operands). May be NULL only for plans compiled with dry_run.
+ *   dtype    MK_F16 / MK_BF16 / MK_F32
+ *   rank     1..4; shape[rank], strides[rank] in elements (strides may be NULL: contiguous)
+ * The tensor is seen as rows x cols with cols = shape[rank-1]. */
+mk_status mk_add_tensor(mk_graph_t g, void* dev_ptr, int32_t dtype, int32_t rank,
+                        const int64_t* shape, const int64_t* strides, int32_t* tensor_id);
+
+/* A rows x cols window of a registered tensor starting at (r0, c0) of its 2-D view; used to
+ * name a layer of stacked weights, a slice of columns (q | k | v), a cache row, ... */
+mk_status mk_add_view(mk_graph_t g, int32_t base, int64_t r0, int64_t c0, int64_t rows,
+                      int64_t cols, int32_t* view_id);
+
+/* Epilogue flags of a matmul ("Implementing a Mega Kernel for B300", §2: SILU_MUL,
+ * ADD_RESIDUAL, RMS_NORM_INPUT; bias + ReLU: "MegaKittens Internals", §02). */
+enum {
+  MK_EPI_BIAS = 1u << 0,           /* + bias[m, n]; bias is a full M x N tensor */
+  MK_EPI_RELU = 1u << 1,           /* max(., 0) after the bias */
+  MK_EPI_RESIDUAL = 1u << 2,       /* + residual[m, n] after ReLU */
+  MK_EPI_RMSNORM_INPUT = 1u << 3,  /* A := A / sqrt(mean(A^2) + eps) * gamma, row-wise (GEMV only) */
+  MK_EPI_SILU_MUL = 1u << 4,       /* out = silu(A B) * (A b_up) */
+};
+
+typedef struct {
+  uint32_t flags;     /* MK_EPI_* */
+  int32_t bias;       /* tensor id or -1 */
+  int32_t residual;   /* tensor id or -1 */
+  int32_t gamma;      /* tensor id (1 x K) or -1 */
+  int32_t b_up;       /* tensor id (K x N) or -1: second weight of SILU_MUL */
+  float eps;          /* RMS_NORM_INPUT epsilon */
+} mk_epilogue;
+
+/* out[M x N] = epilogue(a[M x K] @ b[K x N]). a, b, out (and bias, residual, b_up) share one
+ * dtype, MK_F16 or MK_BF16; accumulation is fp32. epi may be NULL (plain product). */
+mk_status mk_add_matmul(mk_graph_t g, int32_t a, int32_t b, int32_t out, const mk_epilogue* epi,
+                        int32_t* node_id);
+
+/* Elementwise and row operations ("MegaKittens Internals", §12; "Implementing a Mega Kernel
+ * for B300", §8 RMSNORM and ATTENTION_APPEND). Inputs and outputs of ADD/RELU/COPY/SILU_MUL
+ * have the same shape (no broadcasting). */
+enum {
+  MK_EW_ADD = 0,        /* out = in0 + in1 */
+  MK_EW_RELU = 1,       /* out = max(in0, 0) */
+  MK_EW_COPY = 2,       /* out = in0 */
+  MK_EW_SILU_MUL = 3,   /* out = silu(in0) * in1 */
+  MK_EW_RMSNORM = 16,   /* out = in0 / sqrt(mean(in0^2) + eps) * gamma (row-wise) */
+  MK_EW_ROPE = 17,      /* rotary embedding of q and k heads (+ copy of v), see mk_ew_params */
+};
+
+typedef struct {
+  float eps;            /* RMSNORM */
+  int32_t gamma;        /* RMSNORM: tensor id (1 x cols) */
+  /* ROPE: in0 = x [R x (Hq + Hkv) * d (+ Hkv * d)], columns [q | k (| v)]; row r is position
+   * pos0 + r. out = rotated q [R x Hq*d]; out_k = rotated k [R x Hkv*d]; out_v (or -1) =
+   * copy of v [R x Hkv*d]. Pairs (i, i + d/2) of each head rotate by pos * theta^(-2i/d). */
+  int32_t n_q_heads, n_kv_heads, head_dim;
+  int32_t pos0;
+  float theta;
+  int32_t out_k, out_v;
+} mk_ew_params;
+
+mk_status mk_add_elementwise(mk_graph_t g, int32_t op, const int32_t* ins, int32_t n_in,
+                             int32_t out, const mk_ew_params* p, int32_t* node_id);
+
+/* Attention out = softmax(q k^T * scale [+ causal mask]) v with grouped kv heads.
+ *   q [Tq x Hq*d], k and v [Tk x Hkv*d], out [Tq x Hq*d], all MK_BF16.
+ *   Query row i is at position q_pos0 + i, key row j at position j; causal: j <= q_pos0 + i.
+ *   Tq == 1 lowers to split-KV partial + reduce tiles ("Implementing a Mega Kernel for B300",
+ *   §2); Tq > 1 to causal prefill tiles. scale 0 means 1/sqrt(d). */
+typedef struct {
+  int32_t n_q_heads, n_kv_heads, head_dim;
+  int32_t causal;
+  int32_t q_pos0;
+  float scale;
+} mk_attn_params;
+
+mk_status mk_add_attention(mk_graph_t g, int32_t q, int32_t k, int32_t v, int32_t out,
+                           const mk_attn_params* p, int32_t* node_id);
+
+/* ---------------------------------------------------------------- compile and run */
+
+typedef struct {
+  int32_t n_sm;          /* placement stride = persistent grid size; 0 = the device's SM count */
+  int32_t gemm_tile_m;   /* GEMM output tile rows (the kernel runs 128) */
+  int32_t gemm_tile_n;   /* GEMM output tile columns: 64, 128 or 256 (halved for SILU_MUL) */
+  int32_t cluster;       /* instructions per GEMM tile (CTA-pair duplicates); 1 */
+  int32_t ew_rows, ew_cols, ew_tiles;   /* elementwise instruction = ew_rows x ew_cols*ew_tiles */
+  int32_t norm_rows;     /* rows per RMSNORM / ROPE instruction */
+  int32_t gemv_max_m;    /* matmuls with M <= this lower to GEMV tiles */
+  int32_t gemv_tile_n;   /* GEMV output columns per tile (halved for SILU_MUL) */
+  int32_t gemv_splits;   /* K splits per GEMV tile; 0 = max(1, n_sm / column tiles) */
+  int32_t gemv_kstep;    /* GEMV K chunks are multiples of this */
+  int32_t attn_chunk;    /* keys per split-KV partial */
+  int32_t attn_tile_q;   /* query rows per prefill attention tile */
+  int32_t dry_run;       /* 1: lower only (no device, no kernel-support checks) */
+  int32_t timeout_ms;    /* limit of every device-side wait; 0 = 2000 */
+  int32_t device;        /* CUDA device ordinal; -1 = current */
+  int32_t debug_counter; /* test hook: counter whose target is raised by debug_extra (-1: none) */
+  int32_t debug_extra;
+} mk_compile_opts;
+
+/* Fill *o with the defaults (the values listed above for each field). */
+mk_status mk_default_opts(mk_compile_opts* o);
+
+/* Lower the graph and, unless dry_run, upload the plan to the device: instruction list, node
+ * table, dependency lists, tensor maps, counters, scratch and status word (plan-owned). The
+ * graph may be destroyed afterwards. */
+mk_status mk_compile(mk_graph_t g, const mk_compile_opts* opts, mk_plan_t* out);
+
+/* Enqueue one run on `stream` (a cudaStream_t; NULL = legacy default stream): zero the
+ * counters and status word, then ONE persistent launch. Asynchronous; errors of the launch
+ * itself are returned, device-side failures are reported by mk_sync_status. */
+mk_status mk_run(mk_plan_t p, void* stream);
+
+/* One copy between a registered tensor (or view) and host memory. */
+typedef struct {
+  int32_t tensor;      /* tensor or view id of the compiled graph */
+  void* host;          /* rows x cols elements, densely packed (pinned memory for overlap) */
+  int32_t to_device;   /* 1: host -> tensor before the launch; 0: tensor -> host after it */
+} mk_host_copy;
+
+/* End-to-end call with host buffers: the host->device copies (in order), mk_run, then the
+ * device->host copies, all enqueued on `stream`. */
+mk_status mk_run_host(mk_plan_t p, const mk_host_copy* copies, int32_t n_copies, void* stream);
+
+typedef struct {
+  int32_t code;       /* MK_OK, MK_ERR_TIMEOUT or MK_ERR_DEVICE_CHECK */
+  int32_t instr;      /* instruction index being processed */
+  int32_t counter;    /* counter waited on (-1: an on-chip barrier) */
+  int32_t observed;   /* its value when the wait gave up */
+  int32_t expected;   /* the value waited for */
+  int32_t sm;         /* CTA index */
+  int32_t role;       /* 0 scheduler, 1 loader, 2 MMA, 3 compute */
+  int32_t where;      /* wait site id (kernel-internal) */
+} mk_device_status;
+
+/* Synchronise the device and read the plan's status word. Returns st->code as the status. */
+mk_status mk_sync_status(mk_plan_t p, mk_device_status* st);
+
+mk_status mk_plan_destroy(mk_plan_t p);
+
+/* ---------------------------------------------------------------- introspection */
+
+typedef struct {
+  int64_t n_instr;       /* instructions in the list, Noop padding included */
+  int64_t n_counters;    /* dependency counters */
+  int64_t n_sems;        /* split-K semaphores (after the counters in the counter array) */
+  int64_t n_sm;          /* placement stride */
+  int64_t n_iter;        /* ceil(n_instr / n_sm): iterations of the longest SM queue */
+  double waves;          /* n_instr / n_sm */
+  int64_t n_src;         /* entries of the source list (pairs) */
+  int64_t n_dst;         /* entries of the arrival list */
+  int64_t per_op[16];    /* instructions per op code */
+  int64_t smem_bytes;    /* dynamic shared memory of the launch (0 when dry_run) */
+  int64_t scratch_bytes; /* plan-owned device scratch */
+} mk_stats;
+
+mk_status mk_plan_stats(mk_plan_t p, mk_stats* s);
+
+/* Instruction records, 64 bytes each, little-endian:
+ *   u16 op, u16 flags, i32 node, i32 m0, n0, k0, klen, aux0, aux1, sem,
+ *   i32 n_src, src_off, n_dst, dst_off, i32 pad[3].
+ * bytes must be >= n_instr * 64. */
+mk_status mk_get_instructions(mk_plan_t p, void* host_buf, size_t bytes);
+/* Source list: n_src pairs (counter, target) as int32; n = number of int32 slots. */
+mk_status mk_get_src_list(mk_plan_t p, int32_t* host_buf, size_t n);
+/* Arrival list: n_dst counter ids. */
+mk_status mk_get_dst_list(mk_plan_t p, int32_t* host_buf, size_t n);
+/* Target of every dependency counter (n_counters values). */
+mk_status mk_get_counter_targets(mk_plan_t p, int32_t* host_buf, size_t n);
+/* Device counter array after a run (n_counters + n_sems values); synchronises. */
+mk_status mk_get_counters(mk_plan_t p, int32_t* host_buf, size_t n);
+
+const char* mk_last_error(void);
+int32_t mk_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MK_H_ */

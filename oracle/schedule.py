@@ -23,13 +23,15 @@ Graph description (plain dicts, shared with the tests):
              "causal", "q_pos0"}]
 
 Lowering rules per node (tile sizes come from ``opts``; see ``DEFAULT_OPTS``):
+  matmul with M = 0 or N = 0 -> no instructions.
   matmul, M > gemv_max_m  -> GEMM tiles tile_m × tn (tn = tile_n, or tile_n/2 with a second
       weight "b2" for SiLU·mul), row-major over (mt, nt), each tile repeated ``cluster`` times
       (aux0 = rank). Reads A rows×[0,K), B [0,K)×cols (and b2), bias/residual on the tile box;
       writes the tile box (every instruction of a cluster writes the whole cluster tile).
-  matmul, M <= gemv_max_m -> GEMV tiles: column tiles of gemv_tile_n, each split along K into
+  matmul, M <= gemv_max_m -> GEMV tiles: column tiles of gemv_tile_n (halved with b2), each
+      split along K into
       S chunks (gemv_splits, or max(1, n_sm div n_col_tiles) when 0); the chunk length is
-      ceil(K/S) rounded up to gemv_kstep and S is then recomputed as ceil(K/chunk). Order: column
+      ceil(K/S) rounded up to gemv_kstep (at least gemv_kstep) and S is then recomputed as ceil(K/chunk). Order: column
       tile outer, split inner; aux0 = split index, aux1 = S. Split s reads A[:, chunk] (all of A
       with a norm gamma), B[chunk, cols]; only split 0 carries the output box; every split carries
       split 0's counter arrivals, because the last split to finish reduces and publishes the tile.
@@ -67,7 +69,7 @@ DEFAULT_OPTS = dict(
     gemm_tile_m=128, gemm_tile_n=256, cluster=1,
     ew_rows=128, ew_cols=128, ew_tiles=1,
     norm_rows=16,
-    gemv_max_m=8, gemv_tile_n=128, gemv_splits=0, gemv_kstep=64,
+    gemv_max_m=8, gemv_tile_n=128, gemv_splits=0, gemv_kstep=128,
     attn_chunk=64, attn_tile_q=128,
 )
 
@@ -116,11 +118,13 @@ def _lower_matmul(ni, nd, opts, phases, sem_tiles):
     gamma = nd.get("gamma")
     epi = [(nd[x], x) for x in ("bias", "residual") if nd.get(x) is not None]
     out = []
-    if m <= opts["gemv_max_m"]:
-        w = opts["gemv_tile_n"]
+    if m == 0 or n == 0:
+        pass
+    elif m <= opts["gemv_max_m"]:
+        w = opts["gemv_tile_n"] // 2 if b2 is not None else opts["gemv_tile_n"]
         n_ct = cdiv(n, w)
         s0 = opts["gemv_splits"] if opts["gemv_splits"] > 0 else max(1, opts["n_sm"] // n_ct)
-        chunk = cdiv(cdiv(k, s0), opts["gemv_kstep"]) * opts["gemv_kstep"]
+        chunk = max(opts["gemv_kstep"], cdiv(cdiv(k, s0), opts["gemv_kstep"]) * opts["gemv_kstep"])
         s = max(1, cdiv(k, chunk))
         for ct in range(n_ct):
             n0 = ct * w

@@ -1,0 +1,668 @@
+// Graph construction, validation and the compiler's lowering: ops -> tile instructions ->
+// dependency counters -> static per-SM placement. No CUDA here; this file also builds the
+// plans that dry-run tests inspect on a machine without a GPU.
+//
+// Lowering follows "MegaKittens Internals" §04 (phase 1: contiguous per-node ranges rounded to
+// the cluster size with Noops; phase 3: a consumer waits on the producer instructions whose
+// write boxes meet its read boxes, and each distinct (producer phase, set) is one counter whose
+// target is the set size), §05 (instruction i -> SM i mod S, iteration i div S) and the task
+// fan-out of "Implementing a Mega Kernel for B300" §2 (one GEMV task per column tile, one
+// ATTENTION_PARTIAL per (kv group, chunk) followed by a combine).
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <map>
+
+#include "mk_internal.h"
+
+namespace mk {
+
+static thread_local std::string g_err;
+
+void set_error(const char* fmt, ...) {
+  char buf[1024];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+}
+
+int dtype_size(int dt) { return dt == DT_F32 ? 4 : 2; }
+
+static inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Window [r0,r1) x [c0,c1) of tensor/view `id`, clipped to it, in base coordinates.
+static Box window(const std::vector<TensorRec>& ts, int id, int64_t r0, int64_t r1, int64_t c0,
+                  int64_t c1) {
+  const TensorRec& v = ts[id];
+  Box b;
+  b.t = v.base;
+  r1 = std::min(r1, v.rows);
+  c1 = std::min(c1, v.cols);
+  b.r0 = v.r0 + r0;
+  b.r1 = v.r0 + r1;
+  b.c0 = v.c0 + c0;
+  b.c1 = v.c0 + c1;
+  return b;
+}
+static Box whole(const std::vector<TensorRec>& ts, int id) {
+  return window(ts, id, 0, ts[id].rows, 0, ts[id].cols);
+}
+
+static HInstr make(uint16_t op, int node, int m0 = 0, int n0 = 0, int k0 = 0, int klen = 0,
+                   int aux0 = 0, int aux1 = 0) {
+  HInstr h;
+  h.rec.op = op;
+  h.rec.node = node;
+  h.rec.m0 = m0;
+  h.rec.n0 = n0;
+  h.rec.k0 = k0;
+  h.rec.klen = klen;
+  h.rec.aux0 = aux0;
+  h.rec.aux1 = aux1;
+  return h;
+}
+
+static void lower_matmul(const std::vector<TensorRec>& ts, int ni, const NodeRec& nd,
+                         const mk_compile_opts& o, std::vector<std::vector<HInstr>>& phases,
+                         int& n_tiles_sem, HostPlan* plan) {
+  const int64_t m = ts[nd.a].rows, k = ts[nd.a].cols, n = ts[nd.out].cols;
+  const bool dual = nd.b2 >= 0;
+  std::vector<HInstr> out;
+  if (m == 0 || n == 0) {
+    // nothing to compute
+  } else if (m <= o.gemv_max_m) {
+    const int64_t w = dual ? o.gemv_tile_n / 2 : o.gemv_tile_n;
+    const int64_t nct = cdiv(n, w);
+    int64_t s0 = o.gemv_splits > 0 ? o.gemv_splits : std::max<int64_t>(1, o.n_sm / nct);
+    const int64_t chunk =
+        std::max<int64_t>(o.gemv_kstep, cdiv(cdiv(k, s0), o.gemv_kstep) * o.gemv_kstep);
+    const int64_t s = std::max<int64_t>(1, cdiv(k, chunk));
+    plan->node_splits[ni] = (int)s;
+    plan->node_tile_n[ni] = (int)w;
+    for (int64_t ct = 0; ct < nct; ++ct) {
+      const int64_t n0 = ct * w;
+      const int tile = n_tiles_sem++;
+      for (int64_t si = 0; si < s; ++si) {
+        const int64_t k0 = si * chunk, kl = std::min(chunk, k - k0);
+        HInstr h = make(OP_GEMV, ni, 0, (int)n0, (int)k0, (int)kl, (int)si, (int)s);
+        h.tile = tile;
+        if (nd.gamma >= 0) {
+          h.reads.push_back({whole(ts, nd.a), ROLE_A});
+          h.reads.push_back({whole(ts, nd.gamma), ROLE_A});
+        } else {
+          h.reads.push_back({window(ts, nd.a, 0, m, k0, k0 + kl), ROLE_A});
+        }
+        h.reads.push_back({window(ts, nd.b, k0, k0 + kl, n0, n0 + w), ROLE_B});
+        if (dual) h.reads.push_back({window(ts, nd.b2, k0, k0 + kl, n0, n0 + w), ROLE_B});
+        if (nd.bias >= 0) h.reads.push_back({window(ts, nd.bias, 0, m, n0, n0 + w), ROLE_E});
+        if (nd.res >= 0) h.reads.push_back({window(ts, nd.res, 0, m, n0, n0 + w), ROLE_E});
+        if (si == 0) h.writes.push_back(window(ts, nd.out, 0, m, n0, n0 + w));
+        out.push_back(std::move(h));
+      }
+    }
+  } else {
+    const int64_t tm = o.gemm_tile_m;
+    const int64_t tn = dual ? o.gemm_tile_n / 2 : o.gemm_tile_n;
+    plan->node_tile_n[ni] = (int)tn;
+    for (int64_t mt = 0; mt < cdiv(m, tm); ++mt) {
+      for (int64_t nt = 0; nt < cdiv(n, tn); ++nt) {
+        const int64_t m0 = mt * tm, n0 = nt * tn;
+        for (int r = 0; r < o.cluster; ++r) {
+          HInstr h = make(OP_GEMM, ni, (int)m0, (int)n0, 0, (int)k, r, 0);
+          h.reads.push_back({window(ts, nd.a, m0, m0 + tm, 0, k), ROLE_A});
+          h.reads.push_back({window(ts, nd.b, 0, k, n0, n0 + tn), ROLE_B});
+          if (dual) h.reads.push_back({window(ts, nd.b2, 0, k, n0, n0 + tn), ROLE_B});
+          if (nd.bias >= 0)
+            h.reads.push_back({window(ts, nd.bias, m0, m0 + tm, n0, n0 + tn), ROLE_E});
+          if (nd.res >= 0)
+            h.reads.push_back({window(ts, nd.res, m0, m0 + tm, n0, n0 + tn), ROLE_E});
+          h.writes.push_back(window(ts, nd.out, m0, m0 + tm, n0, n0 + tn));
+          out.push_back(std::move(h));
+        }
+      }
+    }
+  }
+  phases.push_back(std::move(out));
+}
+
+static void lower_ew(const std::vector<TensorRec>& ts, int ni, const NodeRec& nd,
+                     const mk_compile_opts& o, std::vector<std::vector<HInstr>>& phases) {
+  const int64_t rows = ts[nd.out].rows, cols = ts[nd.out].cols;
+  const int64_t er = o.ew_rows, ew = (int64_t)o.ew_cols * o.ew_tiles;
+  std::vector<HInstr> out;
+  for (int64_t rt = 0; rt < cdiv(rows, er); ++rt) {
+    for (int64_t ct = 0; ct < cdiv(cols, ew); ++ct) {
+      const int64_t m0 = rt * er, n0 = ct * ew;
+      HInstr h = make(OP_EW, ni, (int)m0, (int)n0, 0, 0, nd.ewop, 0);
+      for (int i = 0; i < nd.n_in; ++i)
+        h.reads.push_back({window(ts, nd.ins[i], m0, m0 + er, n0, n0 + ew), ROLE_E});
+      h.writes.push_back(window(ts, nd.out, m0, m0 + er, n0, n0 + ew));
+      out.push_back(std::move(h));
+    }
+  }
+  phases.push_back(std::move(out));
+}
+
+static void lower_rows(const std::vector<TensorRec>& ts, int ni, const NodeRec& nd,
+                       const mk_compile_opts& o, uint16_t op,
+                       std::vector<std::vector<HInstr>>& phases) {
+  const int x = nd.ins[0];
+  const int64_t rows = ts[x].rows, nr = o.norm_rows;
+  std::vector<int> outs;
+  for (int id : {nd.out, nd.out_k, nd.out_v})
+    if (id >= 0) outs.push_back(id);
+  std::vector<HInstr> out;
+  for (int64_t rt = 0; rt < cdiv(rows, nr); ++rt) {
+    const int64_t m0 = rt * nr;
+    HInstr h = make(op, ni, (int)m0);
+    h.reads.push_back({window(ts, x, m0, m0 + nr, 0, ts[x].cols), ROLE_E});
+    if (nd.gamma >= 0) h.reads.push_back({whole(ts, nd.gamma), ROLE_E});
+    for (int id : outs) h.writes.push_back(window(ts, id, m0, m0 + nr, 0, ts[id].cols));
+    out.push_back(std::move(h));
+  }
+  phases.push_back(std::move(out));
+}
+
+static void lower_attention(std::vector<TensorRec>& ts, int ni, const NodeRec& nd,
+                            const mk_compile_opts& o, std::vector<std::vector<HInstr>>& phases,
+                            HostPlan* plan) {
+  const int64_t hq = nd.hq, hkv = nd.hkv, d = nd.hd, g_sz = hq / hkv;
+  const int64_t tq = ts[nd.a].rows, tk = ts[nd.b].rows;  // a = q, b = k, b2 = v
+  if (tq == 1) {
+    const int64_t ch = o.attn_chunk, nc = cdiv(tk, ch);
+    TensorRec s;
+    s.dtype = DT_F32;
+    s.rows = hkv * nc * g_sz;
+    s.cols = d + 2;
+    s.ld = d + 2;
+    s.base = (int)ts.size();
+    s.internal = true;
+    const int sid = s.base;
+    ts.push_back(s);
+    plan->node_scratch[ni] = sid;
+    plan->node_chunks[ni] = (int)nc;
+    std::vector<HInstr> part, red;
+    for (int64_t g = 0; g < hkv; ++g) {
+      for (int64_t c = 0; c < nc; ++c) {
+        const int64_t k0 = c * ch, kl = std::min(ch, tk - k0);
+        HInstr h = make(OP_ATTN_PARTIAL, ni, 0, (int)g, (int)k0, (int)kl, (int)c, (int)nc);
+        h.reads.push_back({window(ts, nd.a, 0, 1, g * g_sz * d, (g + 1) * g_sz * d), ROLE_E});
+        h.reads.push_back({window(ts, nd.b, k0, k0 + kl, g * d, (g + 1) * d), ROLE_E});
+        h.reads.push_back({window(ts, nd.b2, k0, k0 + kl, g * d, (g + 1) * d), ROLE_E});
+        const int64_t r0 = (g * nc + c) * g_sz;
+        h.writes.push_back(window(ts, sid, r0, r0 + g_sz, 0, d + 2));
+        part.push_back(std::move(h));
+      }
+    }
+    for (int64_t g = 0; g < hkv; ++g) {
+      HInstr h = make(OP_ATTN_REDUCE, ni, 0, (int)g, 0, 0, 0, (int)nc);
+      const int64_t r0 = g * nc * g_sz;
+      h.reads.push_back({window(ts, sid, r0, r0 + nc * g_sz, 0, d + 2), ROLE_E});
+      h.writes.push_back(window(ts, nd.out, 0, 1, g * g_sz * d, (g + 1) * g_sz * d));
+      red.push_back(std::move(h));
+    }
+    phases.push_back(std::move(part));
+    phases.push_back(std::move(red));
+  } else {
+    const int64_t tt = o.attn_tile_q;
+    std::vector<HInstr> out;
+    for (int64_t t = cdiv(tq, tt) - 1; t >= 0; --t) {
+      const int64_t m0 = t * tt;
+      const int64_t kmax = nd.causal ? std::min(tk, (int64_t)nd.pos0 + m0 + tt) : tk;
+      for (int64_t h = 0; h < hq; ++h) {
+        const int64_t g = h / g_sz;
+        HInstr hi = make(OP_ATTN_PREFILL, ni, (int)m0, (int)h, 0, (int)kmax);
+        hi.reads.push_back({window(ts, nd.a, m0, m0 + tt, h * d, (h + 1) * d), ROLE_E});
+        hi.reads.push_back({window(ts, nd.b, 0, kmax, g * d, (g + 1) * d), ROLE_E});
+        hi.reads.push_back({window(ts, nd.b2, 0, kmax, g * d, (g + 1) * d), ROLE_E});
+        hi.writes.push_back(window(ts, nd.out, m0, m0 + tt, h * d, (h + 1) * d));
+        out.push_back(std::move(hi));
+      }
+    }
+    phases.push_back(std::move(out));
+  }
+}
+
+mk_status lower_graph(const std::vector<TensorRec>& tensors_in, const std::vector<NodeRec>& nodes,
+                      const mk_compile_opts& o, HostPlan* plan) {
+  if (o.n_sm <= 0 || o.cluster <= 0 || o.gemm_tile_m <= 0 || o.gemm_tile_n <= 0 ||
+      o.ew_rows <= 0 || o.ew_cols <= 0 || o.ew_tiles <= 0 || o.norm_rows <= 0 ||
+      o.gemv_tile_n <= 0 || o.gemv_kstep <= 0 || o.attn_chunk <= 0 || o.attn_tile_q <= 0) {
+    set_error("mk_compile: every tile size and n_sm must be positive");
+    return MK_ERR_INVALID_ARG;
+  }
+  std::vector<TensorRec> ts = tensors_in;
+  const int nn = (int)nodes.size();
+  plan->node_scratch.assign(nn, -1);
+  plan->node_splits.assign(nn, 0);
+  plan->node_chunks.assign(nn, 0);
+  plan->node_tile_n.assign(nn, 0);
+  std::vector<std::vector<HInstr>> phases;
+  int n_tiles_sem = 0;
+  for (int ni = 0; ni < nn; ++ni) {
+    const NodeRec& nd = nodes[ni];
+    switch (nd.kind) {
+      case NK_MATMUL: lower_matmul(ts, ni, nd, o, phases, n_tiles_sem, plan); break;
+      case NK_EW: lower_ew(ts, ni, nd, o, phases); break;
+      case NK_RMSNORM: lower_rows(ts, ni, nd, o, OP_RMSNORM, phases); break;
+      case NK_ROPE: lower_rows(ts, ni, nd, o, OP_ROPE, phases); break;
+      case NK_ATTN: lower_attention(ts, ni, nd, o, phases, plan); break;
+      default: set_error("mk_compile: unknown node kind %d", nd.kind); return MK_ERR_INVALID_ARG;
+    }
+  }
+
+  // Phase 1: flatten, padding every phase to a multiple of the cluster size with Noops.
+  std::vector<HInstr> ins;
+  std::vector<int> phase_of;
+  std::vector<std::pair<int, int>> ranges;
+  for (size_t pi = 0; pi < phases.size(); ++pi) {
+    const int start = (int)ins.size();
+    for (auto& h : phases[pi]) ins.push_back(std::move(h));
+    while ((ins.size() - start) % o.cluster) ins.push_back(make(OP_NOOP, 0));
+    ranges.push_back({start, (int)ins.size()});
+    phase_of.resize(ins.size(), (int)pi);
+  }
+
+  // Phase 3: write boxes per base tensor, grouped by phase in phase order.
+  struct PhaseWrites {
+    int phase;
+    std::vector<std::pair<int, Box>> boxes;  // (instruction, box), instruction-ascending
+  };
+  std::vector<std::vector<PhaseWrites>> wtab(ts.size());
+  for (size_t pi = 0; pi < ranges.size(); ++pi) {
+    for (int i = ranges[pi].first; i < ranges[pi].second; ++i) {
+      for (const Box& w : ins[i].writes) {
+        auto& lst = wtab[w.t];
+        if (lst.empty() || lst.back().phase != (int)pi) lst.push_back({(int)pi, {}});
+        lst.back().boxes.push_back({i, w});
+      }
+    }
+  }
+  std::map<std::pair<int, std::vector<int>>, int> keys;
+  std::vector<std::vector<int>> members;
+  std::vector<int32_t> targets;
+  std::vector<int> set;
+  for (size_t ci = 0; ci < ins.size(); ++ci) {
+    HInstr& c = ins[ci];
+    for (const auto& rd : c.reads) {
+      const Box& rb = rd.first;
+      if (rb.empty()) continue;
+      for (const PhaseWrites& pw : wtab[rb.t]) {
+        if (pw.phase >= phase_of[ci]) break;
+        set.clear();
+        for (const auto& ib : pw.boxes)
+          if (meets(rb, ib.second) && (set.empty() || set.back() != ib.first))
+            set.push_back(ib.first);
+        if (set.empty()) continue;
+        auto key = std::make_pair(pw.phase, set);
+        auto it = keys.find(key);
+        int cid;
+        if (it == keys.end()) {
+          cid = (int)targets.size();
+          keys.emplace(key, cid);
+          targets.push_back((int32_t)set.size());
+          members.push_back(set);
+        } else {
+          cid = it->second;
+        }
+        if (rd.second == ROLE_B && (c.rec.op == OP_GEMM || c.rec.op == OP_GEMV))
+          c.rec.flags |= IFLAG_B_DEP;
+        bool seen = false;
+        for (auto& s : c.src) seen |= (s.first == cid);
+        if (!seen) c.src.push_back({cid, (int)set.size()});
+      }
+    }
+  }
+  for (size_t cid = 0; cid < members.size(); ++cid)
+    for (int p : members[cid]) ins[p].dst.push_back((int)cid);
+  const int n_dep = (int)targets.size();
+
+  // GEMV tiles publish through whichever split finishes last: all splits carry split 0's
+  // arrivals and share one semaphore, numbered after the dependency counters.
+  std::vector<int> first_of_tile(n_tiles_sem, -1);
+  for (size_t i = 0; i < ins.size(); ++i)
+    if (ins[i].rec.op == OP_GEMV && ins[i].rec.aux0 == 0) first_of_tile[ins[i].tile] = (int)i;
+  for (auto& h : ins) {
+    if (h.rec.op != OP_GEMV) continue;
+    h.dst = ins[first_of_tile[h.tile]].dst;
+    h.rec.sem = n_dep + h.tile;
+  }
+
+  // Pack.
+  plan->instrs.clear();
+  plan->src_list.clear();
+  plan->dst_list.clear();
+  for (auto& h : ins) {
+    Instr r = h.rec;
+    r.n_src = (int)h.src.size();
+    r.src_off = (int)(plan->src_list.size() / 2);
+    for (auto& s : h.src) {
+      plan->src_list.push_back(s.first);
+      plan->src_list.push_back(s.second);
+    }
+    r.n_dst = (int)h.dst.size();
+    r.dst_off = (int)plan->dst_list.size();
+    for (int d : h.dst) plan->dst_list.push_back(d);
+    plan->instrs.push_back(r);
+  }
+  plan->targets = targets;
+  plan->n_dep = n_dep;
+  plan->n_sem = n_tiles_sem;
+  plan->n_sm = o.n_sm;
+  plan->tensors = ts;
+  return MK_OK;
+}
+
+}  // namespace mk
+
+using namespace mk;
+
+// ------------------------------------------------------------------ C ABI: graph building
+
+extern "C" const char* mk_last_error(void) { return g_err.c_str(); }
+extern "C" int32_t mk_abi_version(void) { return MK_ABI_VERSION; }
+
+extern "C" mk_status mk_graph_create(mk_graph_t* out) {
+  if (!out) {
+    set_error("mk_graph_create: out is NULL");
+    return MK_ERR_INVALID_ARG;
+  }
+  *out = new (std::nothrow) mk_graph();
+  if (!*out) {
+    set_error("mk_graph_create: out of host memory");
+    return MK_ERR_OOM;
+  }
+  return MK_OK;
+}
+
+extern "C" mk_status mk_graph_destroy(mk_graph_t g) {
+  delete g;
+  return MK_OK;
+}
+
+static bool valid_tensor(const mk_graph* g, int id) {
+  return id >= 0 && id < (int)g->tensors.size();
+}
+
+extern "C" mk_status mk_add_tensor(mk_graph_t g, void* dev_ptr, int32_t dtype, int32_t rank,
+                                   const int64_t* shape, const int64_t* strides, int32_t* id) {
+  if (!g || !shape || !id || rank < 1 || rank > 4) {
+    set_error("mk_add_tensor: null argument or rank outside 1..4");
+    return MK_ERR_INVALID_ARG;
+  }
+  if (dtype != MK_F16 && dtype != MK_BF16 && dtype != MK_F32) {
+    set_error("mk_add_tensor: unknown dtype %d", dtype);
+    return MK_ERR_INVALID_ARG;
+  }
+  int64_t st[4];
+  int64_t acc = 1;
+  for (int i = rank - 1; i >= 0; --i) {
+    if (shape[i] < 0) {
+      set_error("mk_add_tensor: negative extent");
+      return MK_ERR_INVALID_ARG;
+    }
+    st[i] = strides ? strides[i] : acc;
+    acc *= std::max<int64_t>(shape[i], 1);
+  }
+  if (st[rank - 1] != 1) {
+    set_error("mk_add_tensor: the innermost dimension must have stride 1");
+    return MK_ERR_UNSUPPORTED;
+  }
+  for (int i = 0; i + 2 < rank; ++i) {
+    if (shape[i] > 1 && st[i] != st[i + 1] * shape[i + 1]) {
+      set_error("mk_add_tensor: outer dimensions must be contiguous over each other");
+      return MK_ERR_UNSUPPORTED;
+    }
+  }
+  TensorRec t;
+  t.ptr = dev_ptr;
+  t.dtype = dtype;
+  t.cols = shape[rank - 1];
+  t.rows = 1;
+  for (int i = 0; i + 1 < rank; ++i) t.rows *= shape[i];
+  t.ld = rank >= 2 ? st[rank - 2] : t.cols;
+  if (t.ld < t.cols) {
+    set_error("mk_add_tensor: row stride %lld smaller than the row length %lld",
+              (long long)t.ld, (long long)t.cols);
+    return MK_ERR_INVALID_ARG;
+  }
+  t.base = (int)g->tensors.size();
+  g->tensors.push_back(t);
+  *id = t.base;
+  return MK_OK;
+}
+
+extern "C" mk_status mk_add_view(mk_graph_t g, int32_t base, int64_t r0, int64_t c0,
+                                 int64_t rows, int64_t cols, int32_t* id) {
+  if (!g || !id || !valid_tensor(g, base)) {
+    set_error("mk_add_view: bad graph or tensor id");
+    return MK_ERR_INVALID_ARG;
+  }
+  const TensorRec& b = g->tensors[base];
+  if (r0 < 0 || c0 < 0 || rows < 0 || cols < 0 || r0 + rows > b.rows || c0 + cols > b.cols) {
+    set_error("mk_add_view: window [%lld+%lld, %lld+%lld] outside the %lldx%lld tensor",
+              (long long)r0, (long long)rows, (long long)c0, (long long)cols, (long long)b.rows,
+              (long long)b.cols);
+    return MK_ERR_INVALID_ARG;
+  }
+  TensorRec v = b;
+  v.rows = rows;
+  v.cols = cols;
+  v.r0 = b.r0 + r0;
+  v.c0 = b.c0 + c0;
+  v.ptr = b.ptr ? (void*)((char*)b.ptr + (r0 * b.ld + c0) * dtype_size(b.dtype)) : nullptr;
+  *id = (int)g->tensors.size();
+  g->tensors.push_back(v);
+  return MK_OK;
+}
+
+static bool same_shape(const mk_graph* g, int a, int64_t rows, int64_t cols) {
+  return g->tensors[a].rows == rows && g->tensors[a].cols == cols;
+}
+
+extern "C" mk_status mk_add_matmul(mk_graph_t g, int32_t a, int32_t b, int32_t out,
+                                   const mk_epilogue* epi, int32_t* node_id) {
+  if (!g || !node_id || !valid_tensor(g, a) || !valid_tensor(g, b) || !valid_tensor(g, out)) {
+    set_error("mk_add_matmul: bad graph, tensor id or node_id pointer");
+    return MK_ERR_INVALID_ARG;
+  }
+  const TensorRec &A = g->tensors[a], &B = g->tensors[b], &C = g->tensors[out];
+  const int64_t m = A.rows, k = A.cols, n = B.cols;
+  if (B.rows != k || !same_shape(g, out, m, n)) {
+    set_error("mk_add_matmul: shapes A %lldx%lld, B %lldx%lld, out %lldx%lld do not chain",
+              (long long)A.rows, (long long)A.cols, (long long)B.rows, (long long)B.cols,
+              (long long)C.rows, (long long)C.cols);
+    return MK_ERR_INVALID_ARG;
+  }
+  if (A.dtype == MK_F32 || B.dtype != A.dtype || C.dtype != A.dtype) {
+    set_error("mk_add_matmul: A, B and out must share one dtype, f16 or bf16");
+    return MK_ERR_UNSUPPORTED;
+  }
+  NodeRec nd;
+  nd.kind = NK_MATMUL;
+  nd.a = a;
+  nd.b = b;
+  nd.out = out;
+  if (epi) {
+    nd.flags = epi->flags;
+    nd.eps = epi->eps;
+    auto need = [&](uint32_t f, int id, int64_t rows, int64_t cols, const char* what) -> bool {
+      if (!(nd.flags & f)) return true;
+      if (!valid_tensor(g, id) || !same_shape(g, id, rows, cols) ||
+          g->tensors[id].dtype != A.dtype) {
+        set_error("mk_add_matmul: %s must be a %lldx%lld tensor of the operands' dtype", what,
+                  (long long)rows, (long long)cols);
+        return false;
+      }
+      return true;
+    };
+    if (!need(MK_EPI_BIAS, epi->bias, m, n, "bias") ||
+        !need(MK_EPI_RESIDUAL, epi->residual, m, n, "residual") ||
+        !need(MK_EPI_RMSNORM_INPUT, epi->gamma, 1, k, "gamma") ||
+        !need(MK_EPI_SILU_MUL, epi->b_up, k, n, "b_up"))
+      return MK_ERR_INVALID_ARG;
+    if (nd.flags & ~(uint32_t)(MK_EPI_BIAS | MK_EPI_RELU | MK_EPI_RESIDUAL |
+                              MK_EPI_RMSNORM_INPUT | MK_EPI_SILU_MUL)) {
+      set_error("mk_add_matmul: unknown epilogue flag bits 0x%x", nd.flags);
+      return MK_ERR_INVALID_ARG;
+    }
+    if (nd.flags & MK_EPI_BIAS) nd.bias = epi->bias;
+    if (nd.flags & MK_EPI_RESIDUAL) nd.res = epi->residual;
+    if (nd.flags & MK_EPI_RMSNORM_INPUT) nd.gamma = epi->gamma;
+    if (nd.flags & MK_EPI_SILU_MUL) nd.b2 = epi->b_up;
+  }
+  *node_id = (int)g->nodes.size();
+  g->nodes.push_back(nd);
+  return MK_OK;
+}
+
+extern "C" mk_status mk_add_elementwise(mk_graph_t g, int32_t op, const int32_t* ins,
+                                        int32_t n_in, int32_t out, const mk_ew_params* p,
+                                        int32_t* node_id) {
+  if (!g || !node_id || !ins || n_in < 1 || n_in > 2 || !valid_tensor(g, out)) {
+    set_error("mk_add_elementwise: bad graph, inputs or output");
+    return MK_ERR_INVALID_ARG;
+  }
+  for (int i = 0; i < n_in; ++i)
+    if (!valid_tensor(g, ins[i])) {
+      set_error("mk_add_elementwise: bad input tensor id %d", ins[i]);
+      return MK_ERR_INVALID_ARG;
+    }
+  const TensorRec& O = g->tensors[out];
+  NodeRec nd;
+  nd.out = out;
+  nd.n_in = n_in;
+  nd.ins[0] = ins[0];
+  if (n_in > 1) nd.ins[1] = ins[1];
+  switch (op) {
+    case MK_EW_ADD:
+    case MK_EW_SILU_MUL:
+    case MK_EW_RELU:
+    case MK_EW_COPY: {
+      const int want = (op == MK_EW_ADD || op == MK_EW_SILU_MUL) ? 2 : 1;
+      if (n_in != want) {
+        set_error("mk_add_elementwise: op %d takes %d inputs", op, want);
+        return MK_ERR_INVALID_ARG;
+      }
+      for (int i = 0; i < n_in; ++i)
+        if (!same_shape(g, ins[i], O.rows, O.cols) || g->tensors[ins[i]].dtype != O.dtype) {
+          set_error("mk_add_elementwise: inputs must match the output's shape and dtype "
+                    "(no broadcasting)");
+          return MK_ERR_INVALID_ARG;
+        }
+      nd.kind = NK_EW;
+      nd.ewop = op;
+      break;
+    }
+    case MK_EW_RMSNORM: {
+      if (!p || n_in != 1 || !same_shape(g, ins[0], O.rows, O.cols) ||
+          !valid_tensor(g, p->gamma) || !same_shape(g, p->gamma, 1, O.cols) ||
+          g->tensors[ins[0]].dtype != O.dtype || g->tensors[p->gamma].dtype != O.dtype) {
+        set_error("mk_add_elementwise: RMSNORM needs x and out of one shape and gamma 1 x cols");
+        return MK_ERR_INVALID_ARG;
+      }
+      nd.kind = NK_RMSNORM;
+      nd.gamma = p->gamma;
+      nd.eps = p->eps;
+      break;
+    }
+    case MK_EW_ROPE: {
+      if (!p || n_in != 1 || p->head_dim <= 0 || p->head_dim % 2 || p->n_q_heads <= 0 ||
+          p->n_kv_heads <= 0 || !valid_tensor(g, p->out_k)) {
+        set_error("mk_add_elementwise: ROPE needs head counts, an even head_dim and out_k");
+        return MK_ERR_INVALID_ARG;
+      }
+      const int64_t d = p->head_dim, r = g->tensors[ins[0]].rows;
+      const int64_t want = (p->n_q_heads + p->n_kv_heads + (p->out_v >= 0 ? p->n_kv_heads : 0)) * d;
+      if (g->tensors[ins[0]].cols != want || !same_shape(g, out, r, p->n_q_heads * d) ||
+          !same_shape(g, p->out_k, r, p->n_kv_heads * d) ||
+          (p->out_v >= 0 && (!valid_tensor(g, p->out_v) ||
+                             !same_shape(g, p->out_v, r, p->n_kv_heads * d)))) {
+        set_error("mk_add_elementwise: ROPE shapes: x [R x %lld], out [R x Hq*d], out_k/out_v "
+                  "[R x Hkv*d]", (long long)want);
+        return MK_ERR_INVALID_ARG;
+      }
+      nd.kind = NK_ROPE;
+      nd.out_k = p->out_k;
+      nd.out_v = p->out_v;
+      nd.hq = p->n_q_heads;
+      nd.hkv = p->n_kv_heads;
+      nd.hd = p->head_dim;
+      nd.pos0 = p->pos0;
+      nd.theta = p->theta;
+      break;
+    }
+    default:
+      set_error("mk_add_elementwise: unknown op %d", op);
+      return MK_ERR_INVALID_ARG;
+  }
+  *node_id = (int)g->nodes.size();
+  g->nodes.push_back(nd);
+  return MK_OK;
+}
+
+extern "C" mk_status mk_add_attention(mk_graph_t g, int32_t q, int32_t k, int32_t v, int32_t out,
+                                      const mk_attn_params* p, int32_t* node_id) {
+  if (!g || !p || !node_id || !valid_tensor(g, q) || !valid_tensor(g, k) ||
+      !valid_tensor(g, v) || !valid_tensor(g, out)) {
+    set_error("mk_add_attention: bad graph, tensor id or params");
+    return MK_ERR_INVALID_ARG;
+  }
+  const int64_t hq = p->n_q_heads, hkv = p->n_kv_heads, d = p->head_dim;
+  if (hq <= 0 || hkv <= 0 || d <= 0 || hq % hkv) {
+    set_error("mk_add_attention: head counts must be positive and Hq divisible by Hkv");
+    return MK_ERR_INVALID_ARG;
+  }
+  const TensorRec &Q = g->tensors[q], &K = g->tensors[k];
+  if (Q.cols != hq * d || K.cols != hkv * d || !same_shape(g, v, K.rows, K.cols) ||
+      !same_shape(g, out, Q.rows, Q.cols) || K.rows < 1) {
+    set_error("mk_add_attention: q [Tq x Hq*d], k and v [Tk x Hkv*d], out [Tq x Hq*d]");
+    return MK_ERR_INVALID_ARG;
+  }
+  NodeRec nd;
+  nd.kind = NK_ATTN;
+  nd.a = q;
+  nd.b = k;
+  nd.b2 = v;
+  nd.out = out;
+  nd.hq = (int)hq;
+  nd.hkv = (int)hkv;
+  nd.hd = (int)d;
+  nd.causal = p->causal;
+  nd.pos0 = p->q_pos0;
+  nd.scale = p->scale;
+  *node_id = (int)g->nodes.size();
+  g->nodes.push_back(nd);
+  return MK_OK;
+}
+
+extern "C" mk_status mk_default_opts(mk_compile_opts* o) {
+  if (!o) {
+    set_error("mk_default_opts: NULL");
+    return MK_ERR_INVALID_ARG;
+  }
+  memset(o, 0, sizeof *o);
+  o->n_sm = 0;
+  o->gemm_tile_m = 128;
+  o->gemm_tile_n = 256;
+  o->cluster = 1;
+  o->ew_rows = 128;
+  o->ew_cols = 128;
+  o->ew_tiles = 1;
+  o->norm_rows = 16;
+  o->gemv_max_m = 8;
+  o->gemv_tile_n = 128;
+  o->gemv_splits = 0;
+  o->gemv_kstep = 128;
+  o->attn_chunk = 64;
+  o->attn_tile_q = 128;
+  o->dry_run = 0;
+  o->timeout_ms = 2000;
+  o->device = -1;
+  o->debug_counter = -1;
+  o->debug_extra = 0;
+  return MK_OK;
+}

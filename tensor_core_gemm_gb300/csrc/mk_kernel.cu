@@ -1,0 +1,942 @@
+// The persistent megakernel: one CTA per SM walks its share of the instruction list.
+//
+// Roles inside a CTA (256 threads):
+//   warp 0      scheduler: publishes instruction descriptors into an 8-slot ring ahead of the
+//               roles and polls the global dependency counters of the oldest published one
+//               ("MegaKittens Internals" §09 controller; §11 barrier wait with acquire).
+//   warp 1      TMA loader: streams operand tiles into a 4-stage shared-memory ring; weight (B)
+//               tiles of an instruction are issued before its activations are ready ("Beating
+//               torch.compile with Megakernels", "TMA Compute Overlap"; MegaKittens §00).
+//   warp 2      MMA issuer: tcgen05.mma into a double-buffered TMEM accumulator ("Hand-writing a
+//               Blackwell GEMM", steps 3 and 8: warp specialisation, persistent kernel with two
+//               accumulator slots).
+//   warp 3      spare.
+//   warps 4-7   compute warpgroup: GEMM epilogue (TMEM -> registers -> fused epilogue -> global),
+//               GEMV tiles, elementwise / RMSNorm / RoPE rows, split-KV attention partial and
+//               combine; publishes finished tiles on the global counters (release).
+// Every wait is bounded: past `timeout_ns` the waiter records MK_ERR_TIMEOUT in the status word,
+// every role drains what it has in flight and the CTA exits normally.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "mk.h"
+#include "mk_ptx.cuh"
+#include "mk_types.h"
+
+namespace mk {
+using namespace ptx;
+
+enum RoleId { R_SCHED = 0, R_LOAD = 1, R_MMA = 2, R_COMPUTE = 3 };
+constexpr unsigned FULL = 0xffffffffu;
+constexpr int kCompute = 128;   // threads of the compute warpgroup
+constexpr int kBarCompute = 1;  // named barrier of the compute warpgroup
+
+struct __align__(1024) Smem {
+  uint8_t stage[kStages][kStageBytes];  // operand ring (1024-byte aligned: 128-byte swizzle)
+  float red[4][8][128];                 // GEMV cross-warp reduction / epilogue exchange
+  float xbuf[8][kGemvRows];             // GEMV activation chunk (normalised when fused)
+  uint8_t slot[kSlots][kSlotBytes];     // instruction record + node entry per slot
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
+  uint64_t instr_ready[kSlots];
+  uint64_t deps_ready[kSlots];
+  uint64_t slot_free[kSlots];
+  uint64_t drain;
+  float rstd[8];
+  uint32_t tmem_base;
+  int32_t flag;
+};
+static_assert(sizeof(Smem) + 1024 <= 232448, "shared memory budget of one CTA");
+
+size_t megakernel_smem_bytes() { return sizeof(Smem) + 1024; }
+
+// ------------------------------------------------------------------ small helpers
+
+__device__ __forceinline__ const Instr& slot_instr(const Smem& s, int slot) {
+  return *reinterpret_cast<const Instr*>(s.slot[slot]);
+}
+__device__ __forceinline__ const Node& slot_node(const Smem& s, int slot) {
+  return *reinterpret_cast<const Node*>(s.slot[slot] + sizeof(Instr));
+}
+__device__ __forceinline__ const void* tmap_at(const Params& p, int i) {
+  return static_cast<const char*>(p.tmaps) + (size_t)i * 128;
+}
+__device__ __forceinline__ int ring_stages(const Instr& in) {
+  if (in.op == OP_GEMM) return (in.klen + kGemmBK - 1) / kGemmBK;
+  if (in.op == OP_GEMV) return (in.klen + kGemvRows - 1) / kGemvRows;
+  return 0;
+}
+__device__ __forceinline__ int instr_index(const Params& p, int it) {
+  return it * p.n_sm + (int)blockIdx.x;
+}
+
+__device__ void report(const Params& p, int code, int instr, int counter, int observed,
+                       int expected, int role, int where) {
+  if (atomicCAS(p.status + ST_CODE, 0, code) == 0) {
+    p.status[ST_INSTR] = instr;
+    p.status[ST_COUNTER] = counter;
+    p.status[ST_OBSERVED] = observed;
+    p.status[ST_EXPECTED] = expected;
+    p.status[ST_SM] = (int)blockIdx.x;
+    p.status[ST_ROLE] = role;
+    p.status[ST_WHERE] = where;
+    __threadfence();
+  }
+}
+
+// Bounded mbarrier wait; false when the limit passed (reported) or another waiter aborted.
+__device__ bool wait_mbar(const Params& p, uint32_t bar, uint32_t parity, int role, int where,
+                          int instr) {
+  if (mbar_try(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try(bar, parity)) return true;
+    if ((n & 15u) == 0) {
+      if (ld_volatile(p.status + ST_CODE) != 0) return false;
+      if (globaltimer() - t0 > p.timeout_ns) {
+        report(p, MK_ERR_TIMEOUT, instr, -1, 0, (int)parity, role, where);
+        return false;
+      }
+    }
+  }
+}
+// Wait used while draining after an abort: ignores the status word, short fixed limit.
+__device__ void wait_mbar_drain(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try(bar, parity))
+    if (globaltimer() - t0 > 200000000ull) return;
+}
+// Compute-warpgroup wait: every thread waits (bounded), then all agree on the outcome so no
+// thread is left alone at a later named barrier.
+__device__ __forceinline__ bool cw_wait(const Params& p, uint32_t bar, uint32_t parity, int where,
+                                        int instr) {
+  const bool ok = wait_mbar(p, bar, parity, R_COMPUTE, where, instr);
+  return bar_and(kBarCompute, kCompute, ok);
+}
+__device__ __forceinline__ void cw_sync() { bar_sync(kBarCompute, kCompute); }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(FULL, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(FULL, v, o));
+  return v;
+}
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
+// 16-bit element conversions (dt: DT_F16 or DT_BF16).
+__device__ __forceinline__ float h2f(uint16_t v, int dt) {
+  return dt == DT_BF16 ? __uint_as_float((uint32_t)v << 16)
+                       : __half2float(__ushort_as_half(v));
+}
+__device__ __forceinline__ uint16_t f2h(float v, int dt) {
+  return dt == DT_BF16 ? __bfloat16_as_ushort(__float2bfloat16_rn(v))
+                       : __half_as_ushort(__float2half_rn(v));
+}
+__device__ __forceinline__ void unpack8(const uint4 raw, int dt, float* x) {
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    x[2 * i] = h2f((uint16_t)(w[i] & 0xffffu), dt);
+    x[2 * i + 1] = h2f((uint16_t)(w[i] >> 16), dt);
+  }
+}
+__device__ __forceinline__ uint4 pack8(const float* x, int dt) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    w[i] = (uint32_t)f2h(x[2 * i], dt) | ((uint32_t)f2h(x[2 * i + 1], dt) << 16);
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+// 8 consecutive elements of an operand at (row, col); data produced inside the kernel is read
+// at L2 (ld.global.cg) so no SM can see a stale L1 line.
+__device__ __forceinline__ void load8(const Operand& o, int row, int col, int dt, float* x) {
+  const uint16_t* ptr = reinterpret_cast<const uint16_t*>(o.ptr) + (size_t)row * o.ld + col;
+  unpack8(__ldcg(reinterpret_cast<const uint4*>(ptr)), dt, x);
+}
+__device__ __forceinline__ void store8(const Operand& o, int row, int col, int dt, const float* x) {
+  uint16_t* ptr = reinterpret_cast<uint16_t*>(o.ptr) + (size_t)row * o.ld + col;
+  *reinterpret_cast<uint4*>(ptr) = pack8(x, dt);
+}
+__device__ __forceinline__ float load1(const Operand& o, int row, int col, int dt) {
+  const uint16_t* ptr = reinterpret_cast<const uint16_t*>(o.ptr) + (size_t)row * o.ld + col;
+  return h2f(__ldcg(reinterpret_cast<const unsigned short*>(ptr)), dt);
+}
+__device__ __forceinline__ void store1(const Operand& o, int row, int col, int dt, float v) {
+  uint16_t* ptr = reinterpret_cast<uint16_t*>(o.ptr) + (size_t)row * o.ld + col;
+  *ptr = f2h(v, dt);
+}
+
+// ------------------------------------------------------------------ scheduler warp
+
+__device__ void run_scheduler(const Params& p, Smem& s) {
+  const int lane = threadIdx.x & 31;
+  int fetched = 0, ready = 0;
+  bool end_published = false;
+  uint32_t idle = 0;
+  uint64_t idle_since = 0;
+  int pend_ctr = -1, pend_obs = 0, pend_tgt = 0;
+  while (true) {
+    bool progress = false;
+    // Publish the next descriptor as soon as its slot is free: roles may run ahead of the
+    // dependency resolution by up to kSlots instructions (the loader prefetches weights).
+    if (!end_published && fetched < ready + kSlots) {
+      const int slot = fetched % kSlots;
+      const uint32_t use = (uint32_t)(fetched / kSlots);
+      if (mbar_try(smem_u32(&s.slot_free[slot]), (use & 1u) ^ 1u)) {
+        uint32_t* dst = reinterpret_cast<uint32_t*>(s.slot[slot]);
+        const int idx = instr_index(p, fetched);
+        if (idx < p.n_instr) {
+          const uint32_t* si = reinterpret_cast<const uint32_t*>(p.instrs + idx);
+          const uint32_t w = lane < 16 ? __ldg(si + lane) : 0u;
+          const int node = __shfl_sync(FULL, (int)w, 1);
+          if (lane < 16) dst[lane] = w;
+          const uint32_t* sn = reinterpret_cast<const uint32_t*>(p.nodes + node);
+          dst[16 + lane] = __ldg(sn + lane);
+          dst[48 + lane] = __ldg(sn + 32 + lane);
+          ++fetched;
+        } else {
+          if (lane == 0) dst[0] = (uint32_t)OP_END;
+          end_published = true;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&s.instr_ready[slot]));
+        progress = true;
+      }
+    }
+    // Resolve the oldest published instruction's sources (one pass, lanes in parallel).
+    if (ready < fetched) {
+      const int slot = ready % kSlots;
+      const Instr& in = slot_instr(s, slot);
+      bool ok = true;
+      pend_ctr = -1;
+      for (int j = lane; j < in.n_src; j += 32) {
+        const int ctr = __ldg(p.src_list + 2 * (in.src_off + j));
+        const int tgt = __ldg(p.src_list + 2 * (in.src_off + j) + 1);
+        const int v = ld_acquire(p.counters + ctr);
+        if (v < tgt) {
+          ok = false;
+          pend_ctr = ctr;
+          pend_obs = v;
+          pend_tgt = tgt;
+        }
+      }
+      if (__all_sync(FULL, ok)) {
+        if (lane == 0) {
+          // later TMA (async-proxy) reads of the producers' data are ordered after the acquire
+          fence_proxy_async_global();
+          mbar_arrive(smem_u32(&s.deps_ready[slot]));
+        }
+        ++ready;
+        progress = true;
+      }
+    }
+    if (end_published && ready == fetched) break;
+    if (progress) {
+      idle = 0;
+      continue;
+    }
+    if (idle++ == 0) {
+      idle_since = globaltimer();
+    } else if ((idle & 15u) == 0) {
+      if (ld_volatile(p.status + ST_CODE) != 0) break;
+      if (globaltimer() - idle_since > p.timeout_ns) {
+        const unsigned who = __ballot_sync(FULL, pend_ctr >= 0);
+        const int src = who ? __ffs(who) - 1 : 0;
+        const int c = __shfl_sync(FULL, pend_ctr, src), o = __shfl_sync(FULL, pend_obs, src),
+                  t = __shfl_sync(FULL, pend_tgt, src);
+        if (lane == 0) report(p, MK_ERR_TIMEOUT, instr_index(p, ready), c, o, t, R_SCHED, 1);
+        break;
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ TMA loader (one thread)
+
+__device__ bool load_gemm(const Params& p, Smem& s, const Instr& in, const Node& nd, int slot,
+                          uint32_t use, uint32_t& fill, int idx) {
+  const int nk = ring_stages(in);
+  if (nk == 0) return true;
+  const bool dual = (nd.flags & EPI_SILU_MUL) != 0;
+  const int tn = nd.tile_n, nbox = tn / 64;
+  const uint32_t bytes = (uint32_t)(kGemmTileM * kGemmBK * 2 + (dual ? 2 : 1) * tn * kGemmBK * 2);
+  const void* ta = tmap_at(p, nd.a.tmap);
+  const void* tb = tmap_at(p, nd.b.tmap);
+  const void* tb2 = dual ? tmap_at(p, nd.b2.tmap) : nullptr;
+  auto load_b = [&](int st, int kb) {
+    const uint32_t base = smem_u32(s.stage[st]) + kGemmTileM * kGemmBK * 2;
+    const uint32_t bar = smem_u32(&s.full[st]);
+    for (int j = 0; j < nbox; ++j)
+      tma_load_2d(base + j * 8192, tb, bar, in.n0 + j * 64, in.k0 + kb * kGemmBK);
+    if (dual)
+      for (int j = 0; j < nbox; ++j)
+        tma_load_2d(base + (nbox + j) * 8192, tb2, bar, in.n0 + j * 64, in.k0 + kb * kGemmBK);
+  };
+  auto load_a = [&](int st, int kb) {
+    tma_load_2d(smem_u32(s.stage[st]), ta, smem_u32(&s.full[st]), in.k0 + kb * kGemmBK, in.m0);
+  };
+  // Weights first: they depend on nothing inside the graph, so they stream into free stages
+  // while the activations are still being produced elsewhere.
+  const int npre = (in.flags & IFLAG_B_DEP) ? 0 : (nk < kStages ? nk : kStages);
+  const uint32_t fill0 = fill;
+  for (int kb = 0; kb < npre; ++kb) {
+    const int st = (int)(fill % kStages);
+    if (!wait_mbar(p, smem_u32(&s.empty[st]), ((fill / kStages) & 1u) ^ 1u, R_LOAD, 11, idx))
+      return false;
+    mbar_expect_tx(smem_u32(&s.full[st]), bytes);
+    load_b(st, kb);
+    ++fill;
+  }
+  if (!wait_mbar(p, smem_u32(&s.deps_ready[slot]), use & 1u, R_LOAD, 12, idx)) return false;
+  fence_proxy_async_global();
+  for (int kb = 0; kb < npre; ++kb) load_a((int)((fill0 + kb) % kStages), kb);
+  for (int kb = npre; kb < nk; ++kb) {
+    const int st = (int)(fill % kStages);
+    if (!wait_mbar(p, smem_u32(&s.empty[st]), ((fill / kStages) & 1u) ^ 1u, R_LOAD, 13, idx))
+      return false;
+    mbar_expect_tx(smem_u32(&s.full[st]), bytes);
+    load_b(st, kb);
+    load_a(st, kb);
+    ++fill;
+  }
+  return true;
+}
+
+__device__ bool load_gemv(const Params& p, Smem& s, const Instr& in, const Node& nd, int slot,
+                          uint32_t use, uint32_t& fill, int idx) {
+  const int nk = ring_stages(in);
+  if (nk == 0) return true;
+  const bool dual = (nd.flags & EPI_SILU_MUL) != 0;
+  const int w = nd.tile_n;
+  const uint32_t part = (uint32_t)(w * kGemvRows * 2);
+  const uint32_t bytes = dual ? 2 * part : part;
+  const void* tb = tmap_at(p, nd.b.tmap);
+  const void* tb2 = dual ? tmap_at(p, nd.b2.tmap) : nullptr;
+  if (in.flags & IFLAG_B_DEP) {
+    if (!wait_mbar(p, smem_u32(&s.deps_ready[slot]), use & 1u, R_LOAD, 14, idx)) return false;
+    fence_proxy_async_global();
+  }
+  for (int kb = 0; kb < nk; ++kb) {
+    const int st = (int)(fill % kStages);
+    if (!wait_mbar(p, smem_u32(&s.empty[st]), ((fill / kStages) & 1u) ^ 1u, R_LOAD, 15, idx))
+      return false;
+    const uint32_t bar = smem_u32(&s.full[st]);
+    mbar_expect_tx(bar, bytes);
+    tma_load_2d(smem_u32(s.stage[st]), tb, bar, in.n0, in.k0 + kb * kGemvRows);
+    if (dual) tma_load_2d(smem_u32(s.stage[st]) + part, tb2, bar, in.n0, in.k0 + kb * kGemvRows);
+    ++fill;
+  }
+  return true;
+}
+
+__device__ void run_loader(const Params& p, Smem& s) {
+  for (int i = 0; i < p.n_tmaps; ++i) tensormap_acquire(tmap_at(p, i));
+  uint32_t fill = 0;
+  for (int it = 0;; ++it) {
+    const int slot = it % kSlots;
+    const uint32_t use = (uint32_t)(it / kSlots);
+    const int idx = instr_index(p, it);
+    if (!wait_mbar(p, smem_u32(&s.instr_ready[slot]), use & 1u, R_LOAD, 10, idx)) break;
+    const Instr& in = slot_instr(s, slot);
+    if (in.op == OP_END) break;
+    const Node& nd = slot_node(s, slot);
+    bool ok = true;
+    if (in.op == OP_GEMM) ok = load_gemm(p, s, in, nd, slot, use, fill, idx);
+    else if (in.op == OP_GEMV) ok = load_gemv(p, s, in, nd, slot, use, fill, idx);
+    if (!ok) break;
+    mbar_arrive(smem_u32(&s.slot_free[slot]));
+  }
+  // Every load issued has landed before the CTA may exit (normally already true).
+  for (uint32_t st = 0; st < (uint32_t)kStages; ++st) {
+    if (fill <= st) continue;
+    const uint32_t fills = (fill - 1 - st) / kStages + 1;
+    wait_mbar_drain(smem_u32(&s.full[st]), (fills - 1) & 1u);
+  }
+}
+
+// ------------------------------------------------------------------ MMA issuer (one thread)
+
+__device__ void run_mma(const Params& p, Smem& s, uint32_t tmem) {
+  uint32_t use = 0, acc_n = 0;
+  bool issued = false;
+  for (int it = 0;; ++it) {
+    const int slot = it % kSlots;
+    const uint32_t u = (uint32_t)(it / kSlots);
+    const int idx = instr_index(p, it);
+    if (!wait_mbar(p, smem_u32(&s.instr_ready[slot]), u & 1u, R_MMA, 20, idx)) break;
+    const Instr& in = slot_instr(s, slot);
+    if (in.op == OP_END) break;
+    const Node& nd = slot_node(s, slot);
+    bool ok = true;
+    if (in.op == OP_GEMM) {
+      const int nk = ring_stages(in);
+      if (nk > 0) {
+        const uint32_t as = acc_n & 1u;
+        if (!wait_mbar(p, smem_u32(&s.acc_empty[as]), ((acc_n >> 1) & 1u) ^ 1u, R_MMA, 21, idx))
+          break;
+        tc_fence_after();
+        const bool dual = (nd.flags & EPI_SILU_MUL) != 0;
+        const int tn = nd.tile_n;
+        const uint32_t idesc = idesc_f16(nd.dtype == DT_BF16, tn);
+        const uint32_t d = tmem + as * 256u;
+        for (int kb = 0; kb < nk && ok; ++kb) {
+          const int st = (int)(use % kStages);
+          if (!wait_mbar(p, smem_u32(&s.full[st]), (use / kStages) & 1u, R_MMA, 22, idx)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(s.stage[st]);
+          const uint32_t b0 = a0 + kGemmTileM * kGemmBK * 2;
+#pragma unroll
+          for (int j = 0; j < kGemmBK / 16; ++j) {
+            // A: K-major, 128-byte rows, 8-row groups 1024 B apart; a 16-wide K slice is 32 B.
+            const uint64_t ad = sdesc_sw128(a0 + j * 32, 16, 1024);
+            // B: N-major, 64-column atoms 8 KB apart (LBO), 8-row K groups 1024 B apart (SBO);
+            // a 16-deep K slice is 16 rows of 128 B.
+            const uint64_t bd = sdesc_sw128(b0 + j * 2048, 8192, 1024);
+            const uint32_t acc = (kb | j) != 0;
+            tc_mma_f16(d, ad, bd, idesc, acc);
+            if (dual) {
+              const uint64_t bd2 = sdesc_sw128(b0 + (tn / 64) * 8192 + j * 2048, 8192, 1024);
+              tc_mma_f16(d + (uint32_t)tn, ad, bd2, idesc, acc);
+            }
+          }
+          tc_commit(smem_u32(&s.empty[st]));  // the stage is free once these MMAs complete
+          issued = true;
+          ++use;
+        }
+        if (!ok) break;
+        tc_commit(smem_u32(&s.acc_full[as]));
+        ++acc_n;
+      }
+    } else if (in.op == OP_GEMV) {
+      use += (uint32_t)ring_stages(in);  // stages consumed by the compute warpgroup
+    }
+    mbar_arrive(smem_u32(&s.slot_free[slot]));
+  }
+  if (issued) {
+    tc_commit(smem_u32(&s.drain));
+    wait_mbar_drain(smem_u32(&s.drain), 0);
+  }
+}
+
+// ------------------------------------------------------------------ compute warpgroup bodies
+
+// GEMM epilogue: TMEM -> registers (one row per thread), fused epilogue, 16-byte stores.
+__device__ bool gemm_epilogue(const Params& p, Smem& s, const Instr& in, const Node& nd, int slot,
+                              uint32_t use, uint32_t tmem, uint32_t& acc_n, int idx) {
+  const int ct = (int)threadIdx.x - (kThreads - kCompute);
+  const int q = ct >> 5, lane = ct & 31;
+  if (!cw_wait(p, smem_u32(&s.deps_ready[slot]), use & 1u, 30, idx)) return false;
+  const int nk = ring_stages(in);
+  const uint32_t as = acc_n & 1u;
+  if (nk > 0) {
+    if (!cw_wait(p, smem_u32(&s.acc_full[as]), (acc_n >> 1) & 1u, 31, idx)) return false;
+    tc_fence_after();
+  }
+  const int dt = nd.dtype;
+  const bool dual = (nd.flags & EPI_SILU_MUL) != 0;
+  const bool bias = (nd.flags & EPI_BIAS) != 0, relu = (nd.flags & EPI_RELU) != 0,
+             res = (nd.flags & EPI_RESIDUAL) != 0;
+  const int tn = nd.tile_n;
+  const int row = in.m0 + q * 32 + lane;
+  const uint32_t tb = tmem + as * 256u + ((uint32_t)(q * 32) << 16);
+  for (int c = 0; c < tn; c += 32) {
+    uint32_t r[32], r2[32];
+    if (nk > 0) {
+      tmem_ld32(tb + (uint32_t)c, r);
+      if (dual) tmem_ld32(tb + (uint32_t)(tn + c), r2);
+      tmem_ld_wait();
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) r[i] = r2[i] = 0u;
+    }
+    if (row < nd.M) {
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        const int col = in.n0 + c + g * 8;
+        if (col >= nd.N) continue;
+        float v[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          v[e] = __uint_as_float(r[g * 8 + e]);
+          if (dual) v[e] = silu(v[e]) * __uint_as_float(r2[g * 8 + e]);
+        }
+        if (bias) {
+          float b[8];
+          load8(nd.bias, row, col, dt, b);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) v[e] += b[e];
+        }
+        if (relu) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) v[e] = fmaxf(v[e], 0.0f);
+        }
+        if (res) {
+          float b[8];
+          load8(nd.res, row, col, dt, b);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) v[e] += b[e];
+        }
+        store8(nd.out, row, col, dt, v);
+      }
+    }
+  }
+  if (nk > 0) {
+    tc_fence_before();
+    cw_sync();
+    if (ct == 0) mbar_arrive(smem_u32(&s.acc_empty[as]));
+    ++acc_n;
+  }
+  return true;
+}
+
+// GEMV tile: out[0..M) x [n0, n0 + w) for one K chunk; split partials reduced by the last split.
+__device__ bool gemv(const Params& p, Smem& s, const Instr& in, const Node& nd, int slot,
+                     uint32_t use, uint32_t& ring, bool* publish, int idx) {
+  const int ct = (int)threadIdx.x - (kThreads - kCompute);
+  const int wp = ct >> 5, lane = ct & 31;
+  if (!cw_wait(p, smem_u32(&s.deps_ready[slot]), use & 1u, 40, idx)) return false;
+  const int M = nd.M, dt = nd.dtype;
+  const bool dual = (nd.flags & EPI_SILU_MUL) != 0;
+  const bool norm = (nd.flags & EPI_RMSNORM_INPUT) != 0;
+  const int wcols = nd.tile_n;
+  if (norm) {
+    // RMS statistic of each whole input row (the norm is fused into the GEMV, as a flag).
+    for (int m = wp; m < M; m += 4) {
+      float ss = 0.f;
+      for (int k = lane * 8; k < nd.K; k += 256) {
+        float x[8];
+        load8(nd.a, m, k, dt, x);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ss += x[e] * x[e];
+      }
+      ss = warp_sum(ss);
+      if (lane == 0) s.rstd[m] = rsqrtf(ss / (float)nd.K + nd.eps);
+    }
+    cw_sync();
+  }
+  float acc[8][4];
+#pragma unroll
+  for (int m = 0; m < 8; ++m)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[m][e] = 0.f;
+  const int nk = ring_stages(in);
+  const int kend = in.k0 + in.klen;
+  for (int kb = 0; kb < nk; ++kb) {
+    const int k = in.k0 + kb * kGemvRows + ct;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      if (m < M) {
+        float x = 0.f;
+        if (k < kend) {
+          x = load1(nd.a, m, k, dt);
+          if (norm) x = x * s.rstd[m] * load1(nd.gamma, 0, k, dt);
+        }
+        s.xbuf[m][ct] = x;
+      }
+    }
+    cw_sync();
+    const int st = (int)(ring % kStages);
+    if (!cw_wait(p, smem_u32(&s.full[st]), (ring / kStages) & 1u, 41, idx)) return false;
+    const uint16_t* W = reinterpret_cast<const uint16_t*>(s.stage[st]);
+    const uint16_t* U = W + wcols * kGemvRows;
+#pragma unroll 4
+    for (int r = 0; r < 32; ++r) {
+      const int kk = wp * 32 + r;
+      float f[4];
+      if (!dual) {
+        const uint2 raw = *reinterpret_cast<const uint2*>(W + kk * wcols + lane * 4);
+        f[0] = h2f((uint16_t)(raw.x & 0xffffu), dt);
+        f[1] = h2f((uint16_t)(raw.x >> 16), dt);
+        f[2] = h2f((uint16_t)(raw.y & 0xffffu), dt);
+        f[3] = h2f((uint16_t)(raw.y >> 16), dt);
+      } else {
+        const uint32_t g = *reinterpret_cast<const uint32_t*>(W + kk * wcols + lane * 2);
+        const uint32_t u2 = *reinterpret_cast<const uint32_t*>(U + kk * wcols + lane * 2);
+        f[0] = h2f((uint16_t)(g & 0xffffu), dt);
+        f[1] = h2f((uint16_t)(g >> 16), dt);
+        f[2] = h2f((uint16_t)(u2 & 0xffffu), dt);
+        f[3] = h2f((uint16_t)(u2 >> 16), dt);
+      }
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        if (m < M) {
+          const float xv = s.xbuf[m][kk];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[m][e] = fmaf(xv, f[e], acc[m][e]);
+        }
+      }
+    }
+    cw_sync();
+    if (ct == 0) mbar_arrive(smem_u32(&s.empty[st]));
+    ++ring;
+  }
+  // Cross-warp reduction: thread ct then owns column ct of [gate | up] (or of the tile).
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    if (m < M) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int col = dual ? (e < 2 ? lane * 2 + e : 64 + lane * 2 + (e - 2)) : lane * 4 + e;
+        s.red[wp][m][col] = acc[m][e];
+      }
+    }
+  }
+  cw_sync();
+  float val[8];
+#pragma unroll
+  for (int m = 0; m < 8; ++m)
+    val[m] = (m < M) ? s.red[0][m][ct] + s.red[1][m][ct] + s.red[2][m][ct] + s.red[3][m][ct] : 0.f;
+  const int S = in.aux1;
+  const int which = dual ? (ct >> 6) : 0;
+  const int n = in.n0 + (dual ? (ct & 63) : ct);
+  const bool colok = (dual || ct < wcols) && n < nd.N;
+  if (S > 1) {
+    float* part = reinterpret_cast<float*>(nd.scratch.ptr);
+    if (colok)
+      for (int m = 0; m < M; ++m)
+        __stcg(part + (size_t)in.aux0 * nd.ldp + ((size_t)which * M + m) * nd.N + n, val[m]);
+    __threadfence();
+    cw_sync();
+    if (ct == 0) s.flag = (atomicAdd(p.counters + in.sem, 1) == S - 1);
+    cw_sync();
+    if (!s.flag) {
+      *publish = false;
+      return true;
+    }
+    __threadfence();
+    if (colok) {
+      for (int m = 0; m < M; ++m) {
+        float t = 0.f;
+        for (int q = 0; q < S; ++q)
+          t += __ldcg(part + (size_t)q * nd.ldp + ((size_t)which * M + m) * nd.N + n);
+        val[m] = t;
+      }
+    }
+  }
+  cw_sync();
+#pragma unroll
+  for (int m = 0; m < 8; ++m)
+    if (m < M) s.red[0][m][ct] = val[m];
+  cw_sync();
+  if ((!dual || ct < 64) && colok) {
+    for (int m = 0; m < M; ++m) {
+      float y = dual ? silu(s.red[0][m][ct]) * s.red[0][m][64 + ct] : val[m];
+      if (nd.flags & EPI_BIAS) y += load1(nd.bias, m, n, dt);
+      if (nd.flags & EPI_RELU) y = fmaxf(y, 0.f);
+      if (nd.flags & EPI_RESIDUAL) y += load1(nd.res, m, n, dt);
+      store1(nd.out, m, n, dt, y);
+    }
+  }
+  *publish = true;
+  return true;
+}
+
+__device__ void ew_body(const Instr& in, const Node& nd) {
+  const int ct = (int)threadIdx.x - (kThreads - kCompute);
+  const int rows = min(nd.tile_m, nd.M - in.m0), cols = min(nd.tile_n, nd.N - in.n0);
+  const int nv = cols / 8, dt = nd.dtype;
+  for (int v = ct; v < rows * nv; v += kCompute) {
+    const int m = in.m0 + v / nv, n = in.n0 + (v % nv) * 8;
+    float a[8], b[8], y[8];
+    load8(nd.a, m, n, dt, a);
+    if (nd.ewop == EWOP_ADD || nd.ewop == EWOP_SILU_MUL) load8(nd.b, m, n, dt, b);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      switch (nd.ewop) {
+        case EWOP_ADD: y[e] = a[e] + b[e]; break;
+        case EWOP_RELU: y[e] = fmaxf(a[e], 0.f); break;
+        case EWOP_SILU_MUL: y[e] = silu(a[e]) * b[e]; break;
+        default: y[e] = a[e]; break;
+      }
+    }
+    store8(nd.out, m, n, dt, y);
+  }
+}
+
+__device__ void rmsnorm_body(const Instr& in, const Node& nd) {
+  const int ct = (int)threadIdx.x - (kThreads - kCompute);
+  const int wp = ct >> 5, lane = ct & 31;
+  const int rows = min(nd.tile_m, nd.M - in.m0), dt = nd.dtype;
+  for (int r = wp; r < rows; r += 4) {
+    const int m = in.m0 + r;
+    float ss = 0.f;
+    for (int k = lane * 8; k < nd.N; k += 256) {
+      float x[8];
+      load8(nd.a, m, k, dt, x);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ss += x[e] * x[e];
+    }
+    const float rstd = rsqrtf(warp_sum(ss) / (float)nd.N + nd.eps);
+    for (int k = lane * 8; k < nd.N; k += 256) {
+      float x[8], g[8];
+      load8(nd.a, m, k, dt, x);
+      load8(nd.gamma, 0, k, dt, g);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] = x[e] * rstd * g[e];
+      store8(nd.out, m, k, dt, x);
+    }
+  }
+}
+
+__device__ void rope_body(const Instr& in, const Node& nd) {
+  const int ct = (int)threadIdx.x - (kThreads - kCompute);
+  const int rows = min(nd.tile_m, nd.M - in.m0), dt = nd.dtype;
+  const int hd = nd.hd, half = hd / 2, nh = nd.hq + nd.hkv;
+  const int pairs = nh * half;
+  const float l2t = log2f(nd.theta);
+  for (int v = ct; v < rows * pairs; v += kCompute) {
+    const int m = in.m0 + v / pairs, pr = v % pairs;
+    const int h = pr / half, i = pr % half;
+    const float x1 = load1(nd.a, m, h * hd + i, dt), x2 = load1(nd.a, m, h * hd + i + half, dt);
+    const float inv = exp2f(-(2.0f * (float)i / (float)hd) * l2t);
+    float sn, cs;
+    sincosf((float)(nd.pos0 + m) * inv, &sn, &cs);
+    const float y1 = x1 * cs - x2 * sn, y2 = x2 * cs + x1 * sn;
+    if (h < nd.hq) {
+      store1(nd.out, m, h * hd + i, dt, y1);
+      store1(nd.out, m, h * hd + i + half, dt, y2);
+    } else {
+      store1(nd.out_k, m, (h - nd.hq) * hd + i, dt, y1);
+      store1(nd.out_k, m, (h - nd.hq) * hd + i + half, dt, y2);
+    }
+  }
+  if (nd.out_v.ptr) {
+    const int nvv = nd.hkv * hd / 8;
+    for (int v = ct; v < rows * nvv; v += kCompute) {
+      const int m = in.m0 + v / nvv, c = (v % nvv) * 8;
+      float x[8];
+      load8(nd.a, m, nh * hd + c, dt, x);
+      store8(nd.out_v, m, c, dt, x);
+    }
+  }
+}
+
+// Split-KV partial for kv group g = n0 and keys [k0, k0 + klen): per query head of the group
+// m = max s, l = sum e^{s - m}, o = sum e^{s - m} v   (head_dim 64, up to 128 keys).
+__device__ void attn_partial_body(const Instr& in, const Node& nd) {
+  const int ct = (int)threadIdx.x - (kThreads - kCompute);
+  const int wp = ct >> 5, lane = ct & 31;
+  const int g = in.n0, G = nd.hq / nd.hkv, C = in.aux1, c = in.aux0;
+  const int k0 = in.k0, kl = in.klen;
+  const __nv_bfloat16* K = reinterpret_cast<const __nv_bfloat16*>(nd.b.ptr);
+  const __nv_bfloat16* V = reinterpret_cast<const __nv_bfloat16*>(nd.b2.ptr);
+  for (int hh = wp; hh < G; hh += 4) {
+    const int h = g * G + hh;
+    float qv[64];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) load8(nd.a, 0, h * 64 + i * 8, DT_BF16, qv + i * 8);
+    float sc[4], pr[4];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int j = lane + 32 * t;
+      float sv = -INFINITY;
+      if (j < kl) {
+        const uint4* kr = reinterpret_cast<const uint4*>(K + (size_t)(k0 + j) * nd.b.ld + g * 64);
+        float dot = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          float kx[8];
+          unpack8(__ldcg(kr + i), DT_BF16, kx);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) dot = fmaf(qv[i * 8 + e], kx[e], dot);
+        }
+        sv = dot * nd.scale;
+      }
+      sc[t] = sv;
+      mx = fmaxf(mx, sv);
+    }
+    mx = warp_max(mx);
+    float l = 0.f;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      pr[t] = (lane + 32 * t < kl) ? expf(sc[t] - mx) : 0.f;
+      l += pr[t];
+    }
+    l = warp_sum(l);
+    float o0 = 0.f, o1 = 0.f;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      for (int jj = 0; jj < 32; ++jj) {
+        const int j = t * 32 + jj;
+        if (j >= kl) break;
+        const float pj = __shfl_sync(FULL, pr[t], jj);
+        const uint32_t vv = __ldcg(reinterpret_cast<const unsigned int*>(
+            V + (size_t)(k0 + j) * nd.b2.ld + g * 64 + lane * 2));
+        o0 = fmaf(pj, __uint_as_float(vv << 16), o0);
+        o1 = fmaf(pj, __uint_as_float(vv & 0xffff0000u), o1);
+      }
+    }
+    float* row = reinterpret_cast<float*>(nd.scratch.ptr) + ((size_t)(g * C + c) * G + hh) * nd.scratch.ld;
+    __stcg(reinterpret_cast<float2*>(row + lane * 2), make_float2(o0, o1));
+    if (lane == 0) {
+      __stcg(row + 64, mx);
+      __stcg(row + 65, l);
+    }
+  }
+}
+
+// LSE merge of one kv group's partials: M = max m_c, L = sum l_c e^{m_c-M},
+// O = sum o_c e^{m_c-M} / L.
+__device__ void attn_reduce_body(const Instr& in, const Node& nd) {
+  const int ct = (int)threadIdx.x - (kThreads - kCompute);
+  const int wp = ct >> 5, lane = ct & 31;
+  const int g = in.n0, G = nd.hq / nd.hkv, C = in.aux1;
+  const float* sc = reinterpret_cast<const float*>(nd.scratch.ptr);
+  const int ld = nd.scratch.ld;
+  for (int hh = wp; hh < G; hh += 4) {
+    const int h = g * G + hh;
+    float mx = -INFINITY;
+    for (int c = lane; c < C; c += 32) mx = fmaxf(mx, __ldcg(sc + ((size_t)(g * C + c) * G + hh) * ld + 64));
+    mx = warp_max(mx);
+    float L = 0.f, o0 = 0.f, o1 = 0.f;
+    for (int c = 0; c < C; ++c) {
+      const float* row = sc + ((size_t)(g * C + c) * G + hh) * ld;
+      const float w = expf(__ldcg(row + 64) - mx);
+      L += __ldcg(row + 65) * w;
+      const float2 o = __ldcg(reinterpret_cast<const float2*>(row + lane * 2));
+      o0 = fmaf(o.x, w, o0);
+      o1 = fmaf(o.y, w, o1);
+    }
+    const float inv = 1.0f / L;
+    __nv_bfloat162 y = __floats2bfloat162_rn(o0 * inv, o1 * inv);
+    *reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(nd.out.ptr) + h * 64 +
+                                       lane * 2) = y;
+  }
+}
+
+__device__ void run_compute(const Params& p, Smem& s, uint32_t tmem) {
+  const int ct = (int)threadIdx.x - (kThreads - kCompute);
+  uint32_t ring = 0, acc_n = 0;
+  for (int it = 0;; ++it) {
+    const int slot = it % kSlots;
+    const uint32_t use = (uint32_t)(it / kSlots);
+    const int idx = instr_index(p, it);
+    if (!cw_wait(p, smem_u32(&s.instr_ready[slot]), use & 1u, 32, idx)) break;
+    const Instr& in = slot_instr(s, slot);
+    if (in.op == OP_END) break;
+    const Node& nd = slot_node(s, slot);
+    bool ok = true, publish = true;
+    switch (in.op) {
+      case OP_GEMM:
+        ok = gemm_epilogue(p, s, in, nd, slot, use, tmem, acc_n, idx);
+        ring += (uint32_t)ring_stages(in);
+        break;
+      case OP_GEMV:
+        ok = gemv(p, s, in, nd, slot, use, ring, &publish, idx);
+        break;
+      case OP_NOOP:
+        break;
+      default:
+        ok = cw_wait(p, smem_u32(&s.deps_ready[slot]), use & 1u, 33, idx);
+        if (!ok) break;
+        if (in.op == OP_EW) ew_body(in, nd);
+        else if (in.op == OP_RMSNORM) rmsnorm_body(in, nd);
+        else if (in.op == OP_ROPE) rope_body(in, nd);
+        else if (in.op == OP_ATTN_PARTIAL) attn_partial_body(in, nd);
+        else if (in.op == OP_ATTN_REDUCE) attn_reduce_body(in, nd);
+        else {
+          if (ct == 0) report(p, MK_ERR_DEVICE_CHECK, idx, -1, in.op, 0, R_COMPUTE, 34);
+          ok = false;
+        }
+        break;
+    }
+    if (!ok) break;
+    // Publish: every thread's stores are ordered before the release increments.
+    __threadfence();
+    cw_sync();
+    if (ct == 0) {
+      if (publish && in.n_dst > 0) {
+        fence_proxy_async_global();
+        for (int j = 0; j < in.n_dst; ++j)
+          red_release_add(p.counters + __ldg(p.dst_list + in.dst_off + j), 1);
+      }
+      mbar_arrive(smem_u32(&s.slot_free[slot]));
+    }
+  }
+}
+
+// ------------------------------------------------------------------ the kernel
+
+__global__ void __launch_bounds__(kThreads, 1) megakernel(const __grid_constant__ Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                     ~static_cast<uintptr_t>(1023));
+  const int warp = (int)threadIdx.x >> 5, lane = (int)threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(smem_u32(&s.full[i]), 1);
+      mbar_init(smem_u32(&s.empty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&s.acc_full[i]), 1);
+      mbar_init(smem_u32(&s.acc_empty[i]), 1);
+    }
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(smem_u32(&s.instr_ready[i]), 1);
+      mbar_init(smem_u32(&s.deps_ready[i]), 1);
+      mbar_init(smem_u32(&s.slot_free[i]), 3);  // loader, MMA issuer, compute warpgroup
+    }
+    mbar_init(smem_u32(&s.drain), 1);
+    mbar_fence_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(smem_u32(&s.tmem_base), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s.tmem_base;
+
+  if (warp == 0) {
+    run_scheduler(p, s);
+  } else if (warp == 1) {
+    if (lane == 0) run_loader(p, s);
+    __syncwarp();
+  } else if (warp == 2) {
+    if (lane == 0) run_mma(p, s, tmem);
+    __syncwarp();
+  } else if (warp >= 4) {
+    run_compute(p, s, tmem);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ------------------------------------------------------------------ host launch stub
+
+cudaError_t configure_megakernel(size_t smem) {
+  return cudaFuncSetAttribute(megakernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+}
+
+cudaError_t launch_megakernel(const Params& p, int grid, size_t smem, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs co-resident (they wait on each other)
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, megakernel, p);
+}
+
+}  // namespace mk

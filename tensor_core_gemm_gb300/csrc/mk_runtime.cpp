@@ -1,0 +1,653 @@
+// Plan compilation (device half), launch, status and introspection of the C ABI.
+//
+// mk_compile uploads once: instruction list, node table, dependency lists, tensor maps and a
+// zero-initialised counter array ("Implementing a Mega Kernel for B300" §6 uploads descriptors
+// and a pointer table once; "MegaKittens Internals" §07 builds tensor maps on the host with
+// cuTensorMapEncodeTiled). Every mk_run zeroes the counters on the caller's stream and launches
+// the persistent kernel once (§07 "Every call: launch").
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <string.h>
+
+#include <algorithm>
+#include <new>
+
+#include "mk_internal.h"
+
+namespace mk {
+// Launch stub and shared-memory size, defined next to the kernel.
+cudaError_t launch_megakernel(const Params& p, int grid, size_t smem, cudaStream_t s);
+cudaError_t configure_megakernel(size_t smem);
+size_t megakernel_smem_bytes();
+}  // namespace mk
+
+using namespace mk;
+
+struct mk_plan {
+  HostPlan hp;
+  mk_compile_opts opts{};
+  std::vector<Node> nodes;
+  bool on_device = false;
+  int device = 0;
+  char* d_mem = nullptr;
+  size_t scratch_bytes = 0;
+  size_t smem = 0;
+  int grid = 0;
+  Params params{};
+};
+
+#define CUDA_TRY(call)                                                                    \
+  do {                                                                                    \
+    cudaError_t e_ = (call);                                                              \
+    if (e_ != cudaSuccess) {                                                              \
+      set_error("%s failed: %s (%s:%d)", #call, cudaGetErrorString(e_), __FILE__, __LINE__); \
+      return MK_ERR_CUDA;                                                                 \
+    }                                                                                     \
+  } while (0)
+
+// ------------------------------------------------------------------ validation
+
+static void node_regions(const mk_graph* g, const NodeRec& nd, std::vector<int>& reads,
+                         std::vector<int>& writes) {
+  reads.clear();
+  writes.clear();
+  for (int id : {nd.a, nd.b, nd.b2, nd.bias, nd.res, nd.gamma, nd.ins[0], nd.ins[1]})
+    if (id >= 0) reads.push_back(id);
+  for (int id : {nd.out, nd.out_k, nd.out_v})
+    if (id >= 0) writes.push_back(id);
+  (void)g;
+}
+
+static Box full_box(const std::vector<TensorRec>& ts, int id) {
+  const TensorRec& v = ts[id];
+  Box b;
+  b.t = v.base;
+  b.r0 = v.r0;
+  b.r1 = v.r0 + v.rows;
+  b.c0 = v.c0;
+  b.c1 = v.c0 + v.cols;
+  return b;
+}
+
+// No node may write a region that it or an earlier node reads or writes: every dependency is
+// then read-after-write and carried by a counter, and a run never races with itself.
+static mk_status check_hazards(const mk_graph* g) {
+  std::vector<int> r_i, w_i, r_j, w_j;
+  for (size_t i = 0; i < g->nodes.size(); ++i) {
+    node_regions(g, g->nodes[i], r_i, w_i);
+    for (size_t j = 0; j <= i; ++j) {
+      node_regions(g, g->nodes[j], r_j, w_j);
+      for (int w : w_i) {
+        const Box bw = full_box(g->tensors, w);
+        for (int other : r_j)
+          if (meets(bw, full_box(g->tensors, other))) {
+            set_error("mk_compile: node %zu writes tensor %d over a region node %zu reads", i, w, j);
+            return MK_ERR_HAZARD;
+          }
+        if (j == i) continue;
+        for (int other : w_j)
+          if (meets(bw, full_box(g->tensors, other))) {
+            set_error("mk_compile: nodes %zu and %zu write overlapping regions", j, i);
+            return MK_ERR_HAZARD;
+          }
+      }
+    }
+  }
+  return MK_OK;
+}
+
+static bool aligned16(const TensorRec& t) {
+  return ((uintptr_t)t.ptr % 16) == 0 && (t.ld * dtype_size(t.dtype)) % 16 == 0;
+}
+
+namespace mk {
+mk_status check_kernel_support(const std::vector<TensorRec>& ts, const std::vector<NodeRec>& nodes,
+                               const mk_compile_opts& o) {
+  if (o.gemm_tile_m != kGemmTileM || o.cluster != 1) {
+    set_error("mk_compile: the kernel runs 128-row GEMM tiles with cluster 1");
+    return MK_ERR_UNSUPPORTED;
+  }
+  if (o.gemm_tile_n != 64 && o.gemm_tile_n != 128 && o.gemm_tile_n != 256) {
+    set_error("mk_compile: gemm_tile_n must be 64, 128 or 256");
+    return MK_ERR_UNSUPPORTED;
+  }
+  if (o.gemv_tile_n != 128 || o.gemv_kstep % kGemvRows || o.gemv_max_m > 8 || o.gemv_max_m < 0) {
+    set_error("mk_compile: the kernel runs 128-column GEMV tiles, K chunks a multiple of %d, "
+              "M <= 8", kGemvRows);
+    return MK_ERR_UNSUPPORTED;
+  }
+  if (o.attn_chunk > kAttnChunkMax) {
+    set_error("mk_compile: attn_chunk must be <= %d", kAttnChunkMax);
+    return MK_ERR_UNSUPPORTED;
+  }
+  for (size_t i = 0; i < nodes.size(); ++i) {
+    const NodeRec& nd = nodes[i];
+    std::vector<int> all;
+    for (int id : {nd.a, nd.b, nd.b2, nd.bias, nd.res, nd.gamma, nd.ins[0], nd.ins[1], nd.out,
+                   nd.out_k, nd.out_v})
+      if (id >= 0) all.push_back(id);
+    for (int id : all) {
+      if (!ts[id].ptr && ts[id].rows * ts[id].cols > 0) {
+        set_error("mk_compile: node %zu uses tensor %d with a NULL device pointer", i, id);
+        return MK_ERR_INVALID_ARG;
+      }
+      if (!aligned16(ts[id]) || ts[id].cols % 8) {
+        set_error("mk_compile: node %zu tensor %d: start address and row stride must be 16-byte "
+                  "aligned and cols a multiple of 8", i, id);
+        return MK_ERR_UNSUPPORTED;
+      }
+    }
+    if (nd.kind == NK_MATMUL) {
+      if ((nd.flags & MK_EPI_SILU_MUL) && ts[nd.a].rows > o.gemv_max_m && o.gemm_tile_n < 128) {
+        set_error("mk_compile: SILU_MUL GEMM tiles need gemm_tile_n >= 128");
+        return MK_ERR_UNSUPPORTED;
+      }
+      if ((nd.flags & MK_EPI_RMSNORM_INPUT) && ts[nd.a].rows > o.gemv_max_m) {
+        set_error("mk_compile: RMS_NORM_INPUT is fused into GEMV tiles only (M <= gemv_max_m); "
+                  "use an RMSNORM node before a GEMM");
+        return MK_ERR_UNSUPPORTED;
+      }
+    }
+    if (nd.kind == NK_ATTN) {
+      if (nd.hd != 64) {
+        set_error("mk_compile: attention runs head_dim 64");
+        return MK_ERR_UNSUPPORTED;
+      }
+      for (int id : {nd.a, nd.b, nd.b2, nd.out})
+        if (ts[id].dtype != DT_BF16) {
+          set_error("mk_compile: attention tensors are bf16");
+          return MK_ERR_UNSUPPORTED;
+        }
+      if (ts[nd.a].rows > 1) {
+        set_error("mk_compile: causal prefill attention tiles are not built in this version");
+        return MK_ERR_UNSUPPORTED;
+      }
+    }
+  }
+  return MK_OK;
+}
+}  // namespace mk
+
+// ------------------------------------------------------------------ tensor maps
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+  }
+  return fn;
+}
+
+struct MapKey {
+  uintptr_t ptr;
+  int64_t rows, cols, ld;
+  int dtype, box_c, box_r, swz;
+  bool operator==(const MapKey& o) const {
+    return ptr == o.ptr && rows == o.rows && cols == o.cols && ld == o.ld && dtype == o.dtype &&
+           box_c == o.box_c && box_r == o.box_r && swz == o.swz;
+  }
+};
+
+static mk_status add_map(std::vector<MapKey>& keys, std::vector<CUtensorMap>& maps,
+                         const TensorRec& t, int box_c, int box_r, bool swizzle128, int* idx) {
+  MapKey k{(uintptr_t)t.ptr, t.rows, t.cols, t.ld, t.dtype, box_c, box_r, swizzle128 ? 1 : 0};
+  for (size_t i = 0; i < keys.size(); ++i)
+    if (keys[i] == k) {
+      *idx = (int)i;
+      return MK_OK;
+    }
+  if ((int)maps.size() >= kMaxTmaps) {
+    set_error("mk_compile: more than %d distinct TMA operands", kMaxTmaps);
+    return MK_ERR_UNSUPPORTED;
+  }
+  auto fn = encode_fn();
+  if (!fn) {
+    set_error("mk_compile: cuTensorMapEncodeTiled is unavailable (no CUDA driver?)");
+    return MK_ERR_CUDA;
+  }
+  CUtensorMap m;
+  memset(&m, 0, sizeof m);
+  cuuint64_t dims[2] = {(cuuint64_t)t.cols, (cuuint64_t)t.rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(t.ld * dtype_size(t.dtype))};
+  cuuint32_t box[2] = {(cuuint32_t)box_c, (cuuint32_t)box_r};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(&m, t.dtype == DT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                  2, t.ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("mk_compile: cuTensorMapEncodeTiled failed (%d) for a %lldx%lld tensor, box %dx%d",
+              (int)r, (long long)t.rows, (long long)t.cols, box_r, box_c);
+    return MK_ERR_CUDA;
+  }
+  keys.push_back(k);
+  maps.push_back(m);
+  *idx = (int)maps.size() - 1;
+  return MK_OK;
+}
+
+static Operand operand(const std::vector<TensorRec>& ts, int id) {
+  Operand o;
+  o.ptr = id >= 0 ? (uint64_t)(uintptr_t)ts[id].ptr : 0;
+  o.ld = id >= 0 ? (int32_t)ts[id].ld : 0;
+  o.tmap = -1;
+  return o;
+}
+
+// Node table and tensor maps for a device plan.
+static mk_status build_nodes(const mk_graph* g, mk_plan* p, std::vector<CUtensorMap>& maps,
+                             const std::vector<uint64_t>& scratch_ptr) {
+  std::vector<MapKey> keys;
+  const auto& ts = p->hp.tensors;
+  p->nodes.assign(g->nodes.size(), Node{});
+  for (size_t i = 0; i < g->nodes.size(); ++i) {
+    const NodeRec& nd = g->nodes[i];
+    Node& n = p->nodes[i];
+    memset(&n, 0, sizeof n);
+    n.flags = nd.flags;
+    n.eps = nd.eps;
+    n.theta = nd.theta;
+    n.hq = nd.hq;
+    n.hkv = nd.hkv;
+    n.hd = nd.hd;
+    n.pos0 = nd.pos0;
+    n.causal = nd.causal;
+    n.ewop = nd.ewop;
+    n.tile_n = p->hp.node_tile_n[i];
+    n.n_splits = p->hp.node_splits[i];
+    n.n_chunks = p->hp.node_chunks[i];
+    n.out = operand(ts, nd.out);
+    n.out_k = operand(ts, nd.out_k);
+    n.out_v = operand(ts, nd.out_v);
+    n.bias = operand(ts, nd.bias);
+    n.res = operand(ts, nd.res);
+    n.gamma = operand(ts, nd.gamma);
+    n.scratch.ptr = scratch_ptr[i];
+    n.scratch.tmap = -1;
+    switch (nd.kind) {
+      case NK_MATMUL: {
+        const TensorRec &A = ts[nd.a], &B = ts[nd.b];
+        n.dtype = A.dtype;
+        n.M = (int)A.rows;
+        n.K = (int)A.cols;
+        n.N = (int)B.cols;
+        n.a = operand(ts, nd.a);
+        n.b = operand(ts, nd.b);
+        n.b2 = operand(ts, nd.b2);
+        const bool gemv = A.rows <= p->opts.gemv_max_m;
+        n.kind = gemv ? OP_GEMV : OP_GEMM;
+        if (gemv) n.ldp = n.M * n.N * ((nd.flags & MK_EPI_SILU_MUL) ? 2 : 1);
+        if (n.M > 0 && n.N > 0 && n.K > 0) {
+          mk_status st;
+          if (!gemv) {
+            if ((st = add_map(keys, maps, A, kGemmBK, kGemmTileM, true, &n.a.tmap))) return st;
+            if ((st = add_map(keys, maps, B, 64, kGemmBK, true, &n.b.tmap))) return st;
+            if (nd.b2 >= 0 && (st = add_map(keys, maps, ts[nd.b2], 64, kGemmBK, true, &n.b2.tmap)))
+              return st;
+          } else {
+            if ((st = add_map(keys, maps, B, n.tile_n, kGemvRows, false, &n.b.tmap))) return st;
+            if (nd.b2 >= 0 &&
+                (st = add_map(keys, maps, ts[nd.b2], n.tile_n, kGemvRows, false, &n.b2.tmap)))
+              return st;
+          }
+        }
+        break;
+      }
+      case NK_EW:
+        n.kind = OP_EW;
+        n.tile_m = p->opts.ew_rows;
+        n.tile_n = p->opts.ew_cols * p->opts.ew_tiles;
+        n.dtype = ts[nd.out].dtype;
+        n.M = (int)ts[nd.out].rows;
+        n.N = (int)ts[nd.out].cols;
+        n.a = operand(ts, nd.ins[0]);
+        n.b = operand(ts, nd.ins[1]);
+        break;
+      case NK_RMSNORM:
+        n.kind = OP_RMSNORM;
+        n.tile_m = p->opts.norm_rows;
+        n.dtype = ts[nd.out].dtype;
+        n.M = (int)ts[nd.out].rows;
+        n.N = (int)ts[nd.out].cols;
+        n.a = operand(ts, nd.ins[0]);
+        break;
+      case NK_ROPE:
+        n.kind = OP_ROPE;
+        n.tile_m = p->opts.norm_rows;
+        n.dtype = ts[nd.out].dtype;
+        n.M = (int)ts[nd.ins[0]].rows;
+        n.N = (int)ts[nd.ins[0]].cols;
+        n.a = operand(ts, nd.ins[0]);
+        break;
+      case NK_ATTN:
+        n.kind = ts[nd.a].rows == 1 ? OP_ATTN_PARTIAL : OP_ATTN_PREFILL;
+        n.dtype = DT_BF16;
+        n.M = (int)ts[nd.a].rows;   // Tq
+        n.K = (int)ts[nd.b].rows;   // Tk
+        n.N = (int)ts[nd.a].cols;
+        n.a = operand(ts, nd.a);
+        n.b = operand(ts, nd.b);
+        n.b2 = operand(ts, nd.b2);
+        n.scale = nd.scale != 0.f ? nd.scale : 1.0f / sqrtf((float)nd.hd);
+        if (p->hp.node_scratch[i] >= 0) n.scratch.ld = (int)ts[p->hp.node_scratch[i]].ld;
+        break;
+    }
+  }
+  return MK_OK;
+}
+
+// ------------------------------------------------------------------ C ABI: compile/run
+
+extern "C" mk_status mk_compile(mk_graph_t g, const mk_compile_opts* opts_in, mk_plan_t* out) {
+  if (!g || !out) {
+    set_error("mk_compile: NULL graph or output");
+    return MK_ERR_INVALID_ARG;
+  }
+  *out = nullptr;
+  mk_compile_opts o;
+  if (opts_in) {
+    o = *opts_in;
+  } else {
+    mk_default_opts(&o);
+  }
+  mk_status st = check_hazards(g);
+  if (st) return st;
+  mk_plan* p = new (std::nothrow) mk_plan();
+  if (!p) {
+    set_error("mk_compile: out of host memory");
+    return MK_ERR_OOM;
+  }
+  int sm_count = 0;
+  if (!o.dry_run) {
+    int dev = o.device;
+    if (dev < 0 && cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+    cudaError_t e = cudaSetDevice(dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) {
+      set_error("mk_compile: no usable CUDA device (%s)", cudaGetErrorString(e));
+      delete p;
+      return MK_ERR_CUDA;
+    }
+    p->device = dev;
+    if (o.n_sm <= 0) o.n_sm = sm_count;
+    if (o.n_sm > sm_count) {
+      set_error("mk_compile: n_sm %d exceeds the device's %d SMs (CTAs must be co-resident)",
+                o.n_sm, sm_count);
+      delete p;
+      return MK_ERR_UNSUPPORTED;
+    }
+    if ((st = check_kernel_support(g->tensors, g->nodes, o))) {
+      delete p;
+      return st;
+    }
+  } else if (o.n_sm <= 0) {
+    set_error("mk_compile: dry_run needs an explicit n_sm");
+    delete p;
+    return MK_ERR_INVALID_ARG;
+  }
+  p->opts = o;
+  if ((st = lower_graph(g->tensors, g->nodes, o, &p->hp))) {
+    delete p;
+    return st;
+  }
+  if (o.debug_counter >= 0) {
+    if (o.debug_counter >= p->hp.n_dep) {
+      set_error("mk_compile: debug_counter %d out of range", o.debug_counter);
+      delete p;
+      return MK_ERR_INVALID_ARG;
+    }
+    // Test hook: raise one counter's target so that its consumers wait on a count nothing
+    // will reach (the device wait limit then ends the run with MK_ERR_TIMEOUT).
+    p->hp.targets[o.debug_counter] += o.debug_extra;
+    for (auto& in : p->hp.instrs)
+      for (int s = 0; s < in.n_src; ++s)
+        if (p->hp.src_list[2 * (in.src_off + s)] == o.debug_counter)
+          p->hp.src_list[2 * (in.src_off + s) + 1] += o.debug_extra;
+  }
+  if (o.dry_run) {
+    *out = p;
+    return MK_OK;
+  }
+
+  // Scratch per node: GEMV split partials (fp32) and attention partials (fp32).
+  const auto& ts = p->hp.tensors;
+  std::vector<size_t> scratch_off(g->nodes.size(), 0), scratch_len(g->nodes.size(), 0);
+  size_t scratch = 0;
+  auto align = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  for (size_t i = 0; i < g->nodes.size(); ++i) {
+    const NodeRec& nd = g->nodes[i];
+    size_t bytes = 0;
+    if (nd.kind == NK_MATMUL && p->hp.node_splits[i] > 0) {
+      bytes = (size_t)p->hp.node_splits[i] * ts[nd.a].rows * ts[nd.out].cols * 4 *
+              ((nd.flags & MK_EPI_SILU_MUL) ? 2 : 1);
+    } else if (p->hp.node_scratch[i] >= 0) {
+      const TensorRec& s = ts[p->hp.node_scratch[i]];
+      bytes = (size_t)s.rows * s.ld * 4;
+    }
+    scratch_off[i] = scratch;
+    scratch_len[i] = bytes;
+    scratch = align(scratch + bytes);
+  }
+  p->scratch_bytes = scratch;
+
+  std::vector<CUtensorMap> maps;
+  std::vector<uint64_t> scratch_ptr(g->nodes.size(), 0);  // patched after allocation
+  const size_t n_ctr = (size_t)p->hp.n_dep + p->hp.n_sem;
+  const size_t off_instr = 0;
+  const size_t off_nodes = align(off_instr + p->hp.instrs.size() * sizeof(Instr));
+  const size_t off_src = align(off_nodes + g->nodes.size() * sizeof(Node));
+  const size_t off_dst = align(off_src + p->hp.src_list.size() * 4);
+  const size_t off_ctr = align(off_dst + p->hp.dst_list.size() * 4);
+  const size_t off_status = align(off_ctr + n_ctr * 4);
+  const size_t off_maps = align(off_status + kStatusWords * 4);
+  const size_t off_scratch = align(off_maps + kMaxTmaps * sizeof(CUtensorMap));
+  const size_t total = off_scratch + scratch;
+  if (cudaMalloc((void**)&p->d_mem, total) != cudaSuccess) {
+    cudaGetLastError();
+    set_error("mk_compile: cudaMalloc of %zu plan bytes failed", total);
+    delete p;
+    return MK_ERR_OOM;
+  }
+  for (size_t i = 0; i < g->nodes.size(); ++i)
+    scratch_ptr[i] = scratch_len[i] ? (uint64_t)(uintptr_t)(p->d_mem + off_scratch + scratch_off[i]) : 0;
+  if ((st = build_nodes(g, p, maps, scratch_ptr))) {
+    cudaFree(p->d_mem);
+    delete p;
+    return st;
+  }
+  auto up = [&](size_t off, const void* src, size_t bytes) -> cudaError_t {
+    return bytes ? cudaMemcpy(p->d_mem + off, src, bytes, cudaMemcpyHostToDevice) : cudaSuccess;
+  };
+  cudaError_t e = up(off_instr, p->hp.instrs.data(), p->hp.instrs.size() * sizeof(Instr));
+  if (e == cudaSuccess) e = up(off_nodes, p->nodes.data(), p->nodes.size() * sizeof(Node));
+  if (e == cudaSuccess) e = up(off_src, p->hp.src_list.data(), p->hp.src_list.size() * 4);
+  if (e == cudaSuccess) e = up(off_dst, p->hp.dst_list.data(), p->hp.dst_list.size() * 4);
+  if (e == cudaSuccess) e = up(off_maps, maps.data(), maps.size() * sizeof(CUtensorMap));
+  if (e == cudaSuccess) e = cudaMemset(p->d_mem + off_ctr, 0, n_ctr * 4 + kStatusWords * 4);
+  if (e == cudaSuccess) {
+    p->smem = megakernel_smem_bytes();
+    e = configure_megakernel(p->smem);
+  }
+  if (e != cudaSuccess) {
+    set_error("mk_compile: device upload failed: %s", cudaGetErrorString(e));
+    cudaFree(p->d_mem);
+    delete p;
+    return MK_ERR_CUDA;
+  }
+  Params& pr = p->params;
+  pr.instrs = (const Instr*)(p->d_mem + off_instr);
+  pr.nodes = (const Node*)(p->d_mem + off_nodes);
+  pr.src_list = (const int32_t*)(p->d_mem + off_src);
+  pr.dst_list = (const int32_t*)(p->d_mem + off_dst);
+  pr.counters = (int32_t*)(p->d_mem + off_ctr);
+  pr.status = (int32_t*)(p->d_mem + off_status);
+  pr.tmaps = (const void*)(p->d_mem + off_maps);
+  pr.n_instr = (int32_t)p->hp.instrs.size();
+  pr.n_sm = o.n_sm;
+  pr.n_tmaps = (int32_t)maps.size();
+  pr.timeout_ns = (uint64_t)(o.timeout_ms > 0 ? o.timeout_ms : 2000) * 1000000ull;
+  p->grid = o.n_sm;
+  p->on_device = true;
+  *out = p;
+  return MK_OK;
+}
+
+extern "C" mk_status mk_run(mk_plan_t p, void* stream) {
+  if (!p || !p->on_device) {
+    set_error("mk_run: plan is NULL or was compiled with dry_run");
+    return MK_ERR_INVALID_ARG;
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  const size_t n_ctr = (size_t)p->hp.n_dep + p->hp.n_sem;
+  // counters and the status word are adjacent (status follows the counters, 256-aligned)
+  CUDA_TRY(cudaMemsetAsync(p->params.counters, 0, n_ctr * 4, s));
+  CUDA_TRY(cudaMemsetAsync(p->params.status, 0, kStatusWords * 4, s));
+  if (p->params.n_instr == 0) return MK_OK;
+  CUDA_TRY(launch_megakernel(p->params, p->grid, p->smem, s));
+  return MK_OK;
+}
+
+static mk_status host_copy(mk_plan_t p, const mk_host_copy& c, cudaStream_t s) {
+  const auto& ts = p->hp.tensors;
+  if (c.tensor < 0 || c.tensor >= (int)ts.size() || ts[c.tensor].internal || !c.host) {
+    set_error("mk_run_host: bad tensor id %d or NULL host pointer", c.tensor);
+    return MK_ERR_INVALID_ARG;
+  }
+  const TensorRec& t = ts[c.tensor];
+  const size_t es = dtype_size(t.dtype);
+  if (t.rows == 0 || t.cols == 0) return MK_OK;
+  if (c.to_device)
+    CUDA_TRY(cudaMemcpy2DAsync(t.ptr, t.ld * es, c.host, t.cols * es, t.cols * es, t.rows,
+                               cudaMemcpyHostToDevice, s));
+  else
+    CUDA_TRY(cudaMemcpy2DAsync(c.host, t.cols * es, t.ptr, t.ld * es, t.cols * es, t.rows,
+                               cudaMemcpyDeviceToHost, s));
+  return MK_OK;
+}
+
+extern "C" mk_status mk_run_host(mk_plan_t p, const mk_host_copy* copies, int32_t n,
+                                 void* stream) {
+  if (!p || (n > 0 && !copies) || n < 0) {
+    set_error("mk_run_host: NULL plan or copies");
+    return MK_ERR_INVALID_ARG;
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  mk_status st;
+  for (int i = 0; i < n; ++i)
+    if (copies[i].to_device && (st = host_copy(p, copies[i], s))) return st;
+  if ((st = mk_run(p, stream))) return st;
+  for (int i = 0; i < n; ++i)
+    if (!copies[i].to_device && (st = host_copy(p, copies[i], s))) return st;
+  return MK_OK;
+}
+
+extern "C" mk_status mk_sync_status(mk_plan_t p, mk_device_status* st) {
+  if (!p || !st || !p->on_device) {
+    set_error("mk_sync_status: NULL plan/status or dry-run plan");
+    return MK_ERR_INVALID_ARG;
+  }
+  CUDA_TRY(cudaDeviceSynchronize());
+  int32_t w[kStatusWords];
+  CUDA_TRY(cudaMemcpy(w, p->params.status, sizeof w, cudaMemcpyDeviceToHost));
+  st->code = w[ST_CODE];
+  st->instr = w[ST_INSTR];
+  st->counter = w[ST_COUNTER];
+  st->observed = w[ST_OBSERVED];
+  st->expected = w[ST_EXPECTED];
+  st->sm = w[ST_SM];
+  st->role = w[ST_ROLE];
+  st->where = w[ST_WHERE];
+  if (st->code) {
+    set_error("device reported %s at instruction %d (SM %d, role %d, site %d): counter %d "
+              "observed %d, expected %d",
+              st->code == MK_ERR_TIMEOUT ? "a wait timeout" : "a failed check", st->instr, st->sm,
+              st->role, st->where, st->counter, st->observed, st->expected);
+  }
+  return st->code;
+}
+
+extern "C" mk_status mk_plan_destroy(mk_plan_t p) {
+  if (p && p->d_mem) cudaFree(p->d_mem);
+  delete p;
+  return MK_OK;
+}
+
+extern "C" mk_status mk_plan_stats(mk_plan_t p, mk_stats* s) {
+  if (!p || !s) {
+    set_error("mk_plan_stats: NULL");
+    return MK_ERR_INVALID_ARG;
+  }
+  memset(s, 0, sizeof *s);
+  s->n_instr = (int64_t)p->hp.instrs.size();
+  s->n_counters = p->hp.n_dep;
+  s->n_sems = p->hp.n_sem;
+  s->n_sm = p->hp.n_sm;
+  s->n_iter = p->hp.n_sm ? (s->n_instr + p->hp.n_sm - 1) / p->hp.n_sm : 0;
+  s->waves = p->hp.n_sm ? (double)s->n_instr / p->hp.n_sm : 0.0;
+  s->n_src = (int64_t)p->hp.src_list.size() / 2;
+  s->n_dst = (int64_t)p->hp.dst_list.size();
+  for (const auto& in : p->hp.instrs)
+    if (in.op < 16) s->per_op[in.op]++;
+  s->smem_bytes = (int64_t)p->smem;
+  s->scratch_bytes = (int64_t)p->scratch_bytes;
+  return MK_OK;
+}
+
+extern "C" mk_status mk_get_instructions(mk_plan_t p, void* buf, size_t bytes) {
+  if (!p || !buf || bytes < p->hp.instrs.size() * sizeof(Instr)) {
+    set_error("mk_get_instructions: NULL or buffer smaller than n_instr * 64");
+    return MK_ERR_INVALID_ARG;
+  }
+  memcpy(buf, p->hp.instrs.data(), p->hp.instrs.size() * sizeof(Instr));
+  return MK_OK;
+}
+
+extern "C" mk_status mk_get_src_list(mk_plan_t p, int32_t* buf, size_t n) {
+  if (!p || (!buf && !p->hp.src_list.empty()) || n < p->hp.src_list.size()) {
+    set_error("mk_get_src_list: NULL or buffer too small");
+    return MK_ERR_INVALID_ARG;
+  }
+  if (!p->hp.src_list.empty()) memcpy(buf, p->hp.src_list.data(), p->hp.src_list.size() * 4);
+  return MK_OK;
+}
+
+extern "C" mk_status mk_get_dst_list(mk_plan_t p, int32_t* buf, size_t n) {
+  if (!p || (!buf && !p->hp.dst_list.empty()) || n < p->hp.dst_list.size()) {
+    set_error("mk_get_dst_list: NULL or buffer too small");
+    return MK_ERR_INVALID_ARG;
+  }
+  if (!p->hp.dst_list.empty()) memcpy(buf, p->hp.dst_list.data(), p->hp.dst_list.size() * 4);
+  return MK_OK;
+}
+
+extern "C" mk_status mk_get_counter_targets(mk_plan_t p, int32_t* buf, size_t n) {
+  if (!p || (!buf && p->hp.n_dep) || n < (size_t)p->hp.n_dep) {
+    set_error("mk_get_counter_targets: NULL or buffer too small");
+    return MK_ERR_INVALID_ARG;
+  }
+  if (p->hp.n_dep) memcpy(buf, p->hp.targets.data(), (size_t)p->hp.n_dep * 4);
+  return MK_OK;
+}
+
+extern "C" mk_status mk_get_counters(mk_plan_t p, int32_t* buf, size_t n) {
+  if (!p || !p->on_device) {
+    set_error("mk_get_counters: NULL or dry-run plan");
+    return MK_ERR_INVALID_ARG;
+  }
+  const size_t need = (size_t)p->hp.n_dep + p->hp.n_sem;
+  if ((!buf && need) || n < need) {
+    set_error("mk_get_counters: NULL, dry-run plan or buffer too small");
+    return MK_ERR_INVALID_ARG;
+  }
+  CUDA_TRY(cudaDeviceSynchronize());
+  if (need) CUDA_TRY(cudaMemcpy(buf, p->params.counters, need * 4, cudaMemcpyDeviceToHost));
+  return MK_OK;
+}

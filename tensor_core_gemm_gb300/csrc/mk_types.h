@@ -1,0 +1,123 @@
+// Host/device layouts of a compiled plan: instruction records, node table, kernel parameters.
+//
+// The instruction record is a fixed-size POD written by the host compiler and read by the
+// persistent kernel, in the manner of the 64-byte TaskDescriptor of "Implementing a Mega Kernel
+// for B300" (§2: op id, flags, indices instead of pointers, static_asserts on the layout) and the
+// fixed-size instruction of "MegaKittens Internals" §06. Source and arrival counter lists live
+// out of line (offsets into two int32 arrays) so no instruction has a fan-in or fan-out limit.
+#pragma once
+#include <stddef.h>
+#include <stdint.h>
+
+namespace mk {
+
+enum Op : uint16_t {
+  OP_NOOP = 0,
+  OP_GEMM = 1,          // tcgen05 output tile of a matmul
+  OP_GEMV = 2,          // split-K column tile of a small-M matmul (CUDA cores)
+  OP_EW = 3,            // elementwise tile
+  OP_RMSNORM = 4,       // block of rows
+  OP_ROPE = 5,          // block of rows: rotary q/k (+ v copy)
+  OP_ATTN_PARTIAL = 6,  // split-KV partial (m, l, o) for one kv group and key chunk
+  OP_ATTN_REDUCE = 7,   // LSE merge of one kv group's partials
+  OP_ATTN_PREFILL = 8,  // causal attention for one (q tile, head)
+  OP_END = 0xFFFF,      // past the end of an SM's queue (never stored in the list)
+};
+
+enum : uint16_t { IFLAG_B_DEP = 1 };  // the B operand is produced inside the graph
+
+struct Instr {
+  uint16_t op;
+  uint16_t flags;
+  int32_t node;
+  int32_t m0, n0, k0, klen;
+  int32_t aux0, aux1;
+  int32_t sem;
+  int32_t n_src, src_off;
+  int32_t n_dst, dst_off;
+  int32_t pad[3];
+};
+static_assert(sizeof(Instr) == 64, "instruction record is 64 bytes");
+static_assert(offsetof(Instr, node) == 4 && offsetof(Instr, sem) == 32 &&
+                  offsetof(Instr, dst_off) == 48,
+              "instruction field offsets are part of the ABI");
+
+enum DType : int32_t { DT_F16 = 0, DT_BF16 = 1, DT_F32 = 2 };
+
+enum : uint32_t {
+  EPI_BIAS = 1u << 0,
+  EPI_RELU = 1u << 1,
+  EPI_RESIDUAL = 1u << 2,
+  EPI_RMSNORM_INPUT = 1u << 3,
+  EPI_SILU_MUL = 1u << 4,
+};
+
+enum : int32_t { EWOP_ADD = 0, EWOP_RELU = 1, EWOP_COPY = 2, EWOP_SILU_MUL = 3 };
+
+// One operand: pointer to the first element of the window and its row stride (elements).
+struct Operand {
+  uint64_t ptr;
+  int32_t ld;
+  int32_t tmap;  // index into the plan's tensor-map array, -1 when not read through TMA
+};
+static_assert(sizeof(Operand) == 16, "operand is 16 bytes");
+
+// Node table entry: everything an instruction body needs about its graph node. 256 bytes; the
+// scheduler warp copies it into the instruction slot next to the instruction record.
+struct Node {
+  int32_t kind;     // Op of the node's (first) phase family
+  int32_t dtype;    // DType of A/B/out
+  uint32_t flags;   // EPI_* for matmuls
+  int32_t M, N, K;  // matmul: out M x N, reduction K; rows/cols for row ops
+  int32_t tile_n;   // output columns per GEMM/GEMV tile
+  int32_t ewop;     // EWOP_* for elementwise nodes
+  Operand a, b, b2, out;        // 64 B
+  Operand bias, res, gamma;     // 48 B (gamma also RMSNORM's weight)
+  Operand out_k, out_v;         // 32 B: ROPE k / v outputs
+  Operand scratch;              // 16 B: fp32 partials (GEMV split-K, attention)
+  float eps, scale, theta;
+  int32_t hq, hkv, hd;          // heads and head dim
+  int32_t pos0;                 // ROPE first position / attention q_pos0
+  int32_t causal;
+  int32_t n_chunks;             // attention decode: chunks per kv group
+  int32_t n_splits;             // GEMV: K splits per tile
+  int32_t ldp;                  // GEMV partial stride (elements per split: M * N * (1 or 2))
+  int32_t tile_m;               // rows per instruction of row/elementwise ops
+  int32_t pad[4];
+};
+static_assert(sizeof(Node) == 256, "node entry is 256 bytes");
+
+constexpr int kMaxTmaps = 256;
+
+// Kernel parameters (plain pointers into plan-owned device memory).
+struct Params {
+  const Instr* instrs;
+  const Node* nodes;
+  const int32_t* src_list;  // pairs (counter, target)
+  const int32_t* dst_list;
+  int32_t* counters;        // dependency counters, then split semaphores
+  int32_t* status;          // 8 int32: mk_device_status
+  const void* tmaps;        // CUtensorMap array (64-byte aligned), global memory
+  int32_t n_instr;
+  int32_t n_sm;             // placement stride
+  int32_t n_tmaps;
+  int32_t pad0;
+  uint64_t timeout_ns;
+};
+
+// Device status record (mirrors mk_device_status).
+enum : int32_t { ST_CODE = 0, ST_INSTR, ST_COUNTER, ST_OBSERVED, ST_EXPECTED, ST_SM, ST_ROLE, ST_WHERE };
+constexpr int kStatusWords = 8;
+
+// Kernel geometry shared with the host (launch configuration and shared-memory budget).
+constexpr int kThreads = 256;          // 8 warps: scheduler, loader, MMA, spare, 4 compute
+constexpr int kStages = 4;             // operand ring depth
+constexpr int kStageBytes = 48 * 1024; // A 128x64 (16 KB) + B 64x256 (32 KB), 16-bit elements
+constexpr int kSlots = 8;              // instruction slots (scheduler lookahead)
+constexpr int kSlotBytes = 64 + 256;   // Instr + Node
+constexpr int kGemmTileM = 128;
+constexpr int kGemmBK = 64;            // K per stage for GEMM (128-byte rows of 16-bit elements)
+constexpr int kGemvRows = 128;         // K rows per stage for GEMV
+constexpr int kAttnChunkMax = 128;     // keys per split-KV partial handled by one instruction
+
+}  // namespace mk

@@ -1,0 +1,345 @@
+"""GPU parity: the megakernel (through the C ABI) against the oracle, element by element.
+
+Tolerance (floating point): relative Frobenius error <= 5e-3 and per-element
+|err| <= 2e-2 * max(1, |ref|). Integer outputs (counters) are compared exactly.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import models, ops
+from oracle import schedule as osched
+from oracle.numerics import BF16, F16
+
+from tensor_core_gemm_gb300 import synth, workloads
+from tensor_core_gemm_gb300._lib import MK_ERR_TIMEOUT
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+def f32(t):
+    return synth.to_numpy_f32(t)
+
+
+def assert_close(got, ref, what=""):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    err = np.abs(got - ref)
+    fro = np.linalg.norm(err) / max(np.linalg.norm(ref), 1e-30)
+    bound = 2e-2 * np.maximum(1.0, np.abs(ref))
+    worst = np.unravel_index(np.argmax(err - bound), err.shape)
+    assert fro <= 5e-3, f"{what}: relative Frobenius error {fro:.3e}"
+    assert np.all(err <= bound), (f"{what}: element {worst} got {got[worst]} ref {ref[worst]}")
+
+
+def run(wl, **opts):
+    g, id_of = workloads.build_graph(wl.desc, wl.data)
+    plan = g.compile(**opts)
+    plan.run()
+    plan.check_status()
+    torch.cuda.synchronize()
+    return plan, id_of
+
+
+def check_counters(plan, wl, opts):
+    py = osched.lower(wl.desc, dict(opts, n_sm=plan.stats()["n_sm"]))
+    assert plan.counters().tolist() == py.final_counters()
+
+
+@pytest.fixture(autouse=True)
+def _sync():
+    yield
+    torch.cuda.synchronize()
+
+
+# ------------------------------------------------------------------ GEMM tiles
+
+@pytest.mark.parametrize("m,n,k,tn,dt", [
+    (128, 64, 64, 64, "f16"), (128, 256, 64, 256, "f16"), (128, 256, 128, 256, "f16"),
+    (256, 256, 256, 256, "f16"), (256, 256, 256, 128, "bf16"), (300, 392, 200, 256, "f16"),
+    (129, 72, 520, 64, "bf16"), (1000, 1024, 777 // 8 * 8, 128, "f16")])
+def test_gemm_full_compare(m, n, k, tn, dt):
+    wl = workloads.gemm(m, n, k, dtype=dt, device=DEV, seed=m + n + k)
+    plan, _ = run(wl, gemm_tile_n=tn)
+    ref = ops.matmul(f32(wl.data[0]), f32(wl.data[1]), F16 if dt == "f16" else BF16)
+    assert_close(f32(wl.data[2]), ref, f"gemm {m}x{n}x{k}")
+    check_counters(plan, wl, dict(gemm_tile_n=tn))
+
+
+def test_gemm_k_zero_writes_epilogue_of_zero():
+    wl = workloads.gemm(200, 64, 0, dtype="f16", device=DEV)
+    wl.data[2].fill_(7.0)
+    run(wl, gemm_tile_n=64)
+    assert torch.count_nonzero(wl.data[2]).item() == 0
+
+
+def test_gemm_4096_sampled_rows_and_256_cube():
+    # the 4096^3 GEMM: 256 seeded random rows checked in full
+    wl = workloads.gemm(4096, 4096, 4096, dtype="f16", device=DEV, seed=0)
+    run(wl)
+    rows = np.sort(torch.randperm(4096, generator=torch.Generator().manual_seed(0))[:256].numpy())
+    a = f32(wl.data[0][torch.as_tensor(rows, device=DEV)])
+    ref = ops.matmul(a, f32(wl.data[1]), F16)
+    assert_close(f32(wl.data[2][torch.as_tensor(rows, device=DEV)]), ref, "4096^3 rows")
+    # complete output of a 256^3 instance
+    wl = workloads.gemm(256, 256, 256, dtype="f16", device=DEV, seed=0)
+    run(wl)
+    assert_close(f32(wl.data[2]), ops.matmul(f32(wl.data[0]), f32(wl.data[1]), F16), "256^3")
+
+
+def test_mlp3_parity_and_identity_pin():
+    wl = workloads.mlp3(device=DEV, seed=0)
+    plan, _ = run(wl, gemm_tile_n=64)
+    x, w, b = f32(wl.data[0]), f32(wl.data[1]).reshape(3, 1024, 1024), \
+        f32(wl.data[2]).reshape(3, 1024, 1024)
+    refs = models.mlp(x, w, b)
+    for i, tid in enumerate(wl.info["outputs"]):
+        assert_close(f32(wl.data[tid]), refs[i], f"mlp layer {i}")
+    check_counters(plan, wl, dict(gemm_tile_n=64))
+    # W = I, b = 0 gives relu(x) exactly
+    wl.data[1].copy_(torch.eye(1024, device=DEV, dtype=torch.float16).repeat(3, 1))
+    wl.data[2].zero_()
+    plan.run()
+    plan.check_status()
+    relu = torch.relu(wl.data[0])
+    for tid in wl.info["outputs"]:
+        assert torch.equal(wl.data[tid], relu)
+
+
+def test_gemm_epilogues_bias_relu_residual_and_silu_mul():
+    m, n, k = 256, 256, 320
+    a = synth.normal((m, k), 1.0, "bf16", 1, DEV)
+    b = synth.normal((k, n), 1 / math.sqrt(k), "bf16", 2, DEV)
+    bu = synth.normal((k, n), 1 / math.sqrt(k), "bf16", 3, DEV)
+    bias = synth.normal((m, n), 0.5, "bf16", 4, DEV)
+    res = synth.normal((m, n), 1.0, "bf16", 5, DEV)
+    o1 = torch.zeros((m, n), dtype=torch.bfloat16, device=DEV)
+    o2 = torch.zeros((m, n), dtype=torch.bfloat16, device=DEV)
+    from tensor_core_gemm_gb300 import Graph
+    g = Graph()
+    ia, ib, ibu, ibias, ires, i1, i2 = (g.tensor(t) for t in (a, b, bu, bias, res, o1, o2))
+    g.matmul(ia, ib, i1, bias=ibias, relu=True, residual=ires)
+    g.matmul(ia, ib, i2, b_up=ibu)
+    p = g.compile(gemm_tile_n=256)
+    p.run()
+    p.check_status()
+    A, B, BU = f32(a), f32(b), f32(bu)
+    assert_close(f32(o1), ops.matmul(A, B, BF16, bias=f32(bias), relu=True, residual=f32(res)),
+                 "bias+relu+residual")
+    assert_close(f32(o2), ops.matmul_silu_mul(A, B, BU, BF16), "silu_mul")
+
+
+# ------------------------------------------------------------------ GEMV tiles
+
+@pytest.mark.parametrize("m,n,k,splits,norm,dual,res", [
+    (1, 256, 512, 0, False, False, False), (1, 3072, 2048, 0, True, False, False),
+    (1, 1024, 2048, 4, True, True, False), (1, 2048, 8192, 0, False, False, True),
+    (5, 392, 1000 // 8 * 8, 3, True, False, True), (8, 128, 128, 1, False, True, False)])
+def test_gemv(m, n, k, splits, norm, dual, res):
+    x = synth.normal((m, k), 1.0, "bf16", 11, DEV)
+    w = synth.normal((k, n), 0.02, "bf16", 12, DEV)
+    wu = synth.normal((k, n), 0.02, "bf16", 13, DEV)
+    gamma = synth.normal((1, k), 0.02, "bf16", 14, DEV, mean=1.0)
+    r = synth.normal((m, n), 1.0, "bf16", 15, DEV)
+    out = torch.zeros((m, n), dtype=torch.bfloat16, device=DEV)
+    from tensor_core_gemm_gb300 import Graph
+    g = Graph()
+    ix, iw, iwu, ig, ir, io = (g.tensor(t) for t in (x, w, wu, gamma, r, out))
+    g.matmul(ix, iw, io, gamma=ig if norm else None, b_up=iwu if dual else None,
+             residual=ir if res else None, eps=1e-5)
+    p = g.compile(gemv_splits=splits)
+    p.run()
+    p.check_status()
+    X, W, WU, G, R = f32(x), f32(w), f32(wu), f32(gamma)[0], f32(r)
+    if norm:
+        ref = ops.matmul_norm_input(X, G, 1e-5, W, BF16, residual=R if res else None,
+                                    w_up=WU if dual else None)
+    elif dual:
+        ref = ops.matmul_silu_mul(X, W, WU, BF16)
+    else:
+        ref = ops.matmul(X, W, BF16, residual=R if res else None)
+    assert_close(f32(out), ref, "gemv")
+    # every split semaphore counted every split; every counter reached its target
+    st = p.stats()
+    ctr = p.counters()
+    assert np.all(ctr[st["n_counters"]:] == p.instructions()["aux1"][0])
+
+
+# ------------------------------------------------------------------ row / elementwise ops
+
+def test_unfused_mlp_elementwise_tiles():
+    import _graphs
+    desc = _graphs.mlp_unfused(m=300, h=256, layers=2, dtype="f16")
+    data = []
+    for i, t in enumerate(desc["tensors"]):
+        std = [1 / 16, 1.0, 0.1][i] if i < 3 else 0.0
+        data.append(synth.normal((t["rows"], t["cols"]), std, "f16", 20 + i, DEV) if i < 3 else
+                    synth.zeros((t["rows"], t["cols"]), "f16", DEV))
+    g, _ = workloads.build_graph(desc, data)
+    p = g.compile(gemm_tile_n=128, ew_rows=64, ew_cols=64, ew_tiles=2)
+    p.run()
+    p.check_status()
+    x, w, b = f32(data[1]), f32(data[0]).reshape(2, 256, 256), f32(data[2]).reshape(2, 300, 256)
+    refs = models.mlp_unfused(x, w, b, F16)
+    for l in range(2):
+        for j in range(3):
+            assert_close(f32(data[3 + 3 * l + j]), refs[l][j], f"layer {l} node {j}")
+
+
+def test_rmsnorm_rows():
+    t, d = 67, 2048
+    x = synth.normal((t, d), 1.0, "bf16", 30, DEV)
+    gm = synth.normal((1, d), 0.02, "bf16", 31, DEV, mean=1.0)
+    out = torch.zeros_like(x)
+    from tensor_core_gemm_gb300 import Graph
+    g = Graph()
+    ix, ig, io = g.tensor(x), g.tensor(gm), g.tensor(out)
+    g.rmsnorm(ix, ig, io, 1e-5)
+    p = g.compile()
+    p.run()
+    p.check_status()
+    assert_close(f32(out), ops.rmsnorm(f32(x), f32(gm)[0], 1e-5, BF16), "rmsnorm")
+
+
+@pytest.mark.parametrize("rows,pos0,with_v", [(1, 1024, True), (40, 0, False), (3, 2045, True)])
+def test_rope(rows, pos0, with_v):
+    hq, hkv, d = 32, 8, 64
+    cols = (hq + hkv + (hkv if with_v else 0)) * d
+    x = synth.normal((rows, cols), 1.0, "bf16", 40, DEV)
+    oq = torch.zeros((rows, hq * d), dtype=torch.bfloat16, device=DEV)
+    ok = torch.zeros((rows, hkv * d), dtype=torch.bfloat16, device=DEV)
+    ov = torch.zeros((rows, hkv * d), dtype=torch.bfloat16, device=DEV)
+    from tensor_core_gemm_gb300 import Graph
+    g = Graph()
+    ix, iq, ik, iv = g.tensor(x), g.tensor(oq), g.tensor(ok), g.tensor(ov)
+    g.rope(ix, iq, ik, out_v=iv if with_v else None, n_q_heads=hq, n_kv_heads=hkv, head_dim=d,
+           pos0=pos0, theta=5e5)
+    p = g.compile()
+    p.run()
+    p.check_status()
+    X = f32(x)
+    pos = pos0 + np.arange(rows)
+    assert_close(f32(oq), ops.rope(X[:, :hq * d], pos, hq, d, 5e5, BF16), "rope q")
+    assert_close(f32(ok), ops.rope(X[:, hq * d:(hq + hkv) * d], pos, hkv, d, 5e5, BF16), "rope k")
+    if with_v:
+        assert torch.equal(ov, x[:, (hq + hkv) * d:])
+
+
+# ------------------------------------------------------------------ split-KV attention
+
+@pytest.mark.parametrize("tk,chunk,hq,hkv", [(1025, 64, 32, 8), (70, 16, 8, 2), (1, 64, 4, 4),
+                                            (300, 128, 32, 8)])
+def test_attention_decode_split_kv(tk, chunk, hq, hkv):
+    d = 64
+    q = synth.normal((1, hq * d), 1.0, "bf16", 50, DEV)
+    k = synth.normal((tk, hkv * d), 1.0, "bf16", 51, DEV)
+    v = synth.normal((tk, hkv * d), 1.0, "bf16", 52, DEV)
+    out = torch.zeros((1, hq * d), dtype=torch.bfloat16, device=DEV)
+    from tensor_core_gemm_gb300 import Graph
+    g = Graph()
+    iq, ik, iv, io = g.tensor(q), g.tensor(k), g.tensor(v), g.tensor(out)
+    g.attention(iq, ik, iv, io, n_q_heads=hq, n_kv_heads=hkv, head_dim=d, q_pos0=tk - 1)
+    p = g.compile(attn_chunk=chunk)
+    p.run()
+    p.check_status()
+    ref = ops.attention(f32(q), f32(k), f32(v), hq, hkv, d, False, tk - 1, 1 / 8, BF16)
+    assert_close(f32(out), ref, "split-KV attention")
+
+
+# ------------------------------------------------------------------ decoder, decode step
+
+def _decode_ref(wl):
+    sh = wl.info["shape"]
+    L, d, f = sh.layers, sh.hidden, sh.ffn
+    D = wl.data
+    w = wl.info["w"]
+    cap, p = wl.info["cap"], wl.info["pos"]
+    wts = models.DecoderWeights(
+        f32(D[w["wqkv"]]).reshape(L, d, sh.qkv), f32(D[w["wo"]]).reshape(L, sh.hq * sh.hd, d),
+        f32(D[w["wg"]]).reshape(L, d, f), f32(D[w["wu"]]).reshape(L, d, f),
+        f32(D[w["wd"]]).reshape(L, f, d), f32(D[w["g_attn"]]), f32(D[w["g_mlp"]]),
+        sh.hq, sh.hkv, sh.hd, sh.eps, sh.theta)
+    kc = f32(D[wl.info["kc"]]).reshape(L, cap, -1)
+    vc = f32(D[wl.info["vc"]]).reshape(L, cap, -1)
+    return wts, kc, vc, p
+
+
+def test_decode_small_decoder():
+    sh = workloads.DecoderShape(layers=3, hidden=512, n_q_heads=8, n_kv_heads=2, head_dim=64,
+                                ffn=1024)
+    wl = workloads.decode(sh, kv_len=200, device=DEV, seed=5)
+    x0 = f32(wl.data[0])
+    kc0 = f32(wl.data[wl.info["kc"]]).reshape(3, 201, -1).copy()
+    vc0 = f32(wl.data[wl.info["vc"]]).reshape(3, 201, -1).copy()
+    plan, _ = run(wl)
+    wts, _, _, p = _decode_ref(wl)
+    per_layer = {}
+    ref, kc, vc = models.decode_step(x0, wts, list(kc0), list(vc0), p,
+                                     layer_fn=lambda l, dd: per_layer.__setitem__(l, dd))
+    out = f32(wl.data[wl.info["out"]])
+    for l in range(3):
+        assert_close(f32(wl.data[wl.info["qkv"]])[l:l + 1], per_layer[l]["qkv"], f"qkv {l}")
+        assert_close(out[l:l + 1], per_layer[l]["x"], f"layer {l} output")
+    assert_close(out[-1:], ref, "decode output")
+    kcg = f32(wl.data[wl.info["kc"]]).reshape(3, 201, -1)
+    for l in range(3):
+        assert_close(kcg[l, p], kc[l][p], f"k cache row, layer {l}")
+    check_counters(plan, wl, {})
+
+
+def test_decode_full_config():
+    wl = workloads.decode(device=DEV, seed=0)
+    x0 = f32(wl.data[0])
+    sh = wl.info["shape"]
+    cap = wl.info["cap"]
+    kc0 = f32(wl.data[wl.info["kc"]]).reshape(sh.layers, cap, -1).copy()
+    vc0 = f32(wl.data[wl.info["vc"]]).reshape(sh.layers, cap, -1).copy()
+    plan, _ = run(wl)
+    wts, _, _, p = _decode_ref(wl)
+    ref, _, _ = models.decode_step(x0, wts, list(kc0), list(vc0), p)
+    assert_close(f32(wl.data[wl.info["out"]])[-1:], ref, "16-layer decode output")
+    check_counters(plan, wl, {})
+
+
+# ------------------------------------------------------------------ runtime behaviour
+
+def test_run_twice_same_result_and_host_path():
+    wl = workloads.gemm(256, 512, 384, dtype="f16", device=DEV, seed=9)
+    g, id_of = workloads.build_graph(wl.desc, wl.data)
+    p = g.compile()
+    p.run()
+    p.check_status()
+    first = wl.data[2].clone()
+    wl.data[2].zero_()
+    p.run()
+    p.check_status()
+    assert torch.equal(first, wl.data[2])
+    # host buffers: copies in, run, copies out, all on one stream
+    a_h = wl.data[0].cpu().pin_memory()
+    c_h = torch.zeros((256, 512), dtype=torch.float16).pin_memory()
+    wl.data[0].zero_()
+    s = torch.cuda.Stream()
+    p.run_host(inputs=[(0, a_h.data_ptr())], outputs=[(2, c_h.data_ptr())], stream=s)
+    s.synchronize()
+    p.check_status()
+    assert torch.equal(c_h, first.cpu())
+
+
+def test_wait_limit_reports_timeout_without_hanging():
+    # A counter target nothing can reach: the consumer's wait runs out after timeout_ms and the
+    # kernel ends with MK_ERR_TIMEOUT; the context stays usable.
+    wl = workloads.mlp3(m=256, h=256, layers=2, device=DEV)
+    g, _ = workloads.build_graph(wl.desc, wl.data)
+    p = g.compile(debug_counter=0, debug_extra=1, timeout_ms=50, gemm_tile_n=64)
+    p.run()
+    code, st = p.sync_status()
+    assert code == MK_ERR_TIMEOUT and st["counter"] == 0 and st["expected"] == st["observed"] + 1
+    ok = workloads.gemm(128, 64, 64, device=DEV)
+    run(ok, gemm_tile_n=64)
+    assert_close(f32(ok.data[2]), ops.matmul(f32(ok.data[0]), f32(ok.data[1]), F16), "after")

@@ -1,0 +1,194 @@
+"""The C-ABI library on the CPU: exports, validation, and the compiler's integer output
+(instruction list, counters, targets, arrivals, placement) bit-exact against the oracle's
+schedule, computed independently by brute-force box intersection."""
+import ctypes as C
+import os
+import re
+
+import numpy as np
+import pytest
+
+import _graphs
+from oracle import schedule as osched
+
+mk = pytest.importorskip("tensor_core_gemm_gb300")
+from tensor_core_gemm_gb300 import _lib, workloads  # noqa: E402
+from tensor_core_gemm_gb300._lib import MkError  # noqa: E402
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+FIELDS = ["op", "flags", "node", "m0", "n0", "k0", "klen", "aux0", "aux1", "sem"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not os.path.exists(_lib.LIB_PATH):
+        from tensor_core_gemm_gb300 import build
+        build.build()
+
+
+def test_library_exports_every_declared_symbol():
+    with open(os.path.join(ROOT, "include", "mk.h")) as f:
+        header = f.read()
+    declared = set(re.findall(r"^\s*(?:mk_status|const char\*|int32_t)\s+(mk_\w+)\s*\(", header,
+                              re.M))
+    assert declared == set(_lib.EXPORTS)
+    lib = C.CDLL(_lib.LIB_PATH)
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert _lib.load().mk_abi_version() == 1
+
+
+def _dry(desc, **opts):
+    g, _ = workloads.build_graph(desc, None)
+    return g.compile(dry_run=1, **opts)
+
+
+def assert_same_plan(desc, opts):
+    """Compiler output == oracle schedule, field by field and list by list."""
+    py = osched.lower(desc, opts)
+    c = _dry(desc, **opts)
+    st = c.stats()
+    assert st["n_instr"] == py.n_instr
+    assert st["n_counters"] == py.n_dep
+    assert st["n_sems"] == py.n_sem
+    assert abs(st["waves"] - py.waves) < 1e-12
+    ins = c.instructions()
+    want = osched.as_array(py)
+    got = np.stack([ins[f].astype(np.int64) for f in FIELDS], axis=1)
+    bad = np.nonzero(np.any(want != got, axis=1))[0]
+    assert bad.size == 0, f"first differing instruction {bad[:5]}: {want[bad[0]]} vs {got[bad[0]]}"
+    src = c.src_list()
+    dst = c.dst_list()
+    want_src = [pair for i in py.instrs for pair in i.src]
+    want_dst = [d for i in py.instrs for d in i.dst]
+    assert [tuple(x) for x in src.tolist()] == want_src
+    assert dst.tolist() == want_dst
+    assert ins["n_src"].tolist() == [len(i.src) for i in py.instrs]
+    assert ins["n_dst"].tolist() == [len(i.dst) for i in py.instrs]
+    assert ins["src_off"].tolist() == list(np.cumsum([0] + [len(i.src) for i in py.instrs])[:-1])
+    assert ins["dst_off"].tolist() == list(np.cumsum([0] + [len(i.dst) for i in py.instrs])[:-1])
+    assert c.counter_targets().tolist() == py.targets
+    assert osched.topologically_valid(py)
+    return py, c
+
+
+def test_p3_mlp_plan_matches_oracle_and_page():
+    py, c = assert_same_plan(_graphs.mlp_unfused(), _graphs.P3_OPTS)
+    st = c.stats()
+    assert st["n_instr"] == 240 and st["n_counters"] == 124 and f"{st['waves']:.2f}" == "1.62"
+
+
+@pytest.mark.parametrize("m,n,k,tn", [(1024, 1024, 1024, 256), (300, 392, 200, 256),
+                                      (128, 64, 64, 64), (4096, 4096, 4096, 256),
+                                      (257, 136, 0, 128)])
+def test_gemm_plans(m, n, k, tn):
+    assert_same_plan(workloads.gemm(m, n, k).desc, dict(n_sm=152, gemm_tile_n=tn))
+
+
+def test_mlp3_plan():
+    py, c = assert_same_plan(workloads.mlp3().desc, dict(n_sm=152, gemm_tile_n=64))
+    # layer-2 tiles wait on exactly the 16 layer-1 tiles of their 128-row block
+    l2 = [i for i in py.instrs if i.node == 1]
+    assert all(len(i.src) == 1 and i.src[0][1] == 16 for i in l2)
+
+
+def test_gemm_list_plans():
+    assert_same_plan(workloads.gemm_list(workloads.LLAMA70B_DECODE).desc, dict(n_sm=152))
+    assert_same_plan(workloads.gemm_list(workloads.LLAMA70B_PREFILL).desc, dict(n_sm=148))
+
+
+def test_decode_plan_full_size():
+    py, c = assert_same_plan(workloads.decode().desc, dict(n_sm=152))
+    per_op = c.stats()["per_op"]
+    assert per_op[osched.OP_ROPE] == 16 and per_op[osched.OP_ATTN_REDUCE] == 16 * 8
+    assert per_op[osched.OP_ATTN_PARTIAL] == 16 * 8 * 17   # 1025 keys in chunks of 64
+
+
+def test_prefill_plan_small():
+    sh = workloads.DecoderShape(layers=2, hidden=256, n_q_heads=4, n_kv_heads=2, head_dim=64,
+                                ffn=512)
+    assert_same_plan(workloads.prefill(sh, tokens=384).desc, dict(n_sm=37))
+
+
+@pytest.mark.slow
+def test_prefill_plan_full_size():
+    assert_same_plan(workloads.prefill(tokens=2048).desc, dict(n_sm=152))
+
+
+def test_gemv_split_and_unfused_elementwise_plans():
+    assert_same_plan(workloads.gemm(1, 3072, 2048, dtype="bf16").desc, dict(n_sm=152))
+    assert_same_plan(workloads.gemm(3, 1000, 520, dtype="bf16").desc,
+                     dict(n_sm=20, gemv_splits=3))
+    assert_same_plan(_graphs.mlp_unfused(m=300, h=256, layers=2, dtype="f16"),
+                     dict(n_sm=16, ew_rows=64, ew_cols=64, ew_tiles=2, gemm_tile_n=128))
+
+
+def test_final_counter_values_definition():
+    py = osched.lower(workloads.gemm(1, 512, 1024, dtype="bf16").desc, dict(n_sm=8))
+    fin = py.final_counters()
+    assert fin[py.n_dep:] == [py.instrs[0].aux1] * py.n_sem
+
+
+# ------------------------------------------------------------------ validation
+
+def test_shape_and_id_errors():
+    g = mk.Graph()
+    a = g.tensor(ptr=0, dtype="f16", shape=[64, 32])
+    b = g.tensor(ptr=0, dtype="f16", shape=[16, 64])
+    c = g.tensor(ptr=0, dtype="f16", shape=[64, 64])
+    with pytest.raises(MkError) as e:
+        g.matmul(a, b, c)
+    assert e.value.code == _lib.MK_ERR_INVALID_ARG
+    with pytest.raises(MkError):
+        g.view(a, 60, 0, 8, 32)
+    with pytest.raises(MkError):
+        g.matmul(a, 99, c)
+    bf = g.tensor(ptr=0, dtype="bf16", shape=[32, 64])
+    with pytest.raises(MkError) as e:
+        g.matmul(a, bf, c)
+    assert e.value.code == _lib.MK_ERR_UNSUPPORTED
+    with pytest.raises(MkError):
+        g.elementwise("add", [a], c)
+
+
+def test_hazards_rejected():
+    g = mk.Graph()
+    x = g.tensor(ptr=0, dtype="f16", shape=[128, 128])
+    w = g.tensor(ptr=0, dtype="f16", shape=[128, 128])
+    g.matmul(x, w, x)                     # in place: writes what it reads
+    with pytest.raises(MkError) as e:
+        g.compile(dry_run=1, n_sm=4)
+    assert e.value.code == _lib.MK_ERR_HAZARD
+    g = mk.Graph()
+    x = g.tensor(ptr=0, dtype="f16", shape=[128, 128])
+    w = g.tensor(ptr=0, dtype="f16", shape=[128, 128])
+    y = g.tensor(ptr=0, dtype="f16", shape=[128, 128])
+    g.matmul(x, w, y)
+    g.elementwise("relu", [x], y)         # second writer of y
+    with pytest.raises(MkError) as e:
+        g.compile(dry_run=1, n_sm=4)
+    assert e.value.code == _lib.MK_ERR_HAZARD
+
+
+def test_dry_run_requires_n_sm_and_run_rejects_dry_plans():
+    g, _ = workloads.build_graph(workloads.gemm(128, 128, 64).desc, None)
+    with pytest.raises(MkError):
+        g.compile(dry_run=1)
+    p = g.compile(dry_run=1, n_sm=4)
+    with pytest.raises(MkError):
+        p.run()
+
+
+def test_empty_graph_and_empty_matmul():
+    g = mk.Graph()
+    p = g.compile(dry_run=1, n_sm=8)
+    assert p.stats()["n_instr"] == 0
+    for m, n, k in [(0, 64, 64), (64, 0, 64), (1, 0, 128)]:
+        d = workloads.gemm(m, n, k, dtype="bf16").desc
+        assert_same_plan(d, dict(n_sm=8))
+        assert _dry(d, n_sm=8).stats()["n_instr"] == 0
+    # K = 0: one instruction per tile whose output is the epilogue of zero
+    for m in (1, 200):
+        py, c = assert_same_plan(workloads.gemm(m, 64, 0, dtype="bf16").desc, dict(n_sm=8))
+        assert c.stats()["n_instr"] == 1 + (m > 128)
