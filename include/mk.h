@@ -163,6 +163,7 @@ typedef struct {
   int32_t device;        /* CUDA device ordinal; -1 = current */
   int32_t debug_counter; /* test hook: counter whose target is raised by debug_extra (-1: none) */
   int32_t debug_extra;
+  int32_t snapshot_counters; /* 1: keep each run's final counter values for mk_get_counters */
 } mk_compile_opts;
 
 /* Fill *o with the defaults (the values listed above for each field). */
@@ -173,9 +174,11 @@ mk_status mk_default_opts(mk_compile_opts* o);
  * graph may be destroyed afterwards. */
 mk_status mk_compile(mk_graph_t g, const mk_compile_opts* opts, mk_plan_t* out);
 
-/* Enqueue one run on `stream` (a cudaStream_t; NULL = legacy default stream): zero the
- * counters and status word, then ONE persistent launch. Asynchronous; errors of the launch
- * itself are returned, device-side failures are reported by mk_sync_status. */
+/* Enqueue one run on `stream` (a cudaStream_t; NULL = legacy default stream): ONE persistent
+ * kernel launch. The CTA that finishes last resets the counters for the next run (also after a
+ * device-side failure) and moves the run's status to where mk_sync_status reads it.
+ * Asynchronous; errors of the launch itself are returned, device-side failures are reported by
+ * mk_sync_status. Runs of one plan must not overlap (use one stream, or order the streams). */
 mk_status mk_run(mk_plan_t p, void* stream);
 
 /* One copy between a registered tensor (or view) and host memory. */
@@ -200,7 +203,8 @@ typedef struct {
   int32_t where;      /* wait site id (kernel-internal) */
 } mk_device_status;
 
-/* Synchronise the device and read the plan's status word. Returns st->code as the status. */
+/* Synchronise the device and read the status of the plan's last completed run. Returns
+ * st->code as the status. */
 mk_status mk_sync_status(mk_plan_t p, mk_device_status* st);
 
 mk_status mk_plan_destroy(mk_plan_t p);
@@ -234,7 +238,9 @@ mk_status mk_get_src_list(mk_plan_t p, int32_t* host_buf, size_t n);
 mk_status mk_get_dst_list(mk_plan_t p, int32_t* host_buf, size_t n);
 /* Target of every dependency counter (n_counters values). */
 mk_status mk_get_counter_targets(mk_plan_t p, int32_t* host_buf, size_t n);
-/* Device counter array after a run (n_counters + n_sems values); synchronises. */
+/* Counter array at the end of the last run (n_counters + n_sems values): each dependency
+ * counter equals its target and each split semaphore its number of K splits. Needs a plan
+ * compiled with snapshot_counters = 1; synchronises. */
 mk_status mk_get_counters(mk_plan_t p, int32_t* host_buf, size_t n);
 
 const char* mk_last_error(void);

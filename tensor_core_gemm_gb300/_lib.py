@@ -40,7 +40,8 @@ class CompileOpts(C.Structure):
     _fields_ = [(n, C.c_int32) for n in (
         "n_sm", "gemm_tile_m", "gemm_tile_n", "cluster", "ew_rows", "ew_cols", "ew_tiles",
         "norm_rows", "gemv_max_m", "gemv_tile_n", "gemv_splits", "gemv_kstep", "attn_chunk",
-        "attn_tile_q", "dry_run", "timeout_ms", "device", "debug_counter", "debug_extra")]
+        "attn_tile_q", "dry_run", "timeout_ms", "device", "debug_counter", "debug_extra",
+        "snapshot_counters")]
 
 
 class HostCopy(C.Structure):

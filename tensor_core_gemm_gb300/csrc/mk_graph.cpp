@@ -664,5 +664,6 @@ extern "C" mk_status mk_default_opts(mk_compile_opts* o) {
   o->device = -1;
   o->debug_counter = -1;
   o->debug_extra = 0;
+  o->snapshot_counters = 0;
   return MK_OK;
 }

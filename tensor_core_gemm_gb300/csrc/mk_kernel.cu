@@ -88,15 +88,18 @@ __device__ void report(const Params& p, int code, int instr, int counter, int ob
 }
 
 // Bounded mbarrier wait; false when the limit passed (reported) or another waiter aborted.
+// On-chip waits get four times the counter-wait limit: when a dependency never completes, the
+// scheduler's counter wait runs out first and the report names the counter.
 __device__ bool wait_mbar(const Params& p, uint32_t bar, uint32_t parity, int role, int where,
                           int instr) {
   if (mbar_try(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
+  const uint64_t limit = 4 * p.timeout_ns;
   for (uint32_t n = 1;; ++n) {
     if (mbar_try(bar, parity)) return true;
     if ((n & 15u) == 0) {
       if (ld_volatile(p.status + ST_CODE) != 0) return false;
-      if (globaltimer() - t0 > p.timeout_ns) {
+      if (globaltimer() - t0 > limit) {
         report(p, MK_ERR_TIMEOUT, instr, -1, 0, (int)parity, role, where);
         return false;
       }
@@ -600,7 +603,9 @@ __device__ bool gemv(const Params& p, Smem& s, const Instr& in, const Node& nd, 
   const int which = dual ? (ct >> 6) : 0;
   const int n = in.n0 + (dual ? (ct & 63) : ct);
   const bool colok = (dual || ct < wcols) && n < nd.N;
-  if (S > 1) {
+  if (S == 1) {
+    if (ct == 0) atomicAdd(p.counters + in.sem, 1);  // the semaphore counts every split
+  } else {
     float* part = reinterpret_cast<float*>(nd.scratch.ptr);
     if (colok)
       for (int m = 0; m < M; ++m)
@@ -916,6 +921,26 @@ __global__ void __launch_bounds__(kThreads, 1) megakernel(const __grid_constant_
   if (warp == 2) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
+  }
+  // The CTA that finishes last (after every other CTA's work, including a drained abort)
+  // publishes the run's status and zeroes the counters, so the next run needs no host reset.
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s.flag = atomicAdd(p.done, 1) == (int)gridDim.x - 1;
+  }
+  __syncthreads();
+  if (s.flag) {
+    __threadfence();
+    for (int i = threadIdx.x; i < p.n_counters; i += kThreads) {
+      const int v = __ldcg(p.counters + i);
+      if (p.snapshot) p.snapshot[i] = v;
+      p.counters[i] = 0;
+    }
+    if (threadIdx.x < kStatusWords) {
+      p.last_status[threadIdx.x] = __ldcg(p.status + threadIdx.x);
+      p.status[threadIdx.x] = 0;
+    }
+    if (threadIdx.x == 0) *p.done = 0;
   }
 }
 

@@ -129,7 +129,8 @@ mk_status check_kernel_support(const std::vector<TensorRec>& ts, const std::vect
                    nd.out_k, nd.out_v})
       if (id >= 0) all.push_back(id);
     for (int id : all) {
-      if (!ts[id].ptr && ts[id].rows * ts[id].cols > 0) {
+      if (ts[id].rows * ts[id].cols == 0) continue;  // never accessed
+      if (!ts[id].ptr) {
         set_error("mk_compile: node %zu uses tensor %d with a NULL device pointer", i, id);
         return MK_ERR_INVALID_ARG;
       }
@@ -447,7 +448,9 @@ extern "C" mk_status mk_compile(mk_graph_t g, const mk_compile_opts* opts_in, mk
   const size_t off_dst = align(off_src + p->hp.src_list.size() * 4);
   const size_t off_ctr = align(off_dst + p->hp.dst_list.size() * 4);
   const size_t off_status = align(off_ctr + n_ctr * 4);
-  const size_t off_maps = align(off_status + kStatusWords * 4);
+  const size_t off_last = off_status + kStatusWords * 4;  // last_status, then `done`
+  const size_t off_snap = align(off_last + (kStatusWords + 1) * 4);
+  const size_t off_maps = align(off_snap + (o.snapshot_counters ? n_ctr * 4 : 0));
   const size_t off_scratch = align(off_maps + kMaxTmaps * sizeof(CUtensorMap));
   const size_t total = off_scratch + scratch;
   if (cudaMalloc((void**)&p->d_mem, total) != cudaSuccess) {
@@ -471,7 +474,7 @@ extern "C" mk_status mk_compile(mk_graph_t g, const mk_compile_opts* opts_in, mk
   if (e == cudaSuccess) e = up(off_src, p->hp.src_list.data(), p->hp.src_list.size() * 4);
   if (e == cudaSuccess) e = up(off_dst, p->hp.dst_list.data(), p->hp.dst_list.size() * 4);
   if (e == cudaSuccess) e = up(off_maps, maps.data(), maps.size() * sizeof(CUtensorMap));
-  if (e == cudaSuccess) e = cudaMemset(p->d_mem + off_ctr, 0, n_ctr * 4 + kStatusWords * 4);
+  if (e == cudaSuccess) e = cudaMemset(p->d_mem + off_ctr, 0, off_maps - off_ctr);
   if (e == cudaSuccess) {
     p->smem = megakernel_smem_bytes();
     e = configure_megakernel(p->smem);
@@ -489,10 +492,14 @@ extern "C" mk_status mk_compile(mk_graph_t g, const mk_compile_opts* opts_in, mk
   pr.dst_list = (const int32_t*)(p->d_mem + off_dst);
   pr.counters = (int32_t*)(p->d_mem + off_ctr);
   pr.status = (int32_t*)(p->d_mem + off_status);
+  pr.last_status = (int32_t*)(p->d_mem + off_last);
+  pr.done = pr.last_status + kStatusWords;
+  pr.snapshot = o.snapshot_counters ? (int32_t*)(p->d_mem + off_snap) : nullptr;
   pr.tmaps = (const void*)(p->d_mem + off_maps);
   pr.n_instr = (int32_t)p->hp.instrs.size();
   pr.n_sm = o.n_sm;
   pr.n_tmaps = (int32_t)maps.size();
+  pr.n_counters = (int32_t)n_ctr;
   pr.timeout_ns = (uint64_t)(o.timeout_ms > 0 ? o.timeout_ms : 2000) * 1000000ull;
   p->grid = o.n_sm;
   p->on_device = true;
@@ -506,10 +513,6 @@ extern "C" mk_status mk_run(mk_plan_t p, void* stream) {
     return MK_ERR_INVALID_ARG;
   }
   cudaStream_t s = (cudaStream_t)stream;
-  const size_t n_ctr = (size_t)p->hp.n_dep + p->hp.n_sem;
-  // counters and the status word are adjacent (status follows the counters, 256-aligned)
-  CUDA_TRY(cudaMemsetAsync(p->params.counters, 0, n_ctr * 4, s));
-  CUDA_TRY(cudaMemsetAsync(p->params.status, 0, kStatusWords * 4, s));
   if (p->params.n_instr == 0) return MK_OK;
   CUDA_TRY(launch_megakernel(p->params, p->grid, p->smem, s));
   return MK_OK;
@@ -556,7 +559,7 @@ extern "C" mk_status mk_sync_status(mk_plan_t p, mk_device_status* st) {
   }
   CUDA_TRY(cudaDeviceSynchronize());
   int32_t w[kStatusWords];
-  CUDA_TRY(cudaMemcpy(w, p->params.status, sizeof w, cudaMemcpyDeviceToHost));
+  CUDA_TRY(cudaMemcpy(w, p->params.last_status, sizeof w, cudaMemcpyDeviceToHost));
   st->code = w[ST_CODE];
   st->instr = w[ST_INSTR];
   st->counter = w[ST_COUNTER];
@@ -643,11 +646,12 @@ extern "C" mk_status mk_get_counters(mk_plan_t p, int32_t* buf, size_t n) {
     return MK_ERR_INVALID_ARG;
   }
   const size_t need = (size_t)p->hp.n_dep + p->hp.n_sem;
-  if ((!buf && need) || n < need) {
-    set_error("mk_get_counters: NULL, dry-run plan or buffer too small");
+  if ((!buf && need) || n < need || !p->params.snapshot) {
+    set_error("mk_get_counters: buffer too small, or the plan was compiled without "
+              "snapshot_counters");
     return MK_ERR_INVALID_ARG;
   }
   CUDA_TRY(cudaDeviceSynchronize());
-  if (need) CUDA_TRY(cudaMemcpy(buf, p->params.counters, need * 4, cudaMemcpyDeviceToHost));
+  if (need) CUDA_TRY(cudaMemcpy(buf, p->params.snapshot, need * 4, cudaMemcpyDeviceToHost));
   return MK_OK;
 }

@@ -98,10 +98,13 @@ struct Params {
   int32_t* counters;        // dependency counters, then split semaphores
   int32_t* status;          // 8 int32: mk_device_status
   const void* tmaps;        // CUtensorMap array (64-byte aligned), global memory
+  int32_t* done;            // CTAs finished in this run (the last one resets the run state)
+  int32_t* last_status;     // status of the last completed run (read by the host)
+  int32_t* snapshot;        // copy of the counters at the end of a run, or null
   int32_t n_instr;
   int32_t n_sm;             // placement stride
   int32_t n_tmaps;
-  int32_t pad0;
+  int32_t n_counters;       // dependency counters + split semaphores
   uint64_t timeout_ns;
 };
 

@@ -40,7 +40,7 @@ def assert_close(got, ref, what=""):
 
 def run(wl, **opts):
     g, id_of = workloads.build_graph(wl.desc, wl.data)
-    plan = g.compile(**opts)
+    plan = g.compile(snapshot_counters=1, **opts)
     plan.run()
     plan.check_status()
     torch.cuda.synchronize()
@@ -48,6 +48,7 @@ def run(wl, **opts):
 
 
 def check_counters(plan, wl, opts):
+    opts = {k: v for k, v in opts.items() if k != "snapshot_counters"}
     py = osched.lower(wl.desc, dict(opts, n_sm=plan.stats()["n_sm"]))
     assert plan.counters().tolist() == py.final_counters()
 
@@ -153,7 +154,7 @@ def test_gemv(m, n, k, splits, norm, dual, res):
     ix, iw, iwu, ig, ir, io = (g.tensor(t) for t in (x, w, wu, gamma, r, out))
     g.matmul(ix, iw, io, gamma=ig if norm else None, b_up=iwu if dual else None,
              residual=ir if res else None, eps=1e-5)
-    p = g.compile(gemv_splits=splits)
+    p = g.compile(gemv_splits=splits, snapshot_counters=1)
     p.run()
     p.check_status()
     X, W, WU, G, R = f32(x), f32(w), f32(wu), f32(gamma)[0], f32(r)
@@ -293,18 +294,58 @@ def test_decode_small_decoder():
     check_counters(plan, wl, {})
 
 
+def check_decode_per_node(wl, kc0, vc0):
+    """Every node of every layer against the oracle applied to the GPU's own inputs of that node
+    (teacher forcing), at full size. End to end, two valid fp32 summation orders of the oracle
+    itself drift apart by ~1.4e-2 relative Frobenius over 16 bf16 layers, so the tolerance is
+    applied per node, where it is meaningful."""
+    sh = wl.info["shape"]
+    wts, _, _, p = _decode_ref(wl)
+    D = wl.data
+    hq, hkv, hd = sh.hq, sh.hkv, sh.hd
+    cap = wl.info["cap"]
+    qkv, qr, att, hh, gu, xo = (f32(D[wl.info[k]]) for k in ("qkv", "qr", "att", "h", "gu", "out"))
+    kc = f32(D[wl.info["kc"]]).reshape(sh.layers, cap, -1)
+    vc = f32(D[wl.info["vc"]]).reshape(sh.layers, cap, -1)
+    x_prev = f32(D[0])
+    for l in range(sh.layers):
+        assert_close(qkv[l:l + 1], ops.matmul_norm_input(x_prev, wts.g_attn[l], sh.eps,
+                                                         wts.wqkv[l], BF16), f"qkv {l}")
+        q_in = qkv[l:l + 1, :hq * hd]
+        k_in = qkv[l:l + 1, hq * hd:(hq + hkv) * hd]
+        v_in = qkv[l:l + 1, (hq + hkv) * hd:]
+        assert_close(qr[l:l + 1], ops.rope(q_in, [p], hq, hd, sh.theta, BF16), f"rope q {l}")
+        assert_close(kc[l, p:p + 1], ops.rope(k_in, [p], hkv, hd, sh.theta, BF16), f"rope k {l}")
+        assert np.array_equal(vc[l, p:p + 1], v_in), f"v append {l}"
+        assert np.array_equal(kc[l, :p], kc0[l, :p]) and np.array_equal(vc[l, :p], vc0[l, :p])
+        assert_close(att[l:l + 1], ops.attention(qr[l:l + 1], kc[l, :p + 1], vc[l, :p + 1], hq,
+                                                 hkv, hd, False, p, 1 / math.sqrt(hd), BF16),
+                     f"attention {l}")
+        assert_close(hh[l:l + 1], ops.matmul(att[l:l + 1], wts.wo[l], BF16, residual=x_prev),
+                     f"o-proj {l}")
+        assert_close(gu[l:l + 1], ops.matmul_norm_input(hh[l:l + 1], wts.g_mlp[l], sh.eps,
+                                                        wts.wg[l], BF16, w_up=wts.wu[l]),
+                     f"gate/up {l}")
+        assert_close(xo[l:l + 1], ops.matmul(gu[l:l + 1], wts.wd[l], BF16,
+                                             residual=hh[l:l + 1]), f"down {l}")
+        x_prev = xo[l:l + 1]
+
+
 def test_decode_full_config():
     wl = workloads.decode(device=DEV, seed=0)
-    x0 = f32(wl.data[0])
     sh = wl.info["shape"]
     cap = wl.info["cap"]
+    x0 = f32(wl.data[0])
     kc0 = f32(wl.data[wl.info["kc"]]).reshape(sh.layers, cap, -1).copy()
     vc0 = f32(wl.data[wl.info["vc"]]).reshape(sh.layers, cap, -1).copy()
     plan, _ = run(wl)
+    check_counters(plan, wl, {})
+    check_decode_per_node(wl, kc0, vc0)
+    # end to end: within twice the oracle-vs-oracle drift of the same depth (1.4e-2)
     wts, _, _, p = _decode_ref(wl)
     ref, _, _ = models.decode_step(x0, wts, list(kc0), list(vc0), p)
-    assert_close(f32(wl.data[wl.info["out"]])[-1:], ref, "16-layer decode output")
-    check_counters(plan, wl, {})
+    got = f32(wl.data[wl.info["out"]])[-1:]
+    assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= 3e-2
 
 
 # ------------------------------------------------------------------ runtime behaviour
