@@ -209,6 +209,28 @@ mk_status mk_sync_status(mk_plan_t p, mk_device_status* st);
 
 mk_status mk_plan_destroy(mk_plan_t p);
 
+/* Allocation-free matrix product for a few rows: out[m x n] = x[m x k] @ w[k x n], run by the
+ * same persistent kernel as split-K GEMV tiles. The pages have no counterpart of this entry
+ * point; it exists for callers that cannot allocate device memory when they need the product
+ * (a serving loop whose device memory an up-front pool owns, code inside that pool's callbacks,
+ * paths where cudaMalloc / cudaFree would synchronise the device). It calls no cudaMalloc,
+ * cudaFree or allocating library routine: all run state (instruction records, node entry,
+ * tensor map, split semaphores, status, fp32 split partials) lives in one file-scope device
+ * array of 4 MiB that every GPU using the library holds until the process exits.
+ *   x, w, out  caller-owned device memory, row-major and contiguous, 16-byte aligned.
+ *   m 1..8; n >= 1 and k >= 0 multiples of 8; n <= 131072 (the array holds 1024 column tiles of
+ *              128); larger sizes return MK_ERR_UNSUPPORTED with a message.
+ *   dtype      MK_F16 or MK_BF16 (fp32 accumulation, one rounding at the end).
+ *   stream     cudaStream_t (NULL = legacy default stream). Asynchronous unless `status` is
+ *              non-NULL: then the call synchronises the stream and fills *status.
+ * The first call on each device, with that device current, looks up the array's device address
+ * (cudaGetSymbolAddress) and sets the kernel's shared-memory limit; make that first call before
+ * any stream capture. Every call shares the array and clears the parts that must start at zero;
+ * the rest keeps the previous call's contents. Calls that overlap on the GPU (different
+ * streams, or host threads calling at once) race on the array and must not be issued. */
+mk_status mk_gemv_noalloc(const void* x, const void* w, void* out, int32_t m, int32_t n,
+                          int32_t k, int32_t dtype, void* stream, mk_device_status* status);
+
 /* ---------------------------------------------------------------- introspection */
 
 typedef struct {

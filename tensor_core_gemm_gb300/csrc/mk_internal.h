@@ -4,6 +4,7 @@
 #include <stdarg.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <string>
 #include <vector>
 
