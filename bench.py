@@ -103,6 +103,31 @@ def value_of(wl, ms, name):
     return wl.flops / (ms * 1e-3) / 1e12
 
 
+def kernel_source_sha():
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("mk_kernel.cu", "mk_ptx.cuh", "mk_types.h"):
+        with open(os.path.join(ROOT, "tensor_core_gemm_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(config):
+    """DRAM bytes per launch from the committed ncu summary of this workload, or None when
+    there is none or the kernel source changed since it was captured."""
+    path = os.path.join(ROOT, "profiles", f"megakernel_{config}.md")
+    if not os.path.exists(path):
+        return None
+    sha, traffic = None, None
+    with open(path) as f:
+        for line in f:
+            if line.startswith("kernel_source_sha:"):
+                sha = line.split()[1]
+            elif line.startswith("dram_bytes_per_launch:"):
+                traffic = int(line.split()[1])
+    return traffic if sha == kernel_source_sha() else None
+
+
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
@@ -119,7 +144,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.th = threading.Thread(target=self._read, daemon=True)
             self.th.start()
@@ -260,7 +285,7 @@ def run_reference(args, world, rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="mk", choices=["mk", "reference"])
     ap.add_argument("--config", default="gemm4096", choices=sorted(CONFIGS))
@@ -367,11 +392,7 @@ def main():
         peak = float(peaks["hbm_gbs"])
         achieved = wl.hbm_bytes / (ms * 1e-3) / 1e9
         runit = "GB/s"
-    traffic = None
-    prof = os.path.join(ROOT, "profiles", f"traffic_{args.config}.json")
-    if os.path.exists(prof):
-        with open(prof) as f:
-            traffic = json.load(f).get("dram_bytes_per_launch")
+    traffic = profiled_traffic(args.config)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
