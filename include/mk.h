@@ -153,7 +153,7 @@ typedef struct {
   int32_t ew_rows, ew_cols, ew_tiles;   /* elementwise instruction = ew_rows x ew_cols*ew_tiles */
   int32_t norm_rows;     /* rows per RMSNORM / ROPE instruction */
   int32_t gemv_max_m;    /* matmuls with M <= this lower to GEMV tiles */
-  int32_t gemv_tile_n;   /* GEMV output columns per tile (halved for SILU_MUL) */
+  int32_t gemv_tile_n;   /* GEMV output columns per tile: 256 (halved for SILU_MUL) */
   int32_t gemv_splits;   /* K splits per GEMV tile; 0 = max(1, n_sm / column tiles) */
   int32_t gemv_kstep;    /* GEMV K chunks are multiples of this */
   int32_t attn_chunk;    /* keys per split-KV partial */
@@ -164,6 +164,9 @@ typedef struct {
   int32_t debug_counter; /* test hook: counter whose target is raised by debug_extra (-1: none) */
   int32_t debug_extra;
   int32_t snapshot_counters; /* 1: keep each run's final counter values for mk_get_counters */
+  int32_t trace;         /* 1: record per-instruction timestamps for mk_get_trace */
+  int32_t l2_prefetch;   /* instructions (current included, <= 8) whose streamed operands the
+                            loader prefetches into L2 ahead of use; 0 = off */
 } mk_compile_opts;
 
 /* Fill *o with the defaults (the values listed above for each field). */
@@ -218,8 +221,8 @@ mk_status mk_plan_destroy(mk_plan_t p);
  * tensor map, split semaphores, status, fp32 split partials) lives in one file-scope device
  * array of 4 MiB that every GPU using the library holds until the process exits.
  *   x, w, out  caller-owned device memory, row-major and contiguous, 16-byte aligned.
- *   m 1..8; n >= 1 and k >= 0 multiples of 8; n <= 131072 (the array holds 1024 column tiles of
- *              128); larger sizes return MK_ERR_UNSUPPORTED with a message.
+ *   m 1..8; n >= 1 and k >= 0 multiples of 8; n <= 262144 (the array holds 1024 column tiles of
+ *              256); larger sizes return MK_ERR_UNSUPPORTED with a message.
  *   dtype      MK_F16 or MK_BF16 (fp32 accumulation, one rounding at the end).
  *   stream     cudaStream_t (NULL = legacy default stream). Asynchronous unless `status` is
  *              non-NULL: then the call synchronises the stream and fills *status.
@@ -264,6 +267,13 @@ mk_status mk_get_counter_targets(mk_plan_t p, int32_t* host_buf, size_t n);
  * counter equals its target and each split semaphore its number of K splits. Needs a plan
  * compiled with snapshot_counters = 1; synchronises. */
 mk_status mk_get_counters(mk_plan_t p, int32_t* host_buf, size_t n);
+
+/* Per-instruction timestamps of the last run (plans compiled with trace = 1), %globaltimer ns:
+ * for instruction i, buf[6i..6i+5] = {the compute warpgroup took the descriptor, the scheduler
+ * saw every source counter complete, the compute warpgroup saw that, the instruction's body
+ * ended, the instruction was published, the SM index}. A slot an op does not reach stays 0.
+ * n >= 6 * n_instr; synchronises. */
+mk_status mk_get_trace(mk_plan_t p, uint64_t* host_buf, size_t n);
 
 const char* mk_last_error(void);
 int32_t mk_abi_version(void);

@@ -29,10 +29,9 @@ Lowering rules per node (tile sizes come from ``opts``; see ``DEFAULT_OPTS``):
       (aux0 = rank). Reads A rows×[0,K), B [0,K)×cols (and b2), bias/residual on the tile box;
       writes the tile box (every instruction of a cluster writes the whole cluster tile).
   matmul, M <= gemv_max_m -> GEMV tiles: column tiles of gemv_tile_n (halved with b2), each
-      split along K into
-      S chunks (gemv_splits, or max(1, n_sm div n_col_tiles) when 0); the chunk length is
-      ceil(K/S) rounded up to gemv_kstep (at least gemv_kstep) and S is then recomputed as ceil(K/chunk). Order: column
-      tile outer, split inner; aux0 = split index, aux1 = S. Split s reads A[:, chunk] (all of A
+      split along K into S chunks (gemv_splits, or max(1, n_sm div n_col_tiles) when 0); the
+      chunk length is ceil(K/S) rounded up to gemv_kstep (at least gemv_kstep) and S is then
+      recomputed as ceil(K/chunk). Order: column tile outer, split inner; aux0 = split index, aux1 = S. Split s reads A[:, chunk] (all of A
       with a norm gamma), B[chunk, cols]; only split 0 carries the output box; every split carries
       split 0's counter arrivals, because the last split to finish reduces and publishes the tile.
       Each tile owns one split semaphore, numbered after the dependency counters.
@@ -50,6 +49,9 @@ Lowering rules per node (tile sizes come from ``opts``; see ``DEFAULT_OPTS``):
   attention with several query rows (prefill) -> one instruction per (q tile t of attn_tile_q
       rows, q head h), t descending (longest first), then h ascending; reads q rows of the tile,
       k and v rows [0, kmax) with kmax = min(Tk, q_pos0 + end of tile) when causal.
+
+Flags: B_DEP marks a GEMM, GEMV or attention-partial instruction whose streamed operand (the
+weight, or the key/value chunk) has a producer inside the graph, so it cannot be prefetched.
 
 Counters: consumer instructions are visited in index order, their read boxes in order, and for
 each the earlier phases in order; a new (phase, set) key takes the next counter id. A consumer's
@@ -69,7 +71,7 @@ DEFAULT_OPTS = dict(
     gemm_tile_m=128, gemm_tile_n=256, cluster=1,
     ew_rows=128, ew_cols=128, ew_tiles=1,
     norm_rows=16,
-    gemv_max_m=8, gemv_tile_n=128, gemv_splits=0, gemv_kstep=128,
+    gemv_max_m=8, gemv_tile_n=256, gemv_splits=0, gemv_kstep=64,
     attn_chunk=64, attn_tile_q=128,
 )
 
@@ -218,9 +220,9 @@ def _lower_attention(ni, nd, opts, phases, tensors):
                 k0 = c * ch
                 kl = min(ch, tk - k0)
                 ins = Instr(OP_ATTN_PARTIAL, ni, 0, g, k0, kl, c, nc)
-                ins.reads.append((_box(q, 0, 1, g * g_sz * d, (g + 1) * g_sz * d), ROLE_E))
-                ins.reads.append((_box(k, k0, k0 + kl, g * d, (g + 1) * d), ROLE_E))
-                ins.reads.append((_box(v, k0, k0 + kl, g * d, (g + 1) * d), ROLE_E))
+                ins.reads.append((_box(q, 0, 1, g * g_sz * d, (g + 1) * g_sz * d), ROLE_A))
+                ins.reads.append((_box(k, k0, k0 + kl, g * d, (g + 1) * d), ROLE_B))
+                ins.reads.append((_box(v, k0, k0 + kl, g * d, (g + 1) * d), ROLE_B))
                 r0 = (g * nc + c) * g_sz
                 ins.writes.append(_box(scratch, r0, r0 + g_sz, 0, d + 2))
                 part.append(ins)
@@ -350,7 +352,7 @@ def lower(graph, opts):
                     targets.append(len(st))
                     members.append(st)
                 cid = keys[key]
-                if role == ROLE_B and c.op in (OP_GEMM, OP_GEMV):
+                if role == ROLE_B and c.op in (OP_GEMM, OP_GEMV, OP_ATTN_PARTIAL):
                     c.flags |= FLAG_B_DEP
                 if cid not in seen:
                     seen.add(cid)

@@ -16,7 +16,7 @@ EXPORTS = [
     "mk_add_elementwise", "mk_add_attention", "mk_default_opts", "mk_compile", "mk_run",
     "mk_run_host", "mk_sync_status", "mk_plan_destroy", "mk_plan_stats", "mk_get_instructions",
     "mk_get_src_list", "mk_get_dst_list", "mk_get_counter_targets", "mk_get_counters",
-    "mk_last_error", "mk_abi_version", "mk_gemv_noalloc",
+    "mk_last_error", "mk_abi_version", "mk_gemv_noalloc", "mk_get_trace",
 ]
 
 
@@ -41,7 +41,7 @@ class CompileOpts(C.Structure):
         "n_sm", "gemm_tile_m", "gemm_tile_n", "cluster", "ew_rows", "ew_cols", "ew_tiles",
         "norm_rows", "gemv_max_m", "gemv_tile_n", "gemv_splits", "gemv_kstep", "attn_chunk",
         "attn_tile_q", "dry_run", "timeout_ms", "device", "debug_counter", "debug_extra",
-        "snapshot_counters")]
+        "snapshot_counters", "trace", "l2_prefetch")]
 
 
 class HostCopy(C.Structure):
@@ -94,6 +94,7 @@ def load():
         "mk_get_dst_list": [P, PI32, C.c_size_t],
         "mk_get_counter_targets": [P, PI32, C.c_size_t],
         "mk_get_counters": [P, PI32, C.c_size_t],
+        "mk_get_trace": [P, C.POINTER(C.c_uint64), C.c_size_t],
         "mk_gemv_noalloc": [VP, VP, VP, I32, I32, I32, I32, VP, C.POINTER(DeviceStatus)],
     }
     for name, args in sig.items():

@@ -196,6 +196,14 @@ class Plan:
     def counter_targets(self):
         return self._ints(self._lib.mk_get_counter_targets, self.stats()["n_counters"])
 
+    def trace(self):
+        """Per-instruction [t_descriptor, t_sources_ready (scheduler), t_sources_seen (compute),
+        t_body_end, t_published, sm] (ns) of the last run."""
+        n = self.stats()["n_instr"]
+        buf = np.zeros(max(1, 6 * n), dtype=np.uint64)
+        check(self._lib.mk_get_trace(self._h, buf.ctypes.data_as(C.POINTER(C.c_uint64)), 6 * n))
+        return buf[:6 * n].reshape(-1, 6)
+
     def counters(self):
         s = self.stats()
         return self._ints(self._lib.mk_get_counters, s["n_counters"] + s["n_sems"])

@@ -189,9 +189,9 @@ static void lower_attention(std::vector<TensorRec>& ts, int ni, const NodeRec& n
       for (int64_t c = 0; c < nc; ++c) {
         const int64_t k0 = c * ch, kl = std::min(ch, tk - k0);
         HInstr h = make(OP_ATTN_PARTIAL, ni, 0, (int)g, (int)k0, (int)kl, (int)c, (int)nc);
-        h.reads.push_back({window(ts, nd.a, 0, 1, g * g_sz * d, (g + 1) * g_sz * d), ROLE_E});
-        h.reads.push_back({window(ts, nd.b, k0, k0 + kl, g * d, (g + 1) * d), ROLE_E});
-        h.reads.push_back({window(ts, nd.b2, k0, k0 + kl, g * d, (g + 1) * d), ROLE_E});
+        h.reads.push_back({window(ts, nd.a, 0, 1, g * g_sz * d, (g + 1) * g_sz * d), ROLE_A});
+        h.reads.push_back({window(ts, nd.b, k0, k0 + kl, g * d, (g + 1) * d), ROLE_B});
+        h.reads.push_back({window(ts, nd.b2, k0, k0 + kl, g * d, (g + 1) * d), ROLE_B});
         const int64_t r0 = (g * nc + c) * g_sz;
         h.writes.push_back(window(ts, sid, r0, r0 + g_sz, 0, d + 2));
         part.push_back(std::move(h));
@@ -308,7 +308,8 @@ mk_status lower_graph(const std::vector<TensorRec>& tensors_in, const std::vecto
         } else {
           cid = it->second;
         }
-        if (rd.second == ROLE_B && (c.rec.op == OP_GEMM || c.rec.op == OP_GEMV))
+        if (rd.second == ROLE_B &&
+            (c.rec.op == OP_GEMM || c.rec.op == OP_GEMV || c.rec.op == OP_ATTN_PARTIAL))
           c.rec.flags |= IFLAG_B_DEP;
         bool seen = false;
         for (auto& s : c.src) seen |= (s.first == cid);
@@ -654,9 +655,9 @@ extern "C" mk_status mk_default_opts(mk_compile_opts* o) {
   o->ew_tiles = 1;
   o->norm_rows = 16;
   o->gemv_max_m = 8;
-  o->gemv_tile_n = 128;
+  o->gemv_tile_n = 256;
   o->gemv_splits = 0;
-  o->gemv_kstep = 128;
+  o->gemv_kstep = 64;
   o->attn_chunk = 64;
   o->attn_tile_q = 128;
   o->dry_run = 0;
@@ -665,5 +666,7 @@ extern "C" mk_status mk_default_opts(mk_compile_opts* o) {
   o->debug_counter = -1;
   o->debug_extra = 0;
   o->snapshot_counters = 0;
+  o->trace = 0;
+  o->l2_prefetch = 0;
   return MK_OK;
 }

@@ -31,11 +31,12 @@ enum RoleId { R_SCHED = 0, R_LOAD = 1, R_MMA = 2, R_COMPUTE = 3 };
 constexpr unsigned FULL = 0xffffffffu;
 constexpr int kCompute = 128;   // threads of the compute warpgroup
 constexpr int kBarCompute = 1;  // named barrier of the compute warpgroup
+constexpr int kXrFloats = 5120; // GEMV activation staging (M x chunk), reused for its epilogue
 
 struct __align__(1024) Smem {
   uint8_t stage[kStages][kStageBytes];  // operand ring (1024-byte aligned: 128-byte swizzle)
-  float red[4][8][128];                 // GEMV cross-warp reduction / epilogue exchange
-  float xbuf[8][kGemvRows];             // GEMV activation chunk (normalised when fused)
+  float xr[kXrFloats];                  // GEMV activations, then its output exchange
+  float red_small[8][4];                // per-row, per-warp partial sums
   uint8_t slot[kSlots][kSlotBytes];     // instruction record + node entry per slot
   uint64_t full[kStages];
   uint64_t empty[kStages];
@@ -67,6 +68,7 @@ __device__ __forceinline__ const void* tmap_at(const Params& p, int i) {
 __device__ __forceinline__ int ring_stages(const Instr& in) {
   if (in.op == OP_GEMM) return (in.klen + kGemmBK - 1) / kGemmBK;
   if (in.op == OP_GEMV) return (in.klen + kGemvRows - 1) / kGemvRows;
+  if (in.op == OP_ATTN_PARTIAL) return 1;  // the key/value chunk
   return 0;
 }
 __device__ __forceinline__ int instr_index(const Params& p, int it) {
@@ -120,6 +122,10 @@ __device__ __forceinline__ bool cw_wait(const Params& p, uint32_t bar, uint32_t 
   return bar_and(kBarCompute, kCompute, ok);
 }
 __device__ __forceinline__ void cw_sync() { bar_sync(kBarCompute, kCompute); }
+// Trace point `k` of instruction `idx` (compute warpgroup, thread 0), when tracing is on.
+__device__ __forceinline__ void trace_mark(const Params& p, int idx, int k) {
+  if (p.trace && threadIdx.x == kThreads - kCompute) p.trace[(size_t)idx * kTraceWords + k] = globaltimer();
+}
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -170,6 +176,11 @@ __device__ __forceinline__ void store8(const Operand& o, int row, int col, int d
 __device__ __forceinline__ float load1(const Operand& o, int row, int col, int dt) {
   const uint16_t* ptr = reinterpret_cast<const uint16_t*>(o.ptr) + (size_t)row * o.ld + col;
   return h2f(__ldcg(reinterpret_cast<const unsigned short*>(ptr)), dt);
+}
+__device__ __forceinline__ void store2(const Operand& o, int row, int col, int dt, float v0,
+                                       float v1) {
+  uint16_t* ptr = reinterpret_cast<uint16_t*>(o.ptr) + (size_t)row * o.ld + col;
+  *reinterpret_cast<uint32_t*>(ptr) = (uint32_t)f2h(v0, dt) | ((uint32_t)f2h(v1, dt) << 16);
 }
 __device__ __forceinline__ void store1(const Operand& o, int row, int col, int dt, float v) {
   uint16_t* ptr = reinterpret_cast<uint16_t*>(o.ptr) + (size_t)row * o.ld + col;
@@ -235,6 +246,7 @@ __device__ void run_scheduler(const Params& p, Smem& s) {
           // later TMA (async-proxy) reads of the producers' data are ordered after the acquire
           fence_proxy_async_global();
           mbar_arrive(smem_u32(&s.deps_ready[slot]));
+          if (p.trace) p.trace[(size_t)instr_index(p, ready) * kTraceWords + 1] = globaltimer();
         }
         ++ready;
         progress = true;
@@ -312,14 +324,16 @@ __device__ bool load_gemm(const Params& p, Smem& s, const Instr& in, const Node&
   return true;
 }
 
+__device__ void prefetch_ahead(const Params& p, const Smem& s, int cur, int& next);
+
 __device__ bool load_gemv(const Params& p, Smem& s, const Instr& in, const Node& nd, int slot,
-                          uint32_t use, uint32_t& fill, int idx) {
+                          uint32_t use, uint32_t& fill, int idx, int it, int& pf_next) {
   const int nk = ring_stages(in);
   if (nk == 0) return true;
   const bool dual = (nd.flags & EPI_SILU_MUL) != 0;
-  const int w = nd.tile_n;
-  const uint32_t part = (uint32_t)(w * kGemvRows * 2);
-  const uint32_t bytes = dual ? 2 * part : part;
+  // a stage is four 64-row x 64-column boxes, 128-byte swizzled (8 KB each): the tile's 256
+  // columns, or 128 gate columns then 128 up columns
+  const uint32_t bytes = 4u * 64u * kGemvRows * 2u;
   const void* tb = tmap_at(p, nd.b.tmap);
   const void* tb2 = dual ? tmap_at(p, nd.b2.tmap) : nullptr;
   if (in.flags & IFLAG_B_DEP) {
@@ -328,20 +342,79 @@ __device__ bool load_gemv(const Params& p, Smem& s, const Instr& in, const Node&
   }
   for (int kb = 0; kb < nk; ++kb) {
     const int st = (int)(fill % kStages);
+    if (kb >= kStages) prefetch_ahead(p, s, it, pf_next);  // descriptors published meanwhile
     if (!wait_mbar(p, smem_u32(&s.empty[st]), ((fill / kStages) & 1u) ^ 1u, R_LOAD, 15, idx))
       return false;
     const uint32_t bar = smem_u32(&s.full[st]);
     mbar_expect_tx(bar, bytes);
-    tma_load_2d(smem_u32(s.stage[st]), tb, bar, in.n0, in.k0 + kb * kGemvRows);
-    if (dual) tma_load_2d(smem_u32(s.stage[st]) + part, tb2, bar, in.n0, in.k0 + kb * kGemvRows);
+    for (int j = 0; j < 4; ++j) {
+      const void* map = (dual && j >= 2) ? tb2 : tb;
+      const int x = in.n0 + 64 * (dual ? (j & 1) : j);
+      tma_load_2d(smem_u32(s.stage[st]) + j * 8192, map, bar, x, in.k0 + kb * kGemvRows);
+    }
     ++fill;
   }
   return true;
 }
 
+// Split-KV partial: the chunk's keys and values (head g = n0, 64 columns each) land in one
+// stage, 128-byte swizzled: keys at offset 0, values at 16 KB. A chunk that does not contain a
+// row appended inside the graph streams before the query is ready.
+__device__ bool load_attn(const Params& p, Smem& s, const Instr& in, const Node& nd, int slot,
+                          uint32_t use, uint32_t& fill, int idx) {
+  if (in.flags & IFLAG_B_DEP) {
+    if (!wait_mbar(p, smem_u32(&s.deps_ready[slot]), use & 1u, R_LOAD, 16, idx)) return false;
+    fence_proxy_async_global();
+  }
+  const int st = (int)(fill % kStages);
+  if (!wait_mbar(p, smem_u32(&s.empty[st]), ((fill / kStages) & 1u) ^ 1u, R_LOAD, 17, idx))
+    return false;
+  const uint32_t bar = smem_u32(&s.full[st]);
+  mbar_expect_tx(bar, (uint32_t)(2 * nd.tile_m * 128));
+  tma_load_2d(smem_u32(s.stage[st]), tmap_at(p, nd.b.tmap), bar, in.n0 * 64, in.k0);
+  tma_load_2d(smem_u32(s.stage[st]) + 16384, tmap_at(p, nd.b2.tmap), bar, in.n0 * 64, in.k0);
+  ++fill;
+  return true;
+}
+
+// L2 prefetch of the streamed operands of instructions already published to later slots: HBM
+// keeps streaming weights (and key/value chunks) while earlier instructions wait for their
+// activations; their shared-memory loads then hit L2. `next` is the first instruction not yet
+// prefetched; instructions whose operand is produced inside the graph are skipped.
+__device__ void prefetch_ahead(const Params& p, const Smem& s, int cur, int& next) {
+  if (next < cur) next = cur;
+  while (next < cur + p.l2_prefetch) {
+    const int slot = next % kSlots;
+    if (!mbar_try(smem_u32(&s.instr_ready[slot]), (uint32_t)(next / kSlots) & 1u)) return;
+    const Instr& f = slot_instr(s, slot);
+    if (f.op == OP_END) {
+      next = 0x3fffffff;
+      return;
+    }
+    const Node& nd = slot_node(s, slot);
+    if (!(f.flags & IFLAG_B_DEP)) {
+      if (f.op == OP_GEMV) {
+        const bool dual = (nd.flags & EPI_SILU_MUL) != 0;
+        const int nk = ring_stages(f);
+        for (int kb = 0; kb < nk; ++kb) {
+          for (int j = 0; j < 4; ++j) {
+            const void* map = tmap_at(p, (dual && j >= 2) ? nd.b2.tmap : nd.b.tmap);
+            tma_prefetch_l2_2d(map, f.n0 + 64 * (dual ? (j & 1) : j), f.k0 + kb * kGemvRows);
+          }
+        }
+      } else if (f.op == OP_ATTN_PARTIAL) {
+        tma_prefetch_l2_2d(tmap_at(p, nd.b.tmap), f.n0 * 64, f.k0);
+        tma_prefetch_l2_2d(tmap_at(p, nd.b2.tmap), f.n0 * 64, f.k0);
+      }
+    }
+    ++next;
+  }
+}
+
 __device__ void run_loader(const Params& p, Smem& s) {
   for (int i = 0; i < p.n_tmaps; ++i) tensormap_acquire(tmap_at(p, i));
   uint32_t fill = 0;
+  int pf_next = 0;
   for (int it = 0;; ++it) {
     const int slot = it % kSlots;
     const uint32_t use = (uint32_t)(it / kSlots);
@@ -350,9 +423,11 @@ __device__ void run_loader(const Params& p, Smem& s) {
     const Instr& in = slot_instr(s, slot);
     if (in.op == OP_END) break;
     const Node& nd = slot_node(s, slot);
+    prefetch_ahead(p, s, it, pf_next);
     bool ok = true;
     if (in.op == OP_GEMM) ok = load_gemm(p, s, in, nd, slot, use, fill, idx);
-    else if (in.op == OP_GEMV) ok = load_gemv(p, s, in, nd, slot, use, fill, idx);
+    else if (in.op == OP_GEMV) ok = load_gemv(p, s, in, nd, slot, use, fill, idx, it, pf_next);
+    else if (in.op == OP_ATTN_PARTIAL) ok = load_attn(p, s, in, nd, slot, use, fill, idx);
     if (!ok) break;
     mbar_arrive(smem_u32(&s.slot_free[slot]));
   }
@@ -420,7 +495,7 @@ __device__ void run_mma(const Params& p, Smem& s, uint32_t tmem) {
         tc_commit(smem_u32(&s.acc_full[as]));
         ++acc_n;
       }
-    } else if (in.op == OP_GEMV) {
+    } else {
       use += (uint32_t)ring_stages(in);  // stages consumed by the compute warpgroup
     }
     mbar_arrive(smem_u32(&s.slot_free[slot]));
@@ -439,6 +514,7 @@ __device__ bool gemm_epilogue(const Params& p, Smem& s, const Instr& in, const N
   const int ct = (int)threadIdx.x - (kThreads - kCompute);
   const int q = ct >> 5, lane = ct & 31;
   if (!cw_wait(p, smem_u32(&s.deps_ready[slot]), use & 1u, 30, idx)) return false;
+  trace_mark(p, idx, 2);
   const int nk = ring_stages(in);
   const uint32_t as = acc_n & 1u;
   if (nk > 0) {
@@ -502,114 +578,168 @@ __device__ bool gemm_epilogue(const Params& p, Smem& s, const Instr& in, const N
   return true;
 }
 
-// GEMV tile: out[0..M) x [n0, n0 + w) for one K chunk; split partials reduced by the last split.
+// One 64-row weight stage of a GEMV for MT activation rows (compile-time), element type BF
+// (compile-time): acc[m][0..1] += sum_kk x[m][kk] * W[kk][col..col+1], W read from a 64-column
+// box in the 128-byte swizzled layout TMA writes. Four activations per shared-memory read; the
+// weight pair of each row is one 4-byte read (a warp covers one 128-byte row: no conflicts).
+template <int MT, bool BF>
+__device__ __forceinline__ void gemv_stage(const uint8_t* B, int ch, const float* xs,
+                                           int xstride, float (&acc)[8][2]) {
+#pragma unroll 2
+  for (int kk = 0; kk < kGemvRows; kk += 4) {
+    float xv[MT][4];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      const float4 x4 = *reinterpret_cast<const float4*>(xs + m * xstride + kk);
+      xv[m][0] = x4.x;
+      xv[m][1] = x4.y;
+      xv[m][2] = x4.z;
+      xv[m][3] = x4.w;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int r = kk + u;  // 128-byte row r of the box; 16-byte chunk ch sits at ch ^ (r & 7)
+      const uint32_t raw = *reinterpret_cast<const uint32_t*>(B + r * 128 + ((ch ^ (r & 7)) << 4));
+      float f0, f1;
+      if (BF) {
+        f0 = __uint_as_float(raw << 16);
+        f1 = __uint_as_float(raw & 0xffff0000u);
+      } else {
+        f0 = __half2float(__ushort_as_half((uint16_t)(raw & 0xffffu)));
+        f1 = __half2float(__ushort_as_half((uint16_t)(raw >> 16)));
+      }
+#pragma unroll
+      for (int m = 0; m < MT; ++m) {
+        acc[m][0] = fmaf(xv[m][u], f0, acc[m][0]);
+        acc[m][1] = fmaf(xv[m][u], f1, acc[m][1]);
+      }
+    }
+  }
+}
+
+template <bool BF>
+__device__ __forceinline__ void gemv_stage_rows(int M, const uint8_t* B, int ch, const float* xs,
+                                                int xstride, float (&acc)[8][2]) {
+  switch (M) {
+    case 1: gemv_stage<1, BF>(B, ch, xs, xstride, acc); break;
+    case 2: gemv_stage<2, BF>(B, ch, xs, xstride, acc); break;
+    case 3: gemv_stage<3, BF>(B, ch, xs, xstride, acc); break;
+    case 4: gemv_stage<4, BF>(B, ch, xs, xstride, acc); break;
+    case 5: gemv_stage<5, BF>(B, ch, xs, xstride, acc); break;
+    case 6: gemv_stage<6, BF>(B, ch, xs, xstride, acc); break;
+    case 7: gemv_stage<7, BF>(B, ch, xs, xstride, acc); break;
+    default: gemv_stage<8, BF>(B, ch, xs, xstride, acc); break;
+  }
+}
+
+// GEMV tile: out[0..M) x [n0, n0 + w) for one K chunk; split partials reduced by the last
+// split to finish. The chunk's activations (normalised when the norm is fused) are staged once
+// in shared memory with batched loads. Each thread owns two adjacent output columns of the tile
+// (with SILU_MUL: threads 0-63 the gate columns, 64-127 the up columns) over every K row, so a
+// stage needs no cross-thread reduction. Weight stages arrive as 128-byte swizzled boxes:
+// unswizzled TMA writes of rows 128 bytes apart land on the same shared-memory banks ("Hand-
+// writing a Blackwell GEMM", step 4).
 __device__ bool gemv(const Params& p, Smem& s, const Instr& in, const Node& nd, int slot,
                      uint32_t use, uint32_t& ring, bool* publish, int idx) {
   const int ct = (int)threadIdx.x - (kThreads - kCompute);
   const int wp = ct >> 5, lane = ct & 31;
   if (!cw_wait(p, smem_u32(&s.deps_ready[slot]), use & 1u, 40, idx)) return false;
+  trace_mark(p, idx, 2);
   const int M = nd.M, dt = nd.dtype;
   const bool dual = (nd.flags & EPI_SILU_MUL) != 0;
   const bool norm = (nd.flags & EPI_RMSNORM_INPUT) != 0;
-  const int wcols = nd.tile_n;
+  const int wcols = nd.tile_n;                 // 256, or 128 per weight with SILU_MUL
+  const int nk = ring_stages(in);
+  const int kpad = nk * kGemvRows;
+  const int kend = in.k0 + in.klen;
+  const bool staged = M * kpad <= kXrFloats;
   if (norm) {
-    // RMS statistic of each whole input row (the norm is fused into the GEMV, as a flag).
-    for (int m = wp; m < M; m += 4) {
+    // RMS statistic of each whole input row (the norm is a flag of this GEMV)
+    for (int m = 0; m < M; ++m) {
       float ss = 0.f;
-      for (int k = lane * 8; k < nd.K; k += 256) {
+      for (int k = ct * 8; k < nd.K; k += kCompute * 8) {
         float x[8];
         load8(nd.a, m, k, dt, x);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) ss += x[e] * x[e];
+        for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
       }
       ss = warp_sum(ss);
-      if (lane == 0) s.rstd[m] = rsqrtf(ss / (float)nd.K + nd.eps);
+      if (lane == 0) s.red_small[m][wp] = ss;
     }
+    cw_sync();
+    if (ct < M)
+      s.rstd[ct] = rsqrtf((s.red_small[ct][0] + s.red_small[ct][1] + s.red_small[ct][2] +
+                           s.red_small[ct][3]) / (float)nd.K + nd.eps);
     cw_sync();
   }
-  float acc[8][4];
+  auto stage_x = [&](int k_first, int rows, int stride) {
+    const int nv = rows / 8;
+    for (int v = ct; v < M * nv; v += kCompute) {
+      const int m = v / nv, kk = (v % nv) * 8, k = k_first + kk;
+      float x[8];
+      if (k < kend) {
+        load8(nd.a, m, k, dt, x);
+        if (norm) {
+          float g[8];
+          load8(nd.gamma, 0, k, dt, g);
+          const float r = s.rstd[m];
 #pragma unroll
-  for (int m = 0; m < 8; ++m)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) acc[m][e] = 0.f;
-  const int nk = ring_stages(in);
-  const int kend = in.k0 + in.klen;
-  for (int kb = 0; kb < nk; ++kb) {
-    const int k = in.k0 + kb * kGemvRows + ct;
-#pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      if (m < M) {
-        float x = 0.f;
-        if (k < kend) {
-          x = load1(nd.a, m, k, dt);
-          if (norm) x = x * s.rstd[m] * load1(nd.gamma, 0, k, dt);
+          for (int e = 0; e < 8; ++e) x[e] = x[e] * r * g[e];
         }
-        s.xbuf[m][ct] = x;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = 0.f;
       }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) s.xr[m * stride + kk + e] = x[e];
     }
     cw_sync();
+  };
+  if (staged && nk > 0) stage_x(in.k0, kpad, kpad);
+  const int which = dual ? (ct >> 6) : 0;
+  const int col = dual ? 2 * (ct & 63) : 2 * ct;  // column pair inside this thread's weight
+  float acc[8][2];
+#pragma unroll
+  for (int m = 0; m < 8; ++m) acc[m][0] = acc[m][1] = 0.f;
+  for (int kb = 0; kb < nk; ++kb) {
+    const float* xs;
+    int xstride;
+    if (staged) {
+      xs = s.xr + kb * kGemvRows;
+      xstride = kpad;
+    } else {
+      stage_x(in.k0 + kb * kGemvRows, kGemvRows, kGemvRows);
+      xs = s.xr;
+      xstride = kGemvRows;
+    }
     const int st = (int)(ring % kStages);
     if (!cw_wait(p, smem_u32(&s.full[st]), (ring / kStages) & 1u, 41, idx)) return false;
-    const uint16_t* W = reinterpret_cast<const uint16_t*>(s.stage[st]);
-    const uint16_t* U = W + wcols * kGemvRows;
-#pragma unroll 4
-    for (int r = 0; r < 32; ++r) {
-      const int kk = wp * 32 + r;
-      float f[4];
-      if (!dual) {
-        const uint2 raw = *reinterpret_cast<const uint2*>(W + kk * wcols + lane * 4);
-        f[0] = h2f((uint16_t)(raw.x & 0xffffu), dt);
-        f[1] = h2f((uint16_t)(raw.x >> 16), dt);
-        f[2] = h2f((uint16_t)(raw.y & 0xffffu), dt);
-        f[3] = h2f((uint16_t)(raw.y >> 16), dt);
-      } else {
-        const uint32_t g = *reinterpret_cast<const uint32_t*>(W + kk * wcols + lane * 2);
-        const uint32_t u2 = *reinterpret_cast<const uint32_t*>(U + kk * wcols + lane * 2);
-        f[0] = h2f((uint16_t)(g & 0xffffu), dt);
-        f[1] = h2f((uint16_t)(g >> 16), dt);
-        f[2] = h2f((uint16_t)(u2 & 0xffffu), dt);
-        f[3] = h2f((uint16_t)(u2 >> 16), dt);
-      }
-#pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        if (m < M) {
-          const float xv = s.xbuf[m][kk];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) acc[m][e] = fmaf(xv, f[e], acc[m][e]);
-        }
-      }
-    }
+    // this thread's column pair: box (which * 2 + col / 64), column col % 64 inside it
+    const int box = (dual ? which * 2 : 0) + (col >> 6), lc = col & 63;
+    const uint8_t* B = s.stage[st] + box * 8192 + (lc & 7) * 2;
+    if (dt == DT_BF16)
+      gemv_stage_rows<true>(M, B, lc >> 3, xs, xstride, acc);
+    else
+      gemv_stage_rows<false>(M, B, lc >> 3, xs, xstride, acc);
     cw_sync();
     if (ct == 0) mbar_arrive(smem_u32(&s.empty[st]));
     ++ring;
   }
-  // Cross-warp reduction: thread ct then owns column ct of [gate | up] (or of the tile).
-#pragma unroll
-  for (int m = 0; m < 8; ++m) {
-    if (m < M) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int col = dual ? (e < 2 ? lane * 2 + e : 64 + lane * 2 + (e - 2)) : lane * 4 + e;
-        s.red[wp][m][col] = acc[m][e];
-      }
-    }
-  }
-  cw_sync();
-  float val[8];
-#pragma unroll
-  for (int m = 0; m < 8; ++m)
-    val[m] = (m < M) ? s.red[0][m][ct] + s.red[1][m][ct] + s.red[2][m][ct] + s.red[3][m][ct] : 0.f;
   const int S = in.aux1;
-  const int which = dual ? (ct >> 6) : 0;
-  const int n = in.n0 + (dual ? (ct & 63) : ct);
-  const bool colok = (dual || ct < wcols) && n < nd.N;
+  const int n = in.n0 + col;
+  const bool colok = n < nd.N;  // N is a multiple of 8: both columns are in or both out
   if (S == 1) {
     if (ct == 0) atomicAdd(p.counters + in.sem, 1);  // the semaphore counts every split
   } else {
     float* part = reinterpret_cast<float*>(nd.scratch.ptr);
-    if (colok)
-      for (int m = 0; m < M; ++m)
-        __stcg(part + (size_t)in.aux0 * nd.ldp + ((size_t)which * M + m) * nd.N + n, val[m]);
+    if (colok) {
+#pragma unroll
+      for (int m = 0; m < 8; ++m)
+        if (m < M)
+          __stcg(reinterpret_cast<float2*>(part + (size_t)in.aux0 * nd.ldp +
+                                           ((size_t)which * M + m) * nd.N + n),
+                 make_float2(acc[m][0], acc[m][1]));
+    }
     __threadfence();
     cw_sync();
     if (ct == 0) s.flag = (atomicAdd(p.counters + in.sem, 1) == S - 1);
@@ -620,26 +750,72 @@ __device__ bool gemv(const Params& p, Smem& s, const Instr& in, const Node& nd, 
     }
     __threadfence();
     if (colok) {
-      for (int m = 0; m < M; ++m) {
-        float t = 0.f;
-        for (int q = 0; q < S; ++q)
-          t += __ldcg(part + (size_t)q * nd.ldp + ((size_t)which * M + m) * nd.N + n);
-        val[m] = t;
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        if (m >= M) continue;
+        const float* c0 = part + ((size_t)which * M + m) * nd.N + n;
+        float2 t = make_float2(0.f, 0.f);
+        int q = 0;
+        for (; q + 4 <= S; q += 4) {  // four loads in flight, summed in split order
+          float2 v[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            v[u] = __ldcg(reinterpret_cast<const float2*>(c0 + (size_t)(q + u) * nd.ldp));
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            t.x += v[u].x;
+            t.y += v[u].y;
+          }
+        }
+        for (; q < S; ++q) {
+          const float2 v = __ldcg(reinterpret_cast<const float2*>(c0 + (size_t)q * nd.ldp));
+          t.x += v.x;
+          t.y += v.y;
+        }
+        acc[m][0] = t.x;
+        acc[m][1] = t.y;
       }
     }
   }
-  cw_sync();
+  if (dual) {
+    // gate and up halves of a column pair live in threads t and t + 64: exchange via smem
+    cw_sync();
 #pragma unroll
-  for (int m = 0; m < 8; ++m)
-    if (m < M) s.red[0][m][ct] = val[m];
-  cw_sync();
-  if ((!dual || ct < 64) && colok) {
-    for (int m = 0; m < M; ++m) {
-      float y = dual ? silu(s.red[0][m][ct]) * s.red[0][m][64 + ct] : val[m];
-      if (nd.flags & EPI_BIAS) y += load1(nd.bias, m, n, dt);
-      if (nd.flags & EPI_RELU) y = fmaxf(y, 0.f);
-      if (nd.flags & EPI_RESIDUAL) y += load1(nd.res, m, n, dt);
-      store1(nd.out, m, n, dt, y);
+    for (int m = 0; m < 8; ++m) {
+      if (m < M) {
+        s.xr[m * 256 + which * 128 + col] = acc[m][0];
+        s.xr[m * 256 + which * 128 + col + 1] = acc[m][1];
+      }
+    }
+    cw_sync();
+    if (which == 0) {
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        if (m < M) {
+          acc[m][0] = silu(s.xr[m * 256 + col]) * s.xr[m * 256 + 128 + col];
+          acc[m][1] = silu(s.xr[m * 256 + col + 1]) * s.xr[m * 256 + 128 + col + 1];
+        }
+      }
+    }
+  }
+  if (which == 0 && colok) {
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      if (m >= M) continue;
+      float y0 = acc[m][0], y1 = acc[m][1];
+      if (nd.flags & EPI_BIAS) {
+        y0 += load1(nd.bias, m, n, dt);
+        y1 += load1(nd.bias, m, n + 1, dt);
+      }
+      if (nd.flags & EPI_RELU) {
+        y0 = fmaxf(y0, 0.f);
+        y1 = fmaxf(y1, 0.f);
+      }
+      if (nd.flags & EPI_RESIDUAL) {
+        y0 += load1(nd.res, m, n, dt);
+        y1 += load1(nd.res, m, n + 1, dt);
+      }
+      store2(nd.out, m, n, dt, y0, y1);
     }
   }
   *publish = true;
@@ -693,27 +869,34 @@ __device__ void rmsnorm_body(const Instr& in, const Node& nd) {
   }
 }
 
+// RoPE rows: thread work item = (row, head, 8 consecutive pair indices); both halves of the
+// pairs arrive as 16-byte vectors and leave the same way.
 __device__ void rope_body(const Instr& in, const Node& nd) {
   const int ct = (int)threadIdx.x - (kThreads - kCompute);
   const int rows = min(nd.tile_m, nd.M - in.m0), dt = nd.dtype;
   const int hd = nd.hd, half = hd / 2, nh = nd.hq + nd.hkv;
-  const int pairs = nh * half;
+  const int groups = half / 8;                 // 8-pair groups per head
+  const int items = nh * groups;
   const float l2t = log2f(nd.theta);
-  for (int v = ct; v < rows * pairs; v += kCompute) {
-    const int m = in.m0 + v / pairs, pr = v % pairs;
-    const int h = pr / half, i = pr % half;
-    const float x1 = load1(nd.a, m, h * hd + i, dt), x2 = load1(nd.a, m, h * hd + i + half, dt);
-    const float inv = exp2f(-(2.0f * (float)i / (float)hd) * l2t);
-    float sn, cs;
-    sincosf((float)(nd.pos0 + m) * inv, &sn, &cs);
-    const float y1 = x1 * cs - x2 * sn, y2 = x2 * cs + x1 * sn;
-    if (h < nd.hq) {
-      store1(nd.out, m, h * hd + i, dt, y1);
-      store1(nd.out, m, h * hd + i + half, dt, y2);
-    } else {
-      store1(nd.out_k, m, (h - nd.hq) * hd + i, dt, y1);
-      store1(nd.out_k, m, (h - nd.hq) * hd + i + half, dt, y2);
+  for (int v = ct; v < rows * items; v += kCompute) {
+    const int m = in.m0 + v / items, it = v % items;
+    const int h = it / groups, i0 = (it % groups) * 8;
+    float x1[8], x2[8], y1[8], y2[8];
+    load8(nd.a, m, h * hd + i0, dt, x1);
+    load8(nd.a, m, h * hd + i0 + half, dt, x2);
+    const float pos = (float)(nd.pos0 + m);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float inv = exp2f(-(2.0f * (float)(i0 + e) / (float)hd) * l2t);
+      float sn, cs;
+      sincosf(pos * inv, &sn, &cs);
+      y1[e] = x1[e] * cs - x2[e] * sn;
+      y2[e] = x2[e] * cs + x1[e] * sn;
     }
+    const Operand& o = h < nd.hq ? nd.out : nd.out_k;
+    const int hh = h < nd.hq ? h : h - nd.hq;
+    store8(o, m, hh * hd + i0, dt, y1);
+    store8(o, m, hh * hd + i0 + half, dt, y2);
   }
   if (nd.out_v.ptr) {
     const int nvv = nd.hkv * hd / 8;
@@ -728,13 +911,18 @@ __device__ void rope_body(const Instr& in, const Node& nd) {
 
 // Split-KV partial for kv group g = n0 and keys [k0, k0 + klen): per query head of the group
 // m = max s, l = sum e^{s - m}, o = sum e^{s - m} v   (head_dim 64, up to 128 keys).
-__device__ void attn_partial_body(const Instr& in, const Node& nd) {
+// Keys and values arrive by TMA in one ring stage, 128-byte swizzled (16-byte chunk c of row r
+// sits at chunk c ^ (r & 7)).
+__device__ bool attn_partial_body(const Params& p, Smem& s, const Instr& in, const Node& nd,
+                                  uint32_t& ring, int idx) {
   const int ct = (int)threadIdx.x - (kThreads - kCompute);
   const int wp = ct >> 5, lane = ct & 31;
   const int g = in.n0, G = nd.hq / nd.hkv, C = in.aux1, c = in.aux0;
-  const int k0 = in.k0, kl = in.klen;
-  const __nv_bfloat16* K = reinterpret_cast<const __nv_bfloat16*>(nd.b.ptr);
-  const __nv_bfloat16* V = reinterpret_cast<const __nv_bfloat16*>(nd.b2.ptr);
+  const int kl = in.klen;
+  const int st = (int)(ring % kStages);
+  if (!cw_wait(p, smem_u32(&s.full[st]), (ring / kStages) & 1u, 42, idx)) return false;
+  const uint8_t* Ks = s.stage[st];
+  const uint8_t* Vs = s.stage[st] + 16384;
   for (int hh = wp; hh < G; hh += 4) {
     const int h = g * G + hh;
     float qv[64];
@@ -747,12 +935,12 @@ __device__ void attn_partial_body(const Instr& in, const Node& nd) {
       const int j = lane + 32 * t;
       float sv = -INFINITY;
       if (j < kl) {
-        const uint4* kr = reinterpret_cast<const uint4*>(K + (size_t)(k0 + j) * nd.b.ld + g * 64);
         float dot = 0.f;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           float kx[8];
-          unpack8(__ldcg(kr + i), DT_BF16, kx);
+          unpack8(*reinterpret_cast<const uint4*>(Ks + j * 128 + ((i ^ (j & 7)) << 4)), DT_BF16,
+                  kx);
 #pragma unroll
           for (int e = 0; e < 8; ++e) dot = fmaf(qv[i * 8 + e], kx[e], dot);
         }
@@ -769,30 +957,40 @@ __device__ void attn_partial_body(const Instr& in, const Node& nd) {
       l += pr[t];
     }
     l = warp_sum(l);
+    // lane owns value columns 2*lane, 2*lane+1: 16-byte chunk lane/4, 4-byte word lane%4
     float o0 = 0.f, o1 = 0.f;
+    const int chunk = lane >> 2, word = lane & 3;
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
+      if (32 * t >= kl) continue;
+#pragma unroll 8
       for (int jj = 0; jj < 32; ++jj) {
         const int j = t * 32 + jj;
-        if (j >= kl) break;
         const float pj = __shfl_sync(FULL, pr[t], jj);
-        const uint32_t vv = __ldcg(reinterpret_cast<const unsigned int*>(
-            V + (size_t)(k0 + j) * nd.b2.ld + g * 64 + lane * 2));
-        o0 = fmaf(pj, __uint_as_float(vv << 16), o0);
-        o1 = fmaf(pj, __uint_as_float(vv & 0xffff0000u), o1);
+        if (j < kl) {
+          const uint32_t vv = *reinterpret_cast<const uint32_t*>(
+              Vs + j * 128 + ((chunk ^ (j & 7)) << 4) + word * 4);
+          o0 = fmaf(pj, __uint_as_float(vv << 16), o0);
+          o1 = fmaf(pj, __uint_as_float(vv & 0xffff0000u), o1);
+        }
       }
     }
-    float* row = reinterpret_cast<float*>(nd.scratch.ptr) + ((size_t)(g * C + c) * G + hh) * nd.scratch.ld;
+    float* row = reinterpret_cast<float*>(nd.scratch.ptr) +
+                 ((size_t)(g * C + c) * G + hh) * nd.scratch.ld;
     __stcg(reinterpret_cast<float2*>(row + lane * 2), make_float2(o0, o1));
     if (lane == 0) {
       __stcg(row + 64, mx);
       __stcg(row + 65, l);
     }
   }
+  cw_sync();
+  if (ct == 0) mbar_arrive(smem_u32(&s.empty[st]));
+  ++ring;
+  return true;
 }
 
 // LSE merge of one kv group's partials: M = max m_c, L = sum l_c e^{m_c-M},
-// O = sum o_c e^{m_c-M} / L.
+// O = sum o_c e^{m_c-M} / L. Lanes hold chunks' statistics; value loads are batched by 8.
 __device__ void attn_reduce_body(const Instr& in, const Node& nd) {
   const int ct = (int)threadIdx.x - (kThreads - kCompute);
   const int wp = ct >> 5, lane = ct & 31;
@@ -801,20 +999,35 @@ __device__ void attn_reduce_body(const Instr& in, const Node& nd) {
   const int ld = nd.scratch.ld;
   for (int hh = wp; hh < G; hh += 4) {
     const int h = g * G + hh;
+    auto row = [&](int c) { return sc + ((size_t)(g * C + c) * G + hh) * ld; };
     float mx = -INFINITY;
-    for (int c = lane; c < C; c += 32) mx = fmaxf(mx, __ldcg(sc + ((size_t)(g * C + c) * G + hh) * ld + 64));
+    for (int c = lane; c < C; c += 32) mx = fmaxf(mx, __ldcg(row(c) + 64));
     mx = warp_max(mx);
-    float L = 0.f, o0 = 0.f, o1 = 0.f;
-    for (int c = 0; c < C; ++c) {
-      const float* row = sc + ((size_t)(g * C + c) * G + hh) * ld;
-      const float w = expf(__ldcg(row + 64) - mx);
-      L += __ldcg(row + 65) * w;
-      const float2 o = __ldcg(reinterpret_cast<const float2*>(row + lane * 2));
-      o0 = fmaf(o.x, w, o0);
-      o1 = fmaf(o.y, w, o1);
+    float L = 0.f;
+    for (int c = lane; c < C; c += 32) L += __ldcg(row(c) + 65) * expf(__ldcg(row(c) + 64) - mx);
+    L = warp_sum(L);
+    float o0 = 0.f, o1 = 0.f;
+    for (int c0 = 0; c0 < C; c0 += 8) {
+      float2 ov[8];
+      float mv[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (c0 + u < C) {
+          ov[u] = __ldcg(reinterpret_cast<const float2*>(row(c0 + u) + lane * 2));
+          mv[u] = __ldcg(row(c0 + u) + 64);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (c0 + u < C) {
+          const float w = expf(mv[u] - mx);
+          o0 = fmaf(ov[u].x, w, o0);
+          o1 = fmaf(ov[u].y, w, o1);
+        }
+      }
     }
     const float inv = 1.0f / L;
-    __nv_bfloat162 y = __floats2bfloat162_rn(o0 * inv, o1 * inv);
+    const __nv_bfloat162 y = __floats2bfloat162_rn(o0 * inv, o1 * inv);
     *reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(nd.out.ptr) + h * 64 +
                                        lane * 2) = y;
   }
@@ -831,6 +1044,7 @@ __device__ void run_compute(const Params& p, Smem& s, uint32_t tmem) {
     const Instr& in = slot_instr(s, slot);
     if (in.op == OP_END) break;
     const Node& nd = slot_node(s, slot);
+    if (p.trace && ct == 0) p.trace[(size_t)idx * kTraceWords + 0] = globaltimer();
     bool ok = true, publish = true;
     switch (in.op) {
       case OP_GEMM:
@@ -842,13 +1056,18 @@ __device__ void run_compute(const Params& p, Smem& s, uint32_t tmem) {
         break;
       case OP_NOOP:
         break;
+      case OP_ATTN_PARTIAL:
+        ok = cw_wait(p, smem_u32(&s.deps_ready[slot]), use & 1u, 33, idx);
+        trace_mark(p, idx, 2);
+        ok = ok && attn_partial_body(p, s, in, nd, ring, idx);
+        break;
       default:
         ok = cw_wait(p, smem_u32(&s.deps_ready[slot]), use & 1u, 33, idx);
         if (!ok) break;
+        trace_mark(p, idx, 2);
         if (in.op == OP_EW) ew_body(in, nd);
         else if (in.op == OP_RMSNORM) rmsnorm_body(in, nd);
         else if (in.op == OP_ROPE) rope_body(in, nd);
-        else if (in.op == OP_ATTN_PARTIAL) attn_partial_body(in, nd);
         else if (in.op == OP_ATTN_REDUCE) attn_reduce_body(in, nd);
         else {
           if (ct == 0) report(p, MK_ERR_DEVICE_CHECK, idx, -1, in.op, 0, R_COMPUTE, 34);
@@ -857,6 +1076,7 @@ __device__ void run_compute(const Params& p, Smem& s, uint32_t tmem) {
         break;
     }
     if (!ok) break;
+    trace_mark(p, idx, 3);
     // Publish: every thread's stores are ordered before the release increments.
     __threadfence();
     cw_sync();
@@ -865,6 +1085,10 @@ __device__ void run_compute(const Params& p, Smem& s, uint32_t tmem) {
         fence_proxy_async_global();
         for (int j = 0; j < in.n_dst; ++j)
           red_release_add(p.counters + __ldg(p.dst_list + in.dst_off + j), 1);
+      }
+      if (p.trace) {
+        p.trace[(size_t)idx * kTraceWords + 4] = globaltimer();
+        p.trace[(size_t)idx * kTraceWords + 5] = blockIdx.x;
       }
       mbar_arrive(smem_u32(&s.slot_free[slot]));
     }

@@ -28,7 +28,7 @@ namespace {
 // Fixed layout of the scratch array (bytes). Every GPU that loads the library holds the whole
 // array until the process exits.
 constexpr size_t kScratchBytes = 4u << 20;                              // 4 MiB
-constexpr int kMaxTiles = 1024;                                         // N <= 131072
+constexpr int kMaxTiles = 1024;                                         // N <= 262144
 constexpr int kMaxInstr = 1024;                                         // tiles x splits
 constexpr size_t kOffInstr = 0;
 constexpr size_t kOffNode = kOffInstr + (size_t)kMaxInstr * sizeof(Instr);
@@ -40,8 +40,8 @@ constexpr size_t kPartFloats = (kScratchBytes - kOffPart) / 4;          // split
 static_assert(kOffMap % 64 == 0, "tensor map alignment");
 static_assert(kOffPart < kScratchBytes, "layout fits");
 
-constexpr int kTileN = 128;     // output columns per GEMV tile
-constexpr int kKStep = 128;     // K chunks are multiples of this
+constexpr int kTileN = 256;     // output columns per GEMV tile
+constexpr int kKStep = kGemvRows;  // K chunks are multiples of the stage depth
 
 // Host staging for the records copied into the array on every call (no heap use).
 Instr h_instr[kMaxInstr];
@@ -153,12 +153,12 @@ extern "C" mk_status mk_gemv_noalloc(const void* x, const void* w, void* out, in
     auto encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fnp);
     cuuint64_t dims[2] = {(cuuint64_t)n, (cuuint64_t)k};
     cuuint64_t strides[1] = {(cuuint64_t)n * 2};
-    cuuint32_t box[2] = {(cuuint32_t)kTileN, (cuuint32_t)kGemvRows};
+    cuuint32_t box[2] = {64u, (cuuint32_t)kGemvRows};  // four 64-column boxes per stage
     cuuint32_t estr[2] = {1, 1};
     CUresult r = encode(&h_map, dtype == MK_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                  : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                         2, const_cast<void*>(w), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(MK_ERR_CUDA, "cuTensorMapEncodeTiled failed");
   }

@@ -62,6 +62,13 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint
       "l"((uint64_t)tmap), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
+// Fetch a tile into L2 only (no shared-memory destination, no completion signal).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   (uint64_t)tmap),
+               "r"(x), "r"(y)
+               : "memory");
+}
 __device__ __forceinline__ void tensormap_acquire(const void* tmap) {
   asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"((uint64_t)tmap)
                : "memory");

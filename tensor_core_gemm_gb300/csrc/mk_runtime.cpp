@@ -113,13 +113,13 @@ mk_status check_kernel_support(const std::vector<TensorRec>& ts, const std::vect
     set_error("mk_compile: gemm_tile_n must be 64, 128 or 256");
     return MK_ERR_UNSUPPORTED;
   }
-  if (o.gemv_tile_n != 128 || o.gemv_kstep % kGemvRows || o.gemv_max_m > 8 || o.gemv_max_m < 0) {
-    set_error("mk_compile: the kernel runs 128-column GEMV tiles, K chunks a multiple of %d, "
-              "M <= 8", kGemvRows);
+  if (o.gemv_tile_n != 256 || o.gemv_kstep % kGemvRows || o.gemv_max_m > 8 || o.gemv_max_m < 0) {
+    set_error("mk_compile: the kernel runs 256-column GEMV tiles (128 with SILU_MUL), K chunks a "
+              "multiple of %d, M <= 8", kGemvRows);
     return MK_ERR_UNSUPPORTED;
   }
-  if (o.attn_chunk > kAttnChunkMax) {
-    set_error("mk_compile: attn_chunk must be <= %d", kAttnChunkMax);
+  if (o.attn_chunk > kAttnChunkMax || o.attn_chunk % 8) {
+    set_error("mk_compile: attn_chunk must be a multiple of 8, at most %d", kAttnChunkMax);
     return MK_ERR_UNSUPPORTED;
   }
   for (size_t i = 0; i < nodes.size(); ++i) {
@@ -150,6 +150,10 @@ mk_status check_kernel_support(const std::vector<TensorRec>& ts, const std::vect
                   "use an RMSNORM node before a GEMM");
         return MK_ERR_UNSUPPORTED;
       }
+    }
+    if (nd.kind == NK_ROPE && nd.hd % 16) {
+      set_error("mk_compile: ROPE runs head_dim a multiple of 16");
+      return MK_ERR_UNSUPPORTED;
     }
     if (nd.kind == NK_ATTN) {
       if (nd.hd != 64) {
@@ -294,9 +298,10 @@ static mk_status build_nodes(const mk_graph* g, mk_plan* p, std::vector<CUtensor
             if (nd.b2 >= 0 && (st = add_map(keys, maps, ts[nd.b2], 64, kGemmBK, true, &n.b2.tmap)))
               return st;
           } else {
-            if ((st = add_map(keys, maps, B, n.tile_n, kGemvRows, false, &n.b.tmap))) return st;
+            // 64 x 64 boxes, 128-byte swizzle (four per 32 KB stage)
+            if ((st = add_map(keys, maps, B, 64, kGemvRows, true, &n.b.tmap))) return st;
             if (nd.b2 >= 0 &&
-                (st = add_map(keys, maps, ts[nd.b2], n.tile_n, kGemvRows, false, &n.b2.tmap)))
+                (st = add_map(keys, maps, ts[nd.b2], 64, kGemvRows, true, &n.b2.tmap)))
               return st;
           }
         }
@@ -339,6 +344,13 @@ static mk_status build_nodes(const mk_graph* g, mk_plan* p, std::vector<CUtensor
         n.b2 = operand(ts, nd.b2);
         n.scale = nd.scale != 0.f ? nd.scale : 1.0f / sqrtf((float)nd.hd);
         if (p->hp.node_scratch[i] >= 0) n.scratch.ld = (int)ts[p->hp.node_scratch[i]].ld;
+        if (n.M == 1) {
+          // key / value chunks stream by TMA: one head (64 columns) x attn_chunk rows
+          n.tile_m = p->opts.attn_chunk;
+          mk_status st;
+          if ((st = add_map(keys, maps, ts[nd.b], 64, n.tile_m, true, &n.b.tmap))) return st;
+          if ((st = add_map(keys, maps, ts[nd.b2], 64, n.tile_m, true, &n.b2.tmap))) return st;
+        }
         break;
     }
   }
@@ -450,7 +462,9 @@ extern "C" mk_status mk_compile(mk_graph_t g, const mk_compile_opts* opts_in, mk
   const size_t off_status = align(off_ctr + n_ctr * 4);
   const size_t off_last = off_status + kStatusWords * 4;  // last_status, then `done`
   const size_t off_snap = align(off_last + (kStatusWords + 1) * 4);
-  const size_t off_maps = align(off_snap + (o.snapshot_counters ? n_ctr * 4 : 0));
+  const size_t off_trace = align(off_snap + (o.snapshot_counters ? n_ctr * 4 : 0));
+  const size_t trace_bytes = o.trace ? p->hp.instrs.size() * kTraceWords * sizeof(uint64_t) : 0;
+  const size_t off_maps = align(off_trace + trace_bytes);
   const size_t off_scratch = align(off_maps + kMaxTmaps * sizeof(CUtensorMap));
   const size_t total = off_scratch + scratch;
   if (cudaMalloc((void**)&p->d_mem, total) != cudaSuccess) {
@@ -495,11 +509,13 @@ extern "C" mk_status mk_compile(mk_graph_t g, const mk_compile_opts* opts_in, mk
   pr.last_status = (int32_t*)(p->d_mem + off_last);
   pr.done = pr.last_status + kStatusWords;
   pr.snapshot = o.snapshot_counters ? (int32_t*)(p->d_mem + off_snap) : nullptr;
+  pr.trace = o.trace ? (uint64_t*)(p->d_mem + off_trace) : nullptr;
   pr.tmaps = (const void*)(p->d_mem + off_maps);
   pr.n_instr = (int32_t)p->hp.instrs.size();
   pr.n_sm = o.n_sm;
   pr.n_tmaps = (int32_t)maps.size();
   pr.n_counters = (int32_t)n_ctr;
+  pr.l2_prefetch = std::min(std::max(o.l2_prefetch, 0), kSlots);
   pr.timeout_ns = (uint64_t)(o.timeout_ms > 0 ? o.timeout_ms : 2000) * 1000000ull;
   p->grid = o.n_sm;
   p->on_device = true;
@@ -637,6 +653,21 @@ extern "C" mk_status mk_get_counter_targets(mk_plan_t p, int32_t* buf, size_t n)
     return MK_ERR_INVALID_ARG;
   }
   if (p->hp.n_dep) memcpy(buf, p->hp.targets.data(), (size_t)p->hp.n_dep * 4);
+  return MK_OK;
+}
+
+extern "C" mk_status mk_get_trace(mk_plan_t p, uint64_t* buf, size_t n) {
+  if (!p || !p->on_device || !p->params.trace) {
+    set_error("mk_get_trace: NULL plan, dry-run plan, or compiled without trace");
+    return MK_ERR_INVALID_ARG;
+  }
+  const size_t need = p->hp.instrs.size() * kTraceWords;
+  if ((!buf && need) || n < need) {
+    set_error("mk_get_trace: buffer smaller than 6 * n_instr");
+    return MK_ERR_INVALID_ARG;
+  }
+  CUDA_TRY(cudaDeviceSynchronize());
+  if (need) CUDA_TRY(cudaMemcpy(buf, p->params.trace, need * 8, cudaMemcpyDeviceToHost));
   return MK_OK;
 }
 

@@ -101,16 +101,20 @@ struct Params {
   int32_t* done;            // CTAs finished in this run (the last one resets the run state)
   int32_t* last_status;     // status of the last completed run (read by the host)
   int32_t* snapshot;        // copy of the counters at the end of a run, or null
+  uint64_t* trace;          // per instruction kTraceWords timestamps (see mk_get_trace), or null
   int32_t n_instr;
   int32_t n_sm;             // placement stride
   int32_t n_tmaps;
   int32_t n_counters;       // dependency counters + split semaphores
+  int32_t l2_prefetch;      // instructions ahead whose streamed operands are prefetched to L2
+  int32_t pad1;
   uint64_t timeout_ns;
 };
 
 // Device status record (mirrors mk_device_status).
 enum : int32_t { ST_CODE = 0, ST_INSTR, ST_COUNTER, ST_OBSERVED, ST_EXPECTED, ST_SM, ST_ROLE, ST_WHERE };
 constexpr int kStatusWords = 8;
+constexpr int kTraceWords = 6;
 
 // Kernel geometry shared with the host (launch configuration and shared-memory budget).
 constexpr int kThreads = 256;          // 8 warps: scheduler, loader, MMA, spare, 4 compute
@@ -120,7 +124,7 @@ constexpr int kSlots = 8;              // instruction slots (scheduler lookahead
 constexpr int kSlotBytes = 64 + 256;   // Instr + Node
 constexpr int kGemmTileM = 128;
 constexpr int kGemmBK = 64;            // K per stage for GEMM (128-byte rows of 16-bit elements)
-constexpr int kGemvRows = 128;         // K rows per stage for GEMV
+constexpr int kGemvRows = 64;          // K rows per stage for GEMV (x 256 columns = 32 KB)
 constexpr int kAttnChunkMax = 128;     // keys per split-KV partial handled by one instruction
 
 }  // namespace mk

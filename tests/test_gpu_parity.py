@@ -384,3 +384,18 @@ def test_wait_limit_reports_timeout_without_hanging():
     ok = workloads.gemm(128, 64, 64, device=DEV)
     run(ok, gemm_tile_n=64)
     assert_close(f32(ok.data[2]), ops.matmul(f32(ok.data[0]), f32(ok.data[1]), F16), "after")
+
+
+def test_trace_timestamps_are_ordered():
+    wl = workloads.mlp3(m=256, h=256, layers=2, device=DEV)
+    g, _ = workloads.build_graph(wl.desc, wl.data)
+    p = g.compile(trace=1, gemm_tile_n=64)
+    p.run()
+    p.check_status()
+    tr = p.trace().astype(np.int64)
+    ins = p.instructions()
+    real = ins["op"] != 0
+    assert np.all(tr[real, 0] > 0) and np.all(tr[real, 1] > 0)
+    assert np.all(tr[real, 2] >= tr[real, 1]) and np.all(tr[real, 3] >= tr[real, 2])
+    assert np.all(tr[real, 4] >= tr[real, 3]) and np.all(tr[real, 3] >= tr[real, 0])
+    assert np.all(tr[real, 5] == np.arange(len(ins))[real] % p.stats()["n_sm"])

@@ -59,7 +59,7 @@ def test_noalloc_rejects_sizes_beyond_its_fixed_scratch():
     w = torch.zeros((64, 8), dtype=torch.bfloat16, device="cuda:0")
     o = torch.zeros((1, 8), dtype=torch.bfloat16, device="cuda:0")
     p = [C.c_void_p(t.data_ptr()) for t in (x, w, o)]
-    rc = lib.mk_gemv_noalloc(*p, 1, 131072 + 8, 64, _lib.MK_BF16, None, None)
+    rc = lib.mk_gemv_noalloc(*p, 1, 262144 + 8, 64, _lib.MK_BF16, None, None)
     assert rc == _lib.MK_ERR_UNSUPPORTED and b"maximum" in lib.mk_last_error()
     rc = lib.mk_gemv_noalloc(*p, 9, 8, 64, _lib.MK_BF16, None, None)
     assert rc == _lib.MK_ERR_UNSUPPORTED
