@@ -290,6 +290,8 @@ def main():
     ap.add_argument("--impl", default="mk", choices=["mk", "reference"])
     ap.add_argument("--config", default="gemm4096", choices=sorted(CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--opt", action="append", default=[], metavar="KEY=INT",
+                    help="override a compile option of the workload, e.g. --opt cluster=2")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -316,6 +318,9 @@ def main():
 
     _lib.load()
     wl, opts = make_workload(args.config, dev)
+    for kv in args.opt:
+        k, v = kv.split("=", 1)
+        opts[k] = int(v)
     g, id_of = W.build_graph(wl.desc, wl.data)
     plan = g.compile(**opts)
     stream = torch.cuda.current_stream()
@@ -410,7 +415,8 @@ def main():
                        "l2": "flushed before every timed run (256 MB device write)",
                        "parallelism": "replicas" if world > 1 else "single GPU",
                        "instructions": plan.stats()["n_instr"],
-                       "waves_per_sm": round(plan.stats()["waves"], 3)},
+                       "waves_per_sm": round(plan.stats()["waves"], 3),
+                       "compile_opts": opts},
             "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": runit,
                          "frac": achieved / peak, "traffic": traffic,
                          "peak_source": f"{peak_src} ({'bf16_tflops' if bound == 'tensor' else 'hbm_gbs'})"},

@@ -34,14 +34,15 @@ constexpr int kBarCompute = 1;  // named barrier of the compute warpgroup
 constexpr int kXrFloats = 5120; // GEMV activation staging (M x chunk), reused for its epilogue
 
 struct __align__(1024) Smem {
-  uint8_t stage[kStages][kStageBytes];  // operand ring (1024-byte aligned: 128-byte swizzle)
+  uint8_t ring[kRingBytes];             // operand ring (stages 1024-byte aligned: 128-byte swizzle)
   float xr[kXrFloats];                  // GEMV activations, then its output exchange
   float red_small[8][4];                // per-row, per-warp partial sums
   uint8_t slot[kSlots][kSlotBytes];     // instruction record + node entry per slot
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
+  uint64_t go;                          // pair mode, odd CTA: released by the even CTA once per GEMM
   uint64_t instr_ready[kSlots];
   uint64_t deps_ready[kSlots];
   uint64_t slot_free[kSlots];
@@ -64,6 +65,41 @@ __device__ __forceinline__ const Node& slot_node(const Smem& s, int slot) {
 }
 __device__ __forceinline__ const void* tmap_at(const Params& p, int i) {
   return static_cast<const char*>(p.tmaps) + (size_t)i * 128;
+}
+// Ring geometry of this launch: 4 stages of 48 KB, or 6 of 32 KB when GEMM tiles run on CTA pairs
+// (every other ring user, a GEMV weight tile or an attention key/value chunk, fits in 32 KB).
+__device__ __forceinline__ uint32_t ring_n(const Params& p) { return (uint32_t)p.stages; }
+__device__ __forceinline__ uint32_t stage_bytes(const Params& p) {
+  return p.stages == kPairStages ? 32768u : 49152u;
+}
+__device__ __forceinline__ uint8_t* stage_ptr(Smem& s, const Params& p, int st) {
+  return s.ring + (size_t)st * stage_bytes(p);
+}
+// Position in the operand ring: stage index and the parity of the current pass over the ring
+// (use count / depth, mod 2), advanced incrementally so hot loops do no division.
+struct RingPos {
+  uint32_t st = 0, ph = 0;
+  __device__ __forceinline__ void next(uint32_t ns) {
+    if (++st == ns) {
+      st = 0;
+      ph ^= 1u;
+    }
+  }
+  __device__ __forceinline__ void advance(uint32_t n, uint32_t ns) {
+    const uint32_t t = st + n;
+    st = t % ns;
+    ph ^= (t / ns) & 1u;
+  }
+  __device__ __forceinline__ void align() {  // to the start of the next pass
+    if (st) {
+      st = 0;
+      ph ^= 1u;
+    }
+  }
+};
+// A plain use count rounded up to the start of the next pass (the compute warpgroup's count).
+__device__ __forceinline__ uint32_t ring_align(uint32_t v, uint32_t ns) {
+  return (v + ns - 1) / ns * ns;
 }
 __device__ __forceinline__ int ring_stages(const Instr& in) {
   if (in.op == OP_GEMM) return (in.klen + kGemmBK - 1) / kGemmBK;
@@ -93,12 +129,13 @@ __device__ void report(const Params& p, int code, int instr, int counter, int ob
 // On-chip waits get four times the counter-wait limit: when a dependency never completes, the
 // scheduler's counter wait runs out first and the report names the counter.
 __device__ bool wait_mbar(const Params& p, uint32_t bar, uint32_t parity, int role, int where,
-                          int instr) {
-  if (mbar_try(bar, parity)) return true;
+                          int instr, bool cluster_scope = false) {
+  auto probe = [&]() { return cluster_scope ? mbar_try_cluster(bar, parity) : mbar_try(bar, parity); };
+  if (probe()) return true;
   const uint64_t t0 = globaltimer();
   const uint64_t limit = 4 * p.timeout_ns;
   for (uint32_t n = 1;; ++n) {
-    if (mbar_try(bar, parity)) return true;
+    if (probe()) return true;
     if ((n & 15u) == 0) {
       if (ld_volatile(p.status + ST_CODE) != 0) return false;
       if (globaltimer() - t0 > limit) {
@@ -107,6 +144,37 @@ __device__ bool wait_mbar(const Params& p, uint32_t bar, uint32_t parity, int ro
       }
     }
   }
+}
+// Warp-converged variant for roles run by a whole warp: every lane polls the same barrier and
+// all lanes leave together (lane 0's view of the limit decides), so the code after it stays
+// converged and its values warp-uniform.
+__device__ __noinline__ bool wait_warp_slow(const Params& p, uint32_t bar, uint32_t parity,
+                                            int role, int where, int instr, bool cluster_scope) {
+  const uint64_t t0 = globaltimer();
+  const uint64_t limit = 4 * p.timeout_ns;
+  for (uint32_t n = 1;; ++n) {
+    const bool done = cluster_scope ? mbar_try_cluster(bar, parity) : mbar_try(bar, parity);
+    if (__all_sync(FULL, done)) return true;
+    if ((n & 15u) == 0) {
+      int stop = 0;
+      if ((threadIdx.x & 31) == 0) {
+        if (ld_volatile(p.status + ST_CODE) != 0) stop = 1;
+        else if (globaltimer() - t0 > limit) stop = 2;
+      }
+      stop = __shfl_sync(FULL, stop, 0);
+      if (stop) {
+        if (stop == 2 && (threadIdx.x & 31) == 0)
+          report(p, MK_ERR_TIMEOUT, instr, -1, 0, (int)parity, role, where);
+        return false;
+      }
+    }
+  }
+}
+__device__ __forceinline__ bool wait_warp(const Params& p, uint32_t bar, uint32_t parity, int role,
+                                          int where, int instr, bool cluster_scope = false) {
+  const bool done = cluster_scope ? mbar_try_cluster(bar, parity) : mbar_try(bar, parity);
+  if (__all_sync(FULL, done)) return true;
+  return wait_warp_slow(p, bar, parity, role, where, instr, cluster_scope);
 }
 // Wait used while draining after an abort: ignores the status word, short fixed limit.
 __device__ void wait_mbar_drain(uint32_t bar, uint32_t parity) {
@@ -273,53 +341,145 @@ __device__ void run_scheduler(const Params& p, Smem& s) {
   }
 }
 
-// ------------------------------------------------------------------ TMA loader (one thread)
+// ------------------------------------------------------------------ TMA loader (one warp)
 
+// The loader runs on a whole warp, converged: every lane polls the barriers, ring positions and
+// coordinates are warp-uniform, and one elected lane issues each barrier operation and copy.
+// The issuing thread's own latency bounds how fast stages are refilled, so the per-stage work is
+// one or two copies and a few uniform integer operations.
+
+// `panels` 64-column panels of B (64 rows each, 8 KB atoms in the 128-byte swizzled layout) from
+// column `col`, row `k`, into consecutive atoms at `dst`. A panel map (3D: column within the
+// panel, row, panel) moves them in one copy; a plain 2D map takes one copy per panel. PC: the
+// copy counts on the even CTA's barrier of a CTA pair.
+template <bool PC>
+__device__ __forceinline__ void load_panels(uint32_t dst, const void* map, bool panel_map,
+                                            uint32_t bar, int col, int k, int panels) {
+  if (panel_map) {
+    if (PC)
+      tma_load_3d_pair(dst, map, bar, 0, k, col >> 6);
+    else
+      tma_load_3d(dst, map, bar, 0, k, col >> 6);
+  } else {
+    for (int j = 0; j < panels; ++j) {
+      if (PC)
+        tma_load_2d_pair(dst + j * 8192, map, bar, col + 64 * j, k);
+      else
+        tma_load_2d(dst + j * 8192, map, bar, col + 64 * j, k);
+    }
+  }
+}
+
+// Ring alignment of pair mode: the two CTAs of a pair have consumed different numbers of stages
+// (their other instructions differ), but one MMA reads both CTAs' shared memory at the same
+// offsets. Before every pair GEMM both CTAs therefore move to the start of the next pass over the
+// ring; each skipped stage is waited free, then both of its barriers are arrived on so their
+// phase counts stay equal to the use count every role tracks.
+template <bool PAIR>
 __device__ bool load_gemm(const Params& p, Smem& s, const Instr& in, const Node& nd, int slot,
-                          uint32_t use, uint32_t& fill, int idx) {
+                          uint32_t use, RingPos& rp, uint32_t& nfill, uint32_t& go_par, int idx) {
+  const uint32_t NS = ring_n(p);
+  if (PAIR) {
+    while (rp.st != 0) {
+      if (!wait_warp(p, smem_u32(&s.empty[rp.st]), rp.ph ^ 1u, R_LOAD, 18, idx)) return false;
+      if (elect_one()) {
+        mbar_arrive(smem_u32(&s.full[rp.st]));
+        mbar_arrive(smem_u32(&s.empty[rp.st]));
+      }
+      __syncwarp();
+      rp.next(NS);
+      ++nfill;
+    }
+  }
   const int nk = ring_stages(in);
   if (nk == 0) return true;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  if (PAIR) {
+    // Between pair GEMMs the two CTAs use their rings for different instructions, so the odd
+    // CTA's bytes must not reach the even CTA's full barriers while one of them still carries
+    // an earlier load. The even CTA waits until the stages of the first pass are free (every
+    // earlier use of them consumed), then releases the odd CTA once per GEMM. Later stages need
+    // no handshake: the odd CTA reuses a stage only after the pair MMA that read it committed,
+    // which is after the even CTA's barrier for it completed. Bytes that land before the even
+    // CTA's expect_tx leave the transaction count negative until it arrives.
+    const int first = nk < (int)NS ? nk : (int)NS;
+    if (rank == 0) {
+      for (int j = 0; j < first; ++j)
+        if (!wait_warp(p, smem_u32(&s.empty[j]), rp.ph ^ 1u, R_LOAD, 17, idx)) return false;
+      if (elect_one()) mbar_arrive_cluster(mapa_shared(smem_u32(&s.go), 1));
+      __syncwarp();
+    } else {
+      if (!wait_warp(p, smem_u32(&s.go), go_par & 1u, R_LOAD, 19, idx, true)) return false;
+      go_par ^= 1u;
+    }
+  }
   const bool dual = (nd.flags & EPI_SILU_MUL) != 0;
-  const int tn = nd.tile_n, nbox = tn / 64;
-  const uint32_t bytes = (uint32_t)(kGemmTileM * kGemmBK * 2 + (dual ? 2 : 1) * tn * kGemmBK * 2);
+  const bool panel = (nd.flags & NF_B_PANELS) != 0;
+  const int tn = nd.tile_n;
+  const int ncol = PAIR ? tn / 2 : tn;  // B columns this CTA loads per weight
+  const int nbox = ncol / 64;
+  const uint32_t own = (uint32_t)(kGemmTileM * kGemmBK * 2 + (dual ? 2 : 1) * ncol * kGemmBK * 2);
+  const int arow = in.m0 + (int)rank * kGemmTileM;
+  const int bcol = in.n0 + (int)rank * ncol;
   const void* ta = tmap_at(p, nd.a.tmap);
   const void* tb = tmap_at(p, nd.b.tmap);
   const void* tb2 = dual ? tmap_at(p, nd.b2.tmap) : nullptr;
-  auto load_b = [&](int st, int kb) {
-    const uint32_t base = smem_u32(s.stage[st]) + kGemmTileM * kGemmBK * 2;
-    const uint32_t bar = smem_u32(&s.full[st]);
-    for (int j = 0; j < nbox; ++j)
-      tma_load_2d(base + j * 8192, tb, bar, in.n0 + j * 64, in.k0 + kb * kGemmBK);
-    if (dual)
-      for (int j = 0; j < nbox; ++j)
-        tma_load_2d(base + (nbox + j) * 8192, tb2, bar, in.n0 + j * 64, in.k0 + kb * kGemmBK);
+  const uint32_t ring0 = smem_u32(s.ring), sb = stage_bytes(p);
+  // bytes of both CTAs of a pair complete on the even CTA's full barrier
+  const uint32_t fb0 = PAIR ? mapa_shared(smem_u32(&s.full[0]), 0) : smem_u32(&s.full[0]);
+  // Arm stage st for this k-step: the even CTA of a pair expects both CTAs' bytes.
+  auto arm = [&](uint32_t st) {
+    if (!PAIR || rank == 0)
+      mbar_expect_tx(smem_u32(&s.full[st]), PAIR ? 2 * own : own);
+    else
+      mbar_arrive(smem_u32(&s.full[st]));  // keeps this CTA's phase count in step
   };
-  auto load_a = [&](int st, int kb) {
-    tma_load_2d(smem_u32(s.stage[st]), ta, smem_u32(&s.full[st]), in.k0 + kb * kGemmBK, in.m0);
+  auto issue_b = [&](uint32_t st, int kb) {
+    const uint32_t dst = ring0 + st * sb + kGemmTileM * kGemmBK * 2;
+    const int k = in.k0 + kb * kGemmBK;
+    load_panels<PAIR>(dst, tb, panel, fb0 + st * 8u, bcol, k, nbox);
+    if (dual) load_panels<PAIR>(dst + nbox * 8192, tb2, panel, fb0 + st * 8u, bcol, k, nbox);
+  };
+  auto issue_a = [&](uint32_t st, int kb) {
+    if (PAIR)
+      tma_load_2d_pair(ring0 + st * sb, ta, fb0 + st * 8u, in.k0 + kb * kGemmBK, arow);
+    else
+      tma_load_2d(ring0 + st * sb, ta, fb0 + st * 8u, in.k0 + kb * kGemmBK, arow);
   };
   // Weights first: they depend on nothing inside the graph, so they stream into free stages
   // while the activations are still being produced elsewhere.
-  const int npre = (in.flags & IFLAG_B_DEP) ? 0 : (nk < kStages ? nk : kStages);
-  const uint32_t fill0 = fill;
+  const int npre = (in.flags & IFLAG_B_DEP) ? 0 : (nk < (int)NS ? nk : (int)NS);
+  const RingPos r0 = rp;
   for (int kb = 0; kb < npre; ++kb) {
-    const int st = (int)(fill % kStages);
-    if (!wait_mbar(p, smem_u32(&s.empty[st]), ((fill / kStages) & 1u) ^ 1u, R_LOAD, 11, idx))
-      return false;
-    mbar_expect_tx(smem_u32(&s.full[st]), bytes);
-    load_b(st, kb);
-    ++fill;
+    if (!wait_warp(p, smem_u32(&s.empty[rp.st]), rp.ph ^ 1u, R_LOAD, 11, idx)) return false;
+    if (elect_one()) {
+      arm(rp.st);
+      issue_b(rp.st, kb);
+    }
+    __syncwarp();
+    rp.next(NS);
+    ++nfill;
   }
-  if (!wait_mbar(p, smem_u32(&s.deps_ready[slot]), use & 1u, R_LOAD, 12, idx)) return false;
-  fence_proxy_async_global();
-  for (int kb = 0; kb < npre; ++kb) load_a((int)((fill0 + kb) % kStages), kb);
+  if (!wait_warp(p, smem_u32(&s.deps_ready[slot]), use & 1u, R_LOAD, 12, idx)) return false;
+  if (elect_one()) {
+    fence_proxy_async_global();
+    RingPos q = r0;
+    for (int kb = 0; kb < npre; ++kb) {
+      issue_a(q.st, kb);
+      q.next(NS);
+    }
+  }
+  __syncwarp();
   for (int kb = npre; kb < nk; ++kb) {
-    const int st = (int)(fill % kStages);
-    if (!wait_mbar(p, smem_u32(&s.empty[st]), ((fill / kStages) & 1u) ^ 1u, R_LOAD, 13, idx))
-      return false;
-    mbar_expect_tx(smem_u32(&s.full[st]), bytes);
-    load_b(st, kb);
-    load_a(st, kb);
-    ++fill;
+    if (!wait_warp(p, smem_u32(&s.empty[rp.st]), rp.ph ^ 1u, R_LOAD, 13, idx)) return false;
+    if (elect_one()) {
+      arm(rp.st);
+      issue_b(rp.st, kb);
+      issue_a(rp.st, kb);
+    }
+    __syncwarp();
+    rp.next(NS);
+    ++nfill;
   }
   return true;
 }
@@ -327,32 +487,42 @@ __device__ bool load_gemm(const Params& p, Smem& s, const Instr& in, const Node&
 __device__ void prefetch_ahead(const Params& p, const Smem& s, int cur, int& next);
 
 __device__ bool load_gemv(const Params& p, Smem& s, const Instr& in, const Node& nd, int slot,
-                          uint32_t use, uint32_t& fill, int idx, int it, int& pf_next) {
+                          uint32_t use, RingPos& rp, uint32_t& nfill, int idx, int it,
+                          int& pf_next) {
+  const uint32_t NS = ring_n(p);
   const int nk = ring_stages(in);
   if (nk == 0) return true;
   const bool dual = (nd.flags & EPI_SILU_MUL) != 0;
-  // a stage is four 64-row x 64-column boxes, 128-byte swizzled (8 KB each): the tile's 256
+  const bool panel = (nd.flags & NF_B_PANELS) != 0;
+  // a stage is four 64-row x 64-column panels, 128-byte swizzled (8 KB each): the tile's 256
   // columns, or 128 gate columns then 128 up columns
   const uint32_t bytes = 4u * 64u * kGemvRows * 2u;
   const void* tb = tmap_at(p, nd.b.tmap);
   const void* tb2 = dual ? tmap_at(p, nd.b2.tmap) : nullptr;
+  const uint32_t ring0 = smem_u32(s.ring), sb = stage_bytes(p);
   if (in.flags & IFLAG_B_DEP) {
-    if (!wait_mbar(p, smem_u32(&s.deps_ready[slot]), use & 1u, R_LOAD, 14, idx)) return false;
-    fence_proxy_async_global();
+    if (!wait_warp(p, smem_u32(&s.deps_ready[slot]), use & 1u, R_LOAD, 14, idx)) return false;
+    if (elect_one()) fence_proxy_async_global();
+    __syncwarp();
   }
   for (int kb = 0; kb < nk; ++kb) {
-    const int st = (int)(fill % kStages);
-    if (kb >= kStages) prefetch_ahead(p, s, it, pf_next);  // descriptors published meanwhile
-    if (!wait_mbar(p, smem_u32(&s.empty[st]), ((fill / kStages) & 1u) ^ 1u, R_LOAD, 15, idx))
-      return false;
-    const uint32_t bar = smem_u32(&s.full[st]);
-    mbar_expect_tx(bar, bytes);
-    for (int j = 0; j < 4; ++j) {
-      const void* map = (dual && j >= 2) ? tb2 : tb;
-      const int x = in.n0 + 64 * (dual ? (j & 1) : j);
-      tma_load_2d(smem_u32(s.stage[st]) + j * 8192, map, bar, x, in.k0 + kb * kGemvRows);
+    if (kb >= (int)NS) prefetch_ahead(p, s, it, pf_next);  // descriptors published meanwhile
+    if (!wait_warp(p, smem_u32(&s.empty[rp.st]), rp.ph ^ 1u, R_LOAD, 15, idx)) return false;
+    if (elect_one()) {
+      const uint32_t bar = smem_u32(&s.full[rp.st]);
+      const uint32_t dst = ring0 + rp.st * sb;
+      const int k = in.k0 + kb * kGemvRows;
+      mbar_expect_tx(bar, bytes);
+      if (dual) {
+        load_panels<false>(dst, tb, panel, bar, in.n0, k, 2);
+        load_panels<false>(dst + 2 * 8192, tb2, panel, bar, in.n0, k, 2);
+      } else {
+        load_panels<false>(dst, tb, panel, bar, in.n0, k, 4);
+      }
     }
-    ++fill;
+    __syncwarp();
+    rp.next(NS);
+    ++nfill;
   }
   return true;
 }
@@ -361,31 +531,38 @@ __device__ bool load_gemv(const Params& p, Smem& s, const Instr& in, const Node&
 // stage, 128-byte swizzled: keys at offset 0, values at 16 KB. A chunk that does not contain a
 // row appended inside the graph streams before the query is ready.
 __device__ bool load_attn(const Params& p, Smem& s, const Instr& in, const Node& nd, int slot,
-                          uint32_t use, uint32_t& fill, int idx) {
+                          uint32_t use, RingPos& rp, uint32_t& nfill, int idx) {
+  const uint32_t NS = ring_n(p);
   if (in.flags & IFLAG_B_DEP) {
-    if (!wait_mbar(p, smem_u32(&s.deps_ready[slot]), use & 1u, R_LOAD, 16, idx)) return false;
-    fence_proxy_async_global();
+    if (!wait_warp(p, smem_u32(&s.deps_ready[slot]), use & 1u, R_LOAD, 16, idx)) return false;
+    if (elect_one()) fence_proxy_async_global();
+    __syncwarp();
   }
-  const int st = (int)(fill % kStages);
-  if (!wait_mbar(p, smem_u32(&s.empty[st]), ((fill / kStages) & 1u) ^ 1u, R_LOAD, 17, idx))
-    return false;
-  const uint32_t bar = smem_u32(&s.full[st]);
-  mbar_expect_tx(bar, (uint32_t)(2 * nd.tile_m * 128));
-  tma_load_2d(smem_u32(s.stage[st]), tmap_at(p, nd.b.tmap), bar, in.n0 * 64, in.k0);
-  tma_load_2d(smem_u32(s.stage[st]) + 16384, tmap_at(p, nd.b2.tmap), bar, in.n0 * 64, in.k0);
-  ++fill;
+  if (!wait_warp(p, smem_u32(&s.empty[rp.st]), rp.ph ^ 1u, R_LOAD, 17, idx)) return false;
+  if (elect_one()) {
+    const uint32_t bar = smem_u32(&s.full[rp.st]);
+    const uint32_t dst = smem_u32(s.ring) + rp.st * stage_bytes(p);
+    mbar_expect_tx(bar, (uint32_t)(2 * nd.tile_m * 128));
+    tma_load_2d(dst, tmap_at(p, nd.b.tmap), bar, in.n0 * 64, in.k0);
+    tma_load_2d(dst + 16384, tmap_at(p, nd.b2.tmap), bar, in.n0 * 64, in.k0);
+  }
+  __syncwarp();
+  rp.next(NS);
+  ++nfill;
   return true;
 }
 
 // L2 prefetch of the streamed operands of instructions already published to later slots: HBM
 // keeps streaming weights (and key/value chunks) while earlier instructions wait for their
 // activations; their shared-memory loads then hit L2. `next` is the first instruction not yet
-// prefetched; instructions whose operand is produced inside the graph are skipped.
+// prefetched; instructions whose operand is produced inside the graph are skipped. Slots are
+// probed without suspending the warp.
 __device__ void prefetch_ahead(const Params& p, const Smem& s, int cur, int& next) {
   if (next < cur) next = cur;
   while (next < cur + p.l2_prefetch) {
     const int slot = next % kSlots;
-    if (!mbar_try(smem_u32(&s.instr_ready[slot]), (uint32_t)(next / kSlots) & 1u)) return;
+    const bool ready = mbar_test(smem_u32(&s.instr_ready[slot]), (uint32_t)(next / kSlots) & 1u);
+    if (!__all_sync(FULL, ready)) return;
     const Instr& f = slot_instr(s, slot);
     if (f.op == OP_END) {
       next = 0x3fffffff;
@@ -393,122 +570,187 @@ __device__ void prefetch_ahead(const Params& p, const Smem& s, int cur, int& nex
     }
     const Node& nd = slot_node(s, slot);
     if (!(f.flags & IFLAG_B_DEP)) {
-      if (f.op == OP_GEMV) {
-        const bool dual = (nd.flags & EPI_SILU_MUL) != 0;
-        const int nk = ring_stages(f);
-        for (int kb = 0; kb < nk; ++kb) {
-          for (int j = 0; j < 4; ++j) {
-            const void* map = tmap_at(p, (dual && j >= 2) ? nd.b2.tmap : nd.b.tmap);
-            tma_prefetch_l2_2d(map, f.n0 + 64 * (dual ? (j & 1) : j), f.k0 + kb * kGemvRows);
+      if (elect_one()) {
+        const bool panel = (nd.flags & NF_B_PANELS) != 0;
+        if (f.op == OP_GEMV) {
+          const bool dual = (nd.flags & EPI_SILU_MUL) != 0;
+          const int nk = ring_stages(f);
+          const void* mb = tmap_at(p, nd.b.tmap);
+          const void* mb2 = dual ? tmap_at(p, nd.b2.tmap) : nullptr;
+          for (int kb = 0; kb < nk; ++kb) {
+            const int k = f.k0 + kb * kGemvRows;
+            if (panel) {
+              tma_prefetch_l2_3d(mb, 0, k, f.n0 >> 6);
+              if (dual) tma_prefetch_l2_3d(mb2, 0, k, f.n0 >> 6);
+            } else {
+              for (int j = 0; j < 4; ++j)
+                tma_prefetch_l2_2d((dual && j >= 2) ? mb2 : mb, f.n0 + 64 * (dual ? (j & 1) : j),
+                                   k);
+            }
           }
+        } else if (f.op == OP_ATTN_PARTIAL) {
+          tma_prefetch_l2_2d(tmap_at(p, nd.b.tmap), f.n0 * 64, f.k0);
+          tma_prefetch_l2_2d(tmap_at(p, nd.b2.tmap), f.n0 * 64, f.k0);
         }
-      } else if (f.op == OP_ATTN_PARTIAL) {
-        tma_prefetch_l2_2d(tmap_at(p, nd.b.tmap), f.n0 * 64, f.k0);
-        tma_prefetch_l2_2d(tmap_at(p, nd.b2.tmap), f.n0 * 64, f.k0);
       }
+      __syncwarp();
     }
     ++next;
   }
 }
 
+template <bool PAIR>
 __device__ void run_loader(const Params& p, Smem& s) {
+  const uint32_t NS = ring_n(p);
   for (int i = 0; i < p.n_tmaps; ++i) tensormap_acquire(tmap_at(p, i));
-  uint32_t fill = 0;
+  RingPos rp;
+  uint32_t nfill = 0, go_par = 0;
   int pf_next = 0;
   for (int it = 0;; ++it) {
     const int slot = it % kSlots;
     const uint32_t use = (uint32_t)(it / kSlots);
     const int idx = instr_index(p, it);
-    if (!wait_mbar(p, smem_u32(&s.instr_ready[slot]), use & 1u, R_LOAD, 10, idx)) break;
+    if (!wait_warp(p, smem_u32(&s.instr_ready[slot]), use & 1u, R_LOAD, 10, idx)) break;
     const Instr& in = slot_instr(s, slot);
     if (in.op == OP_END) break;
     const Node& nd = slot_node(s, slot);
     prefetch_ahead(p, s, it, pf_next);
     bool ok = true;
-    if (in.op == OP_GEMM) ok = load_gemm(p, s, in, nd, slot, use, fill, idx);
-    else if (in.op == OP_GEMV) ok = load_gemv(p, s, in, nd, slot, use, fill, idx, it, pf_next);
-    else if (in.op == OP_ATTN_PARTIAL) ok = load_attn(p, s, in, nd, slot, use, fill, idx);
+    if (in.op == OP_GEMM)
+      ok = load_gemm<PAIR>(p, s, in, nd, slot, use, rp, nfill, go_par, idx);
+    else if (in.op == OP_GEMV)
+      ok = load_gemv(p, s, in, nd, slot, use, rp, nfill, idx, it, pf_next);
+    else if (in.op == OP_ATTN_PARTIAL)
+      ok = load_attn(p, s, in, nd, slot, use, rp, nfill, idx);
     if (!ok) break;
-    mbar_arrive(smem_u32(&s.slot_free[slot]));
+    if (elect_one()) mbar_arrive(smem_u32(&s.slot_free[slot]));
+    __syncwarp();
   }
-  // Every load issued has landed before the CTA may exit (normally already true).
-  for (uint32_t st = 0; st < (uint32_t)kStages; ++st) {
-    if (fill <= st) continue;
-    const uint32_t fills = (fill - 1 - st) / kStages + 1;
-    wait_mbar_drain(smem_u32(&s.full[st]), (fills - 1) & 1u);
+  // Every load issued has landed before the CTA may exit (normally already true): the last fill
+  // of stage st was in the current pass when st < rp.st, else in the previous one.
+  for (uint32_t st = 0; st < NS; ++st) {
+    if (nfill <= st) continue;
+    wait_mbar_drain(smem_u32(&s.full[st]), st < rp.st ? rp.ph : rp.ph ^ 1u);
   }
+  __syncwarp();
 }
 
-// ------------------------------------------------------------------ MMA issuer (one thread)
+// ------------------------------------------------------------------ MMA issuer (one warp)
 
+template <bool PAIR>
 __device__ void run_mma(const Params& p, Smem& s, uint32_t tmem) {
-  uint32_t use = 0, acc_n = 0;
+  // The whole warp runs this loop, converged: ring position, descriptors and flags are
+  // warp-uniform and one elected lane issues each tcgen05 operation. Per k-step the issuer does
+  // a barrier poll, a fence and the MMAs of the stage; descriptors are the stage-0 descriptors
+  // plus the stage's offset in 16-byte units.
+  const uint32_t NS = ring_n(p);
+  const uint32_t units = stage_bytes(p) >> 4;
+  const uint32_t ring0 = smem_u32(s.ring);
+  // A: K-major, 128-byte rows, 8-row groups 1024 B apart; a 16-wide K slice is 32 B (2 units).
+  const uint64_t adesc0 = sdesc_sw128(ring0, 16, 1024);
+  // B: N-major, 64-column atoms 8 KB apart (LBO), 8-row K groups 1024 B apart (SBO); a 16-deep
+  // K slice is 16 rows of 128 B (128 units).
+  const uint64_t bdesc0 = sdesc_sw128(ring0 + kGemmTileM * kGemmBK * 2, 8192, 1024);
+  RingPos rp;
+  uint32_t acc_n = 0;
   bool issued = false;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
   for (int it = 0;; ++it) {
     const int slot = it % kSlots;
     const uint32_t u = (uint32_t)(it / kSlots);
     const int idx = instr_index(p, it);
-    if (!wait_mbar(p, smem_u32(&s.instr_ready[slot]), u & 1u, R_MMA, 20, idx)) break;
+    if (!wait_warp(p, smem_u32(&s.instr_ready[slot]), u & 1u, R_MMA, 20, idx)) break;
     const Instr& in = slot_instr(s, slot);
     if (in.op == OP_END) break;
     const Node& nd = slot_node(s, slot);
     bool ok = true;
     if (in.op == OP_GEMM) {
+      if (PAIR) rp.align();
       const int nk = ring_stages(in);
-      if (nk > 0) {
+      if (nk > 0 && PAIR && rank != 0) {
+        rp.advance((uint32_t)nk, NS);  // the even CTA issues the pair's MMAs
+        ++acc_n;
+      } else if (nk > 0) {
         const uint32_t as = acc_n & 1u;
-        if (!wait_mbar(p, smem_u32(&s.acc_empty[as]), ((acc_n >> 1) & 1u) ^ 1u, R_MMA, 21, idx))
+        // the slot is free once every epilogue that read it (both CTAs' in pair mode) is done
+        if (!wait_warp(p, smem_u32(&s.acc_empty[as]), ((acc_n >> 1) & 1u) ^ 1u, R_MMA, 21, idx,
+                       PAIR))
           break;
         tc_fence_after();
         const bool dual = (nd.flags & EPI_SILU_MUL) != 0;
         const int tn = nd.tile_n;
-        const uint32_t idesc = idesc_f16(nd.dtype == DT_BF16, tn);
+        const int ncol = PAIR ? tn / 2 : tn;  // B columns held by each CTA per weight
+        const uint32_t idesc = idesc_f16(nd.dtype == DT_BF16, tn, PAIR ? 256 : 128);
         const uint32_t d = tmem + as * 256u;
-        for (int kb = 0; kb < nk && ok; ++kb) {
-          const int st = (int)(use % kStages);
-          if (!wait_mbar(p, smem_u32(&s.full[st]), (use / kStages) & 1u, R_MMA, 22, idx)) {
+        const uint64_t up = (uint64_t)((ncol / 64) * (8192 >> 4));  // up-weight atoms
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!wait_warp(p, smem_u32(&s.full[rp.st]), rp.ph, R_MMA, 22, idx)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(s.stage[st]);
-          const uint32_t b0 = a0 + kGemmTileM * kGemmBK * 2;
+          const uint64_t so = (uint64_t)(rp.st * units);
+          if (elect_one()) {
 #pragma unroll
-          for (int j = 0; j < kGemmBK / 16; ++j) {
-            // A: K-major, 128-byte rows, 8-row groups 1024 B apart; a 16-wide K slice is 32 B.
-            const uint64_t ad = sdesc_sw128(a0 + j * 32, 16, 1024);
-            // B: N-major, 64-column atoms 8 KB apart (LBO), 8-row K groups 1024 B apart (SBO);
-            // a 16-deep K slice is 16 rows of 128 B.
-            const uint64_t bd = sdesc_sw128(b0 + j * 2048, 8192, 1024);
-            const uint32_t acc = (kb | j) != 0;
-            tc_mma_f16(d, ad, bd, idesc, acc);
-            if (dual) {
-              const uint64_t bd2 = sdesc_sw128(b0 + (tn / 64) * 8192 + j * 2048, 8192, 1024);
-              tc_mma_f16(d + (uint32_t)tn, ad, bd2, idesc, acc);
+            for (int j = 0; j < kGemmBK / 16; ++j) {
+              const uint64_t ad = adesc0 + so + (uint64_t)(j * 2);
+              const uint64_t bd = bdesc0 + so + (uint64_t)(j * 128);
+              const uint32_t acc = (kb | j) != 0;
+              if (PAIR)
+                tc_mma_f16_pair(d, ad, bd, idesc, acc);
+              else
+                tc_mma_f16(d, ad, bd, idesc, acc);
+              if (dual) {
+                if (PAIR)
+                  tc_mma_f16_pair(d + (uint32_t)tn, ad, bd + up, idesc, acc);
+                else
+                  tc_mma_f16(d + (uint32_t)tn, ad, bd + up, idesc, acc);
+              }
             }
+            // the stage is free (in both CTAs of a pair) once these MMAs complete
+            if (PAIR)
+              tc_commit_pair(smem_u32(&s.empty[rp.st]), 3);
+            else
+              tc_commit(smem_u32(&s.empty[rp.st]));
           }
-          tc_commit(smem_u32(&s.empty[st]));  // the stage is free once these MMAs complete
+          __syncwarp();
           issued = true;
-          ++use;
+          rp.next(NS);
         }
         if (!ok) break;
-        tc_commit(smem_u32(&s.acc_full[as]));
+        if (elect_one()) {
+          if (PAIR)
+            tc_commit_pair(smem_u32(&s.acc_full[as]), 3);
+          else
+            tc_commit(smem_u32(&s.acc_full[as]));
+        }
+        __syncwarp();
         ++acc_n;
       }
     } else {
-      use += (uint32_t)ring_stages(in);  // stages consumed by the compute warpgroup
+      rp.advance((uint32_t)ring_stages(in), NS);  // stages consumed by the compute warpgroup
     }
-    mbar_arrive(smem_u32(&s.slot_free[slot]));
+    if (elect_one()) mbar_arrive(smem_u32(&s.slot_free[slot]));
+    __syncwarp();
   }
   if (issued) {
-    tc_commit(smem_u32(&s.drain));
+    if (elect_one()) {
+      if (PAIR)
+        tc_commit_pair(smem_u32(&s.drain), 1);
+      else
+        tc_commit(smem_u32(&s.drain));
+    }
+    __syncwarp();
     wait_mbar_drain(smem_u32(&s.drain), 0);
   }
+  __syncwarp();
 }
 
 // ------------------------------------------------------------------ compute warpgroup bodies
 
-// GEMM epilogue: TMEM -> registers (one row per thread), fused epilogue, 16-byte stores.
+// GEMM epilogue: TMEM -> registers (one row per thread), fused epilogue, 16-byte stores. In pair
+// mode each CTA drains its own 128 rows of the 256-row tile.
+template <bool PAIR>
 __device__ bool gemm_epilogue(const Params& p, Smem& s, const Instr& in, const Node& nd, int slot,
                               uint32_t use, uint32_t tmem, uint32_t& acc_n, int idx) {
   const int ct = (int)threadIdx.x - (kThreads - kCompute);
@@ -526,7 +768,8 @@ __device__ bool gemm_epilogue(const Params& p, Smem& s, const Instr& in, const N
   const bool bias = (nd.flags & EPI_BIAS) != 0, relu = (nd.flags & EPI_RELU) != 0,
              res = (nd.flags & EPI_RESIDUAL) != 0;
   const int tn = nd.tile_n;
-  const int row = in.m0 + q * 32 + lane;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const int row = in.m0 + (int)rank * kGemmTileM + q * 32 + lane;
   const uint32_t tb = tmem + as * 256u + ((uint32_t)(q * 32) << 16);
   for (int c = 0; c < tn; c += 32) {
     uint32_t r[32], r2[32];
@@ -572,7 +815,12 @@ __device__ bool gemm_epilogue(const Params& p, Smem& s, const Instr& in, const N
   if (nk > 0) {
     tc_fence_before();
     cw_sync();
-    if (ct == 0) mbar_arrive(smem_u32(&s.acc_empty[as]));
+    if (ct == 0) {
+      if (PAIR && rank != 0)
+        mbar_arrive_cluster(mapa_shared(smem_u32(&s.acc_empty[as]), 0));
+      else
+        mbar_arrive(smem_u32(&s.acc_empty[as]));
+    }
     ++acc_n;
   }
   return true;
@@ -641,6 +889,7 @@ __device__ __forceinline__ void gemv_stage_rows(int M, const uint8_t* B, int ch,
 // writing a Blackwell GEMM", step 4).
 __device__ bool gemv(const Params& p, Smem& s, const Instr& in, const Node& nd, int slot,
                      uint32_t use, uint32_t& ring, bool* publish, int idx) {
+  const uint32_t NS = ring_n(p);
   const int ct = (int)threadIdx.x - (kThreads - kCompute);
   const int wp = ct >> 5, lane = ct & 31;
   if (!cw_wait(p, smem_u32(&s.deps_ready[slot]), use & 1u, 40, idx)) return false;
@@ -648,7 +897,6 @@ __device__ bool gemv(const Params& p, Smem& s, const Instr& in, const Node& nd, 
   const int M = nd.M, dt = nd.dtype;
   const bool dual = (nd.flags & EPI_SILU_MUL) != 0;
   const bool norm = (nd.flags & EPI_RMSNORM_INPUT) != 0;
-  const int wcols = nd.tile_n;                 // 256, or 128 per weight with SILU_MUL
   const int nk = ring_stages(in);
   const int kpad = nk * kGemvRows;
   const int kend = in.k0 + in.klen;
@@ -712,11 +960,11 @@ __device__ bool gemv(const Params& p, Smem& s, const Instr& in, const Node& nd, 
       xs = s.xr;
       xstride = kGemvRows;
     }
-    const int st = (int)(ring % kStages);
-    if (!cw_wait(p, smem_u32(&s.full[st]), (ring / kStages) & 1u, 41, idx)) return false;
+    const int st = (int)(ring % NS);
+    if (!cw_wait(p, smem_u32(&s.full[st]), (ring / NS) & 1u, 41, idx)) return false;
     // this thread's column pair: box (which * 2 + col / 64), column col % 64 inside it
     const int box = (dual ? which * 2 : 0) + (col >> 6), lc = col & 63;
-    const uint8_t* B = s.stage[st] + box * 8192 + (lc & 7) * 2;
+    const uint8_t* B = stage_ptr(s, p, st) + box * 8192 + (lc & 7) * 2;
     if (dt == DT_BF16)
       gemv_stage_rows<true>(M, B, lc >> 3, xs, xstride, acc);
     else
@@ -915,14 +1163,15 @@ __device__ void rope_body(const Instr& in, const Node& nd) {
 // sits at chunk c ^ (r & 7)).
 __device__ bool attn_partial_body(const Params& p, Smem& s, const Instr& in, const Node& nd,
                                   uint32_t& ring, int idx) {
+  const uint32_t NS = ring_n(p);
   const int ct = (int)threadIdx.x - (kThreads - kCompute);
   const int wp = ct >> 5, lane = ct & 31;
   const int g = in.n0, G = nd.hq / nd.hkv, C = in.aux1, c = in.aux0;
   const int kl = in.klen;
-  const int st = (int)(ring % kStages);
-  if (!cw_wait(p, smem_u32(&s.full[st]), (ring / kStages) & 1u, 42, idx)) return false;
-  const uint8_t* Ks = s.stage[st];
-  const uint8_t* Vs = s.stage[st] + 16384;
+  const int st = (int)(ring % NS);
+  if (!cw_wait(p, smem_u32(&s.full[st]), (ring / NS) & 1u, 42, idx)) return false;
+  const uint8_t* Ks = stage_ptr(s, p, st);
+  const uint8_t* Vs = stage_ptr(s, p, st) + 16384;
   for (int hh = wp; hh < G; hh += 4) {
     const int h = g * G + hh;
     float qv[64];
@@ -1033,7 +1282,9 @@ __device__ void attn_reduce_body(const Instr& in, const Node& nd) {
   }
 }
 
+template <bool PAIR>
 __device__ void run_compute(const Params& p, Smem& s, uint32_t tmem) {
+  const uint32_t NS = ring_n(p);
   const int ct = (int)threadIdx.x - (kThreads - kCompute);
   uint32_t ring = 0, acc_n = 0;
   for (int it = 0;; ++it) {
@@ -1048,7 +1299,8 @@ __device__ void run_compute(const Params& p, Smem& s, uint32_t tmem) {
     bool ok = true, publish = true;
     switch (in.op) {
       case OP_GEMM:
-        ok = gemm_epilogue(p, s, in, nd, slot, use, tmem, acc_n, idx);
+        if (PAIR) ring = ring_align(ring, NS);
+        ok = gemm_epilogue<PAIR>(p, s, in, nd, slot, use, tmem, acc_n, idx);
         ring += (uint32_t)ring_stages(in);
         break;
       case OP_GEMV:
@@ -1097,19 +1349,20 @@ __device__ void run_compute(const Params& p, Smem& s, uint32_t tmem) {
 
 // ------------------------------------------------------------------ the kernel
 
+template <bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1) megakernel(const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
   Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                      ~static_cast<uintptr_t>(1023));
-  const int warp = (int)threadIdx.x >> 5, lane = (int)threadIdx.x & 31;
+  const int warp = (int)threadIdx.x >> 5;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < kMaxStages; ++i) {
       mbar_init(smem_u32(&s.full[i]), 1);
       mbar_init(smem_u32(&s.empty[i]), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&s.acc_full[i]), 1);
-      mbar_init(smem_u32(&s.acc_empty[i]), 1);
+      mbar_init(smem_u32(&s.acc_empty[i]), PAIR ? 2 : 1);  // both epilogues of a pair
     }
     for (int i = 0; i < kSlots; ++i) {
       mbar_init(smem_u32(&s.instr_ready[i]), 1);
@@ -1117,34 +1370,43 @@ __global__ void __launch_bounds__(kThreads, 1) megakernel(const __grid_constant_
       mbar_init(smem_u32(&s.slot_free[i]), 3);  // loader, MMA issuer, compute warpgroup
     }
     mbar_init(smem_u32(&s.drain), 1);
+    mbar_init(smem_u32(&s.go), 1);
     mbar_fence_init();
   }
   if (warp == 2) {
-    tmem_alloc(smem_u32(&s.tmem_base), 512);
-    tmem_relinquish();
+    if (PAIR) {
+      tmem_alloc_pair(smem_u32(&s.tmem_base), 512);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(&s.tmem_base), 512);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync();  // the peer's barriers are initialised before any remote arrive
   tc_fence_after();
   const uint32_t tmem = s.tmem_base;
 
   if (warp == 0) {
     run_scheduler(p, s);
   } else if (warp == 1) {
-    if (lane == 0) run_loader(p, s);
-    __syncwarp();
+    run_loader<PAIR>(p, s);
   } else if (warp == 2) {
-    if (lane == 0) run_mma(p, s, tmem);
-    __syncwarp();
+    run_mma<PAIR>(p, s, tmem);
   } else if (warp >= 4) {
-    run_compute(p, s, tmem);
+    run_compute<PAIR>(p, s, tmem);
   }
 
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync();  // neither CTA leaves while its peer may still address it
   if (warp == 2) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    if (PAIR)
+      tmem_dealloc_pair(tmem, 512);
+    else
+      tmem_dealloc(tmem, 512);
   }
   // The CTA that finishes last (after every other CTA's work, including a drained abort)
   // publishes the run's status and zeroes the counters, so the next run needs no host reset.
@@ -1171,21 +1433,52 @@ __global__ void __launch_bounds__(kThreads, 1) megakernel(const __grid_constant_
 // ------------------------------------------------------------------ host launch stub
 
 cudaError_t configure_megakernel(size_t smem) {
-  return cudaFuncSetAttribute(megakernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(megakernel<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(megakernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+  return e;
 }
 
-cudaError_t launch_megakernel(const Params& p, int grid, size_t smem, cudaStream_t stream) {
+// Number of 2-CTA clusters of the pair kernel that can be resident at once.
+cudaError_t pair_clusters_resident(size_t smem, int* n) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaOccupancyMaxActiveClusters(n, megakernel<true>, &cfg);
+}
+
+cudaError_t launch_megakernel(const Params& p, int grid, size_t smem, cudaStream_t stream,
+                              bool pair) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs co-resident (they wait on each other)
-  attr[0].val.cooperative = 1;
+  if (pair) {
+    // 2-CTA clusters; co-residency of the whole grid is checked at compile time
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+  } else {
+    attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs co-resident (they wait on each other)
+    attr[0].val.cooperative = 1;
+  }
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, megakernel, p);
+  return pair ? cudaLaunchKernelEx(&cfg, megakernel<true>, p)
+              : cudaLaunchKernelEx(&cfg, megakernel<false>, p);
 }
 
 }  // namespace mk

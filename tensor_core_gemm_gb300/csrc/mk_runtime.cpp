@@ -18,8 +18,9 @@
 
 namespace mk {
 // Launch stub and shared-memory size, defined next to the kernel.
-cudaError_t launch_megakernel(const Params& p, int grid, size_t smem, cudaStream_t s);
+cudaError_t launch_megakernel(const Params& p, int grid, size_t smem, cudaStream_t s, bool pair);
 cudaError_t configure_megakernel(size_t smem);
+cudaError_t pair_clusters_resident(size_t smem, int* n);
 size_t megakernel_smem_bytes();
 }  // namespace mk
 
@@ -105,12 +106,19 @@ static bool aligned16(const TensorRec& t) {
 namespace mk {
 mk_status check_kernel_support(const std::vector<TensorRec>& ts, const std::vector<NodeRec>& nodes,
                                const mk_compile_opts& o) {
-  if (o.gemm_tile_m != kGemmTileM || o.cluster != 1) {
-    set_error("mk_compile: the kernel runs 128-row GEMM tiles with cluster 1");
+  const bool pair = o.cluster == 2;
+  if (!((o.gemm_tile_m == kGemmTileM && o.cluster == 1) ||
+        (o.gemm_tile_m == 2 * kGemmTileM && pair))) {
+    set_error("mk_compile: GEMM tiles are 128 rows on one CTA (cluster 1) or 256 rows on a CTA "
+              "pair (cluster 2)");
     return MK_ERR_UNSUPPORTED;
   }
-  if (o.gemm_tile_n != 64 && o.gemm_tile_n != 128 && o.gemm_tile_n != 256) {
-    set_error("mk_compile: gemm_tile_n must be 64, 128 or 256");
+  if (o.gemm_tile_n != (pair ? 128 : 64) && o.gemm_tile_n != 128 && o.gemm_tile_n != 256) {
+    set_error("mk_compile: gemm_tile_n must be 64, 128 or 256 (128 or 256 on CTA pairs)");
+    return MK_ERR_UNSUPPORTED;
+  }
+  if (pair && o.n_sm % 2) {
+    set_error("mk_compile: CTA pairs need an even n_sm");
     return MK_ERR_UNSUPPORTED;
   }
   if (o.gemv_tile_n != 256 || o.gemv_kstep % kGemvRows || o.gemv_max_m > 8 || o.gemv_max_m < 0) {
@@ -141,8 +149,9 @@ mk_status check_kernel_support(const std::vector<TensorRec>& ts, const std::vect
       }
     }
     if (nd.kind == NK_MATMUL) {
-      if ((nd.flags & MK_EPI_SILU_MUL) && ts[nd.a].rows > o.gemv_max_m && o.gemm_tile_n < 128) {
-        set_error("mk_compile: SILU_MUL GEMM tiles need gemm_tile_n >= 128");
+      if ((nd.flags & MK_EPI_SILU_MUL) && ts[nd.a].rows > o.gemv_max_m &&
+          o.gemm_tile_n < (o.cluster == 2 ? 256 : 128)) {
+        set_error("mk_compile: SILU_MUL GEMM tiles need gemm_tile_n >= 128 (256 on CTA pairs)");
         return MK_ERR_UNSUPPORTED;
       }
       if ((nd.flags & MK_EPI_RMSNORM_INPUT) && ts[nd.a].rows > o.gemv_max_m) {
@@ -193,16 +202,23 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 struct MapKey {
   uintptr_t ptr;
   int64_t rows, cols, ld;
-  int dtype, box_c, box_r, swz;
+  int dtype, box_c, box_r, swz, panels;
   bool operator==(const MapKey& o) const {
     return ptr == o.ptr && rows == o.rows && cols == o.cols && ld == o.ld && dtype == o.dtype &&
-           box_c == o.box_c && box_r == o.box_r && swz == o.swz;
+           box_c == o.box_c && box_r == o.box_r && swz == o.swz && panels == o.panels;
   }
 };
 
+// A 2D tiled map (box_c columns x box_r rows), or with panels > 0 a 3D "panel" map of a matrix
+// whose column count is a multiple of 64: dimensions (column within a 64-column panel, row,
+// panel), strides (row pitch, 128 bytes), box (64, box_r, panels). One copy through it writes
+// `panels` consecutive 64-column atoms, each box_r rows of 128 bytes, the same bytes and layout
+// as `panels` 2D copies of 64 x box_r boxes.
 static mk_status add_map(std::vector<MapKey>& keys, std::vector<CUtensorMap>& maps,
-                         const TensorRec& t, int box_c, int box_r, bool swizzle128, int* idx) {
-  MapKey k{(uintptr_t)t.ptr, t.rows, t.cols, t.ld, t.dtype, box_c, box_r, swizzle128 ? 1 : 0};
+                         const TensorRec& t, int box_c, int box_r, bool swizzle128, int* idx,
+                         int panels = 0) {
+  MapKey k{(uintptr_t)t.ptr, t.rows, t.cols, t.ld, t.dtype, box_c, box_r, swizzle128 ? 1 : 0,
+           panels};
   for (size_t i = 0; i < keys.size(); ++i)
     if (keys[i] == k) {
       *idx = (int)i;
@@ -219,18 +235,28 @@ static mk_status add_map(std::vector<MapKey>& keys, std::vector<CUtensorMap>& ma
   }
   CUtensorMap m;
   memset(&m, 0, sizeof m);
-  cuuint64_t dims[2] = {(cuuint64_t)t.cols, (cuuint64_t)t.rows};
-  cuuint64_t strides[1] = {(cuuint64_t)(t.ld * dtype_size(t.dtype))};
-  cuuint32_t box[2] = {(cuuint32_t)box_c, (cuuint32_t)box_r};
-  cuuint32_t estr[2] = {1, 1};
+  const cuuint64_t pitch = (cuuint64_t)(t.ld * dtype_size(t.dtype));
+  cuuint64_t dims[3] = {(cuuint64_t)t.cols, (cuuint64_t)t.rows, 1};
+  cuuint64_t strides[2] = {pitch, 0};
+  cuuint32_t box[3] = {(cuuint32_t)box_c, (cuuint32_t)box_r, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  cuuint32_t rank = 2;
+  if (panels > 0) {
+    dims[0] = 64;
+    dims[2] = (cuuint64_t)(t.cols / 64);
+    strides[1] = 128;
+    box[0] = 64;
+    box[2] = (cuuint32_t)panels;
+    rank = 3;
+  }
   CUresult r = fn(&m, t.dtype == DT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                          : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                  2, t.ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  rank, t.ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
-    set_error("mk_compile: cuTensorMapEncodeTiled failed (%d) for a %lldx%lld tensor, box %dx%d",
-              (int)r, (long long)t.rows, (long long)t.cols, box_r, box_c);
+    set_error("mk_compile: cuTensorMapEncodeTiled failed (%d) for a %lldx%lld tensor, box %dx%d, "
+              "%d panels", (int)r, (long long)t.rows, (long long)t.cols, box_r, box_c, panels);
     return MK_ERR_CUDA;
   }
   keys.push_back(k);
@@ -292,18 +318,25 @@ static mk_status build_nodes(const mk_graph* g, mk_plan* p, std::vector<CUtensor
         if (gemv) n.ldp = n.M * n.N * ((nd.flags & MK_EPI_SILU_MUL) ? 2 : 1);
         if (n.M > 0 && n.N > 0 && n.K > 0) {
           mk_status st;
+          // B (and b2) move as 64-column panels of 64 rows, 128-byte swizzled: one 3D copy
+          // for all of a stage's panels when every weight has a multiple of 64 columns, else
+          // one 2D copy per panel.
+          const bool dual = nd.b2 >= 0;
+          const bool panel = B.cols % 64 == 0 && (!dual || ts[nd.b2].cols % 64 == 0);
+          int np;
           if (!gemv) {
+            const int tnw = n.tile_n;  // columns per weight of one tile
+            np = (p->opts.cluster == 2 ? tnw / 2 : tnw) / 64;
             if ((st = add_map(keys, maps, A, kGemmBK, kGemmTileM, true, &n.a.tmap))) return st;
-            if ((st = add_map(keys, maps, B, 64, kGemmBK, true, &n.b.tmap))) return st;
-            if (nd.b2 >= 0 && (st = add_map(keys, maps, ts[nd.b2], 64, kGemmBK, true, &n.b2.tmap)))
-              return st;
           } else {
-            // 64 x 64 boxes, 128-byte swizzle (four per 32 KB stage)
-            if ((st = add_map(keys, maps, B, 64, kGemvRows, true, &n.b.tmap))) return st;
-            if (nd.b2 >= 0 &&
-                (st = add_map(keys, maps, ts[nd.b2], 64, kGemvRows, true, &n.b2.tmap)))
-              return st;
+            np = dual ? 2 : 4;  // a 32 KB stage: 256 columns, or 128 gate + 128 up
           }
+          const int rows = gemv ? kGemvRows : kGemmBK;
+          if ((st = add_map(keys, maps, B, 64, rows, true, &n.b.tmap, panel ? np : 0))) return st;
+          if (dual &&
+              (st = add_map(keys, maps, ts[nd.b2], 64, rows, true, &n.b2.tmap, panel ? np : 0)))
+            return st;
+          if (panel) n.flags |= NF_B_PANELS;
         }
         break;
       }
@@ -493,6 +526,16 @@ extern "C" mk_status mk_compile(mk_graph_t g, const mk_compile_opts* opts_in, mk
     p->smem = megakernel_smem_bytes();
     e = configure_megakernel(p->smem);
   }
+  if (e == cudaSuccess && o.cluster == 2) {
+    int clusters = 0;
+    e = pair_clusters_resident(p->smem, &clusters);
+    if (e == cudaSuccess && clusters < o.n_sm / 2) {
+      set_error("mk_compile: only %d CTA pairs can be resident, %d needed", clusters, o.n_sm / 2);
+      cudaFree(p->d_mem);
+      delete p;
+      return MK_ERR_UNSUPPORTED;
+    }
+  }
   if (e != cudaSuccess) {
     set_error("mk_compile: device upload failed: %s", cudaGetErrorString(e));
     cudaFree(p->d_mem);
@@ -516,6 +559,7 @@ extern "C" mk_status mk_compile(mk_graph_t g, const mk_compile_opts* opts_in, mk
   pr.n_tmaps = (int32_t)maps.size();
   pr.n_counters = (int32_t)n_ctr;
   pr.l2_prefetch = std::min(std::max(o.l2_prefetch, 0), kSlots);
+  pr.stages = o.cluster == 2 ? kPairStages : kStages;
   pr.timeout_ns = (uint64_t)(o.timeout_ms > 0 ? o.timeout_ms : 2000) * 1000000ull;
   p->grid = o.n_sm;
   p->on_device = true;
@@ -530,7 +574,7 @@ extern "C" mk_status mk_run(mk_plan_t p, void* stream) {
   }
   cudaStream_t s = (cudaStream_t)stream;
   if (p->params.n_instr == 0) return MK_OK;
-  CUDA_TRY(launch_megakernel(p->params, p->grid, p->smem, s));
+  CUDA_TRY(launch_megakernel(p->params, p->grid, p->smem, s, p->opts.cluster == 2));
   return MK_OK;
 }
 

@@ -50,6 +50,7 @@ enum : uint32_t {
   EPI_RESIDUAL = 1u << 2,
   EPI_RMSNORM_INPUT = 1u << 3,
   EPI_SILU_MUL = 1u << 4,
+  NF_B_PANELS = 1u << 16,  // B (and b2) maps are 3D panel maps: one box per stage, all panels
 };
 
 enum : int32_t { EWOP_ADD = 0, EWOP_RELU = 1, EWOP_COPY = 2, EWOP_SILU_MUL = 3 };
@@ -107,7 +108,7 @@ struct Params {
   int32_t n_tmaps;
   int32_t n_counters;       // dependency counters + split semaphores
   int32_t l2_prefetch;      // instructions ahead whose streamed operands are prefetched to L2
-  int32_t pad1;
+  int32_t stages;           // operand ring depth: 4 stages of 48 KB, or 6 of 32 KB (CTA pairs)
   uint64_t timeout_ns;
 };
 
@@ -118,8 +119,10 @@ constexpr int kTraceWords = 6;
 
 // Kernel geometry shared with the host (launch configuration and shared-memory budget).
 constexpr int kThreads = 256;          // 8 warps: scheduler, loader, MMA, spare, 4 compute
-constexpr int kStages = 4;             // operand ring depth
-constexpr int kStageBytes = 48 * 1024; // A 128x64 (16 KB) + B 64x256 (32 KB), 16-bit elements
+constexpr int kRingBytes = 192 * 1024; // operand ring, split into equal 1024-byte-aligned stages
+constexpr int kStages = 4;              // single-CTA GEMM tiles: A 128x64 (16 KB) + B 64x256 (32 KB)
+constexpr int kPairStages = 6;          // CTA pairs: A 128x64 + half of B (16 KB) per CTA, 32 KB
+constexpr int kMaxStages = kPairStages;
 constexpr int kSlots = 8;              // instruction slots (scheduler lookahead)
 constexpr int kSlotBytes = 64 + 256;   // Instr + Node
 constexpr int kGemmTileM = 128;

@@ -399,3 +399,73 @@ def test_trace_timestamps_are_ordered():
     assert np.all(tr[real, 2] >= tr[real, 1]) and np.all(tr[real, 3] >= tr[real, 2])
     assert np.all(tr[real, 4] >= tr[real, 3]) and np.all(tr[real, 3] >= tr[real, 0])
     assert np.all(tr[real, 5] == np.arange(len(ins))[real] % p.stats()["n_sm"])
+
+
+# ------------------------------------------------------------------ CTA pairs (cta_group::2)
+
+PAIR = dict(gemm_tile_m=256, cluster=2)
+
+
+@pytest.mark.parametrize("m,n,k,tn,dt", [
+    (256, 128, 64, 128, "f16"), (256, 256, 256, 256, "f16"), (300, 392, 200, 256, "f16"),
+    (129, 72, 520, 128, "bf16"), (1000, 1024, 776, 256, "bf16"), (512, 512, 1024, 128, "f16")])
+def test_pair_gemm_full_compare(m, n, k, tn, dt):
+    wl = workloads.gemm(m, n, k, dtype=dt, device=DEV, seed=m + n + k + 1)
+    opts = dict(PAIR, gemm_tile_n=tn)
+    plan, _ = run(wl, **opts)
+    ref = ops.matmul(f32(wl.data[0]), f32(wl.data[1]), F16 if dt == "f16" else BF16)
+    assert_close(f32(wl.data[2]), ref, f"pair gemm {m}x{n}x{k}")
+    check_counters(plan, wl, opts)
+
+
+def test_pair_gemm_4096_sampled_rows():
+    wl = workloads.gemm(4096, 4096, 4096, dtype="f16", device=DEV, seed=0)
+    plan, _ = run(wl, **PAIR)
+    rows = np.sort(torch.randperm(4096, generator=torch.Generator().manual_seed(1))[:256].numpy())
+    a = f32(wl.data[0][torch.as_tensor(rows, device=DEV)])
+    ref = ops.matmul(a, f32(wl.data[1]), F16)
+    assert_close(f32(wl.data[2][torch.as_tensor(rows, device=DEV)]), ref, "pair 4096^3 rows")
+    check_counters(plan, wl, PAIR)
+
+
+def test_pair_epilogues_and_mixed_graph():
+    """Pair GEMMs with bias/ReLU/residual and SiLU·mul epilogues, then a GEMV and a norm in the
+    same launch, so the two CTAs of a pair also run unrelated instructions between pair tiles."""
+    m, n, k = 384, 512, 320
+    a = synth.normal((m, k), 1.0, "bf16", 11, DEV)
+    b = synth.normal((k, n), 1 / math.sqrt(k), "bf16", 12, DEV)
+    bu = synth.normal((k, n), 1 / math.sqrt(k), "bf16", 13, DEV)
+    bias = synth.normal((m, n), 0.5, "bf16", 14, DEV)
+    res = synth.normal((m, n), 1.0, "bf16", 15, DEV)
+    w2 = synth.normal((n, 768), 1 / math.sqrt(n), "bf16", 16, DEV)
+    o1, o2 = (torch.zeros((m, n), dtype=torch.bfloat16, device=DEV) for _ in range(2))
+    o3 = torch.zeros((1, 768), dtype=torch.bfloat16, device=DEV)
+    from tensor_core_gemm_gb300 import Graph
+    g = Graph()
+    ia, ib, ibu, ibias, ires, i1, i2, iw2, i3 = (
+        g.tensor(t) for t in (a, b, bu, bias, res, o1, o2, w2, o3))
+    g.matmul(ia, ib, i1, bias=ibias, relu=True, residual=ires)
+    g.matmul(ia, ib, i2, b_up=ibu)
+    g.matmul(g.view(i1, 0, 0, 1, n), iw2, i3)
+    p = g.compile(gemm_tile_n=256, **PAIR)
+    p.run()
+    p.check_status()
+    A, B, BU = f32(a), f32(b), f32(bu)
+    r1 = ops.matmul(A, B, BF16, bias=f32(bias), relu=True, residual=f32(res))
+    assert_close(f32(o1), r1, "pair bias+relu+residual")
+    assert_close(f32(o2), ops.matmul_silu_mul(A, B, BU, BF16), "pair silu_mul")
+    assert_close(f32(o3), ops.matmul(f32(o1)[:1], f32(w2), BF16), "gemv after pair tiles")
+    p.run()                                   # a second launch reuses the reset counters
+    p.check_status()
+    assert_close(f32(o1), r1, "pair second launch")
+
+
+def test_pair_options_rejected_by_the_kernel_check():
+    from tensor_core_gemm_gb300._lib import MkError
+    wl = workloads.gemm(256, 256, 256, dtype="f16", device=DEV)
+    g, _ = workloads.build_graph(wl.desc, wl.data)
+    for bad in (dict(gemm_tile_m=256, cluster=1), dict(gemm_tile_m=128, cluster=2),
+                dict(gemm_tile_m=256, cluster=2, gemm_tile_n=64),
+                dict(gemm_tile_m=256, cluster=2, n_sm=151)):
+        with pytest.raises(MkError):
+            g.compile(**bad)

@@ -86,6 +86,19 @@ def test_gemm_plans(m, n, k, tn):
     assert_same_plan(workloads.gemm(m, n, k).desc, dict(n_sm=152, gemm_tile_n=tn))
 
 
+@pytest.mark.parametrize("m,n,k,tn", [(4096, 4096, 4096, 256), (300, 392, 200, 128),
+                                      (129, 72, 520, 128)])
+def test_pair_gemm_plans(m, n, k, tn):
+    """CTA-pair tiles: 256 x tn, two instructions per tile on an even/odd SM pair."""
+    opts = dict(n_sm=152, gemm_tile_n=tn, gemm_tile_m=256, cluster=2)
+    py, c = assert_same_plan(workloads.gemm(m, n, k).desc, opts)
+    ins = c.instructions()
+    gem = np.nonzero(ins["op"] == osched.OP_GEMM)[0]
+    assert gem.size == 2 * (-(-m // 256)) * (-(-n // tn))
+    assert np.all(gem[0::2] % 2 == 0) and np.all(gem[1::2] == gem[0::2] + 1)
+    assert np.all(ins["aux0"][gem[0::2]] == 0) and np.all(ins["aux0"][gem[1::2]] == 1)
+
+
 def test_mlp3_plan():
     py, c = assert_same_plan(workloads.mlp3().desc, dict(n_sm=152, gemm_tile_n=64))
     # layer-2 tiles wait on exactly the 16 layer-1 tiles of their 128-row block
