@@ -375,6 +375,81 @@ __device__ __forceinline__ void load_panels(uint32_t dst, const void* map, bool 
 // offsets. Before every pair GEMM both CTAs therefore move to the start of the next pass over the
 // ring; each skipped stage is waited free, then both of its barriers are arrived on so their
 // phase counts stay equal to the use count every role tracks.
+// Everything the k-loop of one GEMM tile's loads needs, as plain values.
+struct LoadTile {
+  uint32_t full0, tx0, empty0, deps, deps_par, ring0, sb, ns, own;
+  int nk, npre, arow, bcol, k0, nbox;
+  const void *ta, *tb, *tb2;
+  bool leader, panel;
+};
+
+// The loads of one GEMM tile, from ring position (st, ph). Out of line so the hot loop compiles
+// on its own. Weights first: the first npre stages get their B operand before the activations
+// are known to be ready (they depend on nothing inside the graph), then A follows for those and
+// both for the rest. Each stage is armed by the CTA whose barrier counts the bytes: the even CTA
+// of a pair expects both CTAs' bytes; the odd CTA arrives on its own barrier only to keep its
+// phase count in step.
+template <bool PAIR, bool DUAL>
+__device__ __noinline__ bool load_tile(const Params& p, const LoadTile& tp, uint32_t st,
+                                       uint32_t ph, int idx) {
+  const LoadTile t = tp;  // a private copy: its fields stay in registers
+  auto arm = [&](uint32_t s_) {
+    if (t.leader)
+      mbar_expect_tx(t.full0 + s_ * 8u, PAIR ? 2 * t.own : t.own);
+    else
+      mbar_arrive(t.full0 + s_ * 8u);
+  };
+  auto issue_b = [&](uint32_t s_, int kb) {
+    const uint32_t dst = t.ring0 + s_ * t.sb + kGemmTileM * kGemmBK * 2;
+    const int k = t.k0 + kb * kGemmBK;
+    load_panels<PAIR>(dst, t.tb, t.panel, t.tx0 + s_ * 8u, t.bcol, k, t.nbox);
+    if (DUAL) load_panels<PAIR>(dst + t.nbox * 8192, t.tb2, t.panel, t.tx0 + s_ * 8u, t.bcol, k, t.nbox);
+  };
+  auto issue_a = [&](uint32_t s_, int kb) {
+    if (PAIR)
+      tma_load_2d_pair(t.ring0 + s_ * t.sb, t.ta, t.tx0 + s_ * 8u, t.k0 + kb * kGemmBK, t.arow);
+    else
+      tma_load_2d(t.ring0 + s_ * t.sb, t.ta, t.tx0 + s_ * 8u, t.k0 + kb * kGemmBK, t.arow);
+  };
+  const uint32_t st0 = st;
+  for (int kb = 0; kb < t.npre; ++kb) {
+    if (!wait_warp(p, t.empty0 + st * 8u, ph ^ 1u, R_LOAD, 11, idx)) return false;
+    if (elect_one()) {
+      arm(st);
+      issue_b(st, kb);
+    }
+    __syncwarp();
+    if (++st == t.ns) {
+      st = 0;
+      ph ^= 1u;
+    }
+  }
+  if (!wait_warp(p, t.deps, t.deps_par, R_LOAD, 12, idx)) return false;
+  if (elect_one()) {
+    fence_proxy_async_global();
+    uint32_t q = st0;
+    for (int kb = 0; kb < t.npre; ++kb) {
+      issue_a(q, kb);
+      if (++q == t.ns) q = 0;
+    }
+  }
+  __syncwarp();
+  for (int kb = t.npre; kb < t.nk; ++kb) {
+    if (!wait_warp(p, t.empty0 + st * 8u, ph ^ 1u, R_LOAD, 13, idx)) return false;
+    if (elect_one()) {
+      arm(st);
+      issue_b(st, kb);
+      issue_a(st, kb);
+    }
+    __syncwarp();
+    if (++st == t.ns) {
+      st = 0;
+      ph ^= 1u;
+    }
+  }
+  return true;
+}
+
 template <bool PAIR>
 __device__ bool load_gemm(const Params& p, Smem& s, const Instr& in, const Node& nd, int slot,
                           uint32_t use, RingPos& rp, uint32_t& nfill, uint32_t& go_par, int idx) {
@@ -417,71 +492,33 @@ __device__ bool load_gemm(const Params& p, Smem& s, const Instr& in, const Node&
   const bool panel = (nd.flags & NF_B_PANELS) != 0;
   const int tn = nd.tile_n;
   const int ncol = PAIR ? tn / 2 : tn;  // B columns this CTA loads per weight
-  const int nbox = ncol / 64;
-  const uint32_t own = (uint32_t)(kGemmTileM * kGemmBK * 2 + (dual ? 2 : 1) * ncol * kGemmBK * 2);
-  const int arow = in.m0 + (int)rank * kGemmTileM;
-  const int bcol = in.n0 + (int)rank * ncol;
-  const void* ta = tmap_at(p, nd.a.tmap);
-  const void* tb = tmap_at(p, nd.b.tmap);
-  const void* tb2 = dual ? tmap_at(p, nd.b2.tmap) : nullptr;
-  const uint32_t ring0 = smem_u32(s.ring), sb = stage_bytes(p);
+  LoadTile t;
+  t.full0 = smem_u32(&s.full[0]);
   // bytes of both CTAs of a pair complete on the even CTA's full barrier
-  const uint32_t fb0 = PAIR ? mapa_shared(smem_u32(&s.full[0]), 0) : smem_u32(&s.full[0]);
-  // Arm stage st for this k-step: the even CTA of a pair expects both CTAs' bytes.
-  auto arm = [&](uint32_t st) {
-    if (!PAIR || rank == 0)
-      mbar_expect_tx(smem_u32(&s.full[st]), PAIR ? 2 * own : own);
-    else
-      mbar_arrive(smem_u32(&s.full[st]));  // keeps this CTA's phase count in step
-  };
-  auto issue_b = [&](uint32_t st, int kb) {
-    const uint32_t dst = ring0 + st * sb + kGemmTileM * kGemmBK * 2;
-    const int k = in.k0 + kb * kGemmBK;
-    load_panels<PAIR>(dst, tb, panel, fb0 + st * 8u, bcol, k, nbox);
-    if (dual) load_panels<PAIR>(dst + nbox * 8192, tb2, panel, fb0 + st * 8u, bcol, k, nbox);
-  };
-  auto issue_a = [&](uint32_t st, int kb) {
-    if (PAIR)
-      tma_load_2d_pair(ring0 + st * sb, ta, fb0 + st * 8u, in.k0 + kb * kGemmBK, arow);
-    else
-      tma_load_2d(ring0 + st * sb, ta, fb0 + st * 8u, in.k0 + kb * kGemmBK, arow);
-  };
-  // Weights first: they depend on nothing inside the graph, so they stream into free stages
-  // while the activations are still being produced elsewhere.
-  const int npre = (in.flags & IFLAG_B_DEP) ? 0 : (nk < (int)NS ? nk : (int)NS);
-  const RingPos r0 = rp;
-  for (int kb = 0; kb < npre; ++kb) {
-    if (!wait_warp(p, smem_u32(&s.empty[rp.st]), rp.ph ^ 1u, R_LOAD, 11, idx)) return false;
-    if (elect_one()) {
-      arm(rp.st);
-      issue_b(rp.st, kb);
-    }
-    __syncwarp();
-    rp.next(NS);
-    ++nfill;
-  }
-  if (!wait_warp(p, smem_u32(&s.deps_ready[slot]), use & 1u, R_LOAD, 12, idx)) return false;
-  if (elect_one()) {
-    fence_proxy_async_global();
-    RingPos q = r0;
-    for (int kb = 0; kb < npre; ++kb) {
-      issue_a(q.st, kb);
-      q.next(NS);
-    }
-  }
-  __syncwarp();
-  for (int kb = npre; kb < nk; ++kb) {
-    if (!wait_warp(p, smem_u32(&s.empty[rp.st]), rp.ph ^ 1u, R_LOAD, 13, idx)) return false;
-    if (elect_one()) {
-      arm(rp.st);
-      issue_b(rp.st, kb);
-      issue_a(rp.st, kb);
-    }
-    __syncwarp();
-    rp.next(NS);
-    ++nfill;
-  }
-  return true;
+  t.tx0 = PAIR ? mapa_shared(t.full0, 0) : t.full0;
+  t.empty0 = smem_u32(&s.empty[0]);
+  t.deps = smem_u32(&s.deps_ready[slot]);
+  t.deps_par = use & 1u;
+  t.ring0 = smem_u32(s.ring);
+  t.sb = stage_bytes(p);
+  t.ns = NS;
+  t.nk = nk;
+  t.npre = (in.flags & IFLAG_B_DEP) ? 0 : (nk < (int)NS ? nk : (int)NS);
+  t.ta = tmap_at(p, nd.a.tmap);
+  t.tb = tmap_at(p, nd.b.tmap);
+  t.tb2 = dual ? tmap_at(p, nd.b2.tmap) : nullptr;
+  t.arow = in.m0 + (int)rank * kGemmTileM;
+  t.bcol = in.n0 + (int)rank * ncol;
+  t.k0 = in.k0;
+  t.nbox = ncol / 64;
+  t.own = (uint32_t)(kGemmTileM * kGemmBK * 2 + (dual ? 2 : 1) * ncol * kGemmBK * 2);
+  t.leader = !PAIR || rank == 0;
+  t.panel = panel;
+  const bool ok = dual ? load_tile<PAIR, true>(p, t, rp.st, rp.ph, idx)
+                       : load_tile<PAIR, false>(p, t, rp.st, rp.ph, idx);
+  rp.advance((uint32_t)nk, NS);
+  nfill += (uint32_t)nk;
+  return ok;
 }
 
 __device__ void prefetch_ahead(const Params& p, const Smem& s, int cur, int& next);
@@ -637,6 +674,64 @@ __device__ void run_loader(const Params& p, Smem& s) {
 
 // ------------------------------------------------------------------ MMA issuer (one warp)
 
+// The MMAs of one GEMM tile: nk k-steps from ring position (st, ph), accumulating into TMEM
+// column d. Out of line and with scalar arguments so the hot loop compiles on its own: few live
+// values, operands that stay warp-uniform. Software-pipelined: an MMA issue waits while the
+// tensor pipe is busy and the pipe queues little ahead, so the next stage's barrier is polled
+// after all but the last K slice of the current stage is issued; the pipe keeps executing
+// meanwhile. Returns the number of k-steps whose MMAs were issued (nk unless a wait gave up).
+template <bool PAIR, bool DUAL>
+__device__ __noinline__ int mma_tile(const Params& p, uint32_t full0, uint32_t empty0,
+                                     uint32_t st, uint32_t ph, uint32_t ns, int nk,
+                                     uint64_t adesc0, uint64_t bdesc0, uint32_t units, uint32_t d,
+                                     uint32_t idesc, int tn, uint64_t up, int idx) {
+  auto slice = [&](uint64_t so, int j, uint32_t acc) {
+    const uint64_t ad = adesc0 + so + (uint64_t)(j * 2);
+    const uint64_t bd = bdesc0 + so + (uint64_t)(j * 128);
+    if (PAIR)
+      tc_mma_f16_pair(d, ad, bd, idesc, acc);
+    else
+      tc_mma_f16(d, ad, bd, idesc, acc);
+    if (DUAL) {
+      if (PAIR)
+        tc_mma_f16_pair(d + (uint32_t)tn, ad, bd + up, idesc, acc);
+      else
+        tc_mma_f16(d + (uint32_t)tn, ad, bd + up, idesc, acc);
+    }
+  };
+  if (!wait_warp(p, full0 + st * 8u, ph, R_MMA, 22, idx)) return 0;
+  tc_fence_after();
+  for (int kb = 0; kb < nk; ++kb) {
+    const uint64_t so = (uint64_t)(st * units);
+    uint32_t nst = st + 1, nph = ph;
+    if (nst == ns) {
+      nst = 0;
+      nph ^= 1u;
+    }
+    if (elect_one()) {
+#pragma unroll
+      for (int j = 0; j < kGemmBK / 16 - 1; ++j) slice(so, j, (kb | j) != 0);
+    }
+    __syncwarp();
+    if (kb + 1 < nk) {
+      if (!wait_warp(p, full0 + nst * 8u, nph, R_MMA, 22, idx)) return kb + 1;
+      tc_fence_after();
+    }
+    if (elect_one()) {
+      slice(so, kGemmBK / 16 - 1, 1u);
+      // the stage is free (in both CTAs of a pair) once these MMAs complete
+      if (PAIR)
+        tc_commit_pair(empty0 + st * 8u, 3);
+      else
+        tc_commit(empty0 + st * 8u);
+    }
+    __syncwarp();
+    st = nst;
+    ph = nph;
+  }
+  return nk;
+}
+
 template <bool PAIR>
 __device__ void run_mma(const Params& p, Smem& s, uint32_t tmem) {
   // The whole warp runs this loop, converged: ring position, descriptors and flags are
@@ -683,41 +778,15 @@ __device__ void run_mma(const Params& p, Smem& s, uint32_t tmem) {
         const uint32_t idesc = idesc_f16(nd.dtype == DT_BF16, tn, PAIR ? 256 : 128);
         const uint32_t d = tmem + as * 256u;
         const uint64_t up = (uint64_t)((ncol / 64) * (8192 >> 4));  // up-weight atoms
-        for (int kb = 0; kb < nk; ++kb) {
-          if (!wait_warp(p, smem_u32(&s.full[rp.st]), rp.ph, R_MMA, 22, idx)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint64_t so = (uint64_t)(rp.st * units);
-          if (elect_one()) {
-#pragma unroll
-            for (int j = 0; j < kGemmBK / 16; ++j) {
-              const uint64_t ad = adesc0 + so + (uint64_t)(j * 2);
-              const uint64_t bd = bdesc0 + so + (uint64_t)(j * 128);
-              const uint32_t acc = (kb | j) != 0;
-              if (PAIR)
-                tc_mma_f16_pair(d, ad, bd, idesc, acc);
-              else
-                tc_mma_f16(d, ad, bd, idesc, acc);
-              if (dual) {
-                if (PAIR)
-                  tc_mma_f16_pair(d + (uint32_t)tn, ad, bd + up, idesc, acc);
-                else
-                  tc_mma_f16(d + (uint32_t)tn, ad, bd + up, idesc, acc);
-              }
-            }
-            // the stage is free (in both CTAs of a pair) once these MMAs complete
-            if (PAIR)
-              tc_commit_pair(smem_u32(&s.empty[rp.st]), 3);
-            else
-              tc_commit(smem_u32(&s.empty[rp.st]));
-          }
-          __syncwarp();
-          issued = true;
-          rp.next(NS);
-        }
-        if (!ok) break;
+        const uint32_t full0 = smem_u32(&s.full[0]), empty0 = smem_u32(&s.empty[0]);
+        const int done = dual ? mma_tile<PAIR, true>(p, full0, empty0, rp.st, rp.ph, NS, nk,
+                                                     adesc0, bdesc0, units, d, idesc, tn, up, idx)
+                              : mma_tile<PAIR, false>(p, full0, empty0, rp.st, rp.ph, NS, nk,
+                                                      adesc0, bdesc0, units, d, idesc, tn, up, idx);
+        if (done > 0) issued = true;
+        ok = done == nk;
+        rp.advance((uint32_t)nk, NS);
+        if (!ok) break;  // MMAs in flight are drained below
         if (elect_one()) {
           if (PAIR)
             tc_commit_pair(smem_u32(&s.acc_full[as]), 3);
