@@ -59,14 +59,15 @@ CONFIGS = {
 
 def make_workload(name, device):
     from tensor_core_gemm_gb300 import workloads as W
+    pair = {"gemm_tile_m": 256, "cluster": 2}   # 256 x 256 tiles on CTA pairs
     if name == "gemm4096":
-        return W.gemm(4096, 4096, 4096, dtype="f16", device=device, seed=0), {}
+        return W.gemm(4096, 4096, 4096, dtype="f16", device=device, seed=0), dict(pair)
     if name == "mlp3":
         return W.mlp3(device=device, seed=0), {"gemm_tile_n": 64}
     if name == "llama_prefill":
-        return W.gemm_list(W.LLAMA70B_PREFILL, device=device, seed=0), {}
+        return W.gemm_list(W.LLAMA70B_PREFILL, device=device, seed=0), dict(pair)
     if name == "llama_decode":
-        return W.gemm_list(W.LLAMA70B_DECODE, device=device, seed=0), {}
+        return W.gemm_list(W.LLAMA70B_DECODE, device=device, seed=0), dict(pair)
     if name == "decode":
         return W.decode(device=device, seed=0), {}
     if name == "prefill":

@@ -43,6 +43,8 @@ struct __align__(1024) Smem {
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint64_t go;                          // pair mode, odd CTA: released by the even CTA once per GEMM
+  // prefill attention: scores S and output blocks O double-buffered in TMEM, P in xr
+  uint64_t att_s_full[2], att_s_free[2], att_p_full, att_o_full[2], att_o_free[2];
   uint64_t instr_ready[kSlots];
   uint64_t deps_ready[kSlots];
   uint64_t slot_free[kSlots];
@@ -105,6 +107,7 @@ __device__ __forceinline__ int ring_stages(const Instr& in) {
   if (in.op == OP_GEMM) return (in.klen + kGemmBK - 1) / kGemmBK;
   if (in.op == OP_GEMV) return (in.klen + kGemvRows - 1) / kGemvRows;
   if (in.op == OP_ATTN_PARTIAL) return 1;  // the key/value chunk
+  if (in.op == OP_ATTN_PREFILL) return (in.klen + kAttnKeyBlock - 1) / kAttnKeyBlock;
   return 0;
 }
 __device__ __forceinline__ int instr_index(const Params& p, int it) {
@@ -589,6 +592,41 @@ __device__ bool load_attn(const Params& p, Smem& s, const Instr& in, const Node&
   return true;
 }
 
+// Causal prefill attention, one (128-row query tile, query head) instruction: per 64-key block a
+// stage holds the query tile (16 KB), the block's keys (8 KB) and values (8 KB) of the head's
+// key/value head, all 128-byte swizzled. The query tile is fetched again with every block (from
+// L2) so each stage is self-contained. All three operands are produced inside the graph, so the
+// loads start once the sources are ready.
+__device__ bool load_attn_prefill(const Params& p, Smem& s, const Instr& in, const Node& nd,
+                                  int slot, uint32_t use, RingPos& rp, uint32_t& nfill, int idx) {
+  const uint32_t NS = ring_n(p);
+  const int nb = ring_stages(in);
+  if (nb == 0) return true;
+  if (!wait_warp(p, smem_u32(&s.deps_ready[slot]), use & 1u, R_LOAD, 28, idx)) return false;
+  if (elect_one()) fence_proxy_async_global();
+  __syncwarp();
+  const int h = in.n0, g = in.n0 / (nd.hq / nd.hkv);
+  const void* tq = tmap_at(p, nd.a.tmap);
+  const void* tk = tmap_at(p, nd.b.tmap);
+  const void* tv = tmap_at(p, nd.b2.tmap);
+  const uint32_t ring0 = smem_u32(s.ring), sb = stage_bytes(p);
+  for (int j = 0; j < nb; ++j) {
+    if (!wait_warp(p, smem_u32(&s.empty[rp.st]), rp.ph ^ 1u, R_LOAD, 29, idx)) return false;
+    if (elect_one()) {
+      const uint32_t bar = smem_u32(&s.full[rp.st]);
+      const uint32_t dst = ring0 + rp.st * sb;
+      mbar_expect_tx(bar, 32768u);
+      tma_load_2d(dst, tq, bar, h * 64, in.m0);
+      tma_load_2d(dst + 16384, tk, bar, g * 64, j * kAttnKeyBlock);
+      tma_load_2d(dst + 24576, tv, bar, g * 64, j * kAttnKeyBlock);
+    }
+    __syncwarp();
+    rp.next(NS);
+    ++nfill;
+  }
+  return true;
+}
+
 // L2 prefetch of the streamed operands of instructions already published to later slots: HBM
 // keeps streaming weights (and key/value chunks) while earlier instructions wait for their
 // activations; their shared-memory loads then hit L2. `next` is the first instruction not yet
@@ -659,6 +697,8 @@ __device__ void run_loader(const Params& p, Smem& s) {
       ok = load_gemv(p, s, in, nd, slot, use, rp, nfill, idx, it, pf_next);
     else if (in.op == OP_ATTN_PARTIAL)
       ok = load_attn(p, s, in, nd, slot, use, rp, nfill, idx);
+    else if (in.op == OP_ATTN_PREFILL)
+      ok = load_attn_prefill(p, s, in, nd, slot, use, rp, nfill, idx);
     if (!ok) break;
     if (elect_one()) mbar_arrive(smem_u32(&s.slot_free[slot]));
     __syncwarp();
@@ -732,6 +772,72 @@ __device__ __noinline__ int mma_tile(const Params& p, uint32_t full0, uint32_t e
   return nk;
 }
 
+// Prefill attention MMAs of one instruction: nb key blocks from ring position (st, ph). Block j:
+// S_j = Q K_j^T into TMEM S[n&1] (M = 128 query rows, N = 64 keys, K = 64 dims; the keys are a
+// K-major B operand), then, once the compute warps have written P_j (bf16, 128-byte swizzled,
+// K-major) to shared memory, O_j = P_j V_j into TMEM O[n&1] (N = 64 dims, K = 64 keys; the values
+// are an N-major B operand). S_{j+1} is issued before P_j is awaited, so the tensor pipe computes
+// the next scores while the softmax of the current block runs. A stage is released when O_j's
+// MMAs complete. `n` counts attention blocks on this SM: it gives every barrier's phase.
+// TMEM columns: S at 0 and 64, O at 128 and 192.
+__device__ __noinline__ bool mma_attn(const Params& p, Smem& s, uint32_t st, uint32_t ph,
+                                      uint32_t ns, int nb, uint32_t tmem, uint32_t& n, int idx) {
+  const uint32_t ring0 = smem_u32(s.ring), units = stage_bytes(p) >> 4;
+  const uint64_t qd = sdesc_sw128(ring0, 16, 1024);            // Q: 128 rows of 128 B
+  const uint64_t kd = sdesc_sw128(ring0 + 16384, 16, 1024);    // K: 64 rows of 128 B
+  const uint64_t vd = sdesc_sw128(ring0 + 24576, 8192, 1024);  // V: 64 rows of 128 B, N-major
+  const uint64_t pd = sdesc_sw128(smem_u32(s.xr), 16, 1024);   // P: 128 rows of 128 B
+  const uint32_t is = idesc_f16_bk(1, kAttnKeyBlock, kAttnTileQ), io = idesc_f16(1, 64, kAttnTileQ);
+  const uint32_t n0 = n;
+  RingPos rs, ro;
+  rs.st = ro.st = st;
+  rs.ph = ro.ph = ph;
+  auto issue_s = [&](int j) -> bool {
+    const uint32_t nn = n0 + (uint32_t)j, b = nn & 1u;
+    if (!wait_warp(p, smem_u32(&s.full[rs.st]), rs.ph, R_MMA, 23, idx)) return false;
+    if (!wait_warp(p, smem_u32(&s.att_s_free[b]), ((nn >> 1) & 1u) ^ 1u, R_MMA, 24, idx))
+      return false;
+    tc_fence_after();
+    const uint64_t so = (uint64_t)(rs.st * units);
+    if (elect_one()) {
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        tc_mma_f16(tmem + b * 64u, qd + so + (uint64_t)(kk * 2), kd + so + (uint64_t)(kk * 2), is,
+                   kk != 0);
+      tc_commit(smem_u32(&s.att_s_full[b]));
+    }
+    __syncwarp();
+    rs.next(ns);
+    return true;
+  };
+  if (!issue_s(0)) return false;
+  for (int j = 0; j < nb; ++j) {
+    if (j + 1 < nb && !issue_s(j + 1)) return false;
+    const uint32_t nn = n0 + (uint32_t)j, b = nn & 1u;
+    if (!wait_warp(p, smem_u32(&s.att_p_full), nn & 1u, R_MMA, 25, idx)) return false;
+    if (!wait_warp(p, smem_u32(&s.att_o_free[b]), ((nn >> 1) & 1u) ^ 1u, R_MMA, 26, idx))
+      return false;
+    tc_fence_after();
+    const uint64_t so = (uint64_t)(ro.st * units);
+    if (elect_one()) {
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        tc_mma_f16(tmem + 128u + b * 64u, pd + (uint64_t)(kk * 2), vd + so + (uint64_t)(kk * 128),
+                   io, kk != 0);
+      tc_commit(smem_u32(&s.att_o_full[b]));
+      tc_commit(smem_u32(&s.empty[ro.st]));
+    }
+    __syncwarp();
+    ro.next(ns);
+  }
+  // The compute warps have read every S and O block of this instruction before TMEM is reused.
+  const uint32_t nl = n0 + (uint32_t)nb - 1u;
+  if (!wait_warp(p, smem_u32(&s.att_o_free[nl & 1u]), (nl >> 1) & 1u, R_MMA, 27, idx))
+    return false;
+  n = n0 + (uint32_t)nb;
+  return true;
+}
+
 template <bool PAIR>
 __device__ void run_mma(const Params& p, Smem& s, uint32_t tmem) {
   // The whole warp runs this loop, converged: ring position, descriptors and flags are
@@ -747,7 +853,7 @@ __device__ void run_mma(const Params& p, Smem& s, uint32_t tmem) {
   // K slice is 16 rows of 128 B (128 units).
   const uint64_t bdesc0 = sdesc_sw128(ring0 + kGemmTileM * kGemmBK * 2, 8192, 1024);
   RingPos rp;
-  uint32_t acc_n = 0;
+  uint32_t acc_n = 0, att_n = 0;
   bool issued = false;
   const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
   for (int it = 0;; ++it) {
@@ -795,6 +901,27 @@ __device__ void run_mma(const Params& p, Smem& s, uint32_t tmem) {
         }
         __syncwarp();
         ++acc_n;
+      }
+    } else if (in.op == OP_ATTN_PREFILL) {
+      const int nb = ring_stages(in);
+      if (PAIR) {
+        report(p, MK_ERR_DEVICE_CHECK, idx, -1, in.op, 0, R_MMA, 35);  // refused by the host
+        break;
+      }
+      if (nb > 0) {
+        // TMEM columns 0..255 are reused: every GEMM epilogue still reading them is done first
+        bool w = true;
+        for (uint32_t k = 0; k < 2 && w; ++k)
+          w = wait_warp(p, smem_u32(&s.acc_empty[(acc_n + k) & 1u]),
+                        (((acc_n + k) >> 1) & 1u) ^ 1u, R_MMA, 21, idx);
+        if (!w) break;
+        tc_fence_after();
+        if (!mma_attn(p, s, rp.st, rp.ph, NS, nb, tmem, att_n, idx)) {
+          issued = true;
+          break;
+        }
+        issued = true;
+        rp.advance((uint32_t)nb, NS);
       }
     } else {
       rp.advance((uint32_t)ring_stages(in), NS);  // stages consumed by the compute warpgroup
@@ -1351,11 +1478,120 @@ __device__ void attn_reduce_body(const Instr& in, const Node& nd) {
   }
 }
 
+// Prefill attention, compute side: thread t of the warpgroup owns query row m0 + t (TMEM lane t).
+// Per key block j: S_j from TMEM, scaled to the log2 domain and masked (key beyond the causal
+// limit of the row or beyond the instruction's key range); online softmax with running max m and
+// sum l (flash attention: a block that raises the max rescales what came before by
+// 2^(m_old - m_new)); P_j = 2^(s - m) as bf16 into shared memory for the P V MMA; the previous
+// block's P V joins the fp32 output accumulator in registers once it completes. At the end the
+// row is divided by l and stored as bf16. `n` counts attention blocks on this SM, as in the MMA
+// warp.
+__device__ __noinline__ bool attn_prefill_body(const Params& p, Smem& s, const Instr& in,
+                                               const Node& nd, uint32_t tmem, uint32_t& n,
+                                               int idx) {
+  const int ct = (int)threadIdx.x - (kThreads - kCompute);
+  const int lane = ct & 31;
+  const uint32_t lanes = (uint32_t)((ct >> 5) * 32) << 16;  // this warp's TMEM lane quarter
+  const int nb = ring_stages(in);
+  const int row = in.m0 + ct;
+  const int qpos = nd.pos0 + row;
+  const int kmax = in.klen;
+  const float sl2 = nd.scale * 1.4426950408889634f;  // scores in log2 units
+  uint8_t* P = reinterpret_cast<uint8_t*>(s.xr);
+  float o[64];
+#pragma unroll
+  for (int i = 0; i < 64; ++i) o[i] = 0.f;
+  float m = -INFINITY, l = 0.f, alpha_prev = 1.f;
+  const uint32_t n0 = n;
+  auto add_o = [&](uint32_t nn, float alpha) -> bool {
+    const uint32_t b = nn & 1u;
+    if (!cw_wait(p, smem_u32(&s.att_o_full[b]), (nn >> 1) & 1u, 44, idx)) return false;
+    tc_fence_after();
+    uint32_t r0[32], r1[32];
+    tmem_ld32(tmem + 128u + b * 64u + lanes, r0);
+    tmem_ld32(tmem + 128u + b * 64u + 32u + lanes, r1);
+    tmem_ld_wait();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&s.att_o_free[b]));
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      o[i] = fmaf(o[i], alpha, __uint_as_float(r0[i]));
+      o[32 + i] = fmaf(o[32 + i], alpha, __uint_as_float(r1[i]));
+    }
+    return true;
+  };
+  for (int j = 0; j < nb; ++j) {
+    const uint32_t nn = n0 + (uint32_t)j, b = nn & 1u;
+    if (!cw_wait(p, smem_u32(&s.att_s_full[b]), (nn >> 1) & 1u, 43, idx)) return false;
+    tc_fence_after();
+    uint32_t r0[32], r1[32];
+    tmem_ld32(tmem + b * 64u + lanes, r0);
+    tmem_ld32(tmem + b * 64u + 32u + lanes, r1);
+    tmem_ld_wait();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&s.att_s_free[b]));
+    const int key0 = j * kAttnKeyBlock;
+    const int lim = nd.causal ? min(kmax, qpos + 1) : kmax;  // keys [0, lim) are visible
+    float mj = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < 64; ++c) {
+      const float x = __uint_as_float(c < 32 ? r0[c] : r1[c - 32]) * sl2;
+      const float v = key0 + c < lim ? x : -INFINITY;
+      if (c < 32) r0[c] = __float_as_uint(v); else r1[c - 32] = __float_as_uint(v);
+      mj = fmaxf(mj, v);
+    }
+    const float mn = fmaxf(m, mj);
+    const bool none = mn == -INFINITY;  // no visible key yet
+    const float alpha = none ? 1.f : exp2f(m - mn);
+    float ls = 0.f;
+    uint4 pk[8];
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch) {
+      float pv[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int c = ch * 8 + e;
+        const float v = __uint_as_float(c < 32 ? r0[c] : r1[c - 32]);
+        pv[e] = none ? 0.f : exp2f(v - mn);
+        ls += pv[e];
+      }
+      pk[ch] = pack8(pv, DT_BF16);
+    }
+    l = fmaf(l, alpha, ls);
+    m = mn;
+    // The previous block's P V (weighted with the previous maximum) joins the accumulator; after
+    // it completes the P buffer may be overwritten.
+    if (j > 0 && !add_o(nn - 1u, alpha_prev)) return false;
+    alpha_prev = alpha;
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch)
+      *reinterpret_cast<uint4*>(P + ct * 128 + ((ch ^ (ct & 7)) << 4)) = pk[ch];
+    fence_proxy_async_shared();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&s.att_p_full));
+  }
+  if (nb > 0 && !add_o(n0 + (uint32_t)nb - 1u, alpha_prev)) return false;
+  n = n0 + (uint32_t)nb;
+  if (row < nd.M) {
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch) {
+      float v[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[e] = o[ch * 8 + e] * inv;
+      store8(nd.out, row, in.n0 * 64 + ch * 8, DT_BF16, v);
+    }
+  }
+  return true;
+}
+
 template <bool PAIR>
 __device__ void run_compute(const Params& p, Smem& s, uint32_t tmem) {
   const uint32_t NS = ring_n(p);
   const int ct = (int)threadIdx.x - (kThreads - kCompute);
-  uint32_t ring = 0, acc_n = 0;
+  uint32_t ring = 0, acc_n = 0, att_n = 0;
   for (int it = 0;; ++it) {
     const int slot = it % kSlots;
     const uint32_t use = (uint32_t)(it / kSlots);
@@ -1381,6 +1617,12 @@ __device__ void run_compute(const Params& p, Smem& s, uint32_t tmem) {
         ok = cw_wait(p, smem_u32(&s.deps_ready[slot]), use & 1u, 33, idx);
         trace_mark(p, idx, 2);
         ok = ok && attn_partial_body(p, s, in, nd, ring, idx);
+        break;
+      case OP_ATTN_PREFILL:
+        // inputs reach this warpgroup only through the loader and the MMAs, which wait for them
+        trace_mark(p, idx, 2);
+        ok = attn_prefill_body(p, s, in, nd, tmem, att_n, idx);
+        ring += (uint32_t)ring_stages(in);
         break;
       default:
         ok = cw_wait(p, smem_u32(&s.deps_ready[slot]), use & 1u, 33, idx);
@@ -1440,6 +1682,13 @@ __global__ void __launch_bounds__(kThreads, 1) megakernel(const __grid_constant_
     }
     mbar_init(smem_u32(&s.drain), 1);
     mbar_init(smem_u32(&s.go), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&s.att_s_full[i]), 1);   // tcgen05.commit
+      mbar_init(smem_u32(&s.att_s_free[i]), 4);   // one lane per compute warp
+      mbar_init(smem_u32(&s.att_o_full[i]), 1);
+      mbar_init(smem_u32(&s.att_o_free[i]), 4);
+    }
+    mbar_init(smem_u32(&s.att_p_full), 4);
     mbar_fence_init();
   }
   if (warp == 2) {

@@ -100,6 +100,11 @@ __device__ __forceinline__ void tensormap_acquire(const void* tmap) {
   asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"((uint64_t)tmap)
                : "memory");
 }
+// Generic-proxy writes to shared memory by this thread become visible to the async proxy
+// (tensor-core operand reads, TMA stores) that later synchronisation orders after them.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
@@ -256,6 +261,10 @@ __device__ __forceinline__ uint32_t idesc_f16(int bf16, int n, int m = 128) {
   const uint32_t ab = bf16 ? 1u : 0u;
   return (1u << 4) | (ab << 7) | (ab << 10) | (0u << 15) | (1u << 16) |
          ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+// The same with B K-major (B^T stored row-major, e.g. the keys of S = Q K^T).
+__device__ __forceinline__ uint32_t idesc_f16_bk(int bf16, int n, int m = 128) {
+  return idesc_f16(bf16, n, m) & ~(1u << 16);
 }
 
 // True in exactly one lane of the (converged, full) warp.

@@ -175,8 +175,16 @@ mk_status check_kernel_support(const std::vector<TensorRec>& ts, const std::vect
           return MK_ERR_UNSUPPORTED;
         }
       if (ts[nd.a].rows > 1) {
-        set_error("mk_compile: causal prefill attention tiles are not built in this version");
-        return MK_ERR_UNSUPPORTED;
+        // prefill tiles: 128 query rows, 64-key blocks, single-CTA tensor-core MMAs (a CTA-pair
+        // launch issues every tcgen05 operation as a pair)
+        if (o.attn_tile_q != kAttnTileQ) {
+          set_error("mk_compile: prefill attention runs attn_tile_q %d", kAttnTileQ);
+          return MK_ERR_UNSUPPORTED;
+        }
+        if (o.cluster != 1) {
+          set_error("mk_compile: prefill attention needs cluster 1 (single-CTA tiles)");
+          return MK_ERR_UNSUPPORTED;
+        }
       }
     }
   }
@@ -383,6 +391,15 @@ static mk_status build_nodes(const mk_graph* g, mk_plan* p, std::vector<CUtensor
           mk_status st;
           if ((st = add_map(keys, maps, ts[nd.b], 64, n.tile_m, true, &n.b.tmap))) return st;
           if ((st = add_map(keys, maps, ts[nd.b2], 64, n.tile_m, true, &n.b2.tmap))) return st;
+        } else if (n.M > 0 && n.K > 0) {
+          // prefill: the query tile (64 columns of one head x 128 rows) and 64-key blocks of
+          // keys and values, all 128-byte swizzled
+          n.tile_m = kAttnKeyBlock;
+          mk_status st;
+          if ((st = add_map(keys, maps, ts[nd.a], 64, kAttnTileQ, true, &n.a.tmap))) return st;
+          if ((st = add_map(keys, maps, ts[nd.b], 64, kAttnKeyBlock, true, &n.b.tmap))) return st;
+          if ((st = add_map(keys, maps, ts[nd.b2], 64, kAttnKeyBlock, true, &n.b2.tmap)))
+            return st;
         }
         break;
     }

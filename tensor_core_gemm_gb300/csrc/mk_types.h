@@ -129,5 +129,7 @@ constexpr int kGemmTileM = 128;
 constexpr int kGemmBK = 64;            // K per stage for GEMM (128-byte rows of 16-bit elements)
 constexpr int kGemvRows = 64;          // K rows per stage for GEMV (x 256 columns = 32 KB)
 constexpr int kAttnChunkMax = 128;     // keys per split-KV partial handled by one instruction
+constexpr int kAttnTileQ = 128;        // query rows of one prefill attention instruction
+constexpr int kAttnKeyBlock = 64;      // keys per ring stage of prefill attention (Q + K + V = 32 KB)
 
 }  // namespace mk

@@ -469,3 +469,120 @@ def test_pair_options_rejected_by_the_kernel_check():
                 dict(gemm_tile_m=256, cluster=2, n_sm=151)):
         with pytest.raises(MkError):
             g.compile(**bad)
+
+
+# ------------------------------------------------------------------ causal prefill attention
+
+@pytest.mark.parametrize("tq,tk,hq,hkv,causal,pos0", [
+    (128, 128, 4, 2, True, 0), (200, 200, 8, 2, True, 0), (384, 384, 32, 8, True, 0),
+    (130, 300, 4, 4, False, 0), (64, 192, 4, 2, True, 128), (1, 64, 2, 1, True, 0)])
+def test_attention_prefill(tq, tk, hq, hkv, causal, pos0):
+    if tq == 1:
+        pytest.skip("a single query row lowers to split-KV decode tiles")
+    d = 64
+    q = synth.normal((tq, hq * d), 1.0, "bf16", 60 + tq, DEV)
+    k = synth.normal((tk, hkv * d), 1.0, "bf16", 61 + tk, DEV)
+    v = synth.normal((tk, hkv * d), 1.0, "bf16", 62, DEV)
+    out = torch.zeros((tq, hq * d), dtype=torch.bfloat16, device=DEV)
+    from tensor_core_gemm_gb300 import Graph
+    g = Graph()
+    iq, ik, iv, io = g.tensor(q), g.tensor(k), g.tensor(v), g.tensor(out)
+    g.attention(iq, ik, iv, io, n_q_heads=hq, n_kv_heads=hkv, head_dim=d, causal=causal,
+                q_pos0=pos0)
+    p = g.compile()
+    p.run()
+    p.check_status()
+    ref = ops.attention(f32(q), f32(k), f32(v), hq, hkv, d, causal, pos0, 1 / 8, BF16)
+    assert_close(f32(out), ref, f"prefill attention {tq}x{tk}")
+    if causal and pos0 == 0:
+        # row 0 sees key 0 alone: its output is v_0 of the head's key/value head, exactly
+        for h in range(hq):
+            gg = h // (hq // hkv)
+            assert torch.equal(out[0, h * d:(h + 1) * d], v[0, gg * d:(gg + 1) * d])
+    p.run()                                   # a second launch gives the same bytes
+    p.check_status()
+    again = out.clone()
+    p.run()
+    p.check_status()
+    assert torch.equal(out, again)
+
+
+def test_attention_prefill_refused_on_cta_pairs():
+    from tensor_core_gemm_gb300 import Graph
+    from tensor_core_gemm_gb300._lib import MkError
+    q = torch.zeros((128, 128), dtype=torch.bfloat16, device=DEV)
+    kv = torch.zeros((128, 64), dtype=torch.bfloat16, device=DEV)
+    g = Graph()
+    iq, ik, iv, io = g.tensor(q), g.tensor(kv), g.tensor(kv.clone()), g.tensor(q.clone())
+    g.attention(iq, ik, iv, io, n_q_heads=2, n_kv_heads=1, head_dim=64, causal=True)
+    with pytest.raises(MkError):
+        g.compile(gemm_tile_m=256, cluster=2)
+
+
+# ------------------------------------------------------------------ decoder, causal prefill
+
+def _prefill_weights(wl):
+    sh = wl.info["shape"]
+    L, d, f = sh.layers, sh.hidden, sh.ffn
+    D = wl.data
+    w = wl.info["w"]
+    return models.DecoderWeights(
+        f32(D[w["wqkv"]]).reshape(L, d, sh.qkv), f32(D[w["wo"]]).reshape(L, sh.hq * sh.hd, d),
+        f32(D[w["wg"]]).reshape(L, d, f), f32(D[w["wu"]]).reshape(L, d, f),
+        f32(D[w["wd"]]).reshape(L, f, d), f32(D[w["g_attn"]]), f32(D[w["g_mlp"]]),
+        sh.hq, sh.hkv, sh.hd, sh.eps, sh.theta)
+
+
+def check_prefill_per_node(wl, rows):
+    """Every node of every layer on query rows [0, rows) against the oracle applied to the GPU's
+    own inputs of that node (teacher forcing). Row t of every prefill output depends only on
+    rows 0..t, so a prefix of the rows is checked exactly by running the oracle on it."""
+    sh = wl.info["shape"]
+    wts = _prefill_weights(wl)
+    D, T = wl.data, wl.info["tokens"]
+    hq, hkv, hd = sh.hq, sh.hkv, sh.hd
+    L = sh.layers
+
+    def node(key):
+        return f32(D[wl.info[key]]).reshape(L, T, -1)[:, :rows]
+
+    xn, qkv, qr, kr, att, hh, hn, gu, xo = (node(k) for k in ("xn", "qkv", "qr", "kr", "att",
+                                                               "h", "hn", "gu", "out"))
+    pos = np.arange(rows)
+    x_prev = f32(D[0])[:rows]
+    for l in range(L):
+        assert_close(xn[l], ops.rmsnorm(x_prev, wts.g_attn[l], sh.eps, BF16), f"rmsnorm {l}")
+        assert_close(qkv[l], ops.matmul(xn[l], wts.wqkv[l], BF16), f"qkv {l}")
+        assert_close(qr[l], ops.rope(qkv[l][:, :hq * hd], pos, hq, hd, sh.theta, BF16),
+                     f"rope q {l}")
+        assert_close(kr[l], ops.rope(qkv[l][:, hq * hd:(hq + hkv) * hd], pos, hkv, hd, sh.theta,
+                                     BF16), f"rope k {l}")
+        v = qkv[l][:, (hq + hkv) * hd:]
+        assert_close(att[l], ops.attention(qr[l], kr[l], v, hq, hkv, hd, True, 0,
+                                           1 / math.sqrt(hd), BF16), f"attention {l}")
+        assert_close(hh[l], ops.matmul(att[l], wts.wo[l], BF16, residual=x_prev), f"o-proj {l}")
+        assert_close(hn[l], ops.rmsnorm(hh[l], wts.g_mlp[l], sh.eps, BF16), f"rmsnorm mlp {l}")
+        assert_close(gu[l], ops.matmul_silu_mul(hn[l], wts.wg[l], wts.wu[l], BF16),
+                     f"gate/up {l}")
+        assert_close(xo[l], ops.matmul(gu[l], wts.wd[l], BF16, residual=hh[l]), f"down {l}")
+        x_prev = xo[l]
+
+
+def test_prefill_small_decoder():
+    sh = workloads.DecoderShape(layers=2, hidden=256, n_q_heads=4, n_kv_heads=2, head_dim=64,
+                                ffn=512)
+    wl = workloads.prefill(sh, tokens=384, device=DEV, seed=7)
+    plan, _ = run(wl)
+    check_counters(plan, wl, {})
+    check_prefill_per_node(wl, 384)
+    # end to end against the oracle's own chain
+    ref = models.prefill(f32(wl.data[0]), _prefill_weights(wl))
+    got = f32(wl.data[wl.info["out"]]).reshape(2, 384, -1)[-1]
+    assert_close(got, ref, "prefill output")
+
+
+def test_prefill_full_config_causal_prefix():
+    wl = workloads.prefill(device=DEV, seed=0)
+    plan, _ = run(wl)
+    check_counters(plan, wl, {})
+    check_prefill_per_node(wl, 256)
