@@ -1534,31 +1534,33 @@ __device__ __noinline__ bool attn_prefill_body(const Params& p, Smem& s, const I
     if (lane == 0) mbar_arrive(smem_u32(&s.att_s_free[b]));
     const int key0 = j * kAttnKeyBlock;
     const int lim = nd.causal ? min(kmax, qpos + 1) : kmax;  // keys [0, lim) are visible
-    float mj = -INFINITY;
+    float sv[64];
 #pragma unroll
     for (int c = 0; c < 64; ++c) {
       const float x = __uint_as_float(c < 32 ? r0[c] : r1[c - 32]) * sl2;
-      const float v = key0 + c < lim ? x : -INFINITY;
-      if (c < 32) r0[c] = __float_as_uint(v); else r1[c - 32] = __float_as_uint(v);
-      mj = fmaxf(mj, v);
+      sv[c] = key0 + c < lim ? x : -INFINITY;
     }
+    float mx4[4] = {sv[0], sv[1], sv[2], sv[3]};
+#pragma unroll
+    for (int c = 4; c < 64; ++c) mx4[c & 3] = fmaxf(mx4[c & 3], sv[c]);
+    const float mj = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
     const float mn = fmaxf(m, mj);
     const bool none = mn == -INFINITY;  // no visible key yet
-    const float alpha = none ? 1.f : exp2f(m - mn);
-    float ls = 0.f;
+    const float alpha = none ? 1.f : ex2(m - mn);
+    const float mo = none ? 0.f : mn;   // masked scores give 2^-inf = 0 either way
+    float ls4[4] = {0.f, 0.f, 0.f, 0.f};
     uint4 pk[8];
 #pragma unroll
     for (int ch = 0; ch < 8; ++ch) {
       float pv[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const int c = ch * 8 + e;
-        const float v = __uint_as_float(c < 32 ? r0[c] : r1[c - 32]);
-        pv[e] = none ? 0.f : exp2f(v - mn);
-        ls += pv[e];
+        pv[e] = ex2(sv[ch * 8 + e] - mo);
+        ls4[e & 3] += pv[e];
       }
       pk[ch] = pack8(pv, DT_BF16);
     }
+    const float ls = (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
     l = fmaf(l, alpha, ls);
     m = mn;
     // The previous block's P V (weighted with the previous maximum) joins the accumulator; after

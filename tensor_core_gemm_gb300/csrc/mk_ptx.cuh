@@ -278,6 +278,13 @@ __device__ __forceinline__ bool elect_one() {
   return e != 0;
 }
 
+// 2^x by the special-function unit (PTX ex2.approx; flushes denormal results to zero).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ---------------------------------------------------------------- global counters
 __device__ __forceinline__ int ld_acquire(const int* p) {
   int v;
