@@ -965,8 +965,18 @@ __device__ bool gemm_epilogue(const Params& p, Smem& s, const Instr& in, const N
              res = (nd.flags & EPI_RESIDUAL) != 0;
   const int tn = nd.tile_n;
   const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
-  const int row = in.m0 + (int)rank * kGemmTileM + q * 32 + lane;
+  const int row0 = in.m0 + (int)rank * kGemmTileM + q * 32;  // this warp's 32 rows
+  const int row = row0 + lane;
   const uint32_t tb = tmem + as * 256u + ((uint32_t)(q * 32) << 16);
+  // Each warp stages its 32 x 32 block of a chunk in one of two 2 KB buffers (64-byte rows,
+  // 64-byte swizzle: 16-byte chunk j of row r at j ^ ((r >> 1) & 3), conflict-free) and one lane
+  // stores it with TMA; a buffer is rewritten once the store issued from it has read it.
+  const uint32_t xr0 = smem_u32(s.xr) + (uint32_t)q * 4096u;
+  if (nd.out.tmap < 0) {  // the host builds the output map of every GEMM node
+    if (ct == 0) report(p, MK_ERR_DEVICE_CHECK, idx, -1, nd.out.tmap, 0, R_COMPUTE, 36);
+    return false;
+  }
+  const void* omap = tmap_at(p, nd.out.tmap);
   for (int c = 0; c < tn; c += 32) {
     uint32_t r[32], r2[32];
     if (nk > 0) {
@@ -977,36 +987,54 @@ __device__ bool gemm_epilogue(const Params& p, Smem& s, const Instr& in, const N
 #pragma unroll
       for (int i = 0; i < 32; ++i) r[i] = r2[i] = 0u;
     }
-    if (row < nd.M) {
-#pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        const int col = in.n0 + c + g * 8;
-        if (col >= nd.N) continue;
-        float v[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          v[e] = __uint_as_float(r[g * 8 + e]);
-          if (dual) v[e] = silu(v[e]) * __uint_as_float(r2[g * 8 + e]);
-        }
-        if (bias) {
-          float b[8];
-          load8(nd.bias, row, col, dt, b);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) v[e] += b[e];
-        }
-        if (relu) {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) v[e] = fmaxf(v[e], 0.0f);
-        }
-        if (res) {
-          float b[8];
-          load8(nd.res, row, col, dt, b);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) v[e] += b[e];
-        }
-        store8(nd.out, row, col, dt, v);
-      }
+    const uint32_t buf = xr0 + (uint32_t)((c >> 5) & 1) * 2048u;
+    if (c >= 64) {
+      if (lane == 0) bulk_wait_read_1();
+      __syncwarp();
     }
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const int col = in.n0 + c + g * 8;
+      const bool inside = row < nd.M && col < nd.N;
+      float v[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        v[e] = __uint_as_float(r[g * 8 + e]);
+        if (dual) v[e] = silu(v[e]) * __uint_as_float(r2[g * 8 + e]);
+      }
+      if (bias && inside) {
+        float b[8];
+        load8(nd.bias, row, col, dt, b);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] += b[e];
+      }
+      if (relu) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = fmaxf(v[e], 0.0f);
+      }
+      if (res && inside) {
+        float b[8];
+        load8(nd.res, row, col, dt, b);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] += b[e];
+      }
+      const uint4 pk = pack8(v, dt);
+      const uint32_t dst = buf + (uint32_t)lane * 64u + (uint32_t)((g ^ ((lane >> 1) & 3)) << 4);
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(pk.x), "r"(pk.y),
+                   "r"(pk.z), "r"(pk.w)
+                   : "memory");
+    }
+    fence_proxy_async_shared();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(omap, buf, in.n0 + c, row0);
+      bulk_commit();
+    }
+  }
+  // the tile's stores are in global memory before its counters are released
+  if (lane == 0) {
+    bulk_wait_all();
+    fence_proxy_async_global();
   }
   if (nk > 0) {
     tc_fence_before();

@@ -89,6 +89,26 @@ __device__ __forceinline__ void tma_prefetch_l2_3d(const void* tmap, int x, int 
                "r"(x), "r"(y), "r"(z)
                : "memory");
 }
+// 2D tiled store shared -> global (bulk async-group completion); coordinates innermost first.
+// Parts of the box outside the tensor are not written.
+__device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+          (uint64_t)tmap),
+      "r"(x), "r"(y), "r"(src)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// This thread's bulk stores, all but the most recent group: done reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+// This thread's bulk stores: complete (written to global memory).
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
 // Fetch a tile into L2 only (no shared-memory destination, no completion signal).
 __device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int x, int y) {
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(

@@ -222,11 +222,12 @@ struct MapKey {
 // panel), strides (row pitch, 128 bytes), box (64, box_r, panels). One copy through it writes
 // `panels` consecutive 64-column atoms, each box_r rows of 128 bytes, the same bytes and layout
 // as `panels` 2D copies of 64 x box_r boxes.
+// swz: shared-memory swizzle span in bytes (0, 64 or 128; true = 128).
 static mk_status add_map(std::vector<MapKey>& keys, std::vector<CUtensorMap>& maps,
-                         const TensorRec& t, int box_c, int box_r, bool swizzle128, int* idx,
+                         const TensorRec& t, int box_c, int box_r, int swz, int* idx,
                          int panels = 0) {
-  MapKey k{(uintptr_t)t.ptr, t.rows, t.cols, t.ld, t.dtype, box_c, box_r, swizzle128 ? 1 : 0,
-           panels};
+  if (swz == 1) swz = 128;
+  MapKey k{(uintptr_t)t.ptr, t.rows, t.cols, t.ld, t.dtype, box_c, box_r, swz, panels};
   for (size_t i = 0; i < keys.size(); ++i)
     if (keys[i] == k) {
       *idx = (int)i;
@@ -260,7 +261,9 @@ static mk_status add_map(std::vector<MapKey>& keys, std::vector<CUtensorMap>& ma
   CUresult r = fn(&m, t.dtype == DT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                          : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                   rank, t.ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  swz == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                  : swz == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                              : CU_TENSOR_MAP_SWIZZLE_NONE,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     set_error("mk_compile: cuTensorMapEncodeTiled failed (%d) for a %lldx%lld tensor, box %dx%d, "
@@ -324,6 +327,12 @@ static mk_status build_nodes(const mk_graph* g, mk_plan* p, std::vector<CUtensor
         const bool gemv = A.rows <= p->opts.gemv_max_m;
         n.kind = gemv ? OP_GEMV : OP_GEMM;
         if (gemv) n.ldp = n.M * n.N * ((nd.flags & MK_EPI_SILU_MUL) ? 2 : 1);
+        if (!gemv && n.M > 0 && n.N > 0) {
+          // GEMM tiles store through TMA in 32 x 32 blocks (one per compute warp), 64-byte
+          // swizzled; K = 0 tiles too (they store the epilogue of zero)
+          mk_status st;
+          if ((st = add_map(keys, maps, ts[nd.out], 32, 32, 64, &n.out.tmap))) return st;
+        }
         if (n.M > 0 && n.N > 0 && n.K > 0) {
           mk_status st;
           // B (and b2) move as 64-column panels of 64 rows, 128-byte swizzled: one 3D copy
