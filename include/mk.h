@@ -167,6 +167,10 @@ typedef struct {
   int32_t trace;         /* 1: record per-instruction timestamps for mk_get_trace */
   int32_t l2_prefetch;   /* instructions (current included, <= 8) whose streamed operands the
                             loader prefetches into L2 ahead of use; 0 = off */
+  int32_t gemm_split_tail; /* 1: the GEMM tiles of a matmul's last, partly filled wave are
+                            split along K, the last split to finish sums the fp32 partials
+                            and runs the epilogue; 0 (default): never split. Measured slower
+                            on the 4096^3 GEMM: the last split's sum is latency-bound */
 } mk_compile_opts;
 
 /* Fill *o with the defaults (the values listed above for each field). */

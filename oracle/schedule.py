@@ -28,6 +28,14 @@ Lowering rules per node (tile sizes come from ``opts``; see ``DEFAULT_OPTS``):
       weight "b2" for SiLU·mul), row-major over (mt, nt), each tile repeated ``cluster`` times
       (aux0 = rank). Reads A rows×[0,K), B [0,K)×cols (and b2), bias/residual on the tile box;
       writes the tile box (every instruction of a cluster writes the whole cluster tile).
+      Split tail (gemm_split_tail = 1; default 0): with T tiles on U = n_sm div cluster units, the last
+      R = T mod U tiles fill a fraction of the last wave. When S = min(U div R, ceil(K/64)) >= 2,
+      each of those R tiles is split along K: chunk = ceil(ceil(K/64) / S)·64, splits
+      ceil(K/chunk); order: tile, then split, then rank; k0/klen = the split's K range, aux0 =
+      rank, aux1 = number of splits. A split reads A and B on its K range, bias/residual on the
+      tile box; only split 0 carries the output box; every split carries split 0's arrivals (of
+      the same rank), because the last split to finish sums the partials and publishes. Each
+      (tile, rank) owns one split semaphore.
   matmul, M <= gemv_max_m -> GEMV tiles: column tiles of gemv_tile_n (halved with b2), each
       split along K into S chunks (gemv_splits, or max(1, n_sm div n_col_tiles) when 0); the
       chunk length is ceil(K/S) rounded up to gemv_kstep (at least gemv_kstep) and S is then
@@ -68,7 +76,7 @@ FLAG_B_DEP = 1
 ROLE_A, ROLE_B, ROLE_E = 0, 1, 2
 
 DEFAULT_OPTS = dict(
-    gemm_tile_m=128, gemm_tile_n=256, cluster=1,
+    gemm_tile_m=128, gemm_tile_n=256, cluster=1, gemm_split_tail=0,
     ew_rows=128, ew_cols=128, ew_tiles=1,
     norm_rows=16,
     gemv_max_m=8, gemv_tile_n=256, gemv_splits=0, gemv_kstep=64,
@@ -153,18 +161,36 @@ def _lower_matmul(ni, nd, opts, phases, sem_tiles):
     else:
         tm = opts["gemm_tile_m"]
         tn = opts["gemm_tile_n"] // 2 if b2 is not None else opts["gemm_tile_n"]
-        for mt in range(cdiv(m, tm)):
-            for nt in range(cdiv(n, tn)):
-                m0, n0 = mt * tm, nt * tn
-                for r in range(opts["cluster"]):
-                    ins = Instr(OP_GEMM, ni, m0, n0, 0, k, r, 0)
-                    ins.reads.append((_box(a, m0, m0 + tm, 0, k), ROLE_A))
-                    ins.reads.append((_box(b, 0, k, n0, n0 + tn), ROLE_B))
+        cl = opts["cluster"]
+        nnt = cdiv(n, tn)
+        t_all = cdiv(m, tm) * nnt
+        units = opts["n_sm"] // cl
+        nks = cdiv(k, 64)
+        r_tail = t_all % units if units > 0 else 0
+        n_split = min(units // r_tail, nks) if (opts["gemm_split_tail"] and r_tail) else 1
+        split_from = t_all - r_tail if n_split >= 2 else t_all
+        for t in range(t_all):
+            m0, n0 = (t // nnt) * tm, (t % nnt) * tn
+            if t < split_from:
+                ranges, base = [(0, k)], None
+            else:
+                chunk = cdiv(nks, n_split) * 64
+                ranges = [(k0, min(chunk, k - k0)) for k0 in range(0, k, chunk)]
+                base = len(sem_tiles)
+                sem_tiles.extend([base] * cl)
+            for si, (k0, kl) in enumerate(ranges):
+                for r in range(cl):
+                    ins = Instr(OP_GEMM, ni, m0, n0, k0, kl, r, 0 if base is None else len(ranges))
+                    if base is not None:
+                        ins.tile = base + r
+                    ins.reads.append((_box(a, m0, m0 + tm, k0, k0 + kl), ROLE_A))
+                    ins.reads.append((_box(b, k0, k0 + kl, n0, n0 + tn), ROLE_B))
                     if b2 is not None:
-                        ins.reads.append((_box(b2, 0, k, n0, n0 + tn), ROLE_B))
+                        ins.reads.append((_box(b2, k0, k0 + kl, n0, n0 + tn), ROLE_B))
                     for ref, _ in epi:
                         ins.reads.append((_box(ref, m0, m0 + tm, n0, n0 + tn), ROLE_E))
-                    ins.writes.append(_box(c, m0, m0 + tm, n0, n0 + tn))
+                    if si == 0:
+                        ins.writes.append(_box(c, m0, m0 + tm, n0, n0 + tn))
                     out.append(ins)
     phases.append(out)
 
@@ -279,7 +305,7 @@ class Plan:
         tile's split semaphore counts its splits."""
         sems = [0] * self.n_sem
         for ins in self.instrs:
-            if ins.op == OP_GEMV:
+            if ins.op == OP_GEMV or (ins.op == OP_GEMM and ins.aux1 > 0):
                 sems[ins.sem - self.n_dep] += 1
         return list(self.targets) + sems
 
@@ -362,14 +388,17 @@ def lower(graph, opts):
             instrs[p].dst.append(cid)
     n_dep = len(targets)
 
-    # GEMV tiles: every split publishes with split 0's arrivals and shares one semaphore.
+    # Split tiles (GEMV, and GEMM split tails per rank): every split publishes with split 0's
+    # arrivals and shares one semaphore.
+    def split(ins):
+        return ins.op == OP_GEMV or (ins.op == OP_GEMM and ins.aux1 > 0)
+
     first = {}
     for ins in instrs:
-        if ins.op == OP_GEMV:
-            if ins.aux0 == 0:
-                first[ins.tile] = ins
+        if split(ins) and ins.k0 == 0:
+            first[ins.tile] = ins
     for ins in instrs:
-        if ins.op == OP_GEMV:
+        if split(ins):
             ins.dst = list(first[ins.tile].dst)
             ins.sem = n_dep + ins.tile
     return Plan(instrs, targets, n_dep, o["n_sm"], len(sem_tiles))
@@ -377,12 +406,14 @@ def lower(graph, opts):
 
 def topologically_valid(plan):
     """Every counter a consumer waits on is fed only by lower-index instructions, and every
-    counter's target equals the number of distinct instructions that arrive on it (split
-    copies of a GEMV tile count once). With placement i -> (i mod S, i div S) this is the
-    deadlock-freedom argument of "MegaKittens Internals" §11."""
+    counter's target equals the number of distinct instructions that arrive on it (the splits
+    of a GEMV tile, or of a split-tail GEMM tile's rank, count once: whichever finishes last
+    arrives). With placement i -> (i mod S, i div S) this is the deadlock-freedom argument of
+    "MegaKittens Internals" §11."""
     feeders = {}
     for i, ins in enumerate(plan.instrs):
-        key = ins.tile if ins.op == OP_GEMV else ("i", i)
+        split = ins.op == OP_GEMV or (ins.op == OP_GEMM and ins.aux1 > 0)
+        key = ("t", ins.tile) if split else ("i", i)
         for cid in ins.dst:
             feeders.setdefault(cid, {})
             feeders[cid].setdefault(key, []).append(i)

@@ -15,7 +15,7 @@ INSTR_DTYPE = np.dtype([
     ("op", "<u2"), ("flags", "<u2"), ("node", "<i4"), ("m0", "<i4"), ("n0", "<i4"),
     ("k0", "<i4"), ("klen", "<i4"), ("aux0", "<i4"), ("aux1", "<i4"), ("sem", "<i4"),
     ("n_src", "<i4"), ("src_off", "<i4"), ("n_dst", "<i4"), ("dst_off", "<i4"),
-    ("pad", "<i4", (3,)),
+    ("slot", "<i4"), ("split", "<i4"), ("pad", "<i4"),
 ])
 assert INSTR_DTYPE.itemsize == 64
 

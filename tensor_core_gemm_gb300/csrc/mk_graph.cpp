@@ -106,24 +106,53 @@ static void lower_matmul(const std::vector<TensorRec>& ts, int ni, const NodeRec
   } else {
     const int64_t tm = o.gemm_tile_m;
     const int64_t tn = dual ? o.gemm_tile_n / 2 : o.gemm_tile_n;
+    const int cl = o.cluster;
     plan->node_tile_n[ni] = (int)tn;
-    for (int64_t mt = 0; mt < cdiv(m, tm); ++mt) {
-      for (int64_t nt = 0; nt < cdiv(n, tn); ++nt) {
-        const int64_t m0 = mt * tm, n0 = nt * tn;
-        for (int r = 0; r < o.cluster; ++r) {
-          HInstr h = make(OP_GEMM, ni, (int)m0, (int)n0, 0, (int)k, r, 0);
-          h.reads.push_back({window(ts, nd.a, m0, m0 + tm, 0, k), ROLE_A});
-          h.reads.push_back({window(ts, nd.b, 0, k, n0, n0 + tn), ROLE_B});
-          if (dual) h.reads.push_back({window(ts, nd.b2, 0, k, n0, n0 + tn), ROLE_B});
+    // Split tail: the tiles of the last, partly filled wave (T mod units) are split along K
+    // when at least two splits fit per tile; the last split to finish sums the partials.
+    const int64_t nnt = cdiv(n, tn), t_all = cdiv(m, tm) * nnt;
+    const int64_t units = o.n_sm / cl, nks = cdiv(k, kGemmBK);
+    const int64_t r_tail = units > 0 ? t_all % units : 0;
+    const int64_t n_split =
+        (o.gemm_split_tail && r_tail) ? std::min<int64_t>(units / r_tail, nks) : 1;
+    const int64_t split_from = n_split >= 2 ? t_all - r_tail : t_all;
+    const int64_t chunk = n_split >= 2 ? cdiv(nks, n_split) * kGemmBK : k;
+    const int64_t n_ranges = n_split >= 2 ? cdiv(k, chunk) : 1;
+    int slots = 0;
+    for (int64_t t = 0; t < t_all; ++t) {
+      const int64_t m0 = (t / nnt) * tm, n0 = (t % nnt) * tn;
+      const bool split = t >= split_from;
+      const int64_t nr = split ? n_ranges : 1;
+      int base = -1, slot0 = 0;
+      if (split) {
+        base = n_tiles_sem;
+        n_tiles_sem += cl;
+        slot0 = slots;
+        slots += (int)nr * cl;
+      }
+      for (int64_t si = 0; si < nr; ++si) {
+        const int64_t k0 = split ? si * chunk : 0, kl = split ? std::min(chunk, k - k0) : k;
+        for (int r = 0; r < cl; ++r) {
+          HInstr h = make(OP_GEMM, ni, (int)m0, (int)n0, (int)k0, (int)kl, r,
+                          split ? (int)nr : 0);
+          if (split) {
+            h.tile = base + r;
+            h.rec.slot = slot0 + r;
+            h.rec.split = (int)si;
+          }
+          h.reads.push_back({window(ts, nd.a, m0, m0 + tm, k0, k0 + kl), ROLE_A});
+          h.reads.push_back({window(ts, nd.b, k0, k0 + kl, n0, n0 + tn), ROLE_B});
+          if (dual) h.reads.push_back({window(ts, nd.b2, k0, k0 + kl, n0, n0 + tn), ROLE_B});
           if (nd.bias >= 0)
             h.reads.push_back({window(ts, nd.bias, m0, m0 + tm, n0, n0 + tn), ROLE_E});
           if (nd.res >= 0)
             h.reads.push_back({window(ts, nd.res, m0, m0 + tm, n0, n0 + tn), ROLE_E});
-          h.writes.push_back(window(ts, nd.out, m0, m0 + tm, n0, n0 + tn));
+          if (si == 0) h.writes.push_back(window(ts, nd.out, m0, m0 + tm, n0, n0 + tn));
           out.push_back(std::move(h));
         }
       }
     }
+    plan->node_gsplit_slots[ni] = slots;
   }
   phases.push_back(std::move(out));
 }
@@ -240,6 +269,7 @@ mk_status lower_graph(const std::vector<TensorRec>& tensors_in, const std::vecto
   plan->node_splits.assign(nn, 0);
   plan->node_chunks.assign(nn, 0);
   plan->node_tile_n.assign(nn, 0);
+  plan->node_gsplit_slots.assign(nn, 0);
   std::vector<std::vector<HInstr>> phases;
   int n_tiles_sem = 0;
   for (int ni = 0; ni < nn; ++ni) {
@@ -321,13 +351,17 @@ mk_status lower_graph(const std::vector<TensorRec>& tensors_in, const std::vecto
     for (int p : members[cid]) ins[p].dst.push_back((int)cid);
   const int n_dep = (int)targets.size();
 
-  // GEMV tiles publish through whichever split finishes last: all splits carry split 0's
-  // arrivals and share one semaphore, numbered after the dependency counters.
+  // Split tiles (GEMV tiles, GEMM split tails per rank) publish through whichever split finishes
+  // last: all splits carry split 0's arrivals and share one semaphore, numbered after the
+  // dependency counters.
+  auto is_split = [](const HInstr& h) {
+    return h.rec.op == OP_GEMV || (h.rec.op == OP_GEMM && h.rec.aux1 > 0);
+  };
   std::vector<int> first_of_tile(n_tiles_sem, -1);
   for (size_t i = 0; i < ins.size(); ++i)
-    if (ins[i].rec.op == OP_GEMV && ins[i].rec.aux0 == 0) first_of_tile[ins[i].tile] = (int)i;
+    if (is_split(ins[i]) && ins[i].rec.k0 == 0) first_of_tile[ins[i].tile] = (int)i;
   for (auto& h : ins) {
-    if (h.rec.op != OP_GEMV) continue;
+    if (!is_split(h)) continue;
     h.dst = ins[first_of_tile[h.tile]].dst;
     h.rec.sem = n_dep + h.tile;
   }
@@ -668,5 +702,6 @@ extern "C" mk_status mk_default_opts(mk_compile_opts* o) {
   o->snapshot_counters = 0;
   o->trace = 0;
   o->l2_prefetch = 0;
+  o->gemm_split_tail = 0;
   return MK_OK;
 }

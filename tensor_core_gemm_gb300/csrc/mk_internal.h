@@ -55,7 +55,7 @@ struct HInstr {
   Instr rec{};
   std::vector<std::pair<Box, int>> reads;  // (box, role)
   std::vector<Box> writes;
-  int tile = -1;  // GEMV tile ordinal
+  int tile = -1;  // split semaphore ordinal (GEMV tile, or GEMM split-tail tile and rank)
   std::vector<std::pair<int, int>> src;
   std::vector<int> dst;
 };
@@ -72,6 +72,7 @@ struct HostPlan {
   std::vector<int> node_splits;            // per node: GEMV K splits (0 otherwise)
   std::vector<int> node_chunks;            // per node: attention decode chunks (0 otherwise)
   std::vector<int> node_tile_n;            // per node: output columns per tile
+  std::vector<int> node_gsplit_slots;      // per node: fp32 partial slots of GEMM split tails
 };
 
 void set_error(const char* fmt, ...);

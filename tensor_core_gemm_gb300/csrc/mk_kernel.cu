@@ -453,11 +453,16 @@ __device__ __noinline__ bool load_tile(const Params& p, const LoadTile& tp, uint
   return true;
 }
 
+// Pair-mode ring sync: `synced` holds while every instruction since the last resync was a pair
+// GEMM (all roles of both CTAs see the same instruction kinds per iteration, so they agree). Then
+// both CTAs consumed the same stages from the same position and every stage's last use was a pair
+// MMA that released it in both CTAs: the next pair GEMM streams straight on. Otherwise it resyncs.
 template <bool PAIR>
 __device__ bool load_gemm(const Params& p, Smem& s, const Instr& in, const Node& nd, int slot,
-                          uint32_t use, RingPos& rp, uint32_t& nfill, uint32_t& go_par, int idx) {
+                          uint32_t use, RingPos& rp, uint32_t& nfill, uint32_t& go_par,
+                          bool& synced, int idx) {
   const uint32_t NS = ring_n(p);
-  if (PAIR) {
+  if (PAIR && !synced) {
     while (rp.st != 0) {
       if (!wait_warp(p, smem_u32(&s.empty[rp.st]), rp.ph ^ 1u, R_LOAD, 18, idx)) return false;
       if (elect_one()) {
@@ -472,17 +477,16 @@ __device__ bool load_gemm(const Params& p, Smem& s, const Instr& in, const Node&
   const int nk = ring_stages(in);
   if (nk == 0) return true;
   const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
-  if (PAIR) {
-    // Between pair GEMMs the two CTAs use their rings for different instructions, so the odd
-    // CTA's bytes must not reach the even CTA's full barriers while one of them still carries
-    // an earlier load. The even CTA waits until the stages of the first pass are free (every
-    // earlier use of them consumed), then releases the odd CTA once per GEMM. Later stages need
-    // no handshake: the odd CTA reuses a stage only after the pair MMA that read it committed,
-    // which is after the even CTA's barrier for it completed. Bytes that land before the even
-    // CTA's expect_tx leave the transaction count negative until it arrives.
-    const int first = nk < (int)NS ? nk : (int)NS;
+  if (PAIR && !synced) {
+    // After other instructions the two CTAs' rings differ, so the odd CTA's bytes must not reach
+    // the even CTA's full barriers while one of them still carries an earlier load. The even CTA
+    // waits until every stage of the pass is free (every earlier use consumed), then releases the
+    // odd CTA once. Later stages need no handshake: the odd CTA reuses a stage only after the
+    // pair MMA that read it committed, which is after the even CTA's barrier for it completed.
+    // Bytes that land before the even CTA's expect_tx leave the transaction count negative
+    // until it arrives.
     if (rank == 0) {
-      for (int j = 0; j < first; ++j)
+      for (int j = 0; j < (int)NS; ++j)
         if (!wait_warp(p, smem_u32(&s.empty[j]), rp.ph ^ 1u, R_LOAD, 17, idx)) return false;
       if (elect_one()) mbar_arrive_cluster(mapa_shared(smem_u32(&s.go), 1));
       __syncwarp();
@@ -491,6 +495,7 @@ __device__ bool load_gemm(const Params& p, Smem& s, const Instr& in, const Node&
       go_par ^= 1u;
     }
   }
+  synced = true;
   const bool dual = (nd.flags & EPI_SILU_MUL) != 0;
   const bool panel = (nd.flags & NF_B_PANELS) != 0;
   const int tn = nd.tile_n;
@@ -680,6 +685,7 @@ __device__ void run_loader(const Params& p, Smem& s) {
   for (int i = 0; i < p.n_tmaps; ++i) tensormap_acquire(tmap_at(p, i));
   RingPos rp;
   uint32_t nfill = 0, go_par = 0;
+  bool synced = true;  // pair-mode ring sync (see load_gemm)
   int pf_next = 0;
   for (int it = 0;; ++it) {
     const int slot = it % kSlots;
@@ -691,8 +697,9 @@ __device__ void run_loader(const Params& p, Smem& s) {
     const Node& nd = slot_node(s, slot);
     prefetch_ahead(p, s, it, pf_next);
     bool ok = true;
+    if (in.op != OP_GEMM) synced = false;
     if (in.op == OP_GEMM)
-      ok = load_gemm<PAIR>(p, s, in, nd, slot, use, rp, nfill, go_par, idx);
+      ok = load_gemm<PAIR>(p, s, in, nd, slot, use, rp, nfill, go_par, synced, idx);
     else if (in.op == OP_GEMV)
       ok = load_gemv(p, s, in, nd, slot, use, rp, nfill, idx, it, pf_next);
     else if (in.op == OP_ATTN_PARTIAL)
@@ -854,7 +861,7 @@ __device__ void run_mma(const Params& p, Smem& s, uint32_t tmem) {
   const uint64_t bdesc0 = sdesc_sw128(ring0 + kGemmTileM * kGemmBK * 2, 8192, 1024);
   RingPos rp;
   uint32_t acc_n = 0, att_n = 0;
-  bool issued = false;
+  bool issued = false, synced = true;
   const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
   for (int it = 0;; ++it) {
     const int slot = it % kSlots;
@@ -866,8 +873,9 @@ __device__ void run_mma(const Params& p, Smem& s, uint32_t tmem) {
     const Node& nd = slot_node(s, slot);
     bool ok = true;
     if (in.op == OP_GEMM) {
-      if (PAIR) rp.align();
       const int nk = ring_stages(in);
+      if (PAIR && !synced) rp.align();  // mirrors the loader's ring sync
+      if (nk > 0) synced = true;
       if (nk > 0 && PAIR && rank != 0) {
         rp.advance((uint32_t)nk, NS);  // the even CTA issues the pair's MMAs
         ++acc_n;
@@ -903,6 +911,7 @@ __device__ void run_mma(const Params& p, Smem& s, uint32_t tmem) {
         ++acc_n;
       }
     } else if (in.op == OP_ATTN_PREFILL) {
+      synced = false;
       const int nb = ring_stages(in);
       if (PAIR) {
         report(p, MK_ERR_DEVICE_CHECK, idx, -1, in.op, 0, R_MMA, 35);  // refused by the host
@@ -924,6 +933,7 @@ __device__ void run_mma(const Params& p, Smem& s, uint32_t tmem) {
         rp.advance((uint32_t)nb, NS);
       }
     } else {
+      synced = false;
       rp.advance((uint32_t)ring_stages(in), NS);  // stages consumed by the compute warpgroup
     }
     if (elect_one()) mbar_arrive(smem_u32(&s.slot_free[slot]));
@@ -944,11 +954,15 @@ __device__ void run_mma(const Params& p, Smem& s, uint32_t tmem) {
 
 // ------------------------------------------------------------------ compute warpgroup bodies
 
-// GEMM epilogue: TMEM -> registers (one row per thread), fused epilogue, 16-byte stores. In pair
-// mode each CTA drains its own 128 rows of the 256-row tile.
+// GEMM epilogue: TMEM -> registers (one row per thread), fused epilogue, then per 32-column chunk
+// a 32 x 32 block per warp staged in shared memory and stored with TMA. In pair mode each CTA
+// drains its own 128 rows of the 256-row tile. A split-tail tile (aux1 = number of K splits)
+// first writes its fp32 partial to scratch and releases TMEM; the last split to finish (tile
+// semaphore) sums the partials in split order and runs the epilogue; the others do not publish.
 template <bool PAIR>
 __device__ bool gemm_epilogue(const Params& p, Smem& s, const Instr& in, const Node& nd, int slot,
-                              uint32_t use, uint32_t tmem, uint32_t& acc_n, int idx) {
+                              uint32_t use, uint32_t tmem, uint32_t& acc_n, bool* publish,
+                              int idx) {
   const int ct = (int)threadIdx.x - (kThreads - kCompute);
   const int q = ct >> 5, lane = ct & 31;
   if (!cw_wait(p, smem_u32(&s.deps_ready[slot]), use & 1u, 30, idx)) return false;
@@ -968,25 +982,29 @@ __device__ bool gemm_epilogue(const Params& p, Smem& s, const Instr& in, const N
   const int row0 = in.m0 + (int)rank * kGemmTileM + q * 32;  // this warp's 32 rows
   const int row = row0 + lane;
   const uint32_t tb = tmem + as * 256u + ((uint32_t)(q * 32) << 16);
-  // Each warp stages its 32 x 32 block of a chunk in one of two 2 KB buffers (64-byte rows,
-  // 64-byte swizzle: 16-byte chunk j of row r at j ^ ((r >> 1) & 3), conflict-free) and one lane
-  // stores it with TMA; a buffer is rewritten once the store issued from it has read it.
-  const uint32_t xr0 = smem_u32(s.xr) + (uint32_t)q * 4096u;
+  auto release_tmem = [&]() {
+    if (nk > 0) {
+      tc_fence_before();
+      cw_sync();
+      if (ct == 0) {
+        if (PAIR && rank != 0)
+          mbar_arrive_cluster(mapa_shared(smem_u32(&s.acc_empty[as]), 0));
+        else
+          mbar_arrive(smem_u32(&s.acc_empty[as]));
+      }
+      ++acc_n;
+    }
+  };
   if (nd.out.tmap < 0) {  // the host builds the output map of every GEMM node
     if (ct == 0) report(p, MK_ERR_DEVICE_CHECK, idx, -1, nd.out.tmap, 0, R_COMPUTE, 36);
     return false;
   }
+  // Each warp stages its 32 x 32 block of a chunk in one of two 2 KB buffers (64-byte rows,
+  // 64-byte swizzle: 16-byte chunk j of row r at j ^ ((r >> 1) & 3), conflict-free) and one lane
+  // stores it with TMA; a buffer is rewritten once the store issued from it has read it.
+  const uint32_t xr0 = smem_u32(s.xr) + (uint32_t)q * 4096u;
   const void* omap = tmap_at(p, nd.out.tmap);
-  for (int c = 0; c < tn; c += 32) {
-    uint32_t r[32], r2[32];
-    if (nk > 0) {
-      tmem_ld32(tb + (uint32_t)c, r);
-      if (dual) tmem_ld32(tb + (uint32_t)(tn + c), r2);
-      tmem_ld_wait();
-    } else {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) r[i] = r2[i] = 0u;
-    }
+  auto store32 = [&](int c, float* v) {
     const uint32_t buf = xr0 + (uint32_t)((c >> 5) & 1) * 2048u;
     if (c >= 64) {
       if (lane == 0) bulk_wait_read_1();
@@ -996,29 +1014,24 @@ __device__ bool gemm_epilogue(const Params& p, Smem& s, const Instr& in, const N
     for (int g = 0; g < 4; ++g) {
       const int col = in.n0 + c + g * 8;
       const bool inside = row < nd.M && col < nd.N;
-      float v[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        v[e] = __uint_as_float(r[g * 8 + e]);
-        if (dual) v[e] = silu(v[e]) * __uint_as_float(r2[g * 8 + e]);
-      }
+      float* w = v + g * 8;
       if (bias && inside) {
         float b[8];
         load8(nd.bias, row, col, dt, b);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) v[e] += b[e];
+        for (int e = 0; e < 8; ++e) w[e] += b[e];
       }
       if (relu) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) v[e] = fmaxf(v[e], 0.0f);
+        for (int e = 0; e < 8; ++e) w[e] = fmaxf(w[e], 0.0f);
       }
       if (res && inside) {
         float b[8];
         load8(nd.res, row, col, dt, b);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) v[e] += b[e];
+        for (int e = 0; e < 8; ++e) w[e] += b[e];
       }
-      const uint4 pk = pack8(v, dt);
+      const uint4 pk = pack8(w, dt);
       const uint32_t dst = buf + (uint32_t)lane * 64u + (uint32_t)((g ^ ((lane >> 1) & 3)) << 4);
       asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(pk.x), "r"(pk.y),
                    "r"(pk.z), "r"(pk.w)
@@ -1030,22 +1043,117 @@ __device__ bool gemm_epilogue(const Params& p, Smem& s, const Instr& in, const N
       tma_store_2d(omap, buf, in.n0 + c, row0);
       bulk_commit();
     }
+  };
+  if (in.aux1 > 0) {
+    // split tail: this split's fp32 partial (gate columns, then up columns with SiLU·mul)
+    const int W = dual ? 2 * tn : tn, S = in.aux1, cl = PAIR ? 2 : 1;
+    const size_t sstride = (size_t)cl * kGemmTileM * W;  // next split, same rank
+    const float* base = reinterpret_cast<const float*>(nd.scratch.ptr) +
+                        ((size_t)in.slot * kGemmTileM + q * 32 + lane) * W;
+    float* mine = const_cast<float*>(base) + (size_t)in.split * sstride;
+    for (int c = 0; c < W; c += 32) {
+      uint32_t r[32];
+      if (nk > 0) {
+        tmem_ld32(tb + (uint32_t)c, r);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) r[i] = 0u;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        __stcg(reinterpret_cast<float4*>(mine + c) + i,
+               make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                           __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3])));
+    }
+    __threadfence();
+    cw_sync();
+    if (ct == 0) s.flag = atomicAdd(p.counters + in.sem, 1) == S - 1;
+    cw_sync();
+    if (!s.flag) {
+      release_tmem();
+      *publish = false;
+      return true;
+    }
+    __threadfence();
+    // The last split sums the partials in split order (its own from TMEM, so the order and the
+    // result do not depend on which split finishes last) and runs the epilogue. The next column
+    // block's partial loads are issued before the current block is summed.
+    auto sum32 = [&](int col, float* acc) {
+      uint32_t r[32];
+      if (nk > 0) {
+        tmem_ld32(tb + (uint32_t)col, r);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) r[i] = 0u;
+      }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+      for (int sp = 0; sp < S; ++sp) {
+        if (sp == in.split) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc[i] += __uint_as_float(r[i]);
+        } else {
+          const float4* src = reinterpret_cast<const float4*>(base + sp * sstride + col);
+          float4 t[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) t[i] = __ldcg(src + i);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            acc[4 * i] += t[i].x;
+            acc[4 * i + 1] += t[i].y;
+            acc[4 * i + 2] += t[i].z;
+            acc[4 * i + 3] += t[i].w;
+          }
+        }
+      }
+    };
+    for (int c = 0; c < tn; c += 32) {
+      // warm L2 -> L1 for the next block of every other split while this block is summed
+      if (c + 32 < tn)
+        for (int sp = 0; sp < S; ++sp)
+          if (sp != in.split) {
+            const float* nx = base + sp * sstride + c + 32;
+            asm volatile("prefetch.global.L1 [%0];" ::"l"(nx) : "memory");
+            if (dual) asm volatile("prefetch.global.L1 [%0];" ::"l"(nx + tn) : "memory");
+          }
+      float v[32];
+      sum32(c, v);
+      if (dual) {
+        float u[32];
+        sum32(tn + c, u);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = silu(v[i]) * u[i];
+      }
+      store32(c, v);
+    }
+    release_tmem();
+  } else {
+    for (int c = 0; c < tn; c += 32) {
+      uint32_t r[32], r2[32];
+      if (nk > 0) {
+        tmem_ld32(tb + (uint32_t)c, r);
+        if (dual) tmem_ld32(tb + (uint32_t)(tn + c), r2);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) r[i] = r2[i] = 0u;
+      }
+      float v[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        v[i] = __uint_as_float(r[i]);
+        if (dual) v[i] = silu(v[i]) * __uint_as_float(r2[i]);
+      }
+      store32(c, v);
+    }
+    release_tmem();
   }
   // the tile's stores are in global memory before its counters are released
   if (lane == 0) {
     bulk_wait_all();
     fence_proxy_async_global();
-  }
-  if (nk > 0) {
-    tc_fence_before();
-    cw_sync();
-    if (ct == 0) {
-      if (PAIR && rank != 0)
-        mbar_arrive_cluster(mapa_shared(smem_u32(&s.acc_empty[as]), 0));
-      else
-        mbar_arrive(smem_u32(&s.acc_empty[as]));
-    }
-    ++acc_n;
   }
   return true;
 }
@@ -1622,6 +1730,7 @@ __device__ void run_compute(const Params& p, Smem& s, uint32_t tmem) {
   const uint32_t NS = ring_n(p);
   const int ct = (int)threadIdx.x - (kThreads - kCompute);
   uint32_t ring = 0, acc_n = 0, att_n = 0;
+  bool synced = true;  // pair-mode ring sync (see load_gemm)
   for (int it = 0;; ++it) {
     const int slot = it % kSlots;
     const uint32_t use = (uint32_t)(it / kSlots);
@@ -1632,10 +1741,12 @@ __device__ void run_compute(const Params& p, Smem& s, uint32_t tmem) {
     const Node& nd = slot_node(s, slot);
     if (p.trace && ct == 0) p.trace[(size_t)idx * kTraceWords + 0] = globaltimer();
     bool ok = true, publish = true;
+    if (in.op != OP_GEMM) synced = false;
     switch (in.op) {
       case OP_GEMM:
-        if (PAIR) ring = ring_align(ring, NS);
-        ok = gemm_epilogue<PAIR>(p, s, in, nd, slot, use, tmem, acc_n, idx);
+        if (PAIR && !synced) ring = ring_align(ring, NS);  // mirrors the loader's ring sync
+        if (ring_stages(in) > 0) synced = true;
+        ok = gemm_epilogue<PAIR>(p, s, in, nd, slot, use, tmem, acc_n, &publish, idx);
         ring += (uint32_t)ring_stages(in);
         break;
       case OP_GEMV:

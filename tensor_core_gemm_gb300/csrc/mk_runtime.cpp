@@ -500,6 +500,10 @@ extern "C" mk_status mk_compile(mk_graph_t g, const mk_compile_opts* opts_in, mk
     if (nd.kind == NK_MATMUL && p->hp.node_splits[i] > 0) {
       bytes = (size_t)p->hp.node_splits[i] * ts[nd.a].rows * ts[nd.out].cols * 4 *
               ((nd.flags & MK_EPI_SILU_MUL) ? 2 : 1);
+    } else if (nd.kind == NK_MATMUL && p->hp.node_gsplit_slots[i] > 0) {
+      // GEMM split tails: one fp32 partial of a CTA's 128 rows x tile columns per slot
+      bytes = (size_t)p->hp.node_gsplit_slots[i] * kGemmTileM * p->hp.node_tile_n[i] * 4 *
+              ((nd.flags & MK_EPI_SILU_MUL) ? 2 : 1);
     } else if (p->hp.node_scratch[i] >= 0) {
       const TensorRec& s = ts[p->hp.node_scratch[i]];
       bytes = (size_t)s.rows * s.ld * 4;

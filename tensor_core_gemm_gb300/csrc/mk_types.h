@@ -35,7 +35,9 @@ struct Instr {
   int32_t sem;
   int32_t n_src, src_off;
   int32_t n_dst, dst_off;
-  int32_t pad[3];
+  int32_t slot;   // GEMM split tail: scratch slot of split 0 (this rank); slot of split s = slot + s * cluster
+  int32_t split;  // GEMM split tail: this instruction's split index
+  int32_t pad;
 };
 static_assert(sizeof(Instr) == 64, "instruction record is 64 bytes");
 static_assert(offsetof(Instr, node) == 4 && offsetof(Instr, sem) == 32 &&

@@ -428,6 +428,17 @@ def test_pair_gemm_4096_sampled_rows():
     check_counters(plan, wl, PAIR)
 
 
+def test_split_tail_gemm_4096_sampled_rows():
+    wl = workloads.gemm(4096, 4096, 4096, dtype="f16", device=DEV, seed=0)
+    opts = dict(PAIR, gemm_split_tail=1)
+    plan, _ = run(wl, **opts)
+    rows = np.sort(torch.randperm(4096, generator=torch.Generator().manual_seed(2))[:256].numpy())
+    a = f32(wl.data[0][torch.as_tensor(rows, device=DEV)])
+    ref = ops.matmul(a, f32(wl.data[1]), F16)
+    assert_close(f32(wl.data[2][torch.as_tensor(rows, device=DEV)]), ref, "split tail 4096^3")
+    check_counters(plan, wl, opts)
+
+
 def test_pair_epilogues_and_mixed_graph():
     """Pair GEMMs with bias/ReLU/residual and SiLU·mul epilogues, then a GEMV and a norm in the
     same launch, so the two CTAs of a pair also run unrelated instructions between pair tiles."""
@@ -586,3 +597,73 @@ def test_prefill_full_config_causal_prefix():
     plan, _ = run(wl)
     check_counters(plan, wl, {})
     check_prefill_per_node(wl, 256)
+
+
+# ------------------------------------------------------------------ GEMM split tails
+
+@pytest.mark.parametrize("pair", [False, True])
+def test_split_tail_epilogues(pair):
+    """Few tiles on many SMs: every tile is a split-tail tile, split along K down to one or two
+    k-steps per split; the last split sums the fp32 partials and runs each fused epilogue."""
+    m, n, k = (384, 512, 640) if not pair else (512, 512, 1024)
+    opts = dict(gemm_tile_m=256, cluster=2, gemm_tile_n=256) if pair else dict(gemm_tile_n=256)
+    opts["gemm_split_tail"] = 1
+    a = synth.normal((m, k), 1.0, "bf16", 21, DEV)
+    b = synth.normal((k, n), 1 / math.sqrt(k), "bf16", 22, DEV)
+    bu = synth.normal((k, n), 1 / math.sqrt(k), "bf16", 23, DEV)
+    bias = synth.normal((m, n), 0.5, "bf16", 24, DEV)
+    res = synth.normal((m, n), 1.0, "bf16", 25, DEV)
+    o1, o2, o3 = (torch.zeros((m, n), dtype=torch.bfloat16, device=DEV) for _ in range(3))
+    from tensor_core_gemm_gb300 import Graph
+    g = Graph()
+    ia, ib, ibu, ibias, ires, i1, i2, i3 = (g.tensor(t) for t in (a, b, bu, bias, res, o1, o2, o3))
+    g.matmul(ia, ib, i1, bias=ibias, relu=True, residual=ires)
+    g.matmul(ia, ib, i2, b_up=ibu)
+    g.matmul(ia, ib, i3)
+    p = g.compile(**opts)
+    ins = p.instructions()
+    assert np.any(ins["aux1"][ins["op"] == osched.OP_GEMM] > 1), "no split-tail tiles"
+    p.run()
+    p.check_status()
+    A, B, BU = f32(a), f32(b), f32(bu)
+    assert_close(f32(o1), ops.matmul(A, B, BF16, bias=f32(bias), relu=True, residual=f32(res)),
+                 "split tail bias+relu+residual")
+    assert_close(f32(o2), ops.matmul_silu_mul(A, B, BU, BF16), "split tail silu_mul")
+    assert_close(f32(o3), ops.matmul(A, B, BF16), "split tail plain")
+    # the partials are summed in split order: repeat launches give the same bytes
+    first = o3.clone()
+    p.run()
+    p.check_status()
+    assert torch.equal(o3, first)
+    # and the unsplit plan agrees within the tolerance
+    o3.zero_()
+    g2 = Graph()
+    j = [g2.tensor(t) for t in (a, b, o3)]
+    g2.matmul(j[0], j[1], j[2])
+    p2 = g2.compile(**dict(opts, gemm_split_tail=0))
+    p2.run()
+    p2.check_status()
+    assert_close(f32(o3), f32(first), "split vs unsplit")
+
+
+def test_pair_gemms_interleaved_with_gemvs():
+    """Pair GEMM tiles after GEMV tiles in one launch: the two CTAs of a pair arrive with rings
+    in different states and resynchronise; consecutive pair tiles stream on without it."""
+    from tensor_core_gemm_gb300 import Graph
+    shapes = [("gemv", 1, 512, 768), ("gemm", 300, 256, 512), ("gemv", 3, 1024, 512),
+              ("gemm", 512, 384, 256), ("gemm", 700, 448, 512), ("gemv", 2, 640, 256)]
+    g = Graph()
+    data, outs = [], []
+    for i, (_, m, k, n) in enumerate(shapes):
+        a = synth.normal((m, k), 1.0, "bf16", 80 + i, DEV)
+        b = synth.normal((k, n), 1 / math.sqrt(k), "bf16", 90 + i, DEV)
+        c = torch.zeros((m, n), dtype=torch.bfloat16, device=DEV)
+        data.append((a, b))
+        outs.append(c)
+        g.matmul(g.tensor(a), g.tensor(b), g.tensor(c))
+    p = g.compile(**PAIR)
+    for _ in range(2):
+        p.run()
+        p.check_status()
+        for (kind, m, k, n), (a, b), c in zip(shapes, data, outs):
+            assert_close(f32(c), ops.matmul(f32(a), f32(b), BF16), f"{kind} {m}x{k}x{n}")

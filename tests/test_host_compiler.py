@@ -90,13 +90,51 @@ def test_gemm_plans(m, n, k, tn):
                                       (129, 72, 520, 128)])
 def test_pair_gemm_plans(m, n, k, tn):
     """CTA-pair tiles: 256 x tn, two instructions per tile on an even/odd SM pair."""
-    opts = dict(n_sm=152, gemm_tile_n=tn, gemm_tile_m=256, cluster=2)
+    opts = dict(n_sm=152, gemm_tile_n=tn, gemm_tile_m=256, cluster=2, gemm_split_tail=0)
     py, c = assert_same_plan(workloads.gemm(m, n, k).desc, opts)
     ins = c.instructions()
     gem = np.nonzero(ins["op"] == osched.OP_GEMM)[0]
     assert gem.size == 2 * (-(-m // 256)) * (-(-n // tn))
     assert np.all(gem[0::2] % 2 == 0) and np.all(gem[1::2] == gem[0::2] + 1)
     assert np.all(ins["aux0"][gem[0::2]] == 0) and np.all(ins["aux0"][gem[1::2]] == 1)
+
+
+@pytest.mark.parametrize("m,n,k,tm,tn,cl", [(4096, 4096, 4096, 256, 256, 2),
+                                            (4096, 4096, 4096, 128, 256, 1),
+                                            (1000, 1024, 776, 128, 128, 1),
+                                            (600, 640, 200, 256, 128, 2)])
+def test_split_tail_plans(m, n, k, tm, tn, cl):
+    """The last, partly filled wave of GEMM tiles is split along K: the plan equals the
+    oracle's, the splits of a tile cover K exactly once per rank in order, split 0 alone carries
+    the output box, and every split of a (tile, rank) shares split 0's arrivals and semaphore."""
+    opts = dict(n_sm=152, gemm_tile_m=tm, gemm_tile_n=tn, cluster=cl, gemm_split_tail=1)
+    py, c = assert_same_plan(workloads.gemm(m, n, k).desc, opts)
+    tiles = -(-m // tm) * -(-n // tn)
+    units = 152 // cl
+    r_tail = tiles % units
+    ins = c.instructions()
+    gem = ins[ins["op"] == osched.OP_GEMM]
+    split = gem[gem["aux1"] > 0]
+    n_split = min(units // r_tail, -(-k // 64)) if r_tail else 1
+    if n_split < 2:
+        assert split.size == 0
+        return
+    nr = int(split["aux1"][0])
+    assert split.size == r_tail * nr * cl
+    assert gem.size == (tiles - r_tail) * cl + split.size
+    for t in range(r_tail):
+        blk = split[t * nr * cl:(t + 1) * nr * cl]
+        assert len(set(zip(blk["m0"], blk["n0"]))) == 1
+        for r in range(cl):
+            mine = blk[blk["aux0"] == r]
+            assert list(mine["split"]) == list(range(nr))
+            assert mine["k0"][0] == 0 and (mine["k0"] + mine["klen"])[-1] == k
+            assert np.all(mine["k0"][1:] == (mine["k0"] + mine["klen"])[:-1])
+            assert len(set(mine["sem"])) == 1
+            assert np.all(mine["slot"] == mine["slot"][0])
+    fin = py.final_counters()
+    sem_vals = fin[py.n_dep:]
+    assert sem_vals.count(nr) == r_tail * cl
 
 
 def test_mlp3_plan():
