@@ -1162,10 +1162,10 @@ __device__ bool gemm_epilogue(const Params& p, Smem& s, const Instr& in, const N
 // (compile-time): acc[m][0..1] += sum_kk x[m][kk] * W[kk][col..col+1], W read from a 64-column
 // box in the 128-byte swizzled layout TMA writes. Four activations per shared-memory read; the
 // weight pair of each row is one 4-byte read (a warp covers one 128-byte row: no conflicts).
-template <int MT, bool BF>
+template <int MT, bool BF, int UNROLL = 2>
 __device__ __forceinline__ void gemv_stage(const uint8_t* B, int ch, const float* xs,
                                            int xstride, float (&acc)[8][2]) {
-#pragma unroll 2
+#pragma unroll UNROLL
   for (int kk = 0; kk < kGemvRows; kk += 4) {
     float xv[MT][4];
 #pragma unroll
@@ -1209,6 +1209,55 @@ __device__ __forceinline__ void gemv_stage_rows(int M, const uint8_t* B, int ch,
     case 6: gemv_stage<6, BF>(B, ch, xs, xstride, acc); break;
     case 7: gemv_stage<7, BF>(B, ch, xs, xstride, acc); break;
     default: gemv_stage<8, BF>(B, ch, xs, xstride, acc); break;
+  }
+}
+
+// The weight stages of a GEMV tile whose activations are all staged in shared memory: nk stages
+// from ring position (st, ph), each consumed and released in turn. Out of line with scalar
+// arguments, so the stage loop compiles on its own (inside the single large kernel function it ran
+// several times slower); the 2·MT sums leave through `out` once.
+template <int MT, bool BF>
+__device__ __noinline__ bool gemv_staged(const Params& p, uint32_t full0, uint32_t empty0,
+                                         const uint8_t* b0, uint32_t sb, uint32_t ns, uint32_t st,
+                                         uint32_t ph, int nk, int ch, const float* xs0, int kpad,
+                                         float* out, int idx) {
+  const int ct = (int)threadIdx.x - (kThreads - kCompute);
+  float acc[8][2];
+#pragma unroll
+  for (int m = 0; m < 8; ++m) acc[m][0] = acc[m][1] = 0.f;
+  for (int kb = 0; kb < nk; ++kb) {
+    if (!cw_wait(p, full0 + st * 8u, ph, 41, idx)) return false;
+    // all 64 rows unrolled: the stage's shared-memory reads issue ahead of their FMAs
+    gemv_stage<MT, BF, 16>(b0 + (size_t)st * sb, ch, xs0 + kb * kGemvRows, kpad, acc);
+    cw_sync();
+    if (ct == 0) mbar_arrive(empty0 + st * 8u);
+    if (++st == ns) {
+      st = 0;
+      ph ^= 1u;
+    }
+  }
+#pragma unroll
+  for (int m = 0; m < MT; ++m) {
+    out[2 * m] = acc[m][0];
+    out[2 * m + 1] = acc[m][1];
+  }
+  return true;
+}
+
+template <bool BF>
+__device__ bool gemv_staged_rows(int M, const Params& p, uint32_t full0, uint32_t empty0,
+                                 const uint8_t* b0, uint32_t sb, uint32_t ns, uint32_t st,
+                                 uint32_t ph, int nk, int ch, const float* xs0, int kpad,
+                                 float* out, int idx) {
+  switch (M) {
+    case 1: return gemv_staged<1, BF>(p, full0, empty0, b0, sb, ns, st, ph, nk, ch, xs0, kpad, out, idx);
+    case 2: return gemv_staged<2, BF>(p, full0, empty0, b0, sb, ns, st, ph, nk, ch, xs0, kpad, out, idx);
+    case 3: return gemv_staged<3, BF>(p, full0, empty0, b0, sb, ns, st, ph, nk, ch, xs0, kpad, out, idx);
+    case 4: return gemv_staged<4, BF>(p, full0, empty0, b0, sb, ns, st, ph, nk, ch, xs0, kpad, out, idx);
+    case 5: return gemv_staged<5, BF>(p, full0, empty0, b0, sb, ns, st, ph, nk, ch, xs0, kpad, out, idx);
+    case 6: return gemv_staged<6, BF>(p, full0, empty0, b0, sb, ns, st, ph, nk, ch, xs0, kpad, out, idx);
+    case 7: return gemv_staged<7, BF>(p, full0, empty0, b0, sb, ns, st, ph, nk, ch, xs0, kpad, out, idx);
+    default: return gemv_staged<8, BF>(p, full0, empty0, b0, sb, ns, st, ph, nk, ch, xs0, kpad, out, idx);
   }
 }
 
@@ -1281,7 +1330,30 @@ __device__ bool gemv(const Params& p, Smem& s, const Instr& in, const Node& nd, 
   float acc[8][2];
 #pragma unroll
   for (int m = 0; m < 8; ++m) acc[m][0] = acc[m][1] = 0.f;
-  for (int kb = 0; kb < nk; ++kb) {
+  if (staged && nk > 0) {
+    // this thread's column pair: box (which * 2 + col / 64), column col % 64 inside it
+    const int box = (dual ? which * 2 : 0) + (col >> 6), lc = col & 63;
+    float sums[16];
+    const bool ok =
+        dt == DT_BF16
+            ? gemv_staged_rows<true>(M, p, smem_u32(&s.full[0]), smem_u32(&s.empty[0]),
+                                     s.ring + box * 8192 + (lc & 7) * 2, stage_bytes(p), NS,
+                                     ring % NS, (ring / NS) & 1u, nk, lc >> 3, s.xr, kpad, sums,
+                                     idx)
+            : gemv_staged_rows<false>(M, p, smem_u32(&s.full[0]), smem_u32(&s.empty[0]),
+                                      s.ring + box * 8192 + (lc & 7) * 2, stage_bytes(p), NS,
+                                      ring % NS, (ring / NS) & 1u, nk, lc >> 3, s.xr, kpad, sums,
+                                      idx);
+    if (!ok) return false;
+#pragma unroll
+    for (int m = 0; m < 8; ++m)
+      if (m < M) {
+        acc[m][0] = sums[2 * m];
+        acc[m][1] = sums[2 * m + 1];
+      }
+    ring += (uint32_t)nk;
+  }
+  for (int kb = 0; kb < nk && !staged; ++kb) {
     const float* xs;
     int xstride;
     if (staged) {
