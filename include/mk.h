@@ -171,6 +171,9 @@ typedef struct {
                             split along K, the last split to finish sums the fp32 partials
                             and runs the epilogue; 0 (default): never split. Measured slower
                             on the 4096^3 GEMM: the last split's sum is latency-bound */
+  int32_t fuse_rope;     /* 1 (default): a ROPE node right after a matmul that lowers to GEMV
+                            tiles, reading exactly its output (head_dim 64, output width a
+                            multiple of gemv_tile_n), runs inside those tiles; 0: never */
 } mk_compile_opts;
 
 /* Fill *o with the defaults (the values listed above for each field). */

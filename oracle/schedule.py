@@ -47,7 +47,11 @@ Lowering rules per node (tile sizes come from ``opts``; see ``DEFAULT_OPTS``):
       output on the same box; aux0 = elementwise op code.
   rmsnorm -> one instruction per norm_rows rows (all columns).
   rope    -> one instruction per norm_rows rows; reads all of x's columns, writes out_q, out_k
-      (and out_v) on those rows.
+      (and out_v) on those rows. Fused (fuse_rope = 1): a rope node right after a matmul that
+      lowers to GEMV tiles (no b2), whose x is exactly that matmul's output, with head_dim 64 and
+      an output width that is a multiple of gemv_tile_n (itself a multiple of 64), emits no
+      instructions: split 0 of each GEMV column tile also carries the rotated q / k (and v)
+      boxes of its columns.
   attention with one query row (decode) -> two phases:
       partial: for kv head g, for chunk c of attn_chunk keys: reads q (the G = Hq/Hkv heads of
         group g), k and v rows of the chunk (columns of head g); writes rows (g·C + c)·G ..+G
@@ -76,7 +80,7 @@ FLAG_B_DEP = 1
 ROLE_A, ROLE_B, ROLE_E = 0, 1, 2
 
 DEFAULT_OPTS = dict(
-    gemm_tile_m=128, gemm_tile_n=256, cluster=1, gemm_split_tail=0,
+    gemm_tile_m=128, gemm_tile_n=256, cluster=1, gemm_split_tail=0, fuse_rope=1,
     ew_rows=128, ew_cols=128, ew_tiles=1,
     norm_rows=16,
     gemv_max_m=8, gemv_tile_n=256, gemv_splits=0, gemv_kstep=64,
@@ -120,7 +124,35 @@ class Instr:
                 self.aux0, self.aux1, self.sem)
 
 
-def _lower_matmul(ni, nd, opts, phases, sem_tiles):
+def rope_fusable(nodes, ri, opts):
+    """Whether rope node ri folds into the GEMV tiles of the matmul right before it."""
+    r = nodes[ri]
+    if not opts["fuse_rope"] or r["kind"] != "rope" or ri == 0:
+        return False
+    p = nodes[ri - 1]
+    if p["kind"] != "matmul" or p.get("b2") is not None:
+        return False
+    m = p["a"][3]
+    return (0 < m <= opts["gemv_max_m"] and tuple(r["x"]) == tuple(p["c"])
+            and r["head_dim"] == 64 and opts["gemv_tile_n"] % 64 == 0
+            and p["c"][4] % opts["gemv_tile_n"] == 0)
+
+
+def _rope_writes(rope, m, c0, c1):
+    """Boxes of the rope outputs that columns [c0, c1) of its input produce."""
+    d = rope["head_dim"]
+    qend, kend = rope["n_q_heads"] * d, (rope["n_q_heads"] + rope["n_kv_heads"]) * d
+    out = []
+    if c0 < qend:
+        out.append(_box(rope["out_q"], 0, m, c0, min(c1, qend)))
+    if c1 > qend and c0 < kend:
+        out.append(_box(rope["out_k"], 0, m, max(c0, qend) - qend, min(c1, kend) - qend))
+    if rope.get("out_v") is not None and c1 > kend:
+        out.append(_box(rope["out_v"], 0, m, max(c0, kend) - kend, c1 - kend))
+    return out
+
+
+def _lower_matmul(ni, nd, opts, phases, sem_tiles, rope=None):
     a, b, c = nd["a"], nd["b"], nd["c"]
     m, k = a[3], a[4]
     n = c[4]
@@ -157,6 +189,8 @@ def _lower_matmul(ni, nd, opts, phases, sem_tiles):
                     ins.reads.append((_box(r, 0, m, n0, n0 + w), ROLE_E))
                 if si == 0:
                     ins.writes.append(_box(c, 0, m, n0, n0 + w))
+                    if rope is not None:
+                        ins.writes.extend(_rope_writes(rope, m, n0, n0 + w))
                 out.append(ins)
     else:
         tm = opts["gemm_tile_m"]
@@ -321,16 +355,20 @@ def lower(graph, opts):
     tensors = [dict(t) for t in graph["tensors"]]
     phases = []
     sem_tiles = []
-    for ni, nd in enumerate(graph["nodes"]):
+    nodes = graph["nodes"]
+    fused = {ri for ri in range(len(nodes)) if rope_fusable(nodes, ri, o)}
+    for ni, nd in enumerate(nodes):
         kind = nd["kind"]
         if kind == "matmul":
-            _lower_matmul(ni, nd, o, phases, sem_tiles)
+            _lower_matmul(ni, nd, o, phases, sem_tiles,
+                          nodes[ni + 1] if ni + 1 in fused else None)
         elif kind == "ew":
             _lower_ew(ni, nd, o, phases)
         elif kind == "rmsnorm":
             _lower_rows(ni, nd, o, phases, OP_RMSNORM)
         elif kind == "rope":
-            _lower_rows(ni, nd, o, phases, OP_ROPE)
+            if ni not in fused:
+                _lower_rows(ni, nd, o, phases, OP_ROPE)
         elif kind == "attention":
             _lower_attention(ni, nd, o, phases, tensors)
         else:

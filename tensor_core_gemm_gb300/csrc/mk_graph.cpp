@@ -65,9 +65,29 @@ static HInstr make(uint16_t op, int node, int m0 = 0, int n0 = 0, int k0 = 0, in
   return h;
 }
 
+// RoPE fusion: a ROPE node right after a matmul that lowers to GEMV tiles (no second weight),
+// whose input is exactly that matmul's output window, with head_dim 64 and an output width that
+// is a multiple of the GEMV tile width, emits no instructions; split 0 of every GEMV column tile
+// also writes the rotated q / k (and v) columns it produced.
+static bool same_window(const std::vector<TensorRec>& ts, int a, int b) {
+  const TensorRec &x = ts[a], &y = ts[b];
+  return x.base == y.base && x.r0 == y.r0 && x.c0 == y.c0 && x.rows == y.rows &&
+         x.cols == y.cols;
+}
+static bool rope_fusable(const std::vector<TensorRec>& ts, const std::vector<NodeRec>& nodes,
+                         int ri, const mk_compile_opts& o) {
+  if (!o.fuse_rope || ri == 0 || nodes[ri].kind != NK_ROPE) return false;
+  const NodeRec& r = nodes[ri];
+  const NodeRec& p = nodes[ri - 1];
+  if (p.kind != NK_MATMUL || p.b2 >= 0) return false;
+  const int64_t m = ts[p.a].rows;
+  return m > 0 && m <= o.gemv_max_m && same_window(ts, r.ins[0], p.out) && r.hd == 64 &&
+         o.gemv_tile_n % 64 == 0 && ts[p.out].cols % o.gemv_tile_n == 0;
+}
+
 static void lower_matmul(const std::vector<TensorRec>& ts, int ni, const NodeRec& nd,
                          const mk_compile_opts& o, std::vector<std::vector<HInstr>>& phases,
-                         int& n_tiles_sem, HostPlan* plan) {
+                         int& n_tiles_sem, HostPlan* plan, const NodeRec* rope = nullptr) {
   const int64_t m = ts[nd.a].rows, k = ts[nd.a].cols, n = ts[nd.out].cols;
   const bool dual = nd.b2 >= 0;
   std::vector<HInstr> out;
@@ -99,7 +119,19 @@ static void lower_matmul(const std::vector<TensorRec>& ts, int ni, const NodeRec
         if (dual) h.reads.push_back({window(ts, nd.b2, k0, k0 + kl, n0, n0 + w), ROLE_B});
         if (nd.bias >= 0) h.reads.push_back({window(ts, nd.bias, 0, m, n0, n0 + w), ROLE_E});
         if (nd.res >= 0) h.reads.push_back({window(ts, nd.res, 0, m, n0, n0 + w), ROLE_E});
-        if (si == 0) h.writes.push_back(window(ts, nd.out, 0, m, n0, n0 + w));
+        if (si == 0) {
+          h.writes.push_back(window(ts, nd.out, 0, m, n0, n0 + w));
+          if (rope) {
+            const int64_t qend = (int64_t)rope->hq * 64, kend = (int64_t)(rope->hq + rope->hkv) * 64;
+            const int64_t c0 = n0, c1 = n0 + w;
+            if (c0 < qend) h.writes.push_back(window(ts, rope->out, 0, m, c0, std::min(c1, qend)));
+            if (c1 > qend && c0 < kend)
+              h.writes.push_back(window(ts, rope->out_k, 0, m, std::max(c0, qend) - qend,
+                                        std::min(c1, kend) - qend));
+            if (rope->out_v >= 0 && c1 > kend)
+              h.writes.push_back(window(ts, rope->out_v, 0, m, std::max(c0, kend) - kend, c1 - kend));
+          }
+        }
         out.push_back(std::move(h));
       }
     }
@@ -270,15 +302,27 @@ mk_status lower_graph(const std::vector<TensorRec>& tensors_in, const std::vecto
   plan->node_chunks.assign(nn, 0);
   plan->node_tile_n.assign(nn, 0);
   plan->node_gsplit_slots.assign(nn, 0);
+  plan->node_rope.assign(nn, -1);
+  std::vector<char> fused(nn, 0);
+  for (int ri = 0; ri < nn; ++ri)
+    if (rope_fusable(ts, nodes, ri, o)) {
+      fused[ri] = 1;
+      plan->node_rope[ri - 1] = ri;
+    }
   std::vector<std::vector<HInstr>> phases;
   int n_tiles_sem = 0;
   for (int ni = 0; ni < nn; ++ni) {
     const NodeRec& nd = nodes[ni];
     switch (nd.kind) {
-      case NK_MATMUL: lower_matmul(ts, ni, nd, o, phases, n_tiles_sem, plan); break;
+      case NK_MATMUL:
+        lower_matmul(ts, ni, nd, o, phases, n_tiles_sem, plan,
+                     plan->node_rope[ni] >= 0 ? &nodes[plan->node_rope[ni]] : nullptr);
+        break;
       case NK_EW: lower_ew(ts, ni, nd, o, phases); break;
       case NK_RMSNORM: lower_rows(ts, ni, nd, o, OP_RMSNORM, phases); break;
-      case NK_ROPE: lower_rows(ts, ni, nd, o, OP_ROPE, phases); break;
+      case NK_ROPE:
+        if (!fused[ni]) lower_rows(ts, ni, nd, o, OP_ROPE, phases);
+        break;
       case NK_ATTN: lower_attention(ts, ni, nd, o, phases, plan); break;
       default: set_error("mk_compile: unknown node kind %d", nd.kind); return MK_ERR_INVALID_ARG;
     }
@@ -703,5 +747,6 @@ extern "C" mk_status mk_default_opts(mk_compile_opts* o) {
   o->trace = 0;
   o->l2_prefetch = 0;
   o->gemm_split_tail = 0;
+  o->fuse_rope = 1;
   return MK_OK;
 }

@@ -73,6 +73,7 @@ struct HostPlan {
   std::vector<int> node_chunks;            // per node: attention decode chunks (0 otherwise)
   std::vector<int> node_tile_n;            // per node: output columns per tile
   std::vector<int> node_gsplit_slots;      // per node: fp32 partial slots of GEMM split tails
+  std::vector<int> node_rope;              // per matmul node: the ROPE node fused into it, or -1
 };
 
 void set_error(const char* fmt, ...);

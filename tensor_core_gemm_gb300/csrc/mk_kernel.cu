@@ -1468,6 +1468,29 @@ __device__ bool gemv(const Params& p, Smem& s, const Instr& in, const Node& nd, 
         y1 += load1(nd.res, m, n + 1, dt);
       }
       store2(nd.out, m, n, dt, y0, y1);
+      if (nd.flags & NF_ROPE) {
+        // RoPE of the following node, on the rounded outputs it would read: the pair partner of
+        // column j of a 64-column head is j ^ 32, held by lane ^ 16 (whole heads per tile, every
+        // lane active: the host fuses only full-width tiles without a second weight)
+        const float r0 = h2f(f2h(y0, dt), dt), r1 = h2f(f2h(y1, dt), dt);
+        const float p0 = __shfl_xor_sync(FULL, r0, 16), p1 = __shfl_xor_sync(FULL, r1, 16);
+        const int qend = nd.hq * 64, kend = (nd.hq + nd.hkv) * 64;
+        if (n < kend) {
+          const int j = n & 63, i = j & 31;
+          const float sgn = j < 32 ? -1.f : 1.f;  // first half: x cos - x' sin; second: + x' sin
+          const float pos = (float)(nd.pos0 + m), l2t = log2f(nd.theta);
+          float sn0, cs0, sn1, cs1;
+          sincosf(pos * exp2f(-(2.0f * (float)i / 64.0f) * l2t), &sn0, &cs0);
+          sincosf(pos * exp2f(-(2.0f * (float)(i + 1) / 64.0f) * l2t), &sn1, &cs1);
+          const float z0 = r0 * cs0 + sgn * p0 * sn0, z1 = r1 * cs1 + sgn * p1 * sn1;
+          if (n < qend)
+            store2(nd.out_q, m, n, dt, z0, z1);
+          else
+            store2(nd.out_k, m, n - qend, dt, z0, z1);
+        } else if (nd.out_v.ptr) {
+          store2(nd.out_v, m, n - kend, dt, r0, r1);
+        }
+      }
     }
   }
   *publish = true;

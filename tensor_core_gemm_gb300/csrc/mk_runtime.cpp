@@ -327,6 +327,19 @@ static mk_status build_nodes(const mk_graph* g, mk_plan* p, std::vector<CUtensor
         const bool gemv = A.rows <= p->opts.gemv_max_m;
         n.kind = gemv ? OP_GEMV : OP_GEMM;
         if (gemv) n.ldp = n.M * n.N * ((nd.flags & MK_EPI_SILU_MUL) ? 2 : 1);
+        if (p->hp.node_rope[i] >= 0) {
+          // the next node's RoPE runs in this GEMV's tiles (same rule as the lowering)
+          const NodeRec& r = g->nodes[p->hp.node_rope[i]];
+          n.flags |= NF_ROPE;
+          n.hq = r.hq;
+          n.hkv = r.hkv;
+          n.hd = r.hd;
+          n.pos0 = r.pos0;
+          n.theta = r.theta;
+          n.out_q = operand(ts, r.out);
+          n.out_k = operand(ts, r.out_k);
+          n.out_v = operand(ts, r.out_v);
+        }
         if (!gemv && n.M > 0 && n.N > 0) {
           // GEMM tiles store through TMA in 32 x 32 blocks (one per compute warp), 64-byte
           // swizzled; K = 0 tiles too (they store the epilogue of zero)

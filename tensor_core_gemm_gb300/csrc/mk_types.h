@@ -53,6 +53,7 @@ enum : uint32_t {
   EPI_RMSNORM_INPUT = 1u << 3,
   EPI_SILU_MUL = 1u << 4,
   NF_B_PANELS = 1u << 16,  // B (and b2) maps are 3D panel maps: one box per stage, all panels
+  NF_ROPE = 1u << 17,      // GEMV tiles also write RoPE's outputs (out_q, out_k, out_v)
 };
 
 enum : int32_t { EWOP_ADD = 0, EWOP_RELU = 1, EWOP_COPY = 2, EWOP_SILU_MUL = 3 };
@@ -86,7 +87,7 @@ struct Node {
   int32_t n_splits;             // GEMV: K splits per tile
   int32_t ldp;                  // GEMV partial stride (elements per split: M * N * (1 or 2))
   int32_t tile_m;               // rows per instruction of row/elementwise ops
-  int32_t pad[4];
+  Operand out_q;                // 16 B: RoPE fused into a GEMV: rotated q output
 };
 static_assert(sizeof(Node) == 256, "node entry is 256 bytes");
 

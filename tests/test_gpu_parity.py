@@ -667,3 +667,18 @@ def test_pair_gemms_interleaved_with_gemvs():
         p.check_status()
         for (kind, m, k, n), (a, b), c in zip(shapes, data, outs):
             assert_close(f32(c), ops.matmul(f32(a), f32(b), BF16), f"{kind} {m}x{k}x{n}")
+
+
+def test_decode_rope_fused_and_unfused_agree():
+    """RoPE inside the QKV GEMV tiles (default) and RoPE as its own row instruction give the
+    same decode step within the tolerance (both rotate the rounded QKV output in fp32)."""
+    sh = workloads.DecoderShape(layers=2, hidden=512, n_q_heads=8, n_kv_heads=2, head_dim=64,
+                                ffn=1024)
+    outs = []
+    for fuse in (1, 0):
+        wl = workloads.decode(sh, kv_len=130, device=DEV, seed=9)
+        plan, _ = run(wl, fuse_rope=fuse)
+        assert (plan.stats()["per_op"][osched.OP_ROPE] == 0) == bool(fuse)
+        outs.append({k: f32(wl.data[wl.info[k]]) for k in ("qr", "kc", "vc", "out")})
+    for k in ("qr", "kc", "vc", "out"):
+        assert_close(outs[0][k], outs[1][k], f"fused vs unfused {k}")
