@@ -174,6 +174,9 @@ typedef struct {
   int32_t fuse_rope;     /* 1 (default): a ROPE node right after a matmul that lowers to GEMV
                             tiles, reading exactly its output (head_dim 64, output width a
                             multiple of gemv_tile_n), runs inside those tiles; 0: never */
+  int32_t fuse_attn_reduce; /* 1 (default): the last split-KV partial of each key/value head
+                            to finish combines the head's partials (no reduce phase); 0: a
+                            separate reduce instruction per key/value head */
 } mk_compile_opts;
 
 /* Fill *o with the defaults (the values listed above for each field). */

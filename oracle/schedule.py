@@ -58,6 +58,9 @@ Lowering rules per node (tile sizes come from ``opts``; see ``DEFAULT_OPTS``):
         of a per-node fp32 scratch [Hkv·C·G × (d+2)]. n0 = g, k0 = first key, klen = keys,
         aux0 = c, aux1 = C.
       reduce: one per g; reads the group's C·G scratch rows; writes the group's output columns.
+      Fused (fuse_attn_reduce = 1, default): no reduce phase; each g owns a split semaphore, the
+        partial with c = 0 also carries the group's output box, every partial of g carries its
+        arrivals, and the last partial of g to finish combines the group's partials.
   attention with several query rows (prefill) -> one instruction per (q tile t of attn_tile_q
       rows, q head h), t descending (longest first), then h ascending; reads q rows of the tile,
       k and v rows [0, kmax) with kmax = min(Tk, q_pos0 + end of tile) when causal.
@@ -81,6 +84,7 @@ ROLE_A, ROLE_B, ROLE_E = 0, 1, 2
 
 DEFAULT_OPTS = dict(
     gemm_tile_m=128, gemm_tile_n=256, cluster=1, gemm_split_tail=0, fuse_rope=1,
+    fuse_attn_reduce=1,
     ew_rows=128, ew_cols=128, ew_tiles=1,
     norm_rows=16,
     gemv_max_m=8, gemv_tile_n=256, gemv_splits=0, gemv_kstep=64,
@@ -263,7 +267,7 @@ def _lower_rows(ni, nd, opts, phases, op):
     phases.append(out)
 
 
-def _lower_attention(ni, nd, opts, phases, tensors):
+def _lower_attention(ni, nd, opts, phases, tensors, sem_tiles):
     q, k, v, o = nd["q"], nd["k"], nd["v"], nd["out"]
     hq, hkv, d = nd["n_q_heads"], nd["n_kv_heads"], nd["head_dim"]
     g_sz = hq // hkv
@@ -275,17 +279,28 @@ def _lower_attention(ni, nd, opts, phases, tensors):
         tensors.append({"rows": hkv * nc * g_sz, "cols": d + 2, "dtype": "f32", "internal": True})
         scratch = (scratch_id, 0, 0, hkv * nc * g_sz, d + 2)
         part = []
+        fuse = opts["fuse_attn_reduce"]
         for g in range(hkv):
+            tile = None
+            if fuse:
+                tile = len(sem_tiles)
+                sem_tiles.append(tile)
             for c in range(nc):
                 k0 = c * ch
                 kl = min(ch, tk - k0)
                 ins = Instr(OP_ATTN_PARTIAL, ni, 0, g, k0, kl, c, nc)
+                ins.tile = tile
                 ins.reads.append((_box(q, 0, 1, g * g_sz * d, (g + 1) * g_sz * d), ROLE_A))
                 ins.reads.append((_box(k, k0, k0 + kl, g * d, (g + 1) * d), ROLE_B))
                 ins.reads.append((_box(v, k0, k0 + kl, g * d, (g + 1) * d), ROLE_B))
                 r0 = (g * nc + c) * g_sz
                 ins.writes.append(_box(scratch, r0, r0 + g_sz, 0, d + 2))
+                if fuse and c == 0:
+                    ins.writes.append(_box(o, 0, 1, g * g_sz * d, (g + 1) * g_sz * d))
                 part.append(ins)
+        if fuse:
+            phases.append(part)
+            return
         red = []
         for g in range(hkv):
             ins = Instr(OP_ATTN_REDUCE, ni, 0, g, 0, 0, 0, nc)
@@ -339,7 +354,8 @@ class Plan:
         tile's split semaphore counts its splits."""
         sems = [0] * self.n_sem
         for ins in self.instrs:
-            if ins.op == OP_GEMV or (ins.op == OP_GEMM and ins.aux1 > 0):
+            if (ins.op == OP_GEMV or (ins.op == OP_GEMM and ins.aux1 > 0)
+                    or (ins.op == OP_ATTN_PARTIAL and ins.tile is not None)):
                 sems[ins.sem - self.n_dep] += 1
         return list(self.targets) + sems
 
@@ -370,7 +386,7 @@ def lower(graph, opts):
             if ni not in fused:
                 _lower_rows(ni, nd, o, phases, OP_ROPE)
         elif kind == "attention":
-            _lower_attention(ni, nd, o, phases, tensors)
+            _lower_attention(ni, nd, o, phases, tensors, sem_tiles)
         else:
             raise ValueError(kind)
 
@@ -429,7 +445,8 @@ def lower(graph, opts):
     # Split tiles (GEMV, and GEMM split tails per rank): every split publishes with split 0's
     # arrivals and shares one semaphore.
     def split(ins):
-        return ins.op == OP_GEMV or (ins.op == OP_GEMM and ins.aux1 > 0)
+        return (ins.op == OP_GEMV or (ins.op == OP_GEMM and ins.aux1 > 0)
+                or (ins.op == OP_ATTN_PARTIAL and ins.tile is not None))
 
     first = {}
     for ins in instrs:
@@ -450,7 +467,8 @@ def topologically_valid(plan):
     "MegaKittens Internals" §11."""
     feeders = {}
     for i, ins in enumerate(plan.instrs):
-        split = ins.op == OP_GEMV or (ins.op == OP_GEMM and ins.aux1 > 0)
+        split = (ins.op == OP_GEMV or (ins.op == OP_GEMM and ins.aux1 > 0)
+                 or (ins.op == OP_ATTN_PARTIAL and ins.tile is not None))
         key = ("t", ins.tile) if split else ("i", i)
         for cid in ins.dst:
             feeders.setdefault(cid, {})

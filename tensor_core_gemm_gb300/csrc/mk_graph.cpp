@@ -229,7 +229,7 @@ static void lower_rows(const std::vector<TensorRec>& ts, int ni, const NodeRec& 
 
 static void lower_attention(std::vector<TensorRec>& ts, int ni, const NodeRec& nd,
                             const mk_compile_opts& o, std::vector<std::vector<HInstr>>& phases,
-                            HostPlan* plan) {
+                            int& n_tiles_sem, HostPlan* plan) {
   const int64_t hq = nd.hq, hkv = nd.hkv, d = nd.hd, g_sz = hq / hkv;
   const int64_t tq = ts[nd.a].rows, tk = ts[nd.b].rows;  // a = q, b = k, b2 = v
   if (tq == 1) {
@@ -246,17 +246,27 @@ static void lower_attention(std::vector<TensorRec>& ts, int ni, const NodeRec& n
     plan->node_scratch[ni] = sid;
     plan->node_chunks[ni] = (int)nc;
     std::vector<HInstr> part, red;
+    // fused: the last partial of each key/value head combines the head's partials
+    const bool fuse = o.fuse_attn_reduce != 0;
     for (int64_t g = 0; g < hkv; ++g) {
+      const int tile = fuse ? n_tiles_sem++ : -1;
       for (int64_t c = 0; c < nc; ++c) {
         const int64_t k0 = c * ch, kl = std::min(ch, tk - k0);
         HInstr h = make(OP_ATTN_PARTIAL, ni, 0, (int)g, (int)k0, (int)kl, (int)c, (int)nc);
+        h.tile = tile;
         h.reads.push_back({window(ts, nd.a, 0, 1, g * g_sz * d, (g + 1) * g_sz * d), ROLE_A});
         h.reads.push_back({window(ts, nd.b, k0, k0 + kl, g * d, (g + 1) * d), ROLE_B});
         h.reads.push_back({window(ts, nd.b2, k0, k0 + kl, g * d, (g + 1) * d), ROLE_B});
         const int64_t r0 = (g * nc + c) * g_sz;
         h.writes.push_back(window(ts, sid, r0, r0 + g_sz, 0, d + 2));
+        if (fuse && c == 0)
+          h.writes.push_back(window(ts, nd.out, 0, 1, g * g_sz * d, (g + 1) * g_sz * d));
         part.push_back(std::move(h));
       }
+    }
+    if (fuse) {
+      phases.push_back(std::move(part));
+      return;
     }
     for (int64_t g = 0; g < hkv; ++g) {
       HInstr h = make(OP_ATTN_REDUCE, ni, 0, (int)g, 0, 0, 0, (int)nc);
@@ -323,7 +333,7 @@ mk_status lower_graph(const std::vector<TensorRec>& tensors_in, const std::vecto
       case NK_ROPE:
         if (!fused[ni]) lower_rows(ts, ni, nd, o, OP_ROPE, phases);
         break;
-      case NK_ATTN: lower_attention(ts, ni, nd, o, phases, plan); break;
+      case NK_ATTN: lower_attention(ts, ni, nd, o, phases, n_tiles_sem, plan); break;
       default: set_error("mk_compile: unknown node kind %d", nd.kind); return MK_ERR_INVALID_ARG;
     }
   }
@@ -399,7 +409,8 @@ mk_status lower_graph(const std::vector<TensorRec>& tensors_in, const std::vecto
   // last: all splits carry split 0's arrivals and share one semaphore, numbered after the
   // dependency counters.
   auto is_split = [](const HInstr& h) {
-    return h.rec.op == OP_GEMV || (h.rec.op == OP_GEMM && h.rec.aux1 > 0);
+    return h.rec.op == OP_GEMV || (h.rec.op == OP_GEMM && h.rec.aux1 > 0) ||
+           (h.rec.op == OP_ATTN_PARTIAL && h.tile >= 0);
   };
   std::vector<int> first_of_tile(n_tiles_sem, -1);
   for (size_t i = 0; i < ins.size(); ++i)
@@ -748,5 +759,6 @@ extern "C" mk_status mk_default_opts(mk_compile_opts* o) {
   o->l2_prefetch = 0;
   o->gemm_split_tail = 0;
   o->fuse_rope = 1;
+  o->fuse_attn_reduce = 1;
   return MK_OK;
 }

@@ -1853,6 +1853,19 @@ __device__ void run_compute(const Params& p, Smem& s, uint32_t tmem) {
         ok = cw_wait(p, smem_u32(&s.deps_ready[slot]), use & 1u, 33, idx);
         trace_mark(p, idx, 2);
         ok = ok && attn_partial_body(p, s, in, nd, ring, idx);
+        if (ok && (nd.flags & NF_ATTN_FUSED)) {
+          // the last partial of the key/value head to finish combines the head's partials
+          __threadfence();
+          cw_sync();
+          if (ct == 0) s.flag = atomicAdd(p.counters + in.sem, 1) == in.aux1 - 1;
+          cw_sync();
+          if (s.flag) {
+            __threadfence();
+            attn_reduce_body(in, nd);
+          } else {
+            publish = false;
+          }
+        }
         break;
       case OP_ATTN_PREFILL:
         // inputs reach this warpgroup only through the loader and the MMAs, which wait for them

@@ -408,6 +408,7 @@ static mk_status build_nodes(const mk_graph* g, mk_plan* p, std::vector<CUtensor
         n.scale = nd.scale != 0.f ? nd.scale : 1.0f / sqrtf((float)nd.hd);
         if (p->hp.node_scratch[i] >= 0) n.scratch.ld = (int)ts[p->hp.node_scratch[i]].ld;
         if (n.M == 1) {
+          if (p->opts.fuse_attn_reduce) n.flags |= NF_ATTN_FUSED;
           // key / value chunks stream by TMA: one head (64 columns) x attn_chunk rows
           n.tile_m = p->opts.attn_chunk;
           mk_status st;

@@ -54,6 +54,7 @@ enum : uint32_t {
   EPI_SILU_MUL = 1u << 4,
   NF_B_PANELS = 1u << 16,  // B (and b2) maps are 3D panel maps: one box per stage, all panels
   NF_ROPE = 1u << 17,      // GEMV tiles also write RoPE's outputs (out_q, out_k, out_v)
+  NF_ATTN_FUSED = 1u << 18, // split-KV partials: the last one of a key/value head combines
 };
 
 enum : int32_t { EWOP_ADD = 0, EWOP_RELU = 1, EWOP_COPY = 2, EWOP_SILU_MUL = 3 };

@@ -236,7 +236,8 @@ def test_rope(rows, pos0, with_v):
 
 @pytest.mark.parametrize("tk,chunk,hq,hkv", [(1025, 64, 32, 8), (70, 16, 8, 2), (1, 64, 4, 4),
                                             (300, 128, 32, 8)])
-def test_attention_decode_split_kv(tk, chunk, hq, hkv):
+@pytest.mark.parametrize("fuse", [1, 0])
+def test_attention_decode_split_kv(tk, chunk, hq, hkv, fuse):
     d = 64
     q = synth.normal((1, hq * d), 1.0, "bf16", 50, DEV)
     k = synth.normal((tk, hkv * d), 1.0, "bf16", 51, DEV)
@@ -246,11 +247,12 @@ def test_attention_decode_split_kv(tk, chunk, hq, hkv):
     g = Graph()
     iq, ik, iv, io = g.tensor(q), g.tensor(k), g.tensor(v), g.tensor(out)
     g.attention(iq, ik, iv, io, n_q_heads=hq, n_kv_heads=hkv, head_dim=d, q_pos0=tk - 1)
-    p = g.compile(attn_chunk=chunk)
+    p = g.compile(attn_chunk=chunk, fuse_attn_reduce=fuse)
     p.run()
     p.check_status()
     ref = ops.attention(f32(q), f32(k), f32(v), hq, hkv, d, False, tk - 1, 1 / 8, BF16)
     assert_close(f32(out), ref, "split-KV attention")
+    assert (p.stats()["per_op"][osched.OP_ATTN_REDUCE] == 0) == bool(fuse)
 
 
 # ------------------------------------------------------------------ decoder, decode step

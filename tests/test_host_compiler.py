@@ -152,10 +152,18 @@ def test_gemm_list_plans():
 def test_decode_plan_full_size():
     py, c = assert_same_plan(workloads.decode().desc, dict(n_sm=152))
     per_op = c.stats()["per_op"]
-    # RoPE runs inside the QKV GEMV tiles (fused by default), or as one row instruction per layer
-    assert per_op[osched.OP_ROPE] == 0 and per_op[osched.OP_ATTN_REDUCE] == 16 * 8
-    py0, c0 = assert_same_plan(workloads.decode().desc, dict(n_sm=152, fuse_rope=0))
+    # RoPE runs inside the QKV GEMV tiles and the split-KV combine inside the last partial of
+    # each key/value head (both fused by default), or as separate instructions
+    assert per_op[osched.OP_ROPE] == 0 and per_op[osched.OP_ATTN_REDUCE] == 0
+    py0, c0 = assert_same_plan(workloads.decode().desc,
+                               dict(n_sm=152, fuse_rope=0, fuse_attn_reduce=0))
     assert c0.stats()["per_op"][osched.OP_ROPE] == 16
+    assert c0.stats()["per_op"][osched.OP_ATTN_REDUCE] == 16 * 8
+    # fused partials: every partial of a head shares one semaphore, which counts all of them
+    parts = [i for i in py.instrs if i.op == osched.OP_ATTN_PARTIAL]
+    assert len({i.sem for i in parts}) == 16 * 8
+    fin = py.final_counters()[py.n_dep:]
+    assert fin.count(17) == 16 * 8
     # the fused QKV tiles carry the rotated q / k and the appended v boxes
     qkv_tiles = [i for i in py.instrs if i.op == osched.OP_GEMV and i.node == 0 and i.k0 == 0]
     assert sum(len(i.writes) for i in qkv_tiles) == 12 + 8 + 2 + 2
