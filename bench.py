@@ -104,10 +104,14 @@ def value_of(wl, ms, name):
     return wl.flops / (ms * 1e-3) / 1e12
 
 
+KERNEL_SETS = ("general", "gemm", "decode", "prefill")  # specialisation mk_run launches
+
+
 def kernel_source_sha():
     import hashlib
     h = hashlib.sha256()
-    for f in ("mk_kernel.cu", "mk_ptx.cuh", "mk_types.h"):
+    for f in ("mk_megakernel.cuh", "mk_ptx.cuh", "mk_types.h", "mk_kernel.cu",
+              "mk_kernel_gemm.cu", "mk_kernel_decode.cu", "mk_kernel_prefill.cu"):
         with open(os.path.join(ROOT, "tensor_core_gemm_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -417,6 +421,7 @@ def main():
                        "parallelism": "replicas" if world > 1 else "single GPU",
                        "instructions": plan.stats()["n_instr"],
                        "waves_per_sm": round(plan.stats()["waves"], 3),
+                       "kernel_set": KERNEL_SETS[plan.stats()["kernel_set"]],
                        "compile_opts": opts},
             "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": runit,
                          "frac": achieved / peak, "traffic": traffic,

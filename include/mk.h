@@ -147,9 +147,11 @@ mk_status mk_add_attention(mk_graph_t g, int32_t q, int32_t k, int32_t v, int32_
 
 typedef struct {
   int32_t n_sm;          /* placement stride = persistent grid size; 0 = the device's SM count */
-  int32_t gemm_tile_m;   /* GEMM output tile rows (the kernel runs 128) */
+  int32_t gemm_tile_m;   /* GEMM output tile rows: 128 (one CTA), or 256 with cluster 2 */
   int32_t gemm_tile_n;   /* GEMM output tile columns: 64, 128 or 256 (halved for SILU_MUL) */
-  int32_t cluster;       /* instructions per GEMM tile (CTA-pair duplicates); 1 */
+  int32_t cluster;       /* instructions per GEMM tile: 1 (default), or 2 for CTA pairs (the
+                            256-row tile runs on both CTAs of a 2-CTA cluster, tcgen05
+                            cta_group::2; needs gemm_tile_m 256 and no prefill attention) */
   int32_t ew_rows, ew_cols, ew_tiles;   /* elementwise instruction = ew_rows x ew_cols*ew_tiles */
   int32_t norm_rows;     /* rows per RMSNORM / ROPE instruction */
   int32_t gemv_max_m;    /* matmuls with M <= this lower to GEMV tiles */
@@ -177,6 +179,12 @@ typedef struct {
   int32_t fuse_attn_reduce; /* 1 (default): the last split-KV partial of each key/value head
                             to finish combines the head's partials (no reduce phase); 0: a
                             separate reduce instruction per key/value head */
+  int32_t kernel_set;    /* 0 (default): launch the smallest specialisation of the kernel whose
+                            instruction kinds cover the plan (GEMM tiles only; decode: GEMV,
+                            split-KV attention and row instructions; prefill: GEMM, prefill
+                            attention and row instructions); 1: the general kernel. Both give
+                            bit-identical results; a specialisation compiles without the code
+                            of the kinds it never runs */
 } mk_compile_opts;
 
 /* Fill *o with the defaults (the values listed above for each field). */
@@ -258,6 +266,8 @@ typedef struct {
   int64_t per_op[16];    /* instructions per op code */
   int64_t smem_bytes;    /* dynamic shared memory of the launch (0 when dry_run) */
   int64_t scratch_bytes; /* plan-owned device scratch */
+  int64_t kernel_set;    /* specialisation mk_run launches: 0 general, 1 GEMM tiles only,
+                            2 decode, 3 prefill */
 } mk_stats;
 
 mk_status mk_plan_stats(mk_plan_t p, mk_stats* s);

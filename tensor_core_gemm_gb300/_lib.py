@@ -42,7 +42,7 @@ class CompileOpts(C.Structure):
         "norm_rows", "gemv_max_m", "gemv_tile_n", "gemv_splits", "gemv_kstep", "attn_chunk",
         "attn_tile_q", "dry_run", "timeout_ms", "device", "debug_counter", "debug_extra",
         "snapshot_counters", "trace", "l2_prefetch", "gemm_split_tail", "fuse_rope",
-        "fuse_attn_reduce")]
+        "fuse_attn_reduce", "kernel_set")]
 
 
 class HostCopy(C.Structure):
@@ -58,7 +58,8 @@ class Stats(C.Structure):
     _fields_ = [("n_instr", C.c_int64), ("n_counters", C.c_int64), ("n_sems", C.c_int64),
                 ("n_sm", C.c_int64), ("n_iter", C.c_int64), ("waves", C.c_double),
                 ("n_src", C.c_int64), ("n_dst", C.c_int64), ("per_op", C.c_int64 * 16),
-                ("smem_bytes", C.c_int64), ("scratch_bytes", C.c_int64)]
+                ("smem_bytes", C.c_int64), ("scratch_bytes", C.c_int64),
+                ("kernel_set", C.c_int64)]
 
 
 _lib = None

@@ -760,5 +760,6 @@ extern "C" mk_status mk_default_opts(mk_compile_opts* o) {
   o->gemm_split_tail = 0;
   o->fuse_rope = 1;
   o->fuse_attn_reduce = 1;
+  o->kernel_set = 0;
   return MK_OK;
 }

@@ -1,0 +1,2088 @@
+// The persistent megakernel: one CTA per SM walks its share of the instruction list.
+//
+// This header holds the kernel template, megakernel<PAIR, KS>: PAIR selects CTA-pair GEMM tiles,
+// KS the instruction kinds compiled in (KernelSet). Each specialisation is instantiated by one
+// small translation unit, so they compile in parallel.
+//
+// Roles inside a CTA (256 threads):
+//   warp 0      scheduler: publishes instruction descriptors into an 8-slot ring ahead of the
+//               roles and polls the global dependency counters of the oldest published one
+//               ("MegaKittens Internals" §09 controller; §11 barrier wait with acquire).
+//   warp 1      TMA loader: streams operand tiles into a 4-stage shared-memory ring; weight (B)
+//               tiles of an instruction are issued before its activations are ready ("Beating
+//               torch.compile with Megakernels", "TMA Compute Overlap"; MegaKittens §00).
+//   warp 2      MMA issuer: tcgen05.mma into a double-buffered TMEM accumulator ("Hand-writing a
+//               Blackwell GEMM", steps 3 and 8: warp specialisation, persistent kernel with two
+//               accumulator slots).
+//   warp 3      spare.
+//   warps 4-7   compute warpgroup: GEMM epilogue (TMEM -> registers -> fused epilogue -> global),
+//               GEMV tiles, elementwise / RMSNorm / RoPE rows, split-KV attention partial and
+//               combine; publishes finished tiles on the global counters (release).
+// Every wait is bounded: past `timeout_ns` the waiter records MK_ERR_TIMEOUT in the status word,
+// every role drains what it has in flight and the CTA exits normally.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "mk.h"
+#include "mk_ptx.cuh"
+#include "mk_types.h"
+
+namespace mk {
+using namespace ptx;
+
+// Device code has internal linkage: every specialisation's translation unit holds its own copy.
+namespace {
+
+enum RoleId { R_SCHED = 0, R_LOAD = 1, R_MMA = 2, R_COMPUTE = 3 };
+constexpr unsigned FULL = 0xffffffffu;
+constexpr int kCompute = 128;   // threads of the compute warpgroup
+constexpr int kBarCompute = 1;  // named barrier of the compute warpgroup
+constexpr int kXrFloats = 5120; // GEMV activation staging (M x chunk), reused for its epilogue
+
+struct __align__(1024) Smem {
+  uint8_t ring[kRingBytes];             // operand ring (stages 1024-byte aligned: 128-byte swizzle)
+  float xr[kXrFloats];                  // GEMV activations, then its output exchange
+  float red_small[8][4];                // per-row, per-warp partial sums
+  uint8_t slot[kSlots][kSlotBytes];     // instruction record + node entry per slot
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
+  uint64_t go;                          // pair mode, odd CTA: released by the even CTA once per GEMM
+  // prefill attention: scores S and output blocks O double-buffered in TMEM, P in xr
+  uint64_t att_s_full[2], att_s_free[2], att_p_full, att_o_full[2], att_o_free[2];
+  uint64_t instr_ready[kSlots];
+  uint64_t deps_ready[kSlots];
+  uint64_t slot_free[kSlots];
+  uint64_t drain;
+  float rstd[8];
+  uint32_t tmem_base;
+  int32_t flag;
+};
+static_assert(sizeof(Smem) + 1024 <= 232448, "shared memory budget of one CTA");
+
+constexpr size_t kMegakernelSmem = sizeof(Smem) + 1024;  // dynamic smem of a launch
+
+// ------------------------------------------------------------------ small helpers
+
+__device__ __forceinline__ const Instr& slot_instr(const Smem& s, int slot) {
+  return *reinterpret_cast<const Instr*>(s.slot[slot]);
+}
+__device__ __forceinline__ const Node& slot_node(const Smem& s, int slot) {
+  return *reinterpret_cast<const Node*>(s.slot[slot] + sizeof(Instr));
+}
+__device__ __forceinline__ const void* tmap_at(const Params& p, int i) {
+  return static_cast<const char*>(p.tmaps) + (size_t)i * 128;
+}
+// Ring geometry of this launch: 4 stages of 48 KB, or 6 of 32 KB when GEMM tiles run on CTA pairs
+// (every other ring user, a GEMV weight tile or an attention key/value chunk, fits in 32 KB).
+__device__ __forceinline__ uint32_t ring_n(const Params& p) { return (uint32_t)p.stages; }
+__device__ __forceinline__ uint32_t stage_bytes(const Params& p) {
+  return p.stages == kPairStages ? 32768u : 49152u;
+}
+__device__ __forceinline__ uint8_t* stage_ptr(Smem& s, const Params& p, int st) {
+  return s.ring + (size_t)st * stage_bytes(p);
+}
+// Position in the operand ring: stage index and the parity of the current pass over the ring
+// (use count / depth, mod 2), advanced incrementally so hot loops do no division.
+struct RingPos {
+  uint32_t st = 0, ph = 0;
+  __device__ __forceinline__ void next(uint32_t ns) {
+    if (++st == ns) {
+      st = 0;
+      ph ^= 1u;
+    }
+  }
+  __device__ __forceinline__ void advance(uint32_t n, uint32_t ns) {
+    const uint32_t t = st + n;
+    st = t % ns;
+    ph ^= (t / ns) & 1u;
+  }
+  __device__ __forceinline__ void align() {  // to the start of the next pass
+    if (st) {
+      st = 0;
+      ph ^= 1u;
+    }
+  }
+};
+// A plain use count rounded up to the start of the next pass (the compute warpgroup's count).
+__device__ __forceinline__ uint32_t ring_align(uint32_t v, uint32_t ns) {
+  return (v + ns - 1) / ns * ns;
+}
+__device__ __forceinline__ int ring_stages(const Instr& in) {
+  if (in.op == OP_GEMM) return (in.klen + kGemmBK - 1) / kGemmBK;
+  if (in.op == OP_GEMV) return (in.klen + kGemvRows - 1) / kGemvRows;
+  if (in.op == OP_ATTN_PARTIAL) return 1;  // the key/value chunk
+  if (in.op == OP_ATTN_PREFILL) return (in.klen + kAttnKeyBlock - 1) / kAttnKeyBlock;
+  return 0;
+}
+__device__ __forceinline__ int instr_index(const Params& p, int it) {
+  return it * p.n_sm + (int)blockIdx.x;
+}
+
+__device__ void report(const Params& p, int code, int instr, int counter, int observed,
+                       int expected, int role, int where) {
+  if (atomicCAS(p.status + ST_CODE, 0, code) == 0) {
+    p.status[ST_INSTR] = instr;
+    p.status[ST_COUNTER] = counter;
+    p.status[ST_OBSERVED] = observed;
+    p.status[ST_EXPECTED] = expected;
+    p.status[ST_SM] = (int)blockIdx.x;
+    p.status[ST_ROLE] = role;
+    p.status[ST_WHERE] = where;
+    __threadfence();
+  }
+}
+
+// Bounded mbarrier wait; false when the limit passed (reported) or another waiter aborted.
+// On-chip waits get four times the counter-wait limit: when a dependency never completes, the
+// scheduler's counter wait runs out first and the report names the counter.
+__device__ bool wait_mbar(const Params& p, uint32_t bar, uint32_t parity, int role, int where,
+                          int instr, bool cluster_scope = false) {
+  auto probe = [&]() { return cluster_scope ? mbar_try_cluster(bar, parity) : mbar_try(bar, parity); };
+  if (probe()) return true;
+  const uint64_t t0 = globaltimer();
+  const uint64_t limit = 4 * p.timeout_ns;
+  for (uint32_t n = 1;; ++n) {
+    if (probe()) return true;
+    if ((n & 15u) == 0) {
+      if (ld_volatile(p.status + ST_CODE) != 0) return false;
+      if (globaltimer() - t0 > limit) {
+        report(p, MK_ERR_TIMEOUT, instr, -1, 0, (int)parity, role, where);
+        return false;
+      }
+    }
+  }
+}
+// Warp-converged variant for roles run by a whole warp: every lane polls the same barrier and
+// all lanes leave together (lane 0's view of the limit decides), so the code after it stays
+// converged and its values warp-uniform.
+__device__ __noinline__ bool wait_warp_slow(const Params& p, uint32_t bar, uint32_t parity,
+                                            int role, int where, int instr, bool cluster_scope) {
+  const uint64_t t0 = globaltimer();
+  const uint64_t limit = 4 * p.timeout_ns;
+  for (uint32_t n = 1;; ++n) {
+    const bool done = cluster_scope ? mbar_try_cluster(bar, parity) : mbar_try(bar, parity);
+    if (__all_sync(FULL, done)) return true;
+    if ((n & 15u) == 0) {
+      int stop = 0;
+      if ((threadIdx.x & 31) == 0) {
+        if (ld_volatile(p.status + ST_CODE) != 0) stop = 1;
+        else if (globaltimer() - t0 > limit) stop = 2;
+      }
+      stop = __shfl_sync(FULL, stop, 0);
+      if (stop) {
+        if (stop == 2 && (threadIdx.x & 31) == 0)
+          report(p, MK_ERR_TIMEOUT, instr, -1, 0, (int)parity, role, where);
+        return false;
+      }
+    }
+  }
+}
+__device__ __forceinline__ bool wait_warp(const Params& p, uint32_t bar, uint32_t parity, int role,
+                                          int where, int instr, bool cluster_scope = false) {
+  const bool done = cluster_scope ? mbar_try_cluster(bar, parity) : mbar_try(bar, parity);
+  if (__all_sync(FULL, done)) return true;
+  return wait_warp_slow(p, bar, parity, role, where, instr, cluster_scope);
+}
+// Wait used while draining after an abort: ignores the status word, short fixed limit.
+__device__ void wait_mbar_drain(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try(bar, parity))
+    if (globaltimer() - t0 > 200000000ull) return;
+}
+// Compute-warpgroup wait: every thread waits (bounded), then all agree on the outcome so no
+// thread is left alone at a later named barrier.
+__device__ __forceinline__ bool cw_wait(const Params& p, uint32_t bar, uint32_t parity, int where,
+                                        int instr) {
+  const bool ok = wait_mbar(p, bar, parity, R_COMPUTE, where, instr);
+  return bar_and(kBarCompute, kCompute, ok);
+}
+__device__ __forceinline__ void cw_sync() { bar_sync(kBarCompute, kCompute); }
+// Trace point `k` of instruction `idx` (compute warpgroup, thread 0), when tracing is on.
+__device__ __forceinline__ void trace_mark(const Params& p, int idx, int k) {
+  if (p.trace && threadIdx.x == kThreads - kCompute) p.trace[(size_t)idx * kTraceWords + k] = globaltimer();
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(FULL, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(FULL, v, o));
+  return v;
+}
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
+// 16-bit element conversions (dt: DT_F16 or DT_BF16).
+__device__ __forceinline__ float h2f(uint16_t v, int dt) {
+  return dt == DT_BF16 ? __uint_as_float((uint32_t)v << 16)
+                       : __half2float(__ushort_as_half(v));
+}
+__device__ __forceinline__ uint16_t f2h(float v, int dt) {
+  return dt == DT_BF16 ? __bfloat16_as_ushort(__float2bfloat16_rn(v))
+                       : __half_as_ushort(__float2half_rn(v));
+}
+__device__ __forceinline__ void unpack8(const uint4 raw, int dt, float* x) {
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    x[2 * i] = h2f((uint16_t)(w[i] & 0xffffu), dt);
+    x[2 * i + 1] = h2f((uint16_t)(w[i] >> 16), dt);
+  }
+}
+__device__ __forceinline__ uint4 pack8(const float* x, int dt) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    w[i] = (uint32_t)f2h(x[2 * i], dt) | ((uint32_t)f2h(x[2 * i + 1], dt) << 16);
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+// 8 consecutive elements of an operand at (row, col); data produced inside the kernel is read
+// at L2 (ld.global.cg) so no SM can see a stale L1 line.
+__device__ __forceinline__ void load8(const Operand& o, int row, int col, int dt, float* x) {
+  const uint16_t* ptr = reinterpret_cast<const uint16_t*>(o.ptr) + (size_t)row * o.ld + col;
+  unpack8(__ldcg(reinterpret_cast<const uint4*>(ptr)), dt, x);
+}
+__device__ __forceinline__ void store8(const Operand& o, int row, int col, int dt, const float* x) {
+  uint16_t* ptr = reinterpret_cast<uint16_t*>(o.ptr) + (size_t)row * o.ld + col;
+  *reinterpret_cast<uint4*>(ptr) = pack8(x, dt);
+}
+__device__ __forceinline__ float load1(const Operand& o, int row, int col, int dt) {
+  const uint16_t* ptr = reinterpret_cast<const uint16_t*>(o.ptr) + (size_t)row * o.ld + col;
+  return h2f(__ldcg(reinterpret_cast<const unsigned short*>(ptr)), dt);
+}
+__device__ __forceinline__ void store2(const Operand& o, int row, int col, int dt, float v0,
+                                       float v1) {
+  uint16_t* ptr = reinterpret_cast<uint16_t*>(o.ptr) + (size_t)row * o.ld + col;
+  *reinterpret_cast<uint32_t*>(ptr) = (uint32_t)f2h(v0, dt) | ((uint32_t)f2h(v1, dt) << 16);
+}
+__device__ __forceinline__ void store1(const Operand& o, int row, int col, int dt, float v) {
+  uint16_t* ptr = reinterpret_cast<uint16_t*>(o.ptr) + (size_t)row * o.ld + col;
+  *ptr = f2h(v, dt);
+}
+
+// ------------------------------------------------------------------ scheduler warp
+
+template <int KS>
+__device__ void run_scheduler(const Params& p, Smem& s) {
+  const int lane = threadIdx.x & 31;
+  int fetched = 0, ready = 0;
+  bool end_published = false;
+  uint32_t idle = 0;
+  uint64_t idle_since = 0;
+  int pend_ctr = -1, pend_obs = 0, pend_tgt = 0;
+  while (true) {
+    bool progress = false;
+    // Publish the next descriptor as soon as its slot is free: roles may run ahead of the
+    // dependency resolution by up to kSlots instructions (the loader prefetches weights).
+    if (!end_published && fetched < ready + kSlots) {
+      const int slot = fetched % kSlots;
+      const uint32_t use = (uint32_t)(fetched / kSlots);
+      if (mbar_try(smem_u32(&s.slot_free[slot]), (use & 1u) ^ 1u)) {
+        uint32_t* dst = reinterpret_cast<uint32_t*>(s.slot[slot]);
+        const int idx = instr_index(p, fetched);
+        if (idx < p.n_instr) {
+          const uint32_t* si = reinterpret_cast<const uint32_t*>(p.instrs + idx);
+          const uint32_t w = lane < 16 ? __ldg(si + lane) : 0u;
+          const int node = __shfl_sync(FULL, (int)w, 1);
+          const int op = (int)(__shfl_sync(FULL, w, 0) & 0xffffu);
+          if (!ks_covers(KS, op)) {  // the host launches a specialisation that covers the plan
+            if (lane == 0) report(p, MK_ERR_DEVICE_CHECK, idx, -1, op, KS, R_SCHED, 2);
+            break;
+          }
+          if (lane < 16) dst[lane] = w;
+          const uint32_t* sn = reinterpret_cast<const uint32_t*>(p.nodes + node);
+          dst[16 + lane] = __ldg(sn + lane);
+          dst[48 + lane] = __ldg(sn + 32 + lane);
+          ++fetched;
+        } else {
+          if (lane == 0) dst[0] = (uint32_t)OP_END;
+          end_published = true;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&s.instr_ready[slot]));
+        progress = true;
+      }
+    }
+    // Resolve the oldest published instruction's sources (one pass, lanes in parallel).
+    if (ready < fetched) {
+      const int slot = ready % kSlots;
+      const Instr& in = slot_instr(s, slot);
+      bool ok = true;
+      pend_ctr = -1;
+      for (int j = lane; j < in.n_src; j += 32) {
+        const int ctr = __ldg(p.src_list + 2 * (in.src_off + j));
+        const int tgt = __ldg(p.src_list + 2 * (in.src_off + j) + 1);
+        const int v = ld_acquire(p.counters + ctr);
+        if (v < tgt) {
+          ok = false;
+          pend_ctr = ctr;
+          pend_obs = v;
+          pend_tgt = tgt;
+        }
+      }
+      if (__all_sync(FULL, ok)) {
+        if (lane == 0) {
+          // later TMA (async-proxy) reads of the producers' data are ordered after the acquire
+          fence_proxy_async_global();
+          mbar_arrive(smem_u32(&s.deps_ready[slot]));
+          if (p.trace) p.trace[(size_t)instr_index(p, ready) * kTraceWords + 1] = globaltimer();
+        }
+        ++ready;
+        progress = true;
+      }
+    }
+    if (end_published && ready == fetched) break;
+    if (progress) {
+      idle = 0;
+      continue;
+    }
+    if (idle++ == 0) {
+      idle_since = globaltimer();
+    } else if ((idle & 15u) == 0) {
+      if (ld_volatile(p.status + ST_CODE) != 0) break;
+      if (globaltimer() - idle_since > p.timeout_ns) {
+        const unsigned who = __ballot_sync(FULL, pend_ctr >= 0);
+        const int src = who ? __ffs(who) - 1 : 0;
+        const int c = __shfl_sync(FULL, pend_ctr, src), o = __shfl_sync(FULL, pend_obs, src),
+                  t = __shfl_sync(FULL, pend_tgt, src);
+        if (lane == 0) report(p, MK_ERR_TIMEOUT, instr_index(p, ready), c, o, t, R_SCHED, 1);
+        break;
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ TMA loader (one warp)
+
+// The loader runs on a whole warp, converged: every lane polls the barriers, ring positions and
+// coordinates are warp-uniform, and one elected lane issues each barrier operation and copy.
+// The issuing thread's own latency bounds how fast stages are refilled, so the per-stage work is
+// one or two copies and a few uniform integer operations.
+
+// `panels` 64-column panels of B (64 rows each, 8 KB atoms in the 128-byte swizzled layout) from
+// column `col`, row `k`, into consecutive atoms at `dst`. A panel map (3D: column within the
+// panel, row, panel) moves them in one copy; a plain 2D map takes one copy per panel. PC: the
+// copy counts on the even CTA's barrier of a CTA pair.
+template <bool PC>
+__device__ __forceinline__ void load_panels(uint32_t dst, const void* map, bool panel_map,
+                                            uint32_t bar, int col, int k, int panels) {
+  if (panel_map) {
+    if (PC)
+      tma_load_3d_pair(dst, map, bar, 0, k, col >> 6);
+    else
+      tma_load_3d(dst, map, bar, 0, k, col >> 6);
+  } else {
+    for (int j = 0; j < panels; ++j) {
+      if (PC)
+        tma_load_2d_pair(dst + j * 8192, map, bar, col + 64 * j, k);
+      else
+        tma_load_2d(dst + j * 8192, map, bar, col + 64 * j, k);
+    }
+  }
+}
+
+// Ring alignment of pair mode: the two CTAs of a pair have consumed different numbers of stages
+// (their other instructions differ), but one MMA reads both CTAs' shared memory at the same
+// offsets. Before every pair GEMM both CTAs therefore move to the start of the next pass over the
+// ring; each skipped stage is waited free, then both of its barriers are arrived on so their
+// phase counts stay equal to the use count every role tracks.
+// Everything the k-loop of one GEMM tile's loads needs, as plain values.
+struct LoadTile {
+  uint32_t full0, tx0, empty0, deps, deps_par, ring0, sb, ns, own;
+  int nk, npre, arow, bcol, k0, nbox;
+  const void *ta, *tb, *tb2;
+  bool leader, panel;
+};
+
+// The loads of one GEMM tile, from ring position (st, ph). Out of line so the hot loop compiles
+// on its own. Weights first: the first npre stages get their B operand before the activations
+// are known to be ready (they depend on nothing inside the graph), then A follows for those and
+// both for the rest. Each stage is armed by the CTA whose barrier counts the bytes: the even CTA
+// of a pair expects both CTAs' bytes; the odd CTA arrives on its own barrier only to keep its
+// phase count in step.
+template <bool PAIR, bool DUAL>
+__device__ __noinline__ bool load_tile(const Params& p, const LoadTile& tp, uint32_t st,
+                                       uint32_t ph, int idx) {
+  const LoadTile t = tp;  // a private copy: its fields stay in registers
+  auto arm = [&](uint32_t s_) {
+    if (t.leader)
+      mbar_expect_tx(t.full0 + s_ * 8u, PAIR ? 2 * t.own : t.own);
+    else
+      mbar_arrive(t.full0 + s_ * 8u);
+  };
+  auto issue_b = [&](uint32_t s_, int kb) {
+    const uint32_t dst = t.ring0 + s_ * t.sb + kGemmTileM * kGemmBK * 2;
+    const int k = t.k0 + kb * kGemmBK;
+    load_panels<PAIR>(dst, t.tb, t.panel, t.tx0 + s_ * 8u, t.bcol, k, t.nbox);
+    if (DUAL) load_panels<PAIR>(dst + t.nbox * 8192, t.tb2, t.panel, t.tx0 + s_ * 8u, t.bcol, k, t.nbox);
+  };
+  auto issue_a = [&](uint32_t s_, int kb) {
+    if (PAIR)
+      tma_load_2d_pair(t.ring0 + s_ * t.sb, t.ta, t.tx0 + s_ * 8u, t.k0 + kb * kGemmBK, t.arow);
+    else
+      tma_load_2d(t.ring0 + s_ * t.sb, t.ta, t.tx0 + s_ * 8u, t.k0 + kb * kGemmBK, t.arow);
+  };
+  const uint32_t st0 = st;
+  for (int kb = 0; kb < t.npre; ++kb) {
+    if (!wait_warp(p, t.empty0 + st * 8u, ph ^ 1u, R_LOAD, 11, idx)) return false;
+    if (elect_one()) {
+      arm(st);
+      issue_b(st, kb);
+    }
+    __syncwarp();
+    if (++st == t.ns) {
+      st = 0;
+      ph ^= 1u;
+    }
+  }
+  if (!wait_warp(p, t.deps, t.deps_par, R_LOAD, 12, idx)) return false;
+  if (elect_one()) {
+    fence_proxy_async_global();
+    uint32_t q = st0;
+    for (int kb = 0; kb < t.npre; ++kb) {
+      issue_a(q, kb);
+      if (++q == t.ns) q = 0;
+    }
+  }
+  __syncwarp();
+  for (int kb = t.npre; kb < t.nk; ++kb) {
+    if (!wait_warp(p, t.empty0 + st * 8u, ph ^ 1u, R_LOAD, 13, idx)) return false;
+    if (elect_one()) {
+      arm(st);
+      issue_b(st, kb);
+      issue_a(st, kb);
+    }
+    __syncwarp();
+    if (++st == t.ns) {
+      st = 0;
+      ph ^= 1u;
+    }
+  }
+  return true;
+}
+
+// Pair-mode ring sync: `synced` holds while every instruction since the last resync was a pair
+// GEMM (all roles of both CTAs see the same instruction kinds per iteration, so they agree). Then
+// both CTAs consumed the same stages from the same position and every stage's last use was a pair
+// MMA that released it in both CTAs: the next pair GEMM streams straight on. Otherwise it resyncs.
+template <bool PAIR>
+__device__ bool load_gemm(const Params& p, Smem& s, const Instr& in, const Node& nd, int slot,
+                          uint32_t use, RingPos& rp, uint32_t& nfill, uint32_t& go_par,
+                          bool& synced, int idx) {
+  const uint32_t NS = ring_n(p);
+  if (PAIR && !synced) {
+    while (rp.st != 0) {
+      if (!wait_warp(p, smem_u32(&s.empty[rp.st]), rp.ph ^ 1u, R_LOAD, 18, idx)) return false;
+      if (elect_one()) {
+        mbar_arrive(smem_u32(&s.full[rp.st]));
+        mbar_arrive(smem_u32(&s.empty[rp.st]));
+      }
+      __syncwarp();
+      rp.next(NS);
+      ++nfill;
+    }
+  }
+  const int nk = ring_stages(in);
+  if (nk == 0) return true;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  if (PAIR && !synced) {
+    // After other instructions the two CTAs' rings differ, so the odd CTA's bytes must not reach
+    // the even CTA's full barriers while one of them still carries an earlier load. The even CTA
+    // waits until every stage of the pass is free (every earlier use consumed), then releases the
+    // odd CTA once. Later stages need no handshake: the odd CTA reuses a stage only after the
+    // pair MMA that read it committed, which is after the even CTA's barrier for it completed.
+    // Bytes that land before the even CTA's expect_tx leave the transaction count negative
+    // until it arrives.
+    if (rank == 0) {
+      for (int j = 0; j < (int)NS; ++j)
+        if (!wait_warp(p, smem_u32(&s.empty[j]), rp.ph ^ 1u, R_LOAD, 17, idx)) return false;
+      if (elect_one()) mbar_arrive_cluster(mapa_shared(smem_u32(&s.go), 1));
+      __syncwarp();
+    } else {
+      if (!wait_warp(p, smem_u32(&s.go), go_par & 1u, R_LOAD, 19, idx, true)) return false;
+      go_par ^= 1u;
+    }
+  }
+  synced = true;
+  const bool dual = (nd.flags & EPI_SILU_MUL) != 0;
+  const bool panel = (nd.flags & NF_B_PANELS) != 0;
+  const int tn = nd.tile_n;
+  const int ncol = PAIR ? tn / 2 : tn;  // B columns this CTA loads per weight
+  LoadTile t;
+  t.full0 = smem_u32(&s.full[0]);
+  // bytes of both CTAs of a pair complete on the even CTA's full barrier
+  t.tx0 = PAIR ? mapa_shared(t.full0, 0) : t.full0;
+  t.empty0 = smem_u32(&s.empty[0]);
+  t.deps = smem_u32(&s.deps_ready[slot]);
+  t.deps_par = use & 1u;
+  t.ring0 = smem_u32(s.ring);
+  t.sb = stage_bytes(p);
+  t.ns = NS;
+  t.nk = nk;
+  t.npre = (in.flags & IFLAG_B_DEP) ? 0 : (nk < (int)NS ? nk : (int)NS);
+  t.ta = tmap_at(p, nd.a.tmap);
+  t.tb = tmap_at(p, nd.b.tmap);
+  t.tb2 = dual ? tmap_at(p, nd.b2.tmap) : nullptr;
+  t.arow = in.m0 + (int)rank * kGemmTileM;
+  t.bcol = in.n0 + (int)rank * ncol;
+  t.k0 = in.k0;
+  t.nbox = ncol / 64;
+  t.own = (uint32_t)(kGemmTileM * kGemmBK * 2 + (dual ? 2 : 1) * ncol * kGemmBK * 2);
+  t.leader = !PAIR || rank == 0;
+  t.panel = panel;
+  const bool ok = dual ? load_tile<PAIR, true>(p, t, rp.st, rp.ph, idx)
+                       : load_tile<PAIR, false>(p, t, rp.st, rp.ph, idx);
+  rp.advance((uint32_t)nk, NS);
+  nfill += (uint32_t)nk;
+  return ok;
+}
+
+__device__ void prefetch_ahead(const Params& p, const Smem& s, int cur, int& next);
+
+__device__ bool load_gemv(const Params& p, Smem& s, const Instr& in, const Node& nd, int slot,
+                          uint32_t use, RingPos& rp, uint32_t& nfill, int idx, int it,
+                          int& pf_next) {
+  const uint32_t NS = ring_n(p);
+  const int nk = ring_stages(in);
+  if (nk == 0) return true;
+  const bool dual = (nd.flags & EPI_SILU_MUL) != 0;
+  const bool panel = (nd.flags & NF_B_PANELS) != 0;
+  // a stage is four 64-row x 64-column panels, 128-byte swizzled (8 KB each): the tile's 256
+  // columns, or 128 gate columns then 128 up columns
+  const uint32_t bytes = 4u * 64u * kGemvRows * 2u;
+  const void* tb = tmap_at(p, nd.b.tmap);
+  const void* tb2 = dual ? tmap_at(p, nd.b2.tmap) : nullptr;
+  const uint32_t ring0 = smem_u32(s.ring), sb = stage_bytes(p);
+  if (in.flags & IFLAG_B_DEP) {
+    if (!wait_warp(p, smem_u32(&s.deps_ready[slot]), use & 1u, R_LOAD, 14, idx)) return false;
+    if (elect_one()) fence_proxy_async_global();
+    __syncwarp();
+  }
+  for (int kb = 0; kb < nk; ++kb) {
+    if (kb >= (int)NS) prefetch_ahead(p, s, it, pf_next);  // descriptors published meanwhile
+    if (!wait_warp(p, smem_u32(&s.empty[rp.st]), rp.ph ^ 1u, R_LOAD, 15, idx)) return false;
+    if (elect_one()) {
+      const uint32_t bar = smem_u32(&s.full[rp.st]);
+      const uint32_t dst = ring0 + rp.st * sb;
+      const int k = in.k0 + kb * kGemvRows;
+      mbar_expect_tx(bar, bytes);
+      if (dual) {
+        load_panels<false>(dst, tb, panel, bar, in.n0, k, 2);
+        load_panels<false>(dst + 2 * 8192, tb2, panel, bar, in.n0, k, 2);
+      } else {
+        load_panels<false>(dst, tb, panel, bar, in.n0, k, 4);
+      }
+    }
+    __syncwarp();
+    rp.next(NS);
+    ++nfill;
+  }
+  return true;
+}
+
+// Split-KV partial: the chunk's keys and values (head g = n0, 64 columns each) land in one
+// stage, 128-byte swizzled: keys at offset 0, values at 16 KB. A chunk that does not contain a
+// row appended inside the graph streams before the query is ready.
+__device__ bool load_attn(const Params& p, Smem& s, const Instr& in, const Node& nd, int slot,
+                          uint32_t use, RingPos& rp, uint32_t& nfill, int idx) {
+  const uint32_t NS = ring_n(p);
+  if (in.flags & IFLAG_B_DEP) {
+    if (!wait_warp(p, smem_u32(&s.deps_ready[slot]), use & 1u, R_LOAD, 16, idx)) return false;
+    if (elect_one()) fence_proxy_async_global();
+    __syncwarp();
+  }
+  if (!wait_warp(p, smem_u32(&s.empty[rp.st]), rp.ph ^ 1u, R_LOAD, 17, idx)) return false;
+  if (elect_one()) {
+    const uint32_t bar = smem_u32(&s.full[rp.st]);
+    const uint32_t dst = smem_u32(s.ring) + rp.st * stage_bytes(p);
+    mbar_expect_tx(bar, (uint32_t)(2 * nd.tile_m * 128));
+    tma_load_2d(dst, tmap_at(p, nd.b.tmap), bar, in.n0 * 64, in.k0);
+    tma_load_2d(dst + 16384, tmap_at(p, nd.b2.tmap), bar, in.n0 * 64, in.k0);
+  }
+  __syncwarp();
+  rp.next(NS);
+  ++nfill;
+  return true;
+}
+
+// Causal prefill attention, one (128-row query tile, query head) instruction: per 64-key block a
+// stage holds the query tile (16 KB), the block's keys (8 KB) and values (8 KB) of the head's
+// key/value head, all 128-byte swizzled. The query tile is fetched again with every block (from
+// L2) so each stage is self-contained. All three operands are produced inside the graph, so the
+// loads start once the sources are ready.
+__device__ bool load_attn_prefill(const Params& p, Smem& s, const Instr& in, const Node& nd,
+                                  int slot, uint32_t use, RingPos& rp, uint32_t& nfill, int idx) {
+  const uint32_t NS = ring_n(p);
+  const int nb = ring_stages(in);
+  if (nb == 0) return true;
+  if (!wait_warp(p, smem_u32(&s.deps_ready[slot]), use & 1u, R_LOAD, 28, idx)) return false;
+  if (elect_one()) fence_proxy_async_global();
+  __syncwarp();
+  const int h = in.n0, g = in.n0 / (nd.hq / nd.hkv);
+  const void* tq = tmap_at(p, nd.a.tmap);
+  const void* tk = tmap_at(p, nd.b.tmap);
+  const void* tv = tmap_at(p, nd.b2.tmap);
+  const uint32_t ring0 = smem_u32(s.ring), sb = stage_bytes(p);
+  for (int j = 0; j < nb; ++j) {
+    if (!wait_warp(p, smem_u32(&s.empty[rp.st]), rp.ph ^ 1u, R_LOAD, 29, idx)) return false;
+    if (elect_one()) {
+      const uint32_t bar = smem_u32(&s.full[rp.st]);
+      const uint32_t dst = ring0 + rp.st * sb;
+      mbar_expect_tx(bar, 32768u);
+      tma_load_2d(dst, tq, bar, h * 64, in.m0);
+      tma_load_2d(dst + 16384, tk, bar, g * 64, j * kAttnKeyBlock);
+      tma_load_2d(dst + 24576, tv, bar, g * 64, j * kAttnKeyBlock);
+    }
+    __syncwarp();
+    rp.next(NS);
+    ++nfill;
+  }
+  return true;
+}
+
+// L2 prefetch of the streamed operands of instructions already published to later slots: HBM
+// keeps streaming weights (and key/value chunks) while earlier instructions wait for their
+// activations; their shared-memory loads then hit L2. `next` is the first instruction not yet
+// prefetched; instructions whose operand is produced inside the graph are skipped. Slots are
+// probed without suspending the warp.
+__device__ void prefetch_ahead(const Params& p, const Smem& s, int cur, int& next) {
+  if (next < cur) next = cur;
+  while (next < cur + p.l2_prefetch) {
+    const int slot = next % kSlots;
+    const bool ready = mbar_test(smem_u32(&s.instr_ready[slot]), (uint32_t)(next / kSlots) & 1u);
+    if (!__all_sync(FULL, ready)) return;
+    const Instr& f = slot_instr(s, slot);
+    if (f.op == OP_END) {
+      next = 0x3fffffff;
+      return;
+    }
+    const Node& nd = slot_node(s, slot);
+    if (!(f.flags & IFLAG_B_DEP)) {
+      if (elect_one()) {
+        const bool panel = (nd.flags & NF_B_PANELS) != 0;
+        if (f.op == OP_GEMV) {
+          const bool dual = (nd.flags & EPI_SILU_MUL) != 0;
+          const int nk = ring_stages(f);
+          const void* mb = tmap_at(p, nd.b.tmap);
+          const void* mb2 = dual ? tmap_at(p, nd.b2.tmap) : nullptr;
+          for (int kb = 0; kb < nk; ++kb) {
+            const int k = f.k0 + kb * kGemvRows;
+            if (panel) {
+              tma_prefetch_l2_3d(mb, 0, k, f.n0 >> 6);
+              if (dual) tma_prefetch_l2_3d(mb2, 0, k, f.n0 >> 6);
+            } else {
+              for (int j = 0; j < 4; ++j)
+                tma_prefetch_l2_2d((dual && j >= 2) ? mb2 : mb, f.n0 + 64 * (dual ? (j & 1) : j),
+                                   k);
+            }
+          }
+        } else if (f.op == OP_ATTN_PARTIAL) {
+          tma_prefetch_l2_2d(tmap_at(p, nd.b.tmap), f.n0 * 64, f.k0);
+          tma_prefetch_l2_2d(tmap_at(p, nd.b2.tmap), f.n0 * 64, f.k0);
+        }
+      }
+      __syncwarp();
+    }
+    ++next;
+  }
+}
+
+template <bool PAIR, int KS>
+__device__ void run_loader(const Params& p, Smem& s) {
+  const uint32_t NS = ring_n(p);
+  for (int i = 0; i < p.n_tmaps; ++i) tensormap_acquire(tmap_at(p, i));
+  RingPos rp;
+  uint32_t nfill = 0, go_par = 0;
+  bool synced = true;  // pair-mode ring sync (see load_gemm)
+  int pf_next = 0;
+  for (int it = 0;; ++it) {
+    const int slot = it % kSlots;
+    const uint32_t use = (uint32_t)(it / kSlots);
+    const int idx = instr_index(p, it);
+    if (!wait_warp(p, smem_u32(&s.instr_ready[slot]), use & 1u, R_LOAD, 10, idx)) break;
+    const Instr& in = slot_instr(s, slot);
+    if (in.op == OP_END) break;
+    const Node& nd = slot_node(s, slot);
+    if (ks_has_gemv(KS)) prefetch_ahead(p, s, it, pf_next);
+    bool ok = true;
+    if (in.op != OP_GEMM) synced = false;
+    if (ks_has_gemm(KS) && in.op == OP_GEMM)
+      ok = load_gemm<PAIR>(p, s, in, nd, slot, use, rp, nfill, go_par, synced, idx);
+    else if (ks_has_gemv(KS) && in.op == OP_GEMV)
+      ok = load_gemv(p, s, in, nd, slot, use, rp, nfill, idx, it, pf_next);
+    else if (ks_has_gemv(KS) && in.op == OP_ATTN_PARTIAL)
+      ok = load_attn(p, s, in, nd, slot, use, rp, nfill, idx);
+    else if (ks_has_attn_prefill(KS) && in.op == OP_ATTN_PREFILL)
+      ok = load_attn_prefill(p, s, in, nd, slot, use, rp, nfill, idx);
+    if (!ok) break;
+    if (elect_one()) mbar_arrive(smem_u32(&s.slot_free[slot]));
+    __syncwarp();
+  }
+  // Every load issued has landed before the CTA may exit (normally already true): the last fill
+  // of stage st was in the current pass when st < rp.st, else in the previous one.
+  for (uint32_t st = 0; st < NS; ++st) {
+    if (nfill <= st) continue;
+    wait_mbar_drain(smem_u32(&s.full[st]), st < rp.st ? rp.ph : rp.ph ^ 1u);
+  }
+  __syncwarp();
+}
+
+// ------------------------------------------------------------------ MMA issuer (one warp)
+
+// The MMAs of one GEMM tile: nk k-steps from ring position (st, ph), accumulating into TMEM
+// column d. Out of line and with scalar arguments so the hot loop compiles on its own: few live
+// values, operands that stay warp-uniform. Software-pipelined: an MMA issue waits while the
+// tensor pipe is busy and the pipe queues little ahead, so the next stage's barrier is polled
+// after all but the last K slice of the current stage is issued; the pipe keeps executing
+// meanwhile. Returns the number of k-steps whose MMAs were issued (nk unless a wait gave up).
+template <bool PAIR, bool DUAL>
+__device__ __noinline__ int mma_tile(const Params& p, uint32_t full0, uint32_t empty0,
+                                     uint32_t st, uint32_t ph, uint32_t ns, int nk,
+                                     uint64_t adesc0, uint64_t bdesc0, uint32_t units, uint32_t d,
+                                     uint32_t idesc, int tn, uint64_t up, int idx) {
+  auto slice = [&](uint64_t so, int j, uint32_t acc) {
+    const uint64_t ad = adesc0 + so + (uint64_t)(j * 2);
+    const uint64_t bd = bdesc0 + so + (uint64_t)(j * 128);
+    if (PAIR)
+      tc_mma_f16_pair(d, ad, bd, idesc, acc);
+    else
+      tc_mma_f16(d, ad, bd, idesc, acc);
+    if (DUAL) {
+      if (PAIR)
+        tc_mma_f16_pair(d + (uint32_t)tn, ad, bd + up, idesc, acc);
+      else
+        tc_mma_f16(d + (uint32_t)tn, ad, bd + up, idesc, acc);
+    }
+  };
+  if (!wait_warp(p, full0 + st * 8u, ph, R_MMA, 22, idx)) return 0;
+  tc_fence_after();
+  for (int kb = 0; kb < nk; ++kb) {
+    const uint64_t so = (uint64_t)(st * units);
+    uint32_t nst = st + 1, nph = ph;
+    if (nst == ns) {
+      nst = 0;
+      nph ^= 1u;
+    }
+    if (elect_one()) {
+#pragma unroll
+      for (int j = 0; j < kGemmBK / 16 - 1; ++j) slice(so, j, (kb | j) != 0);
+    }
+    __syncwarp();
+    if (kb + 1 < nk) {
+      if (!wait_warp(p, full0 + nst * 8u, nph, R_MMA, 22, idx)) return kb + 1;
+      tc_fence_after();
+    }
+    if (elect_one()) {
+      slice(so, kGemmBK / 16 - 1, 1u);
+      // the stage is free (in both CTAs of a pair) once these MMAs complete
+      if (PAIR)
+        tc_commit_pair(empty0 + st * 8u, 3);
+      else
+        tc_commit(empty0 + st * 8u);
+    }
+    __syncwarp();
+    st = nst;
+    ph = nph;
+  }
+  return nk;
+}
+
+// Prefill attention MMAs of one instruction: nb key blocks from ring position (st, ph). Block j:
+// S_j = Q K_j^T into TMEM S[n&1] (M = 128 query rows, N = 64 keys, K = 64 dims; the keys are a
+// K-major B operand), then, once the compute warps have written P_j (bf16, 128-byte swizzled,
+// K-major) to shared memory, O_j = P_j V_j into TMEM O[n&1] (N = 64 dims, K = 64 keys; the values
+// are an N-major B operand). S_{j+1} is issued before P_j is awaited, so the tensor pipe computes
+// the next scores while the softmax of the current block runs. A stage is released when O_j's
+// MMAs complete. `n` counts attention blocks on this SM: it gives every barrier's phase.
+// TMEM columns: S at 0 and 64, O at 128 and 192.
+__device__ __noinline__ bool mma_attn(const Params& p, Smem& s, uint32_t st, uint32_t ph,
+                                      uint32_t ns, int nb, uint32_t tmem, uint32_t& n, int idx) {
+  const uint32_t ring0 = smem_u32(s.ring), units = stage_bytes(p) >> 4;
+  const uint64_t qd = sdesc_sw128(ring0, 16, 1024);            // Q: 128 rows of 128 B
+  const uint64_t kd = sdesc_sw128(ring0 + 16384, 16, 1024);    // K: 64 rows of 128 B
+  const uint64_t vd = sdesc_sw128(ring0 + 24576, 8192, 1024);  // V: 64 rows of 128 B, N-major
+  const uint64_t pd = sdesc_sw128(smem_u32(s.xr), 16, 1024);   // P: 128 rows of 128 B
+  const uint32_t is = idesc_f16_bk(1, kAttnKeyBlock, kAttnTileQ), io = idesc_f16(1, 64, kAttnTileQ);
+  const uint32_t n0 = n;
+  RingPos rs, ro;
+  rs.st = ro.st = st;
+  rs.ph = ro.ph = ph;
+  auto issue_s = [&](int j) -> bool {
+    const uint32_t nn = n0 + (uint32_t)j, b = nn & 1u;
+    if (!wait_warp(p, smem_u32(&s.full[rs.st]), rs.ph, R_MMA, 23, idx)) return false;
+    if (!wait_warp(p, smem_u32(&s.att_s_free[b]), ((nn >> 1) & 1u) ^ 1u, R_MMA, 24, idx))
+      return false;
+    tc_fence_after();
+    const uint64_t so = (uint64_t)(rs.st * units);
+    if (elect_one()) {
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        tc_mma_f16(tmem + b * 64u, qd + so + (uint64_t)(kk * 2), kd + so + (uint64_t)(kk * 2), is,
+                   kk != 0);
+      tc_commit(smem_u32(&s.att_s_full[b]));
+    }
+    __syncwarp();
+    rs.next(ns);
+    return true;
+  };
+  if (!issue_s(0)) return false;
+  for (int j = 0; j < nb; ++j) {
+    if (j + 1 < nb && !issue_s(j + 1)) return false;
+    const uint32_t nn = n0 + (uint32_t)j, b = nn & 1u;
+    if (!wait_warp(p, smem_u32(&s.att_p_full), nn & 1u, R_MMA, 25, idx)) return false;
+    if (!wait_warp(p, smem_u32(&s.att_o_free[b]), ((nn >> 1) & 1u) ^ 1u, R_MMA, 26, idx))
+      return false;
+    tc_fence_after();
+    const uint64_t so = (uint64_t)(ro.st * units);
+    if (elect_one()) {
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        tc_mma_f16(tmem + 128u + b * 64u, pd + (uint64_t)(kk * 2), vd + so + (uint64_t)(kk * 128),
+                   io, kk != 0);
+      tc_commit(smem_u32(&s.att_o_full[b]));
+      tc_commit(smem_u32(&s.empty[ro.st]));
+    }
+    __syncwarp();
+    ro.next(ns);
+  }
+  // The compute warps have read every S and O block of this instruction before TMEM is reused.
+  const uint32_t nl = n0 + (uint32_t)nb - 1u;
+  if (!wait_warp(p, smem_u32(&s.att_o_free[nl & 1u]), (nl >> 1) & 1u, R_MMA, 27, idx))
+    return false;
+  n = n0 + (uint32_t)nb;
+  return true;
+}
+
+template <bool PAIR, int KS>
+__device__ void run_mma(const Params& p, Smem& s, uint32_t tmem) {
+  // The whole warp runs this loop, converged: ring position, descriptors and flags are
+  // warp-uniform and one elected lane issues each tcgen05 operation. Per k-step the issuer does
+  // a barrier poll, a fence and the MMAs of the stage; descriptors are the stage-0 descriptors
+  // plus the stage's offset in 16-byte units.
+  const uint32_t NS = ring_n(p);
+  const uint32_t units = stage_bytes(p) >> 4;
+  const uint32_t ring0 = smem_u32(s.ring);
+  // A: K-major, 128-byte rows, 8-row groups 1024 B apart; a 16-wide K slice is 32 B (2 units).
+  const uint64_t adesc0 = sdesc_sw128(ring0, 16, 1024);
+  // B: N-major, 64-column atoms 8 KB apart (LBO), 8-row K groups 1024 B apart (SBO); a 16-deep
+  // K slice is 16 rows of 128 B (128 units).
+  const uint64_t bdesc0 = sdesc_sw128(ring0 + kGemmTileM * kGemmBK * 2, 8192, 1024);
+  RingPos rp;
+  uint32_t acc_n = 0, att_n = 0;
+  bool issued = false, synced = true;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  for (int it = 0;; ++it) {
+    const int slot = it % kSlots;
+    const uint32_t u = (uint32_t)(it / kSlots);
+    const int idx = instr_index(p, it);
+    if (!wait_warp(p, smem_u32(&s.instr_ready[slot]), u & 1u, R_MMA, 20, idx)) break;
+    const Instr& in = slot_instr(s, slot);
+    if (in.op == OP_END) break;
+    const Node& nd = slot_node(s, slot);
+    bool ok = true;
+    if (ks_has_gemm(KS) && in.op == OP_GEMM) {
+      const int nk = ring_stages(in);
+      if (PAIR && !synced) rp.align();  // mirrors the loader's ring sync
+      if (nk > 0) synced = true;
+      if (nk > 0 && PAIR && rank != 0) {
+        rp.advance((uint32_t)nk, NS);  // the even CTA issues the pair's MMAs
+        ++acc_n;
+      } else if (nk > 0) {
+        const uint32_t as = acc_n & 1u;
+        // the slot is free once every epilogue that read it (both CTAs' in pair mode) is done
+        if (!wait_warp(p, smem_u32(&s.acc_empty[as]), ((acc_n >> 1) & 1u) ^ 1u, R_MMA, 21, idx,
+                       PAIR))
+          break;
+        tc_fence_after();
+        const bool dual = (nd.flags & EPI_SILU_MUL) != 0;
+        const int tn = nd.tile_n;
+        const int ncol = PAIR ? tn / 2 : tn;  // B columns held by each CTA per weight
+        const uint32_t idesc = idesc_f16(nd.dtype == DT_BF16, tn, PAIR ? 256 : 128);
+        const uint32_t d = tmem + as * 256u;
+        const uint64_t up = (uint64_t)((ncol / 64) * (8192 >> 4));  // up-weight atoms
+        const uint32_t full0 = smem_u32(&s.full[0]), empty0 = smem_u32(&s.empty[0]);
+        const int done = dual ? mma_tile<PAIR, true>(p, full0, empty0, rp.st, rp.ph, NS, nk,
+                                                     adesc0, bdesc0, units, d, idesc, tn, up, idx)
+                              : mma_tile<PAIR, false>(p, full0, empty0, rp.st, rp.ph, NS, nk,
+                                                      adesc0, bdesc0, units, d, idesc, tn, up, idx);
+        if (done > 0) issued = true;
+        ok = done == nk;
+        rp.advance((uint32_t)nk, NS);
+        if (!ok) break;  // MMAs in flight are drained below
+        if (elect_one()) {
+          if (PAIR)
+            tc_commit_pair(smem_u32(&s.acc_full[as]), 3);
+          else
+            tc_commit(smem_u32(&s.acc_full[as]));
+        }
+        __syncwarp();
+        ++acc_n;
+      }
+    } else if (ks_has_attn_prefill(KS) && in.op == OP_ATTN_PREFILL) {
+      synced = false;
+      const int nb = ring_stages(in);
+      if (PAIR) {
+        report(p, MK_ERR_DEVICE_CHECK, idx, -1, in.op, 0, R_MMA, 35);  // refused by the host
+        break;
+      }
+      if (nb > 0) {
+        // TMEM columns 0..255 are reused: every GEMM epilogue still reading them is done first
+        bool w = true;
+        for (uint32_t k = 0; k < 2 && w; ++k)
+          w = wait_warp(p, smem_u32(&s.acc_empty[(acc_n + k) & 1u]),
+                        (((acc_n + k) >> 1) & 1u) ^ 1u, R_MMA, 21, idx);
+        if (!w) break;
+        tc_fence_after();
+        if (!mma_attn(p, s, rp.st, rp.ph, NS, nb, tmem, att_n, idx)) {
+          issued = true;
+          break;
+        }
+        issued = true;
+        rp.advance((uint32_t)nb, NS);
+      }
+    } else {
+      synced = false;
+      rp.advance((uint32_t)ring_stages(in), NS);  // stages consumed by the compute warpgroup
+    }
+    if (elect_one()) mbar_arrive(smem_u32(&s.slot_free[slot]));
+    __syncwarp();
+  }
+  if (ks_has_tmem(KS) && issued) {
+    if (elect_one()) {
+      if (PAIR)
+        tc_commit_pair(smem_u32(&s.drain), 1);
+      else
+        tc_commit(smem_u32(&s.drain));
+    }
+    __syncwarp();
+    wait_mbar_drain(smem_u32(&s.drain), 0);
+  }
+  __syncwarp();
+}
+
+// ------------------------------------------------------------------ compute warpgroup bodies
+
+// GEMM epilogue: TMEM -> registers (one row per thread), fused epilogue, then per 32-column chunk
+// a 32 x 32 block per warp staged in shared memory and stored with TMA. In pair mode each CTA
+// drains its own 128 rows of the 256-row tile. A split-tail tile (aux1 = number of K splits)
+// first writes its fp32 partial to scratch and releases TMEM; the last split to finish (tile
+// semaphore) sums the partials in split order and runs the epilogue; the others do not publish.
+template <bool PAIR>
+__device__ bool gemm_epilogue(const Params& p, Smem& s, const Instr& in, const Node& nd, int slot,
+                              uint32_t use, uint32_t tmem, uint32_t& acc_n, bool* publish,
+                              int idx) {
+  const int ct = (int)threadIdx.x - (kThreads - kCompute);
+  const int q = ct >> 5, lane = ct & 31;
+  if (!cw_wait(p, smem_u32(&s.deps_ready[slot]), use & 1u, 30, idx)) return false;
+  trace_mark(p, idx, 2);
+  const int nk = ring_stages(in);
+  const uint32_t as = acc_n & 1u;
+  if (nk > 0) {
+    if (!cw_wait(p, smem_u32(&s.acc_full[as]), (acc_n >> 1) & 1u, 31, idx)) return false;
+    tc_fence_after();
+  }
+  const int dt = nd.dtype;
+  const bool dual = (nd.flags & EPI_SILU_MUL) != 0;
+  const bool bias = (nd.flags & EPI_BIAS) != 0, relu = (nd.flags & EPI_RELU) != 0,
+             res = (nd.flags & EPI_RESIDUAL) != 0;
+  const int tn = nd.tile_n;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const int row0 = in.m0 + (int)rank * kGemmTileM + q * 32;  // this warp's 32 rows
+  const int row = row0 + lane;
+  const uint32_t tb = tmem + as * 256u + ((uint32_t)(q * 32) << 16);
+  auto release_tmem = [&]() {
+    if (nk > 0) {
+      tc_fence_before();
+      cw_sync();
+      if (ct == 0) {
+        if (PAIR && rank != 0)
+          mbar_arrive_cluster(mapa_shared(smem_u32(&s.acc_empty[as]), 0));
+        else
+          mbar_arrive(smem_u32(&s.acc_empty[as]));
+      }
+      ++acc_n;
+    }
+  };
+  if (nd.out.tmap < 0) {  // the host builds the output map of every GEMM node
+    if (ct == 0) report(p, MK_ERR_DEVICE_CHECK, idx, -1, nd.out.tmap, 0, R_COMPUTE, 36);
+    return false;
+  }
+  // Each warp stages its 32 x 32 block of a chunk in one of two 2 KB buffers (64-byte rows,
+  // 64-byte swizzle: 16-byte chunk j of row r at j ^ ((r >> 1) & 3), conflict-free) and one lane
+  // stores it with TMA; a buffer is rewritten once the store issued from it has read it.
+  const uint32_t xr0 = smem_u32(s.xr) + (uint32_t)q * 4096u;
+  const void* omap = tmap_at(p, nd.out.tmap);
+  auto store32 = [&](int c, float* v) {
+    const uint32_t buf = xr0 + (uint32_t)((c >> 5) & 1) * 2048u;
+    if (c >= 64) {
+      if (lane == 0) bulk_wait_read_1();
+      __syncwarp();
+    }
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const int col = in.n0 + c + g * 8;
+      const bool inside = row < nd.M && col < nd.N;
+      float* w = v + g * 8;
+      if (bias && inside) {
+        float b[8];
+        load8(nd.bias, row, col, dt, b);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) w[e] += b[e];
+      }
+      if (relu) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) w[e] = fmaxf(w[e], 0.0f);
+      }
+      if (res && inside) {
+        float b[8];
+        load8(nd.res, row, col, dt, b);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) w[e] += b[e];
+      }
+      const uint4 pk = pack8(w, dt);
+      const uint32_t dst = buf + (uint32_t)lane * 64u + (uint32_t)((g ^ ((lane >> 1) & 3)) << 4);
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(pk.x), "r"(pk.y),
+                   "r"(pk.z), "r"(pk.w)
+                   : "memory");
+    }
+    fence_proxy_async_shared();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(omap, buf, in.n0 + c, row0);
+      bulk_commit();
+    }
+  };
+  if (in.aux1 > 0) {
+    // split tail: this split's fp32 partial (gate columns, then up columns with SiLU·mul)
+    const int W = dual ? 2 * tn : tn, S = in.aux1, cl = PAIR ? 2 : 1;
+    const size_t sstride = (size_t)cl * kGemmTileM * W;  // next split, same rank
+    const float* base = reinterpret_cast<const float*>(nd.scratch.ptr) +
+                        ((size_t)in.slot * kGemmTileM + q * 32 + lane) * W;
+    float* mine = const_cast<float*>(base) + (size_t)in.split * sstride;
+    for (int c = 0; c < W; c += 32) {
+      uint32_t r[32];
+      if (nk > 0) {
+        tmem_ld32(tb + (uint32_t)c, r);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) r[i] = 0u;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        __stcg(reinterpret_cast<float4*>(mine + c) + i,
+               make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                           __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3])));
+    }
+    __threadfence();
+    cw_sync();
+    if (ct == 0) s.flag = atomicAdd(p.counters + in.sem, 1) == S - 1;
+    cw_sync();
+    if (!s.flag) {
+      release_tmem();
+      *publish = false;
+      return true;
+    }
+    __threadfence();
+    // The last split sums the partials in split order (its own from TMEM, so the order and the
+    // result do not depend on which split finishes last) and runs the epilogue. The next column
+    // block's partial loads are issued before the current block is summed.
+    auto sum32 = [&](int col, float* acc) {
+      uint32_t r[32];
+      if (nk > 0) {
+        tmem_ld32(tb + (uint32_t)col, r);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) r[i] = 0u;
+      }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+      for (int sp = 0; sp < S; ++sp) {
+        if (sp == in.split) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc[i] += __uint_as_float(r[i]);
+        } else {
+          const float4* src = reinterpret_cast<const float4*>(base + sp * sstride + col);
+          float4 t[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) t[i] = __ldcg(src + i);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            acc[4 * i] += t[i].x;
+            acc[4 * i + 1] += t[i].y;
+            acc[4 * i + 2] += t[i].z;
+            acc[4 * i + 3] += t[i].w;
+          }
+        }
+      }
+    };
+    for (int c = 0; c < tn; c += 32) {
+      // warm L2 -> L1 for the next block of every other split while this block is summed
+      if (c + 32 < tn)
+        for (int sp = 0; sp < S; ++sp)
+          if (sp != in.split) {
+            const float* nx = base + sp * sstride + c + 32;
+            asm volatile("prefetch.global.L1 [%0];" ::"l"(nx) : "memory");
+            if (dual) asm volatile("prefetch.global.L1 [%0];" ::"l"(nx + tn) : "memory");
+          }
+      float v[32];
+      sum32(c, v);
+      if (dual) {
+        float u[32];
+        sum32(tn + c, u);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = silu(v[i]) * u[i];
+      }
+      store32(c, v);
+    }
+    release_tmem();
+  } else {
+    for (int c = 0; c < tn; c += 32) {
+      uint32_t r[32], r2[32];
+      if (nk > 0) {
+        tmem_ld32(tb + (uint32_t)c, r);
+        if (dual) tmem_ld32(tb + (uint32_t)(tn + c), r2);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) r[i] = r2[i] = 0u;
+      }
+      float v[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        v[i] = __uint_as_float(r[i]);
+        if (dual) v[i] = silu(v[i]) * __uint_as_float(r2[i]);
+      }
+      store32(c, v);
+    }
+    release_tmem();
+  }
+  // the tile's stores are in global memory before its counters are released
+  if (lane == 0) {
+    bulk_wait_all();
+    fence_proxy_async_global();
+  }
+  return true;
+}
+
+// One 64-row weight stage of a GEMV for MT activation rows (compile-time), element type BF
+// (compile-time): acc[m][0..1] += sum_kk x[m][kk] * W[kk][col..col+1], W read from a 64-column
+// box in the 128-byte swizzled layout TMA writes. Four activations per shared-memory read; the
+// weight pair of each row is one 4-byte read (a warp covers one 128-byte row: no conflicts).
+template <int MT, bool BF, int UNROLL = 2>
+__device__ __forceinline__ void gemv_stage(const uint8_t* B, int ch, const float* xs,
+                                           int xstride, float (&acc)[8][2]) {
+#pragma unroll UNROLL
+  for (int kk = 0; kk < kGemvRows; kk += 4) {
+    float xv[MT][4];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      const float4 x4 = *reinterpret_cast<const float4*>(xs + m * xstride + kk);
+      xv[m][0] = x4.x;
+      xv[m][1] = x4.y;
+      xv[m][2] = x4.z;
+      xv[m][3] = x4.w;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int r = kk + u;  // 128-byte row r of the box; 16-byte chunk ch sits at ch ^ (r & 7)
+      const uint32_t raw = *reinterpret_cast<const uint32_t*>(B + r * 128 + ((ch ^ (r & 7)) << 4));
+      float f0, f1;
+      if (BF) {
+        f0 = __uint_as_float(raw << 16);
+        f1 = __uint_as_float(raw & 0xffff0000u);
+      } else {
+        f0 = __half2float(__ushort_as_half((uint16_t)(raw & 0xffffu)));
+        f1 = __half2float(__ushort_as_half((uint16_t)(raw >> 16)));
+      }
+#pragma unroll
+      for (int m = 0; m < MT; ++m) {
+        acc[m][0] = fmaf(xv[m][u], f0, acc[m][0]);
+        acc[m][1] = fmaf(xv[m][u], f1, acc[m][1]);
+      }
+    }
+  }
+}
+
+template <bool BF>
+__device__ __forceinline__ void gemv_stage_rows(int M, const uint8_t* B, int ch, const float* xs,
+                                                int xstride, float (&acc)[8][2]) {
+  switch (M) {
+    case 1: gemv_stage<1, BF>(B, ch, xs, xstride, acc); break;
+    case 2: gemv_stage<2, BF>(B, ch, xs, xstride, acc); break;
+    case 3: gemv_stage<3, BF>(B, ch, xs, xstride, acc); break;
+    case 4: gemv_stage<4, BF>(B, ch, xs, xstride, acc); break;
+    case 5: gemv_stage<5, BF>(B, ch, xs, xstride, acc); break;
+    case 6: gemv_stage<6, BF>(B, ch, xs, xstride, acc); break;
+    case 7: gemv_stage<7, BF>(B, ch, xs, xstride, acc); break;
+    default: gemv_stage<8, BF>(B, ch, xs, xstride, acc); break;
+  }
+}
+
+// The weight stages of a GEMV tile whose activations are all staged in shared memory: nk stages
+// from ring position (st, ph), each consumed and released in turn. Out of line with scalar
+// arguments, so the stage loop compiles on its own (inside the single large kernel function it ran
+// several times slower); the 2·MT sums leave through `out` once.
+template <int MT, bool BF>
+__device__ __noinline__ bool gemv_staged(const Params& p, uint32_t full0, uint32_t empty0,
+                                         const uint8_t* b0, uint32_t sb, uint32_t ns, uint32_t st,
+                                         uint32_t ph, int nk, int ch, const float* xs0, int kpad,
+                                         float* out, int idx) {
+  const int ct = (int)threadIdx.x - (kThreads - kCompute);
+  float acc[8][2];
+#pragma unroll
+  for (int m = 0; m < 8; ++m) acc[m][0] = acc[m][1] = 0.f;
+  for (int kb = 0; kb < nk; ++kb) {
+    if (!cw_wait(p, full0 + st * 8u, ph, 41, idx)) return false;
+    // all 64 rows unrolled: the stage's shared-memory reads issue ahead of their FMAs
+    gemv_stage<MT, BF, 16>(b0 + (size_t)st * sb, ch, xs0 + kb * kGemvRows, kpad, acc);
+    cw_sync();
+    if (ct == 0) mbar_arrive(empty0 + st * 8u);
+    if (++st == ns) {
+      st = 0;
+      ph ^= 1u;
+    }
+  }
+#pragma unroll
+  for (int m = 0; m < MT; ++m) {
+    out[2 * m] = acc[m][0];
+    out[2 * m + 1] = acc[m][1];
+  }
+  return true;
+}
+
+template <bool BF>
+__device__ bool gemv_staged_rows(int M, const Params& p, uint32_t full0, uint32_t empty0,
+                                 const uint8_t* b0, uint32_t sb, uint32_t ns, uint32_t st,
+                                 uint32_t ph, int nk, int ch, const float* xs0, int kpad,
+                                 float* out, int idx) {
+  switch (M) {
+    case 1: return gemv_staged<1, BF>(p, full0, empty0, b0, sb, ns, st, ph, nk, ch, xs0, kpad, out, idx);
+    case 2: return gemv_staged<2, BF>(p, full0, empty0, b0, sb, ns, st, ph, nk, ch, xs0, kpad, out, idx);
+    case 3: return gemv_staged<3, BF>(p, full0, empty0, b0, sb, ns, st, ph, nk, ch, xs0, kpad, out, idx);
+    case 4: return gemv_staged<4, BF>(p, full0, empty0, b0, sb, ns, st, ph, nk, ch, xs0, kpad, out, idx);
+    case 5: return gemv_staged<5, BF>(p, full0, empty0, b0, sb, ns, st, ph, nk, ch, xs0, kpad, out, idx);
+    case 6: return gemv_staged<6, BF>(p, full0, empty0, b0, sb, ns, st, ph, nk, ch, xs0, kpad, out, idx);
+    case 7: return gemv_staged<7, BF>(p, full0, empty0, b0, sb, ns, st, ph, nk, ch, xs0, kpad, out, idx);
+    default: return gemv_staged<8, BF>(p, full0, empty0, b0, sb, ns, st, ph, nk, ch, xs0, kpad, out, idx);
+  }
+}
+
+// GEMV tile: out[0..M) x [n0, n0 + w) for one K chunk; split partials reduced by the last
+// split to finish. The chunk's activations (normalised when the norm is fused) are staged once
+// in shared memory with batched loads. Each thread owns two adjacent output columns of the tile
+// (with SILU_MUL: threads 0-63 the gate columns, 64-127 the up columns) over every K row, so a
+// stage needs no cross-thread reduction. Weight stages arrive as 128-byte swizzled boxes:
+// unswizzled TMA writes of rows 128 bytes apart land on the same shared-memory banks ("Hand-
+// writing a Blackwell GEMM", step 4).
+__device__ bool gemv(const Params& p, Smem& s, const Instr& in, const Node& nd, int slot,
+                     uint32_t use, uint32_t& ring, bool* publish, int idx) {
+  const uint32_t NS = ring_n(p);
+  const int ct = (int)threadIdx.x - (kThreads - kCompute);
+  const int wp = ct >> 5, lane = ct & 31;
+  if (!cw_wait(p, smem_u32(&s.deps_ready[slot]), use & 1u, 40, idx)) return false;
+  trace_mark(p, idx, 2);
+  const int M = nd.M, dt = nd.dtype;
+  const bool dual = (nd.flags & EPI_SILU_MUL) != 0;
+  const bool norm = (nd.flags & EPI_RMSNORM_INPUT) != 0;
+  const int nk = ring_stages(in);
+  const int kpad = nk * kGemvRows;
+  const int kend = in.k0 + in.klen;
+  const bool staged = M * kpad <= kXrFloats;
+  if (norm) {
+    // RMS statistic of each whole input row (the norm is a flag of this GEMV)
+    for (int m = 0; m < M; ++m) {
+      float ss = 0.f;
+      for (int k = ct * 8; k < nd.K; k += kCompute * 8) {
+        float x[8];
+        load8(nd.a, m, k, dt, x);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+      }
+      ss = warp_sum(ss);
+      if (lane == 0) s.red_small[m][wp] = ss;
+    }
+    cw_sync();
+    if (ct < M)
+      s.rstd[ct] = rsqrtf((s.red_small[ct][0] + s.red_small[ct][1] + s.red_small[ct][2] +
+                           s.red_small[ct][3]) / (float)nd.K + nd.eps);
+    cw_sync();
+  }
+  auto stage_x = [&](int k_first, int rows, int stride) {
+    const int nv = rows / 8;
+    for (int v = ct; v < M * nv; v += kCompute) {
+      const int m = v / nv, kk = (v % nv) * 8, k = k_first + kk;
+      float x[8];
+      if (k < kend) {
+        load8(nd.a, m, k, dt, x);
+        if (norm) {
+          float g[8];
+          load8(nd.gamma, 0, k, dt, g);
+          const float r = s.rstd[m];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[e] = x[e] * r * g[e];
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = 0.f;
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) s.xr[m * stride + kk + e] = x[e];
+    }
+    cw_sync();
+  };
+  if (staged && nk > 0) stage_x(in.k0, kpad, kpad);
+  const int which = dual ? (ct >> 6) : 0;
+  const int col = dual ? 2 * (ct & 63) : 2 * ct;  // column pair inside this thread's weight
+  float acc[8][2];
+#pragma unroll
+  for (int m = 0; m < 8; ++m) acc[m][0] = acc[m][1] = 0.f;
+  if (staged && nk > 0) {
+    // this thread's column pair: box (which * 2 + col / 64), column col % 64 inside it
+    const int box = (dual ? which * 2 : 0) + (col >> 6), lc = col & 63;
+    float sums[16];
+    const bool ok =
+        dt == DT_BF16
+            ? gemv_staged_rows<true>(M, p, smem_u32(&s.full[0]), smem_u32(&s.empty[0]),
+                                     s.ring + box * 8192 + (lc & 7) * 2, stage_bytes(p), NS,
+                                     ring % NS, (ring / NS) & 1u, nk, lc >> 3, s.xr, kpad, sums,
+                                     idx)
+            : gemv_staged_rows<false>(M, p, smem_u32(&s.full[0]), smem_u32(&s.empty[0]),
+                                      s.ring + box * 8192 + (lc & 7) * 2, stage_bytes(p), NS,
+                                      ring % NS, (ring / NS) & 1u, nk, lc >> 3, s.xr, kpad, sums,
+                                      idx);
+    if (!ok) return false;
+#pragma unroll
+    for (int m = 0; m < 8; ++m)
+      if (m < M) {
+        acc[m][0] = sums[2 * m];
+        acc[m][1] = sums[2 * m + 1];
+      }
+    ring += (uint32_t)nk;
+  }
+  for (int kb = 0; kb < nk && !staged; ++kb) {
+    const float* xs;
+    int xstride;
+    if (staged) {
+      xs = s.xr + kb * kGemvRows;
+      xstride = kpad;
+    } else {
+      stage_x(in.k0 + kb * kGemvRows, kGemvRows, kGemvRows);
+      xs = s.xr;
+      xstride = kGemvRows;
+    }
+    const int st = (int)(ring % NS);
+    if (!cw_wait(p, smem_u32(&s.full[st]), (ring / NS) & 1u, 41, idx)) return false;
+    // this thread's column pair: box (which * 2 + col / 64), column col % 64 inside it
+    const int box = (dual ? which * 2 : 0) + (col >> 6), lc = col & 63;
+    const uint8_t* B = stage_ptr(s, p, st) + box * 8192 + (lc & 7) * 2;
+    if (dt == DT_BF16)
+      gemv_stage_rows<true>(M, B, lc >> 3, xs, xstride, acc);
+    else
+      gemv_stage_rows<false>(M, B, lc >> 3, xs, xstride, acc);
+    cw_sync();
+    if (ct == 0) mbar_arrive(smem_u32(&s.empty[st]));
+    ++ring;
+  }
+  const int S = in.aux1;
+  const int n = in.n0 + col;
+  const bool colok = n < nd.N;  // N is a multiple of 8: both columns are in or both out
+  if (S == 1) {
+    if (ct == 0) atomicAdd(p.counters + in.sem, 1);  // the semaphore counts every split
+  } else {
+    float* part = reinterpret_cast<float*>(nd.scratch.ptr);
+    if (colok) {
+#pragma unroll
+      for (int m = 0; m < 8; ++m)
+        if (m < M)
+          __stcg(reinterpret_cast<float2*>(part + (size_t)in.aux0 * nd.ldp +
+                                           ((size_t)which * M + m) * nd.N + n),
+                 make_float2(acc[m][0], acc[m][1]));
+    }
+    __threadfence();
+    cw_sync();
+    if (ct == 0) s.flag = (atomicAdd(p.counters + in.sem, 1) == S - 1);
+    cw_sync();
+    if (!s.flag) {
+      *publish = false;
+      return true;
+    }
+    __threadfence();
+    if (colok) {
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        if (m >= M) continue;
+        const float* c0 = part + ((size_t)which * M + m) * nd.N + n;
+        float2 t = make_float2(0.f, 0.f);
+        int q = 0;
+        for (; q + 4 <= S; q += 4) {  // four loads in flight, summed in split order
+          float2 v[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            v[u] = __ldcg(reinterpret_cast<const float2*>(c0 + (size_t)(q + u) * nd.ldp));
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            t.x += v[u].x;
+            t.y += v[u].y;
+          }
+        }
+        for (; q < S; ++q) {
+          const float2 v = __ldcg(reinterpret_cast<const float2*>(c0 + (size_t)q * nd.ldp));
+          t.x += v.x;
+          t.y += v.y;
+        }
+        acc[m][0] = t.x;
+        acc[m][1] = t.y;
+      }
+    }
+  }
+  if (dual) {
+    // gate and up halves of a column pair live in threads t and t + 64: exchange via smem
+    cw_sync();
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      if (m < M) {
+        s.xr[m * 256 + which * 128 + col] = acc[m][0];
+        s.xr[m * 256 + which * 128 + col + 1] = acc[m][1];
+      }
+    }
+    cw_sync();
+    if (which == 0) {
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        if (m < M) {
+          acc[m][0] = silu(s.xr[m * 256 + col]) * s.xr[m * 256 + 128 + col];
+          acc[m][1] = silu(s.xr[m * 256 + col + 1]) * s.xr[m * 256 + 128 + col + 1];
+        }
+      }
+    }
+  }
+  if (which == 0 && colok) {
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      if (m >= M) continue;
+      float y0 = acc[m][0], y1 = acc[m][1];
+      if (nd.flags & EPI_BIAS) {
+        y0 += load1(nd.bias, m, n, dt);
+        y1 += load1(nd.bias, m, n + 1, dt);
+      }
+      if (nd.flags & EPI_RELU) {
+        y0 = fmaxf(y0, 0.f);
+        y1 = fmaxf(y1, 0.f);
+      }
+      if (nd.flags & EPI_RESIDUAL) {
+        y0 += load1(nd.res, m, n, dt);
+        y1 += load1(nd.res, m, n + 1, dt);
+      }
+      store2(nd.out, m, n, dt, y0, y1);
+      if (nd.flags & NF_ROPE) {
+        // RoPE of the following node, on the rounded outputs it would read: the pair partner of
+        // column j of a 64-column head is j ^ 32, held by lane ^ 16 (whole heads per tile, every
+        // lane active: the host fuses only full-width tiles without a second weight)
+        const float r0 = h2f(f2h(y0, dt), dt), r1 = h2f(f2h(y1, dt), dt);
+        const float p0 = __shfl_xor_sync(FULL, r0, 16), p1 = __shfl_xor_sync(FULL, r1, 16);
+        const int qend = nd.hq * 64, kend = (nd.hq + nd.hkv) * 64;
+        if (n < kend) {
+          const int j = n & 63, i = j & 31;
+          const float sgn = j < 32 ? -1.f : 1.f;  // first half: x cos - x' sin; second: + x' sin
+          const float pos = (float)(nd.pos0 + m), l2t = log2f(nd.theta);
+          float sn0, cs0, sn1, cs1;
+          sincosf(pos * exp2f(-(2.0f * (float)i / 64.0f) * l2t), &sn0, &cs0);
+          sincosf(pos * exp2f(-(2.0f * (float)(i + 1) / 64.0f) * l2t), &sn1, &cs1);
+          const float z0 = r0 * cs0 + sgn * p0 * sn0, z1 = r1 * cs1 + sgn * p1 * sn1;
+          if (n < qend)
+            store2(nd.out_q, m, n, dt, z0, z1);
+          else
+            store2(nd.out_k, m, n - qend, dt, z0, z1);
+        } else if (nd.out_v.ptr) {
+          store2(nd.out_v, m, n - kend, dt, r0, r1);
+        }
+      }
+    }
+  }
+  *publish = true;
+  return true;
+}
+
+__device__ void ew_body(const Instr& in, const Node& nd) {
+  const int ct = (int)threadIdx.x - (kThreads - kCompute);
+  const int rows = min(nd.tile_m, nd.M - in.m0), cols = min(nd.tile_n, nd.N - in.n0);
+  const int nv = cols / 8, dt = nd.dtype;
+  for (int v = ct; v < rows * nv; v += kCompute) {
+    const int m = in.m0 + v / nv, n = in.n0 + (v % nv) * 8;
+    float a[8], b[8], y[8];
+    load8(nd.a, m, n, dt, a);
+    if (nd.ewop == EWOP_ADD || nd.ewop == EWOP_SILU_MUL) load8(nd.b, m, n, dt, b);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      switch (nd.ewop) {
+        case EWOP_ADD: y[e] = a[e] + b[e]; break;
+        case EWOP_RELU: y[e] = fmaxf(a[e], 0.f); break;
+        case EWOP_SILU_MUL: y[e] = silu(a[e]) * b[e]; break;
+        default: y[e] = a[e]; break;
+      }
+    }
+    store8(nd.out, m, n, dt, y);
+  }
+}
+
+__device__ void rmsnorm_body(const Instr& in, const Node& nd) {
+  const int ct = (int)threadIdx.x - (kThreads - kCompute);
+  const int wp = ct >> 5, lane = ct & 31;
+  const int rows = min(nd.tile_m, nd.M - in.m0), dt = nd.dtype;
+  for (int r = wp; r < rows; r += 4) {
+    const int m = in.m0 + r;
+    float ss = 0.f;
+    for (int k = lane * 8; k < nd.N; k += 256) {
+      float x[8];
+      load8(nd.a, m, k, dt, x);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ss += x[e] * x[e];
+    }
+    const float rstd = rsqrtf(warp_sum(ss) / (float)nd.N + nd.eps);
+    for (int k = lane * 8; k < nd.N; k += 256) {
+      float x[8], g[8];
+      load8(nd.a, m, k, dt, x);
+      load8(nd.gamma, 0, k, dt, g);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] = x[e] * rstd * g[e];
+      store8(nd.out, m, k, dt, x);
+    }
+  }
+}
+
+// RoPE rows: thread work item = (row, head, 8 consecutive pair indices); both halves of the
+// pairs arrive as 16-byte vectors and leave the same way.
+__device__ void rope_body(const Instr& in, const Node& nd) {
+  const int ct = (int)threadIdx.x - (kThreads - kCompute);
+  const int rows = min(nd.tile_m, nd.M - in.m0), dt = nd.dtype;
+  const int hd = nd.hd, half = hd / 2, nh = nd.hq + nd.hkv;
+  const int groups = half / 8;                 // 8-pair groups per head
+  const int items = nh * groups;
+  const float l2t = log2f(nd.theta);
+  for (int v = ct; v < rows * items; v += kCompute) {
+    const int m = in.m0 + v / items, it = v % items;
+    const int h = it / groups, i0 = (it % groups) * 8;
+    float x1[8], x2[8], y1[8], y2[8];
+    load8(nd.a, m, h * hd + i0, dt, x1);
+    load8(nd.a, m, h * hd + i0 + half, dt, x2);
+    const float pos = (float)(nd.pos0 + m);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float inv = exp2f(-(2.0f * (float)(i0 + e) / (float)hd) * l2t);
+      float sn, cs;
+      sincosf(pos * inv, &sn, &cs);
+      y1[e] = x1[e] * cs - x2[e] * sn;
+      y2[e] = x2[e] * cs + x1[e] * sn;
+    }
+    const Operand& o = h < nd.hq ? nd.out : nd.out_k;
+    const int hh = h < nd.hq ? h : h - nd.hq;
+    store8(o, m, hh * hd + i0, dt, y1);
+    store8(o, m, hh * hd + i0 + half, dt, y2);
+  }
+  if (nd.out_v.ptr) {
+    const int nvv = nd.hkv * hd / 8;
+    for (int v = ct; v < rows * nvv; v += kCompute) {
+      const int m = in.m0 + v / nvv, c = (v % nvv) * 8;
+      float x[8];
+      load8(nd.a, m, nh * hd + c, dt, x);
+      store8(nd.out_v, m, c, dt, x);
+    }
+  }
+}
+
+// Split-KV partial for kv group g = n0 and keys [k0, k0 + klen): per query head of the group
+// m = max s, l = sum e^{s - m}, o = sum e^{s - m} v   (head_dim 64, up to 128 keys).
+// Keys and values arrive by TMA in one ring stage, 128-byte swizzled (16-byte chunk c of row r
+// sits at chunk c ^ (r & 7)).
+__device__ bool attn_partial_body(const Params& p, Smem& s, const Instr& in, const Node& nd,
+                                  uint32_t& ring, int idx) {
+  const uint32_t NS = ring_n(p);
+  const int ct = (int)threadIdx.x - (kThreads - kCompute);
+  const int wp = ct >> 5, lane = ct & 31;
+  const int g = in.n0, G = nd.hq / nd.hkv, C = in.aux1, c = in.aux0;
+  const int kl = in.klen;
+  const int st = (int)(ring % NS);
+  if (!cw_wait(p, smem_u32(&s.full[st]), (ring / NS) & 1u, 42, idx)) return false;
+  const uint8_t* Ks = stage_ptr(s, p, st);
+  const uint8_t* Vs = stage_ptr(s, p, st) + 16384;
+  for (int hh = wp; hh < G; hh += 4) {
+    const int h = g * G + hh;
+    float qv[64];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) load8(nd.a, 0, h * 64 + i * 8, DT_BF16, qv + i * 8);
+    float sc[4], pr[4];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int j = lane + 32 * t;
+      float sv = -INFINITY;
+      if (j < kl) {
+        float dot = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          float kx[8];
+          unpack8(*reinterpret_cast<const uint4*>(Ks + j * 128 + ((i ^ (j & 7)) << 4)), DT_BF16,
+                  kx);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) dot = fmaf(qv[i * 8 + e], kx[e], dot);
+        }
+        sv = dot * nd.scale;
+      }
+      sc[t] = sv;
+      mx = fmaxf(mx, sv);
+    }
+    mx = warp_max(mx);
+    float l = 0.f;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      pr[t] = (lane + 32 * t < kl) ? expf(sc[t] - mx) : 0.f;
+      l += pr[t];
+    }
+    l = warp_sum(l);
+    // lane owns value columns 2*lane, 2*lane+1: 16-byte chunk lane/4, 4-byte word lane%4
+    float o0 = 0.f, o1 = 0.f;
+    const int chunk = lane >> 2, word = lane & 3;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      if (32 * t >= kl) continue;
+#pragma unroll 8
+      for (int jj = 0; jj < 32; ++jj) {
+        const int j = t * 32 + jj;
+        const float pj = __shfl_sync(FULL, pr[t], jj);
+        if (j < kl) {
+          const uint32_t vv = *reinterpret_cast<const uint32_t*>(
+              Vs + j * 128 + ((chunk ^ (j & 7)) << 4) + word * 4);
+          o0 = fmaf(pj, __uint_as_float(vv << 16), o0);
+          o1 = fmaf(pj, __uint_as_float(vv & 0xffff0000u), o1);
+        }
+      }
+    }
+    float* row = reinterpret_cast<float*>(nd.scratch.ptr) +
+                 ((size_t)(g * C + c) * G + hh) * nd.scratch.ld;
+    __stcg(reinterpret_cast<float2*>(row + lane * 2), make_float2(o0, o1));
+    if (lane == 0) {
+      __stcg(row + 64, mx);
+      __stcg(row + 65, l);
+    }
+  }
+  cw_sync();
+  if (ct == 0) mbar_arrive(smem_u32(&s.empty[st]));
+  ++ring;
+  return true;
+}
+
+// LSE merge of one kv group's partials: M = max m_c, L = sum l_c e^{m_c-M},
+// O = sum o_c e^{m_c-M} / L. Lanes hold chunks' statistics; value loads are batched by 8.
+__device__ void attn_reduce_body(const Instr& in, const Node& nd) {
+  const int ct = (int)threadIdx.x - (kThreads - kCompute);
+  const int wp = ct >> 5, lane = ct & 31;
+  const int g = in.n0, G = nd.hq / nd.hkv, C = in.aux1;
+  const float* sc = reinterpret_cast<const float*>(nd.scratch.ptr);
+  const int ld = nd.scratch.ld;
+  for (int hh = wp; hh < G; hh += 4) {
+    const int h = g * G + hh;
+    auto row = [&](int c) { return sc + ((size_t)(g * C + c) * G + hh) * ld; };
+    float mx = -INFINITY;
+    for (int c = lane; c < C; c += 32) mx = fmaxf(mx, __ldcg(row(c) + 64));
+    mx = warp_max(mx);
+    float L = 0.f;
+    for (int c = lane; c < C; c += 32) L += __ldcg(row(c) + 65) * expf(__ldcg(row(c) + 64) - mx);
+    L = warp_sum(L);
+    float o0 = 0.f, o1 = 0.f;
+    for (int c0 = 0; c0 < C; c0 += 8) {
+      float2 ov[8];
+      float mv[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (c0 + u < C) {
+          ov[u] = __ldcg(reinterpret_cast<const float2*>(row(c0 + u) + lane * 2));
+          mv[u] = __ldcg(row(c0 + u) + 64);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (c0 + u < C) {
+          const float w = expf(mv[u] - mx);
+          o0 = fmaf(ov[u].x, w, o0);
+          o1 = fmaf(ov[u].y, w, o1);
+        }
+      }
+    }
+    const float inv = 1.0f / L;
+    const __nv_bfloat162 y = __floats2bfloat162_rn(o0 * inv, o1 * inv);
+    *reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(nd.out.ptr) + h * 64 +
+                                       lane * 2) = y;
+  }
+}
+
+// Prefill attention, compute side: thread t of the warpgroup owns query row m0 + t (TMEM lane t).
+// Per key block j: S_j from TMEM, scaled to the log2 domain and masked (key beyond the causal
+// limit of the row or beyond the instruction's key range); online softmax with running max m and
+// sum l (flash attention: a block that raises the max rescales what came before by
+// 2^(m_old - m_new)); P_j = 2^(s - m) as bf16 into shared memory for the P V MMA; the previous
+// block's P V joins the fp32 output accumulator in registers once it completes. At the end the
+// row is divided by l and stored as bf16. `n` counts attention blocks on this SM, as in the MMA
+// warp.
+__device__ __noinline__ bool attn_prefill_body(const Params& p, Smem& s, const Instr& in,
+                                               const Node& nd, uint32_t tmem, uint32_t& n,
+                                               int idx) {
+  const int ct = (int)threadIdx.x - (kThreads - kCompute);
+  const int lane = ct & 31;
+  const uint32_t lanes = (uint32_t)((ct >> 5) * 32) << 16;  // this warp's TMEM lane quarter
+  const int nb = ring_stages(in);
+  const int row = in.m0 + ct;
+  const int qpos = nd.pos0 + row;
+  const int kmax = in.klen;
+  const float sl2 = nd.scale * 1.4426950408889634f;  // scores in log2 units
+  uint8_t* P = reinterpret_cast<uint8_t*>(s.xr);
+  float o[64];
+#pragma unroll
+  for (int i = 0; i < 64; ++i) o[i] = 0.f;
+  float m = -INFINITY, l = 0.f, alpha_prev = 1.f;
+  const uint32_t n0 = n;
+  auto add_o = [&](uint32_t nn, float alpha) -> bool {
+    const uint32_t b = nn & 1u;
+    if (!cw_wait(p, smem_u32(&s.att_o_full[b]), (nn >> 1) & 1u, 44, idx)) return false;
+    tc_fence_after();
+    uint32_t r0[32], r1[32];
+    tmem_ld32(tmem + 128u + b * 64u + lanes, r0);
+    tmem_ld32(tmem + 128u + b * 64u + 32u + lanes, r1);
+    tmem_ld_wait();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&s.att_o_free[b]));
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      o[i] = fmaf(o[i], alpha, __uint_as_float(r0[i]));
+      o[32 + i] = fmaf(o[32 + i], alpha, __uint_as_float(r1[i]));
+    }
+    return true;
+  };
+  for (int j = 0; j < nb; ++j) {
+    const uint32_t nn = n0 + (uint32_t)j, b = nn & 1u;
+    if (!cw_wait(p, smem_u32(&s.att_s_full[b]), (nn >> 1) & 1u, 43, idx)) return false;
+    tc_fence_after();
+    uint32_t r0[32], r1[32];
+    tmem_ld32(tmem + b * 64u + lanes, r0);
+    tmem_ld32(tmem + b * 64u + 32u + lanes, r1);
+    tmem_ld_wait();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&s.att_s_free[b]));
+    const int key0 = j * kAttnKeyBlock;
+    const int lim = nd.causal ? min(kmax, qpos + 1) : kmax;  // keys [0, lim) are visible
+    float sv[64];
+#pragma unroll
+    for (int c = 0; c < 64; ++c) {
+      const float x = __uint_as_float(c < 32 ? r0[c] : r1[c - 32]) * sl2;
+      sv[c] = key0 + c < lim ? x : -INFINITY;
+    }
+    float mx4[4] = {sv[0], sv[1], sv[2], sv[3]};
+#pragma unroll
+    for (int c = 4; c < 64; ++c) mx4[c & 3] = fmaxf(mx4[c & 3], sv[c]);
+    const float mj = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+    const float mn = fmaxf(m, mj);
+    const bool none = mn == -INFINITY;  // no visible key yet
+    const float alpha = none ? 1.f : ex2(m - mn);
+    const float mo = none ? 0.f : mn;   // masked scores give 2^-inf = 0 either way
+    float ls4[4] = {0.f, 0.f, 0.f, 0.f};
+    uint4 pk[8];
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch) {
+      float pv[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        pv[e] = ex2(sv[ch * 8 + e] - mo);
+        ls4[e & 3] += pv[e];
+      }
+      pk[ch] = pack8(pv, DT_BF16);
+    }
+    const float ls = (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
+    l = fmaf(l, alpha, ls);
+    m = mn;
+    // The previous block's P V (weighted with the previous maximum) joins the accumulator; after
+    // it completes the P buffer may be overwritten.
+    if (j > 0 && !add_o(nn - 1u, alpha_prev)) return false;
+    alpha_prev = alpha;
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch)
+      *reinterpret_cast<uint4*>(P + ct * 128 + ((ch ^ (ct & 7)) << 4)) = pk[ch];
+    fence_proxy_async_shared();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&s.att_p_full));
+  }
+  if (nb > 0 && !add_o(n0 + (uint32_t)nb - 1u, alpha_prev)) return false;
+  n = n0 + (uint32_t)nb;
+  if (row < nd.M) {
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch) {
+      float v[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[e] = o[ch * 8 + e] * inv;
+      store8(nd.out, row, in.n0 * 64 + ch * 8, DT_BF16, v);
+    }
+  }
+  return true;
+}
+
+template <bool PAIR, int KS>
+__device__ void run_compute(const Params& p, Smem& s, uint32_t tmem) {
+  const uint32_t NS = ring_n(p);
+  const int ct = (int)threadIdx.x - (kThreads - kCompute);
+  uint32_t ring = 0, acc_n = 0, att_n = 0;
+  bool synced = true;  // pair-mode ring sync (see load_gemm)
+  for (int it = 0;; ++it) {
+    const int slot = it % kSlots;
+    const uint32_t use = (uint32_t)(it / kSlots);
+    const int idx = instr_index(p, it);
+    if (!cw_wait(p, smem_u32(&s.instr_ready[slot]), use & 1u, 32, idx)) break;
+    const Instr& in = slot_instr(s, slot);
+    if (in.op == OP_END) break;
+    const Node& nd = slot_node(s, slot);
+    if (p.trace && ct == 0) p.trace[(size_t)idx * kTraceWords + 0] = globaltimer();
+    bool ok = true, publish = true;
+    if (in.op != OP_GEMM) synced = false;
+    switch (in.op) {
+      case OP_GEMM:
+        if constexpr (ks_has_gemm(KS)) {
+          if (PAIR && !synced) ring = ring_align(ring, NS);  // mirrors the loader's ring sync
+          if (ring_stages(in) > 0) synced = true;
+          ok = gemm_epilogue<PAIR>(p, s, in, nd, slot, use, tmem, acc_n, &publish, idx);
+          ring += (uint32_t)ring_stages(in);
+        }
+        break;
+      case OP_GEMV:
+        if constexpr (ks_has_gemv(KS)) ok = gemv(p, s, in, nd, slot, use, ring, &publish, idx);
+        break;
+      case OP_NOOP:
+        break;
+      case OP_ATTN_PARTIAL:
+        if constexpr (ks_has_gemv(KS)) {
+          ok = cw_wait(p, smem_u32(&s.deps_ready[slot]), use & 1u, 33, idx);
+          trace_mark(p, idx, 2);
+          ok = ok && attn_partial_body(p, s, in, nd, ring, idx);
+          if (ok && (nd.flags & NF_ATTN_FUSED)) {
+            // the last partial of the key/value head to finish combines the head's partials
+            __threadfence();
+            cw_sync();
+            if (ct == 0) s.flag = atomicAdd(p.counters + in.sem, 1) == in.aux1 - 1;
+            cw_sync();
+            if (s.flag) {
+              __threadfence();
+              attn_reduce_body(in, nd);
+            } else {
+              publish = false;
+            }
+          }
+        }
+        break;
+      case OP_ATTN_PREFILL:
+        if constexpr (ks_has_attn_prefill(KS)) {
+          // inputs reach this warpgroup only through the loader and the MMAs, which wait
+          trace_mark(p, idx, 2);
+          ok = attn_prefill_body(p, s, in, nd, tmem, att_n, idx);
+          ring += (uint32_t)ring_stages(in);
+        }
+        break;
+      default:
+        ok = cw_wait(p, smem_u32(&s.deps_ready[slot]), use & 1u, 33, idx);
+        if (!ok) break;
+        trace_mark(p, idx, 2);
+        if (ks_has_rows(KS) && in.op == OP_EW) ew_body(in, nd);
+        else if (ks_has_rows(KS) && in.op == OP_RMSNORM) rmsnorm_body(in, nd);
+        else if (ks_has_rows(KS) && in.op == OP_ROPE) rope_body(in, nd);
+        else if (ks_has_gemv(KS) && in.op == OP_ATTN_REDUCE) attn_reduce_body(in, nd);
+        else {
+          if (ct == 0) report(p, MK_ERR_DEVICE_CHECK, idx, -1, in.op, 0, R_COMPUTE, 34);
+          ok = false;
+        }
+        break;
+    }
+    if (!ok) break;
+    trace_mark(p, idx, 3);
+    // Publish: every thread's stores are ordered before the release increments.
+    __threadfence();
+    cw_sync();
+    if (ct == 0) {
+      if (publish && in.n_dst > 0) {
+        fence_proxy_async_global();
+        for (int j = 0; j < in.n_dst; ++j)
+          red_release_add(p.counters + __ldg(p.dst_list + in.dst_off + j), 1);
+      }
+      if (p.trace) {
+        p.trace[(size_t)idx * kTraceWords + 4] = globaltimer();
+        p.trace[(size_t)idx * kTraceWords + 5] = blockIdx.x;
+      }
+      mbar_arrive(smem_u32(&s.slot_free[slot]));
+    }
+  }
+}
+
+// ------------------------------------------------------------------ the kernel
+
+template <bool PAIR, int KS>
+__global__ void __launch_bounds__(kThreads, 1) megakernel(const __grid_constant__ Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                     ~static_cast<uintptr_t>(1023));
+  const int warp = (int)threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kMaxStages; ++i) {
+      mbar_init(smem_u32(&s.full[i]), 1);
+      mbar_init(smem_u32(&s.empty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&s.acc_full[i]), 1);
+      mbar_init(smem_u32(&s.acc_empty[i]), PAIR ? 2 : 1);  // both epilogues of a pair
+    }
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(smem_u32(&s.instr_ready[i]), 1);
+      mbar_init(smem_u32(&s.deps_ready[i]), 1);
+      mbar_init(smem_u32(&s.slot_free[i]), 3);  // loader, MMA issuer, compute warpgroup
+    }
+    mbar_init(smem_u32(&s.drain), 1);
+    mbar_init(smem_u32(&s.go), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&s.att_s_full[i]), 1);   // tcgen05.commit
+      mbar_init(smem_u32(&s.att_s_free[i]), 4);   // one lane per compute warp
+      mbar_init(smem_u32(&s.att_o_full[i]), 1);
+      mbar_init(smem_u32(&s.att_o_free[i]), 4);
+    }
+    mbar_init(smem_u32(&s.att_p_full), 4);
+    mbar_fence_init();
+  }
+  if (ks_has_tmem(KS) && warp == 2) {
+    if (PAIR) {
+      tmem_alloc_pair(smem_u32(&s.tmem_base), 512);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(&s.tmem_base), 512);
+      tmem_relinquish();
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (PAIR) cluster_sync();  // the peer's barriers are initialised before any remote arrive
+  tc_fence_after();
+  const uint32_t tmem = ks_has_tmem(KS) ? s.tmem_base : 0u;
+
+  if (warp == 0) {
+    run_scheduler<KS>(p, s);
+  } else if (warp == 1) {
+    run_loader<PAIR, KS>(p, s);
+  } else if (warp == 2) {
+    run_mma<PAIR, KS>(p, s, tmem);
+  } else if (warp >= 4) {
+    run_compute<PAIR, KS>(p, s, tmem);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (PAIR) cluster_sync();  // neither CTA leaves while its peer may still address it
+  if (ks_has_tmem(KS) && warp == 2) {
+    tc_fence_after();
+    if (PAIR)
+      tmem_dealloc_pair(tmem, 512);
+    else
+      tmem_dealloc(tmem, 512);
+  }
+  // The CTA that finishes last (after every other CTA's work, including a drained abort)
+  // publishes the run's status and zeroes the counters, so the next run needs no host reset.
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s.flag = atomicAdd(p.done, 1) == (int)gridDim.x - 1;
+  }
+  __syncthreads();
+  if (s.flag) {
+    __threadfence();
+    for (int i = threadIdx.x; i < p.n_counters; i += kThreads) {
+      const int v = __ldcg(p.counters + i);
+      if (p.snapshot) p.snapshot[i] = v;
+      p.counters[i] = 0;
+    }
+    if (threadIdx.x < kStatusWords) {
+      p.last_status[threadIdx.x] = __ldcg(p.status + threadIdx.x);
+      p.status[threadIdx.x] = 0;
+    }
+    if (threadIdx.x == 0) *p.done = 0;
+  }
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ host launch stubs
+
+// The host entry points of one specialisation; each translation unit that instantiates a
+// specialisation returns them from a plain function (variant_*), the dispatcher picks one.
+struct KernelVariant {
+  cudaError_t (*configure)(size_t smem);
+  cudaError_t (*launch)(const Params& p, int grid, size_t smem, cudaStream_t stream);
+  cudaError_t (*clusters_resident)(size_t smem, int* n);  // 2-CTA clusters resident at once
+};
+
+template <bool PAIR, int KS>
+cudaError_t configure_variant(size_t smem) {
+  return cudaFuncSetAttribute(megakernel<PAIR, KS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)smem);
+}
+
+template <bool PAIR, int KS>
+cudaError_t clusters_resident_variant(size_t smem, int* n) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaOccupancyMaxActiveClusters(n, megakernel<PAIR, KS>, &cfg);
+}
+
+template <bool PAIR, int KS>
+cudaError_t launch_variant(const Params& p, int grid, size_t smem, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  if (PAIR) {
+    // 2-CTA clusters; co-residency of the whole grid is checked at compile time
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+  } else {
+    attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs co-resident (they wait on each other)
+    attr[0].val.cooperative = 1;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, megakernel<PAIR, KS>, p);
+}
+
+template <bool PAIR, int KS>
+KernelVariant make_variant() {
+  return {&configure_variant<PAIR, KS>, &launch_variant<PAIR, KS>,
+          &clusters_resident_variant<PAIR, KS>};
+}
+
+KernelVariant variant_all(bool pair);
+KernelVariant variant_gemm(bool pair);
+KernelVariant variant_decode();
+KernelVariant variant_prefill();
+
+}  // namespace mk

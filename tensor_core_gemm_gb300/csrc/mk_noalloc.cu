@@ -14,12 +14,8 @@
 #include <string.h>
 
 #include "mk_internal.h"
+#include "mk_launch.h"
 
-namespace mk {
-cudaError_t launch_megakernel(const Params& p, int grid, size_t smem, cudaStream_t s, bool pair);
-cudaError_t configure_megakernel(size_t smem);
-size_t megakernel_smem_bytes();
-}  // namespace mk
 
 using namespace mk;
 
@@ -192,8 +188,8 @@ extern "C" mk_status mk_gemv_noalloc(const void* x, const void* w, void* out, in
   p.n_tmaps = k > 0 ? 1 : 0;
   p.n_counters = (int32_t)tiles;
   p.timeout_ns = 2000000000ull;
-  p.stages = kStages;
-  e = launch_megakernel(p, sms, megakernel_smem_bytes(), st, false);
+  p.stages = kPairStages;  // GEMV tiles only: 32 KB stages
+  e = launch_megakernel(p, sms, megakernel_smem_bytes(), st, false, KS_DECODE);
   if (e != cudaSuccess) return fail(MK_ERR_CUDA, "launch", e);
 
   if (status) {

@@ -15,14 +15,7 @@
 #include <new>
 
 #include "mk_internal.h"
-
-namespace mk {
-// Launch stub and shared-memory size, defined next to the kernel.
-cudaError_t launch_megakernel(const Params& p, int grid, size_t smem, cudaStream_t s, bool pair);
-cudaError_t configure_megakernel(size_t smem);
-cudaError_t pair_clusters_resident(size_t smem, int* n);
-size_t megakernel_smem_bytes();
-}  // namespace mk
+#include "mk_launch.h"
 
 using namespace mk;
 
@@ -36,8 +29,25 @@ struct mk_plan {
   size_t scratch_bytes = 0;
   size_t smem = 0;
   int grid = 0;
+  int kernel_set = KS_ALL;  // specialisation launched by mk_run
   Params params{};
 };
+
+// The smallest kernel specialisation that runs every instruction of the list (KS_ALL when
+// kernel_set = 1 asks for the general kernel); CTA-pair plans outside KS_GEMM run KS_ALL.
+static int pick_kernel_set(const std::vector<Instr>& instrs, const mk_compile_opts& o) {
+  if (o.kernel_set == 1) return KS_ALL;
+  int ks = KS_ALL;
+  for (int cand : {KS_GEMM, KS_DECODE, KS_PREFILL}) {
+    bool ok = true;
+    for (const Instr& in : instrs) ok = ok && ks_covers(cand, in.op);
+    if (ok) {
+      ks = cand;
+      break;
+    }
+  }
+  return launched_kernel_set(ks, o.cluster == 2);
+}
 
 #define CUDA_TRY(call)                                                                    \
   do {                                                                                    \
@@ -119,6 +129,10 @@ mk_status check_kernel_support(const std::vector<TensorRec>& ts, const std::vect
   }
   if (pair && o.n_sm % 2) {
     set_error("mk_compile: CTA pairs need an even n_sm");
+    return MK_ERR_UNSUPPORTED;
+  }
+  if (o.kernel_set != 0 && o.kernel_set != 1) {
+    set_error("mk_compile: kernel_set is 0 (smallest specialisation) or 1 (general kernel)");
     return MK_ERR_UNSUPPORTED;
   }
   if (o.gemv_tile_n != 256 || o.gemv_kstep % kGemvRows || o.gemv_max_m > 8 || o.gemv_max_m < 0) {
@@ -498,6 +512,7 @@ extern "C" mk_status mk_compile(mk_graph_t g, const mk_compile_opts* opts_in, mk
         if (p->hp.src_list[2 * (in.src_off + s)] == o.debug_counter)
           p->hp.src_list[2 * (in.src_off + s) + 1] += o.debug_extra;
   }
+  p->kernel_set = pick_kernel_set(p->hp.instrs, o);
   if (o.dry_run) {
     *out = p;
     return MK_OK;
@@ -572,7 +587,7 @@ extern "C" mk_status mk_compile(mk_graph_t g, const mk_compile_opts* opts_in, mk
   }
   if (e == cudaSuccess && o.cluster == 2) {
     int clusters = 0;
-    e = pair_clusters_resident(p->smem, &clusters);
+    e = pair_clusters_resident(p->smem, p->kernel_set, &clusters);
     if (e == cudaSuccess && clusters < o.n_sm / 2) {
       set_error("mk_compile: only %d CTA pairs can be resident, %d needed", clusters, o.n_sm / 2);
       cudaFree(p->d_mem);
@@ -603,7 +618,13 @@ extern "C" mk_status mk_compile(mk_graph_t g, const mk_compile_opts* opts_in, mk
   pr.n_tmaps = (int32_t)maps.size();
   pr.n_counters = (int32_t)n_ctr;
   pr.l2_prefetch = std::min(std::max(o.l2_prefetch, 0), kSlots);
-  pr.stages = o.cluster == 2 ? kPairStages : kStages;
+  // 48 KB stages only where a single-CTA GEMM tile needs them; every other ring user (a GEMV
+  // weight tile, an attention key/value chunk or prefill block) fits 32 KB, so such plans
+  // prefetch 192 KB of operands per SM instead of 128 KB.
+  bool single_gemm = false;
+  for (const Instr& in : p->hp.instrs) single_gemm |= in.op == OP_GEMM;
+  single_gemm &= o.cluster != 2;
+  pr.stages = single_gemm ? kStages : kPairStages;
   pr.timeout_ns = (uint64_t)(o.timeout_ms > 0 ? o.timeout_ms : 2000) * 1000000ull;
   p->grid = o.n_sm;
   p->on_device = true;
@@ -618,7 +639,8 @@ extern "C" mk_status mk_run(mk_plan_t p, void* stream) {
   }
   cudaStream_t s = (cudaStream_t)stream;
   if (p->params.n_instr == 0) return MK_OK;
-  CUDA_TRY(launch_megakernel(p->params, p->grid, p->smem, s, p->opts.cluster == 2));
+  CUDA_TRY(launch_megakernel(p->params, p->grid, p->smem, s, p->opts.cluster == 2,
+                             p->kernel_set));
   return MK_OK;
 }
 
@@ -705,6 +727,7 @@ extern "C" mk_status mk_plan_stats(mk_plan_t p, mk_stats* s) {
     if (in.op < 16) s->per_op[in.op]++;
   s->smem_bytes = (int64_t)p->smem;
   s->scratch_bytes = (int64_t)p->scratch_bytes;
+  s->kernel_set = p->kernel_set;
   return MK_OK;
 }
 

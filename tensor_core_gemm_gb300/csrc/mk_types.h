@@ -9,6 +9,12 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#ifdef __CUDACC__
+#define MK_HD __host__ __device__
+#else
+#define MK_HD
+#endif
+
 namespace mk {
 
 enum Op : uint16_t {
@@ -135,5 +141,28 @@ constexpr int kGemvRows = 64;          // K rows per stage for GEMV (x 256 colum
 constexpr int kAttnChunkMax = 128;     // keys per split-KV partial handled by one instruction
 constexpr int kAttnTileQ = 128;        // query rows of one prefill attention instruction
 constexpr int kAttnKeyBlock = 64;      // keys per ring stage of prefill attention (Q + K + V = 32 KB)
+
+// Specialisations of the kernel by the instruction kinds they run. The host launches the
+// smallest one that covers every instruction of a plan: a specialisation leaves out the code,
+// and with it the register pressure, of every role path it never meets.
+enum KernelSet : int32_t {
+  KS_ALL = 0,      // every instruction kind
+  KS_GEMM = 1,     // tcgen05 GEMM tiles only
+  KS_DECODE = 2,   // GEMV tiles, split-KV attention partials and combines, row instructions
+  KS_PREFILL = 3,  // GEMM tiles, causal prefill attention, row instructions
+};
+MK_HD constexpr bool ks_has_gemm(int ks) { return ks != KS_DECODE; }
+MK_HD constexpr bool ks_has_gemv(int ks) { return ks == KS_ALL || ks == KS_DECODE; }
+MK_HD constexpr bool ks_has_attn_prefill(int ks) { return ks == KS_ALL || ks == KS_PREFILL; }
+MK_HD constexpr bool ks_has_rows(int ks) { return ks != KS_GEMM; }
+MK_HD constexpr bool ks_has_tmem(int ks) { return ks_has_gemm(ks) || ks_has_attn_prefill(ks); }
+MK_HD constexpr bool ks_covers(int ks, int op) {
+  return op == OP_NOOP || op == OP_END                ? true
+         : op == OP_GEMM                              ? ks_has_gemm(ks)
+         : op == OP_GEMV || op == OP_ATTN_PARTIAL ||
+                   op == OP_ATTN_REDUCE               ? ks_has_gemv(ks)
+         : op == OP_ATTN_PREFILL                      ? ks_has_attn_prefill(ks)
+                                                      : ks_has_rows(ks);
+}
 
 }  // namespace mk

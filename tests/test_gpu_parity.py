@@ -684,3 +684,35 @@ def test_decode_rope_fused_and_unfused_agree():
         outs.append({k: f32(wl.data[wl.info[k]]) for k in ("qr", "kc", "vc", "out")})
     for k in ("qr", "kc", "vc", "out"):
         assert_close(outs[0][k], outs[1][k], f"fused vs unfused {k}")
+
+
+@pytest.mark.parametrize("kind", ["decode", "prefill", "gemm", "gemm_pair", "mlp3"])
+def test_kernel_specialisations_bit_identical(kind):
+    """The specialisation mk_run picks for a plan and the general kernel (kernel_set = 1) run
+    the same instruction bodies, so their outputs agree bit for bit; the specialisation is the
+    one the plan statistics name."""
+    sh = workloads.DecoderShape(layers=2, hidden=512, n_q_heads=8, n_kv_heads=2, head_dim=64,
+                                ffn=1024)
+    pair = dict(gemm_tile_m=256, cluster=2)
+    make, opts, want = {
+        "decode": (lambda: workloads.decode(sh, kv_len=130, device=DEV, seed=9), {}, 2),
+        "prefill": (lambda: workloads.prefill(sh, tokens=320, device=DEV, seed=3), {}, 3),
+        "gemm": (lambda: workloads.gemm(640, 768, 1088, device=DEV, seed=4), {}, 1),
+        "gemm_pair": (lambda: workloads.gemm(640, 768, 1088, device=DEV, seed=4), pair, 1),
+        "mlp3": (lambda: workloads.mlp3(device=DEV), dict(gemm_tile_n=64), 1),
+    }[kind]
+    outs = []
+    for ks in (0, 1):
+        wl = make()
+        plan, _ = run(wl, kernel_set=ks, **opts)
+        assert plan.stats()["kernel_set"] == (want if ks == 0 else 0)
+        outs.append([t.clone() for t in wl.data])
+    for i, (a, b) in enumerate(zip(*outs)):
+        assert torch.equal(a.view(torch.int16) if a.element_size() == 2 else a,
+                           b.view(torch.int16) if b.element_size() == 2 else b), f"tensor {i}"
+
+
+def test_kernel_set_option_validated():
+    g, _ = workloads.build_graph(workloads.gemm(64, 64, 64).desc, None)
+    with pytest.raises(Exception, match="kernel_set"):
+        g.compile(kernel_set=2)

@@ -257,3 +257,42 @@ def test_empty_graph_and_empty_matmul():
     for m in (1, 200):
         py, c = assert_same_plan(workloads.gemm(m, 64, 0, dtype="bf16").desc, dict(n_sm=8))
         assert c.stats()["n_instr"] == 1 + (m > 128)
+
+
+# ------------------------------------------------------------------ kernel specialisation
+
+def _mixed_gemv_gemm(h=256):
+    """One GEMV-sized product (1 row) and one GEMM-sized product (256 rows) sharing a weight."""
+    t = [{"rows": h, "cols": h, "dtype": "bf16"}, {"rows": 1, "cols": h, "dtype": "bf16"},
+         {"rows": 1, "cols": h, "dtype": "bf16"}, {"rows": 256, "cols": h, "dtype": "bf16"},
+         {"rows": 256, "cols": h, "dtype": "bf16"}]
+    w = (0, 0, 0, h, h)
+    return {"tensors": t, "nodes": [
+        {"kind": "matmul", "a": (1, 0, 0, 1, h), "b": w, "c": (2, 0, 0, 1, h)},
+        {"kind": "matmul", "a": (3, 0, 0, 256, h), "b": w, "c": (4, 0, 0, 256, h)}]}
+
+
+def test_kernel_specialisation_choice():
+    """mk_run launches the smallest specialisation whose instruction kinds cover the plan:
+    0 general, 1 GEMM tiles only, 2 decode (GEMV, split-KV attention, rows), 3 prefill (GEMM,
+    prefill attention, rows); CTA-pair kernels exist for the GEMM-only and general sets."""
+    sh = workloads.DecoderShape(layers=2, hidden=256, n_q_heads=4, n_kv_heads=2, head_dim=64,
+                                ffn=512)
+    pair = dict(gemm_tile_m=256, cluster=2)
+    unf = _graphs.mlp_unfused(m=300, h=256, layers=2, dtype="f16")
+    cases = [
+        (workloads.gemm(512, 512, 256).desc, dict(n_sm=8), 1),
+        (workloads.gemm(512, 512, 256).desc, dict(n_sm=8, **pair), 1),
+        (workloads.mlp3().desc, dict(n_sm=152, gemm_tile_n=64), 1),
+        (workloads.gemm(1, 3072, 2048, dtype="bf16").desc, dict(n_sm=152), 2),
+        (workloads.decode(sh, kv_len=200).desc, dict(n_sm=40), 2),
+        (workloads.decode(sh, kv_len=200).desc, dict(n_sm=40, fuse_rope=0, fuse_attn_reduce=0), 2),
+        (workloads.prefill(sh, tokens=384).desc, dict(n_sm=37), 3),
+        (unf, dict(n_sm=16, gemm_tile_n=128), 3),
+        (unf, dict(n_sm=16, **pair), 0),  # GEMM + rows on pairs: the general pair kernel
+        (_mixed_gemv_gemm(), dict(n_sm=16), 0),
+        (workloads.gemm(512, 512, 256).desc, dict(n_sm=8, kernel_set=1), 0),
+        (workloads.decode(sh, kv_len=200).desc, dict(n_sm=40, kernel_set=1), 0),
+    ]
+    for desc, opts, want in cases:
+        assert _dry(desc, **opts).stats()["kernel_set"] == want, (opts, want)
