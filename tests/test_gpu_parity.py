@@ -686,17 +686,23 @@ def test_decode_rope_fused_and_unfused_agree():
         assert_close(outs[0][k], outs[1][k], f"fused vs unfused {k}")
 
 
-@pytest.mark.parametrize("kind", ["decode", "prefill", "gemm", "gemm_pair", "mlp3"])
+@pytest.mark.parametrize("kind", ["decode", "prefill", "prefill_ragged", "prefill_rows96",
+                                  "gemm", "gemm_pair", "mlp3"])
 def test_kernel_specialisations_bit_identical(kind):
-    """The specialisation mk_run picks for a plan and the general kernel (kernel_set = 1) run
-    the same instruction bodies, so their outputs agree bit for bit; the specialisation is the
-    one the plan statistics name."""
+    """The specialisation mk_run picks for a plan and the general kernel (kernel_set = 1) give
+    bit-identical outputs; the specialisation is the one the plan statistics name. The prefill
+    specialisation's register-resident RMSNorm rows and tabled RoPE angles take the same
+    arithmetic in the same order as the general kernel's two-pass loops."""
     sh = workloads.DecoderShape(layers=2, hidden=512, n_q_heads=8, n_kv_heads=2, head_dim=64,
                                 ffn=1024)
     pair = dict(gemm_tile_m=256, cluster=2)
     make, opts, want = {
         "decode": (lambda: workloads.decode(sh, kv_len=130, device=DEV, seed=9), {}, 2),
         "prefill": (lambda: workloads.prefill(sh, tokens=320, device=DEV, seed=3), {}, 3),
+        # a ragged last row block; row blocks too tall for the shared RoPE angle table
+        "prefill_ragged": (lambda: workloads.prefill(sh, tokens=200, device=DEV, seed=6), {}, 3),
+        "prefill_rows96": (lambda: workloads.prefill(sh, tokens=320, device=DEV, seed=8),
+                           dict(norm_rows=96), 3),
         "gemm": (lambda: workloads.gemm(640, 768, 1088, device=DEV, seed=4), {}, 1),
         "gemm_pair": (lambda: workloads.gemm(640, 768, 1088, device=DEV, seed=4), pair, 1),
         "mlp3": (lambda: workloads.mlp3(device=DEV), dict(gemm_tile_n=64), 1),
