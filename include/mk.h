@@ -289,10 +289,11 @@ mk_status mk_get_counter_targets(mk_plan_t p, int32_t* host_buf, size_t n);
 mk_status mk_get_counters(mk_plan_t p, int32_t* host_buf, size_t n);
 
 /* Per-instruction timestamps of the last run (plans compiled with trace = 1), %globaltimer ns:
- * for instruction i, buf[6i..6i+5] = {the compute warpgroup took the descriptor, the scheduler
+ * for instruction i, buf[8i..8i+7] = {the compute warpgroup took the descriptor, the scheduler
  * saw every source counter complete, the compute warpgroup saw that, the instruction's body
- * ended, the instruction was published, the SM index}. A slot an op does not reach stays 0.
- * n >= 6 * n_instr; synchronises. */
+ * ended, the instruction was published, the SM index, the accumulation ended (GEMM: the
+ * accumulator is complete in tensor memory; GEMV: the last weight stage is consumed), 0}.
+ * A slot an op does not reach stays 0. n >= 8 * n_instr; synchronises. */
 mk_status mk_get_trace(mk_plan_t p, uint64_t* host_buf, size_t n);
 
 const char* mk_last_error(void);

@@ -198,11 +198,11 @@ class Plan:
 
     def trace(self):
         """Per-instruction [t_descriptor, t_sources_ready (scheduler), t_sources_seen (compute),
-        t_body_end, t_published, sm] (ns) of the last run."""
+        t_body_end, t_published, sm, t_accumulated (GEMM / GEMV), 0] (ns) of the last run."""
         n = self.stats()["n_instr"]
-        buf = np.zeros(max(1, 6 * n), dtype=np.uint64)
-        check(self._lib.mk_get_trace(self._h, buf.ctypes.data_as(C.POINTER(C.c_uint64)), 6 * n))
-        return buf[:6 * n].reshape(-1, 6)
+        buf = np.zeros(max(1, 8 * n), dtype=np.uint64)
+        check(self._lib.mk_get_trace(self._h, buf.ctypes.data_as(C.POINTER(C.c_uint64)), 8 * n))
+        return buf[:8 * n].reshape(-1, 8)
 
     def counters(self):
         s = self.stats()

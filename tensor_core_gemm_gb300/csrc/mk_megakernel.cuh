@@ -968,12 +968,135 @@ __device__ void run_mma(const Params& p, Smem& s, uint32_t tmem) {
 
 // ------------------------------------------------------------------ compute warpgroup bodies
 
+// The column chunks of one warp's 32 rows of a GEMM tile, after the accumulator is complete:
+// per 32-column chunk, TMEM -> registers (lane = row) -> bias, ReLU, residual or SiLU·mul ->
+// 16-bit values in a 32 x 32 block of shared memory (64-byte rows, 64-byte swizzle: 16-byte
+// chunk j of row r at j ^ ((r >> 1) & 3), conflict-free) -> one TMA store by lane 0. Two 2 KB
+// buffers at xr alternate; a buffer is rewritten once the store issued from it has read it.
+// The next chunk's bias / residual loads are in flight while the current chunk is processed.
+// Out of line with scalar arguments, like the mainloops: compiled inside the kernel function
+// the same loop took about a microsecond per chunk. nk == 0 (K = 0) stores the epilogue of 0.
+template <bool DUAL, bool SIDE, bool AHEAD = true>
+__device__ __noinline__ void epi_chunks(uint32_t tb, int tn, int nk, uint32_t flags, int dt,
+                                        const uint16_t* bias, int ldb, const uint16_t* res,
+                                        int ldr, const void* omap, uint32_t xr, int row0, int n0,
+                                        int M, int N) {
+  const int lane = threadIdx.x & 31;
+  const int row = row0 + lane;
+  const bool has_bias = SIDE && (flags & EPI_BIAS) != 0, relu = (flags & EPI_RELU) != 0,
+             has_res = SIDE && (flags & EPI_RESIDUAL) != 0;
+  // bias / residual vectors of a chunk (4 groups of 8 columns), loaded one chunk ahead (AHEAD)
+  // or at the start of the chunk, before its TMEM loads
+  uint4 sb[SIDE ? 4 : 1], sr[SIDE ? 4 : 1], nb[SIDE && AHEAD ? 4 : 1], nr[SIDE && AHEAD ? 4 : 1];
+  auto load_side = [&](int c, uint4* b, uint4* rr) {
+#pragma unroll
+    for (int g = 0; g < (SIDE ? 4 : 0); ++g) {
+      const int col = n0 + c + g * 8;
+      const bool inside = row < M && col < N;
+      b[g] = rr[g] = make_uint4(0u, 0u, 0u, 0u);
+      if (has_bias && inside)
+        b[g] = __ldcg(reinterpret_cast<const uint4*>(bias + (size_t)row * ldb + col));
+      if (has_res && inside)
+        rr[g] = __ldcg(reinterpret_cast<const uint4*>(res + (size_t)row * ldr + col));
+    }
+  };
+  if (SIDE && AHEAD) load_side(0, sb, sr);
+  for (int c = 0; c < tn; c += 32) {
+    if (SIDE && AHEAD && c + 32 < tn) load_side(c + 32, nb, nr);
+    if (SIDE && !AHEAD) load_side(c, sb, sr);
+    uint32_t r[32], r2[DUAL ? 32 : 1];
+    if (nk > 0) {
+      tmem_ld32(tb + (uint32_t)c, r);
+      if (DUAL) tmem_ld32(tb + (uint32_t)(tn + c), r2);
+      tmem_ld_wait();
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) r[i] = 0u;
+#pragma unroll
+      for (int i = 0; i < (DUAL ? 32 : 1); ++i) r2[i] = 0u;
+    }
+    if (DUAL) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        r[i] = __float_as_uint(silu(__uint_as_float(r[i])) * __uint_as_float(r2[i]));
+    }
+    const uint32_t buf = xr + (uint32_t)((c >> 5) & 1) * 2048u;
+    if (c >= 64) {
+      if (lane == 0) bulk_wait_read_1();
+      __syncwarp();
+    }
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const bool inside = row < M && n0 + c + g * 8 < N;
+      float w[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) w[e] = __uint_as_float(r[g * 8 + e]);
+      if (has_bias && inside) {
+        float b[8];
+        unpack8(sb[g], dt, b);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) w[e] += b[e];
+      }
+      if (relu) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) w[e] = fmaxf(w[e], 0.0f);
+      }
+      if (has_res && inside) {
+        float b[8];
+        unpack8(sr[g], dt, b);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) w[e] += b[e];
+      }
+      const uint4 pk = pack8(w, dt);
+      const uint32_t dst = buf + (uint32_t)lane * 64u + (uint32_t)((g ^ ((lane >> 1) & 3)) << 4);
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(pk.x), "r"(pk.y),
+                   "r"(pk.z), "r"(pk.w)
+                   : "memory");
+    }
+    fence_proxy_async_shared();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(omap, buf, n0 + c, row0);
+      bulk_commit();
+    }
+    if (SIDE && AHEAD) {
+#pragma unroll
+      for (int g = 0; g < (SIDE && AHEAD ? 4 : 0); ++g) {
+        sb[g] = nb[g];
+        sr[g] = nr[g];
+      }
+    }
+  }
+}
+
+// One call site for the four epilogue loops (SiLU·mul or not, bias / residual or not); the
+// node's fields are read here, so few values are live across the call.
+__device__ __noinline__ void epi_tile(const Node& nd, int n0, uint32_t tb, int nk,
+                                      const void* omap, uint32_t xr, int row0) {
+  const uint32_t flags = nd.flags;
+  const int tn = nd.tile_n, dt = nd.dtype, M = nd.M, N = nd.N;
+  const uint16_t* bias = reinterpret_cast<const uint16_t*>(nd.bias.ptr);
+  const uint16_t* res = reinterpret_cast<const uint16_t*>(nd.res.ptr);
+  const int ldb = nd.bias.ld, ldr = nd.res.ld;
+  const bool dual = (flags & EPI_SILU_MUL) != 0;
+  const bool side = (flags & (EPI_BIAS | EPI_RESIDUAL)) != 0;
+  if (dual && side)
+    epi_chunks<true, true>(tb, tn, nk, flags, dt, bias, ldb, res, ldr, omap, xr, row0, n0, M, N);
+  else if (dual)
+    epi_chunks<true, false>(tb, tn, nk, flags, dt, bias, ldb, res, ldr, omap, xr, row0, n0, M, N);
+  else if (side)
+    epi_chunks<false, true>(tb, tn, nk, flags, dt, bias, ldb, res, ldr, omap, xr, row0, n0, M, N);
+  else
+    epi_chunks<false, false>(tb, tn, nk, flags, dt, bias, ldb, res, ldr, omap, xr, row0, n0, M,
+                             N);
+}
+
 // GEMM epilogue: TMEM -> registers (one row per thread), fused epilogue, then per 32-column chunk
 // a 32 x 32 block per warp staged in shared memory and stored with TMA. In pair mode each CTA
 // drains its own 128 rows of the 256-row tile. A split-tail tile (aux1 = number of K splits)
 // first writes its fp32 partial to scratch and releases TMEM; the last split to finish (tile
 // semaphore) sums the partials in split order and runs the epilogue; the others do not publish.
-template <bool PAIR>
+template <bool PAIR, int KS>
 __device__ bool gemm_epilogue(const Params& p, Smem& s, const Instr& in, const Node& nd, int slot,
                               uint32_t use, uint32_t tmem, uint32_t& acc_n, bool* publish,
                               int idx) {
@@ -987,6 +1110,7 @@ __device__ bool gemm_epilogue(const Params& p, Smem& s, const Instr& in, const N
     if (!cw_wait(p, smem_u32(&s.acc_full[as]), (acc_n >> 1) & 1u, 31, idx)) return false;
     tc_fence_after();
   }
+  trace_mark(p, idx, 6);
   const int dt = nd.dtype;
   const bool dual = (nd.flags & EPI_SILU_MUL) != 0;
   const bool bias = (nd.flags & EPI_BIAS) != 0, relu = (nd.flags & EPI_RELU) != 0,
@@ -1144,23 +1268,18 @@ __device__ bool gemm_epilogue(const Params& p, Smem& s, const Instr& in, const N
     }
     release_tmem();
   } else {
-    for (int c = 0; c < tn; c += 32) {
-      uint32_t r[32], r2[32];
-      if (nk > 0) {
-        tmem_ld32(tb + (uint32_t)c, r);
-        if (dual) tmem_ld32(tb + (uint32_t)(tn + c), r2);
-        tmem_ld_wait();
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) r[i] = r2[i] = 0u;
-      }
-      float v[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        v[i] = __uint_as_float(r[i]);
-        if (dual) v[i] = silu(v[i]) * __uint_as_float(r2[i]);
-      }
-      store32(c, v);
+    if constexpr (KS == KS_GEMM) {
+      epi_tile(nd, in.n0, tb, nk, omap, xr0, row0);
+    } else {
+      const uint16_t* bp = reinterpret_cast<const uint16_t*>(nd.bias.ptr);
+      const uint16_t* rp = reinterpret_cast<const uint16_t*>(nd.res.ptr);
+      // fewer registers in the callee: fewer values saved around the call in these kernels
+      if (dual)
+        epi_chunks<true, true, false>(tb, tn, nk, nd.flags, dt, bp, nd.bias.ld, rp, nd.res.ld,
+                                      omap, xr0, row0, in.n0, nd.M, nd.N);
+      else
+        epi_chunks<false, true, false>(tb, tn, nk, nd.flags, dt, bp, nd.bias.ld, rp, nd.res.ld,
+                                       omap, xr0, row0, in.n0, nd.M, nd.N);
     }
     release_tmem();
   }
@@ -1359,6 +1478,7 @@ __device__ bool gemv(const Params& p, Smem& s, const Instr& in, const Node& nd, 
                                       ring % NS, (ring / NS) & 1u, nk, lc >> 3, s.xr, kpad, sums,
                                       idx);
     if (!ok) return false;
+    trace_mark(p, idx, 6);
 #pragma unroll
     for (int m = 0; m < 8; ++m)
       if (m < M) {
@@ -1952,7 +2072,7 @@ __device__ void run_compute(const Params& p, Smem& s, uint32_t tmem) {
         if constexpr (ks_has_gemm(KS)) {
           if (PAIR && !synced) ring = ring_align(ring, NS);  // mirrors the loader's ring sync
           if (ring_stages(in) > 0) synced = true;
-          ok = gemm_epilogue<PAIR>(p, s, in, nd, slot, use, tmem, acc_n, &publish, idx);
+          ok = gemm_epilogue<PAIR, KS>(p, s, in, nd, slot, use, tmem, acc_n, &publish, idx);
           ring += (uint32_t)ring_stages(in);
         }
         break;

@@ -774,7 +774,7 @@ extern "C" mk_status mk_get_trace(mk_plan_t p, uint64_t* buf, size_t n) {
   }
   const size_t need = p->hp.instrs.size() * kTraceWords;
   if ((!buf && need) || n < need) {
-    set_error("mk_get_trace: buffer smaller than 6 * n_instr");
+    set_error("mk_get_trace: buffer smaller than 8 * n_instr");
     return MK_ERR_INVALID_ARG;
   }
   CUDA_TRY(cudaDeviceSynchronize());

@@ -125,7 +125,7 @@ struct Params {
 // Device status record (mirrors mk_device_status).
 enum : int32_t { ST_CODE = 0, ST_INSTR, ST_COUNTER, ST_OBSERVED, ST_EXPECTED, ST_SM, ST_ROLE, ST_WHERE };
 constexpr int kStatusWords = 8;
-constexpr int kTraceWords = 6;
+constexpr int kTraceWords = 8;
 
 // Kernel geometry shared with the host (launch configuration and shared-memory budget).
 constexpr int kThreads = 256;          // 8 warps: scheduler, loader, MMA, spare, 4 compute

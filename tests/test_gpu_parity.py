@@ -401,6 +401,9 @@ def test_trace_timestamps_are_ordered():
     assert np.all(tr[real, 2] >= tr[real, 1]) and np.all(tr[real, 3] >= tr[real, 2])
     assert np.all(tr[real, 4] >= tr[real, 3]) and np.all(tr[real, 3] >= tr[real, 0])
     assert np.all(tr[real, 5] == np.arange(len(ins))[real] % p.stats()["n_sm"])
+    # GEMM tiles: the accumulator is complete after the sources are seen, before the body ends
+    assert np.all(tr[real, 6] >= tr[real, 2]) and np.all(tr[real, 3] >= tr[real, 6])
+    assert np.all(tr[:, 7] == 0)
 
 
 # ------------------------------------------------------------------ CTA pairs (cta_group::2)
