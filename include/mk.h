@@ -185,6 +185,13 @@ typedef struct {
                             attention and row instructions); 1: the general kernel. Both give
                             bit-identical results; a specialisation compiles without the code
                             of the kinds it never runs */
+  int32_t gemv_pack;     /* 1 (default): the weights of GEMV tiles that no node of the graph
+                            writes are copied at mk_compile into a plan-owned packed layout
+                            (each 64-row stage of a tile contiguous, in its shared-memory
+                            layout) and streamed from there with one bulk copy per stage; the
+                            copy follows mk_run_host copies into the weight, and mk_plan_repack
+                            refreshes it after any other change to such a weight. 0: stream
+                            them from the tensors through tensor maps */
 } mk_compile_opts;
 
 /* Fill *o with the defaults (the values listed above for each field). */
@@ -223,6 +230,11 @@ typedef struct {
   int32_t role;       /* 0 scheduler, 1 loader, 2 MMA, 3 compute */
   int32_t where;      /* wait site id (kernel-internal) */
 } mk_device_status;
+
+/* Re-read every weight the plan holds a packed copy of (gemv_pack = 1) into that copy, on
+ * `stream` (ordered before later work on it). Needed after a change to such a weight made
+ * outside mk_run_host; without it mk_run keeps using the weight as it was when packed. */
+mk_status mk_plan_repack(mk_plan_t p, void* stream);
 
 /* Synchronise the device and read the status of the plan's last completed run. Returns
  * st->code as the status. */
@@ -268,6 +280,7 @@ typedef struct {
   int64_t scratch_bytes; /* plan-owned device scratch */
   int64_t kernel_set;    /* specialisation mk_run launches: 0 general, 1 GEMM tiles only,
                             2 decode, 3 prefill */
+  int64_t packed_bytes;  /* device bytes of packed GEMV weight copies (gemv_pack) */
 } mk_stats;
 
 mk_status mk_plan_stats(mk_plan_t p, mk_stats* s);

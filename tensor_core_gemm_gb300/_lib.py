@@ -16,7 +16,7 @@ EXPORTS = [
     "mk_add_elementwise", "mk_add_attention", "mk_default_opts", "mk_compile", "mk_run",
     "mk_run_host", "mk_sync_status", "mk_plan_destroy", "mk_plan_stats", "mk_get_instructions",
     "mk_get_src_list", "mk_get_dst_list", "mk_get_counter_targets", "mk_get_counters",
-    "mk_last_error", "mk_abi_version", "mk_gemv_noalloc", "mk_get_trace",
+    "mk_last_error", "mk_abi_version", "mk_gemv_noalloc", "mk_get_trace", "mk_plan_repack",
 ]
 
 
@@ -42,7 +42,7 @@ class CompileOpts(C.Structure):
         "norm_rows", "gemv_max_m", "gemv_tile_n", "gemv_splits", "gemv_kstep", "attn_chunk",
         "attn_tile_q", "dry_run", "timeout_ms", "device", "debug_counter", "debug_extra",
         "snapshot_counters", "trace", "l2_prefetch", "gemm_split_tail", "fuse_rope",
-        "fuse_attn_reduce", "kernel_set")]
+        "fuse_attn_reduce", "kernel_set", "gemv_pack")]
 
 
 class HostCopy(C.Structure):
@@ -59,7 +59,7 @@ class Stats(C.Structure):
                 ("n_sm", C.c_int64), ("n_iter", C.c_int64), ("waves", C.c_double),
                 ("n_src", C.c_int64), ("n_dst", C.c_int64), ("per_op", C.c_int64 * 16),
                 ("smem_bytes", C.c_int64), ("scratch_bytes", C.c_int64),
-                ("kernel_set", C.c_int64)]
+                ("kernel_set", C.c_int64), ("packed_bytes", C.c_int64)]
 
 
 _lib = None
@@ -89,6 +89,7 @@ def load():
         "mk_run": [P, VP],
         "mk_run_host": [P, C.POINTER(HostCopy), I32, VP],
         "mk_sync_status": [P, C.POINTER(DeviceStatus)],
+        "mk_plan_repack": [P, VP],
         "mk_plan_destroy": [P],
         "mk_plan_stats": [P, C.POINTER(Stats)],
         "mk_get_instructions": [P, VP, C.c_size_t],

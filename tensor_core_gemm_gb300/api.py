@@ -149,6 +149,11 @@ class Plan:
         """Enqueue one run (counter reset + one persistent launch) on `stream`."""
         check(self._lib.mk_run(self._h, _stream_handle(stream)))
 
+    def repack(self, stream=None):
+        """Refresh the plan's packed copies of GEMV weights after changing such a weight in
+        device memory (runs mk_plan_repack on `stream`)."""
+        check(self._lib.mk_plan_repack(self._h, _stream_handle(stream)))
+
     def run_host(self, inputs=(), outputs=(), stream=None):
         """inputs/outputs: lists of (tensor_id, host pointer); host->device copies, the run and
         device->host copies are all enqueued on `stream`."""

@@ -761,5 +761,6 @@ extern "C" mk_status mk_default_opts(mk_compile_opts* o) {
   o->fuse_rope = 1;
   o->fuse_attn_reduce = 1;
   o->kernel_set = 0;
+  o->gemv_pack = 1;
   return MK_OK;
 }

@@ -51,6 +51,7 @@ struct __align__(1024) Smem {
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint64_t go;                          // pair mode, odd CTA: released by the even CTA once per GEMM
+  uint64_t gx_full;                     // tensor-core GEMV: the activation operand is staged
   // prefill attention: scores S and output blocks O double-buffered in TMEM, P in xr
   uint64_t att_s_full[2], att_s_free[2], att_p_full, att_o_full[2], att_o_free[2];
   uint64_t instr_ready[kSlots];
@@ -559,6 +560,16 @@ __device__ bool load_gemv(const Params& p, Smem& s, const Instr& in, const Node&
   const void* tb = tmap_at(p, nd.b.tmap);
   const void* tb2 = dual ? tmap_at(p, nd.b2.tmap) : nullptr;
   const uint32_t ring0 = smem_u32(s.ring), sb = stage_bytes(p);
+  // packed weights: each stage is one contiguous unit per weight, already in the swizzled layout
+  const bool packed = (nd.flags & NF_B_PACKED) != 0;
+  const uint32_t unit = dual ? 16384u : 32768u;
+  const uint8_t* pb = nullptr;
+  const uint8_t* pb2 = nullptr;
+  if (packed) {
+    const size_t first = (size_t)(in.n0 / (dual ? 128 : 256)) * (size_t)nd.b.ld + in.k0 / 64;
+    pb = reinterpret_cast<const uint8_t*>(nd.b.ptr) + first * unit;
+    if (dual) pb2 = reinterpret_cast<const uint8_t*>(nd.b2.ptr) + first * unit;
+  }
   if (in.flags & IFLAG_B_DEP) {
     if (!wait_warp(p, smem_u32(&s.deps_ready[slot]), use & 1u, R_LOAD, 14, idx)) return false;
     if (elect_one()) fence_proxy_async_global();
@@ -572,7 +583,10 @@ __device__ bool load_gemv(const Params& p, Smem& s, const Instr& in, const Node&
       const uint32_t dst = ring0 + rp.st * sb;
       const int k = in.k0 + kb * kGemvRows;
       mbar_expect_tx(bar, bytes);
-      if (dual) {
+      if (packed) {
+        bulk_load(dst, pb + (size_t)kb * unit, unit, bar);
+        if (dual) bulk_load(dst + unit, pb2 + (size_t)kb * unit, unit, bar);
+      } else if (dual) {
         load_panels<false>(dst, tb, panel, bar, in.n0, k, 2);
         load_panels<false>(dst + 2 * 8192, tb2, panel, bar, in.n0, k, 2);
       } else {
@@ -666,7 +680,15 @@ __device__ void prefetch_ahead(const Params& p, const Smem& s, int cur, int& nex
     if (!(f.flags & IFLAG_B_DEP)) {
       if (elect_one()) {
         const bool panel = (nd.flags & NF_B_PANELS) != 0;
-        if (f.op == OP_GEMV) {
+        if (f.op == OP_GEMV && (nd.flags & NF_B_PACKED)) {
+          const bool dual = (nd.flags & EPI_SILU_MUL) != 0;
+          const uint32_t unit = dual ? 16384u : 32768u;
+          const size_t first = (size_t)(f.n0 / (dual ? 128 : 256)) * (size_t)nd.b.ld + f.k0 / 64;
+          const uint32_t bytes = (uint32_t)ring_stages(f) * unit;
+          bulk_prefetch_l2(reinterpret_cast<const uint8_t*>(nd.b.ptr) + first * unit, bytes);
+          if (dual)
+            bulk_prefetch_l2(reinterpret_cast<const uint8_t*>(nd.b2.ptr) + first * unit, bytes);
+        } else if (f.op == OP_GEMV) {
           const bool dual = (nd.flags & EPI_SILU_MUL) != 0;
           const int nk = ring_stages(f);
           const void* mb = tmap_at(p, nd.b.tmap);
@@ -793,6 +815,53 @@ __device__ __noinline__ int mma_tile(const Params& p, uint32_t full0, uint32_t e
   return nk;
 }
 
+// GEMV tiles run on the tensor cores with the operands swapped: D [256 weight columns x 16] =
+// W^T x^T as two M = 128 halves, N = 16 >= M activation rows, K = 16 per MMA. The weight stage
+// is the A operand exactly as TMA wrote it (MN-major); the compute warpgroup stages the K chunk's
+// activations as the K-major B operand in the staging buffer, one 1 KB block (8 rows x 64 K) per
+// weight stage. The chunk must fit that buffer with one spare block (rows 8-15 of the last block's
+// MMAs read past it), and CTA-pair kernels keep the CUDA-core path (a kernel uses one cta_group).
+constexpr int kGemvTensorBlocks = kXrFloats * 4 / 1024 - 1;
+template <bool PAIR>
+__device__ __forceinline__ bool gemv_on_tensor(const Instr& in, const Node& nd) {
+  const int nk = ring_stages(in);
+  return !PAIR && nk > 0 && nk <= kGemvTensorBlocks && nd.M <= 8;
+}
+
+// The MMAs of one tensor-core GEMV tile: per weight stage, 4 K slices x 2 column halves. A: the
+// stage (64-column atoms 8 KB apart, 8-row K groups 1 KB apart; a 16-row K slice is 128 units,
+// the second half of the columns 1024 units on). B: block kb of the staged activations (2 units
+// per K slice). Rows 8-15 of B are the next block's rows 0-7: they only fill accumulator columns
+// 8-15, which nobody reads (M <= 8). A stage is released when its MMAs complete. Returns the
+// number of stages whose MMAs were issued (nk unless a wait gave up).
+__device__ __noinline__ int mma_gemv(const Params& p, uint32_t full0, uint32_t empty0,
+                                     uint32_t st, uint32_t ph, uint32_t ns, int nk,
+                                     uint64_t adesc0, uint64_t bdesc0, uint32_t units, uint32_t d,
+                                     uint32_t idesc, int idx) {
+  for (int kb = 0; kb < nk; ++kb) {
+    if (!wait_warp(p, full0 + st * 8u, ph, R_MMA, 23, idx)) return kb;
+    tc_fence_after();
+    if (elect_one()) {
+      const uint64_t so = (uint64_t)(st * units);
+#pragma unroll
+      for (int j = 0; j < kGemvRows / 16; ++j) {
+        const uint64_t ad = adesc0 + so + (uint64_t)(j * 128);
+        const uint64_t bd = bdesc0 + (uint64_t)(kb * 64 + j * 2);
+        const uint32_t acc = (kb | j) != 0;
+        tc_mma_f16(d, ad, bd, idesc, acc);
+        tc_mma_f16(d + 16u, ad + 1024u, bd, idesc, acc);
+      }
+      tc_commit(empty0 + st * 8u);
+    }
+    __syncwarp();
+    if (++st == ns) {
+      st = 0;
+      ph ^= 1u;
+    }
+  }
+  return nk;
+}
+
 // Prefill attention MMAs of one instruction: nb key blocks from ring position (st, ph). Block j:
 // S_j = Q K_j^T into TMEM S[n&1] (M = 128 query rows, N = 64 keys, K = 64 dims; the keys are a
 // K-major B operand), then, once the compute warps have written P_j (bf16, 128-byte swizzled,
@@ -874,7 +943,7 @@ __device__ void run_mma(const Params& p, Smem& s, uint32_t tmem) {
   // K slice is 16 rows of 128 B (128 units).
   const uint64_t bdesc0 = sdesc_sw128(ring0 + kGemmTileM * kGemmBK * 2, 8192, 1024);
   RingPos rp;
-  uint32_t acc_n = 0, att_n = 0;
+  uint32_t acc_n = 0, att_n = 0, gx_n = 0;
   bool issued = false, synced = true;
   const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
   for (int it = 0;; ++it) {
@@ -946,6 +1015,27 @@ __device__ void run_mma(const Params& p, Smem& s, uint32_t tmem) {
         issued = true;
         rp.advance((uint32_t)nb, NS);
       }
+    } else if (ks_has_gemv(KS) && in.op == OP_GEMV && gemv_on_tensor<PAIR>(in, nd)) {
+      synced = false;
+      const int nk = ring_stages(in);
+      const uint32_t as = acc_n & 1u;
+      // the accumulator slot is free, and the activations are staged
+      if (!wait_warp(p, smem_u32(&s.acc_empty[as]), ((acc_n >> 1) & 1u) ^ 1u, R_MMA, 21, idx))
+        break;
+      if (!wait_warp(p, smem_u32(&s.gx_full), gx_n & 1u, R_MMA, 24, idx)) break;
+      ++gx_n;
+      tc_fence_after();
+      const uint32_t ring0 = smem_u32(s.ring);
+      const int done = mma_gemv(p, smem_u32(&s.full[0]), smem_u32(&s.empty[0]), rp.st, rp.ph, NS,
+                                nk, sdesc_sw128(ring0, 8192, 1024),
+                                sdesc_sw128(smem_u32(s.xr), 16, 1024), units, tmem + as * 256u,
+                                idesc_f16_amn(nd.dtype == DT_BF16, 16, 128), idx);
+      if (done > 0) issued = true;
+      rp.advance((uint32_t)nk, NS);
+      if (done != nk) break;
+      if (elect_one()) tc_commit(smem_u32(&s.acc_full[as]));
+      __syncwarp();
+      ++acc_n;
     } else {
       synced = false;
       rp.advance((uint32_t)ring_stages(in), NS);  // stages consumed by the compute warpgroup
@@ -1401,8 +1491,10 @@ __device__ bool gemv_staged_rows(int M, const Params& p, uint32_t full0, uint32_
 // stage needs no cross-thread reduction. Weight stages arrive as 128-byte swizzled boxes:
 // unswizzled TMA writes of rows 128 bytes apart land on the same shared-memory banks ("Hand-
 // writing a Blackwell GEMM", step 4).
+template <bool PAIR>
 __device__ bool gemv(const Params& p, Smem& s, const Instr& in, const Node& nd, int slot,
-                     uint32_t use, uint32_t& ring, bool* publish, int idx) {
+                     uint32_t use, uint32_t& ring, bool* publish, int idx, uint32_t tmem,
+                     uint32_t& acc_n) {
   const uint32_t NS = ring_n(p);
   const int ct = (int)threadIdx.x - (kThreads - kCompute);
   const int wp = ct >> 5, lane = ct & 31;
@@ -1457,13 +1549,69 @@ __device__ bool gemv(const Params& p, Smem& s, const Instr& in, const Node& nd, 
     }
     cw_sync();
   };
-  if (staged && nk > 0) stage_x(in.k0, kpad, kpad);
+  const bool tensor = gemv_on_tensor<PAIR>(in, nd);
+  if (tensor) {
+    // the K-major B operand of the tensor-core tile: per 64-K block a 1 KB atom of 8 rows x 128
+    // bytes, 16-byte chunk c of row m at c ^ m; the activations rounded to the weight type
+    uint8_t* xb = reinterpret_cast<uint8_t*>(s.xr);
+    const int nv = kpad / 8;
+    for (int v = ct; v < M * nv; v += kCompute) {
+      const int m = v / nv, kk = (v % nv) * 8, k = in.k0 + kk;
+      float x[8];
+      if (k < kend) {
+        load8(nd.a, m, k, dt, x);
+        if (norm) {
+          float g[8];
+          load8(nd.gamma, 0, k, dt, g);
+          const float r = s.rstd[m];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[e] = x[e] * r * g[e];
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = 0.f;
+      }
+      *reinterpret_cast<uint4*>(xb + (kk >> 6) * 1024 + m * 128 + ((((kk & 63) >> 3) ^ m) << 4)) =
+          pack8(x, dt);
+    }
+    fence_proxy_async_shared();
+    cw_sync();
+    if (ct == 0) mbar_arrive(smem_u32(&s.gx_full));
+  } else if (staged && nk > 0) {
+    stage_x(in.k0, kpad, kpad);
+  }
   const int which = dual ? (ct >> 6) : 0;
   const int col = dual ? 2 * (ct & 63) : 2 * ct;  // column pair inside this thread's weight
   float acc[8][2];
 #pragma unroll
   for (int m = 0; m < 8; ++m) acc[m][0] = acc[m][1] = 0.f;
-  if (staged && nk > 0) {
+  if (tensor) {
+    const uint32_t as = acc_n & 1u;
+    if (!cw_wait(p, smem_u32(&s.acc_full[as]), (acc_n >> 1) & 1u, 42, idx)) return false;
+    tc_fence_after();
+    trace_mark(p, idx, 6);
+    // accumulator lanes are the tile's weight columns (this warp: 32 of each half), its columns
+    // the activation rows; through the staging buffer into the column-pair layout below
+    uint32_t r[32];
+    tmem_ld32(tmem + as * 256u + ((uint32_t)(wp * 32) << 16), r);
+    tmem_ld_wait();
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int m = 0; m < 8; ++m)
+        if (m < M) s.xr[m * 256 + h * 128 + wp * 32 + lane] = __uint_as_float(r[h * 16 + m]);
+    tc_fence_before();
+    cw_sync();
+    if (ct == 0) mbar_arrive(smem_u32(&s.acc_empty[as]));
+    ++acc_n;
+#pragma unroll
+    for (int m = 0; m < 8; ++m)
+      if (m < M) {
+        acc[m][0] = s.xr[m * 256 + which * 128 + col];
+        acc[m][1] = s.xr[m * 256 + which * 128 + col + 1];
+      }
+    ring += (uint32_t)nk;  // the MMA issuer consumed and released the stages
+  } else if (staged && nk > 0) {
     // this thread's column pair: box (which * 2 + col / 64), column col % 64 inside it
     const int box = (dual ? which * 2 : 0) + (col >> 6), lc = col & 63;
     float sums[16];
@@ -1487,7 +1635,7 @@ __device__ bool gemv(const Params& p, Smem& s, const Instr& in, const Node& nd, 
       }
     ring += (uint32_t)nk;
   }
-  for (int kb = 0; kb < nk && !staged; ++kb) {
+  for (int kb = 0; kb < nk && !staged && !tensor; ++kb) {
     const float* xs;
     int xstride;
     if (staged) {
@@ -2077,7 +2225,8 @@ __device__ void run_compute(const Params& p, Smem& s, uint32_t tmem) {
         }
         break;
       case OP_GEMV:
-        if constexpr (ks_has_gemv(KS)) ok = gemv(p, s, in, nd, slot, use, ring, &publish, idx);
+        if constexpr (ks_has_gemv(KS))
+          ok = gemv<PAIR>(p, s, in, nd, slot, use, ring, &publish, idx, tmem, acc_n);
         break;
       case OP_NOOP:
         break;
@@ -2167,6 +2316,7 @@ __global__ void __launch_bounds__(kThreads, 1) megakernel(const __grid_constant_
     }
     mbar_init(smem_u32(&s.drain), 1);
     mbar_init(smem_u32(&s.go), 1);
+    mbar_init(smem_u32(&s.gx_full), 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&s.att_s_full[i]), 1);   // tcgen05.commit
       mbar_init(smem_u32(&s.att_s_free[i]), 4);   // one lane per compute warp

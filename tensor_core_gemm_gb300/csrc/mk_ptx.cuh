@@ -66,6 +66,19 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
 }
 
 // ---------------------------------------------------------------- TMA
+// Contiguous global -> shared copy of `bytes` (16-byte aligned ends), completing on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "l"((uint64_t)src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"((uint64_t)src), "r"(bytes)
+               : "memory");
+}
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint32_t bar, int x,
                                             int y) {
   asm volatile(
@@ -285,6 +298,10 @@ __device__ __forceinline__ uint32_t idesc_f16(int bf16, int n, int m = 128) {
 // The same with B K-major (B^T stored row-major, e.g. the keys of S = Q K^T).
 __device__ __forceinline__ uint32_t idesc_f16_bk(int bf16, int n, int m = 128) {
   return idesc_f16(bf16, n, m) & ~(1u << 16);
+}
+// A MN-major and B K-major (A = a row-major K x M weight read along M, B = activations).
+__device__ __forceinline__ uint32_t idesc_f16_amn(int bf16, int n, int m = 128) {
+  return (idesc_f16(bf16, n, m) & ~(1u << 16)) | (1u << 15);
 }
 
 // True in exactly one lane of the (converged, full) warp.

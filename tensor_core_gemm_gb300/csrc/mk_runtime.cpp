@@ -30,8 +30,34 @@ struct mk_plan {
   size_t smem = 0;
   int grid = 0;
   int kernel_set = KS_ALL;  // specialisation launched by mk_run
+  // Packed copies of GEMV weights (see mk_pack.cu): one job per (node, weight), refreshed by
+  // mk_plan_repack and by mk_run_host copies into the weight's tensor.
+  struct PackJob {
+    int node = -1, tensor = -1;  // graph node; weight tensor id (a base tensor or a view)
+    const void* src = nullptr;
+    long long ld = 0;
+    int K = 0, N = 0, tw = 0;
+    size_t off = 0;  // offset of the packed copy in d_mem
+  };
+  std::vector<PackJob> packs;
+  size_t packed_bytes = 0;
   Params params{};
 };
+
+namespace mk {
+size_t packed_gemv_bytes(int K, int N, int tw);
+cudaError_t pack_gemv_weight(const void* w, long long ld, int K, int N, int tw, void* dst,
+                             cudaStream_t stream);
+}  // namespace mk
+
+static cudaError_t run_packs(mk_plan* p, cudaStream_t s, int base_tensor = -1) {
+  for (const auto& j : p->packs) {
+    if (base_tensor >= 0 && p->hp.tensors[j.tensor].base != base_tensor) continue;
+    const cudaError_t e = pack_gemv_weight(j.src, j.ld, j.K, j.N, j.tw, p->d_mem + j.off, s);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
 
 // The smallest kernel specialisation that runs every instruction of the list (KS_ALL when
 // kernel_set = 1 asks for the general kernel); CTA-pair plans outside KS_GEMM run KS_ALL.
@@ -129,6 +155,10 @@ mk_status check_kernel_support(const std::vector<TensorRec>& ts, const std::vect
   }
   if (pair && o.n_sm % 2) {
     set_error("mk_compile: CTA pairs need an even n_sm");
+    return MK_ERR_UNSUPPORTED;
+  }
+  if (o.gemv_pack != 0 && o.gemv_pack != 1) {
+    set_error("mk_compile: gemv_pack is 0 or 1");
     return MK_ERR_UNSUPPORTED;
   }
   if (o.kernel_set != 0 && o.kernel_set != 1) {
@@ -381,6 +411,14 @@ static mk_status build_nodes(const mk_graph* g, mk_plan* p, std::vector<CUtensor
               (st = add_map(keys, maps, ts[nd.b2], 64, rows, true, &n.b2.tmap, panel ? np : 0)))
             return st;
           if (panel) n.flags |= NF_B_PANELS;
+          int w = 0;  // the node's packed weights, b then b2
+          for (const auto& j : p->packs) {
+            if (j.node != (int)i) continue;
+            Operand& op = w++ == 0 ? n.b : n.b2;
+            op.ptr = (uint64_t)(uintptr_t)(p->d_mem + j.off);
+            op.ld = (j.K + 63) / 64;  // 64-row blocks per column tile
+            n.flags |= NF_B_PACKED;
+          }
         }
         break;
       }
@@ -513,6 +551,36 @@ extern "C" mk_status mk_compile(mk_graph_t g, const mk_compile_opts* opts_in, mk
           p->hp.src_list[2 * (in.src_off + s) + 1] += o.debug_extra;
   }
   p->kernel_set = pick_kernel_set(p->hp.instrs, o);
+  if (o.gemv_pack) {
+    // GEMV weights that no instruction of the plan writes get a packed copy
+    std::vector<char> bdep(g->nodes.size(), 0);
+    for (const Instr& in : p->hp.instrs)
+      if (in.op == OP_GEMV && (in.flags & IFLAG_B_DEP)) bdep[in.node] = 1;
+    size_t off = 0;
+    for (size_t i = 0; i < g->nodes.size(); ++i) {
+      const NodeRec& nd = g->nodes[i];
+      if (nd.kind != NK_MATMUL || bdep[i]) continue;
+      const TensorRec &A = p->hp.tensors[nd.a], &B = p->hp.tensors[nd.b];
+      if (A.rows > o.gemv_max_m || A.rows == 0 || A.cols == 0 || B.cols == 0) continue;
+      const int tw = nd.b2 >= 0 ? 128 : 256;  // columns per weight of one GEMV tile
+      for (int w : {nd.b, nd.b2}) {
+        if (w < 0) continue;
+        const TensorRec& W = p->hp.tensors[w];
+        mk_plan::PackJob j;
+        j.node = (int)i;
+        j.tensor = w;
+        j.src = W.ptr;
+        j.ld = W.ld;
+        j.K = (int)A.cols;
+        j.N = (int)W.cols;
+        j.tw = tw;
+        j.off = off;
+        off = (off + packed_gemv_bytes(j.K, j.N, tw) + 1023) & ~(size_t)1023;
+        p->packs.push_back(j);
+      }
+    }
+    p->packed_bytes = off;
+  }
   if (o.dry_run) {
     *out = p;
     return MK_OK;
@@ -558,7 +626,9 @@ extern "C" mk_status mk_compile(mk_graph_t g, const mk_compile_opts* opts_in, mk
   const size_t trace_bytes = o.trace ? p->hp.instrs.size() * kTraceWords * sizeof(uint64_t) : 0;
   const size_t off_maps = align(off_trace + trace_bytes);
   const size_t off_scratch = align(off_maps + kMaxTmaps * sizeof(CUtensorMap));
-  const size_t total = off_scratch + scratch;
+  const size_t off_pack = (off_scratch + scratch + 1023) & ~(size_t)1023;
+  const size_t total = off_pack + p->packed_bytes;
+  for (auto& j : p->packs) j.off += off_pack;
   if (cudaMalloc((void**)&p->d_mem, total) != cudaSuccess) {
     cudaGetLastError();
     set_error("mk_compile: cudaMalloc of %zu plan bytes failed", total);
@@ -581,6 +651,10 @@ extern "C" mk_status mk_compile(mk_graph_t g, const mk_compile_opts* opts_in, mk
   if (e == cudaSuccess) e = up(off_dst, p->hp.dst_list.data(), p->hp.dst_list.size() * 4);
   if (e == cudaSuccess) e = up(off_maps, maps.data(), maps.size() * sizeof(CUtensorMap));
   if (e == cudaSuccess) e = cudaMemset(p->d_mem + off_ctr, 0, off_maps - off_ctr);
+  if (e == cudaSuccess && !p->packs.empty()) {
+    e = run_packs(p, 0);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  }
   if (e == cudaSuccess) {
     p->smem = megakernel_smem_bytes();
     e = configure_megakernel(p->smem);
@@ -670,11 +744,24 @@ extern "C" mk_status mk_run_host(mk_plan_t p, const mk_host_copy* copies, int32_
   }
   cudaStream_t s = (cudaStream_t)stream;
   mk_status st;
-  for (int i = 0; i < n; ++i)
-    if (copies[i].to_device && (st = host_copy(p, copies[i], s))) return st;
+  for (int i = 0; i < n; ++i) {
+    if (!copies[i].to_device) continue;
+    if ((st = host_copy(p, copies[i], s))) return st;
+    if (p->on_device && !p->packs.empty())  // a packed GEMV weight follows its tensor
+      CUDA_TRY(run_packs(p, s, p->hp.tensors[copies[i].tensor].base));
+  }
   if ((st = mk_run(p, stream))) return st;
   for (int i = 0; i < n; ++i)
     if (!copies[i].to_device && (st = host_copy(p, copies[i], s))) return st;
+  return MK_OK;
+}
+
+extern "C" mk_status mk_plan_repack(mk_plan_t p, void* stream) {
+  if (!p || !p->on_device) {
+    set_error("mk_plan_repack: NULL plan or dry-run plan");
+    return MK_ERR_INVALID_ARG;
+  }
+  CUDA_TRY(run_packs(p, (cudaStream_t)stream));
   return MK_OK;
 }
 
@@ -728,6 +815,7 @@ extern "C" mk_status mk_plan_stats(mk_plan_t p, mk_stats* s) {
   s->smem_bytes = (int64_t)p->smem;
   s->scratch_bytes = (int64_t)p->scratch_bytes;
   s->kernel_set = p->kernel_set;
+  s->packed_bytes = (int64_t)p->packed_bytes;
   return MK_OK;
 }
 

@@ -61,6 +61,8 @@ enum : uint32_t {
   NF_B_PANELS = 1u << 16,  // B (and b2) maps are 3D panel maps: one box per stage, all panels
   NF_ROPE = 1u << 17,      // GEMV tiles also write RoPE's outputs (out_q, out_k, out_v)
   NF_ATTN_FUSED = 1u << 18, // split-KV partials: the last one of a key/value head combines
+  NF_B_PACKED = 1u << 19,   // GEMV: b / b2 point at the plan's packed copies (ld = 64-row blocks
+                            // per column tile), one contiguous unit per weight stage
 };
 
 enum : int32_t { EWOP_ADD = 0, EWOP_RELU = 1, EWOP_COPY = 2, EWOP_SILU_MUL = 3 };
@@ -155,7 +157,9 @@ MK_HD constexpr bool ks_has_gemm(int ks) { return ks != KS_DECODE; }
 MK_HD constexpr bool ks_has_gemv(int ks) { return ks == KS_ALL || ks == KS_DECODE; }
 MK_HD constexpr bool ks_has_attn_prefill(int ks) { return ks == KS_ALL || ks == KS_PREFILL; }
 MK_HD constexpr bool ks_has_rows(int ks) { return ks != KS_GEMM; }
-MK_HD constexpr bool ks_has_tmem(int ks) { return ks_has_gemm(ks) || ks_has_attn_prefill(ks); }
+MK_HD constexpr bool ks_has_tmem(int ks) {
+  return ks_has_gemm(ks) || ks_has_attn_prefill(ks) || ks_has_gemv(ks);  // GEMV: tensor cores
+}
 MK_HD constexpr bool ks_covers(int ks, int op) {
   return op == OP_NOOP || op == OP_END                ? true
          : op == OP_GEMM                              ? ks_has_gemm(ks)

@@ -172,6 +172,82 @@ def test_gemv(m, n, k, splits, norm, dual, res):
     assert np.all(ctr[st["n_counters"]:] == p.instructions()["aux1"][0])
 
 
+@pytest.mark.parametrize("m,n,k,dual", [(1, 3072, 2048, False), (5, 392, 1000, False),
+                                        (3, 1000, 520, True), (8, 128, 4096, True)])
+def test_gemv_packed_weights_bit_identical(m, n, k, dual):
+    """GEMV tiles streaming packed weight copies (gemv_pack = 1, one bulk copy per stage) and
+    the weights themselves through tensor maps (gemv_pack = 0) fill shared memory with the same
+    bytes, so the outputs agree bit for bit; ragged N and K are zero outside the weight."""
+    x = synth.normal((m, k), 1.0, "bf16", 31, DEV)
+    w = synth.normal((k, n), 0.02, "bf16", 32, DEV)
+    wu = synth.normal((k, n), 0.02, "bf16", 33, DEV)
+    outs = []
+    from tensor_core_gemm_gb300 import Graph
+    for pack in (1, 0):
+        out = torch.full((m, n), float("nan"), dtype=torch.bfloat16, device=DEV)
+        g = Graph()
+        ix, iw, iwu, io = (g.tensor(t) for t in (x, w, wu, out))
+        g.matmul(ix, iw, io, b_up=iwu if dual else None)
+        p = g.compile(gemv_pack=pack)
+        assert (p.stats()["packed_bytes"] > 0) == bool(pack)
+        p.run()
+        p.check_status()
+        outs.append(out)
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    ref = (ops.matmul_silu_mul(f32(x), f32(w), f32(wu), BF16) if dual
+           else ops.matmul(f32(x), f32(w), BF16))
+    assert_close(f32(outs[0]), ref, "packed gemv")
+
+
+def test_gemv_packed_weights_follow_changes():
+    """A packed weight is refreshed by mk_run_host copies into its tensor and by repack()."""
+    m, n, k = 2, 512, 1024
+    x = synth.normal((m, k), 1.0, "bf16", 41, DEV)
+    w = synth.normal((k, n), 0.02, "bf16", 42, DEV)
+    out = torch.zeros((m, n), dtype=torch.bfloat16, device=DEV)
+    from tensor_core_gemm_gb300 import Graph
+    g = Graph()
+    ix, iw, io = (g.tensor(t) for t in (x, w, out))
+    g.matmul(ix, iw, io)
+    p = g.compile()
+    assert p.stats()["packed_bytes"] > 0
+    w2 = synth.normal((k, n), 0.02, "bf16", 43, DEV)
+    # a device-side change followed by repack()
+    w.copy_(w2)
+    p.repack()
+    p.run()
+    p.check_status()
+    assert_close(f32(out), ops.matmul(f32(x), f32(w2), BF16), "after repack")
+    # a host copy into the weight through run_host
+    w3 = synth.normal((k, n), 0.02, "bf16", 44, DEV)
+    w3_h = w3.cpu().pin_memory()
+    s = torch.cuda.Stream()
+    p.run_host(inputs=[(iw, w3_h.data_ptr())], stream=s)
+    s.synchronize()
+    p.check_status()
+    assert_close(f32(out), ops.matmul(f32(x), f32(w3), BF16), "after run_host weight copy")
+
+
+def test_gemv_weight_written_in_graph_is_not_packed():
+    """A GEMV whose weight another node writes reads it through its tensor map after the
+    producer's tiles (no packed copy)."""
+    m, n, k = 1, 256, 256
+    x = synth.normal((m, k), 1.0, "bf16", 51, DEV)
+    w0 = synth.normal((k, n), 0.02, "bf16", 52, DEV)
+    w = torch.zeros((k, n), dtype=torch.bfloat16, device=DEV)
+    out = torch.zeros((m, n), dtype=torch.bfloat16, device=DEV)
+    from tensor_core_gemm_gb300 import Graph
+    g = Graph()
+    ix, iw0, iw, io = (g.tensor(t) for t in (x, w0, w, out))
+    g.elementwise("relu", [iw0], iw)
+    g.matmul(ix, iw, io)
+    p = g.compile()
+    assert p.stats()["packed_bytes"] == 0
+    p.run()
+    p.check_status()
+    assert_close(f32(out), ops.matmul(f32(x), np.maximum(f32(w0), 0), BF16), "in-graph weight")
+
+
 # ------------------------------------------------------------------ row / elementwise ops
 
 def test_unfused_mlp_elementwise_tiles():
