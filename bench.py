@@ -4,7 +4,8 @@
 
 Default workload: the single fp16 GEMM C = A @ B, M = N = K = 4096 (A, B ~N(0, 1/64)), one
 megakernel launch per step. Other workloads (--config): mlp3, llama_prefill, llama_decode,
-decode, prefill.
+decode, prefill, and decode_sample (decode followed by greedy sampling over a 128256-token
+vocabulary).
 
 Timing: W untimed warm-up runs, then K runs, each bracketed by CUDA events on the launch stream
 with a 256 MB L2 flush (a device write larger than the 129 MB L2) before each run, outside the
@@ -54,6 +55,8 @@ CONFIGS = {
     "decode": "batch-1 decode, 16-layer decoder hidden 2048, 32/8 heads x 64, MLP 8192, "
               "KV 1024, bf16",
     "prefill": "causal prefill 2048 tokens, 16-layer decoder hidden 2048, bf16",
+    "decode_sample": "batch-1 decode as 'decode', then final RMSNorm + lm_head GEMV over a "
+                     "synthetic 128256-token vocabulary + greedy ARGMAX, bf16 (int32 token)",
 }
 
 
@@ -70,13 +73,15 @@ def make_workload(name, device):
         return W.gemm_list(W.LLAMA70B_DECODE, device=device, seed=0), dict(pair)
     if name == "decode":
         return W.decode(device=device, seed=0), {}
+    if name == "decode_sample":
+        return W.decode(device=device, seed=0, vocab=128256), {}
     if name == "prefill":
         return W.prefill(device=device, seed=0), {}
     raise ValueError(name)
 
 
 def metric_of(name):
-    if name == "decode":
+    if name in ("decode", "decode_sample"):
         return "batch-1 decode latency", "us/token", False
     return "megakernel TFLOP/s", "TFLOP/s", True
 
@@ -101,14 +106,15 @@ def io_tensors(wl):
     if n == "mlp3":
         return [wl.info["x"], wl.info["w"], wl.info["b"]], [wl.info["outputs"][-1]]
     if n == "decode":
-        return [wl.info["x"]], [wl.info["out"]]
+        out = wl.info["token"] if wl.info.get("vocab") else wl.info["out"]
+        return [wl.info["x"]], [out]
     if n == "prefill":
         return [wl.info["x"]], [wl.info["out"]]
     raise ValueError(n)
 
 
 def value_of(wl, ms, name):
-    if name == "decode":
+    if name in ("decode", "decode_sample"):
         return ms * 1e3
     return wl.flops / (ms * 1e-3) / 1e12
 
@@ -234,7 +240,7 @@ def oracle_sample(name, seconds_budget=15.0):
         models.mlp(x, w, b)
         t = time.perf_counter() - t0
         return 2.0 * 3 * 1024 ** 3 / t / 1e12, "the full 3-layer MLP"
-    if name == "decode":
+    if name in ("decode", "decode_sample"):
         # two layers of the decoder, scaled to 16 (the layers are identical in cost)
         from tensor_core_gemm_gb300 import workloads as W
         sh = W.DecoderShape(layers=2)
@@ -247,9 +253,15 @@ def oracle_sample(name, seconds_budget=15.0):
         vc = [rng.standard_normal((1025, 512), dtype=np.float32) for _ in range(2)]
         x = rng.standard_normal((1, d), dtype=np.float32)
         t0 = time.perf_counter()
-        models.decode_step(x, wts, kc, vc, 1024)
+        x, _, _ = models.decode_step(x, wts, kc, vc, 1024)
         t = (time.perf_counter() - t0) * 8
-        return t * 1e6, "2 of 16 decoder layers, time x8"
+        if name == "decode":
+            return t * 1e6, "2 of 16 decoder layers, time x8"
+        w_lm = bf(d, 128256)
+        t0 = time.perf_counter()
+        models.decode_head(x, 1 + bf(d), w_lm, sh.eps)
+        t += time.perf_counter() - t0
+        return t * 1e6, "2 of 16 decoder layers, time x8, plus the full sampling head"
     if name == "prefill":
         from tensor_core_gemm_gb300 import workloads as W
         sh = W.DecoderShape(layers=1)
@@ -419,7 +431,7 @@ def main():
         cpu = {"value": v, "unit": unit, "cores": CORES, "kind": "oracle", "sample": sample}
 
     if rank == 0:
-        dtype = "bf16" if args.config in ("decode", "prefill") else "f16"
+        dtype = "bf16" if args.config in ("decode", "prefill", "decode_sample") else "f16"
         line = {
             "metric": metric, "value": value, "unit": unit, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,

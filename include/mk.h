@@ -20,7 +20,8 @@
  *  - Tensors are caller-owned device memory, registered by pointer. The library never frees
  *    or allocates them. A plan is bound to the pointers given at compile time.
  *  - Tensor ids and node ids are small non-negative integers local to one graph.
- *  - Element types: MK_F16 (IEEE half), MK_BF16 (bfloat16), MK_F32.
+ *  - Element types: MK_F16 (IEEE half), MK_BF16 (bfloat16), MK_F32; MK_I32 for the indices an
+ *    ARGMAX node writes.
  *  - Row-major 2-D view of every tensor: the innermost dimension is the column dimension and
  *    must have stride 1; all outer dimensions fold into rows and must be contiguous with each
  *    other. Row stride (elements) = strides[rank-2].
@@ -54,7 +55,7 @@ enum {
   MK_ERR_DEVICE_CHECK = 7,  /* a device-side consistency check failed; see mk_device_status */
 };
 
-enum { MK_F16 = 0, MK_BF16 = 1, MK_F32 = 2 };
+enum { MK_F16 = 0, MK_BF16 = 1, MK_F32 = 2, MK_I32 = 3 };
 
 /* ---------------------------------------------------------------- graph construction */
 
@@ -66,7 +67,7 @@ mk_status mk_graph_destroy(mk_graph_t g);
 /* Register a caller-owned device tensor.
  *   dev_ptr  device address (16-byte aligned for any tensor read or written by TMA: GEMM and
  *            GEMV operands). May be NULL only for plans compiled with dry_run.
- *   dtype    MK_F16 / MK_BF16 / MK_F32
+ *   dtype    MK_F16 / MK_BF16 / MK_F32 / MK_I32 (int32: ARGMAX outputs only)
  *   rank     1..4; shape[rank], strides[rank] in elements (strides may be NULL: contiguous)
  * The tensor is seen as rows x cols with cols = shape[rank-1]. */
 mk_status mk_add_tensor(mk_graph_t g, void* dev_ptr, int32_t dtype, int32_t rank,
@@ -111,6 +112,9 @@ enum {
   MK_EW_SILU_MUL = 3,   /* out = silu(in0) * in1 */
   MK_EW_RMSNORM = 16,   /* out = in0 / sqrt(mean(in0^2) + eps) * gamma (row-wise) */
   MK_EW_ROPE = 17,      /* rotary embedding of q and k heads (+ copy of v), see mk_ew_params */
+  MK_EW_ARGMAX = 18,    /* out[r] (MK_I32, R x 1) = the first column of in0's row r (f16 / bf16,
+                           R x C) holding its largest value; NaN entries are ignored, a row
+                           without a number gives -1 (greedy sampling of logits) */
 };
 
 typedef struct {
@@ -192,6 +196,8 @@ typedef struct {
                             copy follows mk_run_host copies into the weight, and mk_plan_repack
                             refreshes it after any other change to such a weight. 0: stream
                             them from the tensors through tensor maps */
+  int32_t argmax_chunk;  /* columns per ARGMAX partial instruction (multiple of 8); a reduce
+                            instruction per row block picks the winner of the partials */
 } mk_compile_opts;
 
 /* Fill *o with the defaults (the values listed above for each field). */

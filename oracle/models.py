@@ -108,6 +108,14 @@ def decode_step(x, wts, k_cache, v_cache, pos, layer_fn=None):
     return x, kc, vc
 
 
+def decode_head(x, g_final, w_lm, eps):
+    """Greedy sampling after the last layer: logits = GEMV(x, W_lm, RMS_NORM_INPUT g_final)
+    rounded to bf16, token = the first column holding the largest logit
+    ("Implementing a Mega Kernel for B300" §8: final norm, lm_head, SAMPLE)."""
+    logits = ops.matmul_norm_input(x, g_final, eps, w_lm, BF16)
+    return logits, ops.argmax_rows(logits)
+
+
 def prefill(x, wts, layer_fn=None):
     """Causal prefill of T tokens (positions 0..T-1) through every layer, batch 1.
 

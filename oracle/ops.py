@@ -234,3 +234,17 @@ def attention_reduce(m, l, o, out_dtype):
     big_l = np.sum(l * w, axis=1, dtype=np.float32)      # [H]
     big_o = np.sum(o * w[:, :, None], axis=1, dtype=np.float32) / big_l[:, None]
     return round_to(big_o.reshape(1, -1), out_dtype)
+
+
+def argmax_rows(x):
+    """Greedy sampling: per row the first column holding the row's largest value ([B300] §8
+    SAMPLE, the argmax of the logits). NaN entries take no part; a row without a number gives -1.
+    Returns int32 [rows × 1]. Pinned by brute force and planted ties (tests).
+    """
+    x = _f32(x)
+    out = np.full((x.shape[0], 1), -1, dtype=np.int32)
+    for r in range(x.shape[0]):
+        cols = np.nonzero(~np.isnan(x[r]))[0]
+        if cols.size:
+            out[r, 0] = cols[np.argmax(x[r, cols])]   # np.argmax: the first maximum
+    return out

@@ -20,7 +20,8 @@ Graph description (plain dicts, shared with the tests):
             {"kind": "rmsnorm", "x", "gamma", "out"},
             {"kind": "rope", "x", "out_q", "out_k", "out_v"?, "n_q_heads", "n_kv_heads", "head_dim"},
             {"kind": "attention", "q", "k", "v", "out", "n_q_heads", "n_kv_heads", "head_dim",
-             "causal", "q_pos0"}]
+             "causal", "q_pos0"},
+            {"kind": "argmax", "x", "out"}]
 
 Lowering rules per node (tile sizes come from ``opts``; see ``DEFAULT_OPTS``):
   matmul with M = 0 or N = 0 -> no instructions.
@@ -61,6 +62,11 @@ Lowering rules per node (tile sizes come from ``opts``; see ``DEFAULT_OPTS``):
       Fused (fuse_attn_reduce = 1, default): no reduce phase; each g owns a split semaphore, the
         partial with c = 0 also carries the group's output box, every partial of g carries its
         arrivals, and the last partial of g to finish combines the group's partials.
+  argmax  -> two phases. Partial: per block of norm_rows rows (outer), per chunk c of
+      argmax_chunk columns (inner): reads the block's rows of x on the chunk, writes columns
+      2c, 2c+1 of those rows of a per-node fp32 scratch [R x 2C]; n0 = first column, klen =
+      columns, aux0 = c. Reduce: one per row block; reads the block's scratch rows, writes its
+      rows of the output column; aux1 = C.
   attention with several query rows (prefill) -> one instruction per (q tile t of attn_tile_q
       rows, q head h), t descending (longest first), then h ascending; reads q rows of the tile,
       k and v rows [0, kmax) with kmax = min(Tk, q_pos0 + end of tile) when causal.
@@ -76,7 +82,7 @@ counters they arrive on in increasing id order.
 import numpy as np
 
 OP_NOOP, OP_GEMM, OP_GEMV, OP_EW, OP_RMSNORM, OP_ROPE, OP_ATTN_PARTIAL, OP_ATTN_REDUCE, \
-    OP_ATTN_PREFILL = range(9)
+    OP_ATTN_PREFILL, OP_ARGMAX, OP_ARGMAX_REDUCE = range(11)
 EW_CODES = {"add": 0, "relu": 1, "copy": 2, "silu_mul": 3}
 FLAG_B_DEP = 1
 
@@ -88,7 +94,7 @@ DEFAULT_OPTS = dict(
     ew_rows=128, ew_cols=128, ew_tiles=1,
     norm_rows=16,
     gemv_max_m=8, gemv_tile_n=256, gemv_splits=0, gemv_kstep=64,
-    attn_chunk=64, attn_tile_q=128,
+    attn_chunk=64, attn_tile_q=128, argmax_chunk=4096,
 )
 
 
@@ -267,6 +273,30 @@ def _lower_rows(ni, nd, opts, phases, op):
     phases.append(out)
 
 
+def _lower_argmax(ni, nd, opts, phases, tensors):
+    x, o = nd["x"], nd["out"]
+    rows, cols = x[3], x[4]
+    nr, ch = opts["norm_rows"], opts["argmax_chunk"]
+    nc = cdiv(cols, ch)
+    scratch_id = len(tensors)
+    tensors.append({"rows": rows, "cols": 2 * nc, "dtype": "f32", "internal": True})
+    scratch = (scratch_id, 0, 0, rows, 2 * nc)
+    part, red = [], []
+    for rt in range(cdiv(rows, nr)):
+        m0 = rt * nr
+        for c in range(nc):
+            ins = Instr(OP_ARGMAX, ni, m0, c * ch, 0, min(ch, cols - c * ch), c, 0)
+            ins.reads.append((_box(x, m0, m0 + nr, c * ch, c * ch + ch), ROLE_E))
+            ins.writes.append(_box(scratch, m0, m0 + nr, 2 * c, 2 * c + 2))
+            part.append(ins)
+        ins = Instr(OP_ARGMAX_REDUCE, ni, m0, 0, 0, 0, 0, nc)
+        ins.reads.append((_box(scratch, m0, m0 + nr, 0, 2 * nc), ROLE_E))
+        ins.writes.append(_box(o, m0, m0 + nr, 0, 1))
+        red.append(ins)
+    phases.append(part)
+    phases.append(red)
+
+
 def _lower_attention(ni, nd, opts, phases, tensors, sem_tiles):
     q, k, v, o = nd["q"], nd["k"], nd["v"], nd["out"]
     hq, hkv, d = nd["n_q_heads"], nd["n_kv_heads"], nd["head_dim"]
@@ -387,6 +417,8 @@ def lower(graph, opts):
                 _lower_rows(ni, nd, o, phases, OP_ROPE)
         elif kind == "attention":
             _lower_attention(ni, nd, o, phases, tensors, sem_tiles)
+        elif kind == "argmax":
+            _lower_argmax(ni, nd, o, phases, tensors)
         else:
             raise ValueError(kind)
 

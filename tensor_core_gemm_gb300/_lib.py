@@ -7,9 +7,9 @@ LIB_PATH = os.path.join(_PKG, "libmk.so")
 
 MK_OK, MK_ERR_INVALID_ARG, MK_ERR_UNSUPPORTED, MK_ERR_HAZARD, MK_ERR_OOM, MK_ERR_CUDA, \
     MK_ERR_TIMEOUT, MK_ERR_DEVICE_CHECK = range(8)
-MK_F16, MK_BF16, MK_F32 = 0, 1, 2
+MK_F16, MK_BF16, MK_F32, MK_I32 = 0, 1, 2, 3
 EPI_BIAS, EPI_RELU, EPI_RESIDUAL, EPI_RMSNORM_INPUT, EPI_SILU_MUL = 1, 2, 4, 8, 16
-EW_ADD, EW_RELU, EW_COPY, EW_SILU_MUL, EW_RMSNORM, EW_ROPE = 0, 1, 2, 3, 16, 17
+EW_ADD, EW_RELU, EW_COPY, EW_SILU_MUL, EW_RMSNORM, EW_ROPE, EW_ARGMAX = 0, 1, 2, 3, 16, 17, 18
 
 EXPORTS = [
     "mk_graph_create", "mk_graph_destroy", "mk_add_tensor", "mk_add_view", "mk_add_matmul",
@@ -42,7 +42,7 @@ class CompileOpts(C.Structure):
         "norm_rows", "gemv_max_m", "gemv_tile_n", "gemv_splits", "gemv_kstep", "attn_chunk",
         "attn_tile_q", "dry_run", "timeout_ms", "device", "debug_counter", "debug_extra",
         "snapshot_counters", "trace", "l2_prefetch", "gemm_split_tail", "fuse_rope",
-        "fuse_attn_reduce", "kernel_set", "gemv_pack")]
+        "fuse_attn_reduce", "kernel_set", "gemv_pack", "argmax_chunk")]
 
 
 class HostCopy(C.Structure):

@@ -19,13 +19,13 @@ INSTR_DTYPE = np.dtype([
 ])
 assert INSTR_DTYPE.itemsize == 64
 
-_DT = {"f16": _lib.MK_F16, "bf16": _lib.MK_BF16, "f32": _lib.MK_F32}
+_DT = {"f16": _lib.MK_F16, "bf16": _lib.MK_BF16, "f32": _lib.MK_F32, "i32": _lib.MK_I32}
 
 
 def _torch_dtype_code(t):
     import torch
     return {torch.float16: _lib.MK_F16, torch.bfloat16: _lib.MK_BF16,
-            torch.float32: _lib.MK_F32}[t.dtype]
+            torch.float32: _lib.MK_F32, torch.int32: _lib.MK_I32}[t.dtype]
 
 
 def _stream_handle(stream):
@@ -49,7 +49,8 @@ class Graph:
             self._h = C.c_void_p()
 
     def tensor(self, t=None, *, ptr=0, dtype=None, shape=None, strides=None):
-        """Register a torch tensor, or raw (ptr, dtype 'f16'|'bf16'|'f32', shape, strides)."""
+        """Register a torch tensor, or raw (ptr, dtype 'f16'|'bf16'|'f32'|'i32', shape,
+        strides)."""
         if t is not None:
             ptr = t.data_ptr()
             dtype = _torch_dtype_code(t)
@@ -114,6 +115,10 @@ class Graph:
         p = _lib.EwParams(0.0, -1, n_q_heads, n_kv_heads, head_dim, pos0, float(theta), out_k,
                           -1 if out_v is None else out_v)
         return self._ew(_lib.EW_ROPE, [x], out_q, p)
+
+    def argmax(self, x, out):
+        """out [R x 1] int32 = per row of x the first column holding its largest value."""
+        return self._ew(_lib.EW_ARGMAX, [x], out)
 
     def attention(self, q, k, v, out, *, n_q_heads, n_kv_heads, head_dim, causal=False,
                   q_pos0=0, scale=0.0):

@@ -29,7 +29,8 @@ void set_error(const char* fmt, ...) {
   g_err = buf;
 }
 
-int dtype_size(int dt) { return dt == DT_F32 ? 4 : 2; }
+int dtype_size(int dt) { return dt == DT_F32 || dt == DT_I32 ? 4 : 2; }
+static bool half_type(int dt) { return dt == DT_F16 || dt == DT_BF16; }
 
 static inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -227,6 +228,48 @@ static void lower_rows(const std::vector<TensorRec>& ts, int ni, const NodeRec& 
   phases.push_back(std::move(out));
 }
 
+// ARGMAX of every row of x [R x C]: per block of norm_rows rows, one instruction per chunk of
+// argmax_chunk columns writes the chunk's (largest value, first column holding it) of each row
+// to an internal fp32 tensor [R x 2 * chunks] (the column as a float: exact below 2^24), then
+// one instruction per row block picks the winner of the row's partials (ties: the lower
+// column) and writes it as int32.
+static void lower_argmax(std::vector<TensorRec>& ts, int ni, const NodeRec& nd,
+                         const mk_compile_opts& o, std::vector<std::vector<HInstr>>& phases,
+                         HostPlan* plan) {
+  const int x = nd.ins[0];
+  const int64_t rows = ts[x].rows, cols = ts[x].cols, nr = o.norm_rows;
+  const int64_t ch = o.argmax_chunk, nc = cdiv(cols, ch);
+  TensorRec s;
+  s.dtype = DT_F32;
+  s.rows = rows;
+  s.cols = 2 * nc;
+  s.ld = 2 * nc;
+  s.base = (int)ts.size();
+  s.internal = true;
+  const int sid = s.base;
+  ts.push_back(s);
+  plan->node_scratch[ni] = sid;
+  plan->node_chunks[ni] = (int)nc;
+  std::vector<HInstr> part, red;
+  for (int64_t rt = 0; rt < cdiv(rows, nr); ++rt) {
+    const int64_t m0 = rt * nr;
+    for (int64_t c = 0; c < nc; ++c) {
+      HInstr h = make(OP_ARGMAX, ni, (int)m0, (int)(c * ch), 0, (int)std::min(ch, cols - c * ch));
+      h.rec.aux0 = (int)c;
+      h.reads.push_back({window(ts, x, m0, m0 + nr, c * ch, c * ch + ch), ROLE_E});
+      h.writes.push_back(window(ts, sid, m0, m0 + nr, 2 * c, 2 * c + 2));
+      part.push_back(std::move(h));
+    }
+    HInstr h = make(OP_ARGMAX_REDUCE, ni, (int)m0);
+    h.rec.aux1 = (int)nc;
+    h.reads.push_back({window(ts, sid, m0, m0 + nr, 0, 2 * nc), ROLE_E});
+    h.writes.push_back(window(ts, nd.out, m0, m0 + nr, 0, 1));
+    red.push_back(std::move(h));
+  }
+  phases.push_back(std::move(part));
+  phases.push_back(std::move(red));
+}
+
 static void lower_attention(std::vector<TensorRec>& ts, int ni, const NodeRec& nd,
                             const mk_compile_opts& o, std::vector<std::vector<HInstr>>& phases,
                             int& n_tiles_sem, HostPlan* plan) {
@@ -301,8 +344,10 @@ mk_status lower_graph(const std::vector<TensorRec>& tensors_in, const std::vecto
                       const mk_compile_opts& o, HostPlan* plan) {
   if (o.n_sm <= 0 || o.cluster <= 0 || o.gemm_tile_m <= 0 || o.gemm_tile_n <= 0 ||
       o.ew_rows <= 0 || o.ew_cols <= 0 || o.ew_tiles <= 0 || o.norm_rows <= 0 ||
-      o.gemv_tile_n <= 0 || o.gemv_kstep <= 0 || o.attn_chunk <= 0 || o.attn_tile_q <= 0) {
-    set_error("mk_compile: every tile size and n_sm must be positive");
+      o.gemv_tile_n <= 0 || o.gemv_kstep <= 0 || o.attn_chunk <= 0 || o.attn_tile_q <= 0 ||
+      o.argmax_chunk <= 0 || o.argmax_chunk % 8) {
+    set_error("mk_compile: every tile size and n_sm must be positive (argmax_chunk a multiple "
+              "of 8)");
     return MK_ERR_INVALID_ARG;
   }
   std::vector<TensorRec> ts = tensors_in;
@@ -334,6 +379,7 @@ mk_status lower_graph(const std::vector<TensorRec>& tensors_in, const std::vecto
         if (!fused[ni]) lower_rows(ts, ni, nd, o, OP_ROPE, phases);
         break;
       case NK_ATTN: lower_attention(ts, ni, nd, o, phases, n_tiles_sem, plan); break;
+      case NK_ARGMAX: lower_argmax(ts, ni, nd, o, phases, plan); break;
       default: set_error("mk_compile: unknown node kind %d", nd.kind); return MK_ERR_INVALID_ARG;
     }
   }
@@ -483,7 +529,7 @@ extern "C" mk_status mk_add_tensor(mk_graph_t g, void* dev_ptr, int32_t dtype, i
     set_error("mk_add_tensor: null argument or rank outside 1..4");
     return MK_ERR_INVALID_ARG;
   }
-  if (dtype != MK_F16 && dtype != MK_BF16 && dtype != MK_F32) {
+  if (dtype != MK_F16 && dtype != MK_BF16 && dtype != MK_F32 && dtype != MK_I32) {
     set_error("mk_add_tensor: unknown dtype %d", dtype);
     return MK_ERR_INVALID_ARG;
   }
@@ -567,7 +613,7 @@ extern "C" mk_status mk_add_matmul(mk_graph_t g, int32_t a, int32_t b, int32_t o
               (long long)C.rows, (long long)C.cols);
     return MK_ERR_INVALID_ARG;
   }
-  if (A.dtype == MK_F32 || B.dtype != A.dtype || C.dtype != A.dtype) {
+  if (!half_type(A.dtype) || B.dtype != A.dtype || C.dtype != A.dtype) {
     set_error("mk_add_matmul: A, B and out must share one dtype, f16 or bf16");
     return MK_ERR_UNSUPPORTED;
   }
@@ -638,7 +684,8 @@ extern "C" mk_status mk_add_elementwise(mk_graph_t g, int32_t op, const int32_t*
         return MK_ERR_INVALID_ARG;
       }
       for (int i = 0; i < n_in; ++i)
-        if (!same_shape(g, ins[i], O.rows, O.cols) || g->tensors[ins[i]].dtype != O.dtype) {
+        if (!same_shape(g, ins[i], O.rows, O.cols) || g->tensors[ins[i]].dtype != O.dtype ||
+            O.dtype == MK_I32) {
           set_error("mk_add_elementwise: inputs must match the output's shape and dtype "
                     "(no broadcasting)");
           return MK_ERR_INVALID_ARG;
@@ -648,7 +695,7 @@ extern "C" mk_status mk_add_elementwise(mk_graph_t g, int32_t op, const int32_t*
       break;
     }
     case MK_EW_RMSNORM: {
-      if (!p || n_in != 1 || !same_shape(g, ins[0], O.rows, O.cols) ||
+      if (!p || n_in != 1 || !same_shape(g, ins[0], O.rows, O.cols) || !half_type(O.dtype) ||
           !valid_tensor(g, p->gamma) || !same_shape(g, p->gamma, 1, O.cols) ||
           g->tensors[ins[0]].dtype != O.dtype || g->tensors[p->gamma].dtype != O.dtype) {
         set_error("mk_add_elementwise: RMSNORM needs x and out of one shape and gamma 1 x cols");
@@ -675,6 +722,10 @@ extern "C" mk_status mk_add_elementwise(mk_graph_t g, int32_t op, const int32_t*
                   "[R x Hkv*d]", (long long)want);
         return MK_ERR_INVALID_ARG;
       }
+      if (!half_type(g->tensors[ins[0]].dtype)) {
+        set_error("mk_add_elementwise: ROPE runs f16 / bf16");
+        return MK_ERR_UNSUPPORTED;
+      }
       nd.kind = NK_ROPE;
       nd.out_k = p->out_k;
       nd.out_v = p->out_v;
@@ -683,6 +734,15 @@ extern "C" mk_status mk_add_elementwise(mk_graph_t g, int32_t op, const int32_t*
       nd.hd = p->head_dim;
       nd.pos0 = p->pos0;
       nd.theta = p->theta;
+      break;
+    }
+    case MK_EW_ARGMAX: {
+      const TensorRec& X = g->tensors[ins[0]];
+      if (n_in != 1 || !half_type(X.dtype) || O.dtype != MK_I32 || !same_shape(g, out, X.rows, 1)) {
+        set_error("mk_add_elementwise: ARGMAX takes x [R x C] f16 / bf16 and out [R x 1] i32");
+        return MK_ERR_INVALID_ARG;
+      }
+      nd.kind = NK_ARGMAX;
       break;
     }
     default:
@@ -748,6 +808,7 @@ extern "C" mk_status mk_default_opts(mk_compile_opts* o) {
   o->gemv_splits = 0;
   o->gemv_kstep = 64;
   o->attn_chunk = 64;
+  o->argmax_chunk = 4096;
   o->attn_tile_q = 128;
   o->dry_run = 0;
   o->timeout_ms = 2000;

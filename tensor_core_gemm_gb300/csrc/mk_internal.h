@@ -24,7 +24,7 @@ struct TensorRec {
   bool internal = false;    // plan-owned scratch created by the lowering
 };
 
-enum NodeKind { NK_MATMUL = 0, NK_EW = 1, NK_RMSNORM = 2, NK_ROPE = 3, NK_ATTN = 4 };
+enum NodeKind { NK_MATMUL = 0, NK_EW = 1, NK_RMSNORM = 2, NK_ROPE = 3, NK_ATTN = 4, NK_ARGMAX = 5 };
 
 struct NodeRec {
   int kind = 0;

@@ -1962,6 +1962,92 @@ __device__ __forceinline__ void rope_body(Smem& s, const Instr& in, const Node& 
   }
 }
 
+// ARGMAX: (value, column) pairs where a larger value wins and equal values go to the lower
+// column; a column < 0 marks "no number yet" and loses to any number (NaN entries are skipped).
+__device__ __forceinline__ void argmax_take(float& bv, int& bi, float v, int i) {
+  if (i >= 0 && (bi < 0 || v > bv || (v == bv && i < bi))) {
+    bv = v;
+    bi = i;
+  }
+}
+__device__ __forceinline__ void argmax_warp(float& bv, int& bi) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    const float v = __shfl_xor_sync(FULL, bv, o);
+    const int i = __shfl_xor_sync(FULL, bi, o);
+    argmax_take(bv, bi, v, i);
+  }
+}
+
+// ARGMAX partial: rows [m0, m0 + tile_m) x columns [n0, n0 + klen) of x. Per row the largest
+// value and the first column holding it go to the node's fp32 scratch as two floats at columns
+// 2 * aux0 (a column as a float is exact below 2^24). A warp per row; each lane scans its
+// 8-column vectors in increasing column order, four vectors in flight.
+__device__ __forceinline__ void argmax_partial_body(const Instr& in, const Node& nd) {
+  const int ct = (int)threadIdx.x - (kThreads - kCompute);
+  const int wp = ct >> 5, lane = ct & 31;
+  const int rows = min(nd.tile_m, nd.M - in.m0), dt = nd.dtype;
+  const int c1 = in.n0 + in.klen;
+  const uint16_t* x = reinterpret_cast<const uint16_t*>(nd.a.ptr);
+  float* sc = reinterpret_cast<float*>(nd.scratch.ptr);
+  for (int r = wp; r < rows; r += 4) {
+    const uint16_t* row = x + (size_t)(in.m0 + r) * nd.a.ld;
+    const bool vec = ((uintptr_t)row & 15u) == 0;  // 16-byte loads need an aligned row
+    float bv = -INFINITY;
+    int bi = -1;
+    for (int v0 = in.n0 + lane * 8; v0 < c1; v0 += 4 * 256) {
+      uint4 q[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int c = v0 + u * 256;
+        if (c < c1 && vec && c + 8 <= c1) q[u] = __ldcg(reinterpret_cast<const uint4*>(row + c));
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int c = v0 + u * 256;
+        if (c >= c1) continue;
+        float f[8];
+        if (vec && c + 8 <= c1) {
+          unpack8(q[u], dt, f);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) f[e] = c + e < c1 ? h2f(__ldcg(row + c + e), dt) : NAN;
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          if (f[e] == f[e]) argmax_take(bv, bi, f[e], c + e);
+      }
+    }
+    argmax_warp(bv, bi);
+    if (lane == 0) {
+      float* o = sc + (size_t)(in.m0 + r) * nd.scratch.ld + 2 * in.aux0;
+      o[0] = bv;
+      o[1] = (float)bi;
+    }
+  }
+}
+
+// ARGMAX reduce: per row of the block, the winner of the aux1 chunk partials, as int32 (-1 when
+// the row holds no number).
+__device__ __forceinline__ void argmax_reduce_body(const Instr& in, const Node& nd) {
+  const int ct = (int)threadIdx.x - (kThreads - kCompute);
+  const int wp = ct >> 5, lane = ct & 31;
+  const int rows = min(nd.tile_m, nd.M - in.m0), C = in.aux1;
+  const float* sc = reinterpret_cast<const float*>(nd.scratch.ptr);
+  int32_t* out = reinterpret_cast<int32_t*>(nd.out.ptr);
+  for (int r = wp; r < rows; r += 4) {
+    const float* pr = sc + (size_t)(in.m0 + r) * nd.scratch.ld;
+    float bv = -INFINITY;
+    int bi = -1;
+    for (int c = lane; c < C; c += 32) {
+      const float2 vi = __ldcg(reinterpret_cast<const float2*>(pr + 2 * c));
+      argmax_take(bv, bi, vi.x, (int)vi.y);
+    }
+    argmax_warp(bv, bi);
+    if (lane == 0) out[(size_t)(in.m0 + r) * nd.out.ld] = bi;
+  }
+}
+
 // Split-KV partial for kv group g = n0 and keys [k0, k0 + klen): per query head of the group
 // m = max s, l = sum e^{s - m}, o = sum e^{s - m} v   (head_dim 64, up to 128 keys).
 // Keys and values arrive by TMA in one ring stage, 128-byte swizzled (16-byte chunk c of row r
@@ -2266,6 +2352,8 @@ __device__ void run_compute(const Params& p, Smem& s, uint32_t tmem) {
         else if (ks_has_rows(KS) && in.op == OP_RMSNORM) rmsnorm_body<KS != KS_PREFILL>(in, nd);
         else if (ks_has_rows(KS) && in.op == OP_ROPE) rope_body<KS != KS_PREFILL>(s, in, nd);
         else if (ks_has_gemv(KS) && in.op == OP_ATTN_REDUCE) attn_reduce_body(in, nd);
+        else if (ks_has_rows(KS) && in.op == OP_ARGMAX) argmax_partial_body(in, nd);
+        else if (ks_has_rows(KS) && in.op == OP_ARGMAX_REDUCE) argmax_reduce_body(in, nd);
         else {
           if (ct == 0) report(p, MK_ERR_DEVICE_CHECK, idx, -1, in.op, 0, R_COMPUTE, 34);
           ok = false;

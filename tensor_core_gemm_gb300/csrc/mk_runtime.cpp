@@ -186,7 +186,8 @@ mk_status check_kernel_support(const std::vector<TensorRec>& ts, const std::vect
         set_error("mk_compile: node %zu uses tensor %d with a NULL device pointer", i, id);
         return MK_ERR_INVALID_ARG;
       }
-      if (!aligned16(ts[id]) || ts[id].cols % 8) {
+      // ARGMAX reads rows that are not 16-byte aligned element by element and stores one int32
+      if (nd.kind != NK_ARGMAX && (!aligned16(ts[id]) || ts[id].cols % 8)) {
         set_error("mk_compile: node %zu tensor %d: start address and row stride must be 16-byte "
                   "aligned and cols a multiple of 8", i, id);
         return MK_ERR_UNSUPPORTED;
@@ -447,6 +448,16 @@ static mk_status build_nodes(const mk_graph* g, mk_plan* p, std::vector<CUtensor
         n.M = (int)ts[nd.ins[0]].rows;
         n.N = (int)ts[nd.ins[0]].cols;
         n.a = operand(ts, nd.ins[0]);
+        break;
+      case NK_ARGMAX:
+        n.kind = OP_ARGMAX;
+        n.tile_m = p->opts.norm_rows;
+        n.dtype = ts[nd.ins[0]].dtype;
+        n.M = (int)ts[nd.ins[0]].rows;
+        n.N = (int)ts[nd.ins[0]].cols;
+        n.a = operand(ts, nd.ins[0]);
+        n.n_chunks = p->hp.node_chunks[i];
+        if (p->hp.node_scratch[i] >= 0) n.scratch.ld = (int)ts[p->hp.node_scratch[i]].ld;
         break;
       case NK_ATTN:
         n.kind = ts[nd.a].rows == 1 ? OP_ATTN_PARTIAL : OP_ATTN_PREFILL;

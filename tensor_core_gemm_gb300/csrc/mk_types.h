@@ -27,6 +27,8 @@ enum Op : uint16_t {
   OP_ATTN_PARTIAL = 6,  // split-KV partial (m, l, o) for one kv group and key chunk
   OP_ATTN_REDUCE = 7,   // LSE merge of one kv group's partials
   OP_ATTN_PREFILL = 8,  // causal attention for one (q tile, head)
+  OP_ARGMAX = 9,        // block of rows x column chunk: (max, first index) partials
+  OP_ARGMAX_REDUCE = 10,  // block of rows: the winner of the row's partials
   OP_END = 0xFFFF,      // past the end of an SM's queue (never stored in the list)
 };
 
@@ -50,7 +52,7 @@ static_assert(offsetof(Instr, node) == 4 && offsetof(Instr, sem) == 32 &&
                   offsetof(Instr, dst_off) == 48,
               "instruction field offsets are part of the ABI");
 
-enum DType : int32_t { DT_F16 = 0, DT_BF16 = 1, DT_F32 = 2 };
+enum DType : int32_t { DT_F16 = 0, DT_BF16 = 1, DT_F32 = 2, DT_I32 = 3 };
 
 enum : uint32_t {
   EPI_BIAS = 1u << 0,

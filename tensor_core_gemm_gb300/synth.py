@@ -6,7 +6,8 @@ not depend on creation order across workloads.
 """
 import torch
 
-DTYPES = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+DTYPES = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32,
+          "i32": torch.int32}
 
 
 def normal(shape, std, dtype, seed, device="cpu", mean=0.0):

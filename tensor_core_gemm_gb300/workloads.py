@@ -143,9 +143,11 @@ def _decoder_weights(sh, tensors, specs):
     return ids
 
 
-def decode(sh=None, kv_len=1024, device=None, seed=0):
+def decode(sh=None, kv_len=1024, device=None, seed=0, vocab=0):
     """Batch-1 decode of one token at position p = kv_len through every layer; the cache holds
-    positions 0..p-1 (~N(0,1)) and gets row p appended; split-KV attention over p+1 keys."""
+    positions 0..p-1 (~N(0,1)) and gets row p appended; split-KV attention over p+1 keys.
+    vocab > 0 adds greedy sampling: final RMSNorm (gamma ~N(1,0.02)) fused into an lm_head GEMV
+    (W_lm [hidden x vocab] ~N(0,0.02)) writing bf16 logits, then ARGMAX -> int32 token."""
     sh = sh or DecoderShape()
     d, f, L, hd = sh.hidden, sh.ffn, sh.layers, sh.hd
     kvw = sh.hkv * hd
@@ -190,16 +192,29 @@ def decode(sh=None, kv_len=1024, device=None, seed=0):
         nodes.append({"kind": "matmul", "a": (gu, l, 0, 1, f), "b": (w["wd"], l * f, 0, f, d),
                       "c": (xo, l, 0, 1, d), "residual": (hh, l, 0, 1, d)})
         x_prev = (xo, l, 0, 1, d)
+    head = {}
+    if vocab > 0:
+        head["w_lm"] = add(d, vocab, ("normal", 0.02))
+        head["g_f"] = add(1, d, ("normal", 0.02, 1.0))
+        head["logits"] = add(1, vocab)
+        tensors.append({"rows": 1, "cols": 1, "dtype": "i32"})
+        specs.append(("zeros",))
+        head["token"] = len(tensors) - 1
+        nodes.append({"kind": "matmul", "a": x_prev, "b": full(head["w_lm"], d, vocab),
+                      "c": full(head["logits"], 1, vocab), "gamma": full(head["g_f"], 1, d),
+                      "eps": sh.eps})
+        nodes.append({"kind": "argmax", "x": full(head["logits"], 1, vocab),
+                      "out": full(head["token"], 1, 1)})
     data = _mk(tensors, specs, device, seed)
     if data is not None:
         for l in range(L):            # the new token's cache row starts empty
             data[kc][l * cap + p].zero_()
             data[vc][l * cap + p].zero_()
     kv_bytes = 2 * L * 2 * (p + 1) * kvw
-    hbm = sh.weight_bytes() + kv_bytes
-    flops = 2.0 * (sh.weight_bytes() / 2) + 4.0 * L * sh.hq * hd * (p + 1)
+    hbm = sh.weight_bytes() + kv_bytes + 2 * d * vocab
+    flops = 2.0 * (sh.weight_bytes() / 2) + 4.0 * L * sh.hq * hd * (p + 1) + 2.0 * d * vocab
     info = dict(shape=sh, x=0, w=w, kc=kc, vc=vc, qkv=qkv, qr=qr, att=att, h=hh, gu=gu, out=xo,
-                cap=cap, pos=p)
+                cap=cap, pos=p, vocab=vocab, **head)
     return Workload("decode", {"tensors": tensors, "nodes": nodes}, data, flops, hbm, info)
 
 
@@ -295,6 +310,8 @@ def build_graph(desc, data=None):
                    out_v=id_of(nd.get("out_v")), n_q_heads=nd["n_q_heads"],
                    n_kv_heads=nd["n_kv_heads"], head_dim=nd["head_dim"], pos0=nd.get("pos0", 0),
                    theta=nd.get("theta", 5e5))
+        elif k == "argmax":
+            g.argmax(id_of(nd["x"]), id_of(nd["out"]))
         elif k == "attention":
             g.attention(id_of(nd["q"]), id_of(nd["k"]), id_of(nd["v"]), id_of(nd["out"]),
                         n_q_heads=nd["n_q_heads"], n_kv_heads=nd["n_kv_heads"],

@@ -801,3 +801,52 @@ def test_kernel_set_option_validated():
     g, _ = workloads.build_graph(workloads.gemm(64, 64, 64).desc, None)
     with pytest.raises(Exception, match="kernel_set"):
         g.compile(kernel_set=2)
+
+
+# ------------------------------------------------------------------ greedy sampling (ARGMAX)
+
+@pytest.mark.parametrize("rows,cols,dt,chunk", [(1, 128256, "bf16", 4096), (37, 10000, "bf16", 1024),
+                                               (5, 777, "f16", 64), (3, 4096, "bf16", 4096)])
+def test_argmax_rows_exact(rows, cols, dt, chunk):
+    """The chosen column is bit-exact against the oracle on the same stored values, including
+    planted ties (the lower column wins), NaN entries (skipped) and a row of NaN (-1)."""
+    x = synth.normal((rows, cols), 1.0, dt, 61, DEV)
+    if rows > 1:
+        x[1, cols // 3] = 8.0
+        x[1, cols - 1] = 8.0
+        x[min(2, rows - 1), :] = float("nan")
+    if rows > 3:
+        x[3, 0] = float("nan")
+        x[3, cols // 2] = 9.0
+    out = torch.full((rows, 1), -7, dtype=torch.int32, device=DEV)
+    from tensor_core_gemm_gb300 import Graph
+    g = Graph()
+    ix, io = g.tensor(x), g.tensor(out)
+    g.argmax(ix, io)
+    p = g.compile(argmax_chunk=chunk, snapshot_counters=1)
+    p.run()
+    p.check_status()
+    want = ops.argmax_rows(f32(x))
+    assert out.cpu().numpy().tolist() == want.tolist()
+
+
+def test_decode_greedy_sampling_head():
+    """Final RMSNorm fused into the lm_head GEMV, then ARGMAX: the logits match the oracle's
+    head applied to the GPU's last residual row, and the token is exactly the first maximum of
+    the GPU's own logits (and the oracle's token where its top two logits are apart)."""
+    sh = workloads.DecoderShape(layers=2, hidden=512, n_q_heads=8, n_kv_heads=2, head_dim=64,
+                                ffn=1024)
+    wl = workloads.decode(sh, kv_len=130, device=DEV, seed=5, vocab=5000)
+    plan, _ = run(wl)
+    check_counters(plan, wl, {})
+    info = wl.info
+    x_last = f32(wl.data[info["out"]])[-1:]
+    logits_ref, token_ref = models.decode_head(x_last, f32(wl.data[info["g_f"]])[0], f32(wl.data[info["w_lm"]]),
+                                               sh.eps)
+    logits = f32(wl.data[info["logits"]])
+    assert_close(logits, logits_ref, "logits")
+    token = int(wl.data[info["token"]].item())
+    assert token == int(ops.argmax_rows(logits)[0, 0])
+    top = np.sort(logits_ref[0])[-2:]
+    if top[1] - top[0] > 2e-2 * max(1.0, abs(top[1])):
+        assert token == int(token_ref[0, 0])

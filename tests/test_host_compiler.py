@@ -189,6 +189,21 @@ def test_gemv_split_and_unfused_elementwise_plans():
                      dict(n_sm=16, ew_rows=64, ew_cols=64, ew_tiles=2, gemm_tile_n=128))
 
 
+def test_argmax_plans():
+    """ARGMAX lowers to chunk partials and one reduce per row block, bit-exact with the oracle
+    (ragged rows and chunks; the decode head after the last layer)."""
+    desc = {"tensors": [{"rows": 37, "cols": 10000, "dtype": "bf16"},
+                        {"rows": 37, "cols": 1, "dtype": "i32"}],
+            "nodes": [{"kind": "argmax", "x": (0, 0, 0, 37, 10000), "out": (1, 0, 0, 37, 1)}]}
+    py, c = assert_same_plan(desc, dict(n_sm=16, argmax_chunk=1024))
+    assert c.stats()["per_op"][osched.OP_ARGMAX] == 3 * 10
+    assert c.stats()["per_op"][osched.OP_ARGMAX_REDUCE] == 3
+    sh = workloads.DecoderShape(layers=2, hidden=256, n_q_heads=4, n_kv_heads=2, head_dim=64,
+                                ffn=512)
+    assert_same_plan(workloads.decode(sh, kv_len=100, vocab=5000).desc, dict(n_sm=40))
+    assert_same_plan(workloads.decode(vocab=128256).desc, dict(n_sm=152))
+
+
 def test_final_counter_values_definition():
     py = osched.lower(workloads.gemm(1, 512, 1024, dtype="bf16").desc, dict(n_sm=8))
     fin = py.final_counters()

@@ -367,3 +367,42 @@ def test_schedule_brute_force_matches_naive_pairs():
         for cid, _ in c.src:
             got |= {j for j, p in enumerate(plan.instrs) if cid in p.dst}
         assert got == want
+
+
+def test_argmax_rows_first_maximum_nan_and_empty_rows():
+    """Greedy sampling: the first column of the row maximum; NaN ignored; no number -> -1.
+    Checked against a plain scan and hand-placed cases (ties, -inf only, all NaN)."""
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((7, 37)).astype(np.float32)
+    x[1, [5, 20]] = 9.0                      # tie: the lower column wins
+    x[2, :] = np.nan
+    x[2, 30] = -np.inf                       # the only number is -inf
+    x[3, :] = np.nan                         # no number at all
+    x[4, 0] = np.nan
+    x[4, 7] = 50.0
+    x[5, :] = 0.0                            # all equal: column 0
+    x[6, :] = np.float32(np.finfo(np.float32).max)
+    x[6, 36] = np.inf                        # +inf beats every finite value
+    got = ops.argmax_rows(x).ravel().tolist()
+    want = []
+    for row in x:
+        best = -1
+        for j, v in enumerate(row):
+            if v != v:
+                continue
+            if best < 0 or v > row[best]:
+                best = j
+        want.append(best)
+    assert got == want
+    assert got[1] == 5 and got[2] == 30 and got[3] == -1 and got[4] == 7 and got[5] == 0
+    assert got[6] == 36
+
+
+def test_argmax_on_rounded_logits_decides_on_the_stored_values():
+    """Two logits that differ in fp32 but round to one bf16 value tie after rounding: the
+    decision is taken on the stored (rounded) values, so the lower column wins."""
+    a = np.float32(1.0)
+    b = np.nextafter(a, np.float32(2.0))     # fp32 neighbour, same bf16
+    x = round_to(np.array([[0.5, a, b, 0.25]], dtype=np.float32), BF16)
+    assert x[0, 1] == x[0, 2]
+    assert ops.argmax_rows(x)[0, 0] == 1
