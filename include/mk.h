@@ -198,6 +198,9 @@ typedef struct {
                             them from the tensors through tensor maps */
   int32_t argmax_chunk;  /* columns per ARGMAX partial instruction (multiple of 8); a reduce
                             instruction per row block picks the winner of the partials */
+  int32_t gemm_group_m;  /* GEMM tile order: groups of this many row tiles, column by column
+                            inside a group (L2 reuse of the B and A panels of a wave);
+                            1: row-major. Default 8 */
 } mk_compile_opts;
 
 /* Fill *o with the defaults (the values listed above for each field). */

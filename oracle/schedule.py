@@ -26,7 +26,9 @@ Graph description (plain dicts, shared with the tests):
 Lowering rules per node (tile sizes come from ``opts``; see ``DEFAULT_OPTS``):
   matmul with M = 0 or N = 0 -> no instructions.
   matmul, M > gemv_max_m  -> GEMM tiles tile_m × tn (tn = tile_n, or tile_n/2 with a second
-      weight "b2" for SiLU·mul), row-major over (mt, nt), each tile repeated ``cluster`` times
+      weight "b2" for SiLU·mul) in groups of gemm_group_m row tiles (the last group may be
+      shorter): group by group, inside a group column by column and row by row within a column
+      (gemm_group_m = 1: row-major over (mt, nt)); each tile repeated ``cluster`` times
       (aux0 = rank). Reads A rows×[0,K), B [0,K)×cols (and b2), bias/residual on the tile box;
       writes the tile box (every instruction of a cluster writes the whole cluster tile).
       Split tail (gemm_split_tail = 1; default 0): with T tiles on U = n_sm div cluster units, the last
@@ -94,7 +96,7 @@ DEFAULT_OPTS = dict(
     ew_rows=128, ew_cols=128, ew_tiles=1,
     norm_rows=16,
     gemv_max_m=8, gemv_tile_n=256, gemv_splits=0, gemv_kstep=64,
-    attn_chunk=64, attn_tile_q=128, argmax_chunk=4096,
+    attn_chunk=64, attn_tile_q=128, argmax_chunk=4096, gemm_group_m=8,
 )
 
 
@@ -213,8 +215,11 @@ def _lower_matmul(ni, nd, opts, phases, sem_tiles, rope=None):
         r_tail = t_all % units if units > 0 else 0
         n_split = min(units // r_tail, nks) if (opts["gemm_split_tail"] and r_tail) else 1
         split_from = t_all - r_tail if n_split >= 2 else t_all
+        nmt, gm = cdiv(m, tm), max(1, opts["gemm_group_m"])
         for t in range(t_all):
-            m0, n0 = (t // nnt) * tm, (t % nnt) * tn
+            g, r = divmod(t, gm * nnt)
+            rows_g = min(gm, nmt - g * gm)
+            m0, n0 = (g * gm + r % rows_g) * tm, (r // rows_g) * tn
             if t < split_from:
                 ranges, base = [(0, k)], None
             else:

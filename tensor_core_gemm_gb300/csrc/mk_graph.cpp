@@ -152,8 +152,13 @@ static void lower_matmul(const std::vector<TensorRec>& ts, int ni, const NodeRec
     const int64_t chunk = n_split >= 2 ? cdiv(nks, n_split) * kGemmBK : k;
     const int64_t n_ranges = n_split >= 2 ? cdiv(k, chunk) : 1;
     int slots = 0;
+    // Tile order: groups of gemm_group_m row tiles, column-major inside a group (consecutive
+    // tiles share B panels and a group's A panels stay in L2); 1 = row-major.
+    const int64_t nmt = cdiv(m, tm), gm = std::max(1, o.gemm_group_m);
     for (int64_t t = 0; t < t_all; ++t) {
-      const int64_t m0 = (t / nnt) * tm, n0 = (t % nnt) * tn;
+      const int64_t g = t / (gm * nnt), r = t % (gm * nnt);
+      const int64_t rows_g = std::min(gm, nmt - g * gm);
+      const int64_t m0 = (g * gm + r % rows_g) * tm, n0 = (r / rows_g) * tn;
       const bool split = t >= split_from;
       const int64_t nr = split ? n_ranges : 1;
       int base = -1, slot0 = 0;
@@ -809,6 +814,7 @@ extern "C" mk_status mk_default_opts(mk_compile_opts* o) {
   o->gemv_kstep = 64;
   o->attn_chunk = 64;
   o->argmax_chunk = 4096;
+  o->gemm_group_m = 8;
   o->attn_tile_q = 128;
   o->dry_run = 0;
   o->timeout_ms = 2000;

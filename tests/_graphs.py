@@ -26,4 +26,5 @@ def mlp_unfused(m=1024, h=1024, layers=3, dtype="bf16"):
 
 
 P3_OPTS = dict(n_sm=148, gemm_tile_m=512, gemm_tile_n=256, cluster=2, gemm_split_tail=0,
+               gemm_group_m=1,
                ew_rows=128, ew_cols=128, ew_tiles=2)

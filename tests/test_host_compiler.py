@@ -189,6 +189,21 @@ def test_gemv_split_and_unfused_elementwise_plans():
                      dict(n_sm=16, ew_rows=64, ew_cols=64, ew_tiles=2, gemm_tile_n=128))
 
 
+@pytest.mark.parametrize("gm", [1, 2, 3, 8])
+def test_grouped_gemm_tile_order(gm):
+    """Tiles go group by group of gm row tiles, column by column inside a group, row by row
+    within a column (the last group shorter), bit-exact with the oracle for every group size."""
+    desc = workloads.gemm(5 * 128, 3 * 256, 192).desc
+    py, c = assert_same_plan(desc, dict(n_sm=8, gemm_group_m=gm))
+    order = [(i.m0 // 128, i.n0 // 256) for i in py.instrs if i.op == osched.OP_GEMM]
+    want = []
+    for g0 in range(0, 5, gm):
+        rows = list(range(g0, min(5, g0 + gm)))
+        for nt in range(3):
+            want += [(mt, nt) for mt in rows]
+    assert order == want
+
+
 def test_argmax_plans():
     """ARGMAX lowers to chunk partials and one reduce per row block, bit-exact with the oracle
     (ragged rows and chunks; the decode head after the last layer)."""
