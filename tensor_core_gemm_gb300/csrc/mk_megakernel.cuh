@@ -865,11 +865,11 @@ __device__ __noinline__ int mma_gemv(const Params& p, uint32_t full0, uint32_t e
 // Prefill attention MMAs of one instruction: nb key blocks from ring position (st, ph). Block j:
 // S_j = Q K_j^T into TMEM S[n&1] (M = 128 query rows, N = 64 keys, K = 64 dims; the keys are a
 // K-major B operand), then, once the compute warps have written P_j (bf16, 128-byte swizzled,
-// K-major) to shared memory, O_j = P_j V_j into TMEM O[n&1] (N = 64 dims, K = 64 keys; the values
-// are an N-major B operand). S_{j+1} is issued before P_j is awaited, so the tensor pipe computes
-// the next scores while the softmax of the current block runs. A stage is released when O_j's
-// MMAs complete. `n` counts attention blocks on this SM: it gives every barrier's phase.
-// TMEM columns: S at 0 and 64, O at 128 and 192.
+// K-major) to shared memory, O += P_j V_j into the one TMEM output (N = 64 dims, K = 64 keys; the
+// values are an N-major B operand; block 0 overwrites it). S_{j+1} is issued before P_j is
+// awaited, so the tensor pipe computes the next scores while the softmax of the current block
+// runs. A stage is released when the block's P V completes. `n` counts attention blocks on this
+// SM: it gives every barrier's phase. TMEM columns: S at 0 and 64, O at 128.
 __device__ __noinline__ bool mma_attn(const Params& p, Smem& s, uint32_t st, uint32_t ph,
                                       uint32_t ns, int nb, uint32_t tmem, uint32_t& n, int idx) {
   const uint32_t ring0 = smem_u32(s.ring), units = stage_bytes(p) >> 4;
@@ -904,16 +904,15 @@ __device__ __noinline__ bool mma_attn(const Params& p, Smem& s, uint32_t st, uin
   for (int j = 0; j < nb; ++j) {
     if (j + 1 < nb && !issue_s(j + 1)) return false;
     const uint32_t nn = n0 + (uint32_t)j, b = nn & 1u;
+    // P_j is written (and any rescale of O by the compute warps is stored) before p_full
     if (!wait_warp(p, smem_u32(&s.att_p_full), nn & 1u, R_MMA, 25, idx)) return false;
-    if (!wait_warp(p, smem_u32(&s.att_o_free[b]), ((nn >> 1) & 1u) ^ 1u, R_MMA, 26, idx))
-      return false;
     tc_fence_after();
     const uint64_t so = (uint64_t)(ro.st * units);
     if (elect_one()) {
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)
-        tc_mma_f16(tmem + 128u + b * 64u, pd + (uint64_t)(kk * 2), vd + so + (uint64_t)(kk * 128),
-                   io, kk != 0);
+        tc_mma_f16(tmem + 128u, pd + (uint64_t)(kk * 2), vd + so + (uint64_t)(kk * 128), io,
+                   (j | kk) != 0);
       tc_commit(smem_u32(&s.att_o_full[b]));
       tc_commit(smem_u32(&s.empty[ro.st]));
     }
@@ -2175,46 +2174,38 @@ __device__ void attn_reduce_body(const Instr& in, const Node& nd) {
 
 // Prefill attention, compute side: thread t of the warpgroup owns query row m0 + t (TMEM lane t).
 // Per key block j: S_j from TMEM, scaled to the log2 domain and masked (key beyond the causal
-// limit of the row or beyond the instruction's key range); online softmax with running max m and
-// sum l (flash attention: a block that raises the max rescales what came before by
-// 2^(m_old - m_new)); P_j = 2^(s - m) as bf16 into shared memory for the P V MMA; the previous
-// block's P V joins the fp32 output accumulator in registers once it completes. At the end the
-// row is divided by l and stored as bf16. `n` counts attention blocks on this SM, as in the MMA
-// warp.
+// limit of the row or beyond the instruction's key range); P_j = 2^(s - m) as bf16 into shared
+// memory for the P V MMA, which accumulates the output in TMEM; l sums the unrounded P. The
+// maximum m in use only moves when a block's maximum exceeds it by more than 8 (log2 units):
+// then l and the row of O in TMEM are rescaled by 2^(m_old - m_new) (flash attention's rescale,
+// taken lazily: P stays <= 2^8, and O / l does not depend on which m was used). A warp rescales
+// its rows only when one of its lanes needs it. At the end the row of O is read once, divided by
+// l and stored as bf16. `n` counts attention blocks on this SM, as in the MMA warp.
 __device__ __noinline__ bool attn_prefill_body(const Params& p, Smem& s, const Instr& in,
                                                const Node& nd, uint32_t tmem, uint32_t& n,
                                                int idx) {
   const int ct = (int)threadIdx.x - (kThreads - kCompute);
   const int lane = ct & 31;
   const uint32_t lanes = (uint32_t)((ct >> 5) * 32) << 16;  // this warp's TMEM lane quarter
+  const uint32_t otm = tmem + 128u + lanes;                   // this warp's rows of O
   const int nb = ring_stages(in);
   const int row = in.m0 + ct;
   const int qpos = nd.pos0 + row;
   const int kmax = in.klen;
   const float sl2 = nd.scale * 1.4426950408889634f;  // scores in log2 units
   uint8_t* P = reinterpret_cast<uint8_t*>(s.xr);
-  float o[64];
-#pragma unroll
-  for (int i = 0; i < 64; ++i) o[i] = 0.f;
-  float m = -INFINITY, l = 0.f, alpha_prev = 1.f;
+  float m = -INFINITY, l = 0.f;
   const uint32_t n0 = n;
-  auto add_o = [&](uint32_t nn, float alpha) -> bool {
-    const uint32_t b = nn & 1u;
-    if (!cw_wait(p, smem_u32(&s.att_o_full[b]), (nn >> 1) & 1u, 44, idx)) return false;
+  // P V of block nn has completed: the P buffer is free and O holds blocks up to nn
+  auto o_done = [&](uint32_t nn) -> bool {
+    if (!cw_wait(p, smem_u32(&s.att_o_full[nn & 1u]), (nn >> 1) & 1u, 44, idx)) return false;
     tc_fence_after();
-    uint32_t r0[32], r1[32];
-    tmem_ld32(tmem + 128u + b * 64u + lanes, r0);
-    tmem_ld32(tmem + 128u + b * 64u + 32u + lanes, r1);
-    tmem_ld_wait();
+    return true;
+  };
+  auto o_release = [&](uint32_t nn) {
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&s.att_o_free[b]));
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      o[i] = fmaf(o[i], alpha, __uint_as_float(r0[i]));
-      o[32 + i] = fmaf(o[32 + i], alpha, __uint_as_float(r1[i]));
-    }
-    return true;
+    if (lane == 0) mbar_arrive(smem_u32(&s.att_o_free[nn & 1u]));
   };
   for (int j = 0; j < nb; ++j) {
     const uint32_t nn = n0 + (uint32_t)j, b = nn & 1u;
@@ -2239,10 +2230,10 @@ __device__ __noinline__ bool attn_prefill_body(const Params& p, Smem& s, const I
 #pragma unroll
     for (int c = 4; c < 64; ++c) mx4[c & 3] = fmaxf(mx4[c & 3], sv[c]);
     const float mj = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-    const float mn = fmaxf(m, mj);
-    const bool none = mn == -INFINITY;  // no visible key yet
-    const float alpha = none ? 1.f : ex2(m - mn);
-    const float mo = none ? 0.f : mn;   // masked scores give 2^-inf = 0 either way
+    const bool need = mj > m + 8.f;          // false while no key is visible (mj = -inf)
+    const float mn = need ? mj : m;
+    const float alpha = need ? ex2(m - mn) : 1.f;
+    const float mo = mn == -INFINITY ? 0.f : mn;  // masked scores give 2^-inf = 0 either way
     float ls4[4] = {0.f, 0.f, 0.f, 0.f};
     uint4 pk[8];
 #pragma unroll
@@ -2258,26 +2249,49 @@ __device__ __noinline__ bool attn_prefill_body(const Params& p, Smem& s, const I
     const float ls = (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
     l = fmaf(l, alpha, ls);
     m = mn;
-    // The previous block's P V (weighted with the previous maximum) joins the accumulator; after
-    // it completes the P buffer may be overwritten.
-    if (j > 0 && !add_o(nn - 1u, alpha_prev)) return false;
-    alpha_prev = alpha;
+    if (j > 0) {
+      if (!o_done(nn - 1u)) return false;
+      if (__any_sync(FULL, need)) {  // rescale this warp's rows of O (alpha = 1 where not needed)
+        uint32_t o0[32], o1[32];
+        tmem_ld32(otm, o0);
+        tmem_ld32(otm + 32u, o1);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          o0[i] = __float_as_uint(__uint_as_float(o0[i]) * alpha);
+          o1[i] = __float_as_uint(__uint_as_float(o1[i]) * alpha);
+        }
+        tmem_st32(otm, o0);
+        tmem_st32(otm + 32u, o1);
+        tmem_st_wait();
+      }
+      o_release(nn - 1u);
+    }
 #pragma unroll
     for (int ch = 0; ch < 8; ++ch)
       *reinterpret_cast<uint4*>(P + ct * 128 + ((ch ^ (ct & 7)) << 4)) = pk[ch];
     fence_proxy_async_shared();
+    tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&s.att_p_full));
   }
-  if (nb > 0 && !add_o(n0 + (uint32_t)nb - 1u, alpha_prev)) return false;
   n = n0 + (uint32_t)nb;
+  if (nb == 0) return true;
+  const uint32_t nl = n0 + (uint32_t)nb - 1u;
+  if (!o_done(nl)) return false;
+  uint32_t o0[32], o1[32];
+  tmem_ld32(otm, o0);
+  tmem_ld32(otm + 32u, o1);
+  tmem_ld_wait();
+  o_release(nl);
   if (row < nd.M) {
     const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
     for (int ch = 0; ch < 8; ++ch) {
       float v[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) v[e] = o[ch * 8 + e] * inv;
+      for (int e = 0; e < 8; ++e)
+        v[e] = __uint_as_float(ch < 4 ? o0[ch * 8 + e] : o1[ch * 8 - 32 + e]) * inv;
       store8(nd.out, row, in.n0 * 64 + ch * 8, DT_BF16, v);
     }
   }
