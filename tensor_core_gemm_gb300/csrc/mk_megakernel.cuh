@@ -2220,16 +2220,20 @@ __device__ __noinline__ bool attn_prefill_body(const Params& p, Smem& s, const I
     if (lane == 0) mbar_arrive(smem_u32(&s.att_s_free[b]));
     const int key0 = j * kAttnKeyBlock;
     const int lim = nd.causal ? min(kmax, qpos + 1) : kmax;  // keys [0, lim) are visible
-    float sv[64];
+    // raw scores; masked keys only in a block that reaches the row's limit
+    float x[64];
 #pragma unroll
-    for (int c = 0; c < 64; ++c) {
-      const float x = __uint_as_float(c < 32 ? r0[c] : r1[c - 32]) * sl2;
-      sv[c] = key0 + c < lim ? x : -INFINITY;
+    for (int c = 0; c < 64; ++c) x[c] = __uint_as_float(c < 32 ? r0[c] : r1[c - 32]);
+    if (key0 + 64 > lim) {
+#pragma unroll
+      for (int c = 0; c < 64; ++c)
+        if (key0 + c >= lim) x[c] = -INFINITY;
     }
-    float mx4[4] = {sv[0], sv[1], sv[2], sv[3]};
+    float mx4[4] = {x[0], x[1], x[2], x[3]};
 #pragma unroll
-    for (int c = 4; c < 64; ++c) mx4[c & 3] = fmaxf(mx4[c & 3], sv[c]);
-    const float mj = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+    for (int c = 4; c < 64; ++c) mx4[c & 3] = fmaxf(mx4[c & 3], x[c]);
+    // the scale is positive: the maximum of the scaled scores is the scaled maximum
+    const float mj = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * sl2;
     const bool need = mj > m + 8.f;          // false while no key is visible (mj = -inf)
     const float mn = need ? mj : m;
     const float alpha = need ? ex2(m - mn) : 1.f;
@@ -2241,10 +2245,16 @@ __device__ __noinline__ bool attn_prefill_body(const Params& p, Smem& s, const I
       float pv[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        pv[e] = ex2(sv[ch * 8 + e] - mo);
+        pv[e] = ex2(fmaf(x[ch * 8 + e], sl2, -mo));
         ls4[e & 3] += pv[e];
       }
-      pk[ch] = pack8(pv, DT_BF16);
+      uint32_t w[4];
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const __nv_bfloat162 t = __floats2bfloat162_rn(pv[2 * h], pv[2 * h + 1]);
+        w[h] = *reinterpret_cast<const uint32_t*>(&t);
+      }
+      pk[ch] = make_uint4(w[0], w[1], w[2], w[3]);
     }
     const float ls = (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
     l = fmaf(l, alpha, ls);
