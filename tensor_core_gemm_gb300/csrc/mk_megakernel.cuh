@@ -2196,9 +2196,13 @@ __device__ __noinline__ bool attn_prefill_body(const Params& p, Smem& s, const I
   uint8_t* P = reinterpret_cast<uint8_t*>(s.xr);
   float m = -INFINITY, l = 0.f;
   const uint32_t n0 = n;
+  // Every barrier here takes one arrival per warp and nothing in the body synchronises the
+  // warpgroup, so each warp waits on its own (bounded): warps do not run in lockstep, and one
+  // whose wait gives up returns while the others' waits end by the same limit.
   // P V of block nn has completed: the P buffer is free and O holds blocks up to nn
   auto o_done = [&](uint32_t nn) -> bool {
-    if (!cw_wait(p, smem_u32(&s.att_o_full[nn & 1u]), (nn >> 1) & 1u, 44, idx)) return false;
+    if (!wait_warp(p, smem_u32(&s.att_o_full[nn & 1u]), (nn >> 1) & 1u, R_COMPUTE, 44, idx))
+      return false;
     tc_fence_after();
     return true;
   };
@@ -2209,7 +2213,8 @@ __device__ __noinline__ bool attn_prefill_body(const Params& p, Smem& s, const I
   };
   for (int j = 0; j < nb; ++j) {
     const uint32_t nn = n0 + (uint32_t)j, b = nn & 1u;
-    if (!cw_wait(p, smem_u32(&s.att_s_full[b]), (nn >> 1) & 1u, 43, idx)) return false;
+    if (!wait_warp(p, smem_u32(&s.att_s_full[b]), (nn >> 1) & 1u, R_COMPUTE, 43, idx))
+      return false;
     tc_fence_after();
     uint32_t r0[32], r1[32];
     tmem_ld32(tmem + b * 64u + lanes, r0);
@@ -2365,6 +2370,7 @@ __device__ void run_compute(const Params& p, Smem& s, uint32_t tmem) {
           // inputs reach this warpgroup only through the loader and the MMAs, which wait
           trace_mark(p, idx, 2);
           ok = attn_prefill_body(p, s, in, nd, tmem, att_n, idx);
+          ok = bar_and(kBarCompute, kCompute, ok);  // its warps waited on their own
           ring += (uint32_t)ring_stages(in);
         }
         break;
