@@ -201,6 +201,9 @@ typedef struct {
   int32_t gemm_group_m;  /* GEMM tile order: groups of this many row tiles, column by column
                             inside a group (L2 reuse of the B and A panels of a wave);
                             1: row-major. Default 8 */
+  int32_t wave_pack;     /* 1 (default): consecutive independent GEMM nodes are placed as one
+                            run, tiles longest K first on the least loaded SM (or CTA pair),
+                            padded with Noops; 0: each node's tiles in order */
 } mk_compile_opts;
 
 /* Fill *o with the defaults (the values listed above for each field). */

@@ -73,6 +73,13 @@ Lowering rules per node (tile sizes come from ``opts``; see ``DEFAULT_OPTS``):
       rows, q head h), t descending (longest first), then h ascending; reads q rows of the tile,
       k and v rows [0, kmax) with kmax = min(Tk, q_pos0 + end of tile) when causal.
 
+Wave packing (wave_pack = 1, default): a run of two or more consecutive GEMM phases without
+split tails, none reading a region that an earlier phase of the run writes (bounding boxes per
+tensor), becomes one phase. Its cluster groups (a tile's instructions) are stably sorted by cost
+= klen × number of B operands, longest first; each goes to the unit (n_sm div cluster units)
+with the least cost so far, the lowest on ties; row r of the run then holds every unit's r-th
+group in unit order, Noop groups where a unit has none, trailing Noops dropped.
+
 Flags: B_DEP marks a GEMM, GEMV or attention-partial instruction whose streamed operand (the
 weight, or the key/value chunk) has a producer inside the graph, so it cannot be prefetched.
 
@@ -96,7 +103,7 @@ DEFAULT_OPTS = dict(
     ew_rows=128, ew_cols=128, ew_tiles=1,
     norm_rows=16,
     gemv_max_m=8, gemv_tile_n=256, gemv_splits=0, gemv_kstep=64,
-    attn_chunk=64, attn_tile_q=128, argmax_chunk=4096, gemm_group_m=8,
+    attn_chunk=64, attn_tile_q=128, argmax_chunk=4096, gemm_group_m=8, wave_pack=1,
 )
 
 
@@ -278,6 +285,89 @@ def _lower_rows(ni, nd, opts, phases, op):
     phases.append(out)
 
 
+def _bounds(ph, reads):
+    """Bounding box per tensor of a phase's read (or write) boxes."""
+    bb = {}
+    for ins in ph:
+        boxes = [b for b, _ in ins.reads] if reads else ins.writes
+        for (t, r0, r1, c0, c1) in boxes:
+            if r0 >= r1 or c0 >= c1:
+                continue
+            if t in bb:
+                u = bb[t]
+                bb[t] = (t, min(u[1], r0), max(u[2], r1), min(u[3], c0), max(u[4], c1))
+            else:
+                bb[t] = (t, r0, r1, c0, c1)
+    return bb
+
+
+def _meets(a, b):
+    return (a[0] == b[0] and a[1] < a[2] and a[3] < a[4] and b[1] < b[2] and b[3] < b[4]
+            and a[1] < b[2] and b[1] < a[2] and a[3] < b[4] and b[3] < a[4])
+
+
+def _pack_waves(phases, o):
+    cl = o["cluster"]
+    units = o["n_sm"] // cl
+    if units <= 0:
+        return phases
+
+    def gemm_phase(ph):
+        return (len(ph) > 0 and len(ph) % cl == 0
+                and all(i.op == OP_GEMM and i.aux1 == 0 for i in ph))
+
+    out, i = [], 0
+    while i < len(phases):
+        if not gemm_phase(phases[i]):
+            out.append(phases[i])
+            i += 1
+            continue
+        j = i + 1
+        written = _bounds(phases[i], False)
+        while j < len(phases) and gemm_phase(phases[j]):
+            if any(t in written and _meets(written[t], b)
+                   for t, b in _bounds(phases[j], True).items()):
+                break
+            for t, b in _bounds(phases[j], False).items():
+                if t in written:
+                    u = written[t]
+                    written[t] = (t, min(u[1], b[1]), max(u[2], b[2]), min(u[3], b[3]),
+                                  max(u[4], b[4]))
+                else:
+                    written[t] = b
+            j += 1
+        if j - i < 2:
+            out.append(phases[i])
+            i += 1
+            continue
+        groups, cost = [], []
+        for ph in phases[i:j]:
+            for g in range(0, len(ph), cl):
+                grp = ph[g:g + cl]
+                groups.append(grp)
+                cost.append(grp[0].klen * sum(1 for _, role in grp[0].reads if role == ROLE_B))
+        order = sorted(range(len(groups)), key=lambda g: -cost[g])   # stable
+        load = [0] * units
+        queue = [[] for _ in range(units)]
+        for g in order:
+            u = min(range(units), key=lambda v: (load[v], v))
+            load[u] += cost[g]
+            queue[u].append(g)
+        rows = max(len(q) for q in queue)
+        run = []
+        for r in range(rows):
+            for u in range(units):
+                if r < len(queue[u]):
+                    run.extend(groups[queue[u][r]])
+                else:
+                    run.extend(Instr(OP_NOOP, 0) for _ in range(cl))
+        while run and run[-1].op == OP_NOOP:
+            run.pop()
+        out.append(run)
+        i = j
+    return out
+
+
 def _lower_argmax(ni, nd, opts, phases, tensors):
     x, o = nd["x"], nd["out"]
     rows, cols = x[3], x[4]
@@ -426,6 +516,9 @@ def lower(graph, opts):
             _lower_argmax(ni, nd, o, phases, tensors)
         else:
             raise ValueError(kind)
+
+    if o["wave_pack"]:
+        phases = _pack_waves(phases, o)
 
     # Phase 1: contiguous ranges, each rounded up to the cluster size with Noops.
     instrs, phase_of, ranges = [], [], []

@@ -42,7 +42,8 @@ class CompileOpts(C.Structure):
         "norm_rows", "gemv_max_m", "gemv_tile_n", "gemv_splits", "gemv_kstep", "attn_chunk",
         "attn_tile_q", "dry_run", "timeout_ms", "device", "debug_counter", "debug_extra",
         "snapshot_counters", "trace", "l2_prefetch", "gemm_split_tail", "fuse_rope",
-        "fuse_attn_reduce", "kernel_set", "gemv_pack", "argmax_chunk", "gemm_group_m")]
+        "fuse_attn_reduce", "kernel_set", "gemv_pack", "argmax_chunk", "gemm_group_m",
+        "wave_pack")]
 
 
 class HostCopy(C.Structure):

@@ -345,6 +345,122 @@ static void lower_attention(std::vector<TensorRec>& ts, int ni, const NodeRec& n
   }
 }
 
+// Wave packing. A run of consecutive GEMM phases (no split tails) none of which reads what an
+// earlier phase of the run writes is placed as one phase: its cluster groups (the `cluster`
+// instructions of a tile), stably sorted by cost (K length x B operands) longest first, each go
+// to the unit (CTA, or CTA pair) with the least cost so far (the lowest unit on ties), and the
+// run is laid out row by row, row r holding every unit's r-th group in unit order (Noops where a
+// unit has none; trailing Noops dropped), so that with instruction i on SM i mod n_sm every
+// group runs on its unit. Equal costs reproduce the tiles' own order.
+static void pack_waves(std::vector<std::vector<HInstr>>& phases, const mk_compile_opts& o) {
+  const int cl = o.cluster, units = o.n_sm / cl;
+  if (units <= 0) return;
+  auto gemm_phase = [&](const std::vector<HInstr>& ph) {
+    if (ph.empty() || ph.size() % cl) return false;
+    for (const HInstr& h : ph)
+      if (h.rec.op != OP_GEMM || h.rec.aux1 != 0) return false;
+    return true;
+  };
+  // bounding boxes of a phase's reads and writes, per base tensor
+  auto bounds = [](const std::vector<HInstr>& ph, bool reads) {
+    std::map<int, Box> bb;
+    for (const HInstr& h : ph) {
+      std::vector<Box> boxes;
+      if (reads)
+        for (const auto& r : h.reads) boxes.push_back(r.first);
+      else
+        boxes = h.writes;
+      for (const Box& b : boxes) {
+        if (b.empty()) continue;
+        auto it = bb.find(b.t);
+        if (it == bb.end()) {
+          bb[b.t] = b;
+        } else {
+          Box& u = it->second;
+          u.r0 = std::min(u.r0, b.r0);
+          u.r1 = std::max(u.r1, b.r1);
+          u.c0 = std::min(u.c0, b.c0);
+          u.c1 = std::max(u.c1, b.c1);
+        }
+      }
+    }
+    return bb;
+  };
+  std::vector<std::vector<HInstr>> out;
+  size_t i = 0;
+  while (i < phases.size()) {
+    if (!gemm_phase(phases[i])) {
+      out.push_back(std::move(phases[i++]));
+      continue;
+    }
+    size_t j = i + 1;
+    std::map<int, Box> written = bounds(phases[i], false);
+    while (j < phases.size() && gemm_phase(phases[j])) {
+      bool dep = false;
+      for (const auto& r : bounds(phases[j], true)) {
+        auto w = written.find(r.first);
+        if (w != written.end() && meets(w->second, r.second)) dep = true;
+      }
+      if (dep) break;
+      for (const auto& w : bounds(phases[j], false)) {
+        auto it = written.find(w.first);
+        if (it == written.end()) {
+          written[w.first] = w.second;
+        } else {
+          Box& u = it->second;
+          u.r0 = std::min(u.r0, w.second.r0);
+          u.r1 = std::max(u.r1, w.second.r1);
+          u.c0 = std::min(u.c0, w.second.c0);
+          u.c1 = std::max(u.c1, w.second.c1);
+        }
+      }
+      ++j;
+    }
+    if (j - i < 2) {
+      out.push_back(std::move(phases[i++]));
+      continue;
+    }
+    std::vector<std::vector<HInstr>> groups;
+    std::vector<int64_t> cost;
+    for (size_t q = i; q < j; ++q)
+      for (size_t g = 0; g < phases[q].size(); g += cl) {
+        groups.emplace_back();
+        for (int r = 0; r < cl; ++r) groups.back().push_back(std::move(phases[q][g + r]));
+        int nb = 0;
+        for (const auto& rd : groups.back()[0].reads) nb += rd.second == ROLE_B;
+        cost.push_back((int64_t)groups.back()[0].rec.klen * nb);
+      }
+    std::vector<size_t> order(groups.size());
+    for (size_t g = 0; g < order.size(); ++g) order[g] = g;
+    std::stable_sort(order.begin(), order.end(),
+                     [&](size_t a, size_t b) { return cost[a] > cost[b]; });
+    std::vector<int64_t> load(units, 0);
+    std::vector<std::vector<size_t>> queue(units);
+    for (size_t g : order) {
+      int u = 0;
+      for (int v = 1; v < units; ++v)
+        if (load[v] < load[u]) u = v;
+      load[u] += cost[g];
+      queue[u].push_back(g);
+    }
+    size_t rows = 0;
+    for (const auto& q : queue) rows = std::max(rows, q.size());
+    std::vector<HInstr> run;
+    for (size_t r = 0; r < rows; ++r)
+      for (int u = 0; u < units; ++u) {
+        if (r < queue[u].size()) {
+          for (auto& h : groups[queue[u][r]]) run.push_back(std::move(h));
+        } else {
+          for (int k = 0; k < cl; ++k) run.push_back(make(OP_NOOP, 0));
+        }
+      }
+    while (!run.empty() && run.back().rec.op == OP_NOOP) run.pop_back();
+    out.push_back(std::move(run));
+    i = j;
+  }
+  phases = std::move(out);
+}
+
 mk_status lower_graph(const std::vector<TensorRec>& tensors_in, const std::vector<NodeRec>& nodes,
                       const mk_compile_opts& o, HostPlan* plan) {
   if (o.n_sm <= 0 || o.cluster <= 0 || o.gemm_tile_m <= 0 || o.gemm_tile_n <= 0 ||
@@ -388,6 +504,8 @@ mk_status lower_graph(const std::vector<TensorRec>& tensors_in, const std::vecto
       default: set_error("mk_compile: unknown node kind %d", nd.kind); return MK_ERR_INVALID_ARG;
     }
   }
+
+  if (o.wave_pack) pack_waves(phases, o);
 
   // Phase 1: flatten, padding every phase to a multiple of the cluster size with Noops.
   std::vector<HInstr> ins;
@@ -815,6 +933,7 @@ extern "C" mk_status mk_default_opts(mk_compile_opts* o) {
   o->attn_chunk = 64;
   o->argmax_chunk = 4096;
   o->gemm_group_m = 8;
+  o->wave_pack = 1;
   o->attn_tile_q = 128;
   o->dry_run = 0;
   o->timeout_ms = 2000;

@@ -204,6 +204,35 @@ def test_grouped_gemm_tile_order(gm):
     assert order == want
 
 
+def test_wave_packing_of_independent_gemms():
+    """Independent GEMM nodes are placed as one run, longest K first on the least loaded CTA
+    pair: the same tiles as without packing, each pair's total K within the longest-first bound
+    (average + one tile), the list mirrored bit for bit by the oracle; equal costs keep the
+    order."""
+    desc = workloads.gemm_list(workloads.LLAMA70B_DECODE).desc
+    opts = dict(n_sm=152, gemm_tile_m=256, cluster=2)
+    packed, _ = assert_same_plan(desc, dict(opts, wave_pack=1))
+    plain, _ = assert_same_plan(desc, dict(opts, wave_pack=0))
+    tiles = lambda py: sorted(i.key() for i in py.instrs if i.op == osched.OP_GEMM)
+    assert tiles(packed) == tiles(plain)
+    load = {}
+    for idx, ins in enumerate(packed.instrs):
+        if ins.op == osched.OP_GEMM and ins.aux0 == 0:
+            load[(idx % 152) // 2] = load.get((idx % 152) // 2, 0) + ins.klen
+    loads = [load.get(u, 0) for u in range(76)]
+    assert max(loads) <= sum(loads) / 76 + 28672
+    plain_load = {}
+    for idx, ins in enumerate(plain.instrs):
+        if ins.op == osched.OP_GEMM and ins.aux0 == 0:
+            plain_load[(idx % 152) // 2] = plain_load.get((idx % 152) // 2, 0) + ins.klen
+    assert max(loads) < max(plain_load.values())
+    # equal K everywhere: the packed list is the plain one
+    pre = workloads.gemm_list(workloads.LLAMA70B_PREFILL).desc
+    a, _ = assert_same_plan(pre, dict(opts, wave_pack=1))
+    b, _ = assert_same_plan(pre, dict(opts, wave_pack=0))
+    assert [i.key() for i in a.instrs] == [i.key() for i in b.instrs]
+
+
 def test_argmax_plans():
     """ARGMAX lowers to chunk partials and one reduce per row block, bit-exact with the oracle
     (ragged rows and chunks; the decode head after the last layer)."""
