@@ -153,7 +153,8 @@ static void lower_matmul(const std::vector<TensorRec>& ts, int ni, const NodeRec
     const int64_t n_ranges = n_split >= 2 ? cdiv(k, chunk) : 1;
     int slots = 0;
     // Tile order: groups of gemm_group_m row tiles, column-major inside a group (consecutive
-    // tiles share B panels and a group's A panels stay in L2); 1 = row-major.
+    // tiles share B panels and a group's A panels stay in L2; "Hand-writing a Blackwell GEMM",
+    // Experiments, "Threadblock swizzle"); 1 = row-major.
     const int64_t nmt = cdiv(m, tm), gm = std::max(1, o.gemm_group_m);
     for (int64_t t = 0; t < t_all; ++t) {
       const int64_t g = t / (gm * nnt), r = t % (gm * nnt);
