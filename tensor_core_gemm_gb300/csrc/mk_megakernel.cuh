@@ -8,16 +8,19 @@
 //   warp 0      scheduler: publishes instruction descriptors into an 8-slot ring ahead of the
 //               roles and polls the global dependency counters of the oldest published one
 //               ("MegaKittens Internals" §09 controller; §11 barrier wait with acquire).
-//   warp 1      TMA loader: streams operand tiles into a 4-stage shared-memory ring; weight (B)
-//               tiles of an instruction are issued before its activations are ready ("Beating
-//               torch.compile with Megakernels", "TMA Compute Overlap"; MegaKittens §00).
-//   warp 2      MMA issuer: tcgen05.mma into a double-buffered TMEM accumulator ("Hand-writing a
-//               Blackwell GEMM", steps 3 and 8: warp specialisation, persistent kernel with two
-//               accumulator slots).
+//   warp 1      TMA loader: streams operand tiles into a shared-memory ring (4 stages of 48 KB,
+//               or 6 of 32 KB); weight (B) tiles of an instruction are issued before its
+//               activations are ready ("Beating torch.compile with Megakernels", "TMA Compute
+//               Overlap"; MegaKittens §00); packed GEMV weights move as one bulk copy per stage.
+//   warp 2      MMA issuer: tcgen05.mma into TMEM: GEMM tiles into a double-buffered accumulator
+//               ("Hand-writing a Blackwell GEMM", steps 3 and 8: warp specialisation, persistent
+//               kernel with two accumulator slots), GEMV tiles with swapped operands, and the
+//               S = QK^T and O += PV products of prefill attention.
 //   warp 3      spare.
-//   warps 4-7   compute warpgroup: GEMM epilogue (TMEM -> registers -> fused epilogue -> global),
-//               GEMV tiles, elementwise / RMSNorm / RoPE rows, split-KV attention partial and
-//               combine; publishes finished tiles on the global counters (release).
+//   warps 4-7   compute warpgroup: GEMM epilogue (TMEM -> registers -> fused epilogue -> TMA
+//               store), GEMV activation staging and split-K epilogue, elementwise / RMSNorm /
+//               RoPE / ARGMAX rows, split-KV attention partial and combine, prefill attention
+//               softmax; publishes finished tiles on the global counters (release).
 // Every wait is bounded: past `timeout_ns` the waiter records MK_ERR_TIMEOUT in the status word,
 // every role drains what it has in flight and the CTA exits normally.
 #pragma once
