@@ -73,12 +73,13 @@ Lowering rules per node (tile sizes come from ``opts``; see ``DEFAULT_OPTS``):
       rows, q head h), t descending (longest first), then h ascending; reads q rows of the tile,
       k and v rows [0, kmax) with kmax = min(Tk, q_pos0 + end of tile) when causal.
 
-Wave packing (wave_pack = 1, default): a run of two or more consecutive GEMM phases without
-split tails, none reading a region that an earlier phase of the run writes (bounding boxes per
-tensor), becomes one phase. Its cluster groups (a tile's instructions) are stably sorted by cost
-= klen × number of B operands, longest first; each goes to the unit (n_sm div cluster units)
-with the least cost so far, the lowest on ties; row r of the run then holds every unit's r-th
-group in unit order, Noop groups where a unit has none, trailing Noops dropped.
+Wave packing (wave_pack = 1, default): a run of consecutive phases of one kind, none reading a
+region that an earlier phase of the run writes (bounding boxes per tensor), becomes one phase:
+GEMM phases without split tails (runs of two or more; cost = klen × number of B operands) or
+prefill attention phases (runs of one or more; cost = klen). Its cluster groups (a tile's
+instructions) are stably sorted by cost, longest first; each goes to the unit (n_sm div cluster
+units) with the least cost so far, the lowest on ties; row r of the run then holds every unit's
+r-th group in unit order, Noop groups where a unit has none, trailing Noops dropped.
 
 Flags: B_DEP marks a GEMM, GEMV or attention-partial instruction whose streamed operand (the
 weight, or the key/value chunk) has a producer inside the graph, so it cannot be prefetched.
@@ -312,19 +313,25 @@ def _pack_waves(phases, o):
     if units <= 0:
         return phases
 
-    def gemm_phase(ph):
-        return (len(ph) > 0 and len(ph) % cl == 0
-                and all(i.op == OP_GEMM and i.aux1 == 0 for i in ph))
+    def kind(ph):
+        if len(ph) == 0 or len(ph) % cl:
+            return 0
+        if all(i.op == OP_GEMM and i.aux1 == 0 for i in ph):
+            return 1
+        if all(i.op == OP_ATTN_PREFILL for i in ph):
+            return 2
+        return 0
 
     out, i = [], 0
     while i < len(phases):
-        if not gemm_phase(phases[i]):
+        k0 = kind(phases[i])
+        if k0 == 0:
             out.append(phases[i])
             i += 1
             continue
         j = i + 1
         written = _bounds(phases[i], False)
-        while j < len(phases) and gemm_phase(phases[j]):
+        while j < len(phases) and kind(phases[j]) == k0:
             if any(t in written and _meets(written[t], b)
                    for t, b in _bounds(phases[j], True).items()):
                 break
@@ -336,7 +343,7 @@ def _pack_waves(phases, o):
                 else:
                     written[t] = b
             j += 1
-        if j - i < 2:
+        if k0 == 1 and j - i < 2:
             out.append(phases[i])
             i += 1
             continue
@@ -345,7 +352,8 @@ def _pack_waves(phases, o):
             for g in range(0, len(ph), cl):
                 grp = ph[g:g + cl]
                 groups.append(grp)
-                cost.append(grp[0].klen * sum(1 for _, role in grp[0].reads if role == ROLE_B))
+                nb = sum(1 for _, role in grp[0].reads if role == ROLE_B)
+                cost.append(grp[0].klen * (nb if k0 == 1 else 1))
         order = sorted(range(len(groups)), key=lambda g: -cost[g])   # stable
         load = [0] * units
         queue = [[] for _ in range(units)]

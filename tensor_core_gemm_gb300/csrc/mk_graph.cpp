@@ -346,21 +346,26 @@ static void lower_attention(std::vector<TensorRec>& ts, int ni, const NodeRec& n
   }
 }
 
-// Wave packing. A run of consecutive GEMM phases (no split tails) none of which reads what an
-// earlier phase of the run writes is placed as one phase: its cluster groups (the `cluster`
-// instructions of a tile), stably sorted by cost (K length x B operands) longest first, each go
-// to the unit (CTA, or CTA pair) with the least cost so far (the lowest unit on ties), and the
-// run is laid out row by row, row r holding every unit's r-th group in unit order (Noops where a
-// unit has none; trailing Noops dropped), so that with instruction i on SM i mod n_sm every
-// group runs on its unit. Equal costs reproduce the tiles' own order.
+// Wave packing. A run of consecutive phases of one kind, none reading what an earlier phase of
+// the run writes, is placed as one phase: GEMM phases without split tails (runs of two or more;
+// cost of a tile = K length x B operands) or causal prefill attention phases (runs of one or
+// more; cost = keys). Its cluster groups (the `cluster` instructions of a tile), stably sorted by
+// cost longest first, each go to the unit (CTA, or CTA pair) with the least cost so far (the
+// lowest unit on ties), and the run is laid out row by row, row r holding every unit's r-th group
+// in unit order (Noops where a unit has none; trailing Noops dropped), so that with instruction i
+// on SM i mod n_sm every group runs on its unit. Equal costs reproduce the tiles' own order.
 static void pack_waves(std::vector<std::vector<HInstr>>& phases, const mk_compile_opts& o) {
   const int cl = o.cluster, units = o.n_sm / cl;
   if (units <= 0) return;
-  auto gemm_phase = [&](const std::vector<HInstr>& ph) {
-    if (ph.empty() || ph.size() % cl) return false;
-    for (const HInstr& h : ph)
-      if (h.rec.op != OP_GEMM || h.rec.aux1 != 0) return false;
-    return true;
+  // 1: GEMM phase, 2: prefill attention phase, 0: neither
+  auto kind = [&](const std::vector<HInstr>& ph) {
+    if (ph.empty() || ph.size() % cl) return 0;
+    bool gemm = true, attn = true;
+    for (const HInstr& h : ph) {
+      gemm = gemm && h.rec.op == OP_GEMM && h.rec.aux1 == 0;
+      attn = attn && h.rec.op == OP_ATTN_PREFILL;
+    }
+    return gemm ? 1 : attn ? 2 : 0;
   };
   // bounding boxes of a phase's reads and writes, per base tensor
   auto bounds = [](const std::vector<HInstr>& ph, bool reads) {
@@ -390,13 +395,14 @@ static void pack_waves(std::vector<std::vector<HInstr>>& phases, const mk_compil
   std::vector<std::vector<HInstr>> out;
   size_t i = 0;
   while (i < phases.size()) {
-    if (!gemm_phase(phases[i])) {
+    const int k0 = kind(phases[i]);
+    if (k0 == 0) {
       out.push_back(std::move(phases[i++]));
       continue;
     }
     size_t j = i + 1;
     std::map<int, Box> written = bounds(phases[i], false);
-    while (j < phases.size() && gemm_phase(phases[j])) {
+    while (j < phases.size() && kind(phases[j]) == k0) {
       bool dep = false;
       for (const auto& r : bounds(phases[j], true)) {
         auto w = written.find(r.first);
@@ -417,7 +423,7 @@ static void pack_waves(std::vector<std::vector<HInstr>>& phases, const mk_compil
       }
       ++j;
     }
-    if (j - i < 2) {
+    if (k0 == 1 && j - i < 2) {
       out.push_back(std::move(phases[i++]));
       continue;
     }
@@ -429,7 +435,7 @@ static void pack_waves(std::vector<std::vector<HInstr>>& phases, const mk_compil
         for (int r = 0; r < cl; ++r) groups.back().push_back(std::move(phases[q][g + r]));
         int nb = 0;
         for (const auto& rd : groups.back()[0].reads) nb += rd.second == ROLE_B;
-        cost.push_back((int64_t)groups.back()[0].rec.klen * nb);
+        cost.push_back((int64_t)groups.back()[0].rec.klen * (k0 == 1 ? nb : 1));
       }
     std::vector<size_t> order(groups.size());
     for (size_t g = 0; g < order.size(); ++g) order[g] = g;
