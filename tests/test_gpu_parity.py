@@ -850,3 +850,35 @@ def test_decode_greedy_sampling_head():
     top = np.sort(logits_ref[0])[-2:]
     if top[1] - top[0] > 2e-2 * max(1.0, abs(top[1])):
         assert token == int(token_ref[0, 0])
+
+
+# ------------------------------------------------------------------ Llama-70B GEMM lists
+
+@pytest.mark.parametrize("which", ["prefill", "decode"])
+def test_llama_gemm_lists_full_size_sampled_rows(which):
+    """The Llama-70B linear lists at full size in the benchmark's launch configuration (CTA
+    pairs, grouped tile order, wave packing): 64 seeded rows of every GEMM against the oracle."""
+    shapes = workloads.LLAMA70B_PREFILL if which == "prefill" else workloads.LLAMA70B_DECODE
+    wl = workloads.gemm_list(shapes, device=DEV, seed=0)
+    opts = dict(gemm_tile_m=256, cluster=2)
+    plan, _ = run(wl, **opts)
+    check_counters(plan, wl, opts)
+    gen = torch.Generator().manual_seed(11)
+    for (a, b, c, m, n, k) in wl.info["gemms"]:
+        rows = np.sort(torch.randperm(m, generator=gen)[:64].numpy())
+        idx = torch.as_tensor(rows, device=DEV)
+        ref = ops.matmul(f32(wl.data[a][idx]), f32(wl.data[b]), F16)
+        assert_close(f32(wl.data[c][idx]), ref, f"{which} {m}x{n}x{k}")
+
+
+def test_tile_order_and_wave_packing_bit_identical():
+    """Grouped tile order and wave packing only move tiles between SMs: the outputs of a list of
+    independent GEMMs with different K agree bit for bit with row-major, unpacked placement."""
+    shapes = [(256, 1024, 512), (300, 768, 2048), (256, 512, 3072), (512, 1280, 1024)]
+    outs = []
+    for opts in (dict(), dict(wave_pack=0, gemm_group_m=1)):
+        wl = workloads.gemm_list(shapes, device=DEV, seed=3)
+        run(wl, gemm_tile_m=256, cluster=2, **opts)
+        outs.append([wl.data[c].clone() for (_, _, c, _, _, _) in wl.info["gemms"]])
+    for x, y in zip(*outs):
+        assert torch.equal(x.view(torch.int16), y.view(torch.int16))
