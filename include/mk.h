@@ -73,6 +73,17 @@ mk_status mk_graph_destroy(mk_graph_t g);
 mk_status mk_add_tensor(mk_graph_t g, void* dev_ptr, int32_t dtype, int32_t rank,
                         const int64_t* shape, const int64_t* strides, int32_t* tensor_id);
 
+/* A plan-owned intermediate of rows x cols elements (no caller memory; rows start 16-byte
+ * aligned). mk_compile places transients in the plan's buffer pool, where one whose accesses are
+ * all finished a wave of instructions earlier (every node touching it ends at least n_sm
+ * instructions before the next writer starts) hands its memory to a later transient of the same
+ * shape and dtype; a reuse counter orders the new writes after the old accesses. Exactly one
+ * node may write a transient (through any of its views), and every node reading it comes later.
+ * mk_plan_tensor_ptr gives its device address once the plan exists; its contents are defined
+ * until its buffer is reused by a later node of the same run. */
+mk_status mk_add_transient(mk_graph_t g, int32_t dtype, int64_t rows, int64_t cols,
+                           int32_t* tensor_id);
+
 /* A rows x cols window of a registered tensor starting at (r0, c0) of its 2-D view; used to
  * name a layer of stacked weights, a slice of columns (q | k | v), a cache row, ... */
 mk_status mk_add_view(mk_graph_t g, int32_t base, int64_t r0, int64_t c0, int64_t rows,
@@ -243,6 +254,10 @@ typedef struct {
   int32_t where;      /* wait site id (kernel-internal) */
 } mk_device_status;
 
+/* Device address of a registered tensor (a transient's place in the buffer pool included) in
+ * plan p; *ptr = NULL for a dry-run plan's transients. */
+mk_status mk_plan_tensor_ptr(mk_plan_t p, int32_t tensor, void** ptr);
+
 /* Re-read every weight the plan holds a packed copy of (gemv_pack = 1) into that copy, on
  * `stream` (ordered before later work on it). Needed after a change to such a weight made
  * outside mk_run_host; without it mk_run keeps using the weight as it was when packed. */
@@ -293,6 +308,8 @@ typedef struct {
   int64_t kernel_set;    /* specialisation mk_run launches: 0 general, 1 GEMM tiles only,
                             2 decode, 3 prefill */
   int64_t packed_bytes;  /* device bytes of packed GEMV weight copies (gemv_pack) */
+  int64_t pool_bytes;    /* device bytes of the transient buffer pool */
+  int64_t n_reuse;       /* transients placed in a buffer an earlier transient used */
 } mk_stats;
 
 mk_status mk_plan_stats(mk_plan_t p, mk_stats* s);

@@ -5,15 +5,15 @@ It follows the scheduler of "MegaKittens Internals" §04: phase 1 (count and pla
 gets a contiguous range, rounded up to the cluster size with Noops), phase 3 (fine-grained
 barriers: a consumer's dependency set is the set of producer instructions whose write boxes
 meet its read boxes; every distinct (producer, set) pair is one counter whose target is the set
-size), and §05 (instruction i runs on SM i mod S in iteration i div S). Phase 2's buffer pool is
-not part of this graph model: every buffer is caller-owned and no node may write a region an
-earlier node reads or writes.
+size), phase 2 (the buffer pool, for tensors marked "transient": see ``_pool``), and §05
+(instruction i runs on SM i mod S in iteration i div S). Every other buffer is caller-owned, and
+no node may write a region an earlier node reads or writes.
 
 Unlike the page, which finds the sets through per-edge GCD unit cells, this module intersects
 every read box with every write box of the earlier phases (brute force).
 
 Graph description (plain dicts, shared with the tests):
-  tensors: [{"rows": R, "cols": C, "dtype": "f16"|"bf16"|"f32"}, ...]
+  tensors: [{"rows": R, "cols": C, "dtype": "f16"|"bf16"|"f32"|"i32", "transient"?: bool}, ...]
   ref      = (tensor_id, r0, c0, rows, cols)      a 2-D window of a tensor
   nodes:   [{"kind": "matmul", "a", "b", "c", "bias"?, "residual"?, "gamma"?, "b2"?, ...},
             {"kind": "ew", "op", "ins": [refs], "out"},
@@ -460,15 +460,123 @@ def _lower_attention(ni, nd, opts, phases, tensors, sem_tiles):
         phases.append(out)
 
 
+ELT_BYTES = {"f16": 2, "bf16": 2, "f32": 4, "i32": 4}
+
+
+def _node_refs(nd):
+    """(refs the node reads, refs it writes) by the fields of its kind."""
+    k = nd["kind"]
+    if k == "matmul":
+        reads = [nd["a"], nd["b"], nd.get("b2"), nd.get("bias"), nd.get("residual"),
+                 nd.get("gamma")]
+        writes = [nd["c"]]
+    elif k == "ew":
+        reads, writes = list(nd["ins"]), [nd["out"]]
+    elif k == "rmsnorm":
+        reads, writes = [nd["x"], nd["gamma"]], [nd["out"]]
+    elif k == "rope":
+        reads, writes = [nd["x"]], [nd["out_q"], nd["out_k"], nd.get("out_v")]
+    elif k == "attention":
+        reads, writes = [nd["q"], nd["k"], nd["v"]], [nd["out"]]
+    elif k == "argmax":
+        reads, writes = [nd["x"]], [nd["out"]]
+    else:
+        raise ValueError(k)
+    return [r for r in reads if r is not None], [w for w in writes if w is not None]
+
+
+def transient_bytes(t):
+    """Pool bytes of a transient: rows of cols elements padded to 16 bytes (at least 16), the
+    whole rounded up to 1 KB."""
+    es = ELT_BYTES[t["dtype"]]
+    per = 16 // es
+    ld = max(cdiv(t["cols"], per) * per, per)
+    return cdiv(t["rows"] * ld * es, 1024) * 1024
+
+
+def _pool(tensors, nodes, instrs, targets, o, split):
+    """Phase 2 of "MegaKittens Internals" §04, for the transient tensors.
+
+    Transients are visited in the order of the node that writes them. One takes a buffer from
+    the pool when its writer's first instruction is at least n_sm instructions past the end
+    (last instruction + 1) of every node that touched the buffer's current occupant, and the
+    occupant has the same dtype and shape; otherwise it gets a new buffer at the end of the
+    pool. The occupant's writer counts among the nodes that touched it. A buffer whose occupant
+    is touched by a node without instructions (fused into another) is never handed on.
+
+    Each reuse is one new counter: every instruction of the nodes that touched the old occupant
+    arrives on it (the splits of one tile once) and every instruction of the new writer waits
+    for that count. Returns (byte offset per tensor id or -1, pool bytes, number of reuses);
+    ``instrs`` and ``targets`` gain the counters.
+    """
+    first, last = {}, {}
+    for i, ins in enumerate(instrs):
+        if ins.op == OP_NOOP:
+            continue
+        first.setdefault(ins.node, i)
+        last[ins.node] = i
+    touched = {}
+    writer = {}
+    for ni, nd in enumerate(nodes):
+        reads, writes = _node_refs(nd)
+        for ref in reads + writes:
+            touched.setdefault(ref[0], [])
+            if ni not in touched[ref[0]]:
+                touched[ref[0]].append(ni)
+        for ref in writes:
+            writer.setdefault(ref[0], ni)
+    trans = [t for t, d in enumerate(tensors) if d.get("transient")]
+    trans.sort(key=lambda t: writer.get(t, len(nodes)))
+    offsets = [-1] * len(tensors)
+    buffers = []          # [offset, occupant, nodes that touched it, may be handed on]
+    end = 0
+    reuses = []           # (nodes that touched the old occupant, new writer)
+    for t in trans:
+        acc = touched.get(t, [])
+        usable = t in writer and all(ni in last for ni in acc)
+        chosen = None
+        if usable:
+            start = first[writer[t]]
+            for b in buffers:
+                old = tensors[b[1]]
+                same = (old["dtype"], old["rows"], old["cols"]) == (
+                    tensors[t]["dtype"], tensors[t]["rows"], tensors[t]["cols"])
+                if b[3] and same and all(start - (last[ni] + 1) >= o["n_sm"] for ni in b[2]):
+                    chosen = b
+                    break
+        if chosen is not None:
+            reuses.append((chosen[2], writer[t]))
+            chosen[1], chosen[2] = t, acc
+        else:
+            chosen = [end, t, acc, usable]
+            buffers.append(chosen)
+            end += transient_bytes(tensors[t])
+        offsets[t] = chosen[0]
+    for old_nodes, new_writer in reuses:
+        cid = len(targets)
+        arrivals = set()
+        for i, ins in enumerate(instrs):
+            if ins.op != OP_NOOP and ins.node in old_nodes:
+                arrivals.add(("t", ins.tile) if split(ins) else ("i", i))
+                ins.dst.append(cid)
+        targets.append(len(arrivals))
+        for ins in instrs:
+            if ins.op != OP_NOOP and ins.node == new_writer:
+                ins.src.append((cid, len(arrivals)))
+    return offsets, end, len(reuses)
+
+
 class Plan:
     """The oracle's schedule: flat instruction list (Noop-padded), counters and placement."""
 
-    def __init__(self, instrs, targets, n_dep, n_sm, sem_count):
+    def __init__(self, instrs, targets, n_dep, n_sm, sem_count, pool=None):
         self.instrs = instrs
-        self.targets = targets          # per dependency counter
+        self.targets = targets          # per dependency counter (reuse counters last)
         self.n_dep = n_dep
         self.n_sem = sem_count
         self.n_sm = n_sm
+        # buffer pool: byte offset of every tensor (-1: caller-owned), bytes, reuse events
+        self.pool_off, self.pool_bytes, self.n_reuse = pool or ([], 0, 0)
 
     @property
     def n_instr(self):
@@ -593,8 +701,14 @@ def lower(graph, opts):
     for ins in instrs:
         if split(ins):
             ins.dst = list(first[ins.tile].dst)
+
+    # Phase 2 after the fact: the pool needs the final instruction order.
+    pool = _pool(tensors, nodes, instrs, targets, o, split)
+    n_dep = len(targets)
+    for ins in instrs:          # semaphores follow every counter, reuse counters included
+        if split(ins):
             ins.sem = n_dep + ins.tile
-    return Plan(instrs, targets, n_dep, o["n_sm"], len(sem_tiles))
+    return Plan(instrs, targets, n_dep, o["n_sm"], len(sem_tiles), pool)
 
 
 def topologically_valid(plan):

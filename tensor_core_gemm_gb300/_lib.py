@@ -17,6 +17,7 @@ EXPORTS = [
     "mk_run_host", "mk_sync_status", "mk_plan_destroy", "mk_plan_stats", "mk_get_instructions",
     "mk_get_src_list", "mk_get_dst_list", "mk_get_counter_targets", "mk_get_counters",
     "mk_last_error", "mk_abi_version", "mk_gemv_noalloc", "mk_get_trace", "mk_plan_repack",
+    "mk_add_transient", "mk_plan_tensor_ptr",
 ]
 
 
@@ -60,7 +61,8 @@ class Stats(C.Structure):
                 ("n_sm", C.c_int64), ("n_iter", C.c_int64), ("waves", C.c_double),
                 ("n_src", C.c_int64), ("n_dst", C.c_int64), ("per_op", C.c_int64 * 16),
                 ("smem_bytes", C.c_int64), ("scratch_bytes", C.c_int64),
-                ("kernel_set", C.c_int64), ("packed_bytes", C.c_int64)]
+                ("kernel_set", C.c_int64), ("packed_bytes", C.c_int64),
+                ("pool_bytes", C.c_int64), ("n_reuse", C.c_int64)]
 
 
 _lib = None
@@ -82,6 +84,8 @@ def load():
         "mk_graph_destroy": [P],
         "mk_add_tensor": [P, VP, I32, I32, C.POINTER(I64), C.POINTER(I64), PI32],
         "mk_add_view": [P, I32, I64, I64, I64, I64, PI32],
+        "mk_add_transient": [P, I32, I64, I64, PI32],
+        "mk_plan_tensor_ptr": [P, I32, C.POINTER(VP)],
         "mk_add_matmul": [P, I32, I32, I32, C.POINTER(Epilogue), PI32],
         "mk_add_elementwise": [P, I32, PI32, I32, I32, C.POINTER(EwParams), PI32],
         "mk_add_attention": [P, I32, I32, I32, I32, C.POINTER(AttnParams), PI32],

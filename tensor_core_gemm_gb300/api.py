@@ -67,6 +67,14 @@ class Graph:
                                       C.byref(tid)))
         return tid.value
 
+    def transient(self, dtype, rows, cols):
+        """A plan-owned rows x cols intermediate ('f16'|'bf16'|'f32'|'i32'): one node writes
+        it, later nodes read it, and mk_compile places it in the plan's buffer pool."""
+        dtype = _DT[dtype] if isinstance(dtype, str) else dtype
+        tid = C.c_int32()
+        check(self._lib.mk_add_transient(self._h, dtype, rows, cols, C.byref(tid)))
+        return tid.value
+
     def view(self, base, r0, c0, rows, cols):
         vid = C.c_int32()
         check(self._lib.mk_add_view(self._h, base, r0, c0, rows, cols, C.byref(vid)))
@@ -178,6 +186,12 @@ class Plan:
         if code != _lib.MK_OK:
             raise _lib.MkError(code, self._lib.mk_last_error().decode(errors="replace"))
         return st
+
+    def tensor_ptr(self, tensor):
+        """Device address of a tensor in this plan (a transient's place in the buffer pool)."""
+        p = C.c_void_p()
+        check(self._lib.mk_plan_tensor_ptr(self._h, tensor, C.byref(p)))
+        return p.value or 0
 
     def stats(self):
         s = _lib.Stats()

@@ -597,6 +597,127 @@ mk_status lower_graph(const std::vector<TensorRec>& tensors_in, const std::vecto
     h.rec.sem = n_dep + h.tile;
   }
 
+  // Buffer pool ("MegaKittens Internals" §04 phase 2, restated). Transient tensors (plan-owned
+  // intermediates) are placed in node order of their writer. A transient takes a pooled buffer of
+  // its exact shape and dtype when the writer's first instruction lies at least n_sm
+  // instructions past the end (last instruction + 1) of every node that accessed the buffer's
+  // current occupant (the one-wave rule: the old accesses sit earlier in every SM's queue); else
+  // it gets a new buffer, the first of the equals that qualify being taken. The occupant's own
+  // writer counts as an accessor, so a region no reader covered is also finished. Each reuse is
+  // one counter, numbered after the dependency counters: every instruction of the accessor nodes
+  // arrives on it (a split tile once), and every instruction of the new writer waits for the
+  // total before it runs. Transients an instruction-less (fused) node touches keep a buffer of
+  // their own.
+  {
+    const int n_t = (int)tensors_in.size();
+    plan->pool_off.assign(ts.size(), -1);
+    plan->pool_bytes = 0;
+    plan->n_reuse = 0;
+    std::vector<int> first(nn, INT32_MAX), last(nn, -1);
+    for (size_t i = 0; i < ins.size(); ++i) {
+      if (ins[i].rec.op == OP_NOOP) continue;
+      const int nd_i = ins[i].rec.node;
+      first[nd_i] = std::min(first[nd_i], (int)i);
+      last[nd_i] = std::max(last[nd_i], (int)i);
+    }
+    auto touches = [&](const NodeRec& nd, int base, bool write) {
+      std::vector<int> ids;
+      if (write) {
+        ids = {nd.out, nd.out_k, nd.out_v};
+      } else {
+        ids = {nd.a, nd.b, nd.b2, nd.bias, nd.res, nd.gamma, nd.ins[0], nd.ins[1]};
+      }
+      for (int id : ids)
+        if (id >= 0 && ts[id].base == base) return true;
+      return false;
+    };
+    struct Occ {
+      int tensor;
+      std::vector<int> nodes;  // accessor nodes of the occupant
+      bool pooled;
+    };
+    std::vector<Occ> buffers;
+    std::vector<int64_t> buf_off, buf_bytes;
+    std::vector<int> order;
+    std::vector<int> writer(n_t, -1);
+    for (int t = 0; t < n_t; ++t) {
+      if (!ts[t].transient || ts[t].base != t) continue;
+      for (int ni = 0; ni < nn && writer[t] < 0; ++ni)
+        if (touches(nodes[ni], t, true)) writer[t] = ni;
+      order.push_back(t);
+    }
+    std::stable_sort(order.begin(), order.end(), [&](int a, int b) {
+      const int wa = writer[a] < 0 ? INT32_MAX : writer[a], wb = writer[b] < 0 ? INT32_MAX : writer[b];
+      return wa < wb;
+    });
+    std::vector<std::pair<std::vector<int>, int>> events;  // (source nodes, writer node)
+    for (int t : order) {
+      std::vector<int> acc;
+      bool ok = writer[t] >= 0;
+      for (int ni = 0; ni < nn; ++ni)
+        if (touches(nodes[ni], t, false) || touches(nodes[ni], t, true)) {
+          acc.push_back(ni);
+          ok = ok && last[ni] >= 0;
+        }
+      const int64_t bytes =
+          ((int64_t)ts[t].rows * ts[t].ld * dtype_size(ts[t].dtype) + 1023) & ~(int64_t)1023;
+      int chosen = -1;
+      if (ok) {
+        const int start = first[writer[t]];
+        for (size_t bi = 0; bi < buffers.size() && chosen < 0; ++bi) {
+          const TensorRec& o_t = ts[buffers[bi].tensor];
+          if (!buffers[bi].pooled || o_t.dtype != ts[t].dtype || o_t.rows != ts[t].rows ||
+              o_t.cols != ts[t].cols)
+            continue;
+          bool free = true;
+          for (int ni : buffers[bi].nodes) free = free && (int64_t)last[ni] + 1 + o.n_sm <= start;
+          if (free) chosen = (int)bi;
+        }
+      }
+      if (chosen >= 0) {
+        events.push_back({buffers[chosen].nodes, writer[t]});
+        buffers[chosen] = {t, acc, true};
+      } else {
+        chosen = (int)buffers.size();
+        buffers.push_back({t, acc, ok});
+        buf_off.push_back(plan->pool_bytes);
+        buf_bytes.push_back(bytes);
+        plan->pool_bytes += bytes;
+      }
+      plan->pool_off[t] = buf_off[chosen];
+    }
+    for (int t = 0; t < (int)ts.size(); ++t)  // views follow their base
+      if (ts[t].transient && ts[t].base != t && plan->pool_off[ts[t].base] >= 0)
+        plan->pool_off[t] = plan->pool_off[ts[t].base] +
+                            ((ts[t].r0 - ts[ts[t].base].r0) * ts[t].ld + ts[t].c0 -
+                             ts[ts[t].base].c0) * dtype_size(ts[t].dtype);
+    for (const auto& ev : events) {
+      const int cid = (int)targets.size();
+      int32_t count = 0;
+      std::vector<char> tile_seen(n_tiles_sem, 0);
+      for (size_t i = 0; i < ins.size(); ++i) {
+        if (ins[i].rec.op == OP_NOOP) continue;
+        if (std::find(ev.first.begin(), ev.first.end(), ins[i].rec.node) == ev.first.end())
+          continue;
+        if (is_split(ins[i])) {
+          if (!tile_seen[ins[i].tile]) ++count;
+          tile_seen[ins[i].tile] = 1;
+        } else {
+          ++count;
+        }
+        ins[i].dst.push_back(cid);
+      }
+      targets.push_back(count);
+      for (size_t i = 0; i < ins.size(); ++i)
+        if (ins[i].rec.op != OP_NOOP && ins[i].rec.node == ev.second)
+          ins[i].src.push_back({cid, count});
+      ++plan->n_reuse;
+    }
+    if (!events.empty())  // the semaphores follow every dependency counter, reuse ones included
+      for (auto& h : ins)
+        if (is_split(h)) h.rec.sem = (int)targets.size() + h.tile;
+  }
+
   // Pack.
   plan->instrs.clear();
   plan->src_list.clear();
@@ -615,7 +736,7 @@ mk_status lower_graph(const std::vector<TensorRec>& tensors_in, const std::vecto
     plan->instrs.push_back(r);
   }
   plan->targets = targets;
-  plan->n_dep = n_dep;
+  plan->n_dep = (int)targets.size();
   plan->n_sem = n_tiles_sem;
   plan->n_sm = o.n_sm;
   plan->tensors = ts;
@@ -698,6 +819,29 @@ extern "C" mk_status mk_add_tensor(mk_graph_t g, void* dev_ptr, int32_t dtype, i
   t.base = (int)g->tensors.size();
   g->tensors.push_back(t);
   *id = t.base;
+  return MK_OK;
+}
+
+extern "C" mk_status mk_add_transient(mk_graph_t g, int32_t dtype, int64_t rows, int64_t cols,
+                                      int32_t* id) {
+  if (!g || !id || rows < 0 || cols < 0) {
+    set_error("mk_add_transient: bad graph, id or extents");
+    return MK_ERR_INVALID_ARG;
+  }
+  if (dtype != MK_F16 && dtype != MK_BF16 && dtype != MK_F32 && dtype != MK_I32) {
+    set_error("mk_add_transient: unknown dtype %d", dtype);
+    return MK_ERR_INVALID_ARG;
+  }
+  TensorRec t;
+  t.dtype = dtype;
+  t.rows = rows;
+  t.cols = cols;
+  const int64_t per16 = 16 / dtype_size(dtype);  // rows start 16-byte aligned
+  t.ld = std::max<int64_t>((cols + per16 - 1) / per16 * per16, per16);
+  t.base = (int)g->tensors.size();
+  t.transient = true;
+  *id = t.base;
+  g->tensors.push_back(t);
   return MK_OK;
 }
 

@@ -22,6 +22,7 @@ struct TensorRec {
   int base = -1;
   int64_t r0 = 0, c0 = 0;   // offset inside the base tensor
   bool internal = false;    // plan-owned scratch created by the lowering
+  bool transient = false;   // plan-owned intermediate placed in the buffer pool (mk_add_transient)
 };
 
 enum NodeKind { NK_MATMUL = 0, NK_EW = 1, NK_RMSNORM = 2, NK_ROPE = 3, NK_ATTN = 4, NK_ARGMAX = 5 };
@@ -74,6 +75,9 @@ struct HostPlan {
   std::vector<int> node_tile_n;            // per node: output columns per tile
   std::vector<int> node_gsplit_slots;      // per node: fp32 partial slots of GEMM split tails
   std::vector<int> node_rope;              // per matmul node: the ROPE node fused into it, or -1
+  std::vector<int64_t> pool_off;           // per tensor: byte offset in the buffer pool, or -1
+  int64_t pool_bytes = 0;
+  int n_reuse = 0;                         // reuse events (one reuse counter each)
 };
 
 void set_error(const char* fmt, ...);

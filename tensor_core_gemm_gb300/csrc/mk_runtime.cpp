@@ -135,8 +135,43 @@ static mk_status check_hazards(const mk_graph* g) {
   return MK_OK;
 }
 
+// A transient (plan-owned) tensor is defined by exactly one node, and every node reading it
+// (through any view) comes after that node: its buffer may hold an earlier transient's data
+// until the writer runs.
+static mk_status check_transients(const mk_graph* g) {
+  std::vector<int> writer(g->tensors.size(), -1), r, w;
+  for (size_t i = 0; i < g->nodes.size(); ++i) {
+    node_regions(g, g->nodes[i], r, w);
+    for (int id : r) {
+      const int b = g->tensors[id].base;
+      if (g->tensors[b].transient && writer[b] < 0) {
+        set_error("mk_compile: node %zu reads transient tensor %d before a node writes it", i, b);
+        return MK_ERR_INVALID_ARG;
+      }
+    }
+    for (int id : w) {
+      const int b = g->tensors[id].base;
+      if (!g->tensors[b].transient) continue;
+      if (writer[b] >= 0 && writer[b] != (int)i) {
+        set_error("mk_compile: transient tensor %d is written by nodes %d and %zu (one writer)", b,
+                  writer[b], i);
+        return MK_ERR_INVALID_ARG;
+      }
+      writer[b] = (int)i;
+    }
+  }
+  return MK_OK;
+}
+
 static bool aligned16(const TensorRec& t) {
   return ((uintptr_t)t.ptr % 16) == 0 && (t.ld * dtype_size(t.dtype)) % 16 == 0;
+}
+
+// Transients have no address before mk_compile places them: their alignment is that of the
+// element offset within the pool buffer (which starts 1 KB aligned).
+static bool aligned16_transient(const TensorRec& t) {
+  const size_t es = dtype_size(t.dtype);
+  return ((t.r0 * t.ld + t.c0) * es) % 16 == 0 && (t.ld * es) % 16 == 0;
 }
 
 namespace mk {
@@ -182,12 +217,14 @@ mk_status check_kernel_support(const std::vector<TensorRec>& ts, const std::vect
       if (id >= 0) all.push_back(id);
     for (int id : all) {
       if (ts[id].rows * ts[id].cols == 0) continue;  // never accessed
-      if (!ts[id].ptr) {
+      const bool transient = ts[ts[id].base].transient;
+      if (!transient && !ts[id].ptr) {
         set_error("mk_compile: node %zu uses tensor %d with a NULL device pointer", i, id);
         return MK_ERR_INVALID_ARG;
       }
+      const bool al = transient ? aligned16_transient(ts[id]) : aligned16(ts[id]);
       // ARGMAX reads rows that are not 16-byte aligned element by element and stores one int32
-      if (nd.kind != NK_ARGMAX && (!aligned16(ts[id]) || ts[id].cols % 8)) {
+      if (nd.kind != NK_ARGMAX && (!al || ts[id].cols % 8)) {
         set_error("mk_compile: node %zu tensor %d: start address and row stride must be 16-byte "
                   "aligned and cols a multiple of 8", i, id);
         return MK_ERR_UNSUPPORTED;
@@ -508,6 +545,7 @@ extern "C" mk_status mk_compile(mk_graph_t g, const mk_compile_opts* opts_in, mk
     mk_default_opts(&o);
   }
   mk_status st = check_hazards(g);
+  if (st == MK_OK) st = check_transients(g);
   if (st) return st;
   mk_plan* p = new (std::nothrow) mk_plan();
   if (!p) {
@@ -638,7 +676,8 @@ extern "C" mk_status mk_compile(mk_graph_t g, const mk_compile_opts* opts_in, mk
   const size_t off_maps = align(off_trace + trace_bytes);
   const size_t off_scratch = align(off_maps + kMaxTmaps * sizeof(CUtensorMap));
   const size_t off_pack = (off_scratch + scratch + 1023) & ~(size_t)1023;
-  const size_t total = off_pack + p->packed_bytes;
+  const size_t off_pool = off_pack + p->packed_bytes;  // packed copies end 1 KB aligned
+  const size_t total = off_pool + (size_t)p->hp.pool_bytes;
   for (auto& j : p->packs) j.off += off_pack;
   if (cudaMalloc((void**)&p->d_mem, total) != cudaSuccess) {
     cudaGetLastError();
@@ -648,6 +687,8 @@ extern "C" mk_status mk_compile(mk_graph_t g, const mk_compile_opts* opts_in, mk
   }
   for (size_t i = 0; i < g->nodes.size(); ++i)
     scratch_ptr[i] = scratch_len[i] ? (uint64_t)(uintptr_t)(p->d_mem + off_scratch + scratch_off[i]) : 0;
+  for (size_t t = 0; t < p->hp.pool_off.size(); ++t)  // transients (and their views) get addresses
+    if (p->hp.pool_off[t] >= 0) p->hp.tensors[t].ptr = p->d_mem + off_pool + p->hp.pool_off[t];
   if ((st = build_nodes(g, p, maps, scratch_ptr))) {
     cudaFree(p->d_mem);
     delete p;
@@ -735,6 +776,10 @@ static mk_status host_copy(mk_plan_t p, const mk_host_copy& c, cudaStream_t s) {
     set_error("mk_run_host: bad tensor id %d or NULL host pointer", c.tensor);
     return MK_ERR_INVALID_ARG;
   }
+  if (c.to_device && ts[ts[c.tensor].base].transient) {
+    set_error("mk_run_host: tensor %d is a transient, which its writer node defines", c.tensor);
+    return MK_ERR_INVALID_ARG;
+  }
   const TensorRec& t = ts[c.tensor];
   const size_t es = dtype_size(t.dtype);
   if (t.rows == 0 || t.cols == 0) return MK_OK;
@@ -749,8 +794,8 @@ static mk_status host_copy(mk_plan_t p, const mk_host_copy& c, cudaStream_t s) {
 
 extern "C" mk_status mk_run_host(mk_plan_t p, const mk_host_copy* copies, int32_t n,
                                  void* stream) {
-  if (!p || (n > 0 && !copies) || n < 0) {
-    set_error("mk_run_host: NULL plan or copies");
+  if (!p || (n > 0 && !copies) || n < 0 || !p->on_device) {
+    set_error("mk_run_host: NULL plan or copies, or a dry-run plan");
     return MK_ERR_INVALID_ARG;
   }
   cudaStream_t s = (cudaStream_t)stream;
@@ -827,6 +872,18 @@ extern "C" mk_status mk_plan_stats(mk_plan_t p, mk_stats* s) {
   s->scratch_bytes = (int64_t)p->scratch_bytes;
   s->kernel_set = p->kernel_set;
   s->packed_bytes = (int64_t)p->packed_bytes;
+  s->pool_bytes = p->hp.pool_bytes;
+  s->n_reuse = p->hp.n_reuse;
+  return MK_OK;
+}
+
+extern "C" mk_status mk_plan_tensor_ptr(mk_plan_t p, int32_t tensor, void** ptr) {
+  if (!p || !ptr || tensor < 0 || tensor >= (int)p->hp.tensors.size() ||
+      p->hp.tensors[tensor].internal) {
+    set_error("mk_plan_tensor_ptr: NULL plan/pointer or bad tensor id %d", tensor);
+    return MK_ERR_INVALID_ARG;
+  }
+  *ptr = p->hp.tensors[tensor].ptr;
   return MK_OK;
 }
 

@@ -267,15 +267,79 @@ def prefill(sh=None, tokens=2048, device=None, seed=0):
                     sh.weight_bytes(), info)
 
 
+def _is_ref(v):
+    return isinstance(v, tuple) and len(v) == 5 and all(isinstance(x, int) for x in v)
+
+
+def with_transients(wl, stacked, block_rows, keep=()):
+    """A copy of workload `wl` in which each tensor id of `stacked` (per-layer row blocks of
+    `block_rows` rows stacked in one tensor) becomes one plan-owned transient per block that a
+    node touches, except the (tensor, block) pairs in `keep`, which stay in the caller's tensor
+    (a graph output). Every other tensor keeps its index and data, so the copy computes the same
+    numbers; new tensors are appended (data None) and info["transients"] lists them."""
+    tensors = [dict(t) for t in wl.desc["tensors"]]
+    new = {}
+
+    def remap(ref):
+        t, r0, c0, rows, cols = ref
+        if t not in stacked:
+            return ref
+        blk = r0 // block_rows
+        if (t, blk) in keep:
+            return ref
+        if r0 + rows > (blk + 1) * block_rows:
+            raise ValueError(f"ref {ref} spans row blocks of tensor {t}")
+        if (t, blk) not in new:
+            tensors.append({"rows": block_rows, "cols": tensors[t]["cols"],
+                            "dtype": tensors[t]["dtype"], "transient": True})
+            new[(t, blk)] = len(tensors) - 1
+        return (new[(t, blk)], r0 - blk * block_rows, c0, rows, cols)
+
+    nodes = []
+    for nd in wl.desc["nodes"]:
+        out = {}
+        for k, v in nd.items():
+            if _is_ref(v):
+                out[k] = remap(v)
+            elif isinstance(v, list) and v and all(_is_ref(x) for x in v):
+                out[k] = [remap(x) for x in v]
+            else:
+                out[k] = v
+        nodes.append(out)
+    data = None
+    if wl.data is not None:
+        data = list(wl.data) + [None] * (len(tensors) - len(wl.data))
+    info = dict(wl.info, transients=sorted(new.values()))
+    return Workload(wl.name, {"tensors": tensors, "nodes": nodes}, data, wl.flops, wl.hbm_bytes,
+                    info)
+
+
+def decoder_intermediates(wl):
+    """with_transients arguments that make every per-layer intermediate of a decode or
+    prefill workload plan-owned, the last layer's output staying the caller's."""
+    inf = wl.info
+    L = inf["shape"].layers
+    if wl.name == "decode":
+        ids = [inf[k] for k in ("qkv", "qr", "att", "h", "gu", "out")]
+        rows = 1
+    else:
+        ids = [inf[k] for k in ("xn", "qkv", "qr", "kr", "att", "h", "hn", "gu", "out")]
+        rows = inf["tokens"]
+    return set(ids), rows, {(inf["out"], L - 1)}
+
+
 # ---------------------------------------------------------------------- builder
 
 def build_graph(desc, data=None):
-    """Register the description's tensors (data: matching torch tensors, or None for a dry run)
-    and add its nodes. Returns (graph, id_of) where id_of(ref) gives the tensor/view id."""
+    """Register the description's tensors (data: matching torch tensors, or None for a dry run;
+    tensors marked "transient" are plan-owned and take no data) and add its nodes. Returns
+    (graph, id_of) where id_of(ref) gives the tensor/view id."""
     g = Graph()
     base = []
     for i, t in enumerate(desc["tensors"]):
-        if data is not None:
+        if t.get("transient"):
+            base.append(g.transient(t["dtype"], t["rows"], t["cols"]))
+        elif data is not None:
             base.append(g.tensor(data[i]))
         else:
             dt = t["dtype"]

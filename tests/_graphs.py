@@ -1,11 +1,11 @@
 """Neutral graph descriptions used by the schedule tests (plain data, no arithmetic)."""
 
 
-def mlp_unfused(m=1024, h=1024, layers=3, dtype="bf16"):
+def mlp_unfused(m=1024, h=1024, layers=3, dtype="bf16", transient=False):
     """The aten graph of the MegaKittens MLP example: per layer mm -> add(bias) -> relu.
 
     Tensors: 0 = W [layers·h × h] (stacked K×N weights), 1 = x [m × h], 2 = b [layers·m × h],
-    then per layer mm, add, relu outputs.
+    then per layer mm, add, relu outputs (plan-owned transients when ``transient``).
     """
     tensors = [{"rows": layers * h, "cols": h, "dtype": dtype},
                {"rows": m, "cols": h, "dtype": dtype},
@@ -16,7 +16,7 @@ def mlp_unfused(m=1024, h=1024, layers=3, dtype="bf16"):
         ids = []
         for _ in range(3):
             ids.append(len(tensors))
-            tensors.append({"rows": m, "cols": h, "dtype": dtype})
+            tensors.append({"rows": m, "cols": h, "dtype": dtype, "transient": transient})
         mm, ad, rl = [(t, 0, 0, m, h) for t in ids]
         nodes.append({"kind": "matmul", "a": cur, "b": (0, i * h, 0, h, h), "c": mm})
         nodes.append({"kind": "ew", "op": "add", "ins": [mm, (2, i * m, 0, m, h)], "out": ad})

@@ -9,12 +9,13 @@ import numpy as np
 import pytest
 import torch
 
+import _graphs
 from oracle import models, ops
 from oracle import schedule as osched
 from oracle.numerics import BF16, F16
 
 from tensor_core_gemm_gb300 import synth, workloads
-from tensor_core_gemm_gb300._lib import MK_ERR_TIMEOUT
+from tensor_core_gemm_gb300._lib import MK_ERR_TIMEOUT, MkError
 
 pytestmark = pytest.mark.gpu
 
@@ -448,6 +449,78 @@ def test_run_twice_same_result_and_host_path():
     s.synchronize()
     p.check_status()
     assert torch.equal(c_h, first.cpu())
+
+
+def _pool_check(plan, desc, transients):
+    """Counters after the run and pool addresses follow the oracle's pooled schedule."""
+    st = plan.stats()
+    py = osched.lower(desc, dict(n_sm=st["n_sm"]))
+    assert st["pool_bytes"] == py.pool_bytes and st["n_reuse"] == py.n_reuse > 0
+    assert plan.counters().tolist() == py.final_counters()
+    base = plan.tensor_ptr(transients[0]) - py.pool_off[transients[0]]
+    assert [plan.tensor_ptr(t) - base for t in transients] == [py.pool_off[t] for t in transients]
+
+
+@pytest.mark.parametrize("kind", ["prefill", "decode"])
+def test_buffer_pool_decoder_bit_identical(kind):
+    # Every per-layer intermediate plan-owned (placed in the pool, buffers handed on under the
+    # one-wave rule, reuse counters) computes the same bits as caller-owned intermediates.
+    sh = workloads.DecoderShape(layers=6, hidden=256, n_q_heads=4, n_kv_heads=2, head_dim=64,
+                                ffn=512)
+    if kind == "prefill":
+        wl = workloads.prefill(sh, tokens=384, device=DEV, seed=5)
+        outs = [wl.info["out"]]
+    else:
+        wl = workloads.decode(sh, kv_len=100, device=DEV, seed=5, vocab=5000)
+        outs = [wl.info["out"], wl.info["logits"], wl.info["token"]]
+    L, rows = sh.layers, (384 if kind == "prefill" else 1)
+    g, _ = workloads.build_graph(wl.desc, wl.data)
+    plain = g.compile()
+    plain.run()
+    plain.check_status()
+    want = [wl.data[t].clone() for t in outs]
+    for t in outs:
+        wl.data[t].zero_()
+    pw = workloads.with_transients(wl, *workloads.decoder_intermediates(wl))
+    g2, _ = workloads.build_graph(pw.desc, pw.data)
+    pooled = g2.compile(snapshot_counters=1)
+    pooled.run()
+    pooled.check_status()
+    torch.cuda.synchronize()
+    for t, w in zip(outs, want):
+        if t == wl.info["out"]:   # only the last layer's block is still the caller's
+            w, got = w[(L - 1) * rows:], wl.data[t][(L - 1) * rows:]
+        else:
+            got = wl.data[t]
+        assert torch.equal(got, w), t
+    _pool_check(pooled, pw.desc, pw.info["transients"])
+
+
+def test_buffer_pool_mlp_example_host_readback():
+    # The MegaKittens MLP (mm -> add(bias) -> relu per layer) with all nine layer outputs
+    # plan-owned; the last ReLU's result comes back through mk_run_host from its pool buffer.
+    m = h = 1024
+    desc_t = _graphs.mlp_unfused(m, h, transient=True)
+    desc_p = _graphs.mlp_unfused(m, h)
+    data = [synth.normal((3 * h, h), h ** -0.5, "bf16", 1, DEV),
+            synth.normal((m, h), 1.0, "bf16", 2, DEV),
+            synth.normal((3 * m, h), 0.1, "bf16", 3, DEV)]
+    data_p = data + [synth.zeros((m, h), "bf16", DEV) for _ in range(9)]
+    g, _ = workloads.build_graph(desc_p, data_p)
+    plain = g.compile()
+    plain.run()
+    plain.check_status()
+    g2, _ = workloads.build_graph(desc_t, data + [None] * 9)
+    pooled = g2.compile(snapshot_counters=1)
+    out_h = torch.zeros((m, h), dtype=torch.bfloat16).pin_memory()
+    s = torch.cuda.Stream()
+    pooled.run_host(outputs=[(11, out_h.data_ptr())], stream=s)
+    s.synchronize()
+    pooled.check_status()
+    assert torch.equal(out_h, data_p[11].cpu())
+    _pool_check(pooled, desc_t, list(range(3, 12)))
+    with pytest.raises(MkError, match="transient"):
+        pooled.run_host(inputs=[(3, out_h.data_ptr())])
 
 
 def test_wait_limit_reports_timeout_without_hanging():

@@ -69,6 +69,7 @@ def assert_same_plan(desc, opts):
     assert ins["src_off"].tolist() == list(np.cumsum([0] + [len(i.src) for i in py.instrs])[:-1])
     assert ins["dst_off"].tolist() == list(np.cumsum([0] + [len(i.dst) for i in py.instrs])[:-1])
     assert c.counter_targets().tolist() == py.targets
+    assert st["pool_bytes"] == py.pool_bytes and st["n_reuse"] == py.n_reuse
     assert osched.topologically_valid(py)
     return py, c
 
@@ -355,3 +356,70 @@ def test_kernel_specialisation_choice():
     ]
     for desc, opts, want in cases:
         assert _dry(desc, **opts).stats()["kernel_set"] == want, (opts, want)
+
+
+# ----------------------------------------------------------------------------- buffer pool
+_SMALL = dict(layers=6, hidden=256, n_q_heads=4, n_kv_heads=2, head_dim=64, ffn=512)
+
+
+def test_p3_mlp_pool_plan_matches_oracle_and_page():
+    py, c = assert_same_plan(_graphs.mlp_unfused(transient=True), _graphs.P3_OPTS)
+    st = c.stats()
+    assert st["n_counters"] == 125 and st["n_reuse"] == 1 and st["n_instr"] == 240
+    assert st["pool_bytes"] == 8 * 1024 * 1024 * 2   # eight 1024 x 1024 bf16 buffers
+
+
+@pytest.mark.parametrize("kind,n_sm", [("prefill", 37), ("decode", 40), ("decode", 8),
+                                       ("decode_full", 152)])
+def test_pooled_decoder_plans_match_oracle(kind, n_sm):
+    sh = workloads.DecoderShape(**_SMALL)
+    wl = {"prefill": lambda: workloads.prefill(sh, tokens=384),
+          "decode": lambda: workloads.decode(sh, kv_len=100, vocab=5000),
+          "decode_full": lambda: workloads.decode(vocab=128256)}[kind]()
+    pw = workloads.with_transients(wl, *workloads.decoder_intermediates(wl))
+    py, c = assert_same_plan(pw.desc, dict(n_sm=n_sm))
+    summed = sum(osched.transient_bytes(pw.desc["tensors"][t]) for t in pw.info["transients"])
+    assert py.n_reuse > 0 and py.pool_bytes < summed
+    # plain and pooled plans run the same instructions; only the counter lists grow
+    plain = osched.lower(wl.desc, dict(n_sm=n_sm))
+    assert np.array_equal(osched.as_array(plain)[:, :9], osched.as_array(py)[:, :9])
+    assert py.n_dep == plain.n_dep + py.n_reuse
+
+
+def test_pool_footprint_llama_prefill():
+    wl = workloads.prefill(tokens=2048)
+    pw = workloads.with_transients(wl, *workloads.decoder_intermediates(wl))
+    c = _dry(pw.desc, n_sm=152)
+    summed = sum(osched.transient_bytes(pw.desc["tensors"][t]) for t in pw.info["transients"])
+    assert c.stats()["pool_bytes"] * 10 < summed
+
+
+def test_transient_validation():
+    g = workloads.Graph()
+    t = g.transient("bf16", 128, 64)
+    o = g.tensor(ptr=0x200000, dtype="bf16", shape=[128, 64])
+    g.elementwise("relu", [t], o)                     # read before any node writes it
+    with pytest.raises(MkError, match="before a node writes"):
+        g.compile(dry_run=1, n_sm=4)
+    g = workloads.Graph()
+    a = g.tensor(ptr=0x1000, dtype="bf16", shape=[128, 64])
+    t = g.transient("bf16", 128, 64)
+    top, bot = g.view(t, 0, 0, 64, 64), g.view(t, 64, 0, 64, 64)
+    g.elementwise("relu", [g.view(a, 0, 0, 64, 64)], top)
+    g.elementwise("relu", [g.view(a, 64, 0, 64, 64)], bot)   # a second writer
+    with pytest.raises(MkError, match="one writer"):
+        g.compile(dry_run=1, n_sm=4)
+    with pytest.raises(MkError, match="unknown dtype"):
+        workloads.Graph().transient(7, 4, 4)
+
+
+def test_transient_addresses_in_dry_plans():
+    g = workloads.Graph()
+    a = g.tensor(ptr=0x1000, dtype="bf16", shape=[128, 64])
+    t = g.transient("bf16", 128, 44)     # 44 columns: rows padded to 48 elements (96 bytes)
+    o = g.tensor(ptr=0x200000, dtype="bf16", shape=[128, 44])
+    g.elementwise("relu", [g.view(a, 0, 0, 128, 44)], t)
+    g.elementwise("relu", [t], o)
+    p = g.compile(dry_run=1, n_sm=4)
+    assert p.tensor_ptr(a) == 0x1000 and p.tensor_ptr(t) == 0
+    assert p.stats()["pool_bytes"] == (128 * 48 * 2 + 1023) // 1024 * 1024

@@ -338,6 +338,55 @@ def test_p3_worked_schedule():
     assert plan.final_counters() == plan.targets
 
 
+def test_p3_buffer_pool_matches_page():
+    g = read_golden("p3_mlp_schedule.txt")
+    desc = _graphs.mlp_unfused(transient=True)
+    plan = schedule.lower(desc, _graphs.P3_OPTS)
+    assert plan.n_dep == int(g["pool_total_barriers"])
+    assert plan.n_reuse == int(g["pool_reuse_barriers"])
+    # every caller-owned tensor is a slot, and each distinct pool buffer is one more
+    slots = sum(1 for o in plan.pool_off[:3] if o < 0) + len(set(plan.pool_off[3:12]))
+    assert slots == int(g["pool_tensor_slots"])
+    mm1, add1, relu3, add3 = 3, 4, 11, 10  # tensor ids: layer 1 mm and add, layer 3 add and relu
+    assert plan.pool_off[relu3] == plan.pool_off[mm1]
+    assert plan.pool_off[add3] not in [plan.pool_off[t] for t in range(3, 10)]
+    node_first = {}
+    node_end = {}
+    for i, ins in enumerate(plan.instrs):
+        node_first.setdefault(ins.node, i)
+        node_end[ins.node] = i + 1
+    assert node_end[1] == int(g["pool_layer1_add_end"])
+    assert node_first[8] == int(g["pool_final_relu_start"])
+    assert node_first[7] == int(g["pool_layer3_add_start"])
+    # the reuse counter: every instruction of layer 1's mm and add arrives, every instruction of
+    # the final ReLU waits for that count (the pair's duplicate GEMM instructions both arrive)
+    cid = plan.n_dep - 1
+    feeders = [i for i, ins in enumerate(plan.instrs) if cid in ins.dst]
+    assert feeders == list(range(0, int(g["pool_layer1_add_end"])))
+    waiters = [i for i, ins in enumerate(plan.instrs) if (cid, len(feeders)) in ins.src]
+    assert waiters == list(range(int(g["pool_final_relu_start"]), 240))
+    assert schedule.topologically_valid(plan)
+    assert plan.final_counters() == plan.targets
+
+
+@pytest.mark.parametrize("n_sm,final_relu,layer3_add", [
+    (148, True, False), (160, True, False), (161, False, False), (128, False, True),
+    (129, True, False)])
+def test_pool_one_wave_threshold(n_sm, final_relu, layer3_add):
+    # start - end >= #SMs, with the end exclusive: the page's final ReLU (208) against layer 1's
+    # add (ends at 48) qualifies up to 160 SMs, layer 3's add (176) up to 128. The lowering of
+    # this chain does not depend on n_sm, so only the threshold moves.
+    plan = schedule.lower(_graphs.mlp_unfused(transient=True), dict(_graphs.P3_OPTS, n_sm=n_sm))
+    assert (plan.pool_off[11] == plan.pool_off[3]) == final_relu
+    assert (plan.pool_off[10] == plan.pool_off[3]) == layer3_add
+    if layer3_add:
+        # T3's buffer now holds layer 3's add; the final ReLU takes layer 1's add buffer, whose
+        # readers (layer 1's add and ReLU) end at 80: 208 - 80 = 128
+        assert plan.pool_off[11] == plan.pool_off[4]
+        assert plan.n_reuse == 2
+    assert schedule.topologically_valid(plan)
+
+
 def test_schedule_levels_are_acyclic_and_placement():
     plan = schedule.lower(_graphs.mlp_unfused(), _graphs.P3_OPTS)
     lv = schedule.levels(plan)
