@@ -215,6 +215,10 @@ typedef struct {
   int32_t wave_pack;     /* 1 (default): consecutive independent GEMM nodes are placed as one
                             run, tiles longest K first on the least loaded SM (or CTA pair),
                             padded with Noops; 0: each node's tiles in order */
+  int32_t row_stage;     /* 1 (default): RMSNorm and RoPE row instructions of single-CTA plans
+                            get their input rows copied into the operand ring by the loader warp
+                            (bulk copies), when a row fits one ring stage; 0: the compute
+                            warpgroup loads them itself */
 } mk_compile_opts;
 
 /* Fill *o with the defaults (the values listed above for each field). */

@@ -1085,6 +1085,7 @@ extern "C" mk_status mk_default_opts(mk_compile_opts* o) {
   o->argmax_chunk = 4096;
   o->gemm_group_m = 8;
   o->wave_pack = 1;
+  o->row_stage = 1;
   o->attn_tile_q = 128;
   o->dry_run = 0;
   o->timeout_ms = 2000;

@@ -42,7 +42,6 @@ enum RoleId { R_SCHED = 0, R_LOAD = 1, R_MMA = 2, R_COMPUTE = 3 };
 constexpr unsigned FULL = 0xffffffffu;
 constexpr int kCompute = 128;   // threads of the compute warpgroup
 constexpr int kBarCompute = 1;  // named barrier of the compute warpgroup
-constexpr int kXrFloats = 5120; // GEMV activation staging (M x chunk), reused for its epilogue
 
 struct __align__(1024) Smem {
   uint8_t ring[kRingBytes];             // operand ring (stages 1024-byte aligned: 128-byte swizzle)
@@ -120,8 +119,12 @@ __device__ __forceinline__ int ring_stages(const Instr& in) {
   if (in.op == OP_GEMV) return (in.klen + kGemvRows - 1) / kGemvRows;
   if (in.op == OP_ATTN_PARTIAL) return 1;  // the key/value chunk
   if (in.op == OP_ATTN_PREFILL) return (in.klen + kAttnKeyBlock - 1) / kAttnKeyBlock;
+  if (in.op == OP_RMSNORM || in.op == OP_ROPE) return in.pad;  // staged rows (0: direct)
   return 0;
 }
+// Columns of each input row a staged row instruction copies: the whole row of x (RMSNorm: the
+// normalised columns; RoPE: the q and k heads, then the v heads when it copies v).
+__device__ __forceinline__ int row_stage_cols(const Node& nd) { return nd.N; }
 __device__ __forceinline__ int instr_index(const Params& p, int it) {
   return it * p.n_sm + (int)blockIdx.x;
 }
@@ -549,6 +552,44 @@ __device__ bool load_gemm(const Params& p, Smem& s, const Instr& in, const Node&
 
 __device__ void prefetch_ahead(const Params& p, const Smem& s, int cur, int& next);
 
+// Staged row instruction (RMSNorm, RoPE): once the sources are complete, the instruction's input
+// rows are copied into consecutive ring stages, as many whole rows per stage as fit, by bulk
+// copies (one per row, one lane each; one per stage when the rows are contiguous). Deep queues
+// of bytes in flight without holding registers: the compute warpgroup reads the rows from
+// shared memory.
+__device__ bool load_rows(const Params& p, Smem& s, const Instr& in, const Node& nd, int slot,
+                          uint32_t use, RingPos& rp, uint32_t& nfill, int idx) {
+  const uint32_t NS = ring_n(p);
+  const int nst = ring_stages(in);
+  if (nst == 0) return true;
+  if (!wait_warp(p, smem_u32(&s.deps_ready[slot]), use & 1u, R_LOAD, 36, idx)) return false;
+  if (elect_one()) fence_proxy_async_global();
+  __syncwarp();
+  const int lane = (int)(threadIdx.x & 31u);
+  const int rows = min(nd.tile_m, nd.M - in.m0);
+  const uint32_t rb = (uint32_t)row_stage_cols(nd) * 2u, sb = stage_bytes(p);
+  const int rps = (int)(sb / rb);
+  const size_t lda = (size_t)nd.a.ld * 2u;
+  const uint8_t* a = reinterpret_cast<const uint8_t*>(nd.a.ptr) + (size_t)in.m0 * lda;
+  const uint32_t ring0 = smem_u32(s.ring);
+  for (int j = 0; j < nst; ++j) {
+    if (!wait_warp(p, smem_u32(&s.empty[rp.st]), rp.ph ^ 1u, R_LOAD, 37, idx)) return false;
+    const int r0 = j * rps, nr = min(rps, rows - r0);
+    const uint32_t bar = smem_u32(&s.full[rp.st]), dst = ring0 + rp.st * sb;
+    if (elect_one()) mbar_expect_tx(bar, (uint32_t)nr * rb);
+    __syncwarp();
+    if (lda == rb) {
+      if (lane == 0) bulk_load(dst, a + (size_t)r0 * lda, (uint32_t)nr * rb, bar);
+    } else {
+      for (int r = lane; r < nr; r += 32) bulk_load(dst + r * rb, a + (size_t)(r0 + r) * lda, rb, bar);
+    }
+    __syncwarp();
+    rp.next(NS);
+    ++nfill;
+  }
+  return true;
+}
+
 __device__ bool load_gemv(const Params& p, Smem& s, const Instr& in, const Node& nd, int slot,
                           uint32_t use, RingPos& rp, uint32_t& nfill, int idx, int it,
                           int& pf_next) {
@@ -745,6 +786,8 @@ __device__ void run_loader(const Params& p, Smem& s) {
       ok = load_attn(p, s, in, nd, slot, use, rp, nfill, idx);
     else if (ks_has_attn_prefill(KS) && in.op == OP_ATTN_PREFILL)
       ok = load_attn_prefill(p, s, in, nd, slot, use, rp, nfill, idx);
+    else if (ks_stages_rows(KS) && (in.op == OP_RMSNORM || in.op == OP_ROPE))
+      ok = load_rows(p, s, in, nd, slot, use, rp, nfill, idx);
     if (!ok) break;
     if (elect_one()) mbar_arrive(smem_u32(&s.slot_free[slot]));
     __syncwarp();
@@ -1964,6 +2007,146 @@ __device__ __forceinline__ void rope_body(Smem& s, const Instr& in, const Node& 
   }
 }
 
+// Staged row instruction (see load_rows): stage j holds rows [j * rps, j * rps + nr) of the
+// instruction, W elements each. RMSNorm: a warp per row, two rows per warp at a time; the
+// statistic and the scaling both read the row from shared memory (lane l takes 16-byte vectors
+// l, l + 32, ...: the summation order of the direct path), gamma is copied to shared memory
+// once, while the rows are in flight. RoPE: a thread per 16-byte chunk (8 elements) of a head;
+// the pair partners sit in the chunk of the other half of the head, held by lane ^ (head_dim /
+// 16) (the host stages RoPE only when head_dim / 8 divides 32, so heads never straddle warps);
+// angles from a table of the instruction's rows computed while the first stage is in flight; v
+// is copied through.
+template <bool ROPE>
+__device__ bool rows_staged(const Params& p, Smem& s, const Instr& in, const Node& nd,
+                            uint32_t& ring, int idx) {
+  const uint32_t NS = ring_n(p);
+  const int ct = (int)threadIdx.x - (kThreads - kCompute);
+  const int wp = ct >> 5, lane = ct & 31;
+  const int rows = min(nd.tile_m, nd.M - in.m0), dt = nd.dtype;
+  const int W = row_stage_cols(nd), nst = ring_stages(in);
+  const int rps = (int)(stage_bytes(p) / (uint32_t)(W * 2));
+  const int hd = nd.hd, half = hd / 2, nh = nd.hq + nd.hkv;
+  float* tcos = s.xr;
+  float* tsin = s.xr + rows * half;
+  const uint4* gm = reinterpret_cast<const uint4*>(nd.gamma.ptr);
+  uint4* gs = reinterpret_cast<uint4*>(s.xr);
+  const bool gshared = !ROPE && W * 2 <= kXrFloats * 4;
+  if (ROPE) {
+    const float l2t = log2f(nd.theta);
+    for (int v = ct; v < rows * half; v += kCompute) {
+      const int r = v / half, i = v % half;
+      const float inv = exp2f(-(2.0f * (float)i / (float)hd) * l2t);
+      sincosf((float)(nd.pos0 + in.m0 + r) * inv, &tsin[v], &tcos[v]);
+    }
+    cw_sync();
+  } else if (gshared) {
+    for (int v = ct; v < W / 8; v += kCompute) gs[v] = __ldg(gm + v);
+    cw_sync();
+  }
+  for (int j = 0; j < nst; ++j) {
+    const int st = (int)(ring % NS);
+    if (!cw_wait(p, smem_u32(&s.full[st]), (ring / NS) & 1u, 46, idx)) return false;
+    if (j == 0) trace_mark(p, idx, 6);
+    const uint8_t* base = stage_ptr(s, p, st);
+    const int r0 = j * rps, nr = min(rps, rows - r0);
+    if (!ROPE) {
+      // Rows r and r + 4 of the stage together (two independent chains per warp); each row's
+      // statistic still sums its lane's vectors in order.
+      uint16_t* out = reinterpret_cast<uint16_t*>(nd.out.ptr);
+      const int nv = W / 8;
+      for (int r = wp; r < nr; r += 8) {
+        const bool two = r + 4 < nr;
+        const uint4* xa = reinterpret_cast<const uint4*>(base + (size_t)r * W * 2);
+        const uint4* xb = reinterpret_cast<const uint4*>(base + (size_t)(two ? r + 4 : r) * W * 2);
+        float sa = 0.f, sb = 0.f;
+        for (int v = lane; v < nv; v += 32) {
+          const uint4 qa = xa[v], qb = xb[v];
+          float fa[8], fb[8];
+          unpack8(qa, dt, fa);
+          unpack8(qb, dt, fb);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            sa += fa[e] * fa[e];
+            sb += fb[e] * fb[e];
+          }
+        }
+        const float ra = rsqrtf(warp_sum(sa) / (float)W + nd.eps);
+        const float rb2 = rsqrtf(warp_sum(sb) / (float)W + nd.eps);
+        uint16_t* oa = out + (size_t)(in.m0 + r0 + r) * nd.out.ld;
+        uint16_t* ob = out + (size_t)(in.m0 + r0 + r + 4) * nd.out.ld;
+#pragma unroll 2
+        for (int v = lane; v < nv; v += 32) {
+          const uint4 qa = xa[v], qb = xb[v], qg = gshared ? gs[v] : __ldg(gm + v);
+          float fa[8], fb[8], gf[8];
+          unpack8(qa, dt, fa);
+          unpack8(qb, dt, fb);
+          unpack8(qg, dt, gf);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            fa[e] = fa[e] * ra * gf[e];
+            fb[e] = fb[e] * rb2 * gf[e];
+          }
+          *reinterpret_cast<uint4*>(oa + v * 8) = pack8(fa, dt);
+          if (two) *reinterpret_cast<uint4*>(ob + v * 8) = pack8(fb, dt);
+        }
+      }
+    } else {
+      // cpr = head_dim / 8 chunks per head, a power of two dividing 32 (host-checked): whole
+      // heads fall in one warp, and the partner chunk is held by lane ^ cph
+      const int cpr = hd / 8, cph = cpr / 2, lc = 31 - __clz(cpr);
+      const int per_row = nh * cpr;
+      for (int r = 0; r < nr; ++r) {
+        const uint8_t* rowp = base + (size_t)r * W * 2;
+        const float* tc = tcos + (r0 + r) * half;
+        const float* ts = tsin + (r0 + r) * half;
+        const int m = in.m0 + r0 + r;
+        for (int c0 = 0; c0 < per_row; c0 += kCompute) {  // warp-uniform (shuffles)
+          const int cix = c0 + ct;
+          const bool live = cix < per_row;
+          uint4 x = make_uint4(0u, 0u, 0u, 0u);
+          if (live) x = *reinterpret_cast<const uint4*>(rowp + (size_t)cix * 16);
+          uint4 q;
+          q.x = __shfl_xor_sync(FULL, x.x, cph);
+          q.y = __shfl_xor_sync(FULL, x.y, cph);
+          q.z = __shfl_xor_sync(FULL, x.z, cph);
+          q.w = __shfl_xor_sync(FULL, x.w, cph);
+          if (!live) continue;
+          const int h = cix >> lc, c = cix & (cpr - 1);
+          const bool first = c < cph;
+          const int i0 = (first ? c : c - cph) * 8;
+          const float4 c_lo = *reinterpret_cast<const float4*>(tc + i0);
+          const float4 c_hi = *reinterpret_cast<const float4*>(tc + i0 + 4);
+          const float4 s_lo = *reinterpret_cast<const float4*>(ts + i0);
+          const float4 s_hi = *reinterpret_cast<const float4*>(ts + i0 + 4);
+          const float cs[8] = {c_lo.x, c_lo.y, c_lo.z, c_lo.w, c_hi.x, c_hi.y, c_hi.z, c_hi.w};
+          const float sn[8] = {s_lo.x, s_lo.y, s_lo.z, s_lo.w, s_hi.x, s_hi.y, s_hi.z, s_hi.w};
+          float xf[8], pf[8], y[8];
+          unpack8(x, dt, xf);
+          unpack8(q, dt, pf);
+          // first half: x cos - x' sin; second half: x cos + x' sin (x' the partner element)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) y[e] = first ? xf[e] * cs[e] - pf[e] * sn[e]
+                                                   : xf[e] * cs[e] + pf[e] * sn[e];
+          const Operand& o = h < nd.hq ? nd.out : nd.out_k;
+          const int hh = h < nd.hq ? h : h - nd.hq;
+          store8(o, m, hh * hd + c * 8, dt, y);
+        }
+        if (nd.out_v.ptr) {
+          const int nvv = nd.hkv * hd / 8;
+          uint16_t* ov = reinterpret_cast<uint16_t*>(nd.out_v.ptr) + (size_t)m * nd.out_v.ld;
+          for (int c = ct; c < nvv; c += kCompute)
+            *reinterpret_cast<uint4*>(ov + c * 8) =
+                *reinterpret_cast<const uint4*>(rowp + (size_t)(nh * hd + c * 8) * 2);
+        }
+      }
+    }
+    cw_sync();
+    if (ct == 0) mbar_arrive(smem_u32(&s.empty[st]));
+    ++ring;
+  }
+  return true;
+}
+
 // ARGMAX: (value, column) pairs where a larger value wins and equal values go to the lower
 // column; a column < 0 marks "no number yet" and loses to any number (NaN entries are skipped).
 __device__ __forceinline__ void argmax_take(float& bv, int& bi, float v, int i) {
@@ -2381,9 +2564,13 @@ __device__ void run_compute(const Params& p, Smem& s, uint32_t tmem) {
         ok = cw_wait(p, smem_u32(&s.deps_ready[slot]), use & 1u, 33, idx);
         if (!ok) break;
         trace_mark(p, idx, 2);
-        if (ks_has_rows(KS) && in.op == OP_EW) ew_body(in, nd);
-        else if (ks_has_rows(KS) && in.op == OP_RMSNORM) rmsnorm_body<KS != KS_PREFILL>(in, nd);
-        else if (ks_has_rows(KS) && in.op == OP_ROPE) rope_body<KS != KS_PREFILL>(s, in, nd);
+        if (ks_stages_rows(KS) && in.op == OP_RMSNORM && in.pad > 0)
+          ok = rows_staged<false>(p, s, in, nd, ring, idx);
+        else if (ks_stages_rows(KS) && in.op == OP_ROPE && in.pad > 0)
+          ok = rows_staged<true>(p, s, in, nd, ring, idx);
+        else if (ks_has_rows(KS) && in.op == OP_EW) ew_body(in, nd);
+        else if (ks_has_rows(KS) && in.op == OP_RMSNORM) rmsnorm_body<true>(in, nd);
+        else if (ks_has_rows(KS) && in.op == OP_ROPE) rope_body<true>(s, in, nd);
         else if (ks_has_gemv(KS) && in.op == OP_ATTN_REDUCE) attn_reduce_body(in, nd);
         else if (ks_has_rows(KS) && in.op == OP_ARGMAX) argmax_partial_body(in, nd);
         else if (ks_has_rows(KS) && in.op == OP_ARGMAX_REDUCE) argmax_reduce_body(in, nd);

@@ -196,6 +196,10 @@ mk_status check_kernel_support(const std::vector<TensorRec>& ts, const std::vect
     set_error("mk_compile: gemv_pack is 0 or 1");
     return MK_ERR_UNSUPPORTED;
   }
+  if (o.row_stage != 0 && o.row_stage != 1) {
+    set_error("mk_compile: row_stage is 0 or 1");
+    return MK_ERR_UNSUPPORTED;
+  }
   if (o.kernel_set != 0 && o.kernel_set != 1) {
     set_error("mk_compile: kernel_set is 0 (smallest specialisation) or 1 (general kernel)");
     return MK_ERR_UNSUPPORTED;
@@ -694,6 +698,31 @@ extern "C" mk_status mk_compile(mk_graph_t g, const mk_compile_opts* opts_in, mk
     delete p;
     return st;
   }
+  // 48 KB stages only where a single-CTA GEMM tile needs them; every other ring user (a GEMV
+  // weight tile, an attention key/value chunk or prefill block, staged rows) fits 32 KB, so such
+  // plans prefetch 192 KB of operands per SM instead of 128 KB.
+  bool single_gemm = false;
+  for (const Instr& in : p->hp.instrs) single_gemm |= in.op == OP_GEMM;
+  single_gemm &= o.cluster != 2;
+  const int stages = single_gemm ? kStages : kPairStages;
+  const int64_t stage_bytes = kRingBytes / stages;
+  if (o.row_stage && o.cluster == 1 && ks_stages_rows(p->kernel_set)) {
+    // staged rows: the ring stages each RMSNorm / RoPE instruction fills (Instr.pad)
+    for (Instr& in : p->hp.instrs) {
+      if (in.op != OP_RMSNORM && in.op != OP_ROPE) continue;
+      const Node& n = p->nodes[in.node];
+      if (n.dtype != DT_F16 && n.dtype != DT_BF16) continue;
+      const int64_t w = n.N;  // the whole row of x (RoPE: q, k and v heads)
+      // RoPE: the angle table fits, and whole heads of 16-byte chunks fall in one warp
+      if (in.op == OP_ROPE && (2 * (int64_t)n.tile_m * (n.hd / 2) > kXrFloats || n.hd % 16 ||
+                               32 % (n.hd / 8)))
+        continue;
+      const int64_t rows = std::min<int64_t>(n.tile_m, n.M - in.m0);
+      const int64_t rps = w > 0 ? stage_bytes / (w * 2) : 0;
+      if (rps == 0 || rows <= 0) continue;
+      in.pad = (int32_t)((rows + rps - 1) / rps);
+    }
+  }
   auto up = [&](size_t off, const void* src, size_t bytes) -> cudaError_t {
     return bytes ? cudaMemcpy(p->d_mem + off, src, bytes, cudaMemcpyHostToDevice) : cudaSuccess;
   };
@@ -744,13 +773,7 @@ extern "C" mk_status mk_compile(mk_graph_t g, const mk_compile_opts* opts_in, mk
   pr.n_tmaps = (int32_t)maps.size();
   pr.n_counters = (int32_t)n_ctr;
   pr.l2_prefetch = std::min(std::max(o.l2_prefetch, 0), kSlots);
-  // 48 KB stages only where a single-CTA GEMM tile needs them; every other ring user (a GEMV
-  // weight tile, an attention key/value chunk or prefill block) fits 32 KB, so such plans
-  // prefetch 192 KB of operands per SM instead of 128 KB.
-  bool single_gemm = false;
-  for (const Instr& in : p->hp.instrs) single_gemm |= in.op == OP_GEMM;
-  single_gemm &= o.cluster != 2;
-  pr.stages = single_gemm ? kStages : kPairStages;
+  pr.stages = stages;
   pr.timeout_ns = (uint64_t)(o.timeout_ms > 0 ? o.timeout_ms : 2000) * 1000000ull;
   p->grid = o.n_sm;
   p->on_device = true;

@@ -103,6 +103,7 @@ struct Node {
 static_assert(sizeof(Node) == 256, "node entry is 256 bytes");
 
 constexpr int kMaxTmaps = 256;
+constexpr int kXrFloats = 5120;  // shared-memory staging of GEMV activations / RoPE angle tables
 
 // Kernel parameters (plain pointers into plan-owned device memory).
 struct Params {
@@ -159,6 +160,8 @@ MK_HD constexpr bool ks_has_gemm(int ks) { return ks != KS_DECODE; }
 MK_HD constexpr bool ks_has_gemv(int ks) { return ks == KS_ALL || ks == KS_DECODE; }
 MK_HD constexpr bool ks_has_attn_prefill(int ks) { return ks == KS_ALL || ks == KS_PREFILL; }
 MK_HD constexpr bool ks_has_rows(int ks) { return ks != KS_GEMM; }
+// RMSNorm and RoPE rows staged through the operand ring by the loader (Instr.pad = stages)
+MK_HD constexpr bool ks_stages_rows(int ks) { return ks == KS_ALL || ks == KS_PREFILL; }
 MK_HD constexpr bool ks_has_tmem(int ks) {
   return ks_has_gemm(ks) || ks_has_attn_prefill(ks) || ks_has_gemv(ks);  // GEMV: tensor cores
 }

@@ -270,18 +270,46 @@ def test_unfused_mlp_elementwise_tiles():
             assert_close(f32(data[3 + 3 * l + j]), refs[l][j], f"layer {l} node {j}")
 
 
-def test_rmsnorm_rows():
-    t, d = 67, 2048
+# Row instructions run three ways: the decode specialisation (rows loaded by the compute
+# warpgroup), the general kernel with the rows staged through the operand ring by bulk copies
+# (row_stage, where a row fits one 32 KB stage), and the general kernel without staging. The
+# three agree bit for bit.
+ROW_MODES = [dict(), dict(kernel_set=1), dict(kernel_set=1, row_stage=0)]
+
+
+def _row_modes(build):
+    results = []
+    for mode in ROW_MODES:
+        g, outs = build()
+        p = g.compile(**mode)
+        p.run()
+        p.check_status()
+        torch.cuda.synchronize()
+        pads = p.instructions()["pad"]
+        results.append(([o.clone() for o in outs], int((pads > 0).sum())))
+    for outs, _ in results[1:]:
+        for a, b in zip(results[0][0], outs):
+            assert torch.equal(a, b)
+    return results[0][0], [n for _, n in results]
+
+
+@pytest.mark.parametrize("t,d,staged", [(67, 2048, True), (16, 16384, True), (3, 20000, False),
+                                        (1, 64, True)])
+def test_rmsnorm_rows(t, d, staged):
     x = synth.normal((t, d), 1.0, "bf16", 30, DEV)
     gm = synth.normal((1, d), 0.02, "bf16", 31, DEV, mean=1.0)
-    out = torch.zeros_like(x)
     from tensor_core_gemm_gb300 import Graph
-    g = Graph()
-    ix, ig, io = g.tensor(x), g.tensor(gm), g.tensor(out)
-    g.rmsnorm(ix, ig, io, 1e-5)
-    p = g.compile()
-    p.run()
-    p.check_status()
+
+    def build():
+        out = torch.zeros_like(x)
+        g = Graph()
+        ix, ig, io = g.tensor(x), g.tensor(gm), g.tensor(out)
+        g.rmsnorm(ix, ig, io, 1e-5)
+        return g, [out]
+
+    (out,), n_staged = _row_modes(build)
+    # 16-row instructions: staged in the general kernel where a row fits 32 KB, never in decode
+    assert n_staged == [0, -(-t // 16) if staged else 0, 0]
     assert_close(f32(out), ops.rmsnorm(f32(x), f32(gm)[0], 1e-5, BF16), "rmsnorm")
 
 
@@ -290,17 +318,20 @@ def test_rope(rows, pos0, with_v):
     hq, hkv, d = 32, 8, 64
     cols = (hq + hkv + (hkv if with_v else 0)) * d
     x = synth.normal((rows, cols), 1.0, "bf16", 40, DEV)
-    oq = torch.zeros((rows, hq * d), dtype=torch.bfloat16, device=DEV)
-    ok = torch.zeros((rows, hkv * d), dtype=torch.bfloat16, device=DEV)
-    ov = torch.zeros((rows, hkv * d), dtype=torch.bfloat16, device=DEV)
     from tensor_core_gemm_gb300 import Graph
-    g = Graph()
-    ix, iq, ik, iv = g.tensor(x), g.tensor(oq), g.tensor(ok), g.tensor(ov)
-    g.rope(ix, iq, ik, out_v=iv if with_v else None, n_q_heads=hq, n_kv_heads=hkv, head_dim=d,
-           pos0=pos0, theta=5e5)
-    p = g.compile()
-    p.run()
-    p.check_status()
+
+    def build():
+        oq = torch.zeros((rows, hq * d), dtype=torch.bfloat16, device=DEV)
+        ok = torch.zeros((rows, hkv * d), dtype=torch.bfloat16, device=DEV)
+        ov = torch.zeros((rows, hkv * d), dtype=torch.bfloat16, device=DEV)
+        g = Graph()
+        ix, iq, ik, iv = g.tensor(x), g.tensor(oq), g.tensor(ok), g.tensor(ov)
+        g.rope(ix, iq, ik, out_v=iv if with_v else None, n_q_heads=hq, n_kv_heads=hkv,
+               head_dim=d, pos0=pos0, theta=5e5)
+        return g, [oq, ok, ov]
+
+    (oq, ok, ov), n_staged = _row_modes(build)
+    assert n_staged == [0, -(-rows // 16), 0]
     X = f32(x)
     pos = pos0 + np.arange(rows)
     assert_close(f32(oq), ops.rope(X[:, :hq * d], pos, hq, d, 5e5, BF16), "rope q")
@@ -874,6 +905,8 @@ def test_kernel_set_option_validated():
     g, _ = workloads.build_graph(workloads.gemm(64, 64, 64).desc, None)
     with pytest.raises(Exception, match="kernel_set"):
         g.compile(kernel_set=2)
+    with pytest.raises(Exception, match="row_stage"):
+        g.compile(row_stage=2)
 
 
 # ------------------------------------------------------------------ greedy sampling (ARGMAX)
