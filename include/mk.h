@@ -219,6 +219,10 @@ typedef struct {
                             get their input rows copied into the operand ring by the loader warp
                             (bulk copies), when a row fits one ring stage; 0: the compute
                             warpgroup loads them itself */
+  int32_t pool_waves;    /* buffer pool reuse distance: a transient takes an earlier buffer only
+                            when its writer starts at least pool_waves * n_sm instructions past
+                            the end of every node that touched the old occupant. Default 1 (one
+                            wave); larger values keep more buffers and wait less */
 } mk_compile_opts;
 
 /* Fill *o with the defaults (the values listed above for each field). */

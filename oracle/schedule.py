@@ -105,6 +105,7 @@ DEFAULT_OPTS = dict(
     norm_rows=16,
     gemv_max_m=8, gemv_tile_n=256, gemv_splits=0, gemv_kstep=64,
     attn_chunk=64, attn_tile_q=128, argmax_chunk=4096, gemm_group_m=8, wave_pack=1,
+    pool_waves=1,
 )
 
 
@@ -498,7 +499,8 @@ def _pool(tensors, nodes, instrs, targets, o, split):
     """Phase 2 of "MegaKittens Internals" §04, for the transient tensors.
 
     Transients are visited in the order of the node that writes them. One takes a buffer from
-    the pool when its writer's first instruction is at least n_sm instructions past the end
+    the pool when its writer's first instruction is at least n_sm instructions (times the
+    option pool_waves, 1 by default: the page's one wave) past the end
     (last instruction + 1) of every node that touched the buffer's current occupant, and the
     occupant has the same dtype and shape; otherwise it gets a new buffer at the end of the
     pool. The occupant's writer counts among the nodes that touched it. A buffer whose occupant
@@ -541,7 +543,8 @@ def _pool(tensors, nodes, instrs, targets, o, split):
                 old = tensors[b[1]]
                 same = (old["dtype"], old["rows"], old["cols"]) == (
                     tensors[t]["dtype"], tensors[t]["rows"], tensors[t]["cols"])
-                if b[3] and same and all(start - (last[ni] + 1) >= o["n_sm"] for ni in b[2]):
+                gap = o["pool_waves"] * o["n_sm"]
+                if b[3] and same and all(start - (last[ni] + 1) >= gap for ni in b[2]):
                     chosen = b
                     break
         if chosen is not None:

@@ -44,7 +44,7 @@ class CompileOpts(C.Structure):
         "attn_tile_q", "dry_run", "timeout_ms", "device", "debug_counter", "debug_extra",
         "snapshot_counters", "trace", "l2_prefetch", "gemm_split_tail", "fuse_rope",
         "fuse_attn_reduce", "kernel_set", "gemv_pack", "argmax_chunk", "gemm_group_m",
-        "wave_pack", "row_stage")]
+        "wave_pack", "row_stage", "pool_waves")]
 
 
 class HostCopy(C.Structure):

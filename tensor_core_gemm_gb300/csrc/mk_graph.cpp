@@ -600,8 +600,9 @@ mk_status lower_graph(const std::vector<TensorRec>& tensors_in, const std::vecto
   // Buffer pool ("MegaKittens Internals" §04 phase 2, restated). Transient tensors (plan-owned
   // intermediates) are placed in node order of their writer. A transient takes a pooled buffer of
   // its exact shape and dtype when the writer's first instruction lies at least n_sm
-  // instructions past the end (last instruction + 1) of every node that accessed the buffer's
-  // current occupant (the one-wave rule: the old accesses sit earlier in every SM's queue); else
+  // instructions (pool_waves times that; one wave by default) past the end (last instruction +
+  // 1) of every node that accessed the buffer's current occupant (the one-wave rule: the old
+  // accesses sit earlier in every SM's queue); else
   // it gets a new buffer, the first of the equals that qualify being taken. The occupant's own
   // writer counts as an accessor, so a region no reader covered is also finished. Each reuse is
   // one counter, numbered after the dependency counters: every instruction of the accessor nodes
@@ -670,7 +671,8 @@ mk_status lower_graph(const std::vector<TensorRec>& tensors_in, const std::vecto
               o_t.cols != ts[t].cols)
             continue;
           bool free = true;
-          for (int ni : buffers[bi].nodes) free = free && (int64_t)last[ni] + 1 + o.n_sm <= start;
+          for (int ni : buffers[bi].nodes)
+            free = free && (int64_t)last[ni] + 1 + (int64_t)o.pool_waves * o.n_sm <= start;
           if (free) chosen = (int)bi;
         }
       }
@@ -1086,6 +1088,7 @@ extern "C" mk_status mk_default_opts(mk_compile_opts* o) {
   o->gemm_group_m = 8;
   o->wave_pack = 1;
   o->row_stage = 1;
+  o->pool_waves = 1;
   o->attn_tile_q = 128;
   o->dry_run = 0;
   o->timeout_ms = 2000;

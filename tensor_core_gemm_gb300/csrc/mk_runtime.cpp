@@ -584,6 +584,11 @@ extern "C" mk_status mk_compile(mk_graph_t g, const mk_compile_opts* opts_in, mk
     delete p;
     return MK_ERR_INVALID_ARG;
   }
+  if (o.pool_waves < 1) {
+    set_error("mk_compile: pool_waves must be at least 1");
+    delete p;
+    return MK_ERR_INVALID_ARG;
+  }
   p->opts = o;
   if ((st = lower_graph(g->tensors, g->nodes, o, &p->hp))) {
     delete p;

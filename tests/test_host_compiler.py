@@ -386,6 +386,24 @@ def test_pooled_decoder_plans_match_oracle(kind, n_sm):
     assert py.n_dep == plain.n_dep + py.n_reuse
 
 
+@pytest.mark.parametrize("waves", [2, 5])
+def test_pool_reuse_distance_option(waves):
+    sh = workloads.DecoderShape(**_SMALL)
+    wl = workloads.prefill(sh, tokens=384)
+    pw = workloads.with_transients(wl, *workloads.decoder_intermediates(wl))
+    py, c = assert_same_plan(pw.desc, dict(n_sm=37, pool_waves=waves))
+    one = osched.lower(pw.desc, dict(n_sm=37))
+    # a longer reuse distance hands fewer buffers on and keeps a larger pool
+    assert py.n_reuse <= one.n_reuse and py.pool_bytes >= one.pool_bytes
+    assert py.n_reuse < one.n_reuse or py.pool_bytes > one.pool_bytes or waves == 1
+
+
+def test_pool_waves_validated():
+    g, _ = workloads.build_graph(workloads.gemm(128, 128, 64).desc, None)
+    with pytest.raises(MkError, match="pool_waves"):
+        g.compile(dry_run=1, n_sm=4, pool_waves=0)
+
+
 def test_pool_footprint_llama_prefill():
     wl = workloads.prefill(tokens=2048)
     pw = workloads.with_transients(wl, *workloads.decoder_intermediates(wl))
