@@ -282,6 +282,23 @@ def oracle_sample(name, seconds_budget=15.0):
 
 # ------------------------------------------------------------------ main
 
+def max_over_ranks(x, world, device):
+    """Largest value of x over the ranks of the process group (x itself on one rank)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.item()
+
+
+def job_value(per_rank, unit, world):
+    """Whole-job value of N replicas timed by the slowest one: throughput adds over the
+    replicas; a per-token latency stays the slowest replica's."""
+    return per_rank * world if unit == "TFLOP/s" else per_rank
+
+
 def run_reference(args, world, rank):
     """The oracle, as it stands, timed on this host's cores (the reference arm)."""
     if rank != 0:
@@ -374,11 +391,7 @@ def main():
     clock_info = clocks.stop()
     plan.check_status()
     times = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    ms = statistics.mean(times)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = t.item()
+    ms = max_over_ranks(statistics.mean(times), world, dev)
 
     # End to end through the C ABI with host buffers (pinned), copies inside the timed region.
     ins, outs = io_tensors(wl)
@@ -402,18 +415,11 @@ def main():
     torch.cuda.synchronize()
     barrier()
     plan.check_status()
-    e2e_ms = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = t.item()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
 
     metric, unit, hib = metric_of(args.config)
-    value = value_of(wl, ms, args.config)
-    e2e_value = value_of(wl, e2e_ms, args.config)
-    if unit == "TFLOP/s":
-        value *= world
-        e2e_value *= world
+    value = job_value(value_of(wl, ms, args.config), unit, world)
+    e2e_value = job_value(value_of(wl, e2e_ms, args.config), unit, world)
     peaks, peak_src = load_peaks()
     bound = binding_roof(wl, peaks)
     # fp16 and bf16 have the same dense tensor rate
