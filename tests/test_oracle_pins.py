@@ -294,6 +294,80 @@ def test_decode_step_continues_prefill():
     assert np.max(err) <= 2e-2 * max(1.0, float(np.max(np.abs(full[t]))))
 
 
+def _zero_query_zero_gate(wts):
+    """The tiny decoder with W_q = 0 (every score 0: causal softmax weighs the visible keys
+    equally), W_gate = 0 (silu(0) = 0: the MLP adds exactly 0) and W_o = I (h = a + x)."""
+    hq, d = wts.n_q_heads, wts.head_dim
+    for l in range(wts.n_layers):
+        wts.wqkv[l][:, :hq * d] = 0.0
+        wts.wg[l][:] = 0.0
+        wts.wo[l][:] = np.eye(hq * d, wts.wo[l].shape[1])
+    return wts
+
+
+def _prefix_means(v, hq, hkv, d, first=0):
+    """Row i, query head h: the mean of v rows first..i of kv head h // (hq / hkv), in fp64."""
+    t = v.shape[0]
+    g = hq // hkv
+    out = np.zeros((t - first, hq * d))
+    for i in range(first, t):
+        for h in range(hq):
+            kvh = h // g
+            out[i - first, h * d:(h + 1) * d] = v[:i + 1, kvh * d:(kvh + 1) * d].astype(
+                np.float64).mean(axis=0)
+    return out
+
+
+def test_prefill_closed_form_with_zero_query_and_gate():
+    # Pins the decoder composition (head grouping, causal mask, W_o and residual wiring, the
+    # MLP's zero path) against prefix means of v computed here, not by the attention routine.
+    wts = _zero_query_zero_gate(_tiny_decoder(layers=2))
+    hq, hkv, d = 4, 2, 8
+    x = round_to(RNG.standard_normal((9, 32)), BF16)
+    seen = {}
+    out = models.prefill(x, wts, layer_fn=lambda l, dd: seen.setdefault(l, dd))
+    x_in = x
+    for l in range(2):
+        s = seen[l]
+        np.testing.assert_array_equal(s["q_r"], 0.0)
+        v = s["qkv"][:, (hq + hkv) * d:]
+        a_ref = round_to(_prefix_means(v, hq, hkv, d), BF16)
+        np.testing.assert_allclose(s["a"], a_ref, rtol=2.0 ** -7, atol=1e-30)
+        np.testing.assert_allclose(s["h"], round_to(s["a"].astype(np.float64) + x_in, BF16),
+                                   rtol=0, atol=0)
+        np.testing.assert_array_equal(s["gu"], 0.0)
+        np.testing.assert_array_equal(s["x"], s["h"])
+        x_in = s["x"]
+    np.testing.assert_array_equal(out, x_in)
+
+
+def test_decode_closed_form_with_zero_query_and_gate():
+    # The decode step attends to every cache row plus the appended one with equal weight.
+    wts = _zero_query_zero_gate(_tiny_decoder(layers=2))
+    hq, hkv, d = 4, 2, 8
+    p = 6
+    x = round_to(RNG.standard_normal((1, 32)), BF16)
+    kcs = [round_to(RNG.standard_normal((p + 1, hkv * d)), BF16) for _ in range(2)]
+    vcs = [round_to(RNG.standard_normal((p + 1, hkv * d)), BF16) for _ in range(2)]
+    seen = {}
+    out, kc, vc = models.decode_step(x, wts, kcs, vcs, p,
+                                     layer_fn=lambda l, dd: seen.setdefault(l, dd))
+    x_in = x
+    for l in range(2):
+        s = seen[l]
+        v_new = s["qkv"][:, (hq + hkv) * d:]
+        np.testing.assert_array_equal(vc[l][p], v_new[0])          # appended value row
+        np.testing.assert_array_equal(kc[l][p], s["k_r"][0])       # appended rotated key
+        np.testing.assert_array_equal(vc[l][:p], vcs[l][:p])       # earlier rows untouched
+        a_ref = round_to(_prefix_means(vc[l][:p + 1], hq, hkv, d, first=p), BF16)
+        np.testing.assert_allclose(s["a"], a_ref, rtol=2.0 ** -7, atol=1e-30)
+        np.testing.assert_allclose(s["h"], round_to(s["a"].astype(np.float64) + x_in, BF16),
+                                   rtol=0, atol=0)
+        np.testing.assert_array_equal(s["x"], s["h"])
+        x_in = s["x"]
+    np.testing.assert_array_equal(out, x_in)
+
+
 # ----------------------------------------------------------------------------- schedule
 def test_p3_worked_schedule():
     g = read_golden("p3_mlp_schedule.txt")
