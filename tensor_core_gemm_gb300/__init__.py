@@ -7,4 +7,4 @@ if it has not been built.
 from .api import INSTR_DTYPE, Graph, Plan  # noqa: F401
 
 OPS = {0: "noop", 1: "gemm", 2: "gemv", 3: "ew", 4: "rmsnorm", 5: "rope", 6: "attn_partial",
-       7: "attn_reduce", 8: "attn_prefill"}
+       7: "attn_reduce", 8: "attn_prefill", 9: "argmax", 10: "argmax_reduce"}
