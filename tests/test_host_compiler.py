@@ -441,3 +441,61 @@ def test_transient_addresses_in_dry_plans():
     p = g.compile(dry_run=1, n_sm=4)
     assert p.tensor_ptr(a) == 0x1000 and p.tensor_ptr(t) == 0
     assert p.stats()["pool_bytes"] == (128 * 48 * 2 + 1023) // 1024 * 1024
+
+
+def test_every_entry_point_rejects_null_handles():
+    # Each call validates its handles and pointers before any device work and returns an error
+    # code (never a crash); destroying NULL is a no-op.
+    lib = _lib.load()
+    P = C.c_void_p
+    bad = _lib.MK_ERR_INVALID_ARG
+    i32 = C.c_int32()
+    st = _lib.Stats()
+    ds = _lib.DeviceStatus()
+    buf = (C.c_int32 * 4)()
+    assert lib.mk_graph_create(None) == bad
+    assert lib.mk_graph_destroy(None) == _lib.MK_OK
+    assert lib.mk_plan_destroy(None) == _lib.MK_OK
+    shape = (C.c_int64 * 2)(4, 8)
+    assert lib.mk_add_tensor(None, P(0x1000), _lib.MK_BF16, 2, shape, None, C.byref(i32)) == bad
+    assert lib.mk_add_view(None, 0, 0, 0, 1, 1, C.byref(i32)) == bad
+    assert lib.mk_add_transient(None, _lib.MK_BF16, 4, 8, C.byref(i32)) == bad
+    assert lib.mk_add_matmul(None, 0, 1, 2, None, C.byref(i32)) == bad
+    assert lib.mk_add_elementwise(None, _lib.EW_RELU, buf, 1, 0, None, C.byref(i32)) == bad
+    assert lib.mk_add_attention(None, 0, 1, 2, 3, None, C.byref(i32)) == bad
+    assert lib.mk_compile(None, None, C.byref(P())) == bad
+    assert lib.mk_run(None, None) == bad
+    assert lib.mk_run_host(None, None, 0, None) == bad
+    assert lib.mk_sync_status(None, C.byref(ds)) == bad
+    assert lib.mk_plan_repack(None, None) == bad
+    assert lib.mk_plan_stats(None, C.byref(st)) == bad
+    assert lib.mk_plan_tensor_ptr(None, 0, C.byref(P())) == bad
+    assert lib.mk_get_instructions(None, buf, 16) == bad
+    assert lib.mk_get_src_list(None, buf, 4) == bad
+    assert lib.mk_get_dst_list(None, buf, 4) == bad
+    assert lib.mk_get_counter_targets(None, buf, 4) == bad
+    assert lib.mk_get_counters(None, buf, 4) == bad
+    assert lib.mk_get_trace(None, (C.c_uint64 * 8)(), 8) == bad
+    assert lib.mk_default_opts(None) == bad
+    # the allocation-free GEMV checks its arguments before looking for a device
+    assert lib.mk_gemv_noalloc(None, None, None, 1, 256, 64, _lib.MK_BF16, None, None) == bad
+    assert lib.mk_gemv_noalloc(None, None, None, 9, 256, 64, _lib.MK_BF16, None, None) == \
+        _lib.MK_ERR_UNSUPPORTED
+    assert lib.mk_last_error()  # the last failure left a message
+
+
+def test_dry_plan_getters_check_buffer_sizes():
+    g, _ = workloads.build_graph(workloads.mlp3(m=256, h=256).desc, None)
+    p = g.compile(dry_run=1, n_sm=4, gemm_tile_n=64)
+    n = p.stats()["n_instr"]
+    from tensor_core_gemm_gb300.api import INSTR_DTYPE
+    small = np.zeros(max(1, n - 1), dtype=INSTR_DTYPE)
+    with pytest.raises(MkError):
+        _lib.check(p._lib.mk_get_instructions(p._h, small.ctypes.data_as(C.c_void_p),
+                                              small.nbytes))
+    targets = p.counter_targets()
+    assert len(targets) > 1
+    with pytest.raises(MkError):
+        buf = np.zeros(1, dtype=np.int32)
+        _lib.check(p._lib.mk_get_counter_targets(p._h, buf.ctypes.data_as(C.POINTER(C.c_int32)),
+                                                 max(0, len(targets) - 1)))
