@@ -13,12 +13,16 @@
  *    "Dispatcher, JIT and launch", §11 "The TMEM token and global barriers"
  *  - the GEMM tile (TMA, mbarriers, TMEM, tcgen05): "Hand-writing a Blackwell GEMM", steps 1-8
  *  - split-KV attention partial + combine: "Implementing a Mega Kernel for B300", §2 and §8
+ *  - buffer pool with reuse counters for plan-owned intermediates: "MegaKittens Internals", §04
+ *    phase 2 and phase 3 (reuse barriers)
  *
  * Conventions
  *  - Every function returns an mk_status; MK_OK is 0. On failure mk_last_error() returns a
  *    message (thread-local, valid until the next call on the same thread). No function aborts.
- *  - Tensors are caller-owned device memory, registered by pointer. The library never frees
- *    or allocates them. A plan is bound to the pointers given at compile time.
+ *  - Tensors registered with mk_add_tensor are caller-owned device memory, registered by
+ *    pointer; the library never frees or allocates them, and a plan is bound to the pointers
+ *    given at compile time. Transients (mk_add_transient) are plan-owned: they live in the
+ *    plan's buffer pool.
  *  - Tensor ids and node ids are small non-negative integers local to one graph.
  *  - Element types: MK_F16 (IEEE half), MK_BF16 (bfloat16), MK_F32; MK_I32 for the indices an
  *    ARGMAX node writes.
@@ -229,8 +233,9 @@ typedef struct {
 mk_status mk_default_opts(mk_compile_opts* o);
 
 /* Lower the graph and, unless dry_run, upload the plan to the device: instruction list, node
- * table, dependency lists, tensor maps, counters, scratch and status word (plan-owned). The
- * graph may be destroyed afterwards. */
+ * table, dependency lists, tensor maps, counters, scratch, status word, packed GEMV weight copies
+ * (gemv_pack) and the transients' buffer pool, all in one plan-owned allocation. The graph may
+ * be destroyed afterwards. */
 mk_status mk_compile(mk_graph_t g, const mk_compile_opts* opts, mk_plan_t* out);
 
 /* Enqueue one run on `stream` (a cudaStream_t; NULL = legacy default stream): ONE persistent
