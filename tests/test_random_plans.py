@@ -80,3 +80,30 @@ def test_random_plan_matches_oracle(seed):
     desc = _random_graph(rng)
     opts = _random_opts(rng)
     assert_same_plan(desc, opts)
+
+
+@pytest.mark.parametrize("seed", range(60))
+def test_random_decoder_plan_matches_oracle(seed):
+    # Decoder graphs (split-KV decode with optional sampling head, causal prefill) of random
+    # shapes: attention lowering (key chunks, prefill query tiles, GQA ratios, ragged token
+    # counts), the RoPE and combine fusions, wave packing of attention phases and pooled
+    # intermediates, against the oracle schedule.
+    from tensor_core_gemm_gb300 import workloads
+    rng = np.random.default_rng(5000 + seed)
+    hkv = int(rng.choice([1, 2, 4]))
+    hq = hkv * int(rng.choice([1, 2, 4]))
+    sh = workloads.DecoderShape(layers=int(rng.integers(1, 4)), hidden=int(rng.choice([128, 256])),
+                                n_q_heads=hq, n_kv_heads=hkv, head_dim=64,
+                                ffn=int(rng.choice([256, 512])))
+    if rng.random() < 0.5:
+        wl = workloads.decode(sh, kv_len=int(rng.choice([1, 17, 100, 300])),
+                              vocab=int(rng.choice([0, 0, 1000])))
+    else:
+        wl = workloads.prefill(sh, tokens=int(rng.choice([64, 130, 256, 384])))
+    if rng.random() < 0.4:
+        wl = workloads.with_transients(wl, *workloads.decoder_intermediates(wl))
+    opts = dict(n_sm=int(rng.choice([8, 37, 152])), attn_chunk=int(rng.choice([16, 64])),
+                fuse_rope=int(rng.integers(0, 2)), fuse_attn_reduce=int(rng.integers(0, 2)),
+                wave_pack=int(rng.integers(0, 2)), gemm_group_m=int(rng.choice([1, 8])),
+                gemv_splits=int(rng.choice([0, 2])), norm_rows=int(rng.choice([4, 16])))
+    assert_same_plan(wl.desc, opts)
