@@ -9,6 +9,7 @@ import numpy as np
 import pytest
 import torch
 
+import _drift
 import _graphs
 from oracle import models, ops
 from oracle import schedule as osched
@@ -451,11 +452,14 @@ def test_decode_full_config():
     plan, _ = run(wl)
     check_counters(plan, wl, {})
     check_decode_per_node(wl, kc0, vc0)
-    # end to end: within twice the oracle-vs-oracle drift of the same depth (1.4e-2)
+    # End to end: two valid summation orders of the oracle itself drift apart by ~1.4e-2
+    # relative Frobenius over 16 bf16 layers (tests/test_oracle_drift.py); the drift is measured
+    # here on these very inputs and the GPU held to MARGIN times it.
     wts, _, _, p = _decode_ref(wl)
-    ref, _, _ = models.decode_step(x0, wts, list(kc0), list(vc0), p)
+    drift, ref = _drift.decode_drift(x0, wts, list(kc0), list(vc0), p)
     got = f32(wl.data[wl.info["out"]])[-1:]
-    assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= 3e-2
+    ok, seen = _drift.within_drift(got, ref, drift)
+    assert ok, f"16-layer decode: gap {seen} against oracle drift {drift}"
 
 
 # ------------------------------------------------------------------ runtime behaviour
@@ -782,6 +786,16 @@ def test_prefill_full_config_causal_prefix():
     plan, _ = run(wl)
     check_counters(plan, wl, {})
     check_prefill_per_node(wl, 256)
+    # End to end over all 16 layers: rows 0..255 of the last layer's output depend only on the
+    # first 256 tokens, so the oracle runs the whole decoder on that prefix. Held to MARGIN
+    # times the oracle-vs-oracle drift measured on the same prefix (~1.7e-2 after 16 layers,
+    # tests/test_oracle_drift.py).
+    sh, T = wl.info["shape"], wl.info["tokens"]
+    rows = 256
+    drift, ref = _drift.prefill_drift(f32(wl.data[0])[:rows], _prefill_weights(wl))
+    got = f32(wl.data[wl.info["out"]]).reshape(sh.layers, T, -1)[-1, :rows]
+    ok, seen = _drift.within_drift(got, ref, drift)
+    assert ok, f"16-layer prefill prefix: gap {seen} against oracle drift {drift}"
 
 
 # ------------------------------------------------------------------ GEMM split tails
