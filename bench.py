@@ -1,9 +1,14 @@
 """Benchmark of the persistent megakernel (one JSON line on rank 0).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mk|reference] [--config NAME]
+                    [--only]
 
 Default workload: the single fp16 GEMM C = A @ B, M = N = K = 4096 (A, B ~N(0, 1/64)), one
-megakernel launch per step. Other workloads (--config): mlp3, llama_prefill, llama_decode,
+megakernel launch per step; its figures are the line's top-level keys. The default run then
+measures the rest of the suite the same way in the same process (batch-1 decode of the
+16-layer decoder in us/token and HBM GB/s, its 2048-token causal prefill, the Llama-70B prefill
+and decode linear lists, the 3-layer MLP) and nests each record under "configs". Other
+workloads alone (--config, or --only for the GEMM alone): mlp3, llama_prefill, llama_decode,
 decode, prefill, and decode_sample (decode followed by greedy sampling over a 128256-token
 vocabulary).
 
@@ -325,43 +330,21 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
-def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--impl", default="mk", choices=["mk", "reference"])
-    ap.add_argument("--config", default="gemm4096", choices=sorted(CONFIGS))
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--opt", action="append", default=[], metavar="KEY=INT",
-                    help="override a compile option of the workload, e.g. --opt cluster=2")
-    args = ap.parse_args()
-    if args.warmup < 3:
-        args.warmup = 3
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if args.impl == "reference":
-        run_reference(args, world, rank)
-        return
+# The default run times the headline workload, then every other workload of the suite, each
+# measured the same way in the same process; their records nest under "configs".
+SUITE = ("decode", "prefill", "llama_prefill", "llama_decode", "mlp3")
 
+
+def measure(name, args, world, rank, local, dev, barrier, opt_overrides=()):
+    """One workload through the megakernel: W warm-up runs, K timed runs (CUDA events on the
+    launch stream, L2 flushed before each), the end-to-end runs through host buffers, clocks
+    sampled during the timed region, and (rank 0, one GPU) the oracle on a bounded sample.
+    Returns the JSON record (without the run-level keys n_gpus / steps / warmup)."""
     import torch
-    import torch.distributed as dist
     from tensor_core_gemm_gb300 import workloads as W
-    from tensor_core_gemm_gb300 import _lib
 
-    torch.cuda.set_device(local)
-    dev = f"cuda:{local}"
-    if world > 1:
-        dist.init_process_group("nccl", device_id=torch.device(dev))
-
-    def barrier():
-        if world > 1:
-            dist.barrier()
-
-    _lib.load()
-    wl, opts = make_workload(args.config, dev)
-    for kv in args.opt:
+    wl, opts = make_workload(name, dev)
+    for kv in opt_overrides:
         k, v = kv.split("=", 1)
         opts[k] = int(v)
     g, id_of = W.build_graph(wl.desc, wl.data)
@@ -395,10 +378,13 @@ def main():
 
     # End to end through the C ABI with host buffers (pinned), copies inside the timed region.
     ins, outs = io_tensors(wl)
-    host_in = [(id_of((t, 0, 0, wl.desc["tensors"][t]["rows"], wl.desc["tensors"][t]["cols"])),
-                wl.data[t].cpu().pin_memory()) for t in ins]
-    host_out = [(id_of((t, 0, 0, wl.desc["tensors"][t]["rows"], wl.desc["tensors"][t]["cols"])),
-                 torch.empty_like(wl.data[t], device="cpu").pin_memory()) for t in outs]
+
+    def ref_of(t):
+        return id_of((t, 0, 0, wl.desc["tensors"][t]["rows"], wl.desc["tensors"][t]["cols"]))
+
+    host_in = [(ref_of(t), wl.data[t].cpu().pin_memory()) for t in ins]
+    host_out = [(ref_of(t), torch.empty_like(wl.data[t], device="cpu").pin_memory())
+                for t in outs]
     h2d = sum(h.numel() * h.element_size() for _, h in host_in)
     d2h = sum(h.numel() * h.element_size() for _, h in host_out)
     e_in = [(tid, h.data_ptr()) for tid, h in host_in]
@@ -417,9 +403,9 @@ def main():
     plan.check_status()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
 
-    metric, unit, hib = metric_of(args.config)
-    value = job_value(value_of(wl, ms, args.config), unit, world)
-    e2e_value = job_value(value_of(wl, e2e_ms, args.config), unit, world)
+    metric, unit, hib = metric_of(name)
+    value = job_value(value_of(wl, ms, name), unit, world)
+    e2e_value = job_value(value_of(wl, e2e_ms, name), unit, world)
     peaks, peak_src = load_peaks()
     bound = binding_roof(wl, peaks)
     # fp16 and bf16 have the same dense tensor rate
@@ -429,37 +415,90 @@ def main():
     other = "hbm" if bound == "tensor" else "tensor"
     secondary = {"bound": other, "achieved": roofs[other][0], "peak": roofs[other][1],
                  "unit": roofs[other][2], "frac": roofs[other][0] / roofs[other][1]}
-    traffic = profiled_traffic(args.config)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, sample = oracle_sample(args.config)
+        v, sample = oracle_sample(name)
         cpu = {"value": v, "unit": unit, "cores": CORES, "kind": "oracle", "sample": sample}
 
+    st = plan.stats()
+    dtype = "bf16" if name in ("decode", "prefill", "decode_sample") else "f16"
+    rec = {
+        "metric": metric, "value": value, "unit": unit, "ms_per_step": ms,
+        "higher_is_better": hib, "scaling": "weak", "vs_baseline": None, "dtype": dtype,
+        "data": "synthetic",
+        "config": {"workload": CONFIGS[name],
+                   "l2": "flushed before every timed run (256 MB device write)",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "instructions": st["n_instr"], "waves_per_sm": round(st["waves"], 3),
+                   "kernel_set": KERNEL_SETS[st["kernel_set"]], "compile_opts": opts},
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": runit,
+                     "frac": achieved / peak, "traffic": profiled_traffic(name),
+                     "peak_source": f"{peak_src} "
+                                    f"({'bf16_tflops' if bound == 'tensor' else 'hbm_gbs'})",
+                     "secondary": secondary},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps,
+        "clocks": clock_info,
+    }
+    if unit == "us/token":   # the decode metric's other half: HBM GB/s of the token
+        rec["hbm_gbs"] = roofs["hbm"][0]
+    del plan, g, wl, flush, host_in, host_out
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return rec
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="mk", choices=["mk", "reference"])
+    ap.add_argument("--config", default="gemm4096", choices=sorted(CONFIGS))
+    ap.add_argument("--only", action="store_true",
+                    help="time the named workload alone (the default run adds the others)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--opt", action="append", default=[], metavar="KEY=INT",
+                    help="override a compile option of the workload, e.g. --opt cluster=2")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+
+    import torch
+    import torch.distributed as dist
+    from tensor_core_gemm_gb300 import _lib
+
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device(dev))
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    _lib.load()
+    rec = measure(args.config, args, world, rank, local, dev, barrier, args.opt)
+    line = {"metric": rec["metric"], "value": rec["value"], "unit": rec["unit"],
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup}
+    line.update({k: v for k, v in rec.items() if k not in line})
+    if args.config == "gemm4096" and not args.only and not args.opt:
+        line["configs"] = {}
+        for name in SUITE:
+            try:
+                line["configs"][name] = measure(name, args, world, rank, local, dev, barrier)
+            except Exception as e:  # a failure of one workload leaves the others' records
+                line["configs"][name] = {"error": f"{type(e).__name__}: {e}"}
     if rank == 0:
-        dtype = "bf16" if args.config in ("decode", "prefill", "decode_sample") else "f16"
-        line = {
-            "metric": metric, "value": value, "unit": unit, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-            "higher_is_better": hib, "scaling": "weak", "vs_baseline": None, "dtype": dtype,
-            "data": "synthetic",
-            "config": {"workload": CONFIGS[args.config],
-                       "l2": "flushed before every timed run (256 MB device write)",
-                       "parallelism": "replicas" if world > 1 else "single GPU",
-                       "instructions": plan.stats()["n_instr"],
-                       "waves_per_sm": round(plan.stats()["waves"], 3),
-                       "kernel_set": KERNEL_SETS[plan.stats()["kernel_set"]],
-                       "compile_opts": opts},
-            "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": runit,
-                         "frac": achieved / peak, "traffic": traffic,
-                         "peak_source": f"{peak_src} ({'bf16_tflops' if bound == 'tensor' else 'hbm_gbs'})",
-                         "secondary": secondary},
-            "cpu_baseline": cpu,
-            "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
-            "gpu_launches": args.steps,
-            "clocks": clock_info,
-        }
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
