@@ -299,8 +299,11 @@ mk_status mk_plan_destroy(mk_plan_t p);
  * The first call on each device, with that device current, looks up the array's device address
  * (cudaGetSymbolAddress) and sets the kernel's shared-memory limit; make that first call before
  * any stream capture. Every call shares the array and clears the parts that must start at zero;
- * the rest keeps the previous call's contents. Calls that overlap on the GPU (different
- * streams, or host threads calling at once) race on the array and must not be issued. */
+ * the rest keeps the previous call's contents. A call writes its records into the array with a
+ * small set-up kernel that receives them by value, so it reads no host buffer after it returns
+ * and calls from different host threads share no host state. Calls on one stream run one after
+ * the other; calls that can overlap on the same device (different streams, or host threads
+ * calling at once for that device) race on that device's array and must not be issued. */
 mk_status mk_gemv_noalloc(const void* x, const void* w, void* out, int32_t m, int32_t n,
                           int32_t k, int32_t dtype, void* stream, mk_device_status* status);
 

@@ -7,11 +7,15 @@
 // where cudaMalloc / cudaFree would synchronise the device. mk_compile allocates a plan; this
 // entry point allocates nothing. It calls no cudaMalloc, cudaFree or allocating library
 // routine: the instruction records, node entry, tensor map, split semaphores, status words and
-// fp32 split partials all live in g_noalloc_scratch below.
+// fp32 split partials all live in g_noalloc_scratch below. A small set-up kernel, given the
+// records by value, writes them there before each run, so the call reads no host buffer after
+// it returns.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 #include <string.h>
+
+#include <algorithm>
 
 #include "mk_internal.h"
 #include "mk_launch.h"
@@ -39,13 +43,52 @@ static_assert(kOffPart < kScratchBytes, "layout fits");
 constexpr int kTileN = 256;     // output columns per GEMV tile
 constexpr int kKStep = kGemvRows;  // K chunks are multiples of the stage depth
 
-// Host staging for the records copied into the array on every call (no heap use).
-Instr h_instr[kMaxInstr];
-Node h_node;
-CUtensorMap h_map;
-
 constexpr int kMaxDevices = 64;
 char* g_scratch_dev[kMaxDevices];  // device address of the array, per device (set up once)
+
+// Everything a call writes into the array, passed to the set-up kernel by value: kernel
+// parameters are copied when the launch is enqueued, so no host buffer is read after the call
+// returns and calls from several host threads share no host state.
+struct SetupArgs {
+  CUtensorMap map;   // 64-byte aligned first member
+  Node node;
+  char* base;        // device address of the array
+  int32_t tiles, splits, chunk, k, has_map;
+};
+
+// One CTA of 256 threads: the instruction records (one GEMV per column tile and K split, the
+// same order and fields a compiled plan uses), the node entry, the tensor map, and zeros over
+// the split semaphores, status words and CTA completion count.
+__global__ void __launch_bounds__(256) noalloc_setup(const __grid_constant__ SetupArgs a) {
+  Instr* ins = reinterpret_cast<Instr*>(a.base + kOffInstr);
+  const int n = a.tiles * a.splits;
+  for (int i = (int)threadIdx.x; i < n; i += (int)blockDim.x) {
+    const int ct = i / a.splits, si = i % a.splits;
+    Instr r;
+    memset(&r, 0, sizeof r);
+    r.op = OP_GEMV;
+    r.n0 = ct * kTileN;
+    r.k0 = si * a.chunk;
+    r.klen = min(a.chunk, a.k - si * a.chunk);
+    r.aux0 = si;
+    r.aux1 = a.splits;
+    r.sem = ct;
+    ins[i] = r;
+  }
+  const uint32_t* nsrc = reinterpret_cast<const uint32_t*>(&a.node);
+  uint32_t* ndst = reinterpret_cast<uint32_t*>(a.base + kOffNode);
+  for (int i = (int)threadIdx.x; i < (int)(sizeof(Node) / 4); i += (int)blockDim.x)
+    ndst[i] = nsrc[i];
+  if (a.has_map) {
+    const uint32_t* msrc = reinterpret_cast<const uint32_t*>(&a.map);
+    uint32_t* mdst = reinterpret_cast<uint32_t*>(a.base + kOffMap);
+    for (int i = (int)threadIdx.x; i < (int)(sizeof(CUtensorMap) / 4); i += (int)blockDim.x)
+      mdst[i] = msrc[i];
+  }
+  uint32_t* z = reinterpret_cast<uint32_t*>(a.base + kOffCtr);
+  for (int i = (int)threadIdx.x; i < (int)((kOffPart - kOffCtr) / 4); i += (int)blockDim.x)
+    z[i] = 0u;
+}
 
 }  // namespace
 
@@ -109,36 +152,32 @@ extern "C" mk_status mk_gemv_noalloc(const void* x, const void* w, void* out, in
     s = s - 1;
   }
 
-  // Records: one GEMV instruction per (column tile, split); no dependencies between them.
-  int ni = 0;
-  for (int64_t ct = 0; ct < tiles; ++ct) {
-    for (int64_t si = 0; si < s; ++si) {
-      Instr& in = h_instr[ni++];
-      memset(&in, 0, sizeof in);
-      in.op = OP_GEMV;
-      in.n0 = (int32_t)(ct * kTileN);
-      in.k0 = (int32_t)(si * chunk);
-      in.klen = (int32_t)std::min<int64_t>(chunk, (int64_t)k - si * chunk);
-      in.aux0 = (int32_t)si;
-      in.aux1 = (int32_t)s;
-      in.sem = (int32_t)ct;
-    }
-  }
-  memset(&h_node, 0, sizeof h_node);
-  h_node.kind = OP_GEMV;
-  h_node.dtype = dtype;
-  h_node.M = m;
-  h_node.N = n;
-  h_node.K = k;
-  h_node.tile_n = kTileN;
-  h_node.n_splits = (int32_t)s;
-  h_node.ldp = m * n;
-  h_node.a = Operand{(uint64_t)(uintptr_t)x, k, -1};
-  h_node.b = Operand{(uint64_t)(uintptr_t)w, n, k > 0 ? 0 : -1};
-  h_node.out = Operand{(uint64_t)(uintptr_t)out, n, -1};
-  h_node.scratch = Operand{(uint64_t)(uintptr_t)(base + kOffPart), 0, -1};
-  h_node.b2.tmap = h_node.bias.tmap = h_node.res.tmap = h_node.gamma.tmap = -1;
-  h_node.out_k.tmap = h_node.out_v.tmap = -1;
+  // Records: one GEMV instruction per (column tile, split), no dependencies between them,
+  // written on the device by the set-up kernel from the arguments below.
+  SetupArgs sa;
+  memset(&sa, 0, sizeof sa);
+  sa.base = base;
+  sa.tiles = (int32_t)tiles;
+  sa.splits = (int32_t)s;
+  sa.chunk = (int32_t)chunk;
+  sa.k = k;
+  sa.has_map = k > 0;
+  const int ni = (int)(tiles * s);
+  Node& nd = sa.node;
+  nd.kind = OP_GEMV;
+  nd.dtype = dtype;
+  nd.M = m;
+  nd.N = n;
+  nd.K = k;
+  nd.tile_n = kTileN;
+  nd.n_splits = (int32_t)s;
+  nd.ldp = m * n;
+  nd.a = Operand{(uint64_t)(uintptr_t)x, k, -1};
+  nd.b = Operand{(uint64_t)(uintptr_t)w, n, k > 0 ? 0 : -1};
+  nd.out = Operand{(uint64_t)(uintptr_t)out, n, -1};
+  nd.scratch = Operand{(uint64_t)(uintptr_t)(base + kOffPart), 0, -1};
+  nd.b2.tmap = nd.bias.tmap = nd.res.tmap = nd.gamma.tmap = -1;
+  nd.out_k.tmap = nd.out_v.tmap = nd.out_q.tmap = -1;
   if (k > 0) {
     void* fnp = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -151,26 +190,21 @@ extern "C" mk_status mk_gemv_noalloc(const void* x, const void* w, void* out, in
     cuuint64_t strides[1] = {(cuuint64_t)n * 2};
     cuuint32_t box[2] = {64u, (cuuint32_t)kGemvRows};  // four 64-column boxes per stage
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = encode(&h_map, dtype == MK_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                                 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+    CUresult r = encode(&sa.map, dtype == MK_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                  : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                         2, const_cast<void*>(w), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(MK_ERR_CUDA, "cuTensorMapEncodeTiled failed");
   }
 
-  // Upload the records (from static host memory) and clear what must start at zero: the split
-  // semaphores, the status words and the CTA completion count. The array keeps the last call's
-  // contents otherwise.
+  // Write the records into the array and clear what must start at zero (the split
+  // semaphores, the status words and the CTA completion count); the array keeps the previous
+  // call's contents otherwise.
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  e = cudaMemcpyAsync(base + kOffInstr, h_instr, (size_t)ni * sizeof(Instr),
-                      cudaMemcpyHostToDevice, st);
-  if (e == cudaSuccess)
-    e = cudaMemcpyAsync(base + kOffNode, &h_node, sizeof h_node, cudaMemcpyHostToDevice, st);
-  if (e == cudaSuccess && k > 0)
-    e = cudaMemcpyAsync(base + kOffMap, &h_map, sizeof h_map, cudaMemcpyHostToDevice, st);
-  if (e == cudaSuccess) e = cudaMemsetAsync(base + kOffCtr, 0, kOffPart - kOffCtr, st);
-  if (e != cudaSuccess) return fail(MK_ERR_CUDA, "upload into the scratch array", e);
+  noalloc_setup<<<1, 256, 0, st>>>(sa);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(MK_ERR_CUDA, "set-up launch", e);
 
   Params p{};
   p.instrs = reinterpret_cast<const Instr*>(base + kOffInstr);
