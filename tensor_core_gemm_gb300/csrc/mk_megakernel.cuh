@@ -1846,164 +1846,77 @@ __device__ void ew_body(const Instr& in, const Node& nd) {
   }
 }
 
-// RMSNorm rows of one instruction (tile_m rows from m0), one warp per row. Rows of up to
-// 32 * kRowVec * 8 elements stay in registers between the statistic and the scaling, and all
-// loads of a row are issued before any is used; longer rows take the two-pass loop, and so does
-// COMPACT: every specialisation but the prefill one, whose registers are tuned for other paths
-// (the decode one meets row instructions only in plans that do not fuse them into GEMV tiles).
-constexpr int kRowVec = 8;  // 16-byte vectors per lane of a register-resident row (2048 elements)
-template <bool COMPACT>
+// RMSNorm rows of one instruction (tile_m rows from m0), one warp per row, read directly from
+// global memory: a pass for the statistic, then a pass that scales by rstd and gamma. Lane l
+// takes the 16-byte vectors l, l + 32, ... of the row (the summation order the staged form
+// keeps too).
 __device__ __forceinline__ void rmsnorm_body(const Instr& in, const Node& nd) {
   const int ct = (int)threadIdx.x - (kThreads - kCompute);
   const int wp = ct >> 5, lane = ct & 31;
-  const int rows = min(nd.tile_m, nd.M - in.m0), dt = nd.dtype, N = nd.N, nv = N / 8;
+  const int rows = min(nd.tile_m, nd.M - in.m0), dt = nd.dtype, N = nd.N;
   const float eps = nd.eps;
-  if (COMPACT || nv > 32 * kRowVec) {
-    for (int r = wp; r < rows; r += 4) {
-      const int m = in.m0 + r;
-      float ss = 0.f;
-      for (int k = lane * 8; k < N; k += 256) {
-        float x[8];
-        load8(nd.a, m, k, dt, x);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) ss += x[e] * x[e];
-      }
-      const float rstd = rsqrtf(warp_sum(ss) / (float)N + eps);
-      for (int k = lane * 8; k < N; k += 256) {
-        float x[8], g[8];
-        load8(nd.a, m, k, dt, x);
-        load8(nd.gamma, 0, k, dt, g);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] = x[e] * rstd * g[e];
-        store8(nd.out, m, k, dt, x);
-      }
-    }
-    return;
-  }
-  const uint16_t* a = reinterpret_cast<const uint16_t*>(nd.a.ptr);
-  const uint16_t* gm = reinterpret_cast<const uint16_t*>(nd.gamma.ptr);
-  uint16_t* out = reinterpret_cast<uint16_t*>(nd.out.ptr);
-  const size_t lda = (size_t)nd.a.ld, ldo = (size_t)nd.out.ld;
-  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
   for (int r = wp; r < rows; r += 4) {
-    uint4 x[kRowVec];
-#pragma unroll
-    for (int j = 0; j < kRowVec; ++j) {
-      const int v = lane + 32 * j;
-      x[j] = v < nv ? __ldcg(reinterpret_cast<const uint4*>(a + (in.m0 + r) * lda + v * 8)) : zero;
-    }
+    const int m = in.m0 + r;
     float ss = 0.f;
+    for (int k = lane * 8; k < N; k += 256) {
+      float x[8];
+      load8(nd.a, m, k, dt, x);
 #pragma unroll
-    for (int j = 0; j < kRowVec; ++j) {
-      if (lane + 32 * j >= nv) continue;
-      float xf[8];
-      unpack8(x[j], dt, xf);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) ss += xf[e] * xf[e];
+      for (int e = 0; e < 8; ++e) ss += x[e] * x[e];
     }
     const float rstd = rsqrtf(warp_sum(ss) / (float)N + eps);
+    for (int k = lane * 8; k < N; k += 256) {
+      float x[8], g[8];
+      load8(nd.a, m, k, dt, x);
+      load8(nd.gamma, 0, k, dt, g);
 #pragma unroll
-    for (int j = 0; j < kRowVec; ++j) {
-      const int v = lane + 32 * j;
-      if (v >= nv) continue;
-      float xf[8], gf[8];
-      unpack8(x[j], dt, xf);
-      unpack8(__ldg(reinterpret_cast<const uint4*>(gm + v * 8)), dt, gf);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) xf[e] = xf[e] * rstd * gf[e];
-      *reinterpret_cast<uint4*>(out + (in.m0 + r) * ldo + v * 8) = pack8(xf, dt);
+      for (int e = 0; e < 8; ++e) x[e] = x[e] * rstd * g[e];
+      store8(nd.out, m, k, dt, x);
     }
   }
 }
 
-// RoPE rows: thread work item = (row, head, 8 consecutive pair indices); both halves of the
-// pairs arrive as 16-byte vectors and leave the same way. The cosine and sine of every
-// (row, pair index) of the instruction are computed once into shared memory (they do not depend
-// on the head), and each thread issues the loads of two items before it rotates either. COMPACT
-// (see rmsnorm_body) rotates item by item with the angles computed inline.
-template <bool COMPACT>
-__device__ __forceinline__ void rope_body(Smem& s, const Instr& in, const Node& nd) {
+// RoPE rows read directly from global memory: thread work item = (row, head, 8 consecutive
+// pair indices); both halves of the pairs arrive as 16-byte vectors and leave the same way, the
+// angles computed inline. The v heads, when the node copies them, follow as 16-byte copies.
+__device__ __forceinline__ void rope_body(const Instr& in, const Node& nd) {
   const int ct = (int)threadIdx.x - (kThreads - kCompute);
   const int rows = min(nd.tile_m, nd.M - in.m0), dt = nd.dtype;
   const int hd = nd.hd, half = hd / 2, nh = nd.hq + nd.hkv;
   const int groups = half / 8;                 // 8-pair groups per head
   const int items = nh * groups;
   const float l2t = log2f(nd.theta);
-  const bool table = !COMPACT && 2 * rows * half <= kXrFloats;
-  constexpr int B = COMPACT ? 1 : 2;  // items whose loads are in flight together
-  float* tcos = s.xr;
-  float* tsin = s.xr + rows * half;
-  if (table) {
-    for (int v = ct; v < rows * half; v += kCompute) {
-      const int r = v / half, i = v % half;
-      const float inv = exp2f(-(2.0f * (float)i / (float)hd) * l2t);
-      sincosf((float)(nd.pos0 + in.m0 + r) * inv, &tsin[v], &tcos[v]);
-    }
-    cw_sync();
-  }
   const uint16_t* a = reinterpret_cast<const uint16_t*>(nd.a.ptr);
   const size_t lda = (size_t)nd.a.ld;
   const int total = rows * items;
-  for (int v0 = ct; v0 < total; v0 += B * kCompute) {
-    uint4 r1[B], r2[B];
+  for (int v = ct; v < total; v += kCompute) {
+    const int m = in.m0 + v / items, it = v % items;
+    const int h = it / groups, i0 = (it % groups) * 8;
+    const uint16_t* src = a + m * lda + h * hd + i0;
+    float x1[8], x2[8], y1[8], y2[8];
+    unpack8(__ldcg(reinterpret_cast<const uint4*>(src)), dt, x1);
+    unpack8(__ldcg(reinterpret_cast<const uint4*>(src + half)), dt, x2);
+    const float pos = (float)(nd.pos0 + m);
 #pragma unroll
-    for (int u = 0; u < B; ++u) {
-      const int v = v0 + u * kCompute;
-      if (v >= total) continue;
-      const int m = in.m0 + v / items, it = v % items;
-      const uint16_t* src = a + m * lda + (it / groups) * hd + (it % groups) * 8;
-      r1[u] = __ldcg(reinterpret_cast<const uint4*>(src));
-      r2[u] = __ldcg(reinterpret_cast<const uint4*>(src + half));
+    for (int e = 0; e < 8; ++e) {
+      float sn, cs;
+      const float inv = exp2f(-(2.0f * (float)(i0 + e) / (float)hd) * l2t);
+      sincosf(pos * inv, &sn, &cs);
+      y1[e] = x1[e] * cs - x2[e] * sn;
+      y2[e] = x2[e] * cs + x1[e] * sn;
     }
-#pragma unroll
-    for (int u = 0; u < B; ++u) {
-      const int v = v0 + u * kCompute;
-      if (v >= total) continue;
-      const int r = v / items, m = in.m0 + r, it = v % items;
-      const int h = it / groups, i0 = (it % groups) * 8;
-      float x1[8], x2[8], y1[8], y2[8];
-      unpack8(r1[u], dt, x1);
-      unpack8(r2[u], dt, x2);
-      const float pos = (float)(nd.pos0 + m);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        float sn, cs;
-        if (table) {
-          cs = tcos[r * half + i0 + e];
-          sn = tsin[r * half + i0 + e];
-        } else {
-          const float inv = exp2f(-(2.0f * (float)(i0 + e) / (float)hd) * l2t);
-          sincosf(pos * inv, &sn, &cs);
-        }
-        y1[e] = x1[e] * cs - x2[e] * sn;
-        y2[e] = x2[e] * cs + x1[e] * sn;
-      }
-      const Operand& o = h < nd.hq ? nd.out : nd.out_k;
-      const int hh = h < nd.hq ? h : h - nd.hq;
-      store8(o, m, hh * hd + i0, dt, y1);
-      store8(o, m, hh * hd + i0 + half, dt, y2);
-    }
+    const Operand& o = h < nd.hq ? nd.out : nd.out_k;
+    const int hh = h < nd.hq ? h : h - nd.hq;
+    store8(o, m, hh * hd + i0, dt, y1);
+    store8(o, m, hh * hd + i0 + half, dt, y2);
   }
   if (nd.out_v.ptr) {
     const int nvv = nd.hkv * hd / 8, tv = rows * nvv;
-    constexpr int BV = COMPACT ? 1 : 4;
-    for (int v0 = ct; v0 < tv; v0 += BV * kCompute) {
-      uint4 x[BV];
-#pragma unroll
-      for (int u = 0; u < BV; ++u) {
-        const int v = v0 + u * kCompute;
-        if (v < tv)
-          x[u] = __ldcg(reinterpret_cast<const uint4*>(
-              a + (in.m0 + v / nvv) * lda + nh * hd + (v % nvv) * 8));
-      }
-#pragma unroll
-      for (int u = 0; u < BV; ++u) {
-        const int v = v0 + u * kCompute;
-        if (v < tv)
-          *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(nd.out_v.ptr) +
-                                    (size_t)(in.m0 + v / nvv) * nd.out_v.ld + (v % nvv) * 8) = x[u];
-      }
-    }
+    for (int v = ct; v < tv; v += kCompute)
+      *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(nd.out_v.ptr) +
+                                (size_t)(in.m0 + v / nvv) * nd.out_v.ld + (v % nvv) * 8) =
+          __ldcg(reinterpret_cast<const uint4*>(a + (in.m0 + v / nvv) * lda + nh * hd +
+                                                (v % nvv) * 8));
   }
 }
 
@@ -2569,8 +2482,8 @@ __device__ void run_compute(const Params& p, Smem& s, uint32_t tmem) {
         else if (ks_stages_rows(KS) && in.op == OP_ROPE && in.pad > 0)
           ok = rows_staged<true>(p, s, in, nd, ring, idx);
         else if (ks_has_rows(KS) && in.op == OP_EW) ew_body(in, nd);
-        else if (ks_has_rows(KS) && in.op == OP_RMSNORM) rmsnorm_body<true>(in, nd);
-        else if (ks_has_rows(KS) && in.op == OP_ROPE) rope_body<true>(s, in, nd);
+        else if (ks_has_rows(KS) && in.op == OP_RMSNORM) rmsnorm_body(in, nd);
+        else if (ks_has_rows(KS) && in.op == OP_ROPE) rope_body(in, nd);
         else if (ks_has_gemv(KS) && in.op == OP_ATTN_REDUCE) attn_reduce_body(in, nd);
         else if (ks_has_rows(KS) && in.op == OP_ARGMAX) argmax_partial_body(in, nd);
         else if (ks_has_rows(KS) && in.op == OP_ARGMAX_REDUCE) argmax_reduce_body(in, nd);

@@ -3,8 +3,9 @@
 // mk_compile uploads once: instruction list, node table, dependency lists, tensor maps and a
 // zero-initialised counter array ("Implementing a Mega Kernel for B300" §6 uploads descriptors
 // and a pointer table once; "MegaKittens Internals" §07 builds tensor maps on the host with
-// cuTensorMapEncodeTiled). Every mk_run zeroes the counters on the caller's stream and launches
-// the persistent kernel once (§07 "Every call: launch").
+// cuTensorMapEncodeTiled). Every mk_run launches the persistent kernel once on the caller's
+// stream (§07 "Every call: launch"); the counters need no reset per call, because the last CTA
+// of each run to finish zeroes them (and the run's other state) for the next run.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
