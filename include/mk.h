@@ -350,7 +350,9 @@ mk_status mk_get_counters(mk_plan_t p, int32_t* host_buf, size_t n);
  * for instruction i, buf[8i..8i+7] = {the compute warpgroup took the descriptor, the scheduler
  * saw every source counter complete, the compute warpgroup saw that, the instruction's body
  * ended, the instruction was published, the SM index, the accumulation ended (GEMM: the
- * accumulator is complete in tensor memory; GEMV: the last weight stage is consumed), 0}.
+ * accumulator is complete in tensor memory; GEMV: the last weight stage is consumed; split-KV
+ * partial: its partial is stored), and for a split-KV partial whose combine is fused the time
+ * its semaphore decided which partial combines (0 otherwise)}.
  * A slot an op does not reach stays 0. n >= 8 * n_instr; synchronises. */
 mk_status mk_get_trace(mk_plan_t p, uint64_t* host_buf, size_t n);
 

@@ -1536,6 +1536,30 @@ __device__ bool gemv_staged_rows(int M, const Params& p, uint32_t full0, uint32_
 // stage needs no cross-thread reduction. Weight stages arrive as 128-byte swizzled boxes:
 // unswizzled TMA writes of rows 128 bytes apart land on the same shared-memory banks ("Hand-
 // writing a Blackwell GEMM", step 4).
+// Sum of a column pair over the S split partials of a GEMV tile, in split order (the result
+// does not depend on which split finished last). Up to 24 partials are loaded at once, so the
+// usual split counts (at most 19 on 152 SMs) cost one round trip to L2 instead of one per few
+// partials.
+__device__ __noinline__ float2 sum_splits(const float* c0, int S, size_t ld) {
+  constexpr int B = 24;
+  float2 t = make_float2(0.f, 0.f);
+  for (int q0 = 0; q0 < S; q0 += B) {
+    float2 v[B];
+#pragma unroll
+    for (int u = 0; u < B; ++u)
+      v[u] = q0 + u < S ? __ldcg(reinterpret_cast<const float2*>(c0 + (size_t)(q0 + u) * ld))
+                        : make_float2(0.f, 0.f);
+#pragma unroll
+    for (int u = 0; u < B; ++u) {
+      if (q0 + u < S) {
+        t.x += v[u].x;
+        t.y += v[u].y;
+      }
+    }
+  }
+  return t;
+}
+
 template <bool PAIR>
 __device__ bool gemv(const Params& p, Smem& s, const Instr& in, const Node& nd, int slot,
                      uint32_t use, uint32_t& ring, bool* publish, int idx, uint32_t tmem,
@@ -1552,7 +1576,12 @@ __device__ bool gemv(const Params& p, Smem& s, const Instr& in, const Node& nd, 
   const int kpad = nk * kGemvRows;
   const int kend = in.k0 + in.klen;
   const bool staged = M * kpad <= kXrFloats;
-  if (norm) {
+  const bool tensor = gemv_on_tensor<PAIR>(in, nd);
+  // One row whose K range is at most one 16-byte item per thread (every decode GEMV): the loads
+  // for the RMS statistic, the K range and gamma are all issued before any is used, so staging
+  // waits on one round trip to L2 instead of two.
+  const bool onepass = tensor && M == 1 && kpad / 8 <= kCompute;
+  if (norm && !onepass) {
     // RMS statistic of each whole input row (the norm is a flag of this GEMV)
     for (int m = 0; m < M; ++m) {
       float ss = 0.f;
@@ -1594,8 +1623,72 @@ __device__ bool gemv(const Params& p, Smem& s, const Instr& in, const Node& nd, 
     }
     cw_sync();
   };
-  const bool tensor = gemv_on_tensor<PAIR>(in, nd);
-  if (tensor) {
+  const int which = dual ? (ct >> 6) : 0;
+  const int col = dual ? 2 * (ct & 63) : 2 * ct;  // column pair inside this thread's weight
+  // the residual pair of a one-row tile is read now, off the critical path of the last split
+  float res0 = 0.f, res1 = 0.f;
+  if (M == 1 && (nd.flags & EPI_RESIDUAL) && which == 0 && in.n0 + col < nd.N) {
+    res0 = load1(nd.res, 0, in.n0 + col, dt);
+    res1 = load1(nd.res, 0, in.n0 + col + 1, dt);
+  }
+  if (onepass) {
+    // the B operand as below (one 1 KB atom per 64-K block, chunk c of row 0 at c), one item
+    // per thread; the statistic's loads of the whole row go out together with it
+    uint8_t* xb = reinterpret_cast<uint8_t*>(s.xr);
+    const int kk = ct * 8, k = in.k0 + kk;
+    const bool item = kk < kpad, have = item && k < kend;
+    const uint16_t* xrow = reinterpret_cast<const uint16_t*>(nd.a.ptr);
+    uint4 xv = make_uint4(0u, 0u, 0u, 0u), gv = xv;
+    if (have) {
+      xv = __ldcg(reinterpret_cast<const uint4*>(xrow + k));
+      if (norm) gv = __ldcg(reinterpret_cast<const uint4*>(
+                    reinterpret_cast<const uint16_t*>(nd.gamma.ptr) + k));
+    }
+    float r = 1.f;
+    if (norm) {
+      constexpr int kRowItems = 4;  // rows up to 4 * 128 * 8 = 4096 elements in one round
+      uint4 rv[kRowItems];
+#pragma unroll
+      for (int u = 0; u < kRowItems; ++u) {
+        const int kr = (ct + u * kCompute) * 8;
+        rv[u] = kr < nd.K ? __ldcg(reinterpret_cast<const uint4*>(xrow + kr))
+                          : make_uint4(0u, 0u, 0u, 0u);
+      }
+      float ss = 0.f;
+#pragma unroll
+      for (int u = 0; u < kRowItems; ++u) {
+        float x[8];
+        unpack8(rv[u], dt, x);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+      }
+      for (int kr = (ct + kRowItems * kCompute) * 8; kr < nd.K; kr += kCompute * 8) {
+        float x[8];
+        load8(nd.a, 0, kr, dt, x);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+      }
+      ss = warp_sum(ss);
+      if (lane == 0) s.red_small[0][wp] = ss;
+      cw_sync();
+      r = rsqrtf((s.red_small[0][0] + s.red_small[0][1] + s.red_small[0][2] +
+                  s.red_small[0][3]) / (float)nd.K + nd.eps);
+    }
+    if (item) {
+      float x[8];
+      unpack8(xv, dt, x);
+      if (norm) {
+        float g[8];
+        unpack8(gv, dt, g);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = x[e] * r * g[e];
+      }
+      *reinterpret_cast<uint4*>(xb + (kk >> 6) * 1024 + (((kk & 63) >> 3) << 4)) = pack8(x, dt);
+    }
+    fence_proxy_async_shared();
+    cw_sync();
+    if (ct == 0) mbar_arrive(smem_u32(&s.gx_full));
+  } else if (tensor) {
     // the K-major B operand of the tensor-core tile: per 64-K block a 1 KB atom of 8 rows x 128
     // bytes, 16-byte chunk c of row m at c ^ m; the activations rounded to the weight type
     uint8_t* xb = reinterpret_cast<uint8_t*>(s.xr);
@@ -1625,8 +1718,6 @@ __device__ bool gemv(const Params& p, Smem& s, const Instr& in, const Node& nd, 
   } else if (staged && nk > 0) {
     stage_x(in.k0, kpad, kpad);
   }
-  const int which = dual ? (ct >> 6) : 0;
-  const int col = dual ? 2 * (ct & 63) : 2 * ct;  // column pair inside this thread's weight
   float acc[8][2];
 #pragma unroll
   for (int m = 0; m < 8; ++m) acc[m][0] = acc[m][1] = 0.f;
@@ -1732,25 +1823,7 @@ __device__ bool gemv(const Params& p, Smem& s, const Instr& in, const Node& nd, 
 #pragma unroll
       for (int m = 0; m < 8; ++m) {
         if (m >= M) continue;
-        const float* c0 = part + ((size_t)which * M + m) * nd.N + n;
-        float2 t = make_float2(0.f, 0.f);
-        int q = 0;
-        for (; q + 4 <= S; q += 4) {  // four loads in flight, summed in split order
-          float2 v[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            v[u] = __ldcg(reinterpret_cast<const float2*>(c0 + (size_t)(q + u) * nd.ldp));
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            t.x += v[u].x;
-            t.y += v[u].y;
-          }
-        }
-        for (; q < S; ++q) {
-          const float2 v = __ldcg(reinterpret_cast<const float2*>(c0 + (size_t)q * nd.ldp));
-          t.x += v.x;
-          t.y += v.y;
-        }
+        const float2 t = sum_splits(part + ((size_t)which * M + m) * nd.N + n, S, nd.ldp);
         acc[m][0] = t.x;
         acc[m][1] = t.y;
       }
@@ -1791,8 +1864,8 @@ __device__ bool gemv(const Params& p, Smem& s, const Instr& in, const Node& nd, 
         y1 = fmaxf(y1, 0.f);
       }
       if (nd.flags & EPI_RESIDUAL) {
-        y0 += load1(nd.res, m, n, dt);
-        y1 += load1(nd.res, m, n + 1, dt);
+        y0 += M == 1 ? res0 : load1(nd.res, m, n, dt);
+        y1 += M == 1 ? res1 : load1(nd.res, m, n + 1, dt);
       }
       store2(nd.out, m, n, dt, y0, y1);
       if (nd.flags & NF_ROPE) {
@@ -2228,14 +2301,47 @@ __device__ bool attn_partial_body(const Params& p, Smem& s, const Instr& in, con
 }
 
 // LSE merge of one kv group's partials: M = max m_c, L = sum l_c e^{m_c-M},
-// O = sum o_c e^{m_c-M} / L. Lanes hold chunks' statistics; value loads are batched by 8.
-__device__ void attn_reduce_body(const Instr& in, const Node& nd) {
+// O = sum o_c e^{m_c-M} / L, one warp per query head. Up to 32 chunks: chunk c's statistics in
+// lane c and every chunk's output pair of the lane's columns are loaded at once (one round trip
+// to L2), the weights e^{m_c-M} broadcast by shuffles. More chunks: lanes stride over the
+// chunks' statistics and value loads are batched by 8. Both sum in chunk order.
+__device__ __noinline__ void attn_reduce_body(const Instr& in, const Node& nd) {
   const int ct = (int)threadIdx.x - (kThreads - kCompute);
   const int wp = ct >> 5, lane = ct & 31;
   const int g = in.n0, G = nd.hq / nd.hkv, C = in.aux1;
   const float* sc = reinterpret_cast<const float*>(nd.scratch.ptr);
   const int ld = nd.scratch.ld;
-  for (int hh = wp; hh < G; hh += 4) {
+  for (int hh = wp; hh < G && C <= 32; hh += 4) {
+    const int h = g * G + hh;
+    auto row = [&](int c) { return sc + ((size_t)(g * C + c) * G + hh) * ld; };
+    float mc = -INFINITY, lc = 0.f;
+    if (lane < C) {
+      mc = __ldcg(row(lane) + 64);
+      lc = __ldcg(row(lane) + 65);
+    }
+    float2 ov[32];
+#pragma unroll
+    for (int u = 0; u < 32; ++u)
+      ov[u] = u < C ? __ldcg(reinterpret_cast<const float2*>(row(u) + lane * 2))
+                    : make_float2(0.f, 0.f);
+    const float mx = warp_max(mc);
+    const float w = lane < C ? expf(mc - mx) : 0.f;
+    const float L = warp_sum(lc * w);
+    float o0 = 0.f, o1 = 0.f;
+#pragma unroll
+    for (int u = 0; u < 32; ++u) {
+      const float wu = __shfl_sync(FULL, w, u);
+      if (u < C) {
+        o0 = fmaf(ov[u].x, wu, o0);
+        o1 = fmaf(ov[u].y, wu, o1);
+      }
+    }
+    const float inv = 1.0f / L;
+    const __nv_bfloat162 y = __floats2bfloat162_rn(o0 * inv, o1 * inv);
+    *reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(nd.out.ptr) + h * 64 +
+                                       lane * 2) = y;
+  }
+  for (int hh = wp; hh < G && C > 32; hh += 4) {
     const int h = g * G + hh;
     auto row = [&](int c) { return sc + ((size_t)(g * C + c) * G + hh) * ld; };
     float mx = -INFINITY;
@@ -2449,12 +2555,14 @@ __device__ void run_compute(const Params& p, Smem& s, uint32_t tmem) {
           ok = cw_wait(p, smem_u32(&s.deps_ready[slot]), use & 1u, 33, idx);
           trace_mark(p, idx, 2);
           ok = ok && attn_partial_body(p, s, in, nd, ring, idx);
+          trace_mark(p, idx, 6);
           if (ok && (nd.flags & NF_ATTN_FUSED)) {
             // the last partial of the key/value head to finish combines the head's partials
             __threadfence();
             cw_sync();
             if (ct == 0) s.flag = atomicAdd(p.counters + in.sem, 1) == in.aux1 - 1;
             cw_sync();
+            trace_mark(p, idx, 7);
             if (s.flag) {
               __threadfence();
               attn_reduce_body(in, nd);
