@@ -42,7 +42,7 @@
 extern "C" {
 #endif
 
-#define MK_ABI_VERSION 1
+#define MK_ABI_VERSION 2
 
 typedef struct mk_graph* mk_graph_t;
 typedef struct mk_plan* mk_plan_t;
@@ -186,8 +186,6 @@ typedef struct {
   int32_t debug_extra;
   int32_t snapshot_counters; /* 1: keep each run's final counter values for mk_get_counters */
   int32_t trace;         /* 1: record per-instruction timestamps for mk_get_trace */
-  int32_t l2_prefetch;   /* instructions (current included, <= 8) whose streamed operands the
-                            loader prefetches into L2 ahead of use; 0 = off */
   int32_t gemm_split_tail; /* 1: the GEMM tiles of a matmul's last, partly filled wave are
                             split along K, the last split to finish sums the fp32 partials
                             and runs the epilogue; 0 (default): never split. Measured slower

@@ -42,7 +42,7 @@ class CompileOpts(C.Structure):
         "n_sm", "gemm_tile_m", "gemm_tile_n", "cluster", "ew_rows", "ew_cols", "ew_tiles",
         "norm_rows", "gemv_max_m", "gemv_tile_n", "gemv_splits", "gemv_kstep", "attn_chunk",
         "attn_tile_q", "dry_run", "timeout_ms", "device", "debug_counter", "debug_extra",
-        "snapshot_counters", "trace", "l2_prefetch", "gemm_split_tail", "fuse_rope",
+        "snapshot_counters", "trace", "gemm_split_tail", "fuse_rope",
         "fuse_attn_reduce", "kernel_set", "gemv_pack", "argmax_chunk", "gemm_group_m",
         "wave_pack", "row_stage", "pool_waves")]
 

@@ -1097,7 +1097,6 @@ extern "C" mk_status mk_default_opts(mk_compile_opts* o) {
   o->debug_extra = 0;
   o->snapshot_counters = 0;
   o->trace = 0;
-  o->l2_prefetch = 0;
   o->gemm_split_tail = 0;
   o->fuse_rope = 1;
   o->fuse_attn_reduce = 1;

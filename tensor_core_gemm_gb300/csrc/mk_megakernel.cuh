@@ -550,8 +550,6 @@ __device__ bool load_gemm(const Params& p, Smem& s, const Instr& in, const Node&
   return ok;
 }
 
-__device__ void prefetch_ahead(const Params& p, const Smem& s, int cur, int& next);
-
 // Staged row instruction (RMSNorm, RoPE): once the sources are complete, the instruction's input
 // rows are copied into consecutive ring stages, as many whole rows per stage as fit, by bulk
 // copies (one per row, one lane each; one per stage when the rows are contiguous). Deep queues
@@ -591,8 +589,7 @@ __device__ bool load_rows(const Params& p, Smem& s, const Instr& in, const Node&
 }
 
 __device__ bool load_gemv(const Params& p, Smem& s, const Instr& in, const Node& nd, int slot,
-                          uint32_t use, RingPos& rp, uint32_t& nfill, int idx, int it,
-                          int& pf_next) {
+                          uint32_t use, RingPos& rp, uint32_t& nfill, int idx) {
   const uint32_t NS = ring_n(p);
   const int nk = ring_stages(in);
   if (nk == 0) return true;
@@ -620,7 +617,6 @@ __device__ bool load_gemv(const Params& p, Smem& s, const Instr& in, const Node&
     __syncwarp();
   }
   for (int kb = 0; kb < nk; ++kb) {
-    if (kb >= (int)NS) prefetch_ahead(p, s, it, pf_next);  // descriptors published meanwhile
     if (!wait_warp(p, smem_u32(&s.empty[rp.st]), rp.ph ^ 1u, R_LOAD, 15, idx)) return false;
     if (elect_one()) {
       const uint32_t bar = smem_u32(&s.full[rp.st]);
@@ -709,56 +705,6 @@ __device__ bool load_attn_prefill(const Params& p, Smem& s, const Instr& in, con
 // activations; their shared-memory loads then hit L2. `next` is the first instruction not yet
 // prefetched; instructions whose operand is produced inside the graph are skipped. Slots are
 // probed without suspending the warp.
-__device__ void prefetch_ahead(const Params& p, const Smem& s, int cur, int& next) {
-  if (next < cur) next = cur;
-  while (next < cur + p.l2_prefetch) {
-    const int slot = next % kSlots;
-    const bool ready = mbar_test(smem_u32(&s.instr_ready[slot]), (uint32_t)(next / kSlots) & 1u);
-    if (!__all_sync(FULL, ready)) return;
-    const Instr& f = slot_instr(s, slot);
-    if (f.op == OP_END) {
-      next = 0x3fffffff;
-      return;
-    }
-    const Node& nd = slot_node(s, slot);
-    if (!(f.flags & IFLAG_B_DEP)) {
-      if (elect_one()) {
-        const bool panel = (nd.flags & NF_B_PANELS) != 0;
-        if (f.op == OP_GEMV && (nd.flags & NF_B_PACKED)) {
-          const bool dual = (nd.flags & EPI_SILU_MUL) != 0;
-          const uint32_t unit = dual ? 16384u : 32768u;
-          const size_t first = (size_t)(f.n0 / (dual ? 128 : 256)) * (size_t)nd.b.ld + f.k0 / 64;
-          const uint32_t bytes = (uint32_t)ring_stages(f) * unit;
-          bulk_prefetch_l2(reinterpret_cast<const uint8_t*>(nd.b.ptr) + first * unit, bytes);
-          if (dual)
-            bulk_prefetch_l2(reinterpret_cast<const uint8_t*>(nd.b2.ptr) + first * unit, bytes);
-        } else if (f.op == OP_GEMV) {
-          const bool dual = (nd.flags & EPI_SILU_MUL) != 0;
-          const int nk = ring_stages(f);
-          const void* mb = tmap_at(p, nd.b.tmap);
-          const void* mb2 = dual ? tmap_at(p, nd.b2.tmap) : nullptr;
-          for (int kb = 0; kb < nk; ++kb) {
-            const int k = f.k0 + kb * kGemvRows;
-            if (panel) {
-              tma_prefetch_l2_3d(mb, 0, k, f.n0 >> 6);
-              if (dual) tma_prefetch_l2_3d(mb2, 0, k, f.n0 >> 6);
-            } else {
-              for (int j = 0; j < 4; ++j)
-                tma_prefetch_l2_2d((dual && j >= 2) ? mb2 : mb, f.n0 + 64 * (dual ? (j & 1) : j),
-                                   k);
-            }
-          }
-        } else if (f.op == OP_ATTN_PARTIAL) {
-          tma_prefetch_l2_2d(tmap_at(p, nd.b.tmap), f.n0 * 64, f.k0);
-          tma_prefetch_l2_2d(tmap_at(p, nd.b2.tmap), f.n0 * 64, f.k0);
-        }
-      }
-      __syncwarp();
-    }
-    ++next;
-  }
-}
-
 template <bool PAIR, int KS>
 __device__ void run_loader(const Params& p, Smem& s) {
   const uint32_t NS = ring_n(p);
@@ -766,7 +712,6 @@ __device__ void run_loader(const Params& p, Smem& s) {
   RingPos rp;
   uint32_t nfill = 0, go_par = 0;
   bool synced = true;  // pair-mode ring sync (see load_gemm)
-  int pf_next = 0;
   for (int it = 0;; ++it) {
     const int slot = it % kSlots;
     const uint32_t use = (uint32_t)(it / kSlots);
@@ -775,13 +720,12 @@ __device__ void run_loader(const Params& p, Smem& s) {
     const Instr& in = slot_instr(s, slot);
     if (in.op == OP_END) break;
     const Node& nd = slot_node(s, slot);
-    if (ks_has_gemv(KS)) prefetch_ahead(p, s, it, pf_next);
     bool ok = true;
     if (in.op != OP_GEMM) synced = false;
     if (ks_has_gemm(KS) && in.op == OP_GEMM)
       ok = load_gemm<PAIR>(p, s, in, nd, slot, use, rp, nfill, go_par, synced, idx);
     else if (ks_has_gemv(KS) && in.op == OP_GEMV)
-      ok = load_gemv(p, s, in, nd, slot, use, rp, nfill, idx, it, pf_next);
+      ok = load_gemv(p, s, in, nd, slot, use, rp, nfill, idx);
     else if (ks_has_gemv(KS) && in.op == OP_ATTN_PARTIAL)
       ok = load_attn(p, s, in, nd, slot, use, rp, nfill, idx);
     else if (ks_has_attn_prefill(KS) && in.op == OP_ATTN_PREFILL)

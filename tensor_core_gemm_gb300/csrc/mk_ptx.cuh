@@ -75,10 +75,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       "l"((uint64_t)src), "r"(bytes), "r"(bar)
       : "memory");
 }
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"((uint64_t)src), "r"(bytes)
-               : "memory");
-}
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint32_t bar, int x,
                                             int y) {
   asm volatile(
@@ -95,12 +91,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, uint
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
       "l"((uint64_t)tmap), "r"(x), "r"(y), "r"(z), "r"(bar)
       : "memory");
-}
-__device__ __forceinline__ void tma_prefetch_l2_3d(const void* tmap, int x, int y, int z) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
-                   (uint64_t)tmap),
-               "r"(x), "r"(y), "r"(z)
-               : "memory");
 }
 // 2D tiled store shared -> global (bulk async-group completion); coordinates innermost first.
 // Parts of the box outside the tensor are not written.
@@ -121,13 +111,6 @@ __device__ __forceinline__ void bulk_wait_read_1() {
 // This thread's bulk stores: complete (written to global memory).
 __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-// Fetch a tile into L2 only (no shared-memory destination, no completion signal).
-__device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int x, int y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                   (uint64_t)tmap),
-               "r"(x), "r"(y)
-               : "memory");
 }
 __device__ __forceinline__ void tensormap_acquire(const void* tmap) {
   asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"((uint64_t)tmap)

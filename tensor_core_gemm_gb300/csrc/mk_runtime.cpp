@@ -778,7 +778,6 @@ extern "C" mk_status mk_compile(mk_graph_t g, const mk_compile_opts* opts_in, mk
   pr.n_sm = o.n_sm;
   pr.n_tmaps = (int32_t)maps.size();
   pr.n_counters = (int32_t)n_ctr;
-  pr.l2_prefetch = std::min(std::max(o.l2_prefetch, 0), kSlots);
   pr.stages = stages;
   pr.timeout_ns = (uint64_t)(o.timeout_ms > 0 ? o.timeout_ms : 2000) * 1000000ull;
   p->grid = o.n_sm;

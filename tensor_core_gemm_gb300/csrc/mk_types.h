@@ -122,7 +122,6 @@ struct Params {
   int32_t n_sm;             // placement stride
   int32_t n_tmaps;
   int32_t n_counters;       // dependency counters + split semaphores
-  int32_t l2_prefetch;      // instructions ahead whose streamed operands are prefetched to L2
   int32_t stages;           // operand ring depth: 4 stages of 48 KB, or 6 of 32 KB (CTA pairs)
   uint64_t timeout_ns;
 };

@@ -36,7 +36,7 @@ def test_library_exports_every_declared_symbol():
     lib = C.CDLL(_lib.LIB_PATH)
     for name in declared:
         assert hasattr(lib, name), name
-    assert _lib.load().mk_abi_version() == 1
+    assert _lib.load().mk_abi_version() == 2
 
 
 def _dry(desc, **opts):
