@@ -69,7 +69,9 @@ def make_workload(name, device):
     from tensor_core_gemm_gb300 import workloads as W
     pair = {"gemm_tile_m": 256, "cluster": 2}   # 256 x 256 tiles on CTA pairs
     if name == "gemm4096":
-        return W.gemm(4096, 4096, 4096, dtype="f16", device=device, seed=0), dict(pair)
+        # 256 pair tiles on 76 pairs: the quarter-full last wave's tiles split along K
+        return (W.gemm(4096, 4096, 4096, dtype="f16", device=device, seed=0),
+                dict(pair, gemm_split_tail=1))
     if name == "mlp3":
         return W.mlp3(device=device, seed=0), {"gemm_tile_n": 64}
     if name == "llama_prefill":

@@ -1170,6 +1170,208 @@ __device__ __noinline__ void epi_tile(const Node& nd, int n0, uint32_t tb, int n
                              N);
 }
 
+// Split-tail partials. A (split, rank) slot holds a CTA's 128 rows x W fp32 columns warp by
+// warp and, inside a warp's 32 rows, column group by column group: the float4 of columns
+// 4j..4j+3 of lane l (row 32q + l) is element (q * W / 4 + j) * 32 + l, so every warp-wide load
+// or store is 512 contiguous bytes. `dst` points at this warp's block and lane.
+__device__ __noinline__ void split_store(uint32_t tb, int W, int nk, float4* dst) {
+  for (int c = 0; c < W; c += 32) {
+    uint32_t r[32];
+    if (nk > 0) {
+      tmem_ld32(tb + (uint32_t)c, r);
+      tmem_ld_wait();
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) r[i] = 0u;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      __stcg(dst + (size_t)(c / 4 + i) * 32,
+             make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                         __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3])));
+  }
+}
+
+// The epilogue of a split-tail tile's last split. Each 32-column chunk is the sum of the splits'
+// partials in split order, starting from zero (this split's own from TMEM, so neither the order
+// nor the result depends on which split finishes last), followed by the fused epilogue and the
+// TMA store of epi_chunks. With two splits (no SiLU·mul) the partner's partial of the next chunk
+// is in flight while a chunk is finished; otherwise each chunk's loads of one partial go out
+// together.
+// `parts` is this warp's block and lane in split 0's slot; pstride the float4 between splits.
+template <bool DUAL, bool SIDE>
+__device__ __noinline__ void epi_split(uint32_t tb, int tn, int nk, uint32_t flags, int dt,
+                                       const uint16_t* bias, int ldb, const uint16_t* res,
+                                       int ldr, const void* omap, uint32_t xr, int row0, int n0,
+                                       int M, int N, const float4* parts, int S, int mine,
+                                       size_t pstride) {
+  constexpr int V = DUAL ? 16 : 8;  // float4 of one chunk of one partial
+  const int lane = threadIdx.x & 31;
+  const int row = row0 + lane;
+  const bool has_bias = SIDE && (flags & EPI_BIAS) != 0, relu = (flags & EPI_RELU) != 0,
+             has_res = SIDE && (flags & EPI_RESIDUAL) != 0;
+  auto issue = [&](int c, const float4* src, float4* v) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __ldcg(src + (size_t)(c / 4 + i) * 32);
+    if (DUAL) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[8 + i] = __ldcg(src + (size_t)((tn + c) / 4 + i) * 32);
+    }
+  };
+  auto add_part = [&](float* w, float* u, const float4* v) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      w[4 * i] += v[i].x;
+      w[4 * i + 1] += v[i].y;
+      w[4 * i + 2] += v[i].z;
+      w[4 * i + 3] += v[i].w;
+      if (DUAL) {
+        u[4 * i] += v[8 + i].x;
+        u[4 * i + 1] += v[8 + i].y;
+        u[4 * i + 2] += v[8 + i].z;
+        u[4 * i + 3] += v[8 + i].w;
+      }
+    }
+  };
+  auto add_own = [&](int c, float* w, float* u) {
+    uint32_t r[32], r2[DUAL ? 32 : 1];
+    if (nk > 0) {
+      tmem_ld32(tb + (uint32_t)c, r);
+      if (DUAL) tmem_ld32(tb + (uint32_t)(tn + c), r2);
+      tmem_ld_wait();
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) r[i] = 0u;
+#pragma unroll
+      for (int i = 0; i < (DUAL ? 32 : 1); ++i) r2[i] = 0u;
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      w[i] += __uint_as_float(r[i]);
+      if (DUAL) u[i] += __uint_as_float(r2[i]);
+    }
+  };
+  auto finish = [&](int c, float* w, const float* u) {
+    if (DUAL) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) w[i] = silu(w[i]) * u[i];
+    }
+    uint4 sb[SIDE ? 4 : 1], sr[SIDE ? 4 : 1];
+#pragma unroll
+    for (int g = 0; g < (SIDE ? 4 : 0); ++g) {
+      const int col = n0 + c + g * 8;
+      const bool inside = row < M && col < N;
+      sb[g] = sr[g] = make_uint4(0u, 0u, 0u, 0u);
+      if (has_bias && inside)
+        sb[g] = __ldcg(reinterpret_cast<const uint4*>(bias + (size_t)row * ldb + col));
+      if (has_res && inside)
+        sr[g] = __ldcg(reinterpret_cast<const uint4*>(res + (size_t)row * ldr + col));
+    }
+    const uint32_t buf = xr + (uint32_t)((c >> 5) & 1) * 2048u;
+    if (c >= 64) {
+      if (lane == 0) bulk_wait_read_1();
+      __syncwarp();
+    }
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const bool inside = row < M && n0 + c + g * 8 < N;
+      float* x = w + g * 8;
+      if (has_bias && inside) {
+        float b[8];
+        unpack8(sb[g], dt, b);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] += b[e];
+      }
+      if (relu) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = fmaxf(x[e], 0.0f);
+      }
+      if (has_res && inside) {
+        float b[8];
+        unpack8(sr[g], dt, b);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] += b[e];
+      }
+      const uint4 pk = pack8(x, dt);
+      const uint32_t dst = buf + (uint32_t)lane * 64u + (uint32_t)((g ^ ((lane >> 1) & 3)) << 4);
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(pk.x), "r"(pk.y),
+                   "r"(pk.z), "r"(pk.w)
+                   : "memory");
+    }
+    fence_proxy_async_shared();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(omap, buf, n0 + c, row0);
+      bulk_commit();
+    }
+  };
+  if (!DUAL && S == 2) {
+    // the partner's partial of the next chunk is in flight while a chunk is finished (a deeper
+    // prefetch raises this callee's registers enough to make the kernel function spill)
+    const float4* other = parts + (size_t)(1 - mine) * pstride;
+    float4 a[V];
+    issue(0, other, a);
+    for (int c = 0; c < tn; c += 32) {
+      float w[32], u[1];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) w[i] = 0.f;
+      if (mine == 0) {
+        add_own(c, w, u);
+        add_part(w, u, a);
+      } else {
+        add_part(w, u, a);
+        add_own(c, w, u);
+      }
+      if (c + 32 < tn) issue(c + 32, other, a);
+      finish(c, w, u);
+    }
+  } else {
+    for (int c = 0; c < tn; c += 32) {
+      float w[32], u[DUAL ? 32 : 1];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) w[i] = 0.f;
+#pragma unroll
+      for (int i = 0; i < (DUAL ? 32 : 1); ++i) u[i] = 0.f;
+      for (int sp = 0; sp < S; ++sp) {
+        if (sp == mine) {
+          add_own(c, w, u);
+        } else {
+          float4 v[V];
+          issue(c, parts + (size_t)sp * pstride, v);
+          add_part(w, u, v);
+        }
+      }
+      finish(c, w, u);
+    }
+  }
+}
+
+// One call site for the four split epilogues, like epi_tile.
+__device__ __noinline__ void epi_split_tile(const Node& nd, int n0, uint32_t tb, int nk,
+                                            const void* omap, uint32_t xr, int row0,
+                                            const float4* parts, int S, int mine,
+                                            size_t pstride) {
+  const uint32_t flags = nd.flags;
+  const int tn = nd.tile_n, dt = nd.dtype, M = nd.M, N = nd.N;
+  const uint16_t* bias = reinterpret_cast<const uint16_t*>(nd.bias.ptr);
+  const uint16_t* res = reinterpret_cast<const uint16_t*>(nd.res.ptr);
+  const int ldb = nd.bias.ld, ldr = nd.res.ld;
+  const bool dual = (flags & EPI_SILU_MUL) != 0;
+  const bool side = (flags & (EPI_BIAS | EPI_RESIDUAL)) != 0;
+  if (dual && side)
+    epi_split<true, true>(tb, tn, nk, flags, dt, bias, ldb, res, ldr, omap, xr, row0, n0, M, N,
+                          parts, S, mine, pstride);
+  else if (dual)
+    epi_split<true, false>(tb, tn, nk, flags, dt, bias, ldb, res, ldr, omap, xr, row0, n0, M, N,
+                           parts, S, mine, pstride);
+  else if (side)
+    epi_split<false, true>(tb, tn, nk, flags, dt, bias, ldb, res, ldr, omap, xr, row0, n0, M, N,
+                           parts, S, mine, pstride);
+  else
+    epi_split<false, false>(tb, tn, nk, flags, dt, bias, ldb, res, ldr, omap, xr, row0, n0, M,
+                            N, parts, S, mine, pstride);
+}
+
 // GEMM epilogue: TMEM -> registers (one row per thread), fused epilogue, then per 32-column chunk
 // a 32 x 32 block per warp staged in shared memory and stored with TMA. In pair mode each CTA
 // drains its own 128 rows of the 256-row tile. A split-tail tile (aux1 = number of K splits)
@@ -1192,12 +1394,9 @@ __device__ bool gemm_epilogue(const Params& p, Smem& s, const Instr& in, const N
   trace_mark(p, idx, 6);
   const int dt = nd.dtype;
   const bool dual = (nd.flags & EPI_SILU_MUL) != 0;
-  const bool bias = (nd.flags & EPI_BIAS) != 0, relu = (nd.flags & EPI_RELU) != 0,
-             res = (nd.flags & EPI_RESIDUAL) != 0;
   const int tn = nd.tile_n;
   const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
   const int row0 = in.m0 + (int)rank * kGemmTileM + q * 32;  // this warp's 32 rows
-  const int row = row0 + lane;
   const uint32_t tb = tmem + as * 256u + ((uint32_t)(q * 32) << 16);
   auto release_tmem = [&]() {
     if (nk > 0) {
@@ -1221,68 +1420,15 @@ __device__ bool gemm_epilogue(const Params& p, Smem& s, const Instr& in, const N
   // stores it with TMA; a buffer is rewritten once the store issued from it has read it.
   const uint32_t xr0 = smem_u32(s.xr) + (uint32_t)q * 4096u;
   const void* omap = tmap_at(p, nd.out.tmap);
-  auto store32 = [&](int c, float* v) {
-    const uint32_t buf = xr0 + (uint32_t)((c >> 5) & 1) * 2048u;
-    if (c >= 64) {
-      if (lane == 0) bulk_wait_read_1();
-      __syncwarp();
-    }
-#pragma unroll
-    for (int g = 0; g < 4; ++g) {
-      const int col = in.n0 + c + g * 8;
-      const bool inside = row < nd.M && col < nd.N;
-      float* w = v + g * 8;
-      if (bias && inside) {
-        float b[8];
-        load8(nd.bias, row, col, dt, b);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) w[e] += b[e];
-      }
-      if (relu) {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) w[e] = fmaxf(w[e], 0.0f);
-      }
-      if (res && inside) {
-        float b[8];
-        load8(nd.res, row, col, dt, b);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) w[e] += b[e];
-      }
-      const uint4 pk = pack8(w, dt);
-      const uint32_t dst = buf + (uint32_t)lane * 64u + (uint32_t)((g ^ ((lane >> 1) & 3)) << 4);
-      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(pk.x), "r"(pk.y),
-                   "r"(pk.z), "r"(pk.w)
-                   : "memory");
-    }
-    fence_proxy_async_shared();
-    __syncwarp();
-    if (lane == 0) {
-      tma_store_2d(omap, buf, in.n0 + c, row0);
-      bulk_commit();
-    }
-  };
   if (in.aux1 > 0) {
-    // split tail: this split's fp32 partial (gate columns, then up columns with SiLU·mul)
+    // Split tail: every split stores its fp32 partial (gate columns, then up columns with
+    // SiLU·mul); the last split to reach the tile's semaphore sums them and runs the epilogue.
     const int W = dual ? 2 * tn : tn, S = in.aux1, cl = PAIR ? 2 : 1;
-    const size_t sstride = (size_t)cl * kGemmTileM * W;  // next split, same rank
-    const float* base = reinterpret_cast<const float*>(nd.scratch.ptr) +
-                        ((size_t)in.slot * kGemmTileM + q * 32 + lane) * W;
-    float* mine = const_cast<float*>(base) + (size_t)in.split * sstride;
-    for (int c = 0; c < W; c += 32) {
-      uint32_t r[32];
-      if (nk > 0) {
-        tmem_ld32(tb + (uint32_t)c, r);
-        tmem_ld_wait();
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) r[i] = 0u;
-      }
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        __stcg(reinterpret_cast<float4*>(mine + c) + i,
-               make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
-                           __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3])));
-    }
+    const size_t slot_f4 = (size_t)kGemmTileM * W / 4;  // float4 per (split, rank) slot
+    const size_t pstride = (size_t)cl * slot_f4;          // next split, same rank
+    float4* part0 = reinterpret_cast<float4*>(nd.scratch.ptr) + (size_t)in.slot * slot_f4 +
+                    (size_t)q * 8 * W + lane;  // this warp's block of split 0, this lane
+    split_store(tb, W, nk, part0 + (size_t)in.split * pstride);
     __threadfence();
     cw_sync();
     if (ct == 0) s.flag = atomicAdd(p.counters + in.sem, 1) == S - 1;
@@ -1293,58 +1439,7 @@ __device__ bool gemm_epilogue(const Params& p, Smem& s, const Instr& in, const N
       return true;
     }
     __threadfence();
-    // The last split sums the partials in split order (its own from TMEM, so the order and the
-    // result do not depend on which split finishes last) and runs the epilogue. The next column
-    // block's partial loads are issued before the current block is summed.
-    auto sum32 = [&](int col, float* acc) {
-      uint32_t r[32];
-      if (nk > 0) {
-        tmem_ld32(tb + (uint32_t)col, r);
-        tmem_ld_wait();
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) r[i] = 0u;
-      }
-#pragma unroll
-      for (int i = 0; i < 32; ++i) acc[i] = 0.f;
-      for (int sp = 0; sp < S; ++sp) {
-        if (sp == in.split) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) acc[i] += __uint_as_float(r[i]);
-        } else {
-          const float4* src = reinterpret_cast<const float4*>(base + sp * sstride + col);
-          float4 t[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) t[i] = __ldcg(src + i);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            acc[4 * i] += t[i].x;
-            acc[4 * i + 1] += t[i].y;
-            acc[4 * i + 2] += t[i].z;
-            acc[4 * i + 3] += t[i].w;
-          }
-        }
-      }
-    };
-    for (int c = 0; c < tn; c += 32) {
-      // warm L2 -> L1 for the next block of every other split while this block is summed
-      if (c + 32 < tn)
-        for (int sp = 0; sp < S; ++sp)
-          if (sp != in.split) {
-            const float* nx = base + sp * sstride + c + 32;
-            asm volatile("prefetch.global.L1 [%0];" ::"l"(nx) : "memory");
-            if (dual) asm volatile("prefetch.global.L1 [%0];" ::"l"(nx + tn) : "memory");
-          }
-      float v[32];
-      sum32(c, v);
-      if (dual) {
-        float u[32];
-        sum32(tn + c, u);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = silu(v[i]) * u[i];
-      }
-      store32(c, v);
-    }
+    epi_split_tile(nd, in.n0, tb, nk, omap, xr0, row0, part0, S, in.split, pstride);
     release_tmem();
   } else {
     if constexpr (KS == KS_GEMM) {
