@@ -223,7 +223,9 @@ __device__ __forceinline__ float warp_max(float v) {
   for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(FULL, v, o));
   return v;
 }
-__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+// silu(z) = z * sigmoid(z), with the fast exponential and division intrinsics: for z below
+// about -87 the denominator passes 2^126 and the quotient is 0 (true value below 1e-36).
+__device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 // 16-bit element conversions (dt: DT_F16 or DT_BF16).
 __device__ __forceinline__ float h2f(uint16_t v, int dt) {
@@ -1080,8 +1082,18 @@ __device__ __noinline__ void epi_chunks(uint32_t tb, int tn, int nk, uint32_t fl
     }
   };
   if (SIDE && AHEAD) load_side(0, sb, sr);
+  // without the register copies of the next chunk, this row's side vectors of the chunk after
+  // next are fetched into L1 (a hint: no registers held)
+  auto prefetch_side = [&](int c) {
+    if (!SIDE || AHEAD || c >= tn || row >= M || n0 + c >= N) return;
+    if (has_bias) asm volatile("prefetch.global.L1 [%0];" ::"l"(bias + (size_t)row * ldb + n0 + c));
+    if (has_res) asm volatile("prefetch.global.L1 [%0];" ::"l"(res + (size_t)row * ldr + n0 + c));
+  };
+  prefetch_side(0);
+  prefetch_side(32);
   for (int c = 0; c < tn; c += 32) {
     if (SIDE && AHEAD && c + 32 < tn) load_side(c + 32, nb, nr);
+    prefetch_side(c + 64);
     if (SIDE && !AHEAD) load_side(c, sb, sr);
     uint32_t r[32], r2[DUAL ? 32 : 1];
     if (nk > 0) {
@@ -2642,14 +2654,29 @@ __device__ void run_compute(const Params& p, Smem& s, uint32_t tmem) {
     }
     if (!ok) break;
     trace_mark(p, idx, 3);
-    // Publish: every thread's stores are ordered before the release increments.
+    // Publish: every thread's stores are ordered before the release increments. One counter:
+    // a release increment. More: the first warp loads the counter ids together, then one
+    // release fence and relaxed increments (a release increment each would wait on the last).
     __threadfence();
     cw_sync();
-    if (ct == 0) {
-      if (publish && in.n_dst > 0) {
+    if (ct < 32 && publish && in.n_dst > 1) {
+      if (ct == 0) {
         fence_proxy_async_global();
-        for (int j = 0; j < in.n_dst; ++j)
-          red_release_add(p.counters + __ldg(p.dst_list + in.dst_off + j), 1);
+        fence_acq_rel_gpu();
+      }
+      for (int j0 = 0; j0 < in.n_dst; j0 += 32) {
+        const int n = min(32, in.n_dst - j0);
+        const int c = ct < n ? __ldg(p.dst_list + in.dst_off + j0 + ct) : 0;
+        for (int k = 0; k < n; ++k) {
+          const int ck = __shfl_sync(FULL, c, k);
+          if (ct == 0) red_relaxed_add(p.counters + ck, 1);
+        }
+      }
+    }
+    if (ct == 0) {
+      if (publish && in.n_dst == 1) {
+        fence_proxy_async_global();
+        red_release_add(p.counters + __ldg(p.dst_list + in.dst_off), 1);
       }
       if (p.trace) {
         p.trace[(size_t)idx * kTraceWords + 4] = globaltimer();
