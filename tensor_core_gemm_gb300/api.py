@@ -228,6 +228,12 @@ class Plan:
         check(self._lib.mk_get_trace(self._h, buf.ctypes.data_as(C.POINTER(C.c_uint64)), 8 * n))
         return buf[:8 * n].reshape(-1, 8)
 
+    def export_trace(self, path, node_names=None):
+        """Write the last run's per-instruction timeline (plan compiled with trace=1) as a
+        Chrome trace-event JSON file, one track per SM (see trace.py); returns the event count."""
+        from .trace import write_chrome_trace
+        return write_chrome_trace(path, self.trace(), self.instructions(), node_names)
+
     def counters(self):
         s = self.stats()
         return self._ints(self._lib.mk_get_counters, s["n_counters"] + s["n_sems"])

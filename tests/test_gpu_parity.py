@@ -4,6 +4,8 @@ Tolerance (floating point): relative Frobenius error <= 5e-3 and per-element
 |err| <= 2e-2 * max(1, |ref|). Integer outputs (counters) are compared exactly.
 """
 import math
+import os
+import tempfile
 
 import numpy as np
 import pytest
@@ -588,6 +590,15 @@ def test_trace_timestamps_are_ordered():
     # GEMM tiles: the accumulator is complete after the sources are seen, before the body ends
     assert np.all(tr[real, 6] >= tr[real, 2]) and np.all(tr[real, 3] >= tr[real, 6])
     assert np.all(tr[:, 7] == 0)
+    # the Chrome trace export: one track per SM that ran a tile, one GEMM slice per tile
+    import json
+    path = os.path.join(tempfile.mkdtemp(), "run.json")
+    p.export_trace(path, node_names=["layer 0", "layer 1"])
+    ev = json.load(open(path))["traceEvents"]
+    tiles = [e for e in ev if e["ph"] == "X" and e["name"] == "gemm"]
+    assert len(tiles) == int(real.sum())
+    assert {e["tid"] for e in tiles} == set(int(x) for x in tr[real, 5])
+    assert all(e["dur"] >= 0 and e["args"]["node_name"].startswith("layer") for e in tiles)
 
 
 # ------------------------------------------------------------------ CTA pairs (cta_group::2)
