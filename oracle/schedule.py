@@ -54,7 +54,11 @@ Lowering rules per node (tile sizes come from ``opts``; see ``DEFAULT_OPTS``):
       lowers to GEMV tiles (no b2), whose x is exactly that matmul's output, with head_dim 64 and
       an output width that is a multiple of gemv_tile_n (itself a multiple of 64), emits no
       instructions: split 0 of each GEMV column tile also carries the rotated q / k (and v)
-      boxes of its columns.
+      boxes of its columns. Also fused: a rope node right after a plain matmul (no bias,
+      residual, relu, gamma or b2) that lowers to GEMM tiles without a split tail, whose x is
+      the left part of that matmul's output window holding exactly the q, k (and, with out_v,
+      v) heads, head_dim 64: every GEMM tile instruction also carries the out_q / out_k
+      (/ out_v) boxes of its rows and of its columns below that width.
   attention with one query row (decode) -> two phases:
       partial: for kv head g, for chunk c of attn_chunk keys: reads q (the G = Hq/Hkv heads of
         group g), k and v rows of the chunk (columns of head g); writes rows (g·C + c)·G ..+G
@@ -145,8 +149,17 @@ class Instr:
                 self.aux0, self.aux1, self.sem)
 
 
+def _rope_width(r):
+    """Columns of its input a rope node reads: the q, k (and, with out_v, v) heads."""
+    heads = r["n_q_heads"] + r["n_kv_heads"] + (r["n_kv_heads"] if r.get("out_v") is not None
+                                                 else 0)
+    return heads * r["head_dim"]
+
+
 def rope_fusable(nodes, ri, opts):
-    """Whether rope node ri folds into the GEMV tiles of the matmul right before it."""
+    """Whether rope node ri folds into the tiles of the matmul right before it: GEMV tiles when
+    its input is exactly the matmul's output window, GEMM tiles (a plain matmul, no split tail)
+    when its input is the left part of that window holding exactly the heads it reads."""
     r = nodes[ri]
     if not opts["fuse_rope"] or r["kind"] != "rope" or ri == 0:
         return False
@@ -154,22 +167,28 @@ def rope_fusable(nodes, ri, opts):
     if p["kind"] != "matmul" or p.get("b2") is not None:
         return False
     m = p["a"][3]
-    return (0 < m <= opts["gemv_max_m"] and tuple(r["x"]) == tuple(p["c"])
-            and r["head_dim"] == 64 and opts["gemv_tile_n"] % 64 == 0
-            and p["c"][4] % opts["gemv_tile_n"] == 0)
+    if m <= 0 or r["head_dim"] != 64:
+        return False
+    if m <= opts["gemv_max_m"]:
+        return (tuple(r["x"]) == tuple(p["c"]) and opts["gemv_tile_n"] % 64 == 0
+                and p["c"][4] % opts["gemv_tile_n"] == 0)
+    plain = all(p.get(f) is None for f in ("bias", "residual", "gamma")) and not p.get("relu")
+    x, c = r["x"], p["c"]
+    return (plain and not opts["gemm_split_tail"] and tuple(x[:4]) == tuple(c[:4])
+            and x[4] == _rope_width(r) and x[4] <= c[4])
 
 
-def _rope_writes(rope, m, c0, c1):
-    """Boxes of the rope outputs that columns [c0, c1) of its input produce."""
+def _rope_writes(rope, r0, r1, c0, c1):
+    """Boxes of the rope outputs that rows [r0, r1) and columns [c0, c1) of its input produce."""
     d = rope["head_dim"]
     qend, kend = rope["n_q_heads"] * d, (rope["n_q_heads"] + rope["n_kv_heads"]) * d
     out = []
     if c0 < qend:
-        out.append(_box(rope["out_q"], 0, m, c0, min(c1, qend)))
+        out.append(_box(rope["out_q"], r0, r1, c0, min(c1, qend)))
     if c1 > qend and c0 < kend:
-        out.append(_box(rope["out_k"], 0, m, max(c0, qend) - qend, min(c1, kend) - qend))
+        out.append(_box(rope["out_k"], r0, r1, max(c0, qend) - qend, min(c1, kend) - qend))
     if rope.get("out_v") is not None and c1 > kend:
-        out.append(_box(rope["out_v"], 0, m, max(c0, kend) - kend, c1 - kend))
+        out.append(_box(rope["out_v"], r0, r1, max(c0, kend) - kend, c1 - kend))
     return out
 
 
@@ -211,7 +230,7 @@ def _lower_matmul(ni, nd, opts, phases, sem_tiles, rope=None):
                 if si == 0:
                     ins.writes.append(_box(c, 0, m, n0, n0 + w))
                     if rope is not None:
-                        ins.writes.extend(_rope_writes(rope, m, n0, n0 + w))
+                        ins.writes.extend(_rope_writes(rope, 0, m, n0, n0 + w))
                 out.append(ins)
     else:
         tm = opts["gemm_tile_m"]
@@ -249,6 +268,9 @@ def _lower_matmul(ni, nd, opts, phases, sem_tiles, rope=None):
                         ins.reads.append((_box(ref, m0, m0 + tm, n0, n0 + tn), ROLE_E))
                     if si == 0:
                         ins.writes.append(_box(c, m0, m0 + tm, n0, n0 + tn))
+                        if rope is not None:
+                            ins.writes.extend(_rope_writes(rope, m0, m0 + tm, n0,
+                                                           min(n0 + tn, _rope_width(rope))))
                     out.append(ins)
     phases.append(out)
 
@@ -495,7 +517,7 @@ def transient_bytes(t):
     return cdiv(t["rows"] * ld * es, 1024) * 1024
 
 
-def _pool(tensors, nodes, instrs, targets, o, split):
+def _pool(tensors, nodes, instrs, targets, o, split, fused=()):
     """Phase 2 of "MegaKittens Internals" §04, for the transient tensors.
 
     Transients are visited in the order of the node that writes them. One takes a buffer from
@@ -503,8 +525,9 @@ def _pool(tensors, nodes, instrs, targets, o, split):
     option pool_waves, 1 by default: the page's one wave) past the end
     (last instruction + 1) of every node that touched the buffer's current occupant, and the
     occupant has the same dtype and shape; otherwise it gets a new buffer at the end of the
-    pool. The occupant's writer counts among the nodes that touched it. A buffer whose occupant
-    is touched by a node without instructions (fused into another) is never handed on.
+    pool. The occupant's writer counts among the nodes that touched it. A node fused into the
+    one before it (``fused``: it has no instructions, that node's carry its work) counts as
+    that node wherever it touches or writes a transient.
 
     Each reuse is one new counter: every instruction of the nodes that touched the old occupant
     arrives on it (the splits of one tile once) and every instruction of the new writer waits
@@ -520,13 +543,14 @@ def _pool(tensors, nodes, instrs, targets, o, split):
     touched = {}
     writer = {}
     for ni, nd in enumerate(nodes):
+        ci = ni - 1 if ni in fused else ni      # the node whose instructions do ni's work
         reads, writes = _node_refs(nd)
         for ref in reads + writes:
             touched.setdefault(ref[0], [])
-            if ni not in touched[ref[0]]:
-                touched[ref[0]].append(ni)
+            if ci not in touched[ref[0]]:
+                touched[ref[0]].append(ci)
         for ref in writes:
-            writer.setdefault(ref[0], ni)
+            writer.setdefault(ref[0], ci)
     trans = [t for t, d in enumerate(tensors) if d.get("transient")]
     trans.sort(key=lambda t: writer.get(t, len(nodes)))
     offsets = [-1] * len(tensors)
@@ -706,7 +730,7 @@ def lower(graph, opts):
             ins.dst = list(first[ins.tile].dst)
 
     # Phase 2 after the fact: the pool needs the final instruction order.
-    pool = _pool(tensors, nodes, instrs, targets, o, split)
+    pool = _pool(tensors, nodes, instrs, targets, o, split, fused)
     n_dep = len(targets)
     for ins in instrs:          # semaphores follow every counter, reuse counters included
         if split(ins):

@@ -66,10 +66,14 @@ static HInstr make(uint16_t op, int node, int m0 = 0, int n0 = 0, int k0 = 0, in
   return h;
 }
 
-// RoPE fusion: a ROPE node right after a matmul that lowers to GEMV tiles (no second weight),
-// whose input is exactly that matmul's output window, with head_dim 64 and an output width that
-// is a multiple of the GEMV tile width, emits no instructions; split 0 of every GEMV column tile
-// also writes the rotated q / k (and v) columns it produced.
+// RoPE fusion: a ROPE node right after a matmul (no second weight) with head_dim 64 emits no
+// instructions when either
+//  - the matmul lowers to GEMV tiles, the rope input is exactly its output window and the
+//    output width is a multiple of the GEMV tile width: split 0 of every GEMV column tile also
+//    writes the rotated q / k (and v) columns it produced; or
+//  - the matmul lowers to GEMM tiles without epilogue flags or a split tail, and the rope input
+//    is the left part of its output window holding exactly the q, k (and, with out_v, v) heads:
+//    every GEMM tile also writes the rotated q / k (and copied v) columns of its rows.
 static bool same_window(const std::vector<TensorRec>& ts, int a, int b) {
   const TensorRec &x = ts[a], &y = ts[b];
   return x.base == y.base && x.r0 == y.r0 && x.c0 == y.c0 && x.rows == y.rows &&
@@ -82,8 +86,26 @@ static bool rope_fusable(const std::vector<TensorRec>& ts, const std::vector<Nod
   const NodeRec& p = nodes[ri - 1];
   if (p.kind != NK_MATMUL || p.b2 >= 0) return false;
   const int64_t m = ts[p.a].rows;
-  return m > 0 && m <= o.gemv_max_m && same_window(ts, r.ins[0], p.out) && r.hd == 64 &&
-         o.gemv_tile_n % 64 == 0 && ts[p.out].cols % o.gemv_tile_n == 0;
+  if (m <= 0 || r.hd != 64) return false;
+  if (m <= o.gemv_max_m)
+    return same_window(ts, r.ins[0], p.out) && o.gemv_tile_n % 64 == 0 &&
+           ts[p.out].cols % o.gemv_tile_n == 0;
+  const TensorRec &x = ts[r.ins[0]], &y = ts[p.out];
+  const int64_t w = (int64_t)(r.hq + r.hkv + (r.out_v >= 0 ? r.hkv : 0)) * r.hd;
+  return p.flags == 0 && !o.gemm_split_tail && x.base == y.base && x.r0 == y.r0 &&
+         x.c0 == y.c0 && x.rows == y.rows && x.cols == w && w <= y.cols;
+}
+
+// Boxes of the rope outputs that rows [r0, r1) and columns [c0, c1) of its input produce.
+static void rope_writes(const std::vector<TensorRec>& ts, const NodeRec& rope, int64_t r0,
+                        int64_t r1, int64_t c0, int64_t c1, std::vector<Box>& out) {
+  const int64_t qend = (int64_t)rope.hq * 64, kend = (int64_t)(rope.hq + rope.hkv) * 64;
+  if (c0 < qend) out.push_back(window(ts, rope.out, r0, r1, c0, std::min(c1, qend)));
+  if (c1 > qend && c0 < kend)
+    out.push_back(window(ts, rope.out_k, r0, r1, std::max(c0, qend) - qend,
+                         std::min(c1, kend) - qend));
+  if (rope.out_v >= 0 && c1 > kend)
+    out.push_back(window(ts, rope.out_v, r0, r1, std::max(c0, kend) - kend, c1 - kend));
 }
 
 static void lower_matmul(const std::vector<TensorRec>& ts, int ni, const NodeRec& nd,
@@ -122,16 +144,7 @@ static void lower_matmul(const std::vector<TensorRec>& ts, int ni, const NodeRec
         if (nd.res >= 0) h.reads.push_back({window(ts, nd.res, 0, m, n0, n0 + w), ROLE_E});
         if (si == 0) {
           h.writes.push_back(window(ts, nd.out, 0, m, n0, n0 + w));
-          if (rope) {
-            const int64_t qend = (int64_t)rope->hq * 64, kend = (int64_t)(rope->hq + rope->hkv) * 64;
-            const int64_t c0 = n0, c1 = n0 + w;
-            if (c0 < qend) h.writes.push_back(window(ts, rope->out, 0, m, c0, std::min(c1, qend)));
-            if (c1 > qend && c0 < kend)
-              h.writes.push_back(window(ts, rope->out_k, 0, m, std::max(c0, qend) - qend,
-                                        std::min(c1, kend) - qend));
-            if (rope->out_v >= 0 && c1 > kend)
-              h.writes.push_back(window(ts, rope->out_v, 0, m, std::max(c0, kend) - kend, c1 - kend));
-          }
+          if (rope) rope_writes(ts, *rope, 0, m, n0, n0 + w, h.writes);
         }
         out.push_back(std::move(h));
       }
@@ -140,6 +153,8 @@ static void lower_matmul(const std::vector<TensorRec>& ts, int ni, const NodeRec
     const int64_t tm = o.gemm_tile_m;
     const int64_t tn = dual ? o.gemm_tile_n / 2 : o.gemm_tile_n;
     const int cl = o.cluster;
+    const int64_t rope_w =  // columns of the output a fused rope reads
+        rope ? (int64_t)(rope->hq + rope->hkv + (rope->out_v >= 0 ? rope->hkv : 0)) * 64 : 0;
     plan->node_tile_n[ni] = (int)tn;
     // Split tail: the tiles of the last, partly filled wave (T mod units) are split along K
     // when at least two splits fit per tile; the last split to finish sums the partials.
@@ -186,7 +201,11 @@ static void lower_matmul(const std::vector<TensorRec>& ts, int ni, const NodeRec
             h.reads.push_back({window(ts, nd.bias, m0, m0 + tm, n0, n0 + tn), ROLE_E});
           if (nd.res >= 0)
             h.reads.push_back({window(ts, nd.res, m0, m0 + tm, n0, n0 + tn), ROLE_E});
-          if (si == 0) h.writes.push_back(window(ts, nd.out, m0, m0 + tm, n0, n0 + tn));
+          if (si == 0) {
+            h.writes.push_back(window(ts, nd.out, m0, m0 + tm, n0, n0 + tn));
+            if (rope) rope_writes(ts, *rope, m0, m0 + tm, n0, std::min<int64_t>(n0 + tn, rope_w),
+                                  h.writes);
+          }
           out.push_back(std::move(h));
         }
       }
@@ -607,8 +626,8 @@ mk_status lower_graph(const std::vector<TensorRec>& tensors_in, const std::vecto
   // writer counts as an accessor, so a region no reader covered is also finished. Each reuse is
   // one counter, numbered after the dependency counters: every instruction of the accessor nodes
   // arrives on it (a split tile once), and every instruction of the new writer waits for the
-  // total before it runs. Transients an instruction-less (fused) node touches keep a buffer of
-  // their own.
+  // total before it runs. A node fused into the one before it (a RoPE in its matmul's tiles)
+  // has no instructions: its accesses count as accesses of that carrier node.
   {
     const int n_t = (int)tensors_in.size();
     plan->pool_off.assign(ts.size(), -1);
@@ -641,10 +660,11 @@ mk_status lower_graph(const std::vector<TensorRec>& tensors_in, const std::vecto
     std::vector<int64_t> buf_off, buf_bytes;
     std::vector<int> order;
     std::vector<int> writer(n_t, -1);
+    auto carrier = [&](int ni) { return fused[ni] ? ni - 1 : ni; };
     for (int t = 0; t < n_t; ++t) {
       if (!ts[t].transient || ts[t].base != t) continue;
       for (int ni = 0; ni < nn && writer[t] < 0; ++ni)
-        if (touches(nodes[ni], t, true)) writer[t] = ni;
+        if (touches(nodes[ni], t, true)) writer[t] = carrier(ni);
       order.push_back(t);
     }
     std::stable_sort(order.begin(), order.end(), [&](int a, int b) {
@@ -657,8 +677,9 @@ mk_status lower_graph(const std::vector<TensorRec>& tensors_in, const std::vecto
       bool ok = writer[t] >= 0;
       for (int ni = 0; ni < nn; ++ni)
         if (touches(nodes[ni], t, false) || touches(nodes[ni], t, true)) {
-          acc.push_back(ni);
-          ok = ok && last[ni] >= 0;
+          const int c = carrier(ni);
+          if (std::find(acc.begin(), acc.end(), c) == acc.end()) acc.push_back(c);
+          ok = ok && last[c] >= 0;
         }
       const int64_t bytes =
           ((int64_t)ts[t].rows * ts[t].ld * dtype_size(ts[t].dtype) + 1023) & ~(int64_t)1023;

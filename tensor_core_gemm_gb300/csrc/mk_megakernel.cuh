@@ -226,6 +226,17 @@ __device__ __forceinline__ float warp_max(float v) {
 // silu(z) = z * sigmoid(z), with the fast exponential and division intrinsics: for z below
 // about -87 the denominator passes 2^126 and the quotient is 0 (true value below 1e-36).
 __device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
+// sin and cos of a RoPE angle (|a| up to ~1e5 rad): Cody and Waite's additive reduction to
+// [-pi, pi], 2*pi split into its fp32 rounding and the remainder of that rounding (two fused
+// multiply-adds, the remainder's term below 1e-7 rad for these angles), then the hardware sine
+// and cosine approximations, which hold 2^-21 absolute accuracy on that interval. Every RoPE
+// path (rows, fused into GEMV and GEMM tiles) takes the same steps, so they agree bit for bit.
+__device__ __forceinline__ void rope_sincos(float a, float* sn, float* cs) {
+  const float k = rintf(a * 0.15915493667125702f);  // a / (2 pi), nearest integer
+  float r = fmaf(-k, 6.2831854820251465f, a);
+  r = fmaf(-k, -1.7484555314695172e-07f, r);
+  __sincosf(r, sn, cs);
+}
 
 // 16-bit element conversions (dt: DT_F16 or DT_BF16).
 __device__ __forceinline__ float h2f(uint16_t v, int dt) {
@@ -1358,6 +1369,95 @@ __device__ __noinline__ void epi_split(uint32_t tb, int tn, int nk, uint32_t fla
   }
 }
 
+// The epilogue of a GEMM tile whose output feeds a fused RoPE (plain matmul, head_dim 64): per
+// 64-column head, TMEM -> registers, the output rounded and stored as usual, then the following
+// rope node's rotation of those rounded values (rotate_half pairing (j, j + 32), position =
+// pos0 + output row, theta^(-2i/64) frequencies, the angle formula of the row path) stored to
+// out_q / out_k, or the value copied to out_v for v heads when the node has one. Each 32 x 32
+// block goes through one of the warp's two staging buffers to a TMA store; a buffer is rewritten
+// once the store issued from it two blocks earlier has read it.
+__device__ __noinline__ void epi_rope(const Params& p, const Node& nd, int n0, uint32_t tb,
+                                      int nk, uint32_t xr, int row0) {
+  const int tn = nd.tile_n, dt = nd.dtype, hq = nd.hq, hkv = nd.hkv, pos0 = nd.pos0;
+  const float l2t = log2f(nd.theta);
+  const void* omap = tmap_at(p, nd.out.tmap);
+  const void* qmap = tmap_at(p, nd.out_q.tmap);
+  const void* kmap = tmap_at(p, nd.out_k.tmap);
+  const void* vmap = nd.out_v.tmap >= 0 ? tmap_at(p, nd.out_v.tmap) : nullptr;
+  const int lane = threadIdx.x & 31;
+  const float pos = (float)(pos0 + row0 + lane);
+  // the row's 32 angles are the same for every head of the tile: their sines and cosines once
+  const float my_inv = exp2f(-(2.0f * (float)lane / 64.0f) * l2t);  // lane i: frequency i
+  float cs[32], sn[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) rope_sincos(pos * __shfl_sync(FULL, my_inv, i), &sn[i], &cs[i]);
+  int nb = 0;  // blocks stored so far by this warp
+  auto store_block = [&](const void* map, int col, const float* v) {
+    const uint32_t buf = xr + (uint32_t)(nb & 1) * 2048u;
+    if (nb >= 2) {
+      if (lane == 0) bulk_wait_read_1();
+      __syncwarp();
+    }
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const uint4 pk = pack8(v + g * 8, dt);
+      const uint32_t dst = buf + (uint32_t)lane * 64u + (uint32_t)((g ^ ((lane >> 1) & 3)) << 4);
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(pk.x), "r"(pk.y),
+                   "r"(pk.z), "r"(pk.w)
+                   : "memory");
+    }
+    fence_proxy_async_shared();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(map, buf, col, row0);
+      bulk_commit();
+    }
+    ++nb;
+  };
+  for (int c = 0; c < tn; c += 64) {
+    float lo[32], hi[32];
+    if (nk > 0) {
+      uint32_t r[32], r2[32];
+      tmem_ld32(tb + (uint32_t)c, r);
+      tmem_ld32(tb + (uint32_t)(c + 32), r2);
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        lo[i] = __uint_as_float(r[i]);
+        hi[i] = __uint_as_float(r2[i]);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) lo[i] = hi[i] = 0.f;
+    }
+    const int col = n0 + c, h = col >> 6;
+    store_block(omap, col, lo);
+    store_block(omap, col + 32, hi);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {  // the values the rope node reads: the stored outputs
+      lo[i] = h2f(f2h(lo[i], dt), dt);
+      hi[i] = h2f(f2h(hi[i], dt), dt);
+    }
+    if (h < hq + hkv) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {  // fully unrolled: the arrays stay in registers
+        const float a = lo[i], b = hi[i];
+        lo[i] = a * cs[i] - b * sn[i];  // first half: x cos - x' sin
+        hi[i] = b * cs[i] + a * sn[i];  // second half: x cos + x' sin
+      }
+      const bool q = h < hq;
+      const void* map = q ? qmap : kmap;
+      const int oc = q ? col : col - hq * 64;
+      store_block(map, oc, lo);
+      store_block(map, oc + 32, hi);
+    } else if (vmap && h < hq + 2 * hkv) {
+      const int oc = col - (hq + hkv) * 64;
+      store_block(vmap, oc, lo);
+      store_block(vmap, oc + 32, hi);
+    }
+  }
+}
+
 // One call site for the four split epilogues, like epi_tile.
 __device__ __noinline__ void epi_split_tile(const Node& nd, int n0, uint32_t tb, int nk,
                                             const void* omap, uint32_t xr, int row0,
@@ -1452,6 +1552,9 @@ __device__ bool gemm_epilogue(const Params& p, Smem& s, const Instr& in, const N
     }
     __threadfence();
     epi_split_tile(nd, in.n0, tb, nk, omap, xr0, row0, part0, S, in.split, pstride);
+    release_tmem();
+  } else if (nd.flags & NF_ROPE) {
+    epi_rope(p, nd, in.n0, tb, nk, xr0, row0);
     release_tmem();
   } else {
     if constexpr (KS == KS_GEMM) {
@@ -1931,8 +2034,8 @@ __device__ bool gemv(const Params& p, Smem& s, const Instr& in, const Node& nd, 
           const float sgn = j < 32 ? -1.f : 1.f;  // first half: x cos - x' sin; second: + x' sin
           const float pos = (float)(nd.pos0 + m), l2t = log2f(nd.theta);
           float sn0, cs0, sn1, cs1;
-          sincosf(pos * exp2f(-(2.0f * (float)i / 64.0f) * l2t), &sn0, &cs0);
-          sincosf(pos * exp2f(-(2.0f * (float)(i + 1) / 64.0f) * l2t), &sn1, &cs1);
+          rope_sincos(pos * exp2f(-(2.0f * (float)i / 64.0f) * l2t), &sn0, &cs0);
+          rope_sincos(pos * exp2f(-(2.0f * (float)(i + 1) / 64.0f) * l2t), &sn1, &cs1);
           const float z0 = r0 * cs0 + sgn * p0 * sn0, z1 = r1 * cs1 + sgn * p1 * sn1;
           if (n < qend)
             store2(nd.out_q, m, n, dt, z0, z1);
@@ -2025,7 +2128,7 @@ __device__ __forceinline__ void rope_body(const Instr& in, const Node& nd) {
     for (int e = 0; e < 8; ++e) {
       float sn, cs;
       const float inv = exp2f(-(2.0f * (float)(i0 + e) / (float)hd) * l2t);
-      sincosf(pos * inv, &sn, &cs);
+      rope_sincos(pos * inv, &sn, &cs);
       y1[e] = x1[e] * cs - x2[e] * sn;
       y2[e] = x2[e] * cs + x1[e] * sn;
     }
@@ -2073,7 +2176,7 @@ __device__ bool rows_staged(const Params& p, Smem& s, const Instr& in, const Nod
     for (int v = ct; v < rows * half; v += kCompute) {
       const int r = v / half, i = v % half;
       const float inv = exp2f(-(2.0f * (float)i / (float)hd) * l2t);
-      sincosf((float)(nd.pos0 + in.m0 + r) * inv, &tsin[v], &tcos[v]);
+      rope_sincos((float)(nd.pos0 + in.m0 + r) * inv, &tsin[v], &tcos[v]);
     }
     cw_sync();
   } else if (gshared) {

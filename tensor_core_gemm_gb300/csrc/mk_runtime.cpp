@@ -415,7 +415,7 @@ static mk_status build_nodes(const mk_graph* g, mk_plan* p, std::vector<CUtensor
         n.kind = gemv ? OP_GEMV : OP_GEMM;
         if (gemv) n.ldp = n.M * n.N * ((nd.flags & MK_EPI_SILU_MUL) ? 2 : 1);
         if (p->hp.node_rope[i] >= 0) {
-          // the next node's RoPE runs in this GEMV's tiles (same rule as the lowering)
+          // the next node's RoPE runs in this matmul's GEMV or GEMM tiles (the lowering's rule)
           const NodeRec& r = g->nodes[p->hp.node_rope[i]];
           n.flags |= NF_ROPE;
           n.hq = r.hq;
@@ -432,6 +432,14 @@ static mk_status build_nodes(const mk_graph* g, mk_plan* p, std::vector<CUtensor
           // swizzled; K = 0 tiles too (they store the epilogue of zero)
           mk_status st;
           if ((st = add_map(keys, maps, ts[nd.out], 32, 32, 64, &n.out.tmap))) return st;
+          if (n.flags & NF_ROPE) {  // the fused rope's outputs leave the epilogue the same way
+            const NodeRec& r = g->nodes[p->hp.node_rope[i]];
+            if ((st = add_map(keys, maps, ts[r.out], 32, 32, 64, &n.out_q.tmap))) return st;
+            if ((st = add_map(keys, maps, ts[r.out_k], 32, 32, 64, &n.out_k.tmap))) return st;
+            if (r.out_v >= 0 &&
+                (st = add_map(keys, maps, ts[r.out_v], 32, 32, 64, &n.out_v.tmap)))
+              return st;
+          }
         }
         if (n.M > 0 && n.N > 0 && n.K > 0) {
           mk_status st;

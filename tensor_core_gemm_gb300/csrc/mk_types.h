@@ -102,7 +102,7 @@ struct Node {
 };
 static_assert(sizeof(Node) == 256, "node entry is 256 bytes");
 
-constexpr int kMaxTmaps = 256;
+constexpr int kMaxTmaps = 1024;
 constexpr int kXrFloats = 5120;  // shared-memory staging of GEMV activations / RoPE angle tables
 
 // Kernel parameters (plain pointers into plan-owned device memory).
