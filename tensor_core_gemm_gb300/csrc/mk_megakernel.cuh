@@ -237,6 +237,15 @@ __device__ __forceinline__ void rope_sincos(float a, float* sn, float* cs) {
   r = fmaf(-k, -1.7484555314695172e-07f, r);
   __sincosf(r, sn, cs);
 }
+// One rotate_half pair (x1 in the first half of the head, x2 its partner in the second):
+// z1 = x1 cos - x2 sin and z2 = x2 cos + x1 sin, each as one rounded product and one fused
+// multiply-add, so that every RoPE path rounds the same way.
+__device__ __forceinline__ float rope_z1(float x1, float x2, float c, float s) {
+  return fmaf(x1, c, -__fmul_rn(x2, s));
+}
+__device__ __forceinline__ float rope_z2(float x1, float x2, float c, float s) {
+  return fmaf(x2, c, __fmul_rn(x1, s));
+}
 
 // 16-bit element conversions (dt: DT_F16 or DT_BF16).
 __device__ __forceinline__ float h2f(uint16_t v, int dt) {
@@ -1442,8 +1451,8 @@ __device__ __noinline__ void epi_rope(const Params& p, const Node& nd, int n0, u
 #pragma unroll
       for (int i = 0; i < 32; ++i) {  // fully unrolled: the arrays stay in registers
         const float a = lo[i], b = hi[i];
-        lo[i] = a * cs[i] - b * sn[i];  // first half: x cos - x' sin
-        hi[i] = b * cs[i] + a * sn[i];  // second half: x cos + x' sin
+        lo[i] = rope_z1(a, b, cs[i], sn[i]);  // first half: x cos - x' sin
+        hi[i] = rope_z2(a, b, cs[i], sn[i]);  // second half: x cos + x' sin
       }
       const bool q = h < hq;
       const void* map = q ? qmap : kmap;
@@ -2031,12 +2040,12 @@ __device__ bool gemv(const Params& p, Smem& s, const Instr& in, const Node& nd, 
         const int qend = nd.hq * 64, kend = (nd.hq + nd.hkv) * 64;
         if (n < kend) {
           const int j = n & 63, i = j & 31;
-          const float sgn = j < 32 ? -1.f : 1.f;  // first half: x cos - x' sin; second: + x' sin
           const float pos = (float)(nd.pos0 + m), l2t = log2f(nd.theta);
           float sn0, cs0, sn1, cs1;
           rope_sincos(pos * exp2f(-(2.0f * (float)i / 64.0f) * l2t), &sn0, &cs0);
           rope_sincos(pos * exp2f(-(2.0f * (float)(i + 1) / 64.0f) * l2t), &sn1, &cs1);
-          const float z0 = r0 * cs0 + sgn * p0 * sn0, z1 = r1 * cs1 + sgn * p1 * sn1;
+          const float z0 = j < 32 ? rope_z1(r0, p0, cs0, sn0) : rope_z2(p0, r0, cs0, sn0);
+          const float z1 = j < 32 ? rope_z1(r1, p1, cs1, sn1) : rope_z2(p1, r1, cs1, sn1);
           if (n < qend)
             store2(nd.out_q, m, n, dt, z0, z1);
           else
@@ -2129,8 +2138,8 @@ __device__ __forceinline__ void rope_body(const Instr& in, const Node& nd) {
       float sn, cs;
       const float inv = exp2f(-(2.0f * (float)(i0 + e) / (float)hd) * l2t);
       rope_sincos(pos * inv, &sn, &cs);
-      y1[e] = x1[e] * cs - x2[e] * sn;
-      y2[e] = x2[e] * cs + x1[e] * sn;
+      y1[e] = rope_z1(x1[e], x2[e], cs, sn);
+      y2[e] = rope_z2(x1[e], x2[e], cs, sn);
     }
     const Operand& o = h < nd.hq ? nd.out : nd.out_k;
     const int hh = h < nd.hq ? h : h - nd.hq;
@@ -2265,8 +2274,8 @@ __device__ bool rows_staged(const Params& p, Smem& s, const Instr& in, const Nod
           unpack8(q, dt, pf);
           // first half: x cos - x' sin; second half: x cos + x' sin (x' the partner element)
 #pragma unroll
-          for (int e = 0; e < 8; ++e) y[e] = first ? xf[e] * cs[e] - pf[e] * sn[e]
-                                                   : xf[e] * cs[e] + pf[e] * sn[e];
+          for (int e = 0; e < 8; ++e) y[e] = first ? rope_z1(xf[e], pf[e], cs[e], sn[e])
+                                                   : rope_z2(pf[e], xf[e], cs[e], sn[e]);
           const Operand& o = h < nd.hq ? nd.out : nd.out_k;
           const int hh = h < nd.hq ? h : h - nd.hq;
           store8(o, m, hh * hd + c * 8, dt, y);

@@ -881,7 +881,8 @@ def test_pair_gemms_interleaved_with_gemvs():
 
 def test_decode_rope_fused_and_unfused_agree():
     """RoPE inside the QKV GEMV tiles (default) and RoPE as its own row instruction give the
-    same decode step within the tolerance (both rotate the rounded QKV output in fp32)."""
+    same decode step bit for bit (both rotate the rounded QKV output with the same angle and
+    rounding steps)."""
     sh = workloads.DecoderShape(layers=2, hidden=512, n_q_heads=8, n_kv_heads=2, head_dim=64,
                                 ffn=1024)
     outs = []
@@ -889,13 +890,30 @@ def test_decode_rope_fused_and_unfused_agree():
         wl = workloads.decode(sh, kv_len=130, device=DEV, seed=9)
         plan, _ = run(wl, fuse_rope=fuse)
         assert (plan.stats()["per_op"][osched.OP_ROPE] == 0) == bool(fuse)
-        outs.append({k: f32(wl.data[wl.info[k]]) for k in ("qr", "kc", "vc", "out")})
+        outs.append({k: wl.data[wl.info[k]].clone() for k in ("qr", "kc", "vc", "out")})
     for k in ("qr", "kc", "vc", "out"):
-        assert_close(outs[0][k], outs[1][k], f"fused vs unfused {k}")
+        assert torch.equal(outs[0][k].view(torch.int16), outs[1][k].view(torch.int16)), k
+
+
+def test_prefill_rope_fused_and_unfused_bit_identical():
+    """RoPE inside the QKV GEMM tiles' epilogue (default) and RoPE as row instructions (staged
+    16-row blocks, and direct 96-row blocks) rotate the same rounded QKV outputs with the same
+    angle steps: q, k and the layer outputs agree bit for bit."""
+    sh = workloads.DecoderShape(layers=2, hidden=512, n_q_heads=8, n_kv_heads=2, head_dim=64,
+                                ffn=1024)
+    outs = []
+    for opts in (dict(), dict(fuse_rope=0), dict(fuse_rope=0, norm_rows=96)):
+        wl = workloads.prefill(sh, tokens=200, device=DEV, seed=12)
+        plan, _ = run(wl, **opts)
+        assert (plan.stats()["per_op"][osched.OP_ROPE] == 0) == ("fuse_rope" not in opts)
+        outs.append([wl.data[wl.info[k]].clone() for k in ("qr", "kr", "qkv", "out")])
+    for other in outs[1:]:
+        for name, a, b in zip(("qr", "kr", "qkv", "out"), outs[0], other):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16)), name
 
 
 @pytest.mark.parametrize("kind", ["decode", "prefill", "prefill_ragged", "prefill_rows96",
-                                  "gemm", "gemm_pair", "mlp3"])
+                                  "prefill_unfused", "gemm", "gemm_pair", "mlp3"])
 def test_kernel_specialisations_bit_identical(kind):
     """The specialisation mk_run picks for a plan and the general kernel (kernel_set = 1) give
     bit-identical outputs; the specialisation is the one the plan statistics name. The prefill
@@ -910,7 +928,10 @@ def test_kernel_specialisations_bit_identical(kind):
         # a ragged last row block; row blocks too tall for the shared RoPE angle table
         "prefill_ragged": (lambda: workloads.prefill(sh, tokens=200, device=DEV, seed=6), {}, 3),
         "prefill_rows96": (lambda: workloads.prefill(sh, tokens=320, device=DEV, seed=8),
-                           dict(norm_rows=96), 3),
+                           dict(norm_rows=96, fuse_rope=0), 3),
+        # RoPE as row instructions (staged blocks) instead of in the QKV tiles
+        "prefill_unfused": (lambda: workloads.prefill(sh, tokens=200, device=DEV, seed=6),
+                            dict(fuse_rope=0), 3),
         "gemm": (lambda: workloads.gemm(640, 768, 1088, device=DEV, seed=4), {}, 1),
         "gemm_pair": (lambda: workloads.gemm(640, 768, 1088, device=DEV, seed=4), pair, 1),
         "mlp3": (lambda: workloads.mlp3(device=DEV), dict(gemm_tile_n=64), 1),
