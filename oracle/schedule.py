@@ -73,9 +73,10 @@ Lowering rules per node (tile sizes come from ``opts``; see ``DEFAULT_OPTS``):
       2c, 2c+1 of those rows of a per-node fp32 scratch [R x 2C]; n0 = first column, klen =
       columns, aux0 = c. Reduce: one per row block; reads the block's scratch rows, writes its
       rows of the output column; aux1 = C.
-  attention with several query rows (prefill) -> one instruction per (q tile t of attn_tile_q
-      rows, q head h), t descending (longest first), then h ascending; reads q rows of the tile,
-      k and v rows [0, kmax) with kmax = min(Tk, q_pos0 + end of tile) when causal.
+  attention with several query rows (prefill) -> one instruction per (q tile t of
+      attn_tile_q·cluster rows, q head h, rank r < cluster), t descending (longest first), then
+      h ascending, then r (aux0 = r); reads q rows of the tile, k and v rows [0, kmax) with
+      kmax = min(Tk, q_pos0 + end of tile) when causal; every rank carries the tile's boxes.
 
 Wave packing (wave_pack = 1, default): a run of consecutive phases of one kind, none reading a
 region that an earlier phase of the run writes (bounding boxes per tensor), becomes one phase:
@@ -467,19 +468,21 @@ def _lower_attention(ni, nd, opts, phases, tensors, sem_tiles):
         phases.append(part)
         phases.append(red)
     else:
-        tt = opts["attn_tile_q"]
+        cl = opts["cluster"]
+        tt = opts["attn_tile_q"] * cl
         out = []
         for t in reversed(range(cdiv(tq, tt))):
             m0 = t * tt
             kmax = min(tk, nd.get("q_pos0", 0) + m0 + tt) if nd["causal"] else tk
             for h in range(hq):
                 g = h // g_sz
-                ins = Instr(OP_ATTN_PREFILL, ni, m0, h, 0, kmax)
-                ins.reads.append((_box(q, m0, m0 + tt, h * d, (h + 1) * d), ROLE_E))
-                ins.reads.append((_box(k, 0, kmax, g * d, (g + 1) * d), ROLE_E))
-                ins.reads.append((_box(v, 0, kmax, g * d, (g + 1) * d), ROLE_E))
-                ins.writes.append(_box(o, m0, m0 + tt, h * d, (h + 1) * d))
-                out.append(ins)
+                for r in range(cl):
+                    ins = Instr(OP_ATTN_PREFILL, ni, m0, h, 0, kmax, r)
+                    ins.reads.append((_box(q, m0, m0 + tt, h * d, (h + 1) * d), ROLE_E))
+                    ins.reads.append((_box(k, 0, kmax, g * d, (g + 1) * d), ROLE_E))
+                    ins.reads.append((_box(v, 0, kmax, g * d, (g + 1) * d), ROLE_E))
+                    ins.writes.append(_box(o, m0, m0 + tt, h * d, (h + 1) * d))
+                    out.append(ins)
         phases.append(out)
 
 

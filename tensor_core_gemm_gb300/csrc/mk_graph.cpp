@@ -346,19 +346,24 @@ static void lower_attention(std::vector<TensorRec>& ts, int ni, const NodeRec& n
     phases.push_back(std::move(part));
     phases.push_back(std::move(red));
   } else {
-    const int64_t tt = o.attn_tile_q;
+    // Query tiles of attn_tile_q rows, or on CTA pairs of cluster x attn_tile_q rows with one
+    // instruction per rank (aux0), each carrying the whole cluster tile's boxes.
+    const int cl = o.cluster;
+    const int64_t tt = o.attn_tile_q * cl;
     std::vector<HInstr> out;
     for (int64_t t = cdiv(tq, tt) - 1; t >= 0; --t) {
       const int64_t m0 = t * tt;
       const int64_t kmax = nd.causal ? std::min(tk, (int64_t)nd.pos0 + m0 + tt) : tk;
       for (int64_t h = 0; h < hq; ++h) {
         const int64_t g = h / g_sz;
-        HInstr hi = make(OP_ATTN_PREFILL, ni, (int)m0, (int)h, 0, (int)kmax);
-        hi.reads.push_back({window(ts, nd.a, m0, m0 + tt, h * d, (h + 1) * d), ROLE_E});
-        hi.reads.push_back({window(ts, nd.b, 0, kmax, g * d, (g + 1) * d), ROLE_E});
-        hi.reads.push_back({window(ts, nd.b2, 0, kmax, g * d, (g + 1) * d), ROLE_E});
-        hi.writes.push_back(window(ts, nd.out, m0, m0 + tt, h * d, (h + 1) * d));
-        out.push_back(std::move(hi));
+        for (int r = 0; r < cl; ++r) {
+          HInstr hi = make(OP_ATTN_PREFILL, ni, (int)m0, (int)h, 0, (int)kmax, r, 0);
+          hi.reads.push_back({window(ts, nd.a, m0, m0 + tt, h * d, (h + 1) * d), ROLE_E});
+          hi.reads.push_back({window(ts, nd.b, 0, kmax, g * d, (g + 1) * d), ROLE_E});
+          hi.reads.push_back({window(ts, nd.b2, 0, kmax, g * d, (g + 1) * d), ROLE_E});
+          hi.writes.push_back(window(ts, nd.out, m0, m0 + tt, h * d, (h + 1) * d));
+          out.push_back(std::move(hi));
+        }
       }
     }
     phases.push_back(std::move(out));

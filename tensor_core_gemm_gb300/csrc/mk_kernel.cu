@@ -14,21 +14,22 @@ size_t megakernel_smem_bytes() { return kMegakernelSmem; }
 
 int launched_kernel_set(int ks, bool pair) {
   if (ks < KS_ALL || ks > KS_PREFILL) return KS_ALL;
-  return pair && ks != KS_GEMM ? KS_ALL : ks;
+  return pair && ks == KS_DECODE ? KS_ALL : ks;
 }
 
 static KernelVariant pick(int ks, bool pair) {
   switch (launched_kernel_set(ks, pair)) {
     case KS_GEMM: return variant_gemm(pair);
     case KS_DECODE: return variant_decode();
-    case KS_PREFILL: return variant_prefill();
+    case KS_PREFILL: return variant_prefill(pair);
     default: return variant_all(pair);
   }
 }
 
 cudaError_t configure_megakernel(size_t smem) {
   const KernelVariant all[] = {variant_all(false), variant_all(true), variant_gemm(false),
-                               variant_gemm(true), variant_decode(), variant_prefill()};
+                               variant_gemm(true), variant_decode(), variant_prefill(false),
+                               variant_prefill(true)};
   for (const KernelVariant& v : all) {
     const cudaError_t e = v.configure(smem);
     if (e != cudaSuccess) return e;

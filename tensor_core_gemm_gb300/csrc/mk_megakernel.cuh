@@ -416,11 +416,6 @@ __device__ __forceinline__ void load_panels(uint32_t dst, const void* map, bool 
   }
 }
 
-// Ring alignment of pair mode: the two CTAs of a pair have consumed different numbers of stages
-// (their other instructions differ), but one MMA reads both CTAs' shared memory at the same
-// offsets. Before every pair GEMM both CTAs therefore move to the start of the next pass over the
-// ring; each skipped stage is waited free, then both of its barriers are arrived on so their
-// phase counts stay equal to the use count every role tracks.
 // Everything the k-loop of one GEMM tile's loads needs, as plain values.
 struct LoadTile {
   uint32_t full0, tx0, empty0, deps, deps_par, ring0, sb, ns, own;
@@ -496,49 +491,59 @@ __device__ __noinline__ bool load_tile(const Params& p, const LoadTile& tp, uint
   return true;
 }
 
-// Pair-mode ring sync: `synced` holds while every instruction since the last resync was a pair
-// GEMM (all roles of both CTAs see the same instruction kinds per iteration, so they agree). Then
-// both CTAs consumed the same stages from the same position and every stage's last use was a pair
-// MMA that released it in both CTAs: the next pair GEMM streams straight on. Otherwise it resyncs.
+// Pair-mode ring sync before a pair instruction (a GEMM or attention tile both CTAs of a pair
+// run together) that fills nst stages. `synced` holds while every instruction since the last
+// resync was such a pair instruction (all roles of both CTAs see the same instruction kinds per
+// iteration, so they agree); then both CTAs consumed the same stages from the same position and
+// every stage's last use was a pair MMA that released it in both CTAs: the instruction streams
+// straight on. Otherwise both CTAs move to the start of the next pass over the ring (each
+// skipped stage waited free, both its barriers arrived on so their phase counts stay equal to
+// the use count every role tracks), and, when the instruction fills stages, the handshake below.
+template <bool PAIR>
+__device__ bool pair_ring_sync(const Params& p, Smem& s, RingPos& rp, uint32_t& nfill,
+                               uint32_t& go_par, bool& synced, int nst, int idx) {
+  if (!PAIR || synced) return true;
+  const uint32_t NS = ring_n(p);
+  while (rp.st != 0) {
+    if (!wait_warp(p, smem_u32(&s.empty[rp.st]), rp.ph ^ 1u, R_LOAD, 18, idx)) return false;
+    if (elect_one()) {
+      mbar_arrive(smem_u32(&s.full[rp.st]));
+      mbar_arrive(smem_u32(&s.empty[rp.st]));
+    }
+    __syncwarp();
+    rp.next(NS);
+    ++nfill;
+  }
+  if (nst == 0) return true;
+  // After other instructions the two CTAs' rings differ, so the odd CTA's bytes must not reach
+  // the even CTA's full barriers while one of them still carries an earlier load. The even CTA
+  // waits until every stage of the pass is free (every earlier use consumed), then releases the
+  // odd CTA once. Later stages need no handshake: the odd CTA reuses a stage only after the
+  // pair MMA that read it committed, which is after the even CTA's barrier for it completed.
+  // Bytes that land before the even CTA's expect_tx leave the transaction count negative
+  // until it arrives.
+  if (cluster_ctarank() == 0) {
+    for (int j = 0; j < (int)NS; ++j)
+      if (!wait_warp(p, smem_u32(&s.empty[j]), rp.ph ^ 1u, R_LOAD, 17, idx)) return false;
+    if (elect_one()) mbar_arrive_cluster(mapa_shared(smem_u32(&s.go), 1));
+    __syncwarp();
+  } else {
+    if (!wait_warp(p, smem_u32(&s.go), go_par & 1u, R_LOAD, 19, idx, true)) return false;
+    go_par ^= 1u;
+  }
+  synced = true;
+  return true;
+}
+
 template <bool PAIR>
 __device__ bool load_gemm(const Params& p, Smem& s, const Instr& in, const Node& nd, int slot,
                           uint32_t use, RingPos& rp, uint32_t& nfill, uint32_t& go_par,
                           bool& synced, int idx) {
   const uint32_t NS = ring_n(p);
-  if (PAIR && !synced) {
-    while (rp.st != 0) {
-      if (!wait_warp(p, smem_u32(&s.empty[rp.st]), rp.ph ^ 1u, R_LOAD, 18, idx)) return false;
-      if (elect_one()) {
-        mbar_arrive(smem_u32(&s.full[rp.st]));
-        mbar_arrive(smem_u32(&s.empty[rp.st]));
-      }
-      __syncwarp();
-      rp.next(NS);
-      ++nfill;
-    }
-  }
   const int nk = ring_stages(in);
+  if (!pair_ring_sync<PAIR>(p, s, rp, nfill, go_par, synced, nk, idx)) return false;
   if (nk == 0) return true;
   const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
-  if (PAIR && !synced) {
-    // After other instructions the two CTAs' rings differ, so the odd CTA's bytes must not reach
-    // the even CTA's full barriers while one of them still carries an earlier load. The even CTA
-    // waits until every stage of the pass is free (every earlier use consumed), then releases the
-    // odd CTA once. Later stages need no handshake: the odd CTA reuses a stage only after the
-    // pair MMA that read it committed, which is after the even CTA's barrier for it completed.
-    // Bytes that land before the even CTA's expect_tx leave the transaction count negative
-    // until it arrives.
-    if (rank == 0) {
-      for (int j = 0; j < (int)NS; ++j)
-        if (!wait_warp(p, smem_u32(&s.empty[j]), rp.ph ^ 1u, R_LOAD, 17, idx)) return false;
-      if (elect_one()) mbar_arrive_cluster(mapa_shared(smem_u32(&s.go), 1));
-      __syncwarp();
-    } else {
-      if (!wait_warp(p, smem_u32(&s.go), go_par & 1u, R_LOAD, 19, idx, true)) return false;
-      go_par ^= 1u;
-    }
-  }
-  synced = true;
   const bool dual = (nd.flags & EPI_SILU_MUL) != 0;
   const bool panel = (nd.flags & NF_B_PANELS) != 0;
   const int tn = nd.tile_n;
@@ -691,11 +696,17 @@ __device__ bool load_attn(const Params& p, Smem& s, const Instr& in, const Node&
 // stage holds the query tile (16 KB), the block's keys (8 KB) and values (8 KB) of the head's
 // key/value head, all 128-byte swizzled. The query tile is fetched again with every block (from
 // L2) so each stage is self-contained. All three operands are produced inside the graph, so the
-// loads start once the sources are ready.
+// loads start once the sources are ready. On a CTA pair (a 256-row query tile, rank r holding
+// rows 128r..) each CTA loads its own query rows, keys 32r..32r+31 of the block (the N half of
+// S = Q K^T it holds) and value columns 32r..32r+31 (the N half of O = P V, 64-byte rows,
+// 64-byte swizzled): 24 KB per CTA, counted on the even CTA's barrier.
+template <bool PAIR>
 __device__ bool load_attn_prefill(const Params& p, Smem& s, const Instr& in, const Node& nd,
-                                  int slot, uint32_t use, RingPos& rp, uint32_t& nfill, int idx) {
+                                  int slot, uint32_t use, RingPos& rp, uint32_t& nfill,
+                                  uint32_t& go_par, bool& synced, int idx) {
   const uint32_t NS = ring_n(p);
   const int nb = ring_stages(in);
+  if (!pair_ring_sync<PAIR>(p, s, rp, nfill, go_par, synced, nb, idx)) return false;
   if (nb == 0) return true;
   if (!wait_warp(p, smem_u32(&s.deps_ready[slot]), use & 1u, R_LOAD, 28, idx)) return false;
   if (elect_one()) fence_proxy_async_global();
@@ -705,15 +716,27 @@ __device__ bool load_attn_prefill(const Params& p, Smem& s, const Instr& in, con
   const void* tk = tmap_at(p, nd.b.tmap);
   const void* tv = tmap_at(p, nd.b2.tmap);
   const uint32_t ring0 = smem_u32(s.ring), sb = stage_bytes(p);
+  const int rank = PAIR ? (int)cluster_ctarank() : 0;
   for (int j = 0; j < nb; ++j) {
     if (!wait_warp(p, smem_u32(&s.empty[rp.st]), rp.ph ^ 1u, R_LOAD, 29, idx)) return false;
     if (elect_one()) {
       const uint32_t bar = smem_u32(&s.full[rp.st]);
       const uint32_t dst = ring0 + rp.st * sb;
-      mbar_expect_tx(bar, 32768u);
-      tma_load_2d(dst, tq, bar, h * 64, in.m0);
-      tma_load_2d(dst + 16384, tk, bar, g * 64, j * kAttnKeyBlock);
-      tma_load_2d(dst + 24576, tv, bar, g * 64, j * kAttnKeyBlock);
+      if (PAIR) {
+        const uint32_t tx = mapa_shared(bar, 0);  // both CTAs' bytes on the even CTA's barrier
+        if (rank == 0)
+          mbar_expect_tx(bar, 2u * 24576u);
+        else
+          mbar_arrive(bar);
+        tma_load_2d_pair(dst, tq, tx, h * 64, in.m0 + rank * kAttnTileQ);
+        tma_load_2d_pair(dst + 16384, tk, tx, g * 64, j * kAttnKeyBlock + rank * 32);
+        tma_load_2d_pair(dst + 20480, tv, tx, g * 64 + rank * 32, j * kAttnKeyBlock);
+      } else {
+        mbar_expect_tx(bar, 32768u);
+        tma_load_2d(dst, tq, bar, h * 64, in.m0);
+        tma_load_2d(dst + 16384, tk, bar, g * 64, j * kAttnKeyBlock);
+        tma_load_2d(dst + 24576, tv, bar, g * 64, j * kAttnKeyBlock);
+      }
     }
     __syncwarp();
     rp.next(NS);
@@ -722,11 +745,6 @@ __device__ bool load_attn_prefill(const Params& p, Smem& s, const Instr& in, con
   return true;
 }
 
-// L2 prefetch of the streamed operands of instructions already published to later slots: HBM
-// keeps streaming weights (and key/value chunks) while earlier instructions wait for their
-// activations; their shared-memory loads then hit L2. `next` is the first instruction not yet
-// prefetched; instructions whose operand is produced inside the graph are skipped. Slots are
-// probed without suspending the warp.
 template <bool PAIR, int KS>
 __device__ void run_loader(const Params& p, Smem& s) {
   const uint32_t NS = ring_n(p);
@@ -743,7 +761,7 @@ __device__ void run_loader(const Params& p, Smem& s) {
     if (in.op == OP_END) break;
     const Node& nd = slot_node(s, slot);
     bool ok = true;
-    if (in.op != OP_GEMM) synced = false;
+    if (in.op != OP_GEMM && in.op != OP_ATTN_PREFILL) synced = false;
     if (ks_has_gemm(KS) && in.op == OP_GEMM)
       ok = load_gemm<PAIR>(p, s, in, nd, slot, use, rp, nfill, go_par, synced, idx);
     else if (ks_has_gemv(KS) && in.op == OP_GEMV)
@@ -751,7 +769,7 @@ __device__ void run_loader(const Params& p, Smem& s) {
     else if (ks_has_gemv(KS) && in.op == OP_ATTN_PARTIAL)
       ok = load_attn(p, s, in, nd, slot, use, rp, nfill, idx);
     else if (ks_has_attn_prefill(KS) && in.op == OP_ATTN_PREFILL)
-      ok = load_attn_prefill(p, s, in, nd, slot, use, rp, nfill, idx);
+      ok = load_attn_prefill<PAIR>(p, s, in, nd, slot, use, rp, nfill, go_par, synced, idx);
     else if (ks_stages_rows(KS) && (in.op == OP_RMSNORM || in.op == OP_ROPE))
       ok = load_rows(p, s, in, nd, slot, use, rp, nfill, idx);
     if (!ok) break;
@@ -882,14 +900,19 @@ __device__ __noinline__ int mma_gemv(const Params& p, uint32_t full0, uint32_t e
 // awaited, so the tensor pipe computes the next scores while the softmax of the current block
 // runs. A stage is released when the block's P V completes. `n` counts attention blocks on this
 // SM: it gives every barrier's phase. TMEM columns: S at 0 and 64, O at 128.
+template <bool PAIR>
 __device__ __noinline__ bool mma_attn(const Params& p, Smem& s, uint32_t st, uint32_t ph,
                                       uint32_t ns, int nb, uint32_t tmem, uint32_t& n, int idx) {
   const uint32_t ring0 = smem_u32(s.ring), units = stage_bytes(p) >> 4;
   const uint64_t qd = sdesc_sw128(ring0, 16, 1024);            // Q: 128 rows of 128 B
-  const uint64_t kd = sdesc_sw128(ring0 + 16384, 16, 1024);    // K: 64 rows of 128 B
-  const uint64_t vd = sdesc_sw128(ring0 + 24576, 8192, 1024);  // V: 64 rows of 128 B, N-major
+  const uint64_t kd = sdesc_sw128(ring0 + 16384, 16, 1024);    // K: 64 (pair: 32) rows of 128 B
+  // V, N-major: 64 rows of 128 B; on a pair each CTA's 32 columns, 64 rows of 64 B
+  const uint64_t vd = PAIR ? sdesc_sw64(ring0 + 20480, 4096, 512)
+                           : sdesc_sw128(ring0 + 24576, 8192, 1024);
+  const uint64_t vk = PAIR ? 64 : 128;  // a 16-key slice of V, 16-byte units
   const uint64_t pd = sdesc_sw128(smem_u32(s.xr), 16, 1024);   // P: 128 rows of 128 B
-  const uint32_t is = idesc_f16_bk(1, kAttnKeyBlock, kAttnTileQ), io = idesc_f16(1, 64, kAttnTileQ);
+  const int mrows = PAIR ? 2 * kAttnTileQ : kAttnTileQ;
+  const uint32_t is = idesc_f16_bk(1, kAttnKeyBlock, mrows), io = idesc_f16(1, 64, mrows);
   const uint32_t n0 = n;
   RingPos rs, ro;
   rs.st = ro.st = st;
@@ -897,16 +920,24 @@ __device__ __noinline__ bool mma_attn(const Params& p, Smem& s, uint32_t st, uin
   auto issue_s = [&](int j) -> bool {
     const uint32_t nn = n0 + (uint32_t)j, b = nn & 1u;
     if (!wait_warp(p, smem_u32(&s.full[rs.st]), rs.ph, R_MMA, 23, idx)) return false;
-    if (!wait_warp(p, smem_u32(&s.att_s_free[b]), ((nn >> 1) & 1u) ^ 1u, R_MMA, 24, idx))
+    if (!wait_warp(p, smem_u32(&s.att_s_free[b]), ((nn >> 1) & 1u) ^ 1u, R_MMA, 24, idx, PAIR))
       return false;
     tc_fence_after();
     const uint64_t so = (uint64_t)(rs.st * units);
     if (elect_one()) {
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        tc_mma_f16(tmem + b * 64u, qd + so + (uint64_t)(kk * 2), kd + so + (uint64_t)(kk * 2), is,
-                   kk != 0);
-      tc_commit(smem_u32(&s.att_s_full[b]));
+      for (int kk = 0; kk < 4; ++kk) {
+        if (PAIR)
+          tc_mma_f16_pair(tmem + b * 64u, qd + so + (uint64_t)(kk * 2),
+                          kd + so + (uint64_t)(kk * 2), is, kk != 0);
+        else
+          tc_mma_f16(tmem + b * 64u, qd + so + (uint64_t)(kk * 2), kd + so + (uint64_t)(kk * 2),
+                     is, kk != 0);
+      }
+      if (PAIR)
+        tc_commit_pair(smem_u32(&s.att_s_full[b]), 3);
+      else
+        tc_commit(smem_u32(&s.att_s_full[b]));
     }
     __syncwarp();
     rs.next(ns);
@@ -917,23 +948,33 @@ __device__ __noinline__ bool mma_attn(const Params& p, Smem& s, uint32_t st, uin
     if (j + 1 < nb && !issue_s(j + 1)) return false;
     const uint32_t nn = n0 + (uint32_t)j, b = nn & 1u;
     // P_j is written (and any rescale of O by the compute warps is stored) before p_full
-    if (!wait_warp(p, smem_u32(&s.att_p_full), nn & 1u, R_MMA, 25, idx)) return false;
+    if (!wait_warp(p, smem_u32(&s.att_p_full), nn & 1u, R_MMA, 25, idx, PAIR)) return false;
     tc_fence_after();
     const uint64_t so = (uint64_t)(ro.st * units);
     if (elect_one()) {
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        tc_mma_f16(tmem + 128u, pd + (uint64_t)(kk * 2), vd + so + (uint64_t)(kk * 128), io,
-                   (j | kk) != 0);
-      tc_commit(smem_u32(&s.att_o_full[b]));
-      tc_commit(smem_u32(&s.empty[ro.st]));
+      for (int kk = 0; kk < 4; ++kk) {
+        if (PAIR)
+          tc_mma_f16_pair(tmem + 128u, pd + (uint64_t)(kk * 2), vd + so + (uint64_t)kk * vk, io,
+                          (j | kk) != 0);
+        else
+          tc_mma_f16(tmem + 128u, pd + (uint64_t)(kk * 2), vd + so + (uint64_t)kk * vk, io,
+                     (j | kk) != 0);
+      }
+      if (PAIR) {
+        tc_commit_pair(smem_u32(&s.att_o_full[b]), 3);
+        tc_commit_pair(smem_u32(&s.empty[ro.st]), 3);
+      } else {
+        tc_commit(smem_u32(&s.att_o_full[b]));
+        tc_commit(smem_u32(&s.empty[ro.st]));
+      }
     }
     __syncwarp();
     ro.next(ns);
   }
   // The compute warps have read every S and O block of this instruction before TMEM is reused.
   const uint32_t nl = n0 + (uint32_t)nb - 1u;
-  if (!wait_warp(p, smem_u32(&s.att_o_free[nl & 1u]), (nl >> 1) & 1u, R_MMA, 27, idx))
+  if (!wait_warp(p, smem_u32(&s.att_o_free[nl & 1u]), (nl >> 1) & 1u, R_MMA, 27, idx, PAIR))
     return false;
   n = n0 + (uint32_t)nb;
   return true;
@@ -1005,21 +1046,20 @@ __device__ void run_mma(const Params& p, Smem& s, uint32_t tmem) {
         ++acc_n;
       }
     } else if (ks_has_attn_prefill(KS) && in.op == OP_ATTN_PREFILL) {
-      synced = false;
       const int nb = ring_stages(in);
-      if (PAIR) {
-        report(p, MK_ERR_DEVICE_CHECK, idx, -1, in.op, 0, R_MMA, 35);  // refused by the host
-        break;
-      }
-      if (nb > 0) {
+      if (PAIR && !synced) rp.align();  // mirrors the loader's ring sync
+      if (nb > 0) synced = true;
+      if (nb > 0 && PAIR && rank != 0) {
+        rp.advance((uint32_t)nb, NS);  // the even CTA issues the pair's MMAs
+      } else if (nb > 0) {
         // TMEM columns 0..255 are reused: every GEMM epilogue still reading them is done first
         bool w = true;
         for (uint32_t k = 0; k < 2 && w; ++k)
           w = wait_warp(p, smem_u32(&s.acc_empty[(acc_n + k) & 1u]),
-                        (((acc_n + k) >> 1) & 1u) ^ 1u, R_MMA, 21, idx);
+                        (((acc_n + k) >> 1) & 1u) ^ 1u, R_MMA, 21, idx, PAIR);
         if (!w) break;
         tc_fence_after();
-        if (!mma_attn(p, s, rp.st, rp.ph, NS, nb, tmem, att_n, idx)) {
+        if (!mma_attn<PAIR>(p, s, rp.st, rp.ph, NS, nb, tmem, att_n, idx)) {
           issued = true;
           break;
         }
@@ -2549,6 +2589,7 @@ __device__ __noinline__ void attn_reduce_body(const Instr& in, const Node& nd) {
 // taken lazily: P stays <= 2^8, and O / l does not depend on which m was used). A warp rescales
 // its rows only when one of its lanes needs it. At the end the row of O is read once, divided by
 // l and stored as bf16. `n` counts attention blocks on this SM, as in the MMA warp.
+template <bool PAIR>
 __device__ __noinline__ bool attn_prefill_body(const Params& p, Smem& s, const Instr& in,
                                                const Node& nd, uint32_t tmem, uint32_t& n,
                                                int idx) {
@@ -2557,7 +2598,15 @@ __device__ __noinline__ bool attn_prefill_body(const Params& p, Smem& s, const I
   const uint32_t lanes = (uint32_t)((ct >> 5) * 32) << 16;  // this warp's TMEM lane quarter
   const uint32_t otm = tmem + 128u + lanes;                   // this warp's rows of O
   const int nb = ring_stages(in);
-  const int row = in.m0 + ct;
+  // on a CTA pair rank r runs rows 128r.. of the 256-row tile; the even CTA issues the MMAs and
+  // its barriers count both CTAs' warps
+  const int row = in.m0 + (PAIR ? (int)cluster_ctarank() * kAttnTileQ : 0) + ct;
+  auto arrive_mma = [&](uint64_t& bar) {
+    if (PAIR)
+      mbar_arrive_cluster(mapa_shared(smem_u32(&bar), 0));
+    else
+      mbar_arrive(smem_u32(&bar));
+  };
   const int qpos = nd.pos0 + row;
   const int kmax = in.klen;
   const float sl2 = nd.scale * 1.4426950408889634f;  // scores in log2 units
@@ -2577,7 +2626,7 @@ __device__ __noinline__ bool attn_prefill_body(const Params& p, Smem& s, const I
   auto o_release = [&](uint32_t nn) {
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&s.att_o_free[nn & 1u]));
+    if (lane == 0) arrive_mma(s.att_o_free[nn & 1u]);
   };
   for (int j = 0; j < nb; ++j) {
     const uint32_t nn = n0 + (uint32_t)j, b = nn & 1u;
@@ -2590,7 +2639,7 @@ __device__ __noinline__ bool attn_prefill_body(const Params& p, Smem& s, const I
     tmem_ld_wait();
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&s.att_s_free[b]));
+    if (lane == 0) arrive_mma(s.att_s_free[b]);
     const int key0 = j * kAttnKeyBlock;
     const int lim = nd.causal ? min(kmax, qpos + 1) : kmax;  // keys [0, lim) are visible
     // raw scores; masked keys only in a block that reaches the row's limit
@@ -2653,10 +2702,13 @@ __device__ __noinline__ bool attn_prefill_body(const Params& p, Smem& s, const I
 #pragma unroll
     for (int ch = 0; ch < 8; ++ch)
       *reinterpret_cast<uint4*>(P + ct * 128 + ((ch ^ (ct & 7)) << 4)) = pk[ch];
-    fence_proxy_async_shared();
+    if (PAIR)
+      fence_proxy_async_all();  // the even CTA's pair MMA reads this CTA's P
+    else
+      fence_proxy_async_shared();
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&s.att_p_full));
+    if (lane == 0) arrive_mma(s.att_p_full);
   }
   n = n0 + (uint32_t)nb;
   if (nb == 0) return true;
@@ -2697,7 +2749,7 @@ __device__ void run_compute(const Params& p, Smem& s, uint32_t tmem) {
     const Node& nd = slot_node(s, slot);
     if (p.trace && ct == 0) p.trace[(size_t)idx * kTraceWords + 0] = globaltimer();
     bool ok = true, publish = true;
-    if (in.op != OP_GEMM) synced = false;
+    if (in.op != OP_GEMM && in.op != OP_ATTN_PREFILL) synced = false;
     switch (in.op) {
       case OP_GEMM:
         if constexpr (ks_has_gemm(KS)) {
@@ -2737,9 +2789,11 @@ __device__ void run_compute(const Params& p, Smem& s, uint32_t tmem) {
         break;
       case OP_ATTN_PREFILL:
         if constexpr (ks_has_attn_prefill(KS)) {
+          if (PAIR && !synced) ring = ring_align(ring, NS);  // mirrors the loader's ring sync
+          if (ring_stages(in) > 0) synced = true;
           // inputs reach this warpgroup only through the loader and the MMAs, which wait
           trace_mark(p, idx, 2);
-          ok = attn_prefill_body(p, s, in, nd, tmem, att_n, idx);
+          ok = attn_prefill_body<PAIR>(p, s, in, nd, tmem, att_n, idx);
           ok = bar_and(kBarCompute, kCompute, ok);  // its warps waited on their own
           ring += (uint32_t)ring_stages(in);
         }
@@ -2826,11 +2880,11 @@ __global__ void __launch_bounds__(kThreads, 1) megakernel(const __grid_constant_
     mbar_init(smem_u32(&s.gx_full), 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&s.att_s_full[i]), 1);   // tcgen05.commit
-      mbar_init(smem_u32(&s.att_s_free[i]), 4);   // one lane per compute warp
+      mbar_init(smem_u32(&s.att_s_free[i]), PAIR ? 8 : 4);  // a lane per compute warp (both CTAs)
       mbar_init(smem_u32(&s.att_o_full[i]), 1);
-      mbar_init(smem_u32(&s.att_o_free[i]), 4);
+      mbar_init(smem_u32(&s.att_o_free[i]), PAIR ? 8 : 4);
     }
-    mbar_init(smem_u32(&s.att_p_full), 4);
+    mbar_init(smem_u32(&s.att_p_full), PAIR ? 8 : 4);
     mbar_fence_init();
   }
   if (ks_has_tmem(KS) && warp == 2) {
@@ -2956,6 +3010,7 @@ KernelVariant make_variant() {
 KernelVariant variant_all(bool pair);
 KernelVariant variant_gemm(bool pair);
 KernelVariant variant_decode();
-KernelVariant variant_prefill();
+KernelVariant variant_prefill(bool pair);
+KernelVariant variant_prefill_pair();
 
 }  // namespace mk

@@ -121,6 +121,11 @@ __device__ __forceinline__ void tensormap_acquire(const void* tmap) {
 __device__ __forceinline__ void fence_proxy_async_shared() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// Generic-proxy writes before async-proxy accesses in every state space (shared memory a peer
+// CTA's tensor-core operation reads included).
+__device__ __forceinline__ void fence_proxy_async_all() {
+  asm volatile("fence.proxy.async;" ::: "memory");
+}
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
@@ -288,6 +293,10 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   d |= (uint64_t)1 << 46;
   d |= (uint64_t)2 << 61;
   return d;
+}
+// The same for a 64-byte swizzled operand (layout type 4): 8-row atoms of 64-byte rows.
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (sdesc_sw128(saddr, lbo, sbo) & ~((uint64_t)7 << 61)) | ((uint64_t)4 << 61);
 }
 // Instruction descriptor for kind::f16: fp32 accumulator, A K-major, B MN-major, M x N.
 __device__ __forceinline__ uint32_t idesc_f16(int bf16, int n, int m = 128) {

@@ -61,7 +61,7 @@ static cudaError_t run_packs(mk_plan* p, cudaStream_t s, int base_tensor = -1) {
 }
 
 // The smallest kernel specialisation that runs every instruction of the list (KS_ALL when
-// kernel_set = 1 asks for the general kernel); CTA-pair plans outside KS_GEMM run KS_ALL.
+// kernel_set = 1 asks for the general kernel); CTA-pair decode plans run KS_ALL.
 static int pick_kernel_set(const std::vector<Instr>& instrs, const mk_compile_opts& o) {
   if (o.kernel_set == 1) return KS_ALL;
   int ks = KS_ALL;
@@ -261,17 +261,10 @@ mk_status check_kernel_support(const std::vector<TensorRec>& ts, const std::vect
           set_error("mk_compile: attention tensors are bf16");
           return MK_ERR_UNSUPPORTED;
         }
-      if (ts[nd.a].rows > 1) {
-        // prefill tiles: 128 query rows, 64-key blocks, single-CTA tensor-core MMAs (a CTA-pair
-        // launch issues every tcgen05 operation as a pair)
-        if (o.attn_tile_q != kAttnTileQ) {
-          set_error("mk_compile: prefill attention runs attn_tile_q %d", kAttnTileQ);
-          return MK_ERR_UNSUPPORTED;
-        }
-        if (o.cluster != 1) {
-          set_error("mk_compile: prefill attention needs cluster 1 (single-CTA tiles)");
-          return MK_ERR_UNSUPPORTED;
-        }
+      if (ts[nd.a].rows > 1 && o.attn_tile_q != kAttnTileQ) {
+        // prefill tiles: 128 query rows per CTA (256 on a CTA pair), 64-key blocks
+        set_error("mk_compile: prefill attention runs attn_tile_q %d", kAttnTileQ);
+        return MK_ERR_UNSUPPORTED;
       }
     }
   }
@@ -530,11 +523,17 @@ static mk_status build_nodes(const mk_graph* g, mk_plan* p, std::vector<CUtensor
         } else if (n.M > 0 && n.K > 0) {
           // prefill: the query tile (64 columns of one head x 128 rows) and 64-key blocks of
           // keys and values, all 128-byte swizzled
+          // CTA pairs: each CTA loads half the keys of a block (32 x 64 columns) and half the
+          // value columns (64 keys x 32 columns, 64-byte rows, 64-byte swizzled)
+          const bool pr = p->opts.cluster == 2;
           n.tile_m = kAttnKeyBlock;
           mk_status st;
           if ((st = add_map(keys, maps, ts[nd.a], 64, kAttnTileQ, true, &n.a.tmap))) return st;
-          if ((st = add_map(keys, maps, ts[nd.b], 64, kAttnKeyBlock, true, &n.b.tmap))) return st;
-          if ((st = add_map(keys, maps, ts[nd.b2], 64, kAttnKeyBlock, true, &n.b2.tmap)))
+          if ((st = add_map(keys, maps, ts[nd.b], 64, pr ? kAttnKeyBlock / 2 : kAttnKeyBlock, true,
+                            &n.b.tmap)))
+            return st;
+          if ((st = pr ? add_map(keys, maps, ts[nd.b2], 32, kAttnKeyBlock, 64, &n.b2.tmap)
+                       : add_map(keys, maps, ts[nd.b2], 64, kAttnKeyBlock, true, &n.b2.tmap)))
             return st;
         }
         break;

@@ -684,10 +684,14 @@ def test_pair_options_rejected_by_the_kernel_check():
 
 # ------------------------------------------------------------------ causal prefill attention
 
+@pytest.mark.parametrize("pair", [False, True])
 @pytest.mark.parametrize("tq,tk,hq,hkv,causal,pos0", [
     (128, 128, 4, 2, True, 0), (200, 200, 8, 2, True, 0), (384, 384, 32, 8, True, 0),
-    (130, 300, 4, 4, False, 0), (64, 192, 4, 2, True, 128), (1, 64, 2, 1, True, 0)])
-def test_attention_prefill(tq, tk, hq, hkv, causal, pos0):
+    (130, 300, 4, 4, False, 0), (64, 192, 4, 2, True, 128), (1, 64, 2, 1, True, 0),
+    (640, 640, 4, 1, True, 0)])
+def test_attention_prefill(tq, tk, hq, hkv, causal, pos0, pair):
+    """Causal (and non-causal) prefill attention against the oracle; on CTA pairs a 256-row
+    query tile runs as cta_group::2 MMAs with each CTA's softmax on its own 128 rows."""
     if tq == 1:
         pytest.skip("a single query row lowers to split-KV decode tiles")
     d = 64
@@ -700,7 +704,8 @@ def test_attention_prefill(tq, tk, hq, hkv, causal, pos0):
     iq, ik, iv, io = g.tensor(q), g.tensor(k), g.tensor(v), g.tensor(out)
     g.attention(iq, ik, iv, io, n_q_heads=hq, n_kv_heads=hkv, head_dim=d, causal=causal,
                 q_pos0=pos0)
-    p = g.compile()
+    p = g.compile(**(PAIR if pair else {}))
+    assert p.stats()["kernel_set"] == 3
     p.run()
     p.check_status()
     ref = ops.attention(f32(q), f32(k), f32(v), hq, hkv, d, causal, pos0, 1 / 8, BF16)
@@ -716,18 +721,6 @@ def test_attention_prefill(tq, tk, hq, hkv, causal, pos0):
     p.run()
     p.check_status()
     assert torch.equal(out, again)
-
-
-def test_attention_prefill_refused_on_cta_pairs():
-    from tensor_core_gemm_gb300 import Graph
-    from tensor_core_gemm_gb300._lib import MkError
-    q = torch.zeros((128, 128), dtype=torch.bfloat16, device=DEV)
-    kv = torch.zeros((128, 64), dtype=torch.bfloat16, device=DEV)
-    g = Graph()
-    iq, ik, iv, io = g.tensor(q), g.tensor(kv), g.tensor(kv.clone()), g.tensor(q.clone())
-    g.attention(iq, ik, iv, io, n_q_heads=2, n_kv_heads=1, head_dim=64, causal=True)
-    with pytest.raises(MkError):
-        g.compile(gemm_tile_m=256, cluster=2)
 
 
 # ------------------------------------------------------------------ decoder, causal prefill
@@ -779,12 +772,16 @@ def check_prefill_per_node(wl, rows):
         x_prev = xo[l]
 
 
-def test_prefill_small_decoder():
+@pytest.mark.parametrize("pair", [False, True])
+def test_prefill_small_decoder(pair):
+    """A 2-layer decoder prefill node by node and end to end; on CTA pairs the GEMMs run
+    256x256 pair tiles and the causal attention 256-row pair tiles."""
     sh = workloads.DecoderShape(layers=2, hidden=256, n_q_heads=4, n_kv_heads=2, head_dim=64,
                                 ffn=512)
     wl = workloads.prefill(sh, tokens=384, device=DEV, seed=7)
-    plan, _ = run(wl)
-    check_counters(plan, wl, {})
+    opts = dict(PAIR) if pair else {}
+    plan, _ = run(wl, **opts)
+    check_counters(plan, wl, opts)
     check_prefill_per_node(wl, 384)
     # end to end against the oracle's own chain
     ref = models.prefill(f32(wl.data[0]), _prefill_weights(wl))
@@ -792,10 +789,12 @@ def test_prefill_small_decoder():
     assert_close(got, ref, "prefill output")
 
 
-def test_prefill_full_config_causal_prefix():
+@pytest.mark.parametrize("pair", [False, True])
+def test_prefill_full_config_causal_prefix(pair):
     wl = workloads.prefill(device=DEV, seed=0)
-    plan, _ = run(wl)
-    check_counters(plan, wl, {})
+    opts = dict(PAIR) if pair else {}
+    plan, _ = run(wl, **opts)
+    check_counters(plan, wl, opts)
     check_prefill_per_node(wl, 256)
     # End to end over all 16 layers: rows 0..255 of the last layer's output depend only on the
     # first 256 tokens, so the oracle runs the whole decoder on that prefix. Held to MARGIN

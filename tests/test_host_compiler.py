@@ -175,6 +175,13 @@ def test_prefill_plan_small():
     sh = workloads.DecoderShape(layers=2, hidden=256, n_q_heads=4, n_kv_heads=2, head_dim=64,
                                 ffn=512)
     assert_same_plan(workloads.prefill(sh, tokens=384).desc, dict(n_sm=37))
+    # on CTA pairs: 256-row GEMM and attention tiles, one instruction per rank
+    py, c = assert_same_plan(workloads.prefill(sh, tokens=384).desc,
+                             dict(n_sm=38, gemm_tile_m=256, cluster=2))
+    ins = c.instructions()
+    att = ins[ins["op"] == osched.OP_ATTN_PREFILL]
+    assert len(att) == 2 * 2 * 4 * 2 and sorted(set(att["m0"])) == [0, 256]  # layers, tiles, heads, ranks
+    assert np.all(att["aux0"][0::2] == 0) and np.all(att["aux0"][1::2] == 1)
 
 
 @pytest.mark.slow
@@ -335,7 +342,8 @@ def _mixed_gemv_gemm(h=256):
 def test_kernel_specialisation_choice():
     """mk_run launches the smallest specialisation whose instruction kinds cover the plan:
     0 general, 1 GEMM tiles only, 2 decode (GEMV, split-KV attention, rows), 3 prefill (GEMM,
-    prefill attention, rows); CTA-pair kernels exist for the GEMM-only and general sets."""
+    prefill attention, rows); CTA-pair kernels exist for the GEMM-only, prefill and general
+    sets."""
     sh = workloads.DecoderShape(layers=2, hidden=256, n_q_heads=4, n_kv_heads=2, head_dim=64,
                                 ffn=512)
     pair = dict(gemm_tile_m=256, cluster=2)
@@ -349,7 +357,9 @@ def test_kernel_specialisation_choice():
         (workloads.decode(sh, kv_len=200).desc, dict(n_sm=40, fuse_rope=0, fuse_attn_reduce=0), 2),
         (workloads.prefill(sh, tokens=384).desc, dict(n_sm=37), 3),
         (unf, dict(n_sm=16, gemm_tile_n=128), 3),
-        (unf, dict(n_sm=16, **pair), 0),  # GEMM + rows on pairs: the general pair kernel
+        (unf, dict(n_sm=16, **pair), 3),  # GEMM + rows on pairs: the prefill pair kernel
+        (workloads.prefill(sh, tokens=384).desc, dict(n_sm=38, **pair), 3),
+        (workloads.decode(sh, kv_len=200).desc, dict(n_sm=40, **pair), 0),
         (_mixed_gemv_gemm(), dict(n_sm=16), 0),
         (workloads.gemm(512, 512, 256).desc, dict(n_sm=8, kernel_set=1), 0),
         (workloads.decode(sh, kv_len=200).desc, dict(n_sm=40, kernel_set=1), 0),
