@@ -56,6 +56,8 @@ struct __align__(1024) Smem {
   uint64_t gx_full;                     // tensor-core GEMV: the activation operand is staged
   // prefill attention: scores S and output blocks O double-buffered in TMEM, P in xr
   uint64_t att_s_full[2], att_s_free[2], att_p_full, att_o_full[2], att_o_free[2];
+  uint64_t att_q_full;                  // CTA pairs: both CTAs' query tiles are in xr
+  uint64_t att_done;                    // CTA pairs: both CTAs have read O (once per tile)
   uint64_t instr_ready[kSlots];
   uint64_t deps_ready[kSlots];
   uint64_t slot_free[kSlots];
@@ -697,9 +699,11 @@ __device__ bool load_attn(const Params& p, Smem& s, const Instr& in, const Node&
 // key/value head, all 128-byte swizzled. The query tile is fetched again with every block (from
 // L2) so each stage is self-contained. All three operands are produced inside the graph, so the
 // loads start once the sources are ready. On a CTA pair (a 256-row query tile, rank r holding
-// rows 128r..) each CTA loads its own query rows, keys 32r..32r+31 of the block (the N half of
-// S = Q K^T it holds) and value columns 32r..32r+31 (the N half of O = P V, 64-byte rows,
-// 64-byte swizzled): 24 KB per CTA, counted on the even CTA's barrier.
+// rows 128r..) the query rows stay in the staging buffer for the whole instruction (loaded by
+// the compute warpgroup) and a stage holds keys 32r..32r+31 of the block (the N half of
+// S = Q K^T this CTA holds) and value columns 32r..32r+31 (the N half of O = P V, 64-byte rows,
+// 64-byte swizzled): 8 KB per CTA, counted on the even CTA's barrier; the block's P tile is
+// written into the same stage (offset 8 KB), so consecutive blocks do not share a P buffer.
 template <bool PAIR>
 __device__ bool load_attn_prefill(const Params& p, Smem& s, const Instr& in, const Node& nd,
                                   int slot, uint32_t use, RingPos& rp, uint32_t& nfill,
@@ -712,7 +716,7 @@ __device__ bool load_attn_prefill(const Params& p, Smem& s, const Instr& in, con
   if (elect_one()) fence_proxy_async_global();
   __syncwarp();
   const int h = in.n0, g = in.n0 / (nd.hq / nd.hkv);
-  const void* tq = tmap_at(p, nd.a.tmap);
+  const void* tq = PAIR ? nullptr : tmap_at(p, nd.a.tmap);
   const void* tk = tmap_at(p, nd.b.tmap);
   const void* tv = tmap_at(p, nd.b2.tmap);
   const uint32_t ring0 = smem_u32(s.ring), sb = stage_bytes(p);
@@ -725,12 +729,11 @@ __device__ bool load_attn_prefill(const Params& p, Smem& s, const Instr& in, con
       if (PAIR) {
         const uint32_t tx = mapa_shared(bar, 0);  // both CTAs' bytes on the even CTA's barrier
         if (rank == 0)
-          mbar_expect_tx(bar, 2u * 24576u);
+          mbar_expect_tx(bar, 2u * 8192u);
         else
           mbar_arrive(bar);
-        tma_load_2d_pair(dst, tq, tx, h * 64, in.m0 + rank * kAttnTileQ);
-        tma_load_2d_pair(dst + 16384, tk, tx, g * 64, j * kAttnKeyBlock + rank * 32);
-        tma_load_2d_pair(dst + 20480, tv, tx, g * 64 + rank * 32, j * kAttnKeyBlock);
+        tma_load_2d_pair(dst, tk, tx, g * 64, j * kAttnKeyBlock + rank * 32);
+        tma_load_2d_pair(dst + 4096, tv, tx, g * 64 + rank * 32, j * kAttnKeyBlock);
       } else {
         mbar_expect_tx(bar, 32768u);
         tma_load_2d(dst, tq, bar, h * 64, in.m0);
@@ -902,25 +905,38 @@ __device__ __noinline__ int mma_gemv(const Params& p, uint32_t full0, uint32_t e
 // SM: it gives every barrier's phase. TMEM columns: S at 0 and 64, O at 128.
 template <bool PAIR>
 __device__ __noinline__ bool mma_attn(const Params& p, Smem& s, uint32_t st, uint32_t ph,
-                                      uint32_t ns, int nb, uint32_t tmem, uint32_t& n, int idx) {
+                                      uint32_t ns, int nb, uint32_t tmem, uint32_t& n,
+                                      uint32_t q_par, int idx) {
   const uint32_t ring0 = smem_u32(s.ring), units = stage_bytes(p) >> 4;
-  const uint64_t qd = sdesc_sw128(ring0, 16, 1024);            // Q: 128 rows of 128 B
-  const uint64_t kd = sdesc_sw128(ring0 + 16384, 16, 1024);    // K: 64 (pair: 32) rows of 128 B
-  // V, N-major: 64 rows of 128 B; on a pair each CTA's 32 columns, 64 rows of 64 B
-  const uint64_t vd = PAIR ? sdesc_sw64(ring0 + 20480, 4096, 512)
+  const uint32_t xr = smem_u32(s.xr);
+  // Single CTA: a stage holds Q (128 rows of 128 B), K (64 rows of 128 B) and V (N-major, 64
+  // rows of 128 B); P is in xr. Pair: Q in xr; a stage holds this CTA's 32 keys (rows of 128 B),
+  // its 32 value columns (N-major, 64 rows of 64 B) and the block's P (128 rows of 128 B).
+  const uint64_t qd = sdesc_sw128(PAIR ? xr : ring0, 16, 1024);
+  const uint64_t kd = sdesc_sw128(ring0 + (PAIR ? 0 : 16384), 16, 1024);
+  const uint64_t vd = PAIR ? sdesc_sw64(ring0 + 4096, 4096, 512)
                            : sdesc_sw128(ring0 + 24576, 8192, 1024);
   const uint64_t vk = PAIR ? 64 : 128;  // a 16-key slice of V, 16-byte units
-  const uint64_t pd = sdesc_sw128(smem_u32(s.xr), 16, 1024);   // P: 128 rows of 128 B
+  const uint64_t pd = sdesc_sw128(PAIR ? ring0 + 8192 : xr, 16, 1024);
+  const uint64_t qs = PAIR ? 0 : 1;     // Q moves with the stage (single CTA) or stays in xr
+  const uint64_t ps = PAIR ? 1 : 0;     // P moves with the stage (pair) or stays in xr
   const int mrows = PAIR ? 2 * kAttnTileQ : kAttnTileQ;
   const uint32_t is = idesc_f16_bk(1, kAttnKeyBlock, mrows), io = idesc_f16(1, 64, mrows);
   const uint32_t n0 = n;
   RingPos rs, ro;
   rs.st = ro.st = st;
   rs.ph = ro.ph = ph;
+  // pair: both CTAs' query tiles are loaded (the compute warpgroups load them)
+  if (PAIR && !wait_warp(p, smem_u32(&s.att_q_full), q_par, R_MMA, 26, idx, true)) return false;
   auto issue_s = [&](int j) -> bool {
     const uint32_t nn = n0 + (uint32_t)j, b = nn & 1u;
     if (!wait_warp(p, smem_u32(&s.full[rs.st]), rs.ph, R_MMA, 23, idx)) return false;
-    if (!wait_warp(p, smem_u32(&s.att_s_free[b]), ((nn >> 1) & 1u) ^ 1u, R_MMA, 24, idx, PAIR))
+    // S_j reuses the buffer of S_{j-2}. Single CTA: its reads are signalled on their own. Pair:
+    // every arrival on the even CTA is a cluster-scope release that holds the arriving warp, so
+    // a block arrives once (P_j); S_j is issued after P V_{j-2}, which waited for P_{j-2}, which
+    // the warps wrote after reading S_{j-2}.
+    if (!PAIR &&
+        !wait_warp(p, smem_u32(&s.att_s_free[b]), ((nn >> 1) & 1u) ^ 1u, R_MMA, 24, idx))
       return false;
     tc_fence_after();
     const uint64_t so = (uint64_t)(rs.st * units);
@@ -928,11 +944,11 @@ __device__ __noinline__ bool mma_attn(const Params& p, Smem& s, uint32_t st, uin
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         if (PAIR)
-          tc_mma_f16_pair(tmem + b * 64u, qd + so + (uint64_t)(kk * 2),
+          tc_mma_f16_pair(tmem + b * 64u, qd + so * qs + (uint64_t)(kk * 2),
                           kd + so + (uint64_t)(kk * 2), is, kk != 0);
         else
-          tc_mma_f16(tmem + b * 64u, qd + so + (uint64_t)(kk * 2), kd + so + (uint64_t)(kk * 2),
-                     is, kk != 0);
+          tc_mma_f16(tmem + b * 64u, qd + so * qs + (uint64_t)(kk * 2),
+                     kd + so + (uint64_t)(kk * 2), is, kk != 0);
       }
       if (PAIR)
         tc_commit_pair(smem_u32(&s.att_s_full[b]), 3);
@@ -955,11 +971,11 @@ __device__ __noinline__ bool mma_attn(const Params& p, Smem& s, uint32_t st, uin
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         if (PAIR)
-          tc_mma_f16_pair(tmem + 128u, pd + (uint64_t)(kk * 2), vd + so + (uint64_t)kk * vk, io,
-                          (j | kk) != 0);
+          tc_mma_f16_pair(tmem + 128u, pd + so * ps + (uint64_t)(kk * 2),
+                          vd + so + (uint64_t)kk * vk, io, (j | kk) != 0);
         else
-          tc_mma_f16(tmem + 128u, pd + (uint64_t)(kk * 2), vd + so + (uint64_t)kk * vk, io,
-                     (j | kk) != 0);
+          tc_mma_f16(tmem + 128u, pd + so * ps + (uint64_t)(kk * 2), vd + so + (uint64_t)kk * vk,
+                     io, (j | kk) != 0);
       }
       if (PAIR) {
         tc_commit_pair(smem_u32(&s.att_o_full[b]), 3);
@@ -974,7 +990,8 @@ __device__ __noinline__ bool mma_attn(const Params& p, Smem& s, uint32_t st, uin
   }
   // The compute warps have read every S and O block of this instruction before TMEM is reused.
   const uint32_t nl = n0 + (uint32_t)nb - 1u;
-  if (!wait_warp(p, smem_u32(&s.att_o_free[nl & 1u]), (nl >> 1) & 1u, R_MMA, 27, idx, PAIR))
+  if (PAIR ? !wait_warp(p, smem_u32(&s.att_done), q_par, R_MMA, 27, idx, true)
+           : !wait_warp(p, smem_u32(&s.att_o_free[nl & 1u]), (nl >> 1) & 1u, R_MMA, 27, idx))
     return false;
   n = n0 + (uint32_t)nb;
   return true;
@@ -995,7 +1012,7 @@ __device__ void run_mma(const Params& p, Smem& s, uint32_t tmem) {
   // K slice is 16 rows of 128 B (128 units).
   const uint64_t bdesc0 = sdesc_sw128(ring0 + kGemmTileM * kGemmBK * 2, 8192, 1024);
   RingPos rp;
-  uint32_t acc_n = 0, att_n = 0, gx_n = 0;
+  uint32_t acc_n = 0, att_n = 0, att_i = 0, gx_n = 0;  // att_i: pair attention instructions
   bool issued = false, synced = true;
   const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
   for (int it = 0;; ++it) {
@@ -1059,11 +1076,12 @@ __device__ void run_mma(const Params& p, Smem& s, uint32_t tmem) {
                         (((acc_n + k) >> 1) & 1u) ^ 1u, R_MMA, 21, idx, PAIR);
         if (!w) break;
         tc_fence_after();
-        if (!mma_attn<PAIR>(p, s, rp.st, rp.ph, NS, nb, tmem, att_n, idx)) {
+        if (!mma_attn<PAIR>(p, s, rp.st, rp.ph, NS, nb, tmem, att_n, att_i & 1u, idx)) {
           issued = true;
           break;
         }
         issued = true;
+        ++att_i;
         rp.advance((uint32_t)nb, NS);
       }
     } else if (ks_has_gemv(KS) && in.op == OP_GEMV && gemv_on_tensor<PAIR>(in, nd)) {
@@ -2592,7 +2610,7 @@ __device__ __noinline__ void attn_reduce_body(const Instr& in, const Node& nd) {
 template <bool PAIR>
 __device__ __noinline__ bool attn_prefill_body(const Params& p, Smem& s, const Instr& in,
                                                const Node& nd, uint32_t tmem, uint32_t& n,
-                                               int idx) {
+                                               uint32_t ring, int slot, uint32_t use, int idx) {
   const int ct = (int)threadIdx.x - (kThreads - kCompute);
   const int lane = ct & 31;
   const uint32_t lanes = (uint32_t)((ct >> 5) * 32) << 16;  // this warp's TMEM lane quarter
@@ -2607,6 +2625,22 @@ __device__ __noinline__ bool attn_prefill_body(const Params& p, Smem& s, const I
     else
       mbar_arrive(smem_u32(&bar));
   };
+  if (PAIR && nb > 0) {
+    // this CTA's query rows into xr for the whole instruction, counted on the even CTA's
+    // barrier, once the sources are complete (earlier uses of xr by this warpgroup are
+    // finished: its generic writes are fenced first)
+    if (!cw_wait(p, smem_u32(&s.deps_ready[slot]), use & 1u, 45, idx)) return false;
+    fence_proxy_async_shared();
+    cw_sync();
+    if (ct == 0) {
+      fence_proxy_async_global();  // the producers' stores before this copy reads them
+      const uint32_t bar = smem_u32(&s.att_q_full);
+      if (cluster_ctarank() == 0) mbar_expect_tx(bar, 2u * 16384u);
+      tma_load_2d_pair(smem_u32(s.xr), tmap_at(p, nd.a.tmap), mapa_shared(bar, 0), in.n0 * 64,
+                       row - ct);
+    }
+  }
+  const uint32_t NS = ring_n(p), sb = stage_bytes(p);
   const int qpos = nd.pos0 + row;
   const int kmax = in.klen;
   const float sl2 = nd.scale * 1.4426950408889634f;  // scores in log2 units
@@ -2639,7 +2673,8 @@ __device__ __noinline__ bool attn_prefill_body(const Params& p, Smem& s, const I
     tmem_ld_wait();
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) arrive_mma(s.att_s_free[b]);
+    // pair: no arrival here (the even CTA's MMA infers it from P_j, below)
+    if (!PAIR && lane == 0) arrive_mma(s.att_s_free[b]);
     const int key0 = j * kAttnKeyBlock;
     const int lim = nd.causal ? min(kmax, qpos + 1) : kmax;  // keys [0, lim) are visible
     // raw scores; masked keys only in a block that reaches the row's limit
@@ -2681,9 +2716,12 @@ __device__ __noinline__ bool attn_prefill_body(const Params& p, Smem& s, const I
     const float ls = (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
     l = fmaf(l, alpha, ls);
     m = mn;
+    // single CTA: P_j goes to the one P buffer once P V of the previous block has read it;
+    // pair: P_j has a buffer of its own, so O is waited for only to rescale it
+    const bool rescale = __any_sync(FULL, need);
     if (j > 0) {
-      if (!o_done(nn - 1u)) return false;
-      if (__any_sync(FULL, need)) {  // rescale this warp's rows of O (alpha = 1 where not needed)
+      if ((!PAIR || rescale) && !o_done(nn - 1u)) return false;
+      if (rescale) {  // rescale this warp's rows of O (alpha = 1 where not needed)
         uint32_t o0[32], o1[32];
         tmem_ld32(otm, o0);
         tmem_ld32(otm + 32u, o1);
@@ -2697,11 +2735,12 @@ __device__ __noinline__ bool attn_prefill_body(const Params& p, Smem& s, const I
         tmem_st32(otm + 32u, o1);
         tmem_st_wait();
       }
-      o_release(nn - 1u);
+      if (!PAIR) o_release(nn - 1u);  // pair: one arrival when O is read at the end
     }
+    uint8_t* Pj = PAIR ? s.ring + (size_t)((ring + (uint32_t)j) % NS) * sb + 8192 : P;
 #pragma unroll
     for (int ch = 0; ch < 8; ++ch)
-      *reinterpret_cast<uint4*>(P + ct * 128 + ((ch ^ (ct & 7)) << 4)) = pk[ch];
+      *reinterpret_cast<uint4*>(Pj + ct * 128 + ((ch ^ (ct & 7)) << 4)) = pk[ch];
     if (PAIR)
       fence_proxy_async_all();  // the even CTA's pair MMA reads this CTA's P
     else
@@ -2718,7 +2757,13 @@ __device__ __noinline__ bool attn_prefill_body(const Params& p, Smem& s, const I
   tmem_ld32(otm, o0);
   tmem_ld32(otm + 32u, o1);
   tmem_ld_wait();
-  o_release(nl);
+  if (PAIR) {  // the tile's TMEM may be reused once both CTAs have read O
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) arrive_mma(s.att_done);
+  } else {
+    o_release(nl);
+  }
   if (row < nd.M) {
     const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
@@ -2793,7 +2838,7 @@ __device__ void run_compute(const Params& p, Smem& s, uint32_t tmem) {
           if (ring_stages(in) > 0) synced = true;
           // inputs reach this warpgroup only through the loader and the MMAs, which wait
           trace_mark(p, idx, 2);
-          ok = attn_prefill_body<PAIR>(p, s, in, nd, tmem, att_n, idx);
+          ok = attn_prefill_body<PAIR>(p, s, in, nd, tmem, att_n, ring, slot, use, idx);
           ok = bar_and(kBarCompute, kCompute, ok);  // its warps waited on their own
           ring += (uint32_t)ring_stages(in);
         }
@@ -2885,6 +2930,8 @@ __global__ void __launch_bounds__(kThreads, 1) megakernel(const __grid_constant_
       mbar_init(smem_u32(&s.att_o_free[i]), PAIR ? 8 : 4);
     }
     mbar_init(smem_u32(&s.att_p_full), PAIR ? 8 : 4);
+    mbar_init(smem_u32(&s.att_q_full), 1);
+    mbar_init(smem_u32(&s.att_done), 8);
     mbar_fence_init();
   }
   if (ks_has_tmem(KS) && warp == 2) {
