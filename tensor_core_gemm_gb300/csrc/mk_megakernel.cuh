@@ -2444,39 +2444,56 @@ __device__ __forceinline__ void argmax_reduce_body(const Instr& in, const Node& 
 // m = max s, l = sum e^{s - m}, o = sum e^{s - m} v   (head_dim 64, up to 128 keys).
 // Keys and values arrive by TMA in one ring stage, 128-byte swizzled (16-byte chunk c of row r
 // sits at chunk c ^ (r & 7)).
-__device__ bool attn_partial_body(const Params& p, Smem& s, const Instr& in, const Node& nd,
-                                  uint32_t& ring, int idx) {
+__device__ __noinline__ bool attn_partial_body(const Params& p, Smem& s, const Instr& in,
+                                               const Node& nd, uint32_t& ring, int idx) {
   const uint32_t NS = ring_n(p);
   const int ct = (int)threadIdx.x - (kThreads - kCompute);
   const int wp = ct >> 5, lane = ct & 31;
   const int g = in.n0, G = nd.hq / nd.hkv, C = in.aux1, c = in.aux0;
   const int kl = in.klen;
   const int st = (int)(ring % NS);
+  // the query head's 64 values are in flight while the key/value chunk lands (a warp per head;
+  // G <= 4 heads per key/value head keeps this one pass)
+  uint4 qraw[8];
+  if (wp < G) {
+    const uint16_t* qp = reinterpret_cast<const uint16_t*>(nd.a.ptr) + (g * G + wp) * 64;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) qraw[i] = __ldcg(reinterpret_cast<const uint4*>(qp + i * 8));
+  }
   if (!cw_wait(p, smem_u32(&s.full[st]), (ring / NS) & 1u, 42, idx)) return false;
-  const uint8_t* Ks = stage_ptr(s, p, st);
-  const uint8_t* Vs = stage_ptr(s, p, st) + 16384;
+  const uint32_t kb = smem_u32(stage_ptr(s, p, st)), vb = kb + 16384;
   for (int hh = wp; hh < G; hh += 4) {
     const int h = g * G + hh;
     float qv[64];
+    if (hh == wp) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) load8(nd.a, 0, h * 64 + i * 8, DT_BF16, qv + i * 8);
+      for (int i = 0; i < 8; ++i) unpack8(qraw[i], DT_BF16, qv + i * 8);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) load8(nd.a, 0, h * 64 + i * 8, DT_BF16, qv + i * 8);
+    }
+    // scores: lane holds keys lane + 32t; each key's eight 16-byte chunks are loaded before its
+    // dot product, which sums in four interleaved partial sums
     float sc[4], pr[4];
     float mx = -INFINITY;
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
       const int j = lane + 32 * t;
       float sv = -INFINITY;
-      if (j < kl) {
-        float dot = 0.f;
+      if (32 * t < kl) {
+        uint4 kr[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          kr[i] = j < kl ? lds_u128(kb + j * 128 + ((i ^ (j & 7)) << 4)) : make_uint4(0, 0, 0, 0);
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           float kx[8];
-          unpack8(*reinterpret_cast<const uint4*>(Ks + j * 128 + ((i ^ (j & 7)) << 4)), DT_BF16,
-                  kx);
+          unpack8(kr[i], DT_BF16, kx);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) dot = fmaf(qv[i * 8 + e], kx[e], dot);
+          for (int e = 0; e < 8; ++e) d[e & 3] = fmaf(qv[i * 8 + e], kx[e], d[e & 3]);
         }
-        sv = dot * nd.scale;
+        if (j < kl) sv = ((d[0] + d[1]) + (d[2] + d[3])) * nd.scale;
       }
       sc[t] = sv;
       mx = fmaxf(mx, sv);
@@ -2489,8 +2506,11 @@ __device__ bool attn_partial_body(const Params& p, Smem& s, const Instr& in, con
       l += pr[t];
     }
     l = warp_sum(l);
-    // lane owns value columns 2*lane, 2*lane+1: 16-byte chunk lane/4, 4-byte word lane%4
-    float o0 = 0.f, o1 = 0.f;
+    // lane owns value columns 2*lane, 2*lane+1: 16-byte chunk lane/4, 4-byte word lane%4; four
+    // interleaved partial sums over the keys
+    float oa[4][2];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) oa[u][0] = oa[u][1] = 0.f;
     const int chunk = lane >> 2, word = lane & 3;
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
@@ -2500,13 +2520,14 @@ __device__ bool attn_partial_body(const Params& p, Smem& s, const Instr& in, con
         const int j = t * 32 + jj;
         const float pj = __shfl_sync(FULL, pr[t], jj);
         if (j < kl) {
-          const uint32_t vv = *reinterpret_cast<const uint32_t*>(
-              Vs + j * 128 + ((chunk ^ (j & 7)) << 4) + word * 4);
-          o0 = fmaf(pj, __uint_as_float(vv << 16), o0);
-          o1 = fmaf(pj, __uint_as_float(vv & 0xffff0000u), o1);
+          const uint32_t vv = lds_u32(vb + j * 128 + ((chunk ^ (j & 7)) << 4) + word * 4);
+          oa[jj & 3][0] = fmaf(pj, __uint_as_float(vv << 16), oa[jj & 3][0]);
+          oa[jj & 3][1] = fmaf(pj, __uint_as_float(vv & 0xffff0000u), oa[jj & 3][1]);
         }
       }
     }
+    const float o0 = (oa[0][0] + oa[1][0]) + (oa[2][0] + oa[3][0]);
+    const float o1 = (oa[0][1] + oa[1][1]) + (oa[2][1] + oa[3][1]);
     float* row = reinterpret_cast<float*>(nd.scratch.ptr) +
                  ((size_t)(g * C + c) * G + hh) * nd.scratch.ld;
     __stcg(reinterpret_cast<float2*>(row + lane * 2), make_float2(o0, o1));

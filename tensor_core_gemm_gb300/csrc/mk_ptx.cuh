@@ -118,6 +118,19 @@ __device__ __forceinline__ void tensormap_acquire(const void* tmap) {
 }
 // Generic-proxy writes to shared memory by this thread become visible to the async proxy
 // (tensor-core operand reads, TMA stores) that later synchronisation orders after them.
+// Shared-memory loads through a 32-bit shared-window address (no generic-address resolution).
+__device__ __forceinline__ uint4 lds_u128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
 __device__ __forceinline__ void fence_proxy_async_shared() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
