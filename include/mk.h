@@ -187,9 +187,11 @@ typedef struct {
   int32_t snapshot_counters; /* 1: keep each run's final counter values for mk_get_counters */
   int32_t trace;         /* 1: record per-instruction timestamps for mk_get_trace */
   int32_t gemm_split_tail; /* 1: the GEMM tiles of a matmul's last, partly filled wave are
-                            split along K, the last split to finish sums the fp32 partials
-                            and runs the epilogue; 0 (default): never split. Measured slower
-                            on the 4096^3 GEMM: the last split's sum is latency-bound */
+                            split along K. With two splits and no SILU_MUL each split stores
+                            the half of its fp32 partial the other finishes and both finish
+                            their half (the later one releases the counters); otherwise the
+                            last split to finish sums the partials and runs the epilogue.
+                            0 (default): never split */
   int32_t fuse_rope;     /* 1 (default): a ROPE node right after a matmul that lowers to GEMV
                             tiles, reading exactly its output (head_dim 64, output width a
                             multiple of gemv_tile_n), runs inside those tiles; 0: never */

@@ -37,8 +37,9 @@ Lowering rules per node (tile sizes come from ``opts``; see ``DEFAULT_OPTS``):
       ceil(K/chunk); order: tile, then split, then rank; k0/klen = the split's K range, aux0 =
       rank, aux1 = number of splits. A split reads A and B on its K range, bias/residual on the
       tile box; only split 0 carries the output box; every split carries split 0's arrivals (of
-      the same rank), because the last split to finish sums the partials and publishes. Each
-      (tile, rank) owns one split semaphore.
+      the same rank), because the split that publishes is known only at run time (the last to
+      finish; with two splits and no b2, each split finishes half the columns and the later of
+      the two publishes). Each (tile, rank) owns one split semaphore.
   matmul, M <= gemv_max_m -> GEMV tiles: column tiles of gemv_tile_n (halved with b2), each
       split along K into S chunks (gemv_splits, or max(1, n_sm div n_col_tiles) when 0); the
       chunk length is ceil(K/S) rounded up to gemv_kstep (at least gemv_kstep) and S is then
@@ -132,7 +133,7 @@ def _full(ref):
 
 class Instr:
     __slots__ = ("op", "flags", "node", "m0", "n0", "k0", "klen", "aux0", "aux1", "sem",
-                 "reads", "writes", "src", "dst", "tile")
+                 "reads", "writes", "src", "dst", "tile", "sem_adds")
 
     def __init__(self, op, node, m0=0, n0=0, k0=0, klen=0, aux0=0, aux1=0):
         self.op, self.node = op, node
@@ -144,6 +145,7 @@ class Instr:
         self.src = []        # (counter, target)
         self.dst = []        # counter ids
         self.tile = None     # GEMV tile ordinal (shares arrivals and semaphore)
+        self.sem_adds = 1    # increments of its split semaphore in one run
 
     def key(self):
         return (self.op, self.flags, self.node, self.m0, self.n0, self.k0, self.klen,
@@ -261,6 +263,8 @@ def _lower_matmul(ni, nd, opts, phases, sem_tiles, rope=None):
                     ins = Instr(OP_GEMM, ni, m0, n0, k0, kl, r, 0 if base is None else len(ranges))
                     if base is not None:
                         ins.tile = base + r
+                        # two splits without b2 meet twice at the semaphore (exchange, finish)
+                        ins.sem_adds = 2 if (len(ranges) == 2 and b2 is None) else 1
                     ins.reads.append((_box(a, m0, m0 + tm, k0, k0 + kl), ROLE_A))
                     ins.reads.append((_box(b, k0, k0 + kl, n0, n0 + tn), ROLE_B))
                     if b2 is not None:
@@ -621,13 +625,14 @@ class Plan:
         return i % self.n_sm, i // self.n_sm
 
     def final_counters(self):
-        """Value of every counter after one complete run: deps reach their targets, each GEMV
-        tile's split semaphore counts its splits."""
+        """Value of every counter after one complete run: deps reach their targets, each split
+        semaphore counts its splits' increments (one per split; two for each split of a GEMM
+        tile with exactly two splits and no b2, whose splits exchange halves and then finish)."""
         sems = [0] * self.n_sem
         for ins in self.instrs:
             if (ins.op == OP_GEMV or (ins.op == OP_GEMM and ins.aux1 > 0)
                     or (ins.op == OP_ATTN_PARTIAL and ins.tile is not None)):
-                sems[ins.sem - self.n_dep] += 1
+                sems[ins.sem - self.n_dep] += ins.sem_adds
         return list(self.targets) + sems
 
     def records(self):

@@ -202,6 +202,32 @@ __device__ void wait_mbar_drain(uint32_t bar, uint32_t parity) {
   while (!mbar_try(bar, parity))
     if (globaltimer() - t0 > 200000000ull) return;
 }
+// Compute warpgroup: its first thread polls a global counter until it reaches `target`
+// (acquire, bounded like every wait), then all threads agree on the outcome.
+__device__ bool cw_wait_counter(const Params& p, const int32_t* ctr, int target, int where,
+                                int instr) {
+  bool ok = true;
+  if (threadIdx.x == kThreads - kCompute && ld_acquire(ctr) < target) {
+    const uint64_t t0 = globaltimer();
+    for (uint32_t n = 1;; ++n) {
+      if (ld_acquire(ctr) >= target) break;
+      if ((n & 15u) == 0) {
+        if (ld_volatile(p.status + ST_CODE) != 0) {
+          ok = false;
+          break;
+        }
+        if (globaltimer() - t0 > p.timeout_ns) {
+          report(p, MK_ERR_TIMEOUT, instr, (int)(ctr - p.counters), ld_volatile(ctr), target,
+                 R_COMPUTE, where);
+          ok = false;
+          break;
+        }
+      }
+    }
+  }
+  return bar_and(kBarCompute, kCompute, ok);
+}
+
 // Compute-warpgroup wait: every thread waits (bounded), then all agree on the outcome so no
 // thread is left alone at a later named barrier.
 __device__ __forceinline__ bool cw_wait(const Params& p, uint32_t bar, uint32_t parity, int where,
@@ -1240,10 +1266,10 @@ __device__ __noinline__ void epi_chunks(uint32_t tb, int tn, int nk, uint32_t fl
 
 // One call site for the four epilogue loops (SiLU·mul or not, bias / residual or not); the
 // node's fields are read here, so few values are live across the call.
-__device__ __noinline__ void epi_tile(const Node& nd, int n0, uint32_t tb, int nk,
+__device__ __noinline__ void epi_tile(const Node& nd, int n0, int tn, uint32_t tb, int nk,
                                       const void* omap, uint32_t xr, int row0) {
   const uint32_t flags = nd.flags;
-  const int tn = nd.tile_n, dt = nd.dtype, M = nd.M, N = nd.N;
+  const int dt = nd.dtype, M = nd.M, N = nd.N;
   const uint16_t* bias = reinterpret_cast<const uint16_t*>(nd.bias.ptr);
   const uint16_t* res = reinterpret_cast<const uint16_t*>(nd.res.ptr);
   const int ldb = nd.bias.ld, ldr = nd.res.ld;
@@ -1263,9 +1289,10 @@ __device__ __noinline__ void epi_tile(const Node& nd, int n0, uint32_t tb, int n
 // Split-tail partials. A (split, rank) slot holds a CTA's 128 rows x W fp32 columns warp by
 // warp and, inside a warp's 32 rows, column group by column group: the float4 of columns
 // 4j..4j+3 of lane l (row 32q + l) is element (q * W / 4 + j) * 32 + l, so every warp-wide load
-// or store is 512 contiguous bytes. `dst` points at this warp's block and lane.
-__device__ __noinline__ void split_store(uint32_t tb, int W, int nk, float4* dst) {
-  for (int c = 0; c < W; c += 32) {
+// or store is 512 contiguous bytes. `dst` points at this warp's block and lane; columns
+// [c0, c1) are stored.
+__device__ __noinline__ void split_store(uint32_t tb, int c0, int c1, int nk, float4* dst) {
+  for (int c = c0; c < c1; c += 32) {
     uint32_t r[32];
     if (nk > 0) {
       tmem_ld32(tb + (uint32_t)c, r);
@@ -1289,8 +1316,10 @@ __device__ __noinline__ void split_store(uint32_t tb, int W, int nk, float4* dst
 // is in flight while a chunk is finished; otherwise each chunk's loads of one partial go out
 // together.
 // `parts` is this warp's block and lane in split 0's slot; pstride the float4 between splits.
+// Columns [c0, c1) of the tile are finished (of each weight's tn with SiLU·mul).
 template <bool DUAL, bool SIDE>
-__device__ __noinline__ void epi_split(uint32_t tb, int tn, int nk, uint32_t flags, int dt,
+__device__ __noinline__ void epi_split(uint32_t tb, int tn, int c0, int c1, int nk,
+                                       uint32_t flags, int dt,
                                        const uint16_t* bias, int ldb, const uint16_t* res,
                                        int ldr, const void* omap, uint32_t xr, int row0, int n0,
                                        int M, int N, const float4* parts, int S, int mine,
@@ -1358,7 +1387,7 @@ __device__ __noinline__ void epi_split(uint32_t tb, int tn, int nk, uint32_t fla
         sr[g] = __ldcg(reinterpret_cast<const uint4*>(res + (size_t)row * ldr + col));
     }
     const uint32_t buf = xr + (uint32_t)((c >> 5) & 1) * 2048u;
-    if (c >= 64) {
+    if (c - c0 >= 64) {
       if (lane == 0) bulk_wait_read_1();
       __syncwarp();
     }
@@ -1400,8 +1429,8 @@ __device__ __noinline__ void epi_split(uint32_t tb, int tn, int nk, uint32_t fla
     // prefetch raises this callee's registers enough to make the kernel function spill)
     const float4* other = parts + (size_t)(1 - mine) * pstride;
     float4 a[V];
-    issue(0, other, a);
-    for (int c = 0; c < tn; c += 32) {
+    issue(c0, other, a);
+    for (int c = c0; c < c1; c += 32) {
       float w[32], u[1];
 #pragma unroll
       for (int i = 0; i < 32; ++i) w[i] = 0.f;
@@ -1412,11 +1441,11 @@ __device__ __noinline__ void epi_split(uint32_t tb, int tn, int nk, uint32_t fla
         add_part(w, u, a);
         add_own(c, w, u);
       }
-      if (c + 32 < tn) issue(c + 32, other, a);
+      if (c + 32 < c1) issue(c + 32, other, a);
       finish(c, w, u);
     }
   } else {
-    for (int c = 0; c < tn; c += 32) {
+    for (int c = c0; c < c1; c += 32) {
       float w[32], u[DUAL ? 32 : 1];
 #pragma unroll
       for (int i = 0; i < 32; ++i) w[i] = 0.f;
@@ -1526,8 +1555,8 @@ __device__ __noinline__ void epi_rope(const Params& p, const Node& nd, int n0, u
 }
 
 // One call site for the four split epilogues, like epi_tile.
-__device__ __noinline__ void epi_split_tile(const Node& nd, int n0, uint32_t tb, int nk,
-                                            const void* omap, uint32_t xr, int row0,
+__device__ __noinline__ void epi_split_tile(const Node& nd, int n0, int c0, int c1, uint32_t tb,
+                                            int nk, const void* omap, uint32_t xr, int row0,
                                             const float4* parts, int S, int mine,
                                             size_t pstride) {
   const uint32_t flags = nd.flags;
@@ -1538,17 +1567,17 @@ __device__ __noinline__ void epi_split_tile(const Node& nd, int n0, uint32_t tb,
   const bool dual = (flags & EPI_SILU_MUL) != 0;
   const bool side = (flags & (EPI_BIAS | EPI_RESIDUAL)) != 0;
   if (dual && side)
-    epi_split<true, true>(tb, tn, nk, flags, dt, bias, ldb, res, ldr, omap, xr, row0, n0, M, N,
-                          parts, S, mine, pstride);
+    epi_split<true, true>(tb, tn, c0, c1, nk, flags, dt, bias, ldb, res, ldr, omap, xr, row0, n0,
+                          M, N, parts, S, mine, pstride);
   else if (dual)
-    epi_split<true, false>(tb, tn, nk, flags, dt, bias, ldb, res, ldr, omap, xr, row0, n0, M, N,
-                           parts, S, mine, pstride);
+    epi_split<true, false>(tb, tn, c0, c1, nk, flags, dt, bias, ldb, res, ldr, omap, xr, row0,
+                           n0, M, N, parts, S, mine, pstride);
   else if (side)
-    epi_split<false, true>(tb, tn, nk, flags, dt, bias, ldb, res, ldr, omap, xr, row0, n0, M, N,
-                           parts, S, mine, pstride);
+    epi_split<false, true>(tb, tn, c0, c1, nk, flags, dt, bias, ldb, res, ldr, omap, xr, row0,
+                           n0, M, N, parts, S, mine, pstride);
   else
-    epi_split<false, false>(tb, tn, nk, flags, dt, bias, ldb, res, ldr, omap, xr, row0, n0, M,
-                            N, parts, S, mine, pstride);
+    epi_split<false, false>(tb, tn, c0, c1, nk, flags, dt, bias, ldb, res, ldr, omap, xr, row0,
+                            n0, M, N, parts, S, mine, pstride);
 }
 
 // GEMM epilogue: TMEM -> registers (one row per thread), fused epilogue, then per 32-column chunk
@@ -1599,7 +1628,48 @@ __device__ bool gemm_epilogue(const Params& p, Smem& s, const Instr& in, const N
   // stores it with TMA; a buffer is rewritten once the store issued from it has read it.
   const uint32_t xr0 = smem_u32(s.xr) + (uint32_t)q * 4096u;
   const void* omap = tmap_at(p, nd.out.tmap);
-  if (in.aux1 > 0) {
+  if (in.aux1 == 2 && !dual) {
+    // Two-split tail, both splits finishing: split s owns columns [s h, s h + h) of the tile
+    // (h = tn / 2). Each stores the half of its fp32 partial the other owns, meets the other at
+    // the tile's semaphore (count 2: the two splits are consecutive instructions, so neither
+    // waits on work queued behind the other), sums its half in split order and runs that half's
+    // epilogue. A second round on the semaphore (count 4) lets the split that finishes last
+    // publish, once both halves' stores are in global memory.
+    const int h = tn / 2, own0 = in.split * h, cl = PAIR ? 2 : 1;
+    const size_t slot_f4 = (size_t)kGemmTileM * tn / 4;  // float4 per (split, rank) slot
+    const size_t pstride = (size_t)cl * slot_f4;          // next split, same rank
+    float4* part0 = reinterpret_cast<float4*>(nd.scratch.ptr) + (size_t)in.slot * slot_f4 +
+                    (size_t)q * 8 * tn + lane;  // this warp's block of split 0, this lane
+    split_store(tb, h - own0, tn - own0, nk, part0 + (size_t)in.split * pstride);
+    __threadfence();
+    cw_sync();
+    if (ct == 0) red_relaxed_add(p.counters + in.sem, 1);
+    if (!cw_wait_counter(p, p.counters + in.sem, 2, 47, idx)) return false;
+    trace_mark(p, idx, 7);
+    __threadfence();
+    epi_split_tile(nd, in.n0, own0, own0 + h, tb, nk, omap, xr0, row0, part0, 2, in.split,
+                   pstride);
+    release_tmem();
+    if (in.n_dst == 0) {  // nothing to publish: the second round only counts
+      if (ct == 0) red_relaxed_add(p.counters + in.sem, 1);
+      if (lane == 0) bulk_wait_read_all();
+      *publish = false;
+      return true;
+    }
+    if (lane == 0) {
+      bulk_wait_all();
+      fence_proxy_async_global();
+    }
+    __threadfence();
+    cw_sync();
+    if (ct == 0) s.flag = atomicAdd(p.counters + in.sem, 1) == 3;
+    cw_sync();
+    if (!s.flag) {
+      *publish = false;
+      return true;
+    }
+    __threadfence();
+  } else if (in.aux1 > 0) {
     // Split tail: every split stores its fp32 partial (gate columns, then up columns with
     // SiLU·mul); the last split to reach the tile's semaphore sums them and runs the epilogue.
     const int W = dual ? 2 * tn : tn, S = in.aux1, cl = PAIR ? 2 : 1;
@@ -1607,7 +1677,7 @@ __device__ bool gemm_epilogue(const Params& p, Smem& s, const Instr& in, const N
     const size_t pstride = (size_t)cl * slot_f4;          // next split, same rank
     float4* part0 = reinterpret_cast<float4*>(nd.scratch.ptr) + (size_t)in.slot * slot_f4 +
                     (size_t)q * 8 * W + lane;  // this warp's block of split 0, this lane
-    split_store(tb, W, nk, part0 + (size_t)in.split * pstride);
+    split_store(tb, 0, W, nk, part0 + (size_t)in.split * pstride);
     __threadfence();
     cw_sync();
     if (ct == 0) s.flag = atomicAdd(p.counters + in.sem, 1) == S - 1;
@@ -1618,14 +1688,14 @@ __device__ bool gemm_epilogue(const Params& p, Smem& s, const Instr& in, const N
       return true;
     }
     __threadfence();
-    epi_split_tile(nd, in.n0, tb, nk, omap, xr0, row0, part0, S, in.split, pstride);
+    epi_split_tile(nd, in.n0, 0, tn, tb, nk, omap, xr0, row0, part0, S, in.split, pstride);
     release_tmem();
   } else if (nd.flags & NF_ROPE) {
     epi_rope(p, nd, in.n0, tb, nk, xr0, row0);
     release_tmem();
   } else {
     if constexpr (KS == KS_GEMM) {
-      epi_tile(nd, in.n0, tb, nk, omap, xr0, row0);
+      epi_tile(nd, in.n0, tn, tb, nk, omap, xr0, row0);
     } else {
       const uint16_t* bp = reinterpret_cast<const uint16_t*>(nd.bias.ptr);
       const uint16_t* rp = reinterpret_cast<const uint16_t*>(nd.res.ptr);
@@ -1639,10 +1709,15 @@ __device__ bool gemm_epilogue(const Params& p, Smem& s, const Instr& in, const N
     }
     release_tmem();
   }
-  // the tile's stores are in global memory before its counters are released
+  // the tile's stores are in global memory before its counters are released; with no counter
+  // to release, the staging buffers need only have been read
   if (lane == 0) {
-    bulk_wait_all();
-    fence_proxy_async_global();
+    if (in.n_dst > 0) {
+      bulk_wait_all();
+      fence_proxy_async_global();
+    } else {
+      bulk_wait_read_all();
+    }
   }
   return true;
 }
@@ -2889,7 +2964,7 @@ __device__ void run_compute(const Params& p, Smem& s, uint32_t tmem) {
     // Publish: every thread's stores are ordered before the release increments. One counter:
     // a release increment. More: the first warp loads the counter ids together, then one
     // release fence and relaxed increments (a release increment each would wait on the last).
-    __threadfence();
+    if (publish && in.n_dst > 0) __threadfence();
     cw_sync();
     if (ct < 32 && publish && in.n_dst > 1) {
       if (ct == 0) {

@@ -855,6 +855,55 @@ def test_split_tail_epilogues(pair):
     assert_close(f32(o3), f32(first), "split vs unsplit")
 
 
+@pytest.mark.parametrize("pair", [False, True])
+def test_split_tail_two_splits_exchange_halves(pair):
+    """A tail of exactly two K splits per tile (n_sm chosen so): each split stores the half of its
+    partial the other finishes, both finish their half (bias + ReLU + residual, plain, ragged last
+    column tile), the later one publishes; SiLU·mul tiles keep the last-split sum. Counters and
+    semaphores end at the oracle's values; a consumer GEMV reads the split tiles' output."""
+    full = workloads.full
+    m, n, k = (768, 1000, 384) if pair else (384, 1000, 256)
+    opts = dict(gemm_tile_m=256, cluster=2, gemm_tile_n=256) if pair else dict(gemm_tile_n=256)
+    opts.update(n_sm=16 if pair else 8, gemm_split_tail=1)
+    shapes = [(m, k), (k, n), (k, n), (m, n), (m, n), (m, n), (m, n), (m, n), (n, 256), (1, 256)]
+    desc = {"tensors": [{"rows": r, "cols": c, "dtype": "bf16"} for r, c in shapes],
+            "nodes": [
+                {"kind": "matmul", "a": full(0, m, k), "b": full(1, k, n), "c": full(5, m, n),
+                 "bias": full(3, m, n), "relu": True, "residual": full(4, m, n)},
+                {"kind": "matmul", "a": full(0, m, k), "b": full(1, k, n), "b2": full(2, k, n),
+                 "c": full(6, m, n)},
+                {"kind": "matmul", "a": full(0, m, k), "b": full(1, k, n), "c": full(7, m, n)},
+                {"kind": "matmul", "a": (5, m - 1, 0, 1, n), "b": full(8, n, 256),
+                 "c": full(9, 1, 256)}]}
+    data = [synth.normal((m, k), 1.0, "bf16", 41, DEV),
+            synth.normal((k, n), 1 / math.sqrt(k), "bf16", 42, DEV),
+            synth.normal((k, n), 1 / math.sqrt(k), "bf16", 43, DEV),
+            synth.normal((m, n), 0.5, "bf16", 44, DEV),
+            synth.normal((m, n), 1.0, "bf16", 45, DEV)]
+    data += [torch.zeros((m, n), dtype=torch.bfloat16, device=DEV) for _ in range(3)]
+    data += [synth.normal((n, 256), 1 / math.sqrt(n), "bf16", 46, DEV),
+             torch.zeros((1, 256), dtype=torch.bfloat16, device=DEV)]
+    g, _ = workloads.build_graph(desc, data)
+    p = g.compile(snapshot_counters=1, **opts)
+    ins = p.instructions()
+    gem = ins["op"] == osched.OP_GEMM
+    assert np.all(np.isin(ins["aux1"][gem], [0, 2])) and np.any(ins["aux1"][gem] == 2)
+    p.run()
+    p.check_status()
+    A, B, BU = f32(data[0]), f32(data[1]), f32(data[2])
+    ref1 = ops.matmul(A, B, BF16, bias=f32(data[3]), relu=True, residual=f32(data[4]))
+    assert_close(f32(data[5]), ref1, "two splits bias+relu+residual")
+    assert_close(f32(data[6]), ops.matmul_silu_mul(A, B, BU, BF16), "two splits silu_mul")
+    assert_close(f32(data[7]), ops.matmul(A, B, BF16), "two splits plain")
+    assert_close(f32(data[9]), ops.matmul(f32(data[5])[m - 1:], f32(data[8]), BF16),
+                 "consumer of split tiles")
+    assert p.counters().tolist() == osched.lower(desc, opts).final_counters()
+    first = data[7].clone()
+    p.run()
+    p.check_status()
+    assert torch.equal(data[7], first), "the split sum order is fixed"
+
+
 def test_pair_gemms_interleaved_with_gemvs():
     """Pair GEMM tiles after GEMV tiles in one launch: the two CTAs of a pair arrive with rings
     in different states and resynchronise; consecutive pair tiles stream on without it."""

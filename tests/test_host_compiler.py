@@ -135,7 +135,8 @@ def test_split_tail_plans(m, n, k, tm, tn, cl):
             assert np.all(mine["slot"] == mine["slot"][0])
     fin = py.final_counters()
     sem_vals = fin[py.n_dep:]
-    assert sem_vals.count(nr) == r_tail * cl
+    # two splits meet twice (exchange of halves, then finish); more splits once each
+    assert sem_vals.count(4 if nr == 2 else nr) == r_tail * cl
 
 
 def test_mlp3_plan():
