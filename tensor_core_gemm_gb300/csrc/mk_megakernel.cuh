@@ -1641,12 +1641,13 @@ __device__ bool gemm_epilogue(const Params& p, Smem& s, const Instr& in, const N
     float4* part0 = reinterpret_cast<float4*>(nd.scratch.ptr) + (size_t)in.slot * slot_f4 +
                     (size_t)q * 8 * tn + lane;  // this warp's block of split 0, this lane
     split_store(tb, h - own0, tn - own0, nk, part0 + (size_t)in.split * pstride);
-    __threadfence();
     cw_sync();
-    if (ct == 0) red_relaxed_add(p.counters + in.sem, 1);
+    if (ct == 0) {
+      fence_acq_rel_gpu();
+      red_relaxed_add(p.counters + in.sem, 1);
+    }
     if (!cw_wait_counter(p, p.counters + in.sem, 2, 47, idx)) return false;
     trace_mark(p, idx, 7);
-    __threadfence();
     epi_split_tile(nd, in.n0, own0, own0 + h, tb, nk, omap, xr0, row0, part0, 2, in.split,
                    pstride);
     release_tmem();
@@ -1660,15 +1661,17 @@ __device__ bool gemm_epilogue(const Params& p, Smem& s, const Instr& in, const N
       bulk_wait_all();
       fence_proxy_async_global();
     }
-    __threadfence();
     cw_sync();
-    if (ct == 0) s.flag = atomicAdd(p.counters + in.sem, 1) == 3;
+    if (ct == 0) {
+      fence_acq_rel_gpu();
+      s.flag = atomicAdd(p.counters + in.sem, 1) == 3;
+      fence_acq_rel_gpu();
+    }
     cw_sync();
     if (!s.flag) {
       *publish = false;
       return true;
     }
-    __threadfence();
   } else if (in.aux1 > 0) {
     // Split tail: every split stores its fp32 partial (gate columns, then up columns with
     // SiLU·mul); the last split to reach the tile's semaphore sums them and runs the epilogue.
@@ -1678,16 +1681,18 @@ __device__ bool gemm_epilogue(const Params& p, Smem& s, const Instr& in, const N
     float4* part0 = reinterpret_cast<float4*>(nd.scratch.ptr) + (size_t)in.slot * slot_f4 +
                     (size_t)q * 8 * W + lane;  // this warp's block of split 0, this lane
     split_store(tb, 0, W, nk, part0 + (size_t)in.split * pstride);
-    __threadfence();
     cw_sync();
-    if (ct == 0) s.flag = atomicAdd(p.counters + in.sem, 1) == S - 1;
+    if (ct == 0) {
+      fence_acq_rel_gpu();
+      s.flag = atomicAdd(p.counters + in.sem, 1) == S - 1;
+      fence_acq_rel_gpu();
+    }
     cw_sync();
     if (!s.flag) {
       release_tmem();
       *publish = false;
       return true;
     }
-    __threadfence();
     epi_split_tile(nd, in.n0, 0, tn, tb, nk, omap, xr0, row0, part0, S, in.split, pstride);
     release_tmem();
   } else if (nd.flags & NF_ROPE) {
@@ -2106,15 +2111,19 @@ __device__ bool gemv(const Params& p, Smem& s, const Instr& in, const Node& nd, 
                                            ((size_t)which * M + m) * nd.N + n),
                  make_float2(acc[m][0], acc[m][1]));
     }
-    __threadfence();
+    // one thread releases the warpgroup's partials (ordered before it by the barrier) and, as
+    // the last split, acquires the others'
     cw_sync();
-    if (ct == 0) s.flag = (atomicAdd(p.counters + in.sem, 1) == S - 1);
+    if (ct == 0) {
+      fence_acq_rel_gpu();
+      s.flag = (atomicAdd(p.counters + in.sem, 1) == S - 1);
+      fence_acq_rel_gpu();
+    }
     cw_sync();
     if (!s.flag) {
       *publish = false;
       return true;
     }
-    __threadfence();
     if (colok) {
 #pragma unroll
       for (int m = 0; m < 8; ++m) {
@@ -2914,13 +2923,15 @@ __device__ void run_compute(const Params& p, Smem& s, uint32_t tmem) {
           trace_mark(p, idx, 6);
           if (ok && (nd.flags & NF_ATTN_FUSED)) {
             // the last partial of the key/value head to finish combines the head's partials
-            __threadfence();
             cw_sync();
-            if (ct == 0) s.flag = atomicAdd(p.counters + in.sem, 1) == in.aux1 - 1;
+            if (ct == 0) {
+              fence_acq_rel_gpu();
+              s.flag = atomicAdd(p.counters + in.sem, 1) == in.aux1 - 1;
+              fence_acq_rel_gpu();
+            }
             cw_sync();
             trace_mark(p, idx, 7);
             if (s.flag) {
-              __threadfence();
               attn_reduce_body(in, nd);
             } else {
               publish = false;
@@ -2961,10 +2972,10 @@ __device__ void run_compute(const Params& p, Smem& s, uint32_t tmem) {
     }
     if (!ok) break;
     trace_mark(p, idx, 3);
-    // Publish: every thread's stores are ordered before the release increments. One counter:
-    // a release increment. More: the first warp loads the counter ids together, then one
-    // release fence and relaxed increments (a release increment each would wait on the last).
-    if (publish && in.n_dst > 0) __threadfence();
+    // Publish: the barrier orders every thread's stores before the first thread's release
+    // (release is cumulative). One counter: a release increment. More: the first warp loads
+    // the counter ids together, then one release fence and relaxed increments (a release
+    // increment each would wait on the last).
     cw_sync();
     if (ct < 32 && publish && in.n_dst > 1) {
       if (ct == 0) {
