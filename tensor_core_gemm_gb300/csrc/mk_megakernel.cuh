@@ -284,19 +284,41 @@ __device__ __forceinline__ uint16_t f2h(float v, int dt) {
   return dt == DT_BF16 ? __bfloat16_as_ushort(__float2bfloat16_rn(v))
                        : __half_as_ushort(__float2half_rn(v));
 }
+// 8 packed elements <-> 8 floats. The element type is uniform, so one branch picks the path;
+// conversions go two elements at a time (one paired instruction each way), the same rounding
+// as element by element.
 __device__ __forceinline__ void unpack8(const uint4 raw, int dt, float* x) {
   const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+  if (dt == DT_BF16) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    x[2 * i] = h2f((uint16_t)(w[i] & 0xffffu), dt);
-    x[2 * i + 1] = h2f((uint16_t)(w[i] >> 16), dt);
+    for (int i = 0; i < 4; ++i) {
+      x[2 * i] = __uint_as_float(w[i] << 16);
+      x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+      x[2 * i] = f.x;
+      x[2 * i + 1] = f.y;
+    }
   }
 }
 __device__ __forceinline__ uint4 pack8(const float* x, int dt) {
   uint32_t w[4];
+  if (dt == DT_BF16) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
-    w[i] = (uint32_t)f2h(x[2 * i], dt) | ((uint32_t)f2h(x[2 * i + 1], dt) << 16);
+    for (int i = 0; i < 4; ++i) {
+      const __nv_bfloat162 t = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
+      w[i] = *reinterpret_cast<const uint32_t*>(&t);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __half2 t = __floats2half2_rn(x[2 * i], x[2 * i + 1]);
+      w[i] = *reinterpret_cast<const uint32_t*>(&t);
+    }
+  }
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 // 8 consecutive elements of an operand at (row, col); data produced inside the kernel is read
@@ -313,10 +335,29 @@ __device__ __forceinline__ float load1(const Operand& o, int row, int col, int d
   const uint16_t* ptr = reinterpret_cast<const uint16_t*>(o.ptr) + (size_t)row * o.ld + col;
   return h2f(__ldcg(reinterpret_cast<const unsigned short*>(ptr)), dt);
 }
+__device__ __forceinline__ uint32_t pack2(float v0, float v1, int dt) {
+  if (dt == DT_BF16) {
+    const __nv_bfloat162 t = __floats2bfloat162_rn(v0, v1);
+    return *reinterpret_cast<const uint32_t*>(&t);
+  }
+  const __half2 t = __floats2half2_rn(v0, v1);
+  return *reinterpret_cast<const uint32_t*>(&t);
+}
+// a and b rounded to the element type and back: the values a later reader of the stored pair
+// sees
+__device__ __forceinline__ void round2(float& a, float& b, int dt) {
+  float2 f;
+  if (dt == DT_BF16)
+    f = __bfloat1622float2(__floats2bfloat162_rn(a, b));
+  else
+    f = __half22float2(__floats2half2_rn(a, b));
+  a = f.x;
+  b = f.y;
+}
 __device__ __forceinline__ void store2(const Operand& o, int row, int col, int dt, float v0,
                                        float v1) {
   uint16_t* ptr = reinterpret_cast<uint16_t*>(o.ptr) + (size_t)row * o.ld + col;
-  *reinterpret_cast<uint32_t*>(ptr) = (uint32_t)f2h(v0, dt) | ((uint32_t)f2h(v1, dt) << 16);
+  *reinterpret_cast<uint32_t*>(ptr) = pack2(v0, v1, dt);
 }
 __device__ __forceinline__ void store1(const Operand& o, int row, int col, int dt, float v) {
   uint16_t* ptr = reinterpret_cast<uint16_t*>(o.ptr) + (size_t)row * o.ld + col;
@@ -1530,9 +1571,9 @@ __device__ __noinline__ void epi_rope(const Params& p, const Node& nd, int n0, u
     store_block(omap, col, lo);
     store_block(omap, col + 32, hi);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {  // the values the rope node reads: the stored outputs
-      lo[i] = h2f(f2h(lo[i], dt), dt);
-      hi[i] = h2f(f2h(hi[i], dt), dt);
+    for (int i = 0; i < 32; i += 2) {  // the values the rope node reads: the stored outputs
+      round2(lo[i], lo[i + 1], dt);
+      round2(hi[i], hi[i + 1], dt);
     }
     if (h < hq + hkv) {
 #pragma unroll
@@ -2177,7 +2218,8 @@ __device__ bool gemv(const Params& p, Smem& s, const Instr& in, const Node& nd, 
         // RoPE of the following node, on the rounded outputs it would read: the pair partner of
         // column j of a 64-column head is j ^ 32, held by lane ^ 16 (whole heads per tile, every
         // lane active: the host fuses only full-width tiles without a second weight)
-        const float r0 = h2f(f2h(y0, dt), dt), r1 = h2f(f2h(y1, dt), dt);
+        float r0 = y0, r1 = y1;
+        round2(r0, r1, dt);
         const float p0 = __shfl_xor_sync(FULL, r0, 16), p1 = __shfl_xor_sync(FULL, r1, 16);
         const int qend = nd.hq * 64, kend = (nd.hq + nd.hkv) * 64;
         if (n < kend) {
