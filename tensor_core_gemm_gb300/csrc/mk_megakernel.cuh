@@ -54,8 +54,8 @@ struct __align__(1024) Smem {
   uint64_t acc_empty[2];
   uint64_t go;                          // pair mode, odd CTA: released by the even CTA once per GEMM
   uint64_t gx_full;                     // tensor-core GEMV: the activation operand is staged
-  // prefill attention: scores S and output blocks O double-buffered in TMEM, P in xr
-  uint64_t att_s_full[2], att_s_free[2], att_p_full, att_o_full[2], att_o_free[2];
+  // prefill attention: scores S double-buffered in TMEM, O in TMEM, each block's P in its stage
+  uint64_t att_s_full[2], att_s_free[2], att_p_full, att_o_full[2];
   uint64_t att_q_full;                  // CTA pairs: both CTAs' query tiles are in xr
   uint64_t att_done;                    // CTA pairs: both CTAs have read O (once per tile)
   uint64_t instr_ready[kSlots];
@@ -762,15 +762,16 @@ __device__ bool load_attn(const Params& p, Smem& s, const Instr& in, const Node&
 }
 
 // Causal prefill attention, one (128-row query tile, query head) instruction: per 64-key block a
-// stage holds the query tile (16 KB), the block's keys (8 KB) and values (8 KB) of the head's
-// key/value head, all 128-byte swizzled. The query tile is fetched again with every block (from
-// L2) so each stage is self-contained. All three operands are produced inside the graph, so the
-// loads start once the sources are ready. On a CTA pair (a 256-row query tile, rank r holding
-// rows 128r..) the query rows stay in the staging buffer for the whole instruction (loaded by
-// the compute warpgroup) and a stage holds keys 32r..32r+31 of the block (the N half of
-// S = Q K^T this CTA holds) and value columns 32r..32r+31 (the N half of O = P V, 64-byte rows,
-// 64-byte swizzled): 8 KB per CTA, counted on the even CTA's barrier; the block's P tile is
-// written into the same stage (offset 8 KB), so consecutive blocks do not share a P buffer.
+// 48 KB stage holds the query tile (16 KB), the block's keys (8 KB) and values (8 KB) of the
+// head's key/value head, all 128-byte swizzled, and then the block's P tile (16 KB, written by
+// the compute warpgroup), so consecutive blocks do not share a P buffer. The query tile is
+// fetched again with every block (from L2) so each stage is self-contained. All three operands
+// are produced inside the graph, so the loads start once the sources are ready. On a CTA pair (a
+// 256-row query tile, rank r holding rows 128r..) the query rows stay in the staging buffer for
+// the whole instruction (loaded by the compute warpgroup) and a stage holds keys 32r..32r+31 of
+// the block (the N half of S = Q K^T this CTA holds) and value columns 32r..32r+31 (the N half
+// of O = P V, 64-byte rows, 64-byte swizzled): 8 KB per CTA, counted on the even CTA's barrier;
+// the block's P tile follows at offset 8 KB.
 template <bool PAIR>
 __device__ bool load_attn_prefill(const Params& p, Smem& s, const Instr& in, const Node& nd,
                                   int slot, uint32_t use, RingPos& rp, uint32_t& nfill,
@@ -976,17 +977,17 @@ __device__ __noinline__ bool mma_attn(const Params& p, Smem& s, uint32_t st, uin
                                       uint32_t q_par, int idx) {
   const uint32_t ring0 = smem_u32(s.ring), units = stage_bytes(p) >> 4;
   const uint32_t xr = smem_u32(s.xr);
-  // Single CTA: a stage holds Q (128 rows of 128 B), K (64 rows of 128 B) and V (N-major, 64
-  // rows of 128 B); P is in xr. Pair: Q in xr; a stage holds this CTA's 32 keys (rows of 128 B),
-  // its 32 value columns (N-major, 64 rows of 64 B) and the block's P (128 rows of 128 B).
+  // Single CTA (48 KB stages): a stage holds Q (128 rows of 128 B), K (64 rows of 128 B), V
+  // (N-major, 64 rows of 128 B) and the block's P (128 rows of 128 B). Pair: Q in xr; a stage
+  // holds this CTA's 32 keys (rows of 128 B), its 32 value columns (N-major, 64 rows of 64 B)
+  // and the block's P (128 rows of 128 B).
   const uint64_t qd = sdesc_sw128(PAIR ? xr : ring0, 16, 1024);
   const uint64_t kd = sdesc_sw128(ring0 + (PAIR ? 0 : 16384), 16, 1024);
   const uint64_t vd = PAIR ? sdesc_sw64(ring0 + 4096, 4096, 512)
                            : sdesc_sw128(ring0 + 24576, 8192, 1024);
   const uint64_t vk = PAIR ? 64 : 128;  // a 16-key slice of V, 16-byte units
-  const uint64_t pd = sdesc_sw128(PAIR ? ring0 + 8192 : xr, 16, 1024);
+  const uint64_t pd = sdesc_sw128(ring0 + (PAIR ? 8192 : kAttnPOffset), 16, 1024);
   const uint64_t qs = PAIR ? 0 : 1;     // Q moves with the stage (single CTA) or stays in xr
-  const uint64_t ps = PAIR ? 1 : 0;     // P moves with the stage (pair) or stays in xr
   const int mrows = PAIR ? 2 * kAttnTileQ : kAttnTileQ;
   const uint32_t is = idesc_f16_bk(1, kAttnKeyBlock, mrows), io = idesc_f16(1, 64, mrows);
   const uint32_t n0 = n;
@@ -1038,10 +1039,10 @@ __device__ __noinline__ bool mma_attn(const Params& p, Smem& s, uint32_t st, uin
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         if (PAIR)
-          tc_mma_f16_pair(tmem + 128u, pd + so * ps + (uint64_t)(kk * 2),
+          tc_mma_f16_pair(tmem + 128u, pd + so + (uint64_t)(kk * 2),
                           vd + so + (uint64_t)kk * vk, io, (j | kk) != 0);
         else
-          tc_mma_f16(tmem + 128u, pd + so * ps + (uint64_t)(kk * 2), vd + so + (uint64_t)kk * vk,
+          tc_mma_f16(tmem + 128u, pd + so + (uint64_t)(kk * 2), vd + so + (uint64_t)kk * vk,
                      io, (j | kk) != 0);
       }
       if (PAIR) {
@@ -1056,10 +1057,7 @@ __device__ __noinline__ bool mma_attn(const Params& p, Smem& s, uint32_t st, uin
     ro.next(ns);
   }
   // The compute warps have read every S and O block of this instruction before TMEM is reused.
-  const uint32_t nl = n0 + (uint32_t)nb - 1u;
-  if (PAIR ? !wait_warp(p, smem_u32(&s.att_done), q_par, R_MMA, 27, idx, true)
-           : !wait_warp(p, smem_u32(&s.att_o_free[nl & 1u]), (nl >> 1) & 1u, R_MMA, 27, idx))
-    return false;
+  if (!wait_warp(p, smem_u32(&s.att_done), q_par, R_MMA, 27, idx, PAIR)) return false;
   n = n0 + (uint32_t)nb;
   return true;
 }
@@ -2791,7 +2789,6 @@ __device__ __noinline__ bool attn_prefill_body(const Params& p, Smem& s, const I
   const int qpos = nd.pos0 + row;
   const int kmax = in.klen;
   const float sl2 = nd.scale * 1.4426950408889634f;  // scores in log2 units
-  uint8_t* P = reinterpret_cast<uint8_t*>(s.xr);
   float m = -INFINITY, l = 0.f;
   const uint32_t n0 = n;
   // Every barrier here takes one arrival per warp and nothing in the body synchronises the
@@ -2803,11 +2800,6 @@ __device__ __noinline__ bool attn_prefill_body(const Params& p, Smem& s, const I
       return false;
     tc_fence_after();
     return true;
-  };
-  auto o_release = [&](uint32_t nn) {
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) arrive_mma(s.att_o_free[nn & 1u]);
   };
   for (int j = 0; j < nb; ++j) {
     const uint32_t nn = n0 + (uint32_t)j, b = nn & 1u;
@@ -2863,12 +2855,11 @@ __device__ __noinline__ bool attn_prefill_body(const Params& p, Smem& s, const I
     const float ls = (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
     l = fmaf(l, alpha, ls);
     m = mn;
-    // single CTA: P_j goes to the one P buffer once P V of the previous block has read it;
-    // pair: P_j has a buffer of its own, so O is waited for only to rescale it
+    // P_j has a buffer of its own (in the block's stage), so O is waited for only to rescale it
     const bool rescale = __any_sync(FULL, need);
-    if (j > 0) {
-      if ((!PAIR || rescale) && !o_done(nn - 1u)) return false;
-      if (rescale) {  // rescale this warp's rows of O (alpha = 1 where not needed)
+    if (j > 0 && rescale) {
+      if (!o_done(nn - 1u)) return false;
+      {  // rescale this warp's rows of O (alpha = 1 where not needed)
         uint32_t o0[32], o1[32];
         tmem_ld32(otm, o0);
         tmem_ld32(otm + 32u, o1);
@@ -2882,9 +2873,8 @@ __device__ __noinline__ bool attn_prefill_body(const Params& p, Smem& s, const I
         tmem_st32(otm + 32u, o1);
         tmem_st_wait();
       }
-      if (!PAIR) o_release(nn - 1u);  // pair: one arrival when O is read at the end
     }
-    uint8_t* Pj = PAIR ? s.ring + (size_t)((ring + (uint32_t)j) % NS) * sb + 8192 : P;
+    uint8_t* Pj = s.ring + (size_t)((ring + (uint32_t)j) % NS) * sb + (PAIR ? 8192 : kAttnPOffset);
 #pragma unroll
     for (int ch = 0; ch < 8; ++ch)
       *reinterpret_cast<uint4*>(Pj + ct * 128 + ((ch ^ (ct & 7)) << 4)) = pk[ch];
@@ -2904,13 +2894,10 @@ __device__ __noinline__ bool attn_prefill_body(const Params& p, Smem& s, const I
   tmem_ld32(otm, o0);
   tmem_ld32(otm + 32u, o1);
   tmem_ld_wait();
-  if (PAIR) {  // the tile's TMEM may be reused once both CTAs have read O
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) arrive_mma(s.att_done);
-  } else {
-    o_release(nl);
-  }
+  // the tile's TMEM may be reused once the warps (of both CTAs) have read O
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) arrive_mma(s.att_done);
   if (row < nd.M) {
     const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
@@ -3076,11 +3063,10 @@ __global__ void __launch_bounds__(kThreads, 1) megakernel(const __grid_constant_
       mbar_init(smem_u32(&s.att_s_full[i]), 1);   // tcgen05.commit
       mbar_init(smem_u32(&s.att_s_free[i]), PAIR ? 8 : 4);  // a lane per compute warp (both CTAs)
       mbar_init(smem_u32(&s.att_o_full[i]), 1);
-      mbar_init(smem_u32(&s.att_o_free[i]), PAIR ? 8 : 4);
     }
     mbar_init(smem_u32(&s.att_p_full), PAIR ? 8 : 4);
     mbar_init(smem_u32(&s.att_q_full), 1);
-    mbar_init(smem_u32(&s.att_done), 8);
+    mbar_init(smem_u32(&s.att_done), PAIR ? 8 : 4);  // a lane per compute warp (both CTAs)
     mbar_fence_init();
   }
   if (ks_has_tmem(KS) && warp == 2) {
