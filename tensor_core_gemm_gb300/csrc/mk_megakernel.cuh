@@ -54,7 +54,7 @@ struct __align__(1024) Smem {
   uint64_t acc_empty[2];
   uint64_t go;                          // pair mode, odd CTA: released by the even CTA once per GEMM
   uint64_t gx_full;                     // tensor-core GEMV: the activation operand is staged
-  // prefill attention: scores S double-buffered in TMEM, O in TMEM, each block's P in its stage
+  // prefill attention: scores S and P double-buffered in TMEM (P in a stage on pairs), O in TMEM
   uint64_t att_s_full[2], att_s_free[2], att_p_full, att_o_full[2];
   uint64_t att_q_full;                  // CTA pairs: both CTAs' query tiles are in xr
   uint64_t att_done;                    // CTA pairs: both CTAs have read O (once per tile)
@@ -762,9 +762,8 @@ __device__ bool load_attn(const Params& p, Smem& s, const Instr& in, const Node&
 }
 
 // Causal prefill attention, one (128-row query tile, query head) instruction: per 64-key block a
-// 48 KB stage holds the query tile (16 KB), the block's keys (8 KB) and values (8 KB) of the
-// head's key/value head, all 128-byte swizzled, and then the block's P tile (16 KB, written by
-// the compute warpgroup), so consecutive blocks do not share a P buffer. The query tile is
+// stage holds the query tile (16 KB), the block's keys (8 KB) and values (8 KB) of the head's
+// key/value head, all 128-byte swizzled; the block's P tile goes to TMEM. The query tile is
 // fetched again with every block (from L2) so each stage is self-contained. All three operands
 // are produced inside the graph, so the loads start once the sources are ready. On a CTA pair (a
 // 256-row query tile, rank r holding rows 128r..) the query rows stay in the staging buffer for
@@ -965,28 +964,30 @@ __device__ __noinline__ int mma_gemv(const Params& p, uint32_t full0, uint32_t e
 
 // Prefill attention MMAs of one instruction: nb key blocks from ring position (st, ph). Block j:
 // S_j = Q K_j^T into TMEM S[n&1] (M = 128 query rows, N = 64 keys, K = 64 dims; the keys are a
-// K-major B operand), then, once the compute warps have written P_j (bf16, 128-byte swizzled,
-// K-major) to shared memory, O += P_j V_j into the one TMEM output (N = 64 dims, K = 64 keys; the
-// values are an N-major B operand; block 0 overwrites it). S_{j+1} is issued before P_j is
-// awaited, so the tensor pipe computes the next scores while the softmax of the current block
-// runs. A stage is released when the block's P V completes. `n` counts attention blocks on this
-// SM: it gives every barrier's phase. TMEM columns: S at 0 and 64, O at 128.
+// K-major B operand), then, once the compute warps have written P_j (bf16: into TMEM on a single
+// CTA, 128-byte swizzled K-major in the stage on a pair), O += P_j V_j into the one TMEM output
+// (N = 64 dims, K = 64 keys; the values are an N-major B operand; block 0 overwrites it).
+// S_{j+1} is issued before P_j is awaited, so the tensor pipe computes the next scores while the
+// softmax of the current block runs. A stage is released when the block's P V completes. `n`
+// counts attention blocks on this SM: it gives every barrier's phase. TMEM columns: S at 0 and
+// 64, O at 128, P at 192 and 224 (single CTA).
 template <bool PAIR>
 __device__ __noinline__ bool mma_attn(const Params& p, Smem& s, uint32_t st, uint32_t ph,
                                       uint32_t ns, int nb, uint32_t tmem, uint32_t& n,
                                       uint32_t q_par, int idx) {
   const uint32_t ring0 = smem_u32(s.ring), units = stage_bytes(p) >> 4;
   const uint32_t xr = smem_u32(s.xr);
-  // Single CTA (48 KB stages): a stage holds Q (128 rows of 128 B), K (64 rows of 128 B), V
-  // (N-major, 64 rows of 128 B) and the block's P (128 rows of 128 B). Pair: Q in xr; a stage
-  // holds this CTA's 32 keys (rows of 128 B), its 32 value columns (N-major, 64 rows of 64 B)
-  // and the block's P (128 rows of 128 B).
+  // Single CTA: a stage holds Q (128 rows of 128 B), K (64 rows of 128 B) and V (N-major, 64
+  // rows of 128 B); P_j is the A operand of P V straight from TMEM (two buffers of 32 columns,
+  // a row per lane, two keys per column). Pair: Q in xr; a stage holds this CTA's 32 keys
+  // (rows of 128 B), its 32 value columns (N-major, 64 rows of 64 B) and the block's P (128
+  // rows of 128 B).
   const uint64_t qd = sdesc_sw128(PAIR ? xr : ring0, 16, 1024);
   const uint64_t kd = sdesc_sw128(ring0 + (PAIR ? 0 : 16384), 16, 1024);
   const uint64_t vd = PAIR ? sdesc_sw64(ring0 + 4096, 4096, 512)
                            : sdesc_sw128(ring0 + 24576, 8192, 1024);
   const uint64_t vk = PAIR ? 64 : 128;  // a 16-key slice of V, 16-byte units
-  const uint64_t pd = sdesc_sw128(ring0 + (PAIR ? 8192 : kAttnPOffset), 16, 1024);
+  const uint64_t pd = sdesc_sw128(ring0 + 8192, 16, 1024);  // pair: P in the stage
   const uint64_t qs = PAIR ? 0 : 1;     // Q moves with the stage (single CTA) or stays in xr
   const int mrows = PAIR ? 2 * kAttnTileQ : kAttnTileQ;
   const uint32_t is = idesc_f16_bk(1, kAttnKeyBlock, mrows), io = idesc_f16(1, 64, mrows);
@@ -1041,9 +1042,9 @@ __device__ __noinline__ bool mma_attn(const Params& p, Smem& s, uint32_t st, uin
         if (PAIR)
           tc_mma_f16_pair(tmem + 128u, pd + so + (uint64_t)(kk * 2),
                           vd + so + (uint64_t)kk * vk, io, (j | kk) != 0);
-        else
-          tc_mma_f16(tmem + 128u, pd + so + (uint64_t)(kk * 2), vd + so + (uint64_t)kk * vk,
-                     io, (j | kk) != 0);
+        else  // P_j from TMEM: 16 keys are 8 columns
+          tc_mma_f16_ts(tmem + 128u, tmem + kAttnPCol + b * 32u + (uint32_t)(kk * 8),
+                        vd + so + (uint64_t)kk * vk, io, (j | kk) != 0);
       }
       if (PAIR) {
         tc_commit_pair(smem_u32(&s.att_o_full[b]), 3);
@@ -2874,14 +2875,28 @@ __device__ __noinline__ bool attn_prefill_body(const Params& p, Smem& s, const I
         tmem_st_wait();
       }
     }
-    uint8_t* Pj = s.ring + (size_t)((ring + (uint32_t)j) % NS) * sb + (PAIR ? 8192 : kAttnPOffset);
+    if (PAIR) {
+      // P_j into the block's stage for the even CTA's pair MMA
+      uint8_t* Pj = s.ring + (size_t)((ring + (uint32_t)j) % NS) * sb + 8192;
 #pragma unroll
-    for (int ch = 0; ch < 8; ++ch)
-      *reinterpret_cast<uint4*>(Pj + ct * 128 + ((ch ^ (ct & 7)) << 4)) = pk[ch];
-    if (PAIR)
-      fence_proxy_async_all();  // the even CTA's pair MMA reads this CTA's P
-    else
-      fence_proxy_async_shared();
+      for (int ch = 0; ch < 8; ++ch)
+        *reinterpret_cast<uint4*>(Pj + ct * 128 + ((ch ^ (ct & 7)) << 4)) = pk[ch];
+      fence_proxy_async_all();
+    } else {
+      // P_j into TMEM (this thread's row, two keys per column), in the buffer P V of block
+      // nn - 2 read: that MMA is complete first
+      if (nn >= 2u && !o_done(nn - 2u)) return false;
+      uint32_t pw[32];
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        pw[4 * ch] = pk[ch].x;
+        pw[4 * ch + 1] = pk[ch].y;
+        pw[4 * ch + 2] = pk[ch].z;
+        pw[4 * ch + 3] = pk[ch].w;
+      }
+      tmem_st32(tmem + kAttnPCol + b * 32u + lanes, pw);
+      tmem_st_wait();
+    }
     tc_fence_before();
     __syncwarp();
     if (lane == 0) arrive_mma(s.att_p_full);

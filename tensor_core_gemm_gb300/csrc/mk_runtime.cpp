@@ -711,13 +711,11 @@ extern "C" mk_status mk_compile(mk_graph_t g, const mk_compile_opts* opts_in, mk
     delete p;
     return st;
   }
-  // 48 KB stages only where a single-CTA GEMM tile or prefill attention block needs them (A and
-  // B of a k-step; Q, K, V and the block's P); every other ring user (a GEMV weight tile, an
-  // attention key/value chunk, a CTA pair's tile, staged rows) fits 32 KB, so such plans prefetch
-  // 192 KB of operands per SM instead of 128 KB.
+  // 48 KB stages only where a single-CTA GEMM tile needs them; every other ring user (a GEMV
+  // weight tile, an attention key/value chunk or prefill block, staged rows) fits 32 KB, so such
+  // plans prefetch 192 KB of operands per SM instead of 128 KB.
   bool single_gemm = false;
-  for (const Instr& in : p->hp.instrs)
-    single_gemm |= in.op == OP_GEMM || in.op == OP_ATTN_PREFILL;
+  for (const Instr& in : p->hp.instrs) single_gemm |= in.op == OP_GEMM;
   single_gemm &= o.cluster != 2;
   const int stages = single_gemm ? kStages : kPairStages;
   const int64_t stage_bytes = kRingBytes / stages;

@@ -145,7 +145,7 @@ constexpr int kGemvRows = 64;          // K rows per stage for GEMV (x 256 colum
 constexpr int kAttnChunkMax = 128;     // keys per split-KV partial handled by one instruction
 constexpr int kAttnTileQ = 128;        // query rows of one prefill attention instruction
 constexpr int kAttnKeyBlock = 64;      // keys per ring stage of prefill attention (Q + K + V = 32 KB)
-constexpr int kAttnPOffset = 32768;    // single CTA: the block's P tile after Q, K and V (48 KB stages)
+constexpr int kAttnPCol = 192;         // single CTA: P tiles in TMEM, two of 32 columns
 
 // Specialisations of the kernel by the instruction kinds they run. The host launches the
 // smallest one that covers every instruction of a plan: a specialisation leaves out the code,
