@@ -240,7 +240,8 @@ mk_status mk_compile(mk_graph_t g, const mk_compile_opts* opts, mk_plan_t* out);
 
 /* Enqueue one run on `stream` (a cudaStream_t; NULL = legacy default stream): ONE persistent
  * kernel launch. The CTA that finishes last resets the counters for the next run (also after a
- * device-side failure) and moves the run's status to where mk_sync_status reads it.
+ * device-side failure) and moves the run's status to where mk_sync_status reads it (keeping an
+ * earlier failure that has not been read).
  * Asynchronous; errors of the launch itself are returned, device-side failures are reported by
  * mk_sync_status. Runs of one plan must not overlap (use one stream, or order the streams). */
 mk_status mk_run(mk_plan_t p, void* stream);
@@ -276,8 +277,9 @@ mk_status mk_plan_tensor_ptr(mk_plan_t p, int32_t tensor, void** ptr);
  * outside mk_run_host; without it mk_run keeps using the weight as it was when packed. */
 mk_status mk_plan_repack(mk_plan_t p, void* stream);
 
-/* Synchronise the device and read the status of the plan's last completed run. Returns
- * st->code as the status. */
+/* Synchronise the device and read the plan's status: the first device-side failure of any run
+ * since the previous mk_sync_status (its record is then cleared), or MK_OK with the last run's
+ * record. Returns st->code as the status. */
 mk_status mk_sync_status(mk_plan_t p, mk_device_status* st);
 
 mk_status mk_plan_destroy(mk_plan_t p);

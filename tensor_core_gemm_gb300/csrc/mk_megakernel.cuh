@@ -55,7 +55,7 @@ struct __align__(1024) Smem {
   uint64_t go;                          // pair mode, odd CTA: released by the even CTA once per GEMM
   uint64_t gx_full;                     // tensor-core GEMV: the activation operand is staged
   // prefill attention: scores S and P double-buffered in TMEM (P in a stage on pairs), O in TMEM
-  uint64_t att_s_full[2], att_s_free[2], att_p_full, att_o_full[2];
+  uint64_t att_s_full[2], att_s_free[2], att_p_full[2], att_o_full[2];
   uint64_t att_q_full;                  // CTA pairs: both CTAs' query tiles are in xr
   uint64_t att_done;                    // CTA pairs: both CTAs have read O (once per tile)
   uint64_t instr_ready[kSlots];
@@ -1032,8 +1032,12 @@ __device__ __noinline__ bool mma_attn(const Params& p, Smem& s, uint32_t st, uin
   for (int j = 0; j < nb; ++j) {
     if (j + 1 < nb && !issue_s(j + 1)) return false;
     const uint32_t nn = n0 + (uint32_t)j, b = nn & 1u;
-    // P_j is written (and any rescale of O by the compute warps is stored) before p_full
-    if (!wait_warp(p, smem_u32(&s.att_p_full), nn & 1u, R_MMA, 25, idx, PAIR)) return false;
+    // P_j is written (and any rescale of O by the compute warps is stored) before p_full. Two
+    // barriers by block parity: the compute warps can arrive for block j + 1 before this warp
+    // has seen block j's arrival (S_{j+1} is issued first), which would move one barrier two
+    // phases past the one awaited.
+    if (!wait_warp(p, smem_u32(&s.att_p_full[b]), (nn >> 1) & 1u, R_MMA, 25, idx, PAIR))
+      return false;
     tc_fence_after();
     const uint64_t so = (uint64_t)(ro.st * units);
     if (elect_one()) {
@@ -2899,7 +2903,7 @@ __device__ __noinline__ bool attn_prefill_body(const Params& p, Smem& s, const I
     }
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) arrive_mma(s.att_p_full);
+    if (lane == 0) arrive_mma(s.att_p_full[b]);
   }
   n = n0 + (uint32_t)nb;
   if (nb == 0) return true;
@@ -3079,7 +3083,7 @@ __global__ void __launch_bounds__(kThreads, 1) megakernel(const __grid_constant_
       mbar_init(smem_u32(&s.att_s_free[i]), PAIR ? 8 : 4);  // a lane per compute warp (both CTAs)
       mbar_init(smem_u32(&s.att_o_full[i]), 1);
     }
-    mbar_init(smem_u32(&s.att_p_full), PAIR ? 8 : 4);
+    for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&s.att_p_full[i]), PAIR ? 8 : 4);
     mbar_init(smem_u32(&s.att_q_full), 1);
     mbar_init(smem_u32(&s.att_done), PAIR ? 8 : 4);  // a lane per compute warp (both CTAs)
     mbar_fence_init();
@@ -3133,8 +3137,13 @@ __global__ void __launch_bounds__(kThreads, 1) megakernel(const __grid_constant_
       if (p.snapshot) p.snapshot[i] = v;
       p.counters[i] = 0;
     }
+    // the run's status joins the record the host reads unless that already holds an unread
+    // failure (the first failure since the last read is kept)
+    int prev = 0;
+    if (threadIdx.x < kStatusWords) prev = __ldcg(p.last_status + ST_CODE);
+    __syncthreads();
     if (threadIdx.x < kStatusWords) {
-      p.last_status[threadIdx.x] = __ldcg(p.status + threadIdx.x);
+      if (prev == 0) p.last_status[threadIdx.x] = __ldcg(p.status + threadIdx.x);
       p.status[threadIdx.x] = 0;
     }
     if (threadIdx.x == 0) *p.done = 0;

@@ -873,6 +873,8 @@ extern "C" mk_status mk_sync_status(mk_plan_t p, mk_device_status* st) {
   st->role = w[ST_ROLE];
   st->where = w[ST_WHERE];
   if (st->code) {
+    // read: the next runs report afresh
+    CUDA_TRY(cudaMemset(p->params.last_status, 0, sizeof w));
     set_error("device reported %s at instruction %d (SM %d, role %d, site %d): counter %d "
               "observed %d, expected %d",
               st->code == MK_ERR_TIMEOUT ? "a wait timeout" : "a failed check", st->instr, st->sm,
