@@ -2280,14 +2280,17 @@ __device__ __forceinline__ void rmsnorm_body(const Instr& in, const Node& nd) {
   const float eps = nd.eps;
   for (int r = wp; r < rows; r += 4) {
     const int m = in.m0 + r;
-    float ss = 0.f;
+    float s0 = 0.f, s1 = 0.f;  // two chains, as the staged path sums them
     for (int k = lane * 8; k < N; k += 256) {
       float x[8];
       load8(nd.a, m, k, dt, x);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) ss += x[e] * x[e];
+      for (int e = 0; e < 4; ++e) {
+        s0 += x[e] * x[e];
+        s1 += x[e + 4] * x[e + 4];
+      }
     }
-    const float rstd = rsqrtf(warp_sum(ss) / (float)N + eps);
+    const float rstd = rsqrtf(warp_sum(s0 + s1) / (float)N + eps);
     for (int k = lane * 8; k < N; k += 256) {
       float x[8], g[8];
       load8(nd.a, m, k, dt, x);
@@ -2386,44 +2389,48 @@ __device__ bool rows_staged(const Params& p, Smem& s, const Instr& in, const Nod
     const uint8_t* base = stage_ptr(s, p, st);
     const int r0 = j * rps, nr = min(rps, rows - r0);
     if (!ROPE) {
-      // Rows r and r + 4 of the stage together (two independent chains per warp); each row's
-      // statistic still sums its lane's vectors in order.
+      // Rows r, r + 4 and r + 8 of the stage together (three independent rows per warp, each
+      // row's squares summed in two chains, the same order as the unstaged path).
       uint16_t* out = reinterpret_cast<uint16_t*>(nd.out.ptr);
       const int nv = W / 8;
-      for (int r = wp; r < nr; r += 8) {
-        const bool two = r + 4 < nr;
-        const uint4* xa = reinterpret_cast<const uint4*>(base + (size_t)r * W * 2);
-        const uint4* xb = reinterpret_cast<const uint4*>(base + (size_t)(two ? r + 4 : r) * W * 2);
-        float sa = 0.f, sb = 0.f;
-        for (int v = lane; v < nv; v += 32) {
-          const uint4 qa = xa[v], qb = xb[v];
-          float fa[8], fb[8];
-          unpack8(qa, dt, fa);
-          unpack8(qb, dt, fb);
+      for (int r = wp; r < nr; r += 12) {
+        const uint4* xq[3];
+        bool live[3];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            sa += fa[e] * fa[e];
-            sb += fb[e] * fb[e];
+        for (int k = 0; k < 3; ++k) {
+          live[k] = r + 4 * k < nr;
+          xq[k] = reinterpret_cast<const uint4*>(base + (size_t)(live[k] ? r + 4 * k : r) * W * 2);
+        }
+        float s0[3] = {0.f, 0.f, 0.f}, s1[3] = {0.f, 0.f, 0.f};
+        for (int v = lane; v < nv; v += 32) {
+#pragma unroll
+          for (int k = 0; k < 3; ++k) {
+            float f[8];
+            unpack8(xq[k][v], dt, f);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              s0[k] += f[e] * f[e];
+              s1[k] += f[e + 4] * f[e + 4];
+            }
           }
         }
-        const float ra = rsqrtf(warp_sum(sa) / (float)W + nd.eps);
-        const float rb2 = rsqrtf(warp_sum(sb) / (float)W + nd.eps);
-        uint16_t* oa = out + (size_t)(in.m0 + r0 + r) * nd.out.ld;
-        uint16_t* ob = out + (size_t)(in.m0 + r0 + r + 4) * nd.out.ld;
+        float rs[3];
+#pragma unroll
+        for (int k = 0; k < 3; ++k) rs[k] = rsqrtf(warp_sum(s0[k] + s1[k]) / (float)W + nd.eps);
 #pragma unroll 2
         for (int v = lane; v < nv; v += 32) {
-          const uint4 qa = xa[v], qb = xb[v], qg = gshared ? gs[v] : __ldg(gm + v);
-          float fa[8], fb[8], gf[8];
-          unpack8(qa, dt, fa);
-          unpack8(qb, dt, fb);
-          unpack8(qg, dt, gf);
+          float gf[8];
+          unpack8(gshared ? gs[v] : __ldg(gm + v), dt, gf);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            fa[e] = fa[e] * ra * gf[e];
-            fb[e] = fb[e] * rb2 * gf[e];
+          for (int k = 0; k < 3; ++k) {
+            if (!live[k]) continue;
+            float f[8];
+            unpack8(xq[k][v], dt, f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = f[e] * rs[k] * gf[e];
+            *reinterpret_cast<uint4*>(out + (size_t)(in.m0 + r0 + r + 4 * k) * nd.out.ld + v * 8) =
+                pack8(f, dt);
           }
-          *reinterpret_cast<uint4*>(oa + v * 8) = pack8(fa, dt);
-          if (two) *reinterpret_cast<uint4*>(ob + v * 8) = pack8(fb, dt);
         }
       }
     } else {
