@@ -280,10 +280,6 @@ __device__ __forceinline__ float h2f(uint16_t v, int dt) {
   return dt == DT_BF16 ? __uint_as_float((uint32_t)v << 16)
                        : __half2float(__ushort_as_half(v));
 }
-__device__ __forceinline__ uint16_t f2h(float v, int dt) {
-  return dt == DT_BF16 ? __bfloat16_as_ushort(__float2bfloat16_rn(v))
-                       : __half_as_ushort(__float2half_rn(v));
-}
 // 8 packed elements <-> 8 floats. The element type is uniform, so one branch picks the path;
 // conversions go two elements at a time (one paired instruction each way), the same rounding
 // as element by element.
@@ -358,10 +354,6 @@ __device__ __forceinline__ void store2(const Operand& o, int row, int col, int d
                                        float v1) {
   uint16_t* ptr = reinterpret_cast<uint16_t*>(o.ptr) + (size_t)row * o.ld + col;
   *reinterpret_cast<uint32_t*>(ptr) = pack2(v0, v1, dt);
-}
-__device__ __forceinline__ void store1(const Operand& o, int row, int col, int dt, float v) {
-  uint16_t* ptr = reinterpret_cast<uint16_t*>(o.ptr) + (size_t)row * o.ld + col;
-  *ptr = f2h(v, dt);
 }
 
 // ------------------------------------------------------------------ scheduler warp
