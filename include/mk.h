@@ -300,7 +300,9 @@ mk_status mk_plan_destroy(mk_plan_t p);
  *              non-NULL: then the call synchronises the stream and fills *status.
  * The first call on each device, with that device current, looks up the array's device address
  * (cudaGetSymbolAddress) and sets the kernel's shared-memory limit; make that first call before
- * any stream capture. Every call shares the array and clears the parts that must start at zero;
+ * any stream capture. A call on a capturing stream must pass status == NULL and come after that
+ * first call; otherwise it returns MK_ERR_UNSUPPORTED with a message and records nothing. A
+ * captured call replays with the arguments it was captured with. Every call shares the array and clears the parts that must start at zero;
  * the rest keeps the previous call's contents. A call writes its records into the array with a
  * small set-up kernel that receives them by value, so it reads no host buffer after it returns
  * and calls from different host threads share no host state. Calls on one stream run one after

@@ -127,6 +127,18 @@ extern "C" mk_status mk_gemv_noalloc(const void* x, const void* w, void* out, in
   if (e != cudaSuccess) return fail(MK_ERR_CUDA, "no current CUDA device", e);
   if (dev >= kMaxDevices) return fail(MK_ERR_UNSUPPORTED, "device ordinal above 63");
 
+  // A capturing stream takes the set-up kernel and the launch as graph nodes (their arguments
+  // are passed by value), but neither the per-device set-up nor the status read (a stream
+  // synchronisation and a copy) is legal while the stream captures.
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  e = cudaStreamIsCapturing(st, &cap);
+  if (e != cudaSuccess) return fail(MK_ERR_CUDA, "cudaStreamIsCapturing", e);
+  if (cap != cudaStreamCaptureStatusNone && (status || !g_scratch_dev[dev]))
+    return fail(MK_ERR_UNSUPPORTED,
+                "a capturing stream needs status == NULL and an earlier uncaptured call on this "
+                "device");
+
   // Set-up, once per device, with that device current: the array's device address, and the
   // kernel's shared-memory limit. The first call on a device does this.
   if (!g_scratch_dev[dev]) {
@@ -201,7 +213,6 @@ extern "C" mk_status mk_gemv_noalloc(const void* x, const void* w, void* out, in
   // Write the records into the array and clear what must start at zero (the split
   // semaphores, the status words and the CTA completion count); the array keeps the previous
   // call's contents otherwise.
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
   noalloc_setup<<<1, 256, 0, st>>>(sa);
   e = cudaGetLastError();
   if (e != cudaSuccess) return fail(MK_ERR_CUDA, "set-up launch", e);

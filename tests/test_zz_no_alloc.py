@@ -8,7 +8,7 @@ keeps its run state in a fixed device array inside the library instead. This tes
 through the C ABI, twice in a row per shape and back to back with shapes whose split counts
 differ, and checks every result element by element against the CPU oracle's matmul on the same
 quantised inputs, within the parity tolerance of the other GPU tests (and against
-mk_compile + mk_run). It sits in a file of its own that pytest collects last.
+mk_compile + mk_run), and runs it inside a stream capture. It sits in a file of its own that pytest collects last.
 """
 import ctypes as C
 
@@ -111,3 +111,29 @@ def test_noalloc_rejects_sizes_beyond_its_fixed_scratch():
     assert rc == _lib.MK_ERR_UNSUPPORTED and b"maximum" in lib.mk_last_error()
     rc = lib.mk_gemv_noalloc(*p, 9, 8, 64, _lib.MK_BF16, None, None)
     assert rc == _lib.MK_ERR_UNSUPPORTED
+
+
+def test_noalloc_inside_a_stream_capture():
+    # a status-reading call is refused on a capturing stream (it would synchronise); a call
+    # without status becomes graph nodes that replay on whatever the captured buffers hold
+    lib = _lib.load()
+    m, n, k, dt = 2, 512, 1024, "bf16"
+    x, w, ref = _inputs(m, n, k, dt, seed=300)
+    out = torch.zeros((m, n), dtype=x.dtype, device=DEV)
+    assert _call(lib, x, w, out, m, n, k, dt) == _lib.MK_OK   # per-device set-up, uncaptured
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        refused = _call(lib, x, w, out, m, n, k, dt, _lib.DeviceStatus())
+        refused_msg = lib.mk_last_error()
+        captured = _call(lib, x, w, out, m, n, k, dt)
+    assert refused == _lib.MK_ERR_UNSUPPORTED and b"capturing" in refused_msg
+    assert captured == _lib.MK_OK, lib.mk_last_error().decode()
+    for seed in (300, 310):
+        x2, w2, ref = _inputs(m, n, k, dt, seed=seed)
+        x.copy_(x2)   # new contents at the captured addresses (w through its tensor map)
+        w.copy_(w2)
+        out.fill_(5.0)
+        graph.replay()
+        torch.cuda.synchronize()
+        _close(synth.to_numpy_f32(out), ref)
